@@ -1,0 +1,72 @@
+"""Block packers for the host tests, written from the public GGML K-quant
+format text (the formats the PocketLLM pages name), in the opposite direction
+to the oracle's decoders: fields in, bytes out.  A round trip through an
+oracle decoder therefore pins that decoder against the format text, not
+against itself.
+"""
+import numpy as np
+
+
+def f16_bits(v):
+    return np.array([v], dtype=np.float16).view(np.uint16)[0]
+
+
+def pack_q4K(d, dmin, sc, mn, q):
+    """d, dmin: floats (stored as f16); sc, mn: 8 ints in 0..63; q: 256 ints in 0..15."""
+    sc = [int(v) for v in sc]
+    mn = [int(v) for v in mn]
+    blk = np.zeros(144, dtype=np.uint8)
+    blk[0:2] = np.array([d], dtype=np.float16).view(np.uint8)
+    blk[2:4] = np.array([dmin], dtype=np.float16).view(np.uint8)
+    t = np.zeros(12, dtype=np.int64)
+    # pairs 0..3: low six bits of bytes 0..3 (scales) and 4..7 (mins)
+    for j in range(4):
+        t[j] |= sc[j] & 63
+        t[j + 4] |= mn[j] & 63
+    # pairs 4..7: low four bits in bytes 8..11 (scale low nibble, min high
+    # nibble); the two top bits go into bits 6-7 of bytes j-4 (scale) and j (min)
+    for j in range(4, 8):
+        t[j + 4] |= (sc[j] & 15) | ((mn[j] & 15) << 4)
+        t[j - 4] |= (sc[j] >> 4) << 6
+        t[j] |= (mn[j] >> 4) << 6
+    blk[4:16] = t.astype(np.uint8)
+    q = np.asarray(q, dtype=np.int64)
+    w = np.arange(256)
+    chunk, within = w // 64, w % 64
+    byte = 32 * chunk + within % 32
+    qs = np.zeros(128, dtype=np.int64)
+    lo = within < 32
+    qs[byte[lo]] |= q[lo]
+    qs[byte[~lo]] |= q[~lo] << 4
+    blk[16:144] = qs.astype(np.uint8)
+    return blk
+
+
+def pack_q6K(d, scales, q):
+    """d: float (f16); scales: 16 ints in -128..127; q: 256 six-bit codes 0..63."""
+    q = np.asarray(q, dtype=np.int64)
+    blk = np.zeros(210, dtype=np.uint8)
+    ql = np.zeros(128, dtype=np.int64)
+    qh = np.zeros(64, dtype=np.int64)
+    for w in range(256):
+        half, r = divmod(w, 128)
+        quarter, l = divmod(r, 32)
+        ql_idx = 64 * half + 32 * (quarter % 2) + l
+        shift = 4 if quarter >= 2 else 0
+        ql[ql_idx] |= (q[w] & 15) << shift
+        qh[32 * half + l] |= (q[w] >> 4) << (2 * quarter)
+    blk[0:128] = ql.astype(np.uint8)
+    blk[128:192] = qh.astype(np.uint8)
+    blk[192:208] = np.asarray(scales, dtype=np.int64).astype(np.int8).view(np.uint8)
+    blk[208:210] = np.array([d], dtype=np.float16).view(np.uint8)
+    return blk
+
+
+def pack_q8K(d, qs):
+    """A q8_K block from its scale and codes; bsums are the 16-element sums."""
+    qs = np.asarray(qs, dtype=np.int64)
+    blk = np.zeros(292, dtype=np.uint8)
+    blk[0:4] = np.array([d], dtype=np.float32).view(np.uint8)
+    blk[4:260] = qs.astype(np.int8).view(np.uint8)
+    blk[260:292] = qs.reshape(16, 16).sum(axis=1).astype(np.int16).view(np.uint8)
+    return blk
