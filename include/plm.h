@@ -1,0 +1,132 @@
+/*
+ * plm -- packed K-quant matmul (gemm_quant) for GB300 (sm_103a).
+ *
+ * The operation is the packed-weight matmul of the PocketLLM pages ("What it
+ * runs": q4_k / q6_k weights decoded inside the kernel and never widened;
+ * "Current status", row "src/ -- the C++ engine": activations quantized to
+ * int8 one 256-element block at a time, the q6_K output head summed in
+ * int32).  The byte formats are the public GGML K-quant blocks those pages
+ * name:
+ *
+ *   q4_K (144 B per 256 weights): f16 d, f16 dmin, u8 scales[12] (eight
+ *        6-bit scale/min pairs), u8 qs[128] (4-bit codes; each 64-weight
+ *        chunk keeps its first 32 weights in the low nibbles, the next 32 in
+ *        the high nibbles).  weight = d*sc_j*q - dmin*m_j.
+ *   q6_K (210 B per 256 weights): u8 ql[128], u8 qh[64], i8 scales[16]
+ *        (one per 16 weights), f16 d.  weight = d*sc*(q6 - 32).
+ *   q8_K (292 B per 256 activations): f32 d, i8 qs[256], i16 bsums[16].
+ *
+ * Shapes and layouts (all row-major, no padding):
+ *   m  activation rows, n weight (output) rows, k reduction length,
+ *      k a positive multiple of 256, nb = k/256.
+ *   x  f32  [m][k]
+ *   xq q8_K [m][nb]      (m*nb*292 bytes)
+ *   w  q4_K [n][nb] or q6_K [n][nb]   (n*nb*144 or n*nb*210 bytes)
+ *   y  f32  [m][n]       y[i][r] = sum over k of x_hat[i][.] * w_hat[r][.]
+ *
+ * Ownership and ordering: every pointer is a DEVICE pointer owned by the
+ * caller; the library allocates nothing and never synchronizes.  Each call
+ * enqueues its work on `stream` (0 = the legacy default stream) and returns
+ * at once; results are visible to later work on that stream.  y is
+ * overwritten, never accumulated into.  Calls on different streams that
+ * write the same buffers race.
+ *
+ * Errors: arguments are checked on the host before anything is enqueued;
+ * a rejected call enqueues nothing.  PLM_ERR_INVALID_ARG: null pointer,
+ * m, n <= 0, k <= 0 or k % 256 != 0, GEMV with m > 8, sizes past int32
+ * indexing.  PLM_ERR_MISALIGNED: a pointer below the alignment its entry
+ * point states.  PLM_ERR_CUDA: the launch itself failed (the CUDA error code
+ * is then available from plm_last_cuda_error on the calling thread).
+ * Faults inside kernels are never used to report errors.
+ */
+#ifndef PLM_H
+#define PLM_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PLM_ABI_VERSION 1
+
+typedef enum {
+    PLM_OK = 0,
+    PLM_ERR_INVALID_ARG = 1,
+    PLM_ERR_MISALIGNED = 2,
+    PLM_ERR_UNSUPPORTED = 3,
+    PLM_ERR_CUDA = 4
+} plm_status;
+
+/* ABI version of the loaded library (PLM_ABI_VERSION at build time). */
+int plm_abi_version(void);
+
+/* Static, NUL-terminated name of a status code; "unknown status" otherwise. */
+const char* plm_status_string(int status);
+
+/* cudaError_t of the last PLM_ERR_CUDA returned on the calling thread
+ * (cudaSuccess if none). */
+int plm_last_cuda_error(void);
+
+/*
+ * q8_K activation quantization ("Current status" row "src/": activations
+ * quantized to int8 the llama.cpp way, one 256-element block per task).
+ * Per 256-element chunk of each row of x: the signed value `max` of largest
+ * magnitude (first occurrence on ties), iscale = -128/max, code =
+ * min(127, round-half-even(iscale*x)), d = 1/iscale, bsums[g] = sum of codes
+ * 16g..16g+15; an all-zero chunk gives d = 0 and zero codes and sums.
+ * Bit-exact with that scalar rule.
+ *   x  : f32 [m][k], 16-byte aligned.       xq : q8_K [m][k/256], 4-byte aligned.
+ */
+plm_status plm_quantize_q8K(const float* x, void* xq, int64_t m, int64_t k,
+                            cudaStream_t stream);
+
+/*
+ * Decode GEMV, y = W . x for m = 1..8 activation rows ("What it runs":
+ * packed weights decoded in the kernel; the weight stream is read once for
+ * all m rows, as the pages' 8-row activation tile does).  Integer sub-block
+ * dots are exact; the f32 result is within 1e-4 of sum_k |w_hat * x_hat|.
+ * The result for activation row i does not depend on m.
+ *   w  : q4_K [n][k/256], 16-byte aligned.  xq : q8_K [m][k/256], 4-byte aligned.
+ *   y  : f32 [m][n], 4-byte aligned.        1 <= m <= 8.
+ */
+plm_status plm_gemv_q4K(const void* w, const void* xq, float* y,
+                        int64_t m, int64_t n, int64_t k, cudaStream_t stream);
+
+/* q6_K decode GEMV (the output head path of "Current status" row "src/",
+ * summed in int32).  Same contract as plm_gemv_q4K; w is q6_K
+ * [n][k/256] and must be 16-byte aligned. */
+plm_status plm_gemv_q6K(const void* w, const void* xq, float* y,
+                        int64_t m, int64_t n, int64_t k, cudaStream_t stream);
+
+/*
+ * Prefill GEMM, y = X . W^T for any m >= 1 (intended for m = 512..2048):
+ * weight tiles are decoded in shared memory into exact integer-valued
+ * operands and contracted on the tensor cores; per-block scales are applied
+ * in f32.  Same buffers, layouts and tolerance as the GEMV; no limit on m.
+ */
+plm_status plm_gemm_q4K(const void* w, const void* xq, float* y,
+                        int64_t m, int64_t n, int64_t k, cudaStream_t stream);
+plm_status plm_gemm_q6K(const void* w, const void* xq, float* y,
+                        int64_t m, int64_t n, int64_t k, cudaStream_t stream);
+
+/*
+ * Verification export: the integer sub-block dots computed by the same
+ * device decode/dot code the GEMV uses.
+ *   q4_K: out int32 [m][n][k/32],  out[i][r][8b+j]  = sum_{l<32} q * q8
+ *         over sub-block j of block b.
+ *   q6_K: out int32 [m][n][k/16],  out[i][r][16b+g] = sum_{l<16} (q6-32) * q8
+ *         over group g of block b.
+ *   Same alignment rules as the GEMV; out 4-byte aligned; 1 <= m <= 8.
+ */
+plm_status plm_subdots_q4K(const void* w, const void* xq, int32_t* out,
+                           int64_t m, int64_t n, int64_t k, cudaStream_t stream);
+plm_status plm_subdots_q6K(const void* w, const void* xq, int32_t* out,
+                           int64_t m, int64_t n, int64_t k, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PLM_H */

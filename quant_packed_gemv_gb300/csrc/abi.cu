@@ -1,0 +1,130 @@
+// The C ABI of libplm: argument checks on the host, then one or more kernel
+// launches on the caller's stream.  Nothing is allocated and nothing waits.
+#include <cstdint>
+
+#include "../../include/plm.h"
+#include "plm_device.cuh"
+#include "plm_internal.h"
+
+namespace plm {
+
+int num_sms() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) return 1;
+    return n;
+}
+
+}  // namespace plm
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+constexpr int64_t kMaxIndex = 0x7FFFFFFFLL;
+
+bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
+
+plm_status cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return PLM_OK;
+    g_last_cuda_error = (int)e;
+    return PLM_ERR_CUDA;
+}
+
+// Shape checks shared by the matmul entry points.
+plm_status check_matmul(const void* w, const void* xq, const void* y, int64_t m, int64_t n,
+                        int64_t k, int64_t max_m) {
+    if (!w || !xq || !y) return PLM_ERR_INVALID_ARG;
+    if (m <= 0 || n <= 0 || k <= 0 || k % plm::QK != 0) return PLM_ERR_INVALID_ARG;
+    if (m > max_m || n > kMaxIndex || k > kMaxIndex) return PLM_ERR_INVALID_ARG;
+    if (m * (k / plm::QK) > kMaxIndex || n * (k / plm::QK) > kMaxIndex) return PLM_ERR_INVALID_ARG;
+    if (!aligned(w, 16) || !aligned(xq, 4) || !aligned(y, 4)) return PLM_ERR_MISALIGNED;
+    return PLM_OK;
+}
+
+plm_status gemv_common(int fmt, const void* w, const void* xq, float* y, int64_t m, int64_t n,
+                       int64_t k, cudaStream_t stream) {
+    plm_status s = check_matmul(w, xq, y, m, n, k, plm::GEMV_MAX_M);
+    if (s != PLM_OK) return s;
+    if (!plm::gemv_supported(fmt, (int)k)) return PLM_ERR_UNSUPPORTED;
+    return cuda_status(plm::launch_gemv(fmt, (const uint8_t*)w, (const uint8_t*)xq, y, (int)m,
+                                        (int)n, (int)k, stream));
+}
+
+plm_status gemm_common(int fmt, const void* w, const void* xq, float* y, int64_t m, int64_t n,
+                       int64_t k, cudaStream_t stream) {
+    plm_status s = check_matmul(w, xq, y, m, n, k, kMaxIndex);
+    if (s != PLM_OK) return s;
+    if (m * n > (int64_t)1 << 40) return PLM_ERR_INVALID_ARG;
+    if (!plm::gemv_supported(fmt, (int)k)) return PLM_ERR_UNSUPPORTED;
+    return cuda_status(plm::launch_gemm(fmt, (const uint8_t*)w, (const uint8_t*)xq, y, m, (int)n,
+                                        (int)k, stream));
+}
+
+plm_status subdots_common(int fmt, const void* w, const void* xq, int32_t* out, int64_t m,
+                          int64_t n, int64_t k, cudaStream_t stream) {
+    plm_status s = check_matmul(w, xq, out, m, n, k, plm::GEMV_MAX_M);
+    if (s != PLM_OK) return s;
+    if (!plm::gemv_supported(fmt, (int)k)) return PLM_ERR_UNSUPPORTED;
+    return cuda_status(plm::launch_subdots(fmt, (const uint8_t*)w, (const uint8_t*)xq, out, (int)m,
+                                           (int)n, (int)k, stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+int plm_abi_version(void) { return PLM_ABI_VERSION; }
+
+const char* plm_status_string(int status) {
+    switch (status) {
+        case PLM_OK: return "ok";
+        case PLM_ERR_INVALID_ARG: return "invalid argument";
+        case PLM_ERR_MISALIGNED: return "misaligned pointer";
+        case PLM_ERR_UNSUPPORTED: return "unsupported size";
+        case PLM_ERR_CUDA: return "CUDA launch error";
+        default: return "unknown status";
+    }
+}
+
+int plm_last_cuda_error(void) { return g_last_cuda_error; }
+
+plm_status plm_quantize_q8K(const float* x, void* xq, int64_t m, int64_t k, cudaStream_t stream) {
+    if (!x || !xq) return PLM_ERR_INVALID_ARG;
+    if (m <= 0 || k <= 0 || k % plm::QK != 0) return PLM_ERR_INVALID_ARG;
+    if (m > kMaxIndex || k > kMaxIndex || m * (k / plm::QK) > kMaxIndex) return PLM_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(xq, 4)) return PLM_ERR_MISALIGNED;
+    return cuda_status(plm::launch_quantize_q8K(x, (uint8_t*)xq, m, k, stream));
+}
+
+plm_status plm_gemv_q4K(const void* w, const void* xq, float* y, int64_t m, int64_t n, int64_t k,
+                        cudaStream_t stream) {
+    return gemv_common(4, w, xq, y, m, n, k, stream);
+}
+
+plm_status plm_gemv_q6K(const void* w, const void* xq, float* y, int64_t m, int64_t n, int64_t k,
+                        cudaStream_t stream) {
+    return gemv_common(6, w, xq, y, m, n, k, stream);
+}
+
+plm_status plm_gemm_q4K(const void* w, const void* xq, float* y, int64_t m, int64_t n, int64_t k,
+                        cudaStream_t stream) {
+    return gemm_common(4, w, xq, y, m, n, k, stream);
+}
+
+plm_status plm_gemm_q6K(const void* w, const void* xq, float* y, int64_t m, int64_t n, int64_t k,
+                        cudaStream_t stream) {
+    return gemm_common(6, w, xq, y, m, n, k, stream);
+}
+
+plm_status plm_subdots_q4K(const void* w, const void* xq, int32_t* out, int64_t m, int64_t n,
+                           int64_t k, cudaStream_t stream) {
+    return subdots_common(4, w, xq, out, m, n, k, stream);
+}
+
+plm_status plm_subdots_q6K(const void* w, const void* xq, int32_t* out, int64_t m, int64_t n,
+                           int64_t k, cudaStream_t stream) {
+    return subdots_common(6, w, xq, out, m, n, k, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,30 @@
+// Host-side declarations shared by the plm translation units.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace plm {
+
+// Number of SMs of the current device (queried per call; no cached state).
+int num_sms();
+
+cudaError_t launch_quantize_q8K(const float* x, uint8_t* xq, long long m, long long k,
+                                cudaStream_t stream);
+
+// False when one activation row of length k does not fit a CTA's shared memory.
+bool gemv_supported(int fmt, int k);
+
+// GEMV for 1 <= m <= 8 (q4_K: fmt = 4, q6_K: fmt = 6).
+cudaError_t launch_gemv(int fmt, const uint8_t* w, const uint8_t* xq, float* y,
+                        int m, int n, int k, cudaStream_t stream);
+
+// Sub-block integer dots through the GEMV's lane decode (1 <= m <= 8).
+cudaError_t launch_subdots(int fmt, const uint8_t* w, const uint8_t* xq, int32_t* out,
+                           int m, int n, int k, cudaStream_t stream);
+
+// Prefill GEMM, any m >= 1.
+cudaError_t launch_gemm(int fmt, const uint8_t* w, const uint8_t* xq, float* y,
+                        long long m, int n, int k, cudaStream_t stream);
+
+}  // namespace plm

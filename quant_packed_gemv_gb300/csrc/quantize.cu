@@ -1,0 +1,90 @@
+// q8_K activation quantization (the int8 activation step of the packed
+// matmul, PocketLLM "Current status" table, row "src/": one 256-element
+// block per task).  One warp per 256-element chunk, 8 values per lane.
+//
+// Bit-exactness with the scalar rule rests on: the first-occurrence signed
+// amax (index carried through the reduction), IEEE f32 division for
+// iscale = -128/max and d = 1/iscale (__fdiv_rn), a single rounded f32
+// multiply iscale*x (__fmul_rn, so no contraction), and round-half-even to
+// integer (__float2int_rn).
+#include "plm_device.cuh"
+#include "plm_internal.h"
+
+namespace plm {
+
+__global__ void __launch_bounds__(256) quantize_q8K_kernel(const float* __restrict__ x,
+                                                           uint8_t* __restrict__ xq,
+                                                           long long nchunks) {
+    const int lane = threadIdx.x & 31;
+    const long long warp0 = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+    for (long long ch = warp0; ch < nchunks; ch += nwarps) {
+        const float4* src = reinterpret_cast<const float4*>(x + ch * QK) + 2 * lane;
+        const float4 a = __ldg(src), b = __ldg(src + 1);
+        const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+
+        // lane-local first-occurrence amax
+        float amax = 0.0f;
+        int idx = 0x7FFFFFFF;
+        float mx = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float av = fabsf(v[i]);
+            if (av > amax) { amax = av; mx = v[i]; idx = 8 * lane + i; }
+        }
+        // warp reduction: larger magnitude wins; on equal magnitude the
+        // smaller index (the earlier element) wins
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float oa = __shfl_xor_sync(0xFFFFFFFFu, amax, o);
+            const float om = __shfl_xor_sync(0xFFFFFFFFu, mx, o);
+            const int oi = __shfl_xor_sync(0xFFFFFFFFu, idx, o);
+            if (oa > amax || (oa == amax && oi < idx)) { amax = oa; mx = om; idx = oi; }
+        }
+
+        uint8_t* blk = xq + ch * Q8K_BYTES;
+        int q[8];
+        float d;
+        if (amax == 0.0f) {
+            d = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) q[i] = 0;
+        } else {
+            const float iscale = __fdiv_rn(-128.0f, mx);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) q[i] = min(127, __float2int_rn(__fmul_rn(iscale, v[i])));
+            d = __fdiv_rn(1.0f, iscale);
+        }
+        uint32_t w0 = 0, w1 = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            w0 |= (uint32_t)(q[i] & 0xFF) << (8 * i);
+            w1 |= (uint32_t)(q[4 + i] & 0xFF) << (8 * i);
+        }
+        uint32_t* qsw = reinterpret_cast<uint32_t*>(blk + 4) + 2 * lane;
+        qsw[0] = w0;
+        qsw[1] = w1;
+        // bsums: group g = lanes 2g, 2g+1
+        int s = q[0] + q[1] + q[2] + q[3] + q[4] + q[5] + q[6] + q[7];
+        s += __shfl_xor_sync(0xFFFFFFFFu, s, 1);
+        const int s_next = __shfl_down_sync(0xFFFFFFFFu, s, 2);
+        if ((lane & 3) == 0) {   // lane 4h writes bsums[2h] and bsums[2h+1]
+            const uint32_t packed = ((uint32_t)s & 0xFFFFu) | ((uint32_t)s_next << 16);
+            reinterpret_cast<uint32_t*>(blk + 260)[lane >> 2] = packed;
+        }
+        if (lane == 0) *reinterpret_cast<float*>(blk) = d;
+    }
+}
+
+cudaError_t launch_quantize_q8K(const float* x, uint8_t* xq, long long m, long long k,
+                                cudaStream_t stream) {
+    const long long nchunks = m * (k / QK);
+    const int threads = 256;
+    long long blocks = (nchunks + 7) / 8;
+    const long long cap = (long long)num_sms() * 16;
+    if (blocks > cap) blocks = cap;
+    quantize_q8K_kernel<<<(unsigned)blocks, threads, 0, stream>>>(x, xq, nchunks);
+    return cudaGetLastError();
+}
+
+}  // namespace plm

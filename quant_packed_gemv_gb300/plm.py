@@ -1,0 +1,127 @@
+"""Python binding of libplm: the C ABI of include/plm.h, same names.
+
+Argument marshalling only.  Device buffers are torch tensors (or raw integer
+device addresses); the stream is a torch.cuda.Stream, a raw cudaStream_t
+integer, or None for torch's current stream.  Every computation runs in the
+library's CUDA kernels; there is no host or library fallback, and loading
+fails loudly when libplm.so is missing.
+"""
+import ctypes
+import os
+
+from . import build as _build
+
+PLM_OK = 0
+PLM_ERR_INVALID_ARG = 1
+PLM_ERR_MISALIGNED = 2
+PLM_ERR_UNSUPPORTED = 3
+PLM_ERR_CUDA = 4
+
+QK = 256
+Q4K_BYTES = 144
+Q6K_BYTES = 210
+Q8K_BYTES = 292
+GEMV_MAX_M = 8
+
+
+class PlmError(RuntimeError):
+    def __init__(self, fn, status, lib):
+        self.status = status
+        msg = lib.plm_status_string(status).decode()
+        if status == PLM_ERR_CUDA:
+            msg += " (cudaError %d)" % lib.plm_last_cuda_error()
+        super().__init__("%s: %s" % (fn, msg))
+
+
+_lib = None
+
+
+def library_path():
+    return _build.LIB
+
+
+def load(build_if_missing=True):
+    """Loads libplm.so (building it first if it is missing or stale)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.LIB
+    if build_if_missing and not _build.up_to_date():
+        _build.build()
+    if not os.path.exists(path):
+        raise RuntimeError("libplm.so not found at %s; run quant_packed_gemv_gb300.build" % path)
+    lib = ctypes.CDLL(path)
+    vp, i64 = ctypes.c_void_p, ctypes.c_int64
+    lib.plm_abi_version.argtypes = []
+    lib.plm_abi_version.restype = ctypes.c_int
+    lib.plm_status_string.argtypes = [ctypes.c_int]
+    lib.plm_status_string.restype = ctypes.c_char_p
+    lib.plm_last_cuda_error.argtypes = []
+    lib.plm_last_cuda_error.restype = ctypes.c_int
+    lib.plm_quantize_q8K.argtypes = [vp, vp, i64, i64, vp]
+    lib.plm_quantize_q8K.restype = ctypes.c_int
+    for name in ("plm_gemv_q4K", "plm_gemv_q6K", "plm_gemm_q4K", "plm_gemm_q6K",
+                 "plm_subdots_q4K", "plm_subdots_q6K"):
+        fn = getattr(lib, name)
+        fn.argtypes = [vp, vp, vp, i64, i64, i64, vp]
+        fn.restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def _addr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return t.data_ptr()
+
+
+def _stream(s):
+    if s is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def _check(fn, status):
+    if status != PLM_OK:
+        raise PlmError(fn, status, _lib)
+
+
+def plm_abi_version():
+    return load().plm_abi_version()
+
+
+def plm_quantize_q8K(x, xq, m, k, stream=None):
+    lib = load()
+    _check("plm_quantize_q8K", lib.plm_quantize_q8K(_addr(x), _addr(xq), m, k, _stream(stream)))
+
+
+def _mm(name):
+    def call(w, xq, y, m, n, k, stream=None):
+        lib = load()
+        _check(name, getattr(lib, name)(_addr(w), _addr(xq), _addr(y), m, n, k, _stream(stream)))
+    call.__name__ = name
+    call.__doc__ = "Binding of the C entry point %s(w, xq, out, m, n, k, stream)." % name
+    return call
+
+
+plm_gemv_q4K = _mm("plm_gemv_q4K")
+plm_gemv_q6K = _mm("plm_gemv_q6K")
+plm_gemm_q4K = _mm("plm_gemm_q4K")
+plm_gemm_q6K = _mm("plm_gemm_q6K")
+plm_subdots_q4K = _mm("plm_subdots_q4K")
+plm_subdots_q6K = _mm("plm_subdots_q6K")
+
+
+def raw_status(name, *args):
+    """Calls an entry point and returns its status code without raising
+    (used by the argument-check tests)."""
+    return getattr(load(), name)(*args)

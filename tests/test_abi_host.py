@@ -1,0 +1,77 @@
+"""Host-only checks of the C ABI: the library loads, exports every entry
+point include/plm.h declares, and rejects bad arguments before any CUDA
+call (no GPU needed; no kernel is launched by these tests)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import quant_packed_gemv_gb300 as q
+from quant_packed_gemv_gb300 import plm as P
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "plm.h")
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(plm_[A-Za-z0-9_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol():
+    lib = q.load()
+    names = declared_symbols()
+    assert "plm_gemv_q4K" in names and "plm_quantize_q8K" in names and len(names) >= 10
+    for name in names:
+        assert hasattr(lib, name), name
+
+
+def test_abi_version_and_status_strings():
+    assert q.plm_abi_version() == 1
+    lib = q.load()
+    assert lib.plm_status_string(0) == b"ok"
+    assert lib.plm_status_string(2) == b"misaligned pointer"
+    assert lib.plm_status_string(99) == b"unknown status"
+    assert lib.plm_last_cuda_error() == 0
+
+
+A = 1 << 20  # a 16-byte aligned fake address; never dereferenced: every call below is rejected
+
+
+@pytest.mark.parametrize("name", ["plm_gemv_q4K", "plm_gemv_q6K", "plm_gemm_q4K", "plm_gemm_q6K",
+                                  "plm_subdots_q4K", "plm_subdots_q6K"])
+def test_matmul_argument_checks(name):
+    st = lambda *a: P.raw_status(name, *a)  # noqa: E731
+    bad = P.PLM_ERR_INVALID_ARG
+    assert st(None, A, A, 1, 8, 256, None) == bad
+    assert st(A, None, A, 1, 8, 256, None) == bad
+    assert st(A, A, None, 1, 8, 256, None) == bad
+    assert st(A, A, A, 0, 8, 256, None) == bad
+    assert st(A, A, A, 1, 0, 256, None) == bad
+    assert st(A, A, A, 1, 8, 0, None) == bad
+    assert st(A, A, A, 1, 8, 300, None) == bad
+    assert st(A, A, A, -1, 8, 256, None) == bad
+    assert st(A, A, A, 1, 1 << 40, 256, None) == bad
+    assert st(A + 8, A, A, 1, 8, 256, None) == P.PLM_ERR_MISALIGNED
+    assert st(A, A + 2, A, 1, 8, 256, None) == P.PLM_ERR_MISALIGNED
+    assert st(A, A, A + 1, 1, 8, 256, None) == P.PLM_ERR_MISALIGNED
+    if "gemm" not in name:
+        assert st(A, A, A, 9, 8, 256, None) == bad
+
+
+def test_quantize_argument_checks():
+    st = lambda *a: P.raw_status("plm_quantize_q8K", *a)  # noqa: E731
+    bad = P.PLM_ERR_INVALID_ARG
+    assert st(None, A, 1, 256, None) == bad
+    assert st(A, None, 1, 256, None) == bad
+    assert st(A, A, 0, 256, None) == bad
+    assert st(A, A, 1, 255, None) == bad
+    assert st(A + 4, A, 1, 256, None) == P.PLM_ERR_MISALIGNED
+    assert st(A, A + 1, 1, 256, None) == P.PLM_ERR_MISALIGNED
+
+
+def test_binding_raises_on_bad_arguments():
+    with pytest.raises(q.PlmError, match="invalid argument"):
+        q.plm_gemv_q4K(A, A, A, 9, 8, 256, stream=0)

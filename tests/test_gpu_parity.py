@@ -1,0 +1,115 @@
+"""GPU parity: the CUDA library, called through its C ABI, against the oracle
+on the same seeded inputs.  Integer results (q8_K bytes, sub-block dots) must
+be bit-exact; f32 outputs must be within 1e-4 of sum_k |w_hat * x_hat|."""
+import numpy as np
+import pytest
+
+import gen
+import oracle
+from tests.gpu_helpers import (assert_close, gpu_matmul, gpu_quantize, gpu_subdots, host,
+                               make_weights, oracle_ref)
+
+pytestmark = pytest.mark.gpu
+
+
+# ------------------------------------------------------------- q8_K bytes
+
+@pytest.mark.parametrize("seed,m,k", [(0, 1, 1024), (1, 7, 2048), (2, 512, 1024), (3, 3, 256),
+                                      (4, 2, 12288)])
+def test_quantize_bit_exact(seed, m, k):
+    x = gen.normal_f32(seed, 100, m, k)
+    x[0, :256:5] = 0.0
+    x[-1, 256 % k:512 % k or k] = 0.0         # an all-zero chunk (or a zero run)
+    mx = np.abs(x[0, :256]).max()
+    x[0, 3], x[0, 7] = -mx, mx                # a magnitude tie, opposite signs
+    np.testing.assert_array_equal(host(gpu_quantize(x)), oracle.quantize_q8K(x))
+
+
+def test_quantize_scaled_and_tiny_values():
+    x = gen.normal_f32(5, 1, 4, 1024)
+    x[1] *= 1e-30
+    x[2] *= 3e30
+    x[3] = np.round(x[3] * 4) / 4            # many exact ties after scaling
+    np.testing.assert_array_equal(host(gpu_quantize(x)), oracle.quantize_q8K(x))
+
+
+# ------------------------------------------------------ integer sub-dots
+
+@pytest.mark.parametrize("fmt", ["q4K", "q6K"])
+@pytest.mark.parametrize("m,n,k", [(1, 1, 256), (1, 33, 1024), (3, 17, 1280), (8, 40, 2048),
+                                   (5, 9, 2816)])
+def test_subdots_bit_exact(fmt, m, n, k):
+    w = make_weights(fmt, 7, 0, n, k)
+    xq = oracle.quantize_q8K(gen.normal_f32(7, 200, m, k))
+    got = gpu_subdots(fmt, w, xq, m, n, k)
+    want = oracle.subdots_q4K(w, xq, m, n, k) if fmt == "q4K" else oracle.subdots_q6K(w, xq, m, n, k)
+    np.testing.assert_array_equal(got, want)
+
+
+# --------------------------------------------------------------- GEMV
+
+@pytest.mark.parametrize("fmt", ["q4K", "q6K"])
+@pytest.mark.parametrize("m", [1, 2, 3, 4, 5, 6, 7, 8])
+@pytest.mark.parametrize("n,k", [(1, 256), (37, 1024), (100, 1280), (64, 3072)])
+def test_gemv_matches_oracle(fmt, m, n, k):
+    w = make_weights(fmt, 11, 0, n, k)
+    xq = oracle.quantize_q8K(gen.normal_f32(11, 300 + m, m, k))
+    y = gpu_matmul("gemv", fmt, w, xq, m, n, k)
+    ref, S = oracle_ref(fmt, w, xq, m, n, k)
+    assert_close(y, ref, S)
+
+
+@pytest.mark.parametrize("fmt", ["q4K", "q6K"])
+def test_gemv_row_result_independent_of_m(fmt):
+    # the pages' tiled kernels are bit-identical to the single-row kernel;
+    # here activation row i must give the same bits at every m
+    n, k = 300, 2048
+    w = make_weights(fmt, 12, 0, n, k)
+    xq = oracle.quantize_q8K(gen.normal_f32(12, 1, 8, k))
+    y8 = gpu_matmul("gemv", fmt, w, xq, 8, n, k)
+    for i in range(8):
+        y1 = gpu_matmul("gemv", fmt, w, xq[i:i + 1], 1, n, k)
+        np.testing.assert_array_equal(y1[0], y8[i])
+
+
+@pytest.mark.parametrize("fmt", ["q4K", "q6K"])
+def test_gemv_adversarial_extremes(fmt):
+    # all codes at the extremes: largest integer sums the formats allow
+    from tests.packers import pack_q4K, pack_q6K
+    k, n, m = 1024, 8, 2
+    if fmt == "q4K":
+        blk = pack_q4K(2e-3, 2e-3, [63] * 8, [63] * 8, np.full(256, 15))
+    else:
+        blk = pack_q6K(2e-3, [-64] * 16, np.zeros(256, dtype=np.int64))
+    w = np.tile(blk, n * k // 256).reshape(n, -1)
+    x = np.full((m, k), -1.0, dtype=np.float32)
+    x[1, ::2] = 1.0
+    xq = oracle.quantize_q8K(x)
+    y = gpu_matmul("gemv", fmt, w, xq, m, n, k)
+    ref, S = oracle_ref(fmt, w, xq, m, n, k)
+    assert_close(y, ref, S)
+
+
+# --------------------------------------------------------------- GEMM
+
+@pytest.mark.parametrize("fmt", ["q4K", "q6K"])
+@pytest.mark.parametrize("m,n,k", [(9, 50, 1024), (17, 33, 256), (64, 128, 2048), (130, 70, 512)])
+def test_gemm_matches_oracle(fmt, m, n, k):
+    w = make_weights(fmt, 13, 0, n, k)
+    xq = oracle.quantize_q8K(gen.normal_f32(13, 400, m, k))
+    y = gpu_matmul("gemm", fmt, w, xq, m, n, k)
+    ref, S = oracle_ref(fmt, w, xq, m, n, k)
+    assert_close(y, ref, S)
+
+
+@pytest.mark.parametrize("fmt", ["q4K", "q6K"])
+def test_gemm_agrees_with_gemv_small_m(fmt):
+    n, k = 96, 1024
+    w = make_weights(fmt, 14, 0, n, k)
+    for m in (1, 5, 8):
+        xq = oracle.quantize_q8K(gen.normal_f32(14, m, m, k))
+        a = gpu_matmul("gemm", fmt, w, xq, m, n, k)
+        b = gpu_matmul("gemv", fmt, w, xq, m, n, k)
+        ref, S = oracle_ref(fmt, w, xq, m, n, k)
+        assert_close(a, ref, S)
+        assert_close(b, ref, S)
