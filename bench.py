@@ -1,23 +1,30 @@
 #!/usr/bin/env python3
 """Benchmark of the packed K-quant matmul (gemm_quant) on one GB300.
 
-Workload (one step): the Qwen3-0.6B decode GEMV set at m = 1 -- 28 layers,
-each with the q/k/v projections (2048x1024, 1024x1024, 1024x1024, stored as
-one contiguous 4096x1024 q4_K matrix because they share their input), o
-(1024x2048), gate/up (3072x1024 each, one contiguous 6144x1024 matrix) and
-down (1024x3072).  Every layer runs four dependent stages, each a q8_K
-quantization of its f32 activation followed by a q4_K decode GEMV, in layer
-order, exactly as a decode step would call them.  Weights are seeded
-synthetic q4_K blocks (seed 1); activations are N(0,1).  The 247.7 MB weight
-set is held twice and consecutive steps alternate copies, so every step reads
-its weights from HBM (each copy is larger than the 129 MB L2).
+Workload of one step: the Qwen3-0.6B decode GEMV set at m = 1.  Each of the
+28 layers holds seven distinct q4_K matrices (n x k): q 2048x1024,
+k 1024x1024, v 1024x1024, o 1024x2048, gate 3072x1024, up 3072x1024,
+down 1024x3072, laid out contiguously (247.7 MB).  Every matrix gets its own
+f32 activation row (N(0,1), seed 1).  A step quantizes all 196 activation
+rows to q8_K (one launch: all k are multiples of 256, so the rows form one
+flat array of 256-element chunks) and runs the 196 GEMVs through the grouped
+entry point (one launch).  The weight set is held twice and consecutive
+steps alternate copies; each copy is larger than the 129 MB L2, so weights
+come from HBM.
 
-Prints one JSON line (rank 0).  `value` is device time over K steps (CUDA
-graph of the C-ABI calls, inputs resident); `e2e` adds the per-step host to
-device copy of the activations and the device to host copy of the outputs;
-`roofline` is the GEMV kernel's algorithmic bytes per launch over its
-average launch time; `cpu_baseline` times the oracle on the host cores.
-`--impl reference` times the oracle alone as the reference arm.
+Reported beside it (same JSON line):
+  decode_chain  the same layers run as a decoder must run them: per layer
+                four dependent stages (qkv as one 4096-row matrix, o,
+                gate/up as one 6144-row matrix, down), each a quantize and a
+                single GEMV launch, in a CUDA graph.  Latency-bound.
+  roofline      the grouped GEMV kernel: algorithmic bytes per launch over
+                its average launch time (CUDA events on its stream).
+  e2e           the step through the C ABI with the activations copied in
+                from pinned host memory and the outputs copied back.
+  cpu_baseline  the oracle on the host cores, on a bounded sample.
+
+`--impl reference` times the oracle alone (the reference arm).
+`--case KIND FMT N K --m ...` times one entry point on one shape.
 """
 import argparse
 import json
@@ -35,14 +42,19 @@ sys.path.insert(0, ROOT)
 
 QK = 256
 Q4K_BYTES = 144
+Q6K_BYTES = 210
 Q8K_BYTES = 292
 
-# (name, n, k) per layer; q/k/v and gate/up are contiguous row ranges
-LAYER = [("qkv", 2048 + 1024 + 1024, 1024), ("o", 1024, 2048),
-         ("gate_up", 3072 + 3072, 1024), ("down", 1024, 3072)]
+# (name, n, k) of the seven matrices of one layer, in storage order
+MATS = [("q", 2048, 1024), ("k", 1024, 1024), ("v", 1024, 1024), ("o", 1024, 2048),
+        ("gate", 3072, 1024), ("up", 3072, 1024), ("down", 1024, 3072)]
+# dependent stages of a decode layer: (first matrix, number of matrices fused by rows)
+CHAIN = [(0, 3), (3, 1), (4, 2), (6, 1)]
 N_LAYERS = 28
 SEED = 1
-WORKLOAD = "qwen3-0.6b decode GEMV set, q4_K, m=1, 28 layers x (qkv, o, gate_up, down)"
+WORKLOAD = ("qwen3-0.6b decode GEMV set: 28 layers x 7 q4_K matrices "
+            "(q 2048x1024, k/v 1024x1024, o 1024x2048, gate/up 3072x1024, down 1024x3072), m=1")
+METRIC = "q4_K decode GEMV throughput (HBM GB/s of algorithmic bytes)"
 
 
 def parse():
@@ -52,33 +64,34 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="plm", choices=["plm", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--case", nargs=4, metavar=("KIND", "FMT", "N", "K"), default=None,
+                    help="time one entry point alone, e.g. --case gemv q6K 151936 2048")
+    ap.add_argument("--m", type=int, nargs="+", default=[1],
+                    help="activation rows for --case (several values: a sweep)")
     return ap.parse_args()
 
 
-def layer_bytes():
-    return sum(n * (k // QK) * Q4K_BYTES for _, n, k in LAYER)
+def mat_list():
+    """(layer, j, n, k, byte offset) of all 196 matrices in storage order."""
+    out, off = [], 0
+    for layer in range(N_LAYERS):
+        for j, (_, n, k) in enumerate(MATS):
+            out.append((layer, j, n, k, off))
+            off += n * (k // QK) * Q4K_BYTES
+    return out, off
 
 
-def step_algorithmic_bytes(m=1):
-    """Bytes the path must move per step: q4_K weights, q8_K activations
-    (written by the quantizer, read by the GEMV), f32 x in and y out."""
-    tot = 0
-    for _, n, k in LAYER:
-        nb = k // QK
-        w = n * nb * Q4K_BYTES
-        xq = m * nb * Q8K_BYTES
-        tot += w + xq + m * n * 4          # GEMV
-        tot += m * k * 4 + xq              # quantize
-    return tot * N_LAYERS
+def gemv_bytes(n, k, m=1):
+    nb = k // QK
+    return n * nb * Q4K_BYTES + m * nb * Q8K_BYTES + m * n * 4
 
 
-def gemv_bytes_per_step(m=1):
-    return N_LAYERS * sum(n * (k // QK) * Q4K_BYTES + m * (k // QK) * Q8K_BYTES + m * n * 4
-                          for _, n, k in LAYER)
+def quant_bytes(k, m=1):
+    return m * k * 4 + m * (k // QK) * Q8K_BYTES
 
 
-def weights_per_step():
-    return N_LAYERS * sum(n * k for _, n, k in LAYER)
+def step_bytes(mats):
+    return sum(gemv_bytes(n, k) + quant_bytes(k) for _, _, n, k, _ in mats)
 
 
 # --------------------------------------------------------------- clocks
@@ -97,7 +110,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -136,158 +149,75 @@ class ClockSampler:
 
 # --------------------------------------------------------------- inputs
 
-def build_inputs(torch, dev, copies=2):
+def host_inputs():
     import gen
-    nb_total = layer_bytes() * N_LAYERS
-    wcopies = []
-    host_w = np.empty(nb_total, dtype=np.uint8)
-    off = 0
-    for layer in range(N_LAYERS):
-        for j, (_, n, k) in enumerate(LAYER):
-            sz = n * (k // QK) * Q4K_BYTES
-            gen.q4K_blocks(SEED, layer * len(LAYER) + j, n, k, out=host_w[off:off + sz].reshape(n, -1))
-            off += sz
-    for _ in range(copies):
-        wcopies.append(torch.from_numpy(host_w).to(dev))
-    xs, offs = [], []
-    for layer in range(N_LAYERS):
-        for j, (_, n, k) in enumerate(LAYER):
-            xs.append(gen.normal_f32(SEED, 1000 + layer * len(LAYER) + j, 1, k))
-    return host_w, wcopies, xs
-
-
-class Plan:
-    """Device buffers and the ordered list of (quantize, GEMV) calls."""
-
-    def __init__(self, torch, dev, wcopies, xs, m=1):
-        self.torch = torch
-        self.m = m
-        self.calls = []
-        xtot = sum(x.size for x in xs)
-        self.x_host = torch.empty(xtot, dtype=torch.float32).pin_memory()
-        self.x_dev = torch.empty(xtot, dtype=torch.float32, device=dev)
-        xq_tot = sum(x.size // QK * Q8K_BYTES for x in xs)
-        self.xq = torch.empty(xq_tot, dtype=torch.uint8, device=dev)
-        ytot = N_LAYERS * sum(n for _, n, _ in LAYER) * m
-        self.y_dev = torch.empty(ytot, dtype=torch.float32, device=dev)
-        self.y_host = torch.empty(ytot, dtype=torch.float32).pin_memory()
-        xo = qo = yo = wo = 0
-        idx = 0
-        for layer in range(N_LAYERS):
-            for (_, n, k) in LAYER:
-                x = xs[idx]
-                idx += 1
-                self.x_host[xo:xo + x.size] = torch.from_numpy(x.ravel())
-                nbq = x.size // QK * Q8K_BYTES
-                self.calls.append(dict(xo=xo, qo=qo, yo=yo, wo=wo, n=n, k=k))
-                xo += x.size
-                qo += nbq
-                yo += n * m
-                wo += n * (k // QK) * Q4K_BYTES
-        self.x_dev.copy_(self.x_host)
-        self.wcopies = wcopies
-
-    def ptrs(self, c, copy):
-        return (self.x_dev.data_ptr() + 4 * c["xo"], self.xq.data_ptr() + c["qo"],
-                self.y_dev.data_ptr() + 4 * c["yo"], self.wcopies[copy].data_ptr() + c["wo"])
-
-    def run(self, q, copy, stream, quantize=True, gemv=True):
-        for c in self.calls:
-            xp, qp, yp, wp = self.ptrs(c, copy)
-            if quantize:
-                q.plm_quantize_q8K(xp, qp, self.m, c["k"], stream=stream)
-            if gemv:
-                q.plm_gemv_q4K(wp, qp, yp, self.m, c["n"], c["k"], stream=stream)
+    mats, total = mat_list()
+    host_w = np.empty(total, dtype=np.uint8)
+    for idx, (layer, j, n, k, off) in enumerate(mats):
+        sz = n * (k // QK) * Q4K_BYTES
+        gen.q4K_blocks(SEED, idx, n, k, out=host_w[off:off + sz].reshape(n, -1))
+    xs = [gen.normal_f32(SEED, 1000 + idx, 1, k) for idx, (_, _, _, k, _) in enumerate(mats)]
+    return mats, host_w, xs
 
 
 # --------------------------------------------------------------- oracle
 
-def cpu_oracle_step(xs, host_w, layers, threads):
+def cpu_oracle_pass(mats, host_w, xs, count, threads):
     import oracle
     oracle.set_threads(threads)
-    off = 0
-    idx = 0
-    for layer in range(N_LAYERS):
-        for (_, n, k) in LAYER:
-            sz = n * (k // QK) * Q4K_BYTES
-            if layer < layers:
-                xq = oracle.quantize_q8K(xs[idx])
-                oracle.gemm_q4K_f32(host_w[off:off + sz], xq, 1, n, k)
-            off += sz
-            idx += 1
+    for idx in range(count):
+        _, _, n, k, off = mats[idx]
+        sz = n * (k // QK) * Q4K_BYTES
+        xq = oracle.quantize_q8K(xs[idx])
+        oracle.gemm_q4K_f32(host_w[off:off + sz], xq, 1, n, k)
 
 
-def cpu_baseline(xs, host_w, budget_s=10.0):
-    import oracle
+def oracle_rate(mats, host_w, xs, budget_s):
+    """Times the oracle (as it stands) on the first matrices of the set,
+    as many full passes as fit the budget; returns (GB/s, sample text, cores)."""
     cores = len(os.sched_getaffinity(0))
-    layer_bytes_alg = step_algorithmic_bytes() / N_LAYERS
     t0 = time.perf_counter()
-    cpu_oracle_step(xs, host_w, 1, cores)           # warm (one layer)
-    dt1 = time.perf_counter() - t0
-    layers = max(1, min(N_LAYERS, int(budget_s / max(dt1, 1e-6) / 2)))
-    reps = 0
-    t0 = time.perf_counter()
+    cpu_oracle_pass(mats, host_w, xs, 7, cores)           # one layer, warm
+    per_layer = time.perf_counter() - t0
+    count = 7 * max(1, min(N_LAYERS, int(budget_s / 4 / max(per_layer, 1e-6))))
+    reps, t0 = 0, time.perf_counter()
     while True:
-        cpu_oracle_step(xs, host_w, layers, cores)
+        cpu_oracle_pass(mats, host_w, xs, count, cores)
         reps += 1
         el = time.perf_counter() - t0
-        if el > budget_s / 2 or reps >= 50:
+        if el > budget_s / 2:
             break
-    gbs = layer_bytes_alg * layers * reps / el / 1e9
-    return {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
-            "threads": oracle.max_threads(),
-            "sample": "%d of 28 layers x %d passes (q8_K quantize + q4_K f32 oracle GEMV, "
-                      "OpenMP over output rows), %.1f s" % (layers, reps, el)}
+    alg = step_bytes(mats[:count]) * reps
+    sample = ("%d of 196 matrices (%d of 28 layers) x %d passes: q8_K quantize + q4_K f32 oracle "
+              "GEMV, OpenMP over output rows, %.1f s" % (count, count // 7, reps, el))
+    return alg / el / 1e9, sample, cores
 
 
-# --------------------------------------------------------------- main
-
-def dist_setup(args):
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    pg = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl" if args.impl == "plm" else "gloo")
-        pg = dist
-    return world, rank, local, pg
-
-
-def run_reference(args, world, rank, pg):
+def run_reference(args, rank):
     if rank != 0:
         return
-    import gen  # noqa: F401
-    host_w = np.empty(layer_bytes() * N_LAYERS, dtype=np.uint8)
-    import gen as G
-    off = 0
-    for layer in range(N_LAYERS):
-        for j, (_, n, k) in enumerate(LAYER):
-            sz = n * (k // QK) * Q4K_BYTES
-            G.q4K_blocks(SEED, layer * len(LAYER) + j, n, k, out=host_w[off:off + sz].reshape(n, -1))
-            off += sz
-    xs = [G.normal_f32(SEED, 1000 + i, 1, k) for i, (_, _, k) in
-          enumerate([c for _ in range(N_LAYERS) for c in LAYER])]
     import oracle
+    mats, host_w, xs = host_inputs()
     cores = len(os.sched_getaffinity(0))
     t0 = time.perf_counter()
-    cpu_oracle_step(xs, host_w, 1, cores)
+    cpu_oracle_pass(mats, host_w, xs, 7, cores)
     per_layer = time.perf_counter() - t0
-    layers = max(1, min(N_LAYERS, int(2.0 / max(per_layer, 1e-6))))
+    # a step is a bounded sample so that warm-up + steps end within minutes
+    count = 7 * max(1, min(N_LAYERS, int(1.0 / max(per_layer, 1e-6))))
     for _ in range(args.warmup):
-        cpu_oracle_step(xs, host_w, layers, cores)
+        cpu_oracle_pass(mats, host_w, xs, count, cores)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        cpu_oracle_step(xs, host_w, layers, cores)
+        cpu_oracle_pass(mats, host_w, xs, count, cores)
     el = time.perf_counter() - t0
-    alg = step_algorithmic_bytes() / N_LAYERS * layers
-    val = alg * args.steps / el / 1e9
-    sample = "%d of 28 layers per step (q8_K quantize + q4_K f32 oracle GEMV, OpenMP rows)" % layers
+    val = step_bytes(mats[:count]) * args.steps / el / 1e9
+    sample = ("%d of 196 matrices per step: q8_K quantize + q4_K f32 oracle GEMV, "
+              "OpenMP over output rows" % count)
     print(json.dumps({
-        "impl": "reference", "metric": "q4_K decode GEMV throughput (HBM GB/s of algorithmic bytes)",
-        "value": val, "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "int8xint4 -> f32", "data": "synthetic",
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "s8 x u4 -> s32 -> f32", "data": "synthetic",
         "config": {"workload": WORKLOAD, "m": 1, "seed": SEED},
         "cpu_baseline": {"value": val, "unit": "GB/s", "cores": cores, "kind": "oracle",
                          "threads": oracle.max_threads(), "sample": sample},
@@ -295,40 +225,142 @@ def run_reference(args, world, rank, pg):
     }), flush=True)
 
 
+# --------------------------------------------------------------- one case
+
+def time_case(args):
+    """Times one entry point on one shape: weights rotated through enough
+    copies to exceed three times the L2, CUDA events on the launch stream."""
+    import torch
+    import gen
+    import quant_packed_gemv_gb300 as q
+    kind, fmt, n, k = args.case[0], args.case[1], int(args.case[2]), int(args.case[3])
+    torch.cuda.set_device(0)
+    nb = k // QK
+    bpb = Q4K_BYTES if fmt == "q4K" else Q6K_BYTES
+    wbytes = n * nb * bpb
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    copies = max(1, -(-3 * l2 // wbytes))
+    w_host = gen.q4K_blocks(4, 0, n, k) if fmt == "q4K" else gen.q6K_blocks(4, 0, n, k)
+    ws = [torch.from_numpy(w_host).cuda() for _ in range(copies)]
+    fn = getattr(q, "plm_%s_%s" % (kind, fmt))
+    stream = torch.cuda.Stream()
+    for m in args.m:
+        x = torch.from_numpy(gen.normal_f32(4, 9, m, k)).cuda()
+        xq = torch.empty(m * nb * Q8K_BYTES, dtype=torch.uint8, device="cuda")
+        y = torch.empty(m * n, dtype=torch.float32, device="cuda")
+        with torch.cuda.stream(stream):
+            q.plm_quantize_q8K(x, xq, m, k, stream=stream)
+            for i in range(max(args.warmup, 3)):
+                fn(ws[i % copies], xq, y, m, n, k, stream=stream)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for i in range(args.steps):
+                fn(ws[i % copies], xq, y, m, n, k, stream=stream)
+            e1.record(stream)
+            torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / args.steps
+        byt = wbytes + m * nb * Q8K_BYTES + m * n * 4
+        print(json.dumps({"case": "%s_%s" % (kind, fmt), "n": n, "k": k, "m": m, "us": us,
+                          "gbs": byt / us / 1e3, "tops": 2.0 * m * n * k / us / 1e6,
+                          "copies": copies, "fault": q.plm_device_fault()}), flush=True)
+
+
+# --------------------------------------------------------------- main arm
+
+class Step:
+    """Device buffers of one step and the C-ABI call sequences over them."""
+
+    def __init__(self, torch, dev, mats, host_w, xs):
+        self.mats = mats
+        self.w = [torch.from_numpy(host_w).to(dev) for _ in range(2)]
+        self.xoff, self.qoff, self.yoff = [], [], []
+        xo = qo = yo = 0
+        for (_, _, n, k, _) in mats:
+            self.xoff.append(xo)
+            self.qoff.append(qo)
+            self.yoff.append(yo)
+            xo += k
+            qo += k // QK * Q8K_BYTES
+            yo += n
+        self.x_host = torch.from_numpy(np.concatenate([x.ravel() for x in xs])).pin_memory()
+        self.x = self.x_host.to(dev)
+        self.xq = torch.empty(qo, dtype=torch.uint8, device=dev)
+        self.y = torch.empty(yo, dtype=torch.float32, device=dev)
+        self.y_host = torch.empty(yo, dtype=torch.float32).pin_memory()
+        self.nchunks = xo // QK
+        # grouped problem lists, one per weight copy
+        self.problems = []
+        for c in range(2):
+            wp = self.w[c].data_ptr()
+            self.problems.append([(wp + off, self.xq.data_ptr() + self.qoff[i],
+                                   self.y.data_ptr() + 4 * self.yoff[i], n, k)
+                                  for i, (_, _, n, k, off) in enumerate(mats)])
+
+    def run(self, q, copy, stream, quantize=True, gemv=True):
+        if quantize:
+            q.plm_quantize_q8K(self.x, self.xq, self.nchunks, QK, stream=stream)
+        if gemv:
+            q.plm_gemv_q4K_grouped(self.problems[copy], 1, stream=stream)
+
+    def run_chain(self, q, copy, stream):
+        """Decode order: per layer, quantize + GEMV for each dependent stage."""
+        wp = self.w[copy].data_ptr()
+        for layer in range(N_LAYERS):
+            for first, cnt in CHAIN:
+                i = layer * 7 + first
+                _, _, _, k, off = self.mats[i]
+                n = sum(self.mats[i + j][2] for j in range(cnt))
+                xq = self.xq.data_ptr() + self.qoff[i]
+                q.plm_quantize_q8K(self.x.data_ptr() + 4 * self.xoff[i], xq, 1, k, stream=stream)
+                q.plm_gemv_q4K(wp + off, xq, self.y.data_ptr() + 4 * self.yoff[i], 1, n, k, stream=stream)
+
+
 def main():
     args = parse()
-    world, rank, local, pg = dist_setup(args)
+    if args.case:
+        time_case(args)
+        return
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
-        run_reference(args, world, rank, pg)
+        run_reference(args, rank)
         return
     import torch
     import quant_packed_gemv_gb300 as q
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA GPU")
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+        pg = dist
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     q.load()
 
-    host_w, wcopies, xs = build_inputs(torch, dev)
-    plan = Plan(torch, dev, wcopies, xs)
+    mats, host_w, xs = host_inputs()
+    st = Step(torch, dev, mats, host_w, xs)
     stream = torch.cuda.Stream(device=dev)
-    launches_per_step = 2 * len(plan.calls)
 
-    # eager warm-up, then one CUDA graph per weight copy
     with torch.cuda.stream(stream):
         for i in range(max(args.warmup, 3)):
-            plan.run(q, i % 2, stream)
+            st.run(q, i % 2, stream)
+            st.run_chain(q, i % 2, stream)
     torch.cuda.synchronize()
-    graphs, gemv_graphs = [], []
-    for copy in range(2):
+    graphs, gemv_graphs, chain_graphs = [], [], []
+    for c in range(2):
+        for lst, kw in ((graphs, {}), (gemv_graphs, {"quantize": False})):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                st.run(q, c, stream, **kw)
+            lst.append(g)
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
-            plan.run(q, copy, stream)
-        graphs.append(g)
-        g2 = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g2, stream=stream):
-            plan.run(q, copy, stream, quantize=False)
-        gemv_graphs.append(g2)
+            st.run_chain(q, c, stream)
+        chain_graphs.append(g)
     torch.cuda.synchronize()
 
     def barrier():
@@ -352,36 +384,39 @@ def main():
             ms = float(t.item())
         return ms
 
+    h2d = st.x_host.numel() * 4
+    d2h = st.y_host.numel() * 4
+
+    def e2e_step(s):
+        st.x.copy_(st.x_host, non_blocking=True)
+        graphs[s % 2].replay()
+        st.y_host.copy_(st.y, non_blocking=True)
+
     with torch.cuda.stream(stream):
         for s in range(args.warmup):
             graphs[s % 2].replay()
-    sampler = ClockSampler(local)
-    sampler.start()
-    with torch.cuda.stream(stream):
+            chain_graphs[s % 2].replay()
+            e2e_step(s)
+        torch.cuda.synchronize()
+        sampler = ClockSampler(local)
+        sampler.start()
+        time.sleep(0.3)
         ms = timed(lambda s: graphs[s % 2].replay(), args.steps)
         gemv_ms = timed(lambda s: gemv_graphs[s % 2].replay(), args.steps)
-
-        # end to end: host activations in, results out, every step
-        h2d = plan.x_host.numel() * 4
-        d2h = plan.y_host.numel() * 4
-
-        def e2e_step(s):
-            plan.x_dev.copy_(plan.x_host, non_blocking=True)
-            graphs[s % 2].replay()
-            plan.y_host.copy_(plan.y_dev, non_blocking=True)
-        for s in range(2):
-            e2e_step(s)
+        chain_ms = timed(lambda s: chain_graphs[s % 2].replay(), args.steps)
         t0 = time.perf_counter()
         e2e_ms = timed(e2e_step, args.steps)
         e2e_wall = (time.perf_counter() - t0) * 1e3
-    clocks = sampler.stop()
+        clocks = sampler.stop()
+    fault = q.plm_device_fault()
 
+    alg = step_bytes(mats)
+    gemv_alg = sum(gemv_bytes(n, k) for _, _, n, k, _ in mats)
     ms_step = ms / args.steps
-    alg = step_algorithmic_bytes()
     value = world * alg / (ms_step * 1e-3) / 1e9
-    gemv_launch_ms = gemv_ms / args.steps / len(plan.calls)
-    gemv_alg_per_launch = gemv_bytes_per_step() / len(plan.calls)
-    achieved = gemv_alg_per_launch / (gemv_launch_ms * 1e-3) / 1e9
+    launches_grouped = -(-len(mats) // 256)                  # grouped GEMV launches per step
+    gemv_launch_ms = gemv_ms / args.steps / launches_grouped
+    achieved = gemv_alg / launches_grouped / (gemv_launch_ms * 1e-3) / 1e9
     peaks = {}
     try:
         peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
@@ -389,31 +424,40 @@ def main():
         pass
     peak = peaks.get("hbm_gbs", 6800.0)
     peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
-    e2e_value = world * alg / (max(e2e_ms, e2e_wall) / args.steps * 1e-3) / 1e9
+    e2e_ms_step = max(e2e_ms, e2e_wall) / args.steps
+    chain_step = chain_ms / args.steps
+    chain_bytes = sum(gemv_bytes(sum(mats[l * 7 + f + j][2] for j in range(c)), mats[l * 7 + f][3])
+                      + quant_bytes(mats[l * 7 + f][3]) for l in range(N_LAYERS) for f, c in CHAIN)
 
     out = {
-        "metric": "q4_K decode GEMV throughput (HBM GB/s of algorithmic bytes)",
-        "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "int8xint4 -> f32",
+        "scaling": "weak", "vs_baseline": None, "dtype": "s8 x u4 -> s32 -> f32",
         "data": "synthetic",
         "config": {"workload": WORKLOAD, "m": 1, "seed": SEED,
-                   "weights_mb": layer_bytes() * N_LAYERS / 1e6,
+                   "weights_mb": sum(n * (k // QK) * Q4K_BYTES for _, _, n, k, _ in mats) / 1e6,
                    "l2": "inputs larger than L2: two 247.7 MB weight copies, alternate steps",
-                   "launch": "CUDA graph of the C-ABI calls, 4 dependent (quantize, GEMV) stages per layer"},
-        "weights_per_s": world * weights_per_step() / (ms_step * 1e-3),
-        "gpu_launches": launches_per_step * args.steps,
+                   "launch": "CUDA graph: 1 q8_K quantize + %d grouped GEMV launch(es)" % launches_grouped},
+        "weights_per_s": world * sum(n * k for _, _, n, k, _ in mats) / (ms_step * 1e-3),
+        "gpu_launches": (1 + launches_grouped) * args.steps,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": None,
-                     "kernel": "gemv_q4K_kernel<1>", "peak_source": peak_src,
+                     "frac": achieved / peak, "traffic": None, "peak_source": peak_src,
+                     "kernel": "gemv_kernel<q4_K, m=1, 32 warps, grouped>",
                      "avg_launch_us": gemv_launch_ms * 1e3,
-                     "bytes_per_launch": gemv_alg_per_launch},
-        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": max(e2e_ms, e2e_wall) / args.steps},
+                     "bytes_per_launch": gemv_alg / launches_grouped},
+        "decode_chain": {"value": world * chain_bytes / (chain_step * 1e-3) / 1e9, "unit": "GB/s",
+                         "ms_per_step": chain_step, "launches_per_step": 8 * N_LAYERS,
+                         "what": "28 layers x 4 dependent (quantize, GEMV) stages, CUDA graph"},
+        "e2e": {"value": world * alg / (e2e_ms_step * 1e-3) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms_step},
         "clocks": clocks,
+        "device_fault": fault,
     }
     if rank == 0 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(xs, host_w)
+        val, sample, cores = oracle_rate(mats, host_w, xs, 12.0)
+        import oracle
+        out["cpu_baseline"] = {"value": val, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                               "threads": oracle.max_threads(), "sample": sample}
     if rank == 0:
         print(json.dumps(out), flush=True)
     if pg is not None:

@@ -70,6 +70,15 @@ const char* plm_status_string(int status);
 int plm_last_cuda_error(void);
 
 /*
+ * Diagnostic: the device fault word of the current device.  Kernels that
+ * stream through asynchronous copies bound every wait; a wait that runs out
+ * sets bit 0 here and the kernel stops (its outputs are then incomplete).
+ * *code receives the word; clear != 0 resets it.  Unlike the compute entry
+ * points this call synchronizes with the device (it copies one word).
+ */
+plm_status plm_device_fault(uint32_t* code, int clear);
+
+/*
  * q8_K activation quantization ("Current status" row "src/": activations
  * quantized to int8 the llama.cpp way, one 256-element block per task).
  * Per 256-element chunk of each row of x: the signed value `max` of largest
@@ -99,6 +108,31 @@ plm_status plm_gemv_q4K(const void* w, const void* xq, float* y,
  * [n][k/256] and must be 16-byte aligned. */
 plm_status plm_gemv_q6K(const void* w, const void* xq, float* y,
                         int64_t m, int64_t n, int64_t k, cudaStream_t stream);
+
+/*
+ * A group of independent decode GEMVs in one launch: problem j computes
+ * y_j = W_j . x_j exactly as plm_gemv_q4K(w_j, xq_j, y_j, m, n_j, k_j) would
+ * (same bits), for matrices that do not depend on one another: the q/k/v or
+ * gate/up projections of a layer kept as separate tensors, the experts of a
+ * mixture-of-experts layer, or a whole set of decode matrices.
+ *   problems : HOST array of `count` descriptors, read during the call only.
+ *   m        : activation rows of every problem, 1 <= m <= 8.
+ * Each descriptor obeys the single-GEMV rules (alignment, k % 256 == 0); the
+ * call checks all of them before launching anything.  Distinct problems may
+ * share w or xq but must not share y.
+ */
+typedef struct {
+    const void* w;    /* q4_K or q6_K [n][k/256] */
+    const void* xq;   /* q8_K [m][k/256] */
+    float* y;         /* f32 [m][n] */
+    int64_t n;
+    int64_t k;
+} plm_gemv_problem;
+
+plm_status plm_gemv_q4K_grouped(const plm_gemv_problem* problems, int64_t count, int64_t m,
+                                cudaStream_t stream);
+plm_status plm_gemv_q6K_grouped(const plm_gemv_problem* problems, int64_t count, int64_t m,
+                                cudaStream_t stream);
 
 /*
  * Prefill GEMM, y = X . W^T for any m >= 1 (intended for m = 512..2048):

@@ -8,6 +8,24 @@
 
 namespace plm {
 
+// Set (bitwise or) by kernels whose bounded wait on an asynchronous copy ran
+// out; read and cleared by plm_device_fault.  One word per device, in the
+// module's static device memory (nothing is allocated).
+__device__ unsigned g_plm_fault = 0;
+
+unsigned* fault_word() {
+    // the symbol's address is fixed per device once the module is loaded;
+    // remember it for the first 64 devices
+    static void* cache[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+    if (dev >= 0 && dev < 64 && cache[dev]) return static_cast<unsigned*>(cache[dev]);
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_plm_fault) != cudaSuccess) return nullptr;
+    if (dev >= 0 && dev < 64) cache[dev] = p;
+    return static_cast<unsigned*>(p);
+}
+
 int num_sms() {
     int dev = 0, n = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 1;
@@ -51,6 +69,32 @@ plm_status gemv_common(int fmt, const void* w, const void* xq, float* y, int64_t
                                         (int)n, (int)k, stream));
 }
 
+plm_status grouped_common(int fmt, const plm_gemv_problem* problems, int64_t count, int64_t m,
+                          cudaStream_t stream) {
+    if (!problems || count <= 0 || count > kMaxIndex) return PLM_ERR_INVALID_ARG;
+    if (m <= 0 || m > plm::GEMV_MAX_M) return PLM_ERR_INVALID_ARG;
+    constexpr int kChunk = 256;
+    plm::GroupItem items[kChunk];
+    // argument checks for every problem first, then size support
+    for (int64_t j = 0; j < count; ++j) {
+        const plm_gemv_problem& p = problems[j];
+        plm_status s = check_matmul(p.w, p.xq, p.y, m, p.n, p.k, plm::GEMV_MAX_M);
+        if (s != PLM_OK) return s;
+    }
+    for (int64_t j = 0; j < count; ++j)
+        if (!plm::gemv_supported(fmt, (int)problems[j].k)) return PLM_ERR_UNSUPPORTED;
+    for (int64_t p0 = 0; p0 < count; p0 += kChunk) {
+        const int cnt = (int)(count - p0 < kChunk ? count - p0 : kChunk);
+        for (int j = 0; j < cnt; ++j) {
+            const plm_gemv_problem& p = problems[p0 + j];
+            items[j] = plm::GroupItem{(const uint8_t*)p.w, (const uint8_t*)p.xq, p.y, (int)p.n, (int)p.k};
+        }
+        plm_status s = cuda_status(plm::launch_gemv_grouped(fmt, items, cnt, (int)m, stream));
+        if (s != PLM_OK) return s;
+    }
+    return PLM_OK;
+}
+
 plm_status gemm_common(int fmt, const void* w, const void* xq, float* y, int64_t m, int64_t n,
                        int64_t k, cudaStream_t stream) {
     plm_status s = check_matmul(w, xq, y, m, n, k, kMaxIndex);
@@ -89,6 +133,20 @@ const char* plm_status_string(int status) {
 
 int plm_last_cuda_error(void) { return g_last_cuda_error; }
 
+plm_status plm_device_fault(uint32_t* code, int clear) {
+    if (!code) return PLM_ERR_INVALID_ARG;
+    unsigned v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, plm::g_plm_fault, sizeof v);
+    if (e != cudaSuccess) return cuda_status(e);
+    *code = v;
+    if (clear && v) {
+        const unsigned zero = 0;
+        e = cudaMemcpyToSymbol(plm::g_plm_fault, &zero, sizeof zero);
+        if (e != cudaSuccess) return cuda_status(e);
+    }
+    return PLM_OK;
+}
+
 plm_status plm_quantize_q8K(const float* x, void* xq, int64_t m, int64_t k, cudaStream_t stream) {
     if (!x || !xq) return PLM_ERR_INVALID_ARG;
     if (m <= 0 || k <= 0 || k % plm::QK != 0) return PLM_ERR_INVALID_ARG;
@@ -105,6 +163,16 @@ plm_status plm_gemv_q4K(const void* w, const void* xq, float* y, int64_t m, int6
 plm_status plm_gemv_q6K(const void* w, const void* xq, float* y, int64_t m, int64_t n, int64_t k,
                         cudaStream_t stream) {
     return gemv_common(6, w, xq, y, m, n, k, stream);
+}
+
+plm_status plm_gemv_q4K_grouped(const plm_gemv_problem* problems, int64_t count, int64_t m,
+                                cudaStream_t stream) {
+    return grouped_common(4, problems, count, m, stream);
+}
+
+plm_status plm_gemv_q6K_grouped(const plm_gemv_problem* problems, int64_t count, int64_t m,
+                                cudaStream_t stream) {
+    return grouped_common(6, problems, count, m, stream);
 }
 
 plm_status plm_gemm_q4K(const void* w, const void* xq, float* y, int64_t m, int64_t n, int64_t k,

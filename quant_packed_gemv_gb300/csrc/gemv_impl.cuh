@@ -1,0 +1,603 @@
+// Decode GEMV for m = 1..8 activation rows over packed q4_K / q6_K weights
+// (PocketLLM "What it runs": K-quant weights decoded inside the kernel,
+// never widened; the weight stream is read once for all m activation rows,
+// as the pages' 8-row activation tile does on the CPU).
+//
+// One launch serves a group of independent problems {w, xq, y, n, k} that
+// share m (a single GEMV is a group of one).  The weight bytes of all
+// problems form one flat byte space, split evenly across persistent CTAs
+// (one per SM, 16 warps each).  A CTA walks the problem segments that fall in its
+// range; for each it stages the problem's q8_K activations in shared memory
+// and splits the segment's rows across its warps.
+//
+// Each warp streams its rows (one contiguous byte range of W) through its
+// own ring of shared-memory stages filled by 1-D bulk copies
+// (cp.async.bulk, completion counted on one mbarrier per stage).  A stage
+// holds whole rows when a row is small, else a 32-block (q4_K) or
+// 16-block (q6_K) chunk of one row.  The
+// first copies of a segment are issued before the CTA stages that
+// segment's activations, so the two overlap.  Every wait is bounded; a wait
+// that runs out records a fault and the warp stops computing (it still
+// takes part in every CTA barrier).
+//
+// Four lanes share one 256-weight block, so a warp handles eight blocks per
+// step.  A q4_K lane owns one 64-weight chunk (sub-blocks 2c, 2c+1); a q6_K
+// lane owns four whole 16-weight groups.  Per block and activation row a
+// lane forms exact integer dots with dp4a, applies the sub-block scales in
+// int32 and adds one f32 term.  When nb divides 8, one step covers 8/nb
+// whole rows and each row is reduced over its own 4*nb lanes; otherwise a
+// row takes ceil(nb/8) steps and is reduced over the warp.  The f32 order
+// of a row depends only on nb (explicit _rn intrinsics), so activation row
+// i gives the same bits for every m and every grouping.
+//
+// q6_K blocks are 210 bytes, so blocks are only 2-byte aligned.  A stage's
+// copy starts at the 16-byte boundary below its first block; fields are read
+// back with aligned loads and funnel shifts.  The last bytes of the matrix,
+// past its final 16-byte boundary, are read with plain loads.
+//
+// With SUBDOTS the same kernel writes the integer sub-block dots instead of
+// the f32 result (verification export).
+#pragma once
+
+#include "plm_device.cuh"
+#include "plm_internal.h"
+
+namespace plm {
+
+constexpr int BLOCKS_PER_STEP = 8;     // 32 lanes, 4 per block
+constexpr int MAX_STAGES = 8;
+constexpr int GEMV_WARPS = 16;
+constexpr int GROUP_MAX = 256;         // problems per grouped launch
+
+template <int FMT> struct Fmt;
+template <> struct Fmt<4> {
+    static constexpr int BYTES = Q4K_BYTES;
+    static constexpr int CHUNK = 32;                           // blocks per stage in row-chunk mode
+    static constexpr int PAYLOAD = CHUNK * Q4K_BYTES;          // 4608
+    static constexpr int SLOT = PAYLOAD;                       // blocks stay 16-byte aligned
+    static constexpr int SUB = 8;                              // sub-dots per block
+};
+template <> struct Fmt<6> {
+    static constexpr int BYTES = Q6K_BYTES;
+    static constexpr int CHUNK = 16;
+    static constexpr int PAYLOAD = CHUNK * Q6K_BYTES;          // 3360
+    static constexpr int SLOT = 3456;                          // + 16-byte alignment slack
+    static constexpr int SUB = 16;
+};
+
+struct GemvProblem {
+    const uint8_t* w;
+    const uint8_t* xq;
+    float* y;
+    int32_t* sub;
+    long long byte_begin;   // offset of this problem's W in the group's flat byte space
+    int n, nb;
+};
+
+template <int MAXP>
+struct GemvBatch {
+    unsigned* fault;
+    long long total_bytes;
+    int count;
+    int nstages;            // ring depth per warp
+    int act_bytes;          // 128-aligned size of the staged-activation region
+    GemvProblem p[MAXP];
+};
+
+__device__ __forceinline__ long long ceil_div_ll(long long a, long long b) { return (a + b - 1) / b; }
+
+// Geometry of one stage, from its first row and first block.
+struct StageGeom {
+    int nrows, nblk;        // rows covered; blocks per row (row-chunk mode: blocks of the chunk)
+    int bytes, tail, delta; // bulk bytes, plain-load tail bytes, first block's offset in the slot
+    long long src;          // 16-byte aligned source offset into W
+};
+
+template <int FMT>
+__device__ __forceinline__ StageGeom stage_geom(int row, int b0, int wb, int rps, int nb, long long wbytes) {
+    constexpr int BYTES = Fmt<FMT>::BYTES;
+    StageGeom g;
+    g.nrows = rps > 0 ? min(rps, wb - row) : 1;
+    g.nblk = rps > 0 ? nb : min(Fmt<FMT>::CHUNK, nb - b0);
+    const long long S = ((long long)row * nb + b0) * BYTES;
+    const long long E = S + (long long)(rps > 0 ? g.nrows * nb : g.nblk) * BYTES;
+    const long long A0 = S & ~15LL;
+    long long end = (E + 15) & ~15LL;
+    g.tail = 0;
+    if (end > wbytes) {        // never read past the end of the matrix
+        end = wbytes & ~15LL;
+        g.tail = (int)(wbytes - end);
+    }
+    g.src = A0;
+    g.bytes = (int)(end - A0);
+    g.delta = (int)(S - A0);
+    return g;
+}
+
+// The activation values one lane needs for one block of one activation row:
+//   q4_K lane t: chunks 4t..4t+3 (codes 64t .. 64t+64), bsums 4t..4t+3
+//   q6_K lane (h, p): chunks 8h+2qq+p for qq = 0..3, bsums 8h+2qq+p
+// bw[0] packs the first two bsums (low half first), bw[1] the last two.
+struct LaneAct {
+    int4 x[4];
+    int bw[2];
+    float dy;
+};
+
+// q4_K: the two bsum pairs of a chunk as 16-bit halves, (bs0+bs1) | (bs2+bs3) << 16
+__device__ __forceinline__ int q4K_pair_sums(const LaneAct& A) {
+    const int s0 = (int)(int16_t)(A.bw[0] & 0xFFFF) + (A.bw[0] >> 16);
+    const int s1 = (int)(int16_t)(A.bw[1] & 0xFFFF) + (A.bw[1] >> 16);
+    return (s0 & 0xFFFF) | (s1 << 16);
+}
+
+template <int FMT>
+__device__ __forceinline__ LaneAct act_from_smem(const ActSmem& a, int blk, int t) {
+    LaneAct r;
+    r.dy = a.dy[blk];
+    if constexpr (FMT == 4) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) r.x[u] = *act_chunk<4>(a, blk, 4 * t + u);
+        const int2 v = *reinterpret_cast<const int2*>(a.bs + (size_t)blk * 16 + 4 * t);
+        r.bw[0] = v.x;
+        r.bw[1] = v.y;
+    } else {
+        const int h = t >> 1, p = t & 1;
+#pragma unroll
+        for (int qq = 0; qq < 4; ++qq) r.x[qq] = *act_chunk<6>(a, blk, 8 * h + 2 * qq + p);
+        const int4 v = *reinterpret_cast<const int4*>(a.bs + (size_t)blk * 16 + 8 * h);
+        // words hold groups (8h+2qq, 8h+2qq+1); keep the half with parity p
+        const int g0 = p ? (v.x >> 16) : (v.x & 0xFFFF), g1 = p ? (v.y >> 16) : (v.y & 0xFFFF);
+        const int g2 = p ? (v.z >> 16) : (v.z & 0xFFFF), g3 = p ? (v.w >> 16) : (v.w & 0xFFFF);
+        r.bw[0] = (g0 & 0xFFFF) | (g1 << 16);
+        r.bw[1] = (g2 & 0xFFFF) | (g3 << 16);
+    }
+    return r;
+}
+
+// Same values straight from the q8_K bytes in global memory (4-byte aligned
+// blocks): used when a lane keeps its activations in registers.
+template <int FMT>
+__device__ __forceinline__ LaneAct act_from_global(const uint8_t* __restrict__ xq, int blk, int t) {
+    LaneAct r;
+    const uint8_t* base = xq + (size_t)blk * Q8K_BYTES;
+    r.dy = __ldg(reinterpret_cast<const float*>(base));
+    const uint32_t* qs = reinterpret_cast<const uint32_t*>(base + 4);
+    const uint32_t* bsw = reinterpret_cast<const uint32_t*>(base + 260);
+    if constexpr (FMT == 4) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const uint32_t* c = qs + 4 * (4 * t + u);
+            r.x[u] = make_int4((int)__ldg(c), (int)__ldg(c + 1), (int)__ldg(c + 2), (int)__ldg(c + 3));
+        }
+        r.bw[0] = (int)__ldg(bsw + 2 * t);
+        r.bw[1] = (int)__ldg(bsw + 2 * t + 1);
+    } else {
+        const int h = t >> 1, p = t & 1;
+        int g[4];
+#pragma unroll
+        for (int qq = 0; qq < 4; ++qq) {
+            const int c = 8 * h + 2 * qq + p;
+            const uint32_t* cp = qs + 4 * c;
+            r.x[qq] = make_int4((int)__ldg(cp), (int)__ldg(cp + 1), (int)__ldg(cp + 2), (int)__ldg(cp + 3));
+            const uint32_t wv = __ldg(bsw + (c >> 1));
+            g[qq] = p ? (int)(wv >> 16) : (int)(wv & 0xFFFF);
+        }
+        r.bw[0] = (g[0] & 0xFFFF) | (g[1] << 16);
+        r.bw[1] = (g[2] & 0xFFFF) | (g[3] << 16);
+    }
+    return r;
+}
+
+__device__ __forceinline__ int lo16(int w) { return (int)(int16_t)(w & 0xFFFF); }
+__device__ __forceinline__ int hi16(int w) { return w >> 16; }
+
+// One q4_K block: lane t = chunk c.  Adds its f32 contribution to v[] or
+// writes the exact sub-dots of sub-blocks 2c, 2c+1.
+template <int M, bool SUBDOTS>
+__device__ __forceinline__ void q4K_block(const uint8_t* blk, const LaneAct* act, const int* bsp, int b, int t,
+                                          const Q4KScaleSel& sel, float* v, int32_t* sub_row,
+                                          size_t sub_stride_i) {
+    const uint4 hdr = *reinterpret_cast<const uint4*>(blk);
+    const uint4 q0 = *reinterpret_cast<const uint4*>(blk + 16 + 32 * t);
+    const uint4 q1 = *reinterpret_cast<const uint4*>(blk + 32 + 32 * t);
+    const Q4KLane L = q4K_lane_decode(hdr, q0, q1, sel);
+#pragma unroll
+    for (int i = 0; i < M; ++i) {
+        const LaneAct& A = act[i];
+        int dlo, dhi;
+        q4K_lane_dots(L, &A.x[0], &A.x[2], dlo, dhi);
+        if constexpr (SUBDOTS) {
+            int32_t* o = sub_row + i * sub_stride_i + (size_t)b * 8 + 2 * t;
+            o[0] = dlo;
+            o[1] = dhi;
+        } else {
+            const int isum = L.sc0 * dlo + L.sc1 * dhi;
+            const int msum = dp2a_lo_su(bsp[i], L.m01, 0);
+            const float tt = __fmaf_rn(L.d, (float)isum, -__fmul_rn(L.dmin, (float)msum));
+            v[i] = __fmaf_rn(A.dy, tt, v[i]);
+        }
+    }
+}
+
+// One q6_K block at an even offset of the slot: lane t = (h, p).
+template <int M, bool SUBDOTS>
+__device__ __forceinline__ void q6K_block(const uint8_t* slot, int off, const LaneAct* act, int b, int t,
+                                          float* v, int32_t* sub_row, size_t sub_stride_i) {
+    const int h = t >> 1, p = t & 1;
+    const uint4 A = lds16_align2(slot, off + 64 * h + 16 * p);
+    const uint4 Bq = lds16_align2(slot, off + 64 * h + 32 + 16 * p);
+    const uint4 H = lds16_align2(slot, off + 128 + 32 * h + 16 * p);
+    const uint2 S = lds8_align2(slot, off + 192 + 8 * h);
+    const uint32_t dbits = *reinterpret_cast<const uint16_t*>(slot + off + 208);
+    const Q6KLane L = q6K_lane_decode(A, Bq, H, S, dbits, p);
+#pragma unroll
+    for (int i = 0; i < M; ++i) {
+        const LaneAct& X = act[i];
+        const int bsum[4] = {lo16(X.bw[0]), hi16(X.bw[0]), lo16(X.bw[1]), hi16(X.bw[1])};
+        int isum = 0;
+#pragma unroll
+        for (int qq = 0; qq < 4; ++qq) {
+            const int dot = q6K_lane_raw(L, qq, X.x[qq]) - 32 * bsum[qq];
+            if constexpr (SUBDOTS)
+                sub_row[i * sub_stride_i + (size_t)b * 16 + 8 * h + 2 * qq + p] = dot;
+            else
+                isum += L.sc[qq] * dot;
+        }
+        if constexpr (!SUBDOTS) v[i] = __fmaf_rn(__fmul_rn(L.d, X.dy), (float)isum, v[i]);
+    }
+}
+
+// AREG: each lane keeps the activations of its (at most two) block columns
+// in registers for the whole segment; requires nb <= 16 and no SUBDOTS.
+template <int FMT, int M, bool SUBDOTS, int WARPS, int MAXP, bool AREG>
+__global__ void __launch_bounds__(WARPS * 32, 1) gemv_kernel(const __grid_constant__ GemvBatch<MAXP> B) {
+    constexpr int SLOT = Fmt<FMT>::SLOT;
+    constexpr int PAYLOAD = Fmt<FMT>::PAYLOAD;
+    constexpr int BYTES = Fmt<FMT>::BYTES;
+    static_assert(!(AREG && SUBDOTS), "register activations serve the f32 path only");
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int quad = lane >> 2, t = lane & 3;
+    const Q4KScaleSel sel = q4K_scale_sel(t);
+    const int NS = B.nstages;
+    uint8_t* ring = smem + B.act_bytes + (size_t)warp * NS * SLOT;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + B.act_bytes + (size_t)WARPS * NS * SLOT) + warp * NS;
+    if (lane == 0) {
+        for (int j = 0; j < NS; ++j) mbar_init(&bars[j], 1);
+        fence_barrier_init();
+    }
+    __syncwarp();
+
+    const long long T = B.total_bytes;
+    const long long B0 = T * blockIdx.x / gridDim.x;
+    const long long B1 = T * (blockIdx.x + 1) / gridDim.x;
+    uint32_t issued = 0, consumed = 0;   // ring counters, uniform in the warp
+    bool ok = true;                      // false once a wait ran out
+
+    for (int pi = 0; pi < B.count; ++pi) {
+        const GemvProblem& P = B.p[pi];
+        const long long rowbytes = (long long)P.nb * BYTES;
+        const long long P0 = P.byte_begin;
+        const long long P1 = P0 + (long long)P.n * rowbytes;
+        if (P1 <= B0 || P0 >= B1) continue;                       // CTA-uniform
+        // rows whose first byte falls in [B0, B1)
+        const int ra = (int)ceil_div_ll(B0 > P0 ? B0 - P0 : 0, rowbytes);
+        const long long rb_ll = ceil_div_ll(B1 - P0, rowbytes);
+        const int rb = (int)(rb_ll < P.n ? rb_ll : P.n);
+        if (ra >= rb) continue;                                    // CTA-uniform
+        const int wa = ra + (int)((long long)(rb - ra) * warp / WARPS);
+        const int wb = ra + (int)((long long)(rb - ra) * (warp + 1) / WARPS);
+        const int nb = P.nb;
+        const long long wbytes = (long long)P.n * rowbytes;
+        const int rps = rowbytes <= PAYLOAD ? (int)(PAYLOAD / rowbytes) : 0;
+        const int per_row = rps > 0 ? 1 : (nb + Fmt<FMT>::CHUNK - 1) / Fmt<FMT>::CHUNK;
+        const int nst = wb > wa ? (rps > 0 ? (wb - wa + rps - 1) / rps : (wb - wa) * per_row) : 0;
+
+        // issue cursor (uniform); lane 0 performs the copies
+        int irow = wa, ib0 = 0, inext = 0;
+        auto issue_one = [&]() {
+            const StageGeom g = stage_geom<FMT>(irow, ib0, wb, rps, nb, wbytes);
+            if (lane == 0) {
+                uint64_t* bar = &bars[issued % NS];
+                uint8_t* dst = ring + (issued % NS) * SLOT;
+                if (g.bytes > 0) {
+                    mbar_arrive_expect_tx(bar, (uint32_t)g.bytes);
+                    bulk_g2s(dst, P.w + g.src, (uint32_t)g.bytes, bar);
+                } else {
+                    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(smem_u32(bar)) : "memory");
+                }
+            }
+            ++issued;
+            ++inext;
+            if (rps > 0) {
+                irow += rps;
+            } else {
+                ib0 += Fmt<FMT>::CHUNK;
+                if (ib0 >= nb) { ib0 = 0; ++irow; }
+            }
+        };
+        if (ok)
+            while (inext < nst && issued - consumed < (uint32_t)NS) issue_one();
+
+        const bool packed = nb <= BLOCKS_PER_STEP && (BLOCKS_PER_STEP % nb) == 0;
+        ActSmem act{};
+        LaneAct areg[AREG ? 2 : 1][M];
+        int absp[AREG ? 2 : 1][M];
+        if constexpr (AREG) {
+            // this lane's block columns: packed rows -> quad % nb; otherwise quad and quad + 8
+            if (nst > 0) {
+                const int b0 = packed ? quad % nb : quad;
+#pragma unroll
+                for (int i = 0; i < M; ++i) {
+                    if (b0 < nb) {
+                        areg[0][i] = act_from_global<FMT>(P.xq, i * nb + b0, t);
+                        absp[0][i] = q4K_pair_sums(areg[0][i]);
+                    }
+                    if (!packed && b0 + 8 < nb) {
+                        areg[1][i] = act_from_global<FMT>(P.xq, i * nb + b0 + 8, t);
+                        absp[1][i] = q4K_pair_sums(areg[1][i]);
+                    }
+                }
+            }
+        } else {
+            __syncthreads();                   // every warp is done with the previous activations
+            act = act_smem_carve(smem, M, nb);
+            act_smem_fill<FMT>(act, P.xq, M, nb);
+            __syncthreads();
+        }
+
+        const size_t sub_stride_i = (size_t)P.n * nb * Fmt<FMT>::SUB;
+        float acc[M];
+#pragma unroll
+        for (int i = 0; i < M; ++i) acc[i] = 0.0f;
+        int crow = wa, cb0 = 0;
+
+        // processes block bb of row rr of the slot; jreg selects the register column
+        auto do_block = [&](uint8_t* slot, const StageGeom& g, int rr, int bb, int b, int jreg, float* v,
+                            int32_t* sub_row) {
+            LaneAct la[M];
+            int lbsp[M];
+            if constexpr (AREG) {
+#pragma unroll
+                for (int i = 0; i < M; ++i) {
+                    la[i] = areg[jreg][i];
+                    lbsp[i] = absp[jreg][i];
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < M; ++i) {
+                    la[i] = act_from_smem<FMT>(act, i * nb + b, t);
+                    lbsp[i] = q4K_pair_sums(la[i]);
+                }
+            }
+            const int off = g.delta + (rr * nb + bb) * BYTES;
+            if constexpr (FMT == 4)
+                q4K_block<M, SUBDOTS>(slot + off, la, lbsp, b, t, sel, v, sub_row, sub_stride_i);
+            else
+                q6K_block<M, SUBDOTS>(slot, off, la, b, t, v, sub_row, sub_stride_i);
+        };
+
+        for (int s = 0; s < nst && ok; ++s) {
+            const uint32_t slot_i = consumed % NS;
+            if (!mbar_wait(&bars[slot_i], (consumed / NS) & 1)) {
+                // a copy never completed: record it, let our other copies land, stop computing
+                if (lane == 0) {
+                    atomicOr(B.fault, 1u);
+                    for (uint32_t c2 = consumed; c2 < issued; ++c2) (void)mbar_wait(&bars[c2 % NS], (c2 / NS) & 1);
+                }
+                __syncwarp();
+                ok = false;
+                break;
+            }
+            uint8_t* slot = ring + slot_i * SLOT;
+            const StageGeom g = stage_geom<FMT>(crow, cb0, wb, rps, nb, wbytes);
+            if (FMT == 6 && g.tail > 0) {
+                if (lane < g.tail) slot[g.bytes + lane] = P.w[g.src + g.bytes + lane];
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+            }
+            if (packed) {
+                // each step covers 8/nb whole rows; a row owns 4*nb lanes
+                const int rpstep = BLOCKS_PER_STEP / nb;
+                const int j = quad / nb, bq = quad - j * nb;
+                for (int r0 = 0; r0 < g.nrows; r0 += rpstep) {
+                    const int rr = r0 + j;
+                    const int row = crow + rr;
+                    float v[M];
+#pragma unroll
+                    for (int i = 0; i < M; ++i) v[i] = 0.0f;
+                    int32_t* sub_row = SUBDOTS ? P.sub + (size_t)row * nb * Fmt<FMT>::SUB : nullptr;
+                    if (rr < g.nrows) do_block(slot, g, rr, bq, bq, 0, v, sub_row);
+                    if constexpr (!SUBDOTS) {
+#pragma unroll
+                        for (int i = 0; i < M; ++i) {
+                            float x = v[i];
+                            for (int o = 2 * nb; o >= 1; o >>= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, o);
+                            if ((lane & (4 * nb - 1)) == 0 && rr < g.nrows) P.y[(size_t)i * P.n + row] = x;
+                        }
+                    }
+                }
+            } else {
+                for (int rr = 0; rr < g.nrows; ++rr) {
+                    const int row = crow + rr;
+                    int32_t* sub_row = SUBDOTS ? P.sub + (size_t)row * nb * Fmt<FMT>::SUB : nullptr;
+                    if constexpr (AREG) {
+                        // whole rows, nb <= 16: at most two blocks per lane
+                        if (quad < nb) do_block(slot, g, rr, quad, quad, 0, acc, sub_row);
+                        if (quad + 8 < nb) do_block(slot, g, rr, quad + 8, quad + 8, 1, acc, sub_row);
+                    } else {
+                        for (int bb = quad; bb < g.nblk; bb += BLOCKS_PER_STEP)
+                            do_block(slot, g, rr, bb, cb0 + bb, 0, acc, sub_row);
+                    }
+                    const bool row_end = rps > 0 || cb0 + g.nblk >= nb;
+                    if (row_end) {
+                        if constexpr (!SUBDOTS) {
+#pragma unroll
+                            for (int i = 0; i < M; ++i) {
+                                const float x = warp_sum(acc[i]);
+                                if (lane == 0) P.y[(size_t)i * P.n + row] = x;
+                                acc[i] = 0.0f;
+                            }
+                        }
+                    }
+                }
+            }
+            ++consumed;
+            if (rps > 0) {
+                crow += rps;
+            } else {
+                cb0 += Fmt<FMT>::CHUNK;
+                if (cb0 >= nb) { cb0 = 0; ++crow; }
+            }
+            __syncwarp();
+            if (inext < nst) issue_one();
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+inline int smem_optin_bytes() {
+    int dev = 0, optin = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    return optin;
+}
+
+inline size_t act_bytes_aligned(int m, int nb) { return (act_smem_bytes(m, nb) + 127) & ~(size_t)127; }
+
+template <int FMT>
+inline int ring_depth(int m, int nb, int warps) {
+    const long long budget = (long long)smem_optin_bytes() - (long long)act_bytes_aligned(m, nb);
+    const long long per_stage = (long long)warps * (Fmt<FMT>::SLOT + 8);
+    long long ns = budget / per_stage;
+    if (ns > MAX_STAGES) ns = MAX_STAGES;
+    return ns >= 2 ? (int)ns : 0;
+}
+
+template <int FMT>
+inline size_t gemv_smem(int m, int nb, int ns, int warps) {
+    return act_bytes_aligned(m, nb) + (size_t)warps * ns * (Fmt<FMT>::SLOT + 8);
+}
+
+struct HostProblem {
+    const uint8_t* w;
+    const uint8_t* xq;
+    float* y;
+    int32_t* sub;
+    int n, nb;
+};
+
+template <int FMT, int M, bool SUB, int WARPS, int MAXP, bool AREG>
+cudaError_t launch_batch(const HostProblem* hp, int count, int max_nb, int ns, cudaStream_t stream) {
+    GemvBatch<MAXP> B;
+    B.fault = fault_word();
+    if (!B.fault) return cudaErrorInvalidDevicePointer;
+    long long off = 0, rows = 0;
+    for (int i = 0; i < count; ++i) {
+        B.p[i].w = hp[i].w;
+        B.p[i].xq = hp[i].xq;
+        B.p[i].y = hp[i].y;
+        B.p[i].sub = hp[i].sub;
+        B.p[i].byte_begin = off;
+        B.p[i].n = hp[i].n;
+        B.p[i].nb = hp[i].nb;
+        off += (long long)hp[i].n * hp[i].nb * Fmt<FMT>::BYTES;
+        rows += hp[i].n;
+    }
+    B.total_bytes = off;
+    B.count = count;
+    B.nstages = ns;
+    B.act_bytes = AREG ? 0 : (int)act_bytes_aligned(M, max_nb);
+    const size_t smem = (size_t)B.act_bytes + (size_t)WARPS * ns * (Fmt<FMT>::SLOT + 8);
+    const void* fn = (const void*)gemv_kernel<FMT, M, SUB, WARPS, MAXP, AREG>;
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    long long grid = num_sms();
+    const long long want = (rows + 7) / 8;
+    if (grid > want) grid = want;
+    if (grid < 1) grid = 1;
+    gemv_kernel<FMT, M, SUB, WARPS, MAXP, AREG><<<(unsigned)grid, WARPS * 32, smem, stream>>>(B);
+    return cudaGetLastError();
+}
+
+// Launches one pass (all problems share m = M rows of activations).
+template <int FMT, int M, bool SUB>
+cudaError_t launch_pass(const HostProblem* hp, int count, int max_nb, cudaStream_t stream) {
+    if constexpr (!SUB && M <= 2) {
+        // activations in registers: rows of at most 16 blocks
+        if (max_nb <= 16) {
+            const int ns = ring_depth<FMT>(0, max_nb, GEMV_WARPS);
+            if (count == 1) return launch_batch<FMT, M, SUB, GEMV_WARPS, 1, true>(hp, count, max_nb, ns, stream);
+            return launch_batch<FMT, M, SUB, GEMV_WARPS, GROUP_MAX, true>(hp, count, max_nb, ns, stream);
+        }
+    }
+    const int ns = ring_depth<FMT>(M, max_nb, GEMV_WARPS);
+    if (ns < 2) return cudaErrorInvalidConfiguration;
+    if constexpr (SUB) {
+        return launch_batch<FMT, M, SUB, GEMV_WARPS, 1, false>(hp, count, max_nb, ns, stream);
+    } else {
+        if (count == 1) return launch_batch<FMT, M, SUB, GEMV_WARPS, 1, false>(hp, count, max_nb, ns, stream);
+        return launch_batch<FMT, M, SUB, GEMV_WARPS, GROUP_MAX, false>(hp, count, max_nb, ns, stream);
+    }
+}
+
+template <int FMT, bool SUB>
+cudaError_t dispatch_m(int m, const HostProblem* hp, int count, int max_nb, cudaStream_t stream) {
+    switch (m) {
+        case 1: return launch_pass<FMT, 1, SUB>(hp, count, max_nb, stream);
+        case 2: return launch_pass<FMT, 2, SUB>(hp, count, max_nb, stream);
+        case 3: return launch_pass<FMT, 3, SUB>(hp, count, max_nb, stream);
+        case 4: return launch_pass<FMT, 4, SUB>(hp, count, max_nb, stream);
+        case 5: return launch_pass<FMT, 5, SUB>(hp, count, max_nb, stream);
+        case 6: return launch_pass<FMT, 6, SUB>(hp, count, max_nb, stream);
+        case 7: return launch_pass<FMT, 7, SUB>(hp, count, max_nb, stream);
+        case 8: return launch_pass<FMT, 8, SUB>(hp, count, max_nb, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+// Rows of activations per pass so that the staged activations leave room
+// for a ring of at least two stages (16 warps).  The work split and the f32
+// order of a row do not depend on m, so splitting m changes no bits.
+template <int FMT>
+int gemv_rows_per_pass(int m, int max_nb) {
+    int step = m;
+    while (step > 1 && ring_depth<FMT>(step, max_nb, GEMV_WARPS) == 0) --step;
+    return ring_depth<FMT>(step, max_nb, GEMV_WARPS) ? step : 0;
+}
+
+// Runs a group of problems with m activation rows each (1 <= m <= 8),
+// taking the activation rows in passes and the problems GROUP_MAX at a time.
+template <int FMT>
+cudaError_t run_group(const HostProblem* probs, int count, int m, bool subdots, cudaStream_t stream) {
+    int max_nb = 1;
+    for (int i = 0; i < count; ++i) max_nb = probs[i].nb > max_nb ? probs[i].nb : max_nb;
+    const int step = gemv_rows_per_pass<FMT>(m, max_nb);
+    if (step < 1) return cudaErrorInvalidConfiguration;
+    HostProblem part[GROUP_MAX];
+    for (int i0 = 0; i0 < m; i0 += step) {
+        const int mm = m - i0 < step ? m - i0 : step;
+        for (int p0 = 0; p0 < count; p0 += GROUP_MAX) {
+            const int cnt = count - p0 < GROUP_MAX ? count - p0 : GROUP_MAX;
+            int pnb = 1;
+            for (int j = 0; j < cnt; ++j) {
+                const HostProblem& s = probs[p0 + j];
+                part[j] = s;
+                part[j].xq = s.xq + (size_t)i0 * s.nb * Q8K_BYTES;
+                part[j].y = s.y ? s.y + (size_t)i0 * s.n : nullptr;
+                part[j].sub = s.sub ? s.sub + (size_t)i0 * s.n * s.nb * Fmt<FMT>::SUB : nullptr;
+                pnb = s.nb > pnb ? s.nb : pnb;
+            }
+            const cudaError_t e = subdots ? dispatch_m<FMT, true>(mm, part, cnt, pnb, stream)
+                                          : dispatch_m<FMT, false>(mm, part, cnt, pnb, stream);
+            if (e != cudaSuccess) return e;
+        }
+    }
+    return cudaSuccess;
+}
+
+}  // namespace plm

@@ -1,0 +1,12 @@
+// q4_K instantiation of the decode GEMV (kernel in gemv_impl.cuh).
+#include "gemv_impl.cuh"
+
+namespace plm {
+
+cudaError_t run_group_q4K(const HostProblem* p, int count, int m, bool subdots, cudaStream_t stream) {
+    return run_group<4>(p, count, m, subdots, stream);
+}
+
+bool gemv_supported_q4K(int k) { return gemv_rows_per_pass<4>(1, k / QK) > 0; }
+
+}  // namespace plm

@@ -1,0 +1,12 @@
+// q6_K instantiation of the decode GEMV (kernel in gemv_impl.cuh).
+#include "gemv_impl.cuh"
+
+namespace plm {
+
+cudaError_t run_group_q6K(const HostProblem* p, int count, int m, bool subdots, cudaStream_t stream) {
+    return run_group<6>(p, count, m, subdots, stream);
+}
+
+bool gemv_supported_q6K(int k) { return gemv_rows_per_pass<6>(1, k / QK) > 0; }
+
+}  // namespace plm

@@ -31,30 +31,46 @@ __device__ __forceinline__ int dp4a(int a, int b, int c) { return __dp4a(a, b, c
 
 // ---------------------------------------------------------------------------
 // q8_K activations staged in shared memory, re-laid out for aligned access:
-//   q8  : int8  [M][k]          (16-byte aligned rows)
-//   dy  : float [M][nb]
-//   bs  : int16 [M][nb][16]
+//   q8  : int8  [M*nb][256]     16-byte chunks XOR-swizzled per block
+//   bs  : int16 [M*nb][16]      (32 bytes per block, 16-byte aligned)
+//   dy  : float [M*nb]
+// Chunk c (bytes 16c..16c+15) of staged block blk sits at chunk slot
+// act_swizzle<FMT>(c, blk).  The swizzle spreads the four lanes of a block,
+// and the two blocks of an 8-lane phase, over distinct bank groups for the
+// access pattern of each format's lane decode.
 // ---------------------------------------------------------------------------
 struct ActSmem {
     int8_t* q8;
-    float* dy;
     int16_t* bs;
+    float* dy;
 };
 
+template <int FMT>
+__host__ __device__ __forceinline__ int act_swizzle(int c, int blk) {
+    const int x = FMT == 4 ? (blk & 1) : ((blk & 1) << 2);
+    return c ^ ((c >> 3) << 1) ^ x;
+}
+
+template <int FMT>
+__device__ __forceinline__ const int4* act_chunk(const ActSmem& a, int blk, int c) {
+    return reinterpret_cast<const int4*>(a.q8 + (size_t)blk * QK + 16 * act_swizzle<FMT>(c, blk));
+}
+
 __host__ __device__ inline size_t act_smem_bytes(int m, int nb) {
-    return (size_t)m * nb * QK + (size_t)m * nb * 4 + (size_t)m * nb * 32;
+    return (size_t)m * nb * (QK + 32 + 4);
 }
 
 __device__ __forceinline__ ActSmem act_smem_carve(uint8_t* base, int m, int nb) {
     ActSmem a;
     a.q8 = reinterpret_cast<int8_t*>(base);
-    a.dy = reinterpret_cast<float*>(base + (size_t)m * nb * QK);
-    a.bs = reinterpret_cast<int16_t*>(base + (size_t)m * nb * QK + (size_t)m * nb * 4);
+    a.bs = reinterpret_cast<int16_t*>(base + (size_t)m * nb * QK);
+    a.dy = reinterpret_cast<float*>(base + (size_t)m * nb * (QK + 32));
     return a;
 }
 
 // Copies m*nb q8_K blocks (4-byte aligned) into the staged layout. All
 // threads of the CTA take part; the caller synchronizes afterwards.
+template <int FMT>
 __device__ __forceinline__ void act_smem_fill(const ActSmem& a, const uint8_t* __restrict__ xq,
                                               int m, int nb) {
     const uint32_t* src = reinterpret_cast<const uint32_t*>(xq);
@@ -63,13 +79,14 @@ __device__ __forceinline__ void act_smem_fill(const ActSmem& a, const uint8_t* _
     uint32_t* q8w = reinterpret_cast<uint32_t*>(a.q8);
     uint32_t* bsw = reinterpret_cast<uint32_t*>(a.bs);
     for (int idx = threadIdx.x; idx < total; idx += blockDim.x) {
-        int blk = idx / words_per_block;
-        int wd = idx - blk * words_per_block;
-        uint32_t v = __ldg(src + idx);
+        const int blk = idx / words_per_block;
+        const int wd = idx - blk * words_per_block;
+        const uint32_t v = __ldg(src + idx);
         if (wd == 0) {
             a.dy[blk] = __uint_as_float(v);
         } else if (wd <= 64) {
-            q8w[blk * 64 + (wd - 1)] = v;
+            const int w = wd - 1;
+            q8w[blk * 64 + 4 * act_swizzle<FMT>(w >> 2, blk) + (w & 3)] = v;
         } else {
             bsw[blk * 8 + (wd - 65)] = v;
         }
@@ -77,99 +94,141 @@ __device__ __forceinline__ void act_smem_fill(const ActSmem& a, const uint8_t* _
 }
 
 // ---------------------------------------------------------------------------
-// q4_K, one block handled by 8 lanes.  Lane t (0..7) owns qs bytes
-// [16t, 16t+16): chunk c = t/2, half p = t%2, i.e. weights
-//   64c + 16p + [0,16)       in the low nibbles  (sub-block 2c)
-//   64c + 32 + 16p + [0,16)  in the high nibbles (sub-block 2c+1)
+// q4_K, one block handled by 4 lanes.  Lane c (0..3) owns the 64-weight
+// chunk c: qs bytes [32c, 32c+32).  Byte 32c+l holds weight 64c+l in its low
+// nibble (sub-block 2c) and weight 64c+32+l in its high nibble (sub-block
+// 2c+1), l = 0..31.
 // ---------------------------------------------------------------------------
-struct Q4KLane {
-    float d, dmin;
-    int sc_lo, sc_hi, m_lo, m_hi;
-    uint32_t lo[4], hi[4];  // 16 four-bit codes each, one per byte
+
+// Mixed-sign 4-way byte dot: unsigned bytes of a times signed bytes of b.
+__device__ __forceinline__ int dp4a_us(uint32_t a, int b, int c) {
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// Two-way dot: signed 16-bit halves of a times unsigned bytes 0, 1 of b.
+__device__ __forceinline__ int dp2a_lo_su(int a, uint32_t b, int c) {
+    int d;
+    asm("dp2a.lo.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// Per-lane constants of the 6-bit scale/min table decode for chunk c:
+// pairs 0..3 sit in the low six bits of scale bytes 0..3 (scales) and 4..7
+// (mins); pairs 4..7 take their low four bits from the nibbles of bytes
+// 8..11 and their top two bits from bits 6-7 of bytes 0..7.
+struct Q4KScaleSel {
+    uint32_t mask_lo, mask_hi;   // 0x3F3F3F3F, 0 (c < 2) or 0x0F0F0F0F, 0x30303030 (c >= 2)
+    int pick_w;                  // c >= 2: take the low bits from scale bytes 8..11
+    int sh;                      // bit offset of pair 2c (mod 4) in the selected word
 };
 
-// hdr: bytes 0..15 of the block (d, dmin, scales[12]); qv: qs[16t..16t+15]
-__device__ __forceinline__ Q4KLane q4K_lane_decode(uint4 hdr, uint4 qv, int t) {
+__device__ __forceinline__ Q4KScaleSel q4K_scale_sel(int c) {
+    Q4KScaleSel s;
+    s.pick_w = c >= 2;
+    s.mask_lo = s.pick_w ? 0x0F0F0F0Fu : 0x3F3F3F3Fu;
+    s.mask_hi = s.pick_w ? 0x30303030u : 0u;
+    s.sh = 16 * (c & 1);
+    return s;
+}
+
+struct Q4KLane {
+    float d, dmin;
+    int sc0, sc1;        // scales of sub-blocks 2c and 2c+1
+    uint32_t m01;        // mins of sub-blocks 2c, 2c+1 in bytes 0, 1
+    uint32_t q[8];       // the chunk's 32 code bytes (low nibble: sub-block 2c, high: 2c+1)
+};
+
+// hdr: bytes 0..15 of the block (d, dmin, scales[12]);
+// q0, q1: qs[32c .. 32c+16) and qs[32c+16 .. 32c+32)
+__device__ __forceinline__ Q4KLane q4K_lane_decode(uint4 hdr, uint4 q0, uint4 q1, const Q4KScaleSel& S) {
     Q4KLane L;
     L.d = half_bits_to_float(hdr.x);
     L.dmin = half_bits_to_float(hdr.x >> 16);
-    const int c = t >> 1;
-    uint32_t scw, mw;
-    if (c < 2) {   // pairs 0..3: low six bits of scale bytes 0..3 / 4..7
-        scw = hdr.y & 0x3F3F3F3Fu;
-        mw = hdr.z & 0x3F3F3F3Fu;
-    } else {       // pairs 4..7: nibbles of bytes 8..11 + top bits of bytes 0..7
-        scw = (hdr.w & 0x0F0F0F0Fu) | ((hdr.y >> 2) & 0x30303030u);
-        mw = ((hdr.w >> 4) & 0x0F0F0F0Fu) | ((hdr.z >> 2) & 0x30303030u);
-    }
-    const int sh = 16 * (c & 1);
-    L.sc_lo = (scw >> sh) & 0xFF;
-    L.sc_hi = (scw >> (sh + 8)) & 0xFF;
-    L.m_lo = (mw >> sh) & 0xFF;
-    L.m_hi = (mw >> (sh + 8)) & 0xFF;
-    const uint32_t q[4] = {qv.x, qv.y, qv.z, qv.w};
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-        L.lo[u] = q[u] & 0x0F0F0F0Fu;
-        L.hi[u] = (q[u] >> 4) & 0x0F0F0F0Fu;
-    }
+    const uint32_t scw = ((S.pick_w ? hdr.w : hdr.y) & S.mask_lo) | ((hdr.y >> 2) & S.mask_hi);
+    const uint32_t mw = ((S.pick_w ? (hdr.w >> 4) : hdr.z) & S.mask_lo) | ((hdr.z >> 2) & S.mask_hi);
+    L.sc0 = (scw >> S.sh) & 0xFF;
+    L.sc1 = (scw >> (S.sh + 8)) & 0xFF;
+    L.m01 = mw >> S.sh;
+    L.q[0] = q0.x; L.q[1] = q0.y; L.q[2] = q0.z; L.q[3] = q0.w;
+    L.q[4] = q1.x; L.q[5] = q1.y; L.q[6] = q1.z; L.q[7] = q1.w;
     return L;
 }
 
-// Integer dots of the lane's 16 low-nibble and 16 high-nibble weights against
-// the matching activation codes (q8lo at weight 64c+16p, q8hi at 64c+32+16p).
-__device__ __forceinline__ void q4K_lane_dots(const Q4KLane& L, int4 q8lo, int4 q8hi,
+// Exact integer dots of sub-blocks 2c (against the activation codes at
+// 64c .. 64c+32, words xl) and 2c+1 (64c+32 .. 64c+64, words xh).  The high
+// nibbles are used in place (16 * q), so their dot is divided by 16, exactly.
+__device__ __forceinline__ void q4K_lane_dots(const Q4KLane& L, const int4 xlo[2], const int4 xhi[2],
                                               int& dlo, int& dhi) {
-    dlo = dp4a((int)L.lo[0], q8lo.x, 0);
-    dlo = dp4a((int)L.lo[1], q8lo.y, dlo);
-    dlo = dp4a((int)L.lo[2], q8lo.z, dlo);
-    dlo = dp4a((int)L.lo[3], q8lo.w, dlo);
-    dhi = dp4a((int)L.hi[0], q8hi.x, 0);
-    dhi = dp4a((int)L.hi[1], q8hi.y, dhi);
-    dhi = dp4a((int)L.hi[2], q8hi.z, dhi);
-    dhi = dp4a((int)L.hi[3], q8hi.w, dhi);
+    const int xl[8] = {xlo[0].x, xlo[0].y, xlo[0].z, xlo[0].w, xlo[1].x, xlo[1].y, xlo[1].z, xlo[1].w};
+    const int xh[8] = {xhi[0].x, xhi[0].y, xhi[0].z, xhi[0].w, xhi[1].x, xhi[1].y, xhi[1].z, xhi[1].w};
+    int lo = 0, hi = 0;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        lo = dp4a_us(L.q[u] & 0x0F0F0F0Fu, xl[u], lo);
+        hi = dp4a_us(L.q[u] & 0xF0F0F0F0u, xh[u], hi);
+    }
+    dlo = lo;
+    dhi = hi >> 4;
 }
 
 // ---------------------------------------------------------------------------
-// q6_K, one block handled by 8 lanes.  Lane t: half h = t/4, u = t%4 owns
-// l in [8u, 8u+8) of every quarter of half h, i.e. the weights
-//   128h + 32*qq + 8u + [0,8),  qq = 0..3
-// Quarter qq takes its low 4 bits from ql[64h + 32*(qq&1) + l] (low nibble
-// for qq < 2, high nibble otherwise) and its top 2 bits from bits 2qq..2qq+1
-// of qh[32h + l].  Its scale / 16-group is 8h + 2qq + u/2.
+// q6_K, one block handled by 4 lanes.  Lane t: half h = t/2, p = t%2 owns
+// l in [16p, 16p+16) of every quarter qq of half h, i.e. the weights
+//   128h + 32qq + 16p + [0,16)  =  the whole 16-group G = 8h + 2qq + p.
+// Quarter qq takes its low 4 bits from ql[64h + 32(qq&1) + l] (low nibble for
+// qq < 2, high nibble otherwise) and its top 2 bits from bits 2qq..2qq+1 of
+// qh[32h + l].
 // ---------------------------------------------------------------------------
 struct Q6KLane {
     float d;
-    int sc[4];          // scale of quarter qq's group
-    uint32_t code[4][2];  // 8 six-bit codes per quarter, one per byte
+    int sc[4];               // scale of group 8h + 2qq + p
+    uint32_t code[4][4];     // 16 six-bit codes per quarter, one per byte
 };
 
-// qlA = ql[64h+8u .. +8], qlB = ql[64h+32+8u .. +8], qhv = qh[32h+8u .. +8],
-// scw = scales[8h .. 8h+8] (i8), dbits = f16 d
-__device__ __forceinline__ Q6KLane q6K_lane_decode(uint2 qlA, uint2 qlB, uint2 qhv, uint2 scw,
-                                                   uint32_t dbits, int u) {
+// A = ql[64h+16p .. +16], B = ql[64h+32+16p .. +16], H = qh[32h+16p .. +16],
+// S = scales[8h .. 8h+8] (i8), dbits = f16 d
+__device__ __forceinline__ Q6KLane q6K_lane_decode(uint4 A, uint4 B, uint4 H, uint2 S, uint32_t dbits, int p) {
     Q6KLane L;
     L.d = half_bits_to_float(dbits);
-    const uint32_t sca[2] = {scw.x, scw.y};
+    const uint32_t a[4] = {A.x, A.y, A.z, A.w};
+    const uint32_t bq[4] = {B.x, B.y, B.z, B.w};
+    const uint32_t hh[4] = {H.x, H.y, H.z, H.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        L.code[0][i] = (a[i] & 0x0F0F0F0Fu) | ((hh[i] << 4) & 0x30303030u);
+        L.code[1][i] = (bq[i] & 0x0F0F0F0Fu) | ((hh[i] << 2) & 0x30303030u);
+        L.code[2][i] = ((a[i] >> 4) & 0x0F0F0F0Fu) | (hh[i] & 0x30303030u);
+        L.code[3][i] = ((bq[i] >> 4) & 0x0F0F0F0Fu) | ((hh[i] >> 2) & 0x30303030u);
+    }
+    const uint32_t sw[2] = {S.x, S.y};
 #pragma unroll
     for (int qq = 0; qq < 4; ++qq) {
-        const int byte = 2 * qq + (u >> 1);   // index into scales[8h..8h+8)
-        L.sc[qq] = (int)(int8_t)((sca[byte >> 2] >> (8 * (byte & 3))) & 0xFF);
-        const uint2 src = (qq & 1) ? qlB : qlA;
-        const int nsh = (qq & 2) ? 4 : 0;
-        const int hsh = 2 * qq;
-        L.code[qq][0] = ((src.x >> nsh) & 0x0F0F0F0Fu) | (((qhv.x >> hsh) & 0x03030303u) << 4);
-        L.code[qq][1] = ((src.y >> nsh) & 0x0F0F0F0Fu) | (((qhv.y >> hsh) & 0x03030303u) << 4);
+        const int byte = 2 * qq + p;
+        L.sc[qq] = (int)(int8_t)((sw[byte >> 2] >> (8 * (byte & 3))) & 0xFFu);
     }
     return L;
 }
 
-// Raw (unshifted) dots: sum over the lane's 8 weights of quarter qq of q6*q8,
-// q6 in 0..63.  The -32 offset is applied with the q8_K bsums:
-//   dot_g = raw(lane u even) + raw(lane u odd) - 32*bsum_g.
-__device__ __forceinline__ int q6K_lane_raw(const Q6KLane& L, int qq, int2 q8v) {
-    int r = dp4a((int)L.code[qq][0], q8v.x, 0);
-    return dp4a((int)L.code[qq][1], q8v.y, r);
+// Raw dot of quarter qq's 16 codes (q6 in 0..63) with the activation codes
+// x8 at 128h + 32qq + 16p.  The exact group dot is raw - 32*bsum_G.
+__device__ __forceinline__ int q6K_lane_raw(const Q6KLane& L, int qq, int4 x8) {
+    int r = dp4a((int)L.code[qq][0], x8.x, 0);
+    r = dp4a((int)L.code[qq][1], x8.y, r);
+    r = dp4a((int)L.code[qq][2], x8.z, r);
+    return dp4a((int)L.code[qq][3], x8.w, r);
+}
+
+// Reads 16 bytes at an even (2-byte aligned) shared-memory offset using
+// aligned 4-byte loads and funnel shifts.
+__device__ __forceinline__ uint4 lds16_align2(const uint8_t* base, int off) {
+    const int a = off & ~3;
+    const uint32_t* p = reinterpret_cast<const uint32_t*>(base + a);
+    const uint32_t w0 = p[0], w1 = p[1], w2 = p[2], w3 = p[3], w4 = p[4];
+    const int sh = (off & 3) * 8;
+    return make_uint4(__funnelshift_r(w0, w1, sh), __funnelshift_r(w1, w2, sh),
+                      __funnelshift_r(w2, w3, sh), __funnelshift_r(w3, w4, sh));
 }
 
 // Reads 8 bytes at an even (2-byte aligned) shared-memory offset using
@@ -189,6 +248,60 @@ __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
     return v;
+}
+
+}  // namespace plm
+
+// ---------------------------------------------------------------------------
+// mbarrier + bulk-copy (TMA, 1-D) helpers.  Every wait is bounded: a wait that
+// runs out sets a device fault word and returns false, and the caller stops
+// issuing work.
+// ---------------------------------------------------------------------------
+namespace plm {
+
+constexpr unsigned WAIT_LIMIT = 1u << 16;   // try_wait rounds before giving up (each up to SUSPEND_NS)
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                 :: "r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+// Returns true once the phase with the given parity has completed, false if
+// WAIT_LIMIT rounds pass first.  Each round lets the hardware suspend the
+// warp for up to SUSPEND_NS (it resumes as soon as the phase completes), so
+// waiting warps do not spin on the issue slots.
+constexpr unsigned SUSPEND_NS = 20000;
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+    const uint32_t a = smem_u32(bar);
+    for (unsigned it = 0; it < WAIT_LIMIT; ++it) {
+        uint32_t done;
+        asm volatile("{\n\t.reg .pred p;\n\t"
+                     "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+                     "selp.u32 %0, 1, 0, p;\n\t}"
+                     : "=r"(done) : "r"(a), "r"(parity), "r"(SUSPEND_NS) : "memory");
+        if (done) return true;
+    }
+    return false;
+}
+
+// Bulk copy global -> shared (this CTA), completion counted on `bar`.
+// src and dst 16-byte aligned, bytes a positive multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 :: "r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
 }
 
 }  // namespace plm

@@ -9,6 +9,10 @@ namespace plm {
 // Number of SMs of the current device (queried per call; no cached state).
 int num_sms();
 
+// Device address of the library's fault word on the current device (set by a
+// kernel whose bounded wait ran out), or nullptr if it cannot be resolved.
+unsigned* fault_word();
+
 cudaError_t launch_quantize_q8K(const float* x, uint8_t* xq, long long m, long long k,
                                 cudaStream_t stream);
 
@@ -18,6 +22,15 @@ bool gemv_supported(int fmt, int k);
 // GEMV for 1 <= m <= 8 (q4_K: fmt = 4, q6_K: fmt = 6).
 cudaError_t launch_gemv(int fmt, const uint8_t* w, const uint8_t* xq, float* y,
                         int m, int n, int k, cudaStream_t stream);
+
+// A group of independent GEMVs sharing m, in one launch per 256 problems.
+struct GroupItem {
+    const uint8_t* w;
+    const uint8_t* xq;
+    float* y;
+    int n, k;
+};
+cudaError_t launch_gemv_grouped(int fmt, const GroupItem* items, int count, int m, cudaStream_t stream);
 
 // Sub-block integer dots through the GEMV's lane decode (1 <= m <= 8).
 cudaError_t launch_subdots(int fmt, const uint8_t* w, const uint8_t* xq, int32_t* out,

@@ -33,6 +33,11 @@ class PlmError(RuntimeError):
         super().__init__("%s: %s" % (fn, msg))
 
 
+class _Problem(ctypes.Structure):
+    _fields_ = [("w", ctypes.c_void_p), ("xq", ctypes.c_void_p), ("y", ctypes.c_void_p),
+                ("n", ctypes.c_int64), ("k", ctypes.c_int64)]
+
+
 _lib = None
 
 
@@ -58,8 +63,14 @@ def load(build_if_missing=True):
     lib.plm_status_string.restype = ctypes.c_char_p
     lib.plm_last_cuda_error.argtypes = []
     lib.plm_last_cuda_error.restype = ctypes.c_int
+    lib.plm_device_fault.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]
+    lib.plm_device_fault.restype = ctypes.c_int
     lib.plm_quantize_q8K.argtypes = [vp, vp, i64, i64, vp]
     lib.plm_quantize_q8K.restype = ctypes.c_int
+    for name in ("plm_gemv_q4K_grouped", "plm_gemv_q6K_grouped"):
+        fn = getattr(lib, name)
+        fn.argtypes = [ctypes.POINTER(_Problem), i64, i64, vp]
+        fn.restype = ctypes.c_int
     for name in ("plm_gemv_q4K", "plm_gemv_q6K", "plm_gemm_q4K", "plm_gemm_q6K",
                  "plm_subdots_q4K", "plm_subdots_q6K"):
         fn = getattr(lib, name)
@@ -99,6 +110,14 @@ def plm_abi_version():
     return load().plm_abi_version()
 
 
+def plm_device_fault(clear=True):
+    """Reads (and by default clears) the device fault word; synchronizes."""
+    lib = load()
+    code = ctypes.c_uint32(0)
+    _check("plm_device_fault", lib.plm_device_fault(ctypes.byref(code), 1 if clear else 0))
+    return code.value
+
+
 def plm_quantize_q8K(x, xq, m, k, stream=None):
     lib = load()
     _check("plm_quantize_q8K", lib.plm_quantize_q8K(_addr(x), _addr(xq), m, k, _stream(stream)))
@@ -119,6 +138,23 @@ plm_gemm_q4K = _mm("plm_gemm_q4K")
 plm_gemm_q6K = _mm("plm_gemm_q6K")
 plm_subdots_q4K = _mm("plm_subdots_q4K")
 plm_subdots_q6K = _mm("plm_subdots_q6K")
+
+
+def _grouped(name):
+    def call(problems, m, stream=None):
+        """problems: sequence of (w, xq, y, n, k) with device tensors or addresses."""
+        lib = load()
+        arr = (_Problem * len(problems))()
+        for j, (w, xq, y, n, k) in enumerate(problems):
+            arr[j] = _Problem(_addr(w), _addr(xq), _addr(y), n, k)
+        _check(name, getattr(lib, name)(arr, len(problems), m, _stream(stream)))
+    call.__name__ = name
+    call.__doc__ = "Binding of %s(problems, count, m, stream)." % name
+    return call
+
+
+plm_gemv_q4K_grouped = _grouped("plm_gemv_q4K_grouped")
+plm_gemv_q6K_grouped = _grouped("plm_gemv_q6K_grouped")
 
 
 def raw_status(name, *args):

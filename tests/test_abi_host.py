@@ -75,3 +75,17 @@ def test_quantize_argument_checks():
 def test_binding_raises_on_bad_arguments():
     with pytest.raises(q.PlmError, match="invalid argument"):
         q.plm_gemv_q4K(A, A, A, 9, 8, 256, stream=0)
+
+
+def test_grouped_argument_checks():
+    import ctypes
+    lib = q.load()
+    arr = (P._Problem * 2)()
+    arr[0] = P._Problem(A, A, A, 8, 256)
+    arr[1] = P._Problem(A, A, A, 8, 300)          # bad k in the second problem
+    assert lib.plm_gemv_q4K_grouped(arr, 2, 1, None) == P.PLM_ERR_INVALID_ARG
+    arr[1] = P._Problem(A + 8, A, A, 8, 256)      # misaligned w
+    assert lib.plm_gemv_q6K_grouped(arr, 2, 1, None) == P.PLM_ERR_MISALIGNED
+    assert lib.plm_gemv_q4K_grouped(arr, 0, 1, None) == P.PLM_ERR_INVALID_ARG
+    assert lib.plm_gemv_q4K_grouped(arr, 1, 9, None) == P.PLM_ERR_INVALID_ARG
+    assert lib.plm_gemv_q4K_grouped(None, 1, 1, None) == P.PLM_ERR_INVALID_ARG

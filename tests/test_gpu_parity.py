@@ -113,3 +113,34 @@ def test_gemm_agrees_with_gemv_small_m(fmt):
         ref, S = oracle_ref(fmt, w, xq, m, n, k)
         assert_close(a, ref, S)
         assert_close(b, ref, S)
+
+
+# ------------------------------------------------------- grouped GEMV
+
+@pytest.mark.parametrize("fmt", ["q4K", "q6K"])
+@pytest.mark.parametrize("m", [1, 3, 8])
+def test_grouped_gemv_equals_single_calls(fmt, m):
+    import torch
+    import quant_packed_gemv_gb300 as q
+    from tests.gpu_helpers import dev
+    shapes = [(40, 1024), (7, 256), (130, 2048), (33, 3072), (1, 1280), (64, 512)]
+    probs, want = [], []
+    for j, (n, k) in enumerate(shapes):
+        w = make_weights(fmt, 20 + j, 0, n, k)
+        xq = oracle.quantize_q8K(gen.normal_f32(20 + j, m, m, k))
+        ref, S = oracle_ref(fmt, w, xq, m, n, k)
+        single = gpu_matmul("gemv", fmt, w, xq, m, n, k)
+        assert_close(single, ref, S)
+        wd, xd = dev(w), dev(xq)
+        y = torch.full((m, n), float("nan"), device="cuda")
+        probs.append((wd, xd, y, n, k))
+        want.append(single)
+    getattr(q, "plm_gemv_%s_grouped" % fmt)(probs, m)
+    torch.cuda.synchronize()
+    for (_, _, y, _, _), single in zip(probs, want):
+        np.testing.assert_array_equal(y.cpu().numpy(), single)
+
+
+def test_no_device_fault_recorded():
+    import quant_packed_gemv_gb300 as q
+    assert q.plm_device_fault() == 0
