@@ -25,7 +25,10 @@
  *   y  f32  [m][n]       y[i][r] = sum over k of x_hat[i][.] * w_hat[r][.]
  *
  * Ownership and ordering: every pointer is a DEVICE pointer owned by the
- * caller; the library allocates nothing and never synchronizes.  Each call
+ * caller.  The library never synchronizes.  It allocates nothing, except
+ * that plm_gemm_q4K / plm_gemm_q6K take their temporary workspace from the
+ * device's stream-ordered pool (cudaMallocAsync / cudaFreeAsync on the
+ * call's stream); the _ws forms use a workspace the caller passes.  Each call
  * enqueues its work on `stream` (0 = the legacy default stream) and returns
  * at once; results are visible to later work on that stream.  y is
  * overwritten, never accumulated into.  Calls on different streams that
@@ -135,15 +138,35 @@ plm_status plm_gemv_q6K_grouped(const plm_gemv_problem* problems, int64_t count,
                                 cudaStream_t stream);
 
 /*
- * Prefill GEMM, y = X . W^T for any m >= 1 (intended for m = 512..2048):
- * weight tiles are decoded in shared memory into exact integer-valued
- * operands and contracted on the tensor cores; per-block scales are applied
- * in f32.  Same buffers, layouts and tolerance as the GEMV; no limit on m.
+ * Prefill GEMM, y = X . W^T for any m >= 1 (intended for m = 512..2048).
+ * For m >= 9 the activation codes are first widened to an f16 matrix in a
+ * workspace; weight tiles are decoded in shared memory into exact
+ * integer-valued f16 operands (q4_K: sc*q; q6_K: sc*(q6-32)) and contracted
+ * on the tensor cores (tcgen05, f32 accumulation in tensor memory), one
+ * 256-weight block at a time; the per-block scales are applied in f32.
+ * For m <= 8 it runs the decode GEMV.  Same buffers, layouts and tolerance
+ * as the GEMV; no limit on m.  These two forms take the workspace from the
+ * stream-ordered pool of the current device.
  */
 plm_status plm_gemm_q4K(const void* w, const void* xq, float* y,
                         int64_t m, int64_t n, int64_t k, cudaStream_t stream);
 plm_status plm_gemm_q6K(const void* w, const void* xq, float* y,
                         int64_t m, int64_t n, int64_t k, cudaStream_t stream);
+
+/* Workspace bytes plm_gemm_q4K_ws (fmt = 4) / plm_gemm_q6K_ws (fmt = 6)
+ * need for m activation rows of length k (0 when none is needed, and for
+ * invalid arguments). */
+size_t plm_gemm_workspace_size(int fmt, int64_t m, int64_t k);
+
+/* The GEMM with a caller-owned device workspace of at least
+ * plm_gemm_workspace_size bytes, 256-byte aligned (may be null when that
+ * size is 0).  The workspace must not be used by other work until the call's
+ * kernels have finished on `stream`.  PLM_ERR_INVALID_ARG if it is too
+ * small. */
+plm_status plm_gemm_q4K_ws(const void* w, const void* xq, float* y, int64_t m, int64_t n, int64_t k,
+                           void* workspace, size_t workspace_bytes, cudaStream_t stream);
+plm_status plm_gemm_q6K_ws(const void* w, const void* xq, float* y, int64_t m, int64_t n, int64_t k,
+                           void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
  * Verification export: the integer sub-block dots computed by the same

@@ -105,6 +105,19 @@ plm_status gemm_common(int fmt, const void* w, const void* xq, float* y, int64_t
                                         (int)k, stream));
 }
 
+plm_status gemm_ws_common(int fmt, const void* w, const void* xq, float* y, int64_t m, int64_t n,
+                          int64_t k, void* ws, size_t ws_bytes, cudaStream_t stream) {
+    plm_status s = check_matmul(w, xq, y, m, n, k, kMaxIndex);
+    if (s != PLM_OK) return s;
+    if (m * n > (int64_t)1 << 40) return PLM_ERR_INVALID_ARG;
+    const size_t need = plm::gemm_workspace_need(fmt, m, (int)k);
+    if (need > 0 && (!ws || ws_bytes < need)) return PLM_ERR_INVALID_ARG;
+    if (ws && !aligned(ws, 256)) return PLM_ERR_MISALIGNED;
+    if (!plm::gemv_supported(fmt, (int)k)) return PLM_ERR_UNSUPPORTED;
+    return cuda_status(plm::launch_gemm_ws(fmt, (const uint8_t*)w, (const uint8_t*)xq, y, m, (int)n, (int)k,
+                                           ws, ws_bytes, stream));
+}
+
 plm_status subdots_common(int fmt, const void* w, const void* xq, int32_t* out, int64_t m,
                           int64_t n, int64_t k, cudaStream_t stream) {
     plm_status s = check_matmul(w, xq, out, m, n, k, plm::GEMV_MAX_M);
@@ -183,6 +196,21 @@ plm_status plm_gemm_q4K(const void* w, const void* xq, float* y, int64_t m, int6
 plm_status plm_gemm_q6K(const void* w, const void* xq, float* y, int64_t m, int64_t n, int64_t k,
                         cudaStream_t stream) {
     return gemm_common(6, w, xq, y, m, n, k, stream);
+}
+
+size_t plm_gemm_workspace_size(int fmt, int64_t m, int64_t k) {
+    if ((fmt != 4 && fmt != 6) || m <= 0 || k <= 0 || k % plm::QK != 0 || k > kMaxIndex) return 0;
+    return plm::gemm_workspace_need(fmt, m, (int)k);
+}
+
+plm_status plm_gemm_q4K_ws(const void* w, const void* xq, float* y, int64_t m, int64_t n, int64_t k,
+                           void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    return gemm_ws_common(4, w, xq, y, m, n, k, workspace, workspace_bytes, stream);
+}
+
+plm_status plm_gemm_q6K_ws(const void* w, const void* xq, float* y, int64_t m, int64_t n, int64_t k,
+                           void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    return gemm_ws_common(6, w, xq, y, m, n, k, workspace, workspace_bytes, stream);
 }
 
 plm_status plm_subdots_q4K(const void* w, const void* xq, int32_t* out, int64_t m, int64_t n,

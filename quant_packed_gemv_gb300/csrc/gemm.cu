@@ -1,21 +1,534 @@
-// Prefill GEMM entry.  First version: the activation rows are taken eight at
-// a time through the decode GEMV kernels (correct for any m; W is re-read
-// once per group of eight rows).
+// Prefill GEMM over packed q4_K / q6_K weights on the 5th-generation tensor
+// cores (tcgen05, kind::f16), for m >= 9 activation rows (PocketLLM "What
+// it runs": weights stay packed and are decoded inside the kernel; the
+// matmul is a dense contraction once m is large).
+//
+// Exactness.  Per 256-weight block the method needs exact integers:
+//   q4_K: isum = sum_j sc_j * sum_l q*q8 and msum = sum_g m_(g/2) * bsum_g,
+//         term = d_x*d_w*isum - dmin_x*d_w*msum;
+//   q6_K: isum = sum_g sc_g * sum_l (q6-32)*q8, term = d_x*d_w*isum.
+// The operands are integer-valued and exact in f16: activation codes
+// q8 in [-128, 127]; q4_K weights sc*q <= 945; q6_K weights sc*(q6-32) in
+// [-2048, 2048]; bsums in [-2048, 2048]; mins <= 63.  Products and partial
+// sums are integers accumulated in f32, exact while below 2^24 (only an
+// adversarial block can exceed it; the f32 rounding there is far inside the
+// 1e-4 tolerance).  Because d, dmin and d_x change every block, each block
+// accumulates into fresh TMEM columns and is drained and scaled in f32.
+//
+// Tile: 128 weight rows (MMA M, TMEM lanes) x 128 activation rows (MMA N,
+// TMEM columns).  Roles per CTA (9 warps):
+//   warps 0-3 (producers): thread t decodes weight row t of the tile into
+//     the A operand (f16, 128-byte swizzled K-major, one 64-wide K stage
+//     at a time), writes the per-block min operands and scales, and warp 0
+//     issues the TMA load of the activation stage (f16, same layout) from
+//     the workspace the pre-pass fills;
+//   warp 8 (one thread): issues the MMAs (M=128, N=128, K=16) and commits;
+//   warps 4-7 (epilogue): drain D1/D2 of each block from TMEM, apply the
+//     scales and accumulate the result in registers; store y at the end.
+// A ring of 4 operand stages, double-buffered per-block min operands and
+// scales, and double-buffered TMEM accumulators (2 x (128 + 128) columns)
+// keep the roles overlapped.  Every wait is bounded; a wait that runs out
+// records a fault and the kernel winds down.
+#include <cuda.h>
+#include <cuda_fp16.h>
+
 #include "plm_device.cuh"
 #include "plm_internal.h"
 
 namespace plm {
 
-cudaError_t launch_gemm(int fmt, const uint8_t* w, const uint8_t* xq, float* y,
-                        long long m, int n, int k, cudaStream_t stream) {
+constexpr int GT = 128;                 // tile rows (weights) and columns (activations)
+constexpr int KS = 64;                  // K per operand stage (one 128-byte swizzle row)
+constexpr int NSTAGE = 4;
+constexpr int TILE_BYTES = GT * KS * 2; // 16 KB per operand tile
+constexpr int GEMM_THREADS = 9 * 32;
+
+struct GemmSmem {
+    // offsets from the 1024-aligned base
+    static constexpr int RING = 0;                                  // NSTAGE x (A, B)
+    static constexpr int MIN = RING + NSTAGE * 2 * TILE_BYTES;      // 2 x 16 KB
+    static constexpr int SCL = MIN + 2 * TILE_BYTES;                // 2 x (d, dmin, dx) x 128 f32
+    static constexpr int BAR = SCL + 2 * 3 * GT * 4;
+    static constexpr int NBAR = 2 * NSTAGE + 8;
+    static constexpr int TMEMP = BAR + NBAR * 8;
+    static constexpr int BYTES = TMEMP + 16;
+};
+constexpr int GEMM_SMEM = GemmSmem::BYTES + 1024;   // + alignment slack
+
+// byte offset of element (row, k) in a 128-row x 64-wide f16 tile with the
+// 128-byte swizzle (16-byte chunk index XOR row % 8)
+__device__ __forceinline__ uint32_t sw128_chunk(int row, int chunk) {
+    return (uint32_t)((row >> 3) * 1024 + (row & 7) * 128 + (((chunk ^ (row & 7)) & 7) << 4));
+}
+
+// tcgen05 shared-memory matrix descriptor: K-major, 128-byte swizzle,
+// 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr) {
+    return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// instruction descriptor: D f32, A/B f16, both K-major, M = 128, N = 128
+constexpr uint32_t IDESC_F16_128x128 = (1u << 4) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
+
+__device__ __forceinline__ void mma_f16(uint32_t dtmem, uint64_t da, uint64_t db, uint32_t accumulate) {
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+                 :: "r"(dtmem), "l"(da), "l"(db), "r"(IDESC_F16_128x128), "r"(accumulate));
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 :: "r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.expect_tx.shared::cta.b64 [%0], %1;" :: "r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                 " [%0], [%1, {%2, %3}], [%4];"
+                 :: "r"(smem_u32(dst)), "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+                 "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                   "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+                   "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+                   "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+                   "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+                 : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+                 "%14,%15}, [%16];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                   "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+                   "=r"(r[14]), "=r"(r[15])
+                 : "r"(taddr));
+}
+
+__device__ __forceinline__ void fence_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+__device__ __forceinline__ __half2 bits_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
+
+// ---------------------------------------------------------------------------
+// Weight decoders (one thread = one weight row of the tile)
+// ---------------------------------------------------------------------------
+// q4_K: stage c of a block is chunk c (weights 64c .. 64c+63): K positions
+// 0..31 are the low nibbles of qs[32c .. 32c+31] times sc_(2c), positions
+// 32..63 the high nibbles times sc_(2c+1).
+struct Q4KRow {
+    uint4 raw[9];            // the 144-byte block
+    float d, dmin;
+    uint32_t sc_lo2[4], off_lo2[4], sc_hi2[4], off_hi2[4];   // per chunk c: f16x2 constants
+    int mins[8];
+};
+
+__device__ __forceinline__ void q4K_row_prepare(Q4KRow& R) {
+    const uint4 hdr = R.raw[0];
+    R.d = half_bits_to_float(hdr.x);
+    R.dmin = half_bits_to_float(hdr.x >> 16);
+    const uint32_t sc_a = hdr.y & 0x3F3F3F3Fu;
+    const uint32_t m_a = hdr.z & 0x3F3F3F3Fu;
+    const uint32_t sc_b = (hdr.w & 0x0F0F0F0Fu) | ((hdr.y >> 2) & 0x30303030u);
+    const uint32_t m_b = ((hdr.w >> 4) & 0x0F0F0F0Fu) | ((hdr.z >> 2) & 0x30303030u);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const uint32_t scw = c < 2 ? sc_a : sc_b;
+        const int sh = 16 * (c & 1);
+        const float slo = (float)((scw >> sh) & 0xFF), shi = (float)((scw >> (sh + 8)) & 0xFF);
+        // low nibble magic: (1024 + q) * sc - 1024 * sc; high: (1024 + 16q) * sc/16 - 64 * sc
+        R.sc_lo2[c] = h2_bits(__float2half2_rn(slo));
+        R.off_lo2[c] = h2_bits(__float2half2_rn(-1024.0f * slo));
+        R.sc_hi2[c] = h2_bits(__float2half2_rn(shi * 0.0625f));
+        R.off_hi2[c] = h2_bits(__float2half2_rn(-64.0f * shi));
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const uint32_t mw = j < 4 ? m_a : m_b;
+        R.mins[j] = (mw >> (8 * (j & 3))) & 0xFF;
+    }
+}
+
+// writes the 64 f16 values of stage c into row `row` of a swizzled tile
+__device__ __forceinline__ void q4K_row_stage(const Q4KRow& R, int c, uint8_t* tile, int row) {
+    const uint4 qa = R.raw[1 + 2 * c], qb = R.raw[2 + 2 * c];
+    const uint32_t q[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+    const __half2 slo = bits_h2(R.sc_lo2[c]), olo = bits_h2(R.off_lo2[c]);
+    const __half2 shi = bits_h2(R.sc_hi2[c]), ohi = bits_h2(R.off_hi2[c]);
+#pragma unroll
+    for (int ch = 0; ch < 4; ++ch) {          // 16-byte chunk ch: positions 8ch .. 8ch+7 (and 32 + ...)
+        uint32_t lo[4], hi[4];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint32_t w = q[2 * ch + h];
+            const uint32_t x01 = __byte_perm(w, 0, 0x4140), x23 = __byte_perm(w, 0, 0x4342);
+            lo[2 * h] = h2_bits(__hfma2(bits_h2((x01 & 0x000F000Fu) | 0x64006400u), slo, olo));
+            lo[2 * h + 1] = h2_bits(__hfma2(bits_h2((x23 & 0x000F000Fu) | 0x64006400u), slo, olo));
+            hi[2 * h] = h2_bits(__hfma2(bits_h2((x01 & 0x00F000F0u) | 0x64006400u), shi, ohi));
+            hi[2 * h + 1] = h2_bits(__hfma2(bits_h2((x23 & 0x00F000F0u) | 0x64006400u), shi, ohi));
+        }
+        *reinterpret_cast<uint4*>(tile + sw128_chunk(row, ch)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        *reinterpret_cast<uint4*>(tile + sw128_chunk(row, ch + 4)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// The GEMM kernel (q4_K)
+// ---------------------------------------------------------------------------
+struct GemmArgs {
+    const uint8_t* w;        // q4_K [n][nb]
+    const uint8_t* xq;       // q8_K [m][nb]
+    float* y;                // [m][n]
+    unsigned* fault;
+    int m, n, nb;
+};
+
+__global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_q4K_kernel(const __grid_constant__ CUtensorMap xmap,
+                                                                   const GemmArgs A) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + GemmSmem::BAR);
+    uint64_t* full = bars;                  // [NSTAGE], 4 producer-warp arrivals + TMA bytes
+    uint64_t* empty = bars + NSTAGE;        // [NSTAGE], MMA commit
+    uint64_t* minfull = bars + 2 * NSTAGE;  // [2], 4 producer-warp arrivals
+    uint64_t* minempty = minfull + 2;       // [2], MMA commit
+    uint64_t* tfull = minfull + 4;          // [2], MMA commit
+    uint64_t* tempty = minfull + 6;         // [2], 4 epilogue-warp arrivals
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + GemmSmem::TMEMP);
+    float* scl = reinterpret_cast<float*>(sm + GemmSmem::SCL);   // [2][3][128]
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int r0 = blockIdx.x * GT, i0 = blockIdx.y * GT;
+    const int nb = A.nb;
+
+    if (tid == 0) {
+        for (int s = 0; s < NSTAGE; ++s) {
+            mbar_init(&full[s], 4);
+            mbar_init(&empty[s], 1);
+        }
+        for (int j = 0; j < 2; ++j) {
+            mbar_init(&minfull[j], 4);
+            mbar_init(&minempty[j], 1);
+            mbar_init(&tfull[j], 1);
+            mbar_init(&tempty[j], 4);
+        }
+        fence_barrier_init();
+    }
+    if (warp == 8) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;"
+                     :: "r"(smem_u32(tmem_slot)) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    bool ok = true;
+
+    if (warp < 4) {
+        // ------------------------------------------------------- producers
+        const int t = tid;
+        const int r = r0 + t, i = i0 + t;
+        const bool wrow = r < A.n, xrow = i < A.m;
+        Q4KRow R;
+        auto load_row = [&](int b) {
+            if (wrow) {
+                const uint4* src = reinterpret_cast<const uint4*>(A.w + ((size_t)r * nb + b) * Q4K_BYTES);
+#pragma unroll
+                for (int u = 0; u < 9; ++u) R.raw[u] = __ldg(src + u);
+            } else {
+#pragma unroll
+                for (int u = 0; u < 9; ++u) R.raw[u] = make_uint4(0, 0, 0, 0);
+            }
+        };
+        load_row(0);
+        for (int b = 0; b < nb && ok; ++b) {
+            const int j = b & 1;
+            q4K_row_prepare(R);
+            // min operands and scales of this block
+            if (b >= 2) {
+                ok = mbar_wait(&minempty[j], ((b >> 1) - 1) & 1) && mbar_wait(&tempty[j], ((b >> 1) - 1) & 1);
+                if (!ok) break;
+            }
+            uint8_t* mt = sm + GemmSmem::MIN + j * TILE_BYTES;
+            {
+                // K 0..15: the weight row's mins m_(g/2); K 16..31: the activation row's bsums
+                uint32_t mv[8], bv[8];
+#pragma unroll
+                for (int g = 0; g < 8; ++g) {
+                    const __half hm = __int2half_rn(R.mins[g]);
+                    mv[g] = h2_bits(__halves2half2(hm, hm));
+                }
+                float dx = 0.0f;
+                if (xrow) {
+                    const uint8_t* xb = A.xq + ((size_t)i * nb + b) * Q8K_BYTES;
+                    dx = __ldg(reinterpret_cast<const float*>(xb));
+                    const uint32_t* bw = reinterpret_cast<const uint32_t*>(xb + 260);
+#pragma unroll
+                    for (int g = 0; g < 8; ++g) {
+                        const uint32_t v = __ldg(bw + g);
+                        bv[g] = h2_bits(__halves2half2(__int2half_rn((int)(int16_t)(v & 0xFFFF)),
+                                                       __int2half_rn((int)(int16_t)(v >> 16))));
+                    }
+                } else {
+#pragma unroll
+                    for (int g = 0; g < 8; ++g) bv[g] = 0;
+                }
+                *reinterpret_cast<uint4*>(mt + sw128_chunk(t, 0)) = make_uint4(mv[0], mv[1], mv[2], mv[3]);
+                *reinterpret_cast<uint4*>(mt + sw128_chunk(t, 1)) = make_uint4(mv[4], mv[5], mv[6], mv[7]);
+                *reinterpret_cast<uint4*>(mt + sw128_chunk(t, 2)) = make_uint4(bv[0], bv[1], bv[2], bv[3]);
+                *reinterpret_cast<uint4*>(mt + sw128_chunk(t, 3)) = make_uint4(bv[4], bv[5], bv[6], bv[7]);
+                float* sj = scl + j * 3 * GT;
+                sj[t] = R.d;
+                sj[GT + t] = R.dmin;
+                sj[2 * GT + t] = dx;
+            }
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&minfull[j]);
+
+            Q4KRow Rn;                 // next block's raw bytes, loaded while this one is decoded
+            if (b + 1 < nb && wrow) {
+                const uint4* src = reinterpret_cast<const uint4*>(A.w + ((size_t)r * nb + b + 1) * Q4K_BYTES);
+#pragma unroll
+                for (int u = 0; u < 9; ++u) Rn.raw[u] = __ldg(src + u);
+            } else {
+#pragma unroll
+                for (int u = 0; u < 9; ++u) Rn.raw[u] = make_uint4(0, 0, 0, 0);
+            }
+            for (int c = 0; c < 4; ++c) {
+                const int g = 4 * b + c, s = g % NSTAGE, u = g / NSTAGE;
+                if (g >= NSTAGE && !mbar_wait(&empty[s], (u - 1) & 1)) { ok = false; break; }
+                uint8_t* st = sm + GemmSmem::RING + s * 2 * TILE_BYTES;
+                if (tid == 0) {
+                    mbar_expect_tx(&full[s], TILE_BYTES);
+                    tma_load_2d(st + TILE_BYTES, &xmap, b * QK + c * KS, i0, &full[s]);
+                }
+                q4K_row_stage(R, c, st, t);
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&full[s]);
+            }
+#pragma unroll
+            for (int u = 0; u < 9; ++u) R.raw[u] = Rn.raw[u];
+        }
+    } else if (warp == 8) {
+        // ------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            for (int b = 0; b < nb && ok; ++b) {
+                const int j = b & 1;
+                const uint32_t d1 = tmem + j * 256, d2 = d1 + 128;
+                if (b >= 2 && !mbar_wait(&tempty[j], ((b >> 1) - 1) & 1)) { ok = false; break; }
+                tc_fence_after();
+                for (int c = 0; c < 4 && ok; ++c) {
+                    const int g = 4 * b + c, s = g % NSTAGE, u = g / NSTAGE;
+                    if (!mbar_wait(&full[s], u & 1)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(sm + GemmSmem::RING + s * 2 * TILE_BYTES);
+                    const uint64_t da = umma_desc_sw128(sa), db = umma_desc_sw128(sa + TILE_BYTES);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)    // K = 16 per MMA: +32 bytes = +2 descriptor units
+                        mma_f16(d1, da + 2 * kk, db + 2 * kk, (c | kk) != 0);
+                    mma_commit(&empty[s]);
+                }
+                if (!ok) break;
+                if (!mbar_wait(&minfull[j], (b >> 1) & 1)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t ma = smem_u32(sm + GemmSmem::MIN + j * TILE_BYTES);
+                mma_f16(d2, umma_desc_sw128(ma), umma_desc_sw128(ma) + 2, 0u);
+                mma_commit(&minempty[j]);
+                mma_commit(&tfull[j]);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------- epilogue
+        const int e = tid - 128;                 // TMEM lane = weight row of the tile
+        const int q = warp & 3;                  // this warp's lane quarter
+        float acc[GT];
+#pragma unroll
+        for (int c = 0; c < GT; ++c) acc[c] = 0.0f;
+        for (int b = 0; b < nb && ok; ++b) {
+            const int j = b & 1;
+            if (!mbar_wait(&tfull[j], (b >> 1) & 1) || !mbar_wait(&minfull[j], (b >> 1) & 1)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const float* sj = scl + j * 3 * GT;
+            const float dw = sj[e], dmw = sj[GT + e];
+            const uint32_t base = tmem + ((uint32_t)(q * 32) << 16) + j * 256;
+#pragma unroll
+            for (int cc = 0; cc < 8; ++cc) {
+                uint32_t v1[16], v2[16];
+                tmem_ld16(base + 16 * cc, v1);
+                tmem_ld16(base + 128 + 16 * cc, v2);
+                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    const float dx = sj[2 * GT + 16 * cc + c];
+                    const float tt = __fmaf_rn(dw, __uint_as_float(v1[c]), -__fmul_rn(dmw, __uint_as_float(v2[c])));
+                    acc[16 * cc + c] = __fmaf_rn(dx, tt, acc[16 * cc + c]);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[j]);
+        }
+        const int r = r0 + e;
+        if (r < A.n) {
+#pragma unroll
+            for (int c = 0; c < GT; ++c)
+                if (i0 + c < A.m) A.y[(size_t)(i0 + c) * A.n + r] = acc[c];
+        }
+    }
+    if (!ok && lane == 0) atomicOr(A.fault, 2u);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 8) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" :: "r"(tmem) : "memory");
+    }
+}
+
+// q8_K codes -> f16 activation matrix [m][k] (the GEMM's B operand source)
+__global__ void gemm_x16_kernel(const uint8_t* __restrict__ xq, __half* __restrict__ x16, long long nblocks) {
+    const long long total = nblocks * 32;                 // 8 codes per item
+    for (long long it = (long long)blockIdx.x * blockDim.x + threadIdx.x; it < total;
+         it += (long long)gridDim.x * blockDim.x) {
+        const long long blk = it >> 5;
+        const int part = (int)(it & 31);
+        const uint32_t* src = reinterpret_cast<const uint32_t*>(xq + blk * Q8K_BYTES + 4) + 2 * part;
+        const uint32_t a = __ldg(src), c = __ldg(src + 1);
+        uint32_t o[4];
+        const uint32_t wv[2] = {a, c};
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint32_t v = wv[h];
+            o[2 * h] = h2_bits(__halves2half2(__int2half_rn((int)(int8_t)(v & 0xFF)),
+                                              __int2half_rn((int)(int8_t)((v >> 8) & 0xFF))));
+            o[2 * h + 1] = h2_bits(__halves2half2(__int2half_rn((int)(int8_t)((v >> 16) & 0xFF)),
+                                                  __int2half_rn((int)(int8_t)(v >> 24))));
+        }
+        *reinterpret_cast<uint4*>(x16 + blk * QK + 8 * part) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+size_t gemm_workspace_bytes(long long m, int k) {
+    return (((size_t)m * k * 2) + 255) & ~(size_t)255;
+}
+
+static cudaError_t gemm_q4K_ws(const uint8_t* w, const uint8_t* xq, float* y, long long m, int n, int k,
+                               void* ws, cudaStream_t stream) {
+    const int nb = k / QK;
+    __half* x16 = static_cast<__half*>(ws);
+    {
+        const long long nblocks = m * nb;
+        long long grid = (nblocks * 32 + 255) / 256;
+        const long long cap = (long long)num_sms() * 8;
+        if (grid > cap) grid = cap;
+        gemm_x16_kernel<<<(unsigned)grid, 256, 0, stream>>>(xq, x16, nblocks);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    CUtensorMap map;
+    const cuuint64_t dims[2] = {(cuuint64_t)k, (cuuint64_t)m};
+    const cuuint64_t strides[1] = {(cuuint64_t)k * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)KS, (cuuint32_t)GT};
+    const cuuint32_t estr[2] = {1, 1};
+    if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, x16, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    GemmArgs A;
+    A.w = w;
+    A.xq = xq;
+    A.y = y;
+    A.fault = fault_word();
+    if (!A.fault) return cudaErrorInvalidDevicePointer;
+    A.m = (int)m;
+    A.n = n;
+    A.nb = nb;
+    cudaError_t e = cudaFuncSetAttribute(gemm_q4K_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM);
+    if (e != cudaSuccess) return e;
+    const dim3 grid((unsigned)((n + GT - 1) / GT), (unsigned)((m + GT - 1) / GT));
+    gemm_q4K_kernel<<<grid, GEMM_THREADS, GEMM_SMEM, stream>>>(map, A);
+    return cudaGetLastError();
+}
+
+// Below this many activation rows the decode GEMV kernels (eight rows at a
+// time) serve the GEMM entry point.
+constexpr long long GEMM_MIN_M = 9;
+
+cudaError_t launch_gemm_ws(int fmt, const uint8_t* w, const uint8_t* xq, float* y, long long m, int n, int k,
+                           void* ws, size_t ws_bytes, cudaStream_t stream) {
+    if (fmt == 4 && m >= GEMM_MIN_M && (long long)m <= 0x7FFFFFFF) {
+        if (!ws || ws_bytes < gemm_workspace_bytes(m, k)) return cudaErrorInvalidValue;
+        return gemm_q4K_ws(w, xq, y, m, n, k, ws, stream);
+    }
     const int nb = k / QK;
     for (long long i0 = 0; i0 < m; i0 += GEMV_MAX_M) {
         const int mm = (int)(m - i0 < GEMV_MAX_M ? m - i0 : GEMV_MAX_M);
-        cudaError_t e = launch_gemv(fmt, w, xq + (size_t)i0 * nb * Q8K_BYTES, y + (size_t)i0 * n,
-                                    mm, n, k, stream);
+        cudaError_t e = launch_gemv(fmt, w, xq + (size_t)i0 * nb * Q8K_BYTES, y + (size_t)i0 * n, mm, n, k, stream);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
+}
+
+size_t gemm_workspace_need(int fmt, long long m, int k) {
+    return (fmt == 4 && m >= GEMM_MIN_M) ? gemm_workspace_bytes(m, k) : 0;
+}
+
+cudaError_t launch_gemm(int fmt, const uint8_t* w, const uint8_t* xq, float* y, long long m, int n, int k,
+                        cudaStream_t stream) {
+    const size_t need = gemm_workspace_need(fmt, m, k);
+    if (need == 0) return launch_gemm_ws(fmt, w, xq, y, m, n, k, nullptr, 0, stream);
+    void* ws = nullptr;
+    cudaError_t e = cudaMallocAsync(&ws, need, stream);
+    if (e != cudaSuccess) return e;
+    e = launch_gemm_ws(fmt, w, xq, y, m, n, k, ws, need, stream);
+    const cudaError_t f = cudaFreeAsync(ws, stream);
+    return e != cudaSuccess ? e : f;
 }
 
 }  // namespace plm

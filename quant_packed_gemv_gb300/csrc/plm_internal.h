@@ -36,8 +36,13 @@ cudaError_t launch_gemv_grouped(int fmt, const GroupItem* items, int count, int 
 cudaError_t launch_subdots(int fmt, const uint8_t* w, const uint8_t* xq, int32_t* out,
                            int m, int n, int k, cudaStream_t stream);
 
-// Prefill GEMM, any m >= 1.
+// Prefill GEMM, any m >= 1.  The _ws form uses the caller's workspace
+// (gemm_workspace_need bytes, 256-byte aligned); the plain form takes it from
+// the stream-ordered pool for the duration of the call.
 cudaError_t launch_gemm(int fmt, const uint8_t* w, const uint8_t* xq, float* y,
                         long long m, int n, int k, cudaStream_t stream);
+cudaError_t launch_gemm_ws(int fmt, const uint8_t* w, const uint8_t* xq, float* y, long long m, int n, int k,
+                           void* ws, size_t ws_bytes, cudaStream_t stream);
+size_t gemm_workspace_need(int fmt, long long m, int k);
 
 }  // namespace plm

@@ -67,6 +67,12 @@ def load(build_if_missing=True):
     lib.plm_device_fault.restype = ctypes.c_int
     lib.plm_quantize_q8K.argtypes = [vp, vp, i64, i64, vp]
     lib.plm_quantize_q8K.restype = ctypes.c_int
+    lib.plm_gemm_workspace_size.argtypes = [ctypes.c_int, i64, i64]
+    lib.plm_gemm_workspace_size.restype = ctypes.c_size_t
+    for name in ("plm_gemm_q4K_ws", "plm_gemm_q6K_ws"):
+        fn = getattr(lib, name)
+        fn.argtypes = [vp, vp, vp, i64, i64, i64, vp, ctypes.c_size_t, vp]
+        fn.restype = ctypes.c_int
     for name in ("plm_gemv_q4K_grouped", "plm_gemv_q6K_grouped"):
         fn = getattr(lib, name)
         fn.argtypes = [ctypes.POINTER(_Problem), i64, i64, vp]
@@ -155,6 +161,28 @@ def _grouped(name):
 
 plm_gemv_q4K_grouped = _grouped("plm_gemv_q4K_grouped")
 plm_gemv_q6K_grouped = _grouped("plm_gemv_q6K_grouped")
+
+
+def plm_gemm_workspace_size(fmt, m, k):
+    """fmt: 'q4K' / 'q6K' or 4 / 6."""
+    f = {"q4K": 4, "q6K": 6}.get(fmt, fmt)
+    return load().plm_gemm_workspace_size(f, m, k)
+
+
+def _gemm_ws(name):
+    def call(w, xq, y, m, n, k, workspace, workspace_bytes=None, stream=None):
+        lib = load()
+        if workspace_bytes is None:
+            workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+        _check(name, getattr(lib, name)(_addr(w), _addr(xq), _addr(y), m, n, k, _addr(workspace),
+                                        workspace_bytes, _stream(stream)))
+    call.__name__ = name
+    call.__doc__ = "Binding of %s(w, xq, y, m, n, k, workspace, bytes, stream)." % name
+    return call
+
+
+plm_gemm_q4K_ws = _gemm_ws("plm_gemm_q4K_ws")
+plm_gemm_q6K_ws = _gemm_ws("plm_gemm_q6K_ws")
 
 
 def raw_status(name, *args):

@@ -93,7 +93,8 @@ def test_gemv_adversarial_extremes(fmt):
 # --------------------------------------------------------------- GEMM
 
 @pytest.mark.parametrize("fmt", ["q4K", "q6K"])
-@pytest.mark.parametrize("m,n,k", [(9, 50, 1024), (17, 33, 256), (64, 128, 2048), (130, 70, 512)])
+@pytest.mark.parametrize("m,n,k", [(9, 50, 1024), (17, 33, 256), (64, 128, 2048), (130, 70, 512),
+                                   (128, 128, 256), (200, 300, 1536), (512, 1024, 1024), (257, 129, 4096)])
 def test_gemm_matches_oracle(fmt, m, n, k):
     w = make_weights(fmt, 13, 0, n, k)
     xq = oracle.quantize_q8K(gen.normal_f32(13, 400, m, k))
@@ -144,3 +145,25 @@ def test_grouped_gemv_equals_single_calls(fmt, m):
 def test_no_device_fault_recorded():
     import quant_packed_gemv_gb300 as q
     assert q.plm_device_fault() == 0
+
+
+@pytest.mark.parametrize("fmt", ["q4K", "q6K"])
+def test_gemm_with_caller_workspace_matches(fmt):
+    import torch
+    import quant_packed_gemv_gb300 as q
+    from tests.gpu_helpers import dev
+    m, n, k = 150, 260, 2048
+    w = make_weights(fmt, 30, 0, n, k)
+    xq = oracle.quantize_q8K(gen.normal_f32(30, 1, m, k))
+    need = q.plm_gemm_workspace_size(fmt, m, k)
+    ws = torch.empty(max(need, 1), dtype=torch.uint8, device="cuda")
+    y = torch.full((m, n), float("nan"), device="cuda")
+    getattr(q, "plm_gemm_%s_ws" % fmt)(dev(w), dev(xq), y, m, n, k, ws if need else None, need)
+    ref, S = oracle_ref(fmt, w, xq, m, n, k)
+    assert_close(host(y), ref, S)
+    assert np.array_equal(host(y), gpu_matmul("gemm", fmt, w, xq, m, n, k))
+    if need:
+        from quant_packed_gemv_gb300 import plm as P
+        small = P.raw_status("plm_gemm_%s_ws" % fmt, dev(w).data_ptr(), dev(xq).data_ptr(), y.data_ptr(),
+                             m, n, k, ws.data_ptr(), need - 1, None)
+        assert small == P.PLM_ERR_INVALID_ARG
