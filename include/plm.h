@@ -169,6 +169,31 @@ plm_status plm_gemm_q6K_ws(const void* w, const void* xq, float* y, int64_t m, i
                            void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * Allocation-free q4_K GEMM.  No counterpart on the PocketLLM pages: it is a
+ * library convenience.  Same contract and results as plm_gemm_q4K (within
+ * the same tolerance), except that its temporary f16 copy of the activations
+ * lives in a fixed device array inside this library instead of memory the
+ * call allocates.  It is meant for callers that must not allocate device
+ * memory while running, such as an engine whose memory is entirely claimed
+ * by its own allocator at start-up, or a latency-critical loop that cannot
+ * afford an allocation that might fail or wait.
+ *   - Limit: 2*m*k bytes of workspace (m >= 9; smaller m needs none) must fit
+ *     PLM_NOALLOC_WORKSPACE_BYTES; larger problems return
+ *     PLM_ERR_UNSUPPORTED and enqueue nothing.
+ *   - Calls no cudaMalloc, cudaFree or allocating routine.  Every device
+ *     that loads the library holds the array until the process exits.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture that includes this entry point.
+ *   - All calls share the one array (it keeps the last call's contents, and
+ *     each call rewrites the part it reads), so calls whose kernels may
+ *     overlap on the GPU, e.g. on different streams, race: serialize them.
+ */
+#define PLM_NOALLOC_WORKSPACE_BYTES (32u << 20)
+plm_status plm_gemm_q4K_noalloc(const void* w, const void* xq, float* y, int64_t m, int64_t n, int64_t k,
+                                cudaStream_t stream);
+
+/*
  * Verification export: the integer sub-block dots computed by the same
  * device decode/dot code the GEMV uses.
  *   q4_K: out int32 [m][n][k/32],  out[i][r][8b+j]  = sum_{l<32} q * q8

@@ -213,6 +213,17 @@ plm_status plm_gemm_q6K_ws(const void* w, const void* xq, float* y, int64_t m, i
     return gemm_ws_common(6, w, xq, y, m, n, k, workspace, workspace_bytes, stream);
 }
 
+plm_status plm_gemm_q4K_noalloc(const void* w, const void* xq, float* y, int64_t m, int64_t n, int64_t k,
+                                cudaStream_t stream) {
+    plm_status s = check_matmul(w, xq, y, m, n, k, kMaxIndex);
+    if (s != PLM_OK) return s;
+    if (m * n > (int64_t)1 << 40) return PLM_ERR_INVALID_ARG;
+    if (!plm::gemm_noalloc_fits(m, (int)k)) return PLM_ERR_UNSUPPORTED;   // beyond the fixed array
+    if (!plm::gemv_supported(4, (int)k)) return PLM_ERR_UNSUPPORTED;
+    return cuda_status(plm::launch_gemm_q4K_noalloc((const uint8_t*)w, (const uint8_t*)xq, y, m, (int)n, (int)k,
+                                                    stream));
+}
+
 plm_status plm_subdots_q4K(const void* w, const void* xq, int32_t* out, int64_t m, int64_t n,
                            int64_t k, cudaStream_t stream) {
     return subdots_common(4, w, xq, out, m, n, k, stream);

@@ -532,3 +532,63 @@ cudaError_t launch_gemm(int fmt, const uint8_t* w, const uint8_t* xq, float* y, 
 }
 
 }  // namespace plm
+
+// ---------------------------------------------------------------------------
+// Allocation-free GEMM entry: the same q4_K GEMM, with its f16 activation
+// workspace in a fixed device array compiled into this library instead of
+// memory from cudaMalloc / the stream-ordered pool.  It exists for callers
+// that must not allocate device memory once they are running, for example an
+// engine whose whole memory budget is claimed by its own allocator at start-up,
+// or a latency-critical loop that cannot risk an allocation failing or
+// waiting.  Every device that loads the library reserves the array until the
+// process exits.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+#include "../../include/plm.h"
+
+namespace plm {
+
+static __device__ __align__(256) uint8_t g_noalloc_scratch[PLM_NOALLOC_WORKSPACE_BYTES];
+
+// Device address of the array on the current device.  In host code the
+// array's name is only a host-side stand-in, so the address is looked up with
+// cudaGetSymbolAddress once per device (with that device current) and kept.
+static cudaError_t noalloc_scratch_ptr(void** out) {
+    static std::mutex mu;
+    static void* addr[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        if (!p) return cudaErrorInvalidSymbol;
+        addr[dev] = p;
+    }
+    *out = addr[dev];
+    return cudaSuccess;
+}
+
+bool gemm_noalloc_fits(long long m, int k) {
+    return gemm_workspace_need(4, m, k) <= (size_t)PLM_NOALLOC_WORKSPACE_BYTES;
+}
+
+cudaError_t launch_gemm_q4K_noalloc(const uint8_t* w, const uint8_t* xq, float* y, long long m, int n, int k,
+                                    cudaStream_t stream) {
+    const size_t need = gemm_workspace_need(4, m, k);
+    if (need > (size_t)PLM_NOALLOC_WORKSPACE_BYTES) return cudaErrorInvalidValue;
+    void* ws = nullptr;
+    if (need > 0) {
+        // the pre-pass rewrites all `need` bytes before the GEMM reads them,
+        // so nothing left by an earlier call has to be cleared
+        cudaError_t e = noalloc_scratch_ptr(&ws);
+        if (e != cudaSuccess) return e;
+    }
+    return launch_gemm_ws(4, w, xq, y, m, n, k, ws, need, stream);
+}
+
+}  // namespace plm

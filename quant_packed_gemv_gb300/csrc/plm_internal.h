@@ -45,4 +45,10 @@ cudaError_t launch_gemm_ws(int fmt, const uint8_t* w, const uint8_t* xq, float* 
                            void* ws, size_t ws_bytes, cudaStream_t stream);
 size_t gemm_workspace_need(int fmt, long long m, int k);
 
+// Allocation-free q4_K GEMM: the workspace is a fixed device array inside the
+// library (PLM_NOALLOC_WORKSPACE_BYTES).
+bool gemm_noalloc_fits(long long m, int k);
+cudaError_t launch_gemm_q4K_noalloc(const uint8_t* w, const uint8_t* xq, float* y, long long m, int n, int k,
+                                    cudaStream_t stream);
+
 }  // namespace plm

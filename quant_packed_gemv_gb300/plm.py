@@ -77,7 +77,7 @@ def load(build_if_missing=True):
         fn = getattr(lib, name)
         fn.argtypes = [ctypes.POINTER(_Problem), i64, i64, vp]
         fn.restype = ctypes.c_int
-    for name in ("plm_gemv_q4K", "plm_gemv_q6K", "plm_gemm_q4K", "plm_gemm_q6K",
+    for name in ("plm_gemv_q4K", "plm_gemv_q6K", "plm_gemm_q4K", "plm_gemm_q6K", "plm_gemm_q4K_noalloc",
                  "plm_subdots_q4K", "plm_subdots_q6K"):
         fn = getattr(lib, name)
         fn.argtypes = [vp, vp, vp, i64, i64, i64, vp]
@@ -142,6 +142,9 @@ plm_gemv_q4K = _mm("plm_gemv_q4K")
 plm_gemv_q6K = _mm("plm_gemv_q6K")
 plm_gemm_q4K = _mm("plm_gemm_q4K")
 plm_gemm_q6K = _mm("plm_gemm_q6K")
+# q4_K GEMM whose workspace is a fixed array inside the library: for callers
+# that must not allocate device memory while running (see include/plm.h).
+plm_gemm_q4K_noalloc = _mm("plm_gemm_q4K_noalloc")
 plm_subdots_q4K = _mm("plm_subdots_q4K")
 plm_subdots_q6K = _mm("plm_subdots_q6K")
 
