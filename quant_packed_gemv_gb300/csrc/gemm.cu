@@ -15,6 +15,11 @@
 // 1e-4 tolerance).  Because d, dmin and d_x change every block, each block
 // accumulates into fresh TMEM columns and is drained and scaled in f32.
 //
+// q6_K scales are int8, so sc*(q6-32) can reach 4096 and is not always
+// exact in f16; the scale is split as sc = 16*hi + lo and the two exact
+// operand tiles hi*(q6-32), lo*(q6-32) go to two accumulators, combined as
+// 16*D_hi + D_lo in the epilogue.
+//
 // Tile: 128 weight rows (MMA M, TMEM lanes) x 128 activation rows (MMA N,
 // TMEM columns).  Roles per CTA (9 warps):
 //   warps 0-3 (producers): thread t decodes weight row t of the tile into
@@ -32,6 +37,8 @@
 #include <cuda.h>
 #include <cuda_fp16.h>
 
+#include <type_traits>
+
 #include "plm_device.cuh"
 #include "plm_internal.h"
 
@@ -39,21 +46,29 @@ namespace plm {
 
 constexpr int GT = 128;                 // tile rows (weights) and columns (activations)
 constexpr int KS = 64;                  // K per operand stage (one 128-byte swizzle row)
-constexpr int NSTAGE = 4;
 constexpr int TILE_BYTES = GT * KS * 2; // 16 KB per operand tile
 constexpr int GEMM_THREADS = 9 * 32;
 
+// q4_K: one A tile per stage plus per-block min operands; q6_K: two A tiles
+// per stage (the high and low parts of the scale), no min term.
+template <int FMT> struct GemmCfg;
+template <> struct GemmCfg<4> { static constexpr int ATILES = 1, NSTAGE = 4, MINB = 2 * TILE_BYTES; };
+template <> struct GemmCfg<6> { static constexpr int ATILES = 2, NSTAGE = 3, MINB = 0; };
+
+template <int FMT>
 struct GemmSmem {
     // offsets from the 1024-aligned base
-    static constexpr int RING = 0;                                  // NSTAGE x (A, B)
-    static constexpr int MIN = RING + NSTAGE * 2 * TILE_BYTES;      // 2 x 16 KB
-    static constexpr int SCL = MIN + 2 * TILE_BYTES;                // 2 x (d, dmin, dx) x 128 f32
+    static constexpr int NSTAGE = GemmCfg<FMT>::NSTAGE;
+    static constexpr int STAGE = (GemmCfg<FMT>::ATILES + 1) * TILE_BYTES;   // A tile(s), then B
+    static constexpr int RING = 0;
+    static constexpr int MIN = RING + NSTAGE * STAGE;                        // q4_K: 2 x 16 KB
+    static constexpr int SCL = MIN + GemmCfg<FMT>::MINB;                     // 2 x (d, dmin, dx) x 128 f32
     static constexpr int BAR = SCL + 2 * 3 * GT * 4;
     static constexpr int NBAR = 2 * NSTAGE + 8;
     static constexpr int TMEMP = BAR + NBAR * 8;
     static constexpr int BYTES = TMEMP + 16;
+    static constexpr int ALLOC = BYTES + 1024;   // + alignment slack
 };
-constexpr int GEMM_SMEM = GemmSmem::BYTES + 1024;   // + alignment slack
 
 // byte offset of element (row, k) in a 128-row x 64-wide f16 tile with the
 // 128-byte swizzle (16-byte chunk index XOR row % 8)
@@ -191,30 +206,114 @@ __device__ __forceinline__ void q4K_row_stage(const Q4KRow& R, int c, uint8_t* t
     }
 }
 
+// q6_K: stage c (weights 64c .. 64c+63) lies in half h = c/2, quarters
+// 2(c&1) and 2(c&1)+1.  K position p < 32 is weight 128h + 32*2(c&1) + p,
+// p >= 32 is weight 128h + 32*(2(c&1)+1) + p - 32; their low four bits come
+// from ql[64h + p] (resp. ql[64h + 32 + p - 32]) -- low nibble for c even,
+// high nibble for c odd -- and their top two bits from qh[32h + (p mod 32)]
+// (bits 4(c&1) .. +1 for p < 32, 4(c&1)+2 .. +3 otherwise).  Position p
+// belongs to the 16-group 4c + p/16.  Each int8 scale is split as
+// sc = 16*hi + lo (lo in 0..15), so that both operand tiles hi*(q6-32) and
+// lo*(q6-32) are exact in f16 for every int8 scale.
+struct Q6KRow {
+    uint32_t raw[53];        // the 210-byte block, word i = bytes 4i .. 4i+3 (word 52: bytes 208, 209)
+    float d;
+};
+
+__device__ __forceinline__ void q6K_row_load(Q6KRow& R, const uint8_t* blk, bool valid) {
+    if (!valid) {
+#pragma unroll
+        for (int i = 0; i < 53; ++i) R.raw[i] = 0;
+        return;
+    }
+    // the block starts 2-byte aligned; read aligned words and realign
+    const uintptr_t addr = reinterpret_cast<uintptr_t>(blk);
+    const int mis = (int)(addr & 3);                    // 0 or 2
+    const uint32_t* aw = reinterpret_cast<const uint32_t*>(addr - mis);
+#pragma unroll
+    for (int i = 0; i < 52; ++i) R.raw[i] = __ldg(aw + i);
+    // word 52: with mis == 2 the aligned word at 208 ends at the block's last
+    // byte; with mis == 0 only the last two bytes exist
+    const uint32_t last = mis ? __ldg(aw + 52) : (uint32_t)__ldg(reinterpret_cast<const uint16_t*>(blk + 208));
+    if (mis) {
+#pragma unroll
+        for (int i = 0; i < 51; ++i) R.raw[i] = __funnelshift_r(R.raw[i], R.raw[i + 1], 16);
+        R.raw[51] = __funnelshift_r(R.raw[51], last, 16);
+        R.raw[52] = last >> 16;
+    } else {
+        R.raw[52] = last;
+    }
+}
+
+// writes stage c of the row as two f16 tiles: hi*(q6-32) and lo*(q6-32)
+__device__ __forceinline__ void q6K_row_stage(const Q6KRow& R, int c, uint8_t* tile_hi, uint8_t* tile_lo,
+                                              int row) {
+    const int h = c >> 1, part = c & 1;
+    const uint32_t scw = R.raw[48 + c];                  // scales 4c .. 4c+3
+    __half2 shi[4], ohi[4], slo[4], olo[4];
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        const int sc = (int)(int8_t)((scw >> (8 * g)) & 0xFF);
+        const float hi = (float)(sc >> 4), lo = (float)(sc & 15);
+        // (1024 + q6) * s - 1056 * s = (q6 - 32) * s, exact
+        shi[g] = __float2half2_rn(hi);
+        ohi[g] = __float2half2_rn(-1056.0f * hi);
+        slo[g] = __float2half2_rn(lo);
+        olo[g] = __float2half2_rn(-1056.0f * lo);
+    }
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch) {                      // positions 8ch .. 8ch+7
+        const int second = ch >> 2;                       // 0: p < 32, 1: p >= 32
+        const int g = ch >> 1;                            // 16-group within the stage
+        uint32_t vh[4], vl[4];
+#pragma unroll
+        for (int wv = 0; wv < 2; ++wv) {
+            const int u = 2 * (ch & 3) + wv;              // word index: positions 4u .. 4u+3 of the half
+            const uint32_t ql = R.raw[16 * h + 8 * second + u];
+            const uint32_t qh = R.raw[32 + 8 * h + u];
+            const uint32_t nib = part ? ((ql >> 4) & 0x0F0F0F0Fu) : (ql & 0x0F0F0F0Fu);
+            const uint32_t hb = (qh >> (4 * part + 2 * second)) & 0x03030303u;
+            const uint32_t code = nib | (hb << 4);
+            const uint32_t x01 = (__byte_perm(code, 0, 0x4140) & 0x003F003Fu) | 0x64006400u;
+            const uint32_t x23 = (__byte_perm(code, 0, 0x4342) & 0x003F003Fu) | 0x64006400u;
+            vh[2 * wv] = h2_bits(__hfma2(bits_h2(x01), shi[g], ohi[g]));
+            vh[2 * wv + 1] = h2_bits(__hfma2(bits_h2(x23), shi[g], ohi[g]));
+            vl[2 * wv] = h2_bits(__hfma2(bits_h2(x01), slo[g], olo[g]));
+            vl[2 * wv + 1] = h2_bits(__hfma2(bits_h2(x23), slo[g], olo[g]));
+        }
+        *reinterpret_cast<uint4*>(tile_hi + sw128_chunk(row, ch)) = make_uint4(vh[0], vh[1], vh[2], vh[3]);
+        *reinterpret_cast<uint4*>(tile_lo + sw128_chunk(row, ch)) = make_uint4(vl[0], vl[1], vl[2], vl[3]);
+    }
+}
+
 // ---------------------------------------------------------------------------
-// The GEMM kernel (q4_K)
+// The GEMM kernel
 // ---------------------------------------------------------------------------
 struct GemmArgs {
-    const uint8_t* w;        // q4_K [n][nb]
+    const uint8_t* w;        // q4_K or q6_K [n][nb]
     const uint8_t* xq;       // q8_K [m][nb]
     float* y;                // [m][n]
     unsigned* fault;
     int m, n, nb;
 };
 
-__global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_q4K_kernel(const __grid_constant__ CUtensorMap xmap,
-                                                                   const GemmArgs A) {
+template <int FMT>
+__global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_constant__ CUtensorMap xmap,
+                                                               const GemmArgs A) {
+    using L = GemmSmem<FMT>;
+    constexpr int NSTAGE = L::NSTAGE;
+    constexpr int BOFF = GemmCfg<FMT>::ATILES * TILE_BYTES;   // B tile offset inside a stage
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + GemmSmem::BAR);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BAR);
     uint64_t* full = bars;                  // [NSTAGE], 4 producer-warp arrivals + TMA bytes
     uint64_t* empty = bars + NSTAGE;        // [NSTAGE], MMA commit
-    uint64_t* minfull = bars + 2 * NSTAGE;  // [2], 4 producer-warp arrivals
+    uint64_t* minfull = bars + 2 * NSTAGE;  // [2], 4 producer-warp arrivals (min operands, scales)
     uint64_t* minempty = minfull + 2;       // [2], MMA commit
     uint64_t* tfull = minfull + 4;          // [2], MMA commit
     uint64_t* tempty = minfull + 6;         // [2], 4 epilogue-warp arrivals
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + GemmSmem::TMEMP);
-    float* scl = reinterpret_cast<float*>(sm + GemmSmem::SCL);   // [2][3][128]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::TMEMP);
+    float* scl = reinterpret_cast<float*>(sm + L::SCL);   // [2][3][128]: d, dmin, dx
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int r0 = blockIdx.x * GT, i0 = blockIdx.y * GT;
@@ -249,39 +348,50 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_q4K_kernel(const __grid_
         const int t = tid;
         const int r = r0 + t, i = i0 + t;
         const bool wrow = r < A.n, xrow = i < A.m;
-        Q4KRow R;
-        auto load_row = [&](int b) {
-            if (wrow) {
-                const uint4* src = reinterpret_cast<const uint4*>(A.w + ((size_t)r * nb + b) * Q4K_BYTES);
+        using Row = typename std::conditional<FMT == 4, Q4KRow, Q6KRow>::type;
+        Row R, Rn;
+        auto load_row = [&](Row& dst, int b) {
+            if constexpr (FMT == 4) {
+                if (wrow) {
+                    const uint4* src = reinterpret_cast<const uint4*>(A.w + ((size_t)r * nb + b) * Q4K_BYTES);
 #pragma unroll
-                for (int u = 0; u < 9; ++u) R.raw[u] = __ldg(src + u);
+                    for (int u = 0; u < 9; ++u) dst.raw[u] = __ldg(src + u);
+                } else {
+#pragma unroll
+                    for (int u = 0; u < 9; ++u) dst.raw[u] = make_uint4(0, 0, 0, 0);
+                }
             } else {
-#pragma unroll
-                for (int u = 0; u < 9; ++u) R.raw[u] = make_uint4(0, 0, 0, 0);
+                q6K_row_load(dst, A.w + ((size_t)r * nb + b) * Q6K_BYTES, wrow);
             }
         };
-        load_row(0);
+        load_row(R, 0);
         for (int b = 0; b < nb && ok; ++b) {
             const int j = b & 1;
-            q4K_row_prepare(R);
-            // min operands and scales of this block
+            float dw, dmw = 0.0f;
+            if constexpr (FMT == 4) {
+                q4K_row_prepare(R);
+                dw = R.d;
+                dmw = R.dmin;
+            } else {
+                dw = half_bits_to_float(R.raw[52]);
+            }
             if (b >= 2) {
                 ok = mbar_wait(&minempty[j], ((b >> 1) - 1) & 1) && mbar_wait(&tempty[j], ((b >> 1) - 1) & 1);
                 if (!ok) break;
             }
-            uint8_t* mt = sm + GemmSmem::MIN + j * TILE_BYTES;
-            {
-                // K 0..15: the weight row's mins m_(g/2); K 16..31: the activation row's bsums
+            float dx = 0.0f;
+            const uint8_t* xb = A.xq + ((size_t)i * nb + b) * Q8K_BYTES;
+            if (xrow) dx = __ldg(reinterpret_cast<const float*>(xb));
+            if constexpr (FMT == 4) {
+                // min operands: K 0..15 the weight row's mins m_(g/2); K 16..31 the activation row's bsums
+                uint8_t* mt = sm + L::MIN + j * TILE_BYTES;
                 uint32_t mv[8], bv[8];
 #pragma unroll
                 for (int g = 0; g < 8; ++g) {
                     const __half hm = __int2half_rn(R.mins[g]);
                     mv[g] = h2_bits(__halves2half2(hm, hm));
                 }
-                float dx = 0.0f;
                 if (xrow) {
-                    const uint8_t* xb = A.xq + ((size_t)i * nb + b) * Q8K_BYTES;
-                    dx = __ldg(reinterpret_cast<const float*>(xb));
                     const uint32_t* bw = reinterpret_cast<const uint32_t*>(xb + 260);
 #pragma unroll
                     for (int g = 0; g < 8; ++g) {
@@ -297,39 +407,34 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_q4K_kernel(const __grid_
                 *reinterpret_cast<uint4*>(mt + sw128_chunk(t, 1)) = make_uint4(mv[4], mv[5], mv[6], mv[7]);
                 *reinterpret_cast<uint4*>(mt + sw128_chunk(t, 2)) = make_uint4(bv[0], bv[1], bv[2], bv[3]);
                 *reinterpret_cast<uint4*>(mt + sw128_chunk(t, 3)) = make_uint4(bv[4], bv[5], bv[6], bv[7]);
-                float* sj = scl + j * 3 * GT;
-                sj[t] = R.d;
-                sj[GT + t] = R.dmin;
-                sj[2 * GT + t] = dx;
             }
+            float* sj = scl + j * 3 * GT;
+            sj[t] = dw;
+            sj[GT + t] = dmw;
+            sj[2 * GT + t] = dx;
             fence_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&minfull[j]);
 
-            Q4KRow Rn;                 // next block's raw bytes, loaded while this one is decoded
-            if (b + 1 < nb && wrow) {
-                const uint4* src = reinterpret_cast<const uint4*>(A.w + ((size_t)r * nb + b + 1) * Q4K_BYTES);
+            if (b + 1 < nb) load_row(Rn, b + 1);      // next block's bytes, in flight while this one is decoded
 #pragma unroll
-                for (int u = 0; u < 9; ++u) Rn.raw[u] = __ldg(src + u);
-            } else {
-#pragma unroll
-                for (int u = 0; u < 9; ++u) Rn.raw[u] = make_uint4(0, 0, 0, 0);
-            }
             for (int c = 0; c < 4; ++c) {
                 const int g = 4 * b + c, s = g % NSTAGE, u = g / NSTAGE;
                 if (g >= NSTAGE && !mbar_wait(&empty[s], (u - 1) & 1)) { ok = false; break; }
-                uint8_t* st = sm + GemmSmem::RING + s * 2 * TILE_BYTES;
+                uint8_t* st = sm + L::RING + s * L::STAGE;
                 if (tid == 0) {
                     mbar_expect_tx(&full[s], TILE_BYTES);
-                    tma_load_2d(st + TILE_BYTES, &xmap, b * QK + c * KS, i0, &full[s]);
+                    tma_load_2d(st + BOFF, &xmap, b * QK + c * KS, i0, &full[s]);
                 }
-                q4K_row_stage(R, c, st, t);
+                if constexpr (FMT == 4)
+                    q4K_row_stage(R, c, st, t);
+                else
+                    q6K_row_stage(R, c, st, st + TILE_BYTES, t);
                 fence_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&full[s]);
             }
-#pragma unroll
-            for (int u = 0; u < 9; ++u) R.raw[u] = Rn.raw[u];
+            R = Rn;
         }
     } else if (warp == 8) {
         // ------------------------------------------------------- MMA issuer
@@ -343,18 +448,30 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_q4K_kernel(const __grid_
                     const int g = 4 * b + c, s = g % NSTAGE, u = g / NSTAGE;
                     if (!mbar_wait(&full[s], u & 1)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t sa = smem_u32(sm + GemmSmem::RING + s * 2 * TILE_BYTES);
-                    const uint64_t da = umma_desc_sw128(sa), db = umma_desc_sw128(sa + TILE_BYTES);
+                    const uint32_t sa = smem_u32(sm + L::RING + s * L::STAGE);
+                    const uint64_t db = umma_desc_sw128(sa + BOFF);
+                    if constexpr (FMT == 4) {
+                        const uint64_t da = umma_desc_sw128(sa);
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)    // K = 16 per MMA: +32 bytes = +2 descriptor units
-                        mma_f16(d1, da + 2 * kk, db + 2 * kk, (c | kk) != 0);
+                        for (int kk = 0; kk < 4; ++kk)    // K = 16 per MMA: +32 bytes = +2 descriptor units
+                            mma_f16(d1, da + 2 * kk, db + 2 * kk, (c | kk) != 0);
+                    } else {
+                        const uint64_t dh = umma_desc_sw128(sa), dl = umma_desc_sw128(sa + TILE_BYTES);
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            mma_f16(d1, dh + 2 * kk, db + 2 * kk, (c | kk) != 0);
+                            mma_f16(d2, dl + 2 * kk, db + 2 * kk, (c | kk) != 0);
+                        }
+                    }
                     mma_commit(&empty[s]);
                 }
                 if (!ok) break;
                 if (!mbar_wait(&minfull[j], (b >> 1) & 1)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t ma = smem_u32(sm + GemmSmem::MIN + j * TILE_BYTES);
-                mma_f16(d2, umma_desc_sw128(ma), umma_desc_sw128(ma) + 2, 0u);
+                if constexpr (FMT == 4) {
+                    const uint32_t ma = smem_u32(sm + L::MIN + j * TILE_BYTES);
+                    mma_f16(d2, umma_desc_sw128(ma), umma_desc_sw128(ma) + 2, 0u);
+                }
                 mma_commit(&minempty[j]);
                 mma_commit(&tfull[j]);
             }
@@ -386,7 +503,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_q4K_kernel(const __grid_
 #pragma unroll
                 for (int c = 0; c < 16; ++c) {
                     const float dx = sj[2 * GT + 16 * cc + c];
-                    const float tt = __fmaf_rn(dw, __uint_as_float(v1[c]), -__fmul_rn(dmw, __uint_as_float(v2[c])));
+                    float tt;
+                    if constexpr (FMT == 4)   // d*isum - dmin*msum
+                        tt = __fmaf_rn(dw, __uint_as_float(v1[c]), -__fmul_rn(dmw, __uint_as_float(v2[c])));
+                    else                      // d*(16*hi + lo)
+                        tt = __fmul_rn(dw, __fmaf_rn(16.0f, __uint_as_float(v1[c]), __uint_as_float(v2[c])));
                     acc[16 * cc + c] = __fmaf_rn(dx, tt, acc[16 * cc + c]);
                 }
             }
@@ -456,8 +577,9 @@ size_t gemm_workspace_bytes(long long m, int k) {
     return (((size_t)m * k * 2) + 255) & ~(size_t)255;
 }
 
-static cudaError_t gemm_q4K_ws(const uint8_t* w, const uint8_t* xq, float* y, long long m, int n, int k,
-                               void* ws, cudaStream_t stream) {
+template <int FMT>
+static cudaError_t gemm_tc_ws(const uint8_t* w, const uint8_t* xq, float* y, long long m, int n, int k,
+                              void* ws, cudaStream_t stream) {
     const int nb = k / QK;
     __half* x16 = static_cast<__half*>(ws);
     {
@@ -489,10 +611,11 @@ static cudaError_t gemm_q4K_ws(const uint8_t* w, const uint8_t* xq, float* y, lo
     A.m = (int)m;
     A.n = n;
     A.nb = nb;
-    cudaError_t e = cudaFuncSetAttribute(gemm_q4K_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM);
+    constexpr int SMEM = GemmSmem<FMT>::ALLOC;
+    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
     if (e != cudaSuccess) return e;
     const dim3 grid((unsigned)((n + GT - 1) / GT), (unsigned)((m + GT - 1) / GT));
-    gemm_q4K_kernel<<<grid, GEMM_THREADS, GEMM_SMEM, stream>>>(map, A);
+    gemm_kernel<FMT><<<grid, GEMM_THREADS, SMEM, stream>>>(map, A);
     return cudaGetLastError();
 }
 
@@ -502,9 +625,9 @@ constexpr long long GEMM_MIN_M = 9;
 
 cudaError_t launch_gemm_ws(int fmt, const uint8_t* w, const uint8_t* xq, float* y, long long m, int n, int k,
                            void* ws, size_t ws_bytes, cudaStream_t stream) {
-    if (fmt == 4 && m >= GEMM_MIN_M && (long long)m <= 0x7FFFFFFF) {
+    if (m >= GEMM_MIN_M && (long long)m <= 0x7FFFFFFF) {
         if (!ws || ws_bytes < gemm_workspace_bytes(m, k)) return cudaErrorInvalidValue;
-        return gemm_q4K_ws(w, xq, y, m, n, k, ws, stream);
+        return fmt == 4 ? gemm_tc_ws<4>(w, xq, y, m, n, k, ws, stream) : gemm_tc_ws<6>(w, xq, y, m, n, k, ws, stream);
     }
     const int nb = k / QK;
     for (long long i0 = 0; i0 < m; i0 += GEMV_MAX_M) {
@@ -516,7 +639,8 @@ cudaError_t launch_gemm_ws(int fmt, const uint8_t* w, const uint8_t* xq, float* 
 }
 
 size_t gemm_workspace_need(int fmt, long long m, int k) {
-    return (fmt == 4 && m >= GEMM_MIN_M) ? gemm_workspace_bytes(m, k) : 0;
+    (void)fmt;
+    return m >= GEMM_MIN_M ? gemm_workspace_bytes(m, k) : 0;
 }
 
 cudaError_t launch_gemm(int fmt, const uint8_t* w, const uint8_t* xq, float* y, long long m, int n, int k,
