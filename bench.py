@@ -68,6 +68,8 @@ def parse():
                     help="time one entry point alone, e.g. --case gemv q6K 151936 2048")
     ap.add_argument("--m", type=int, nargs="+", default=[1],
                     help="activation rows for --case (several values: a sweep)")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the prefill GEMM, q6_K head and m-sweep measurements")
     return ap.parse_args()
 
 
@@ -266,6 +268,98 @@ def time_case(args):
                           "copies": copies, "fault": q.plm_device_fault()}), flush=True)
 
 
+# --------------------------------------------------------------- other configs
+
+class ShapeTimer:
+    """Times single entry points on one shape with the weights rotated
+    through enough copies to exceed three times the L2; CUDA events on the
+    launch stream.  GEMMs use the caller-workspace form with a workspace
+    allocated once (allocation is not part of the timed work)."""
+
+    def __init__(self, torch, q, peaks):
+        self.torch, self.q, self.peaks = torch, q, peaks
+        self.l2 = torch.cuda.get_device_properties(0).L2_cache_size
+        self.stream = torch.cuda.Stream()
+
+    def weights(self, fmt, seed, n, k):
+        import gen
+        host = gen.q4K_blocks(seed, 0, n, k) if fmt == "q4K" else gen.q6K_blocks(seed, 0, n, k)
+        copies = max(1, -(-3 * self.l2 // host.nbytes))
+        return [self.torch.from_numpy(host).cuda() for _ in range(copies)], host.nbytes
+
+    def run(self, fmt, ws_list, wbytes, n, k, m, steps, warmup):
+        import gen
+        torch, q = self.torch, self.q
+        nb = k // QK
+        x = torch.from_numpy(gen.normal_f32(7, m, m, k)).cuda()
+        xq = torch.empty(m * nb * Q8K_BYTES, dtype=torch.uint8, device="cuda")
+        y = torch.empty(m * n, dtype=torch.float32, device="cuda")
+        gemv = m <= 8
+        need = 0 if gemv else q.plm_gemm_workspace_size(fmt, m, k)
+        work = torch.empty(max(need, 256), dtype=torch.uint8, device="cuda")
+        fn = getattr(q, ("plm_gemv_%s" if gemv else "plm_gemm_%s_ws") % fmt)
+        s = self.stream
+
+        def call(i):
+            w = ws_list[i % len(ws_list)]
+            if gemv:
+                fn(w, xq, y, m, n, k, stream=s)
+            else:
+                fn(w, xq, y, m, n, k, work, need, stream=s)
+        with torch.cuda.stream(s):
+            q.plm_quantize_q8K(x, xq, m, k, stream=s)
+            for i in range(warmup):
+                call(i)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            for i in range(steps):
+                call(i)
+            e1.record(s)
+            torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / steps
+        byt = wbytes + m * nb * Q8K_BYTES + m * n * 4
+        r = {"fmt": fmt, "n": n, "k": k, "m": m, "us": round(us, 3),
+             "entry": "plm_gemv_%s" % fmt if gemv else "plm_gemm_%s_ws" % fmt}
+        if gemv:
+            gbs = byt / us / 1e3
+            r.update({"GB_per_s": round(gbs, 1), "frac_hbm": round(gbs / self.peaks["hbm_gbs"], 4),
+                      "weights_per_s": n * k / (us * 1e-6)})
+        else:
+            tops = 2.0 * m * n * k / us / 1e6
+            r.update({"TOPS": round(tops, 1),
+                      "frac_f16_dense": round(tops / self.peaks["bf16_tflops"], 4),
+                      "vs_int8_tensor_peak": round(tops / self.peaks["int8_mma_tops"], 3)})
+        return r
+
+
+def run_extras(torch, q, peaks):
+    """Prefill GEMMs (Qwen3 m=512 shapes), the q6_K output head at m = 1, 8,
+    512, and the Qwen3-8B sweep over m, each shape timed alone."""
+    T = ShapeTimer(torch, q, peaks)
+    out = {}
+    res = []
+    for n, k in [(1024, 1024), (6144, 2048), (2048, 6144)]:
+        ws, wb = T.weights("q4K", 2, n, k)
+        res.append(T.run("q4K", ws, wb, n, k, 512, 10, 3))
+        del ws
+    out["prefill_gemm_q4K_m512"] = res
+    ws, wb = T.weights("q6K", 3, 151936, 2048)
+    out["q6K_head_151936x2048"] = [T.run("q6K", ws, wb, 151936, 2048, m, 10 if m <= 8 else 4, 2)
+                                   for m in (1, 8, 512)]
+    del ws
+    sweep = []
+    for fmt, n, k in [("q4K", 12288, 4096), ("q4K", 4096, 12288), ("q6K", 151936, 4096)]:
+        ws, wb = T.weights(fmt, 4, n, k)
+        for m in (1, 2, 4, 8, 64, 512, 2048):
+            steps = 10 if m <= 8 else (5 if n * k * m < 3e11 else 2)
+            sweep.append(T.run(fmt, ws, wb, n, k, m, steps, 1 if m > 512 else 2))
+        del ws
+        torch.cuda.empty_cache()
+    out["sweep_qwen3_8b"] = sweep
+    return out
+
+
 # --------------------------------------------------------------- main arm
 
 class Step:
@@ -453,6 +547,16 @@ def main():
         "clocks": clocks,
         "device_fault": fault,
     }
+    s8_tops, f16_tflops = q.plm_probe_mma_rates()
+    out["peaks"] = {"hbm_gbs": peak, "hbm_source": peak_src,
+                    "bf16_tflops": peaks.get("bf16_tflops", 1900.0),
+                    "int8_mma_tops": s8_tops, "f16_mma_sync_tflops": f16_tflops,
+                    "note": "int8: mma.sync.m16n8k32.s8 measured live (tcgen05 has no int8 kind on sm_103a); "
+                            "the GEMM runs kind::f16, so its roofline is the bf16/f16 dense peak"}
+    if rank == 0 and not args.no_extras:
+        del st
+        torch.cuda.empty_cache()
+        out["configs"] = run_extras(torch, q, out["peaks"])
     if rank == 0 and not args.no_cpu_baseline:
         val, sample, cores = oracle_rate(mats, host_w, xs, 12.0)
         import oracle

@@ -82,6 +82,16 @@ int plm_last_cuda_error(void);
 plm_status plm_device_fault(uint32_t* code, int clear);
 
 /*
+ * Diagnostic (the pages have no counterpart): measured throughput of the
+ * warp-level tensor instructions mma.sync m16n8k32 s8 (*s8_tops, TOPS) and
+ * mma.sync m16n8k16 f16 with f32 accumulation (*f16_tflops, TFLOPS) on the
+ * current device, from register-only loops on the legacy default stream.
+ * tcgen05 on sm_103a has no int8 kind, so the s8 figure is the int8 tensor
+ * rate this part offers.  Synchronizes; allocates nothing.
+ */
+plm_status plm_probe_mma_rates(double* s8_tops, double* f16_tflops);
+
+/*
  * q8_K activation quantization ("Current status" row "src/": activations
  * quantized to int8 the llama.cpp way, one 256-element block per task).
  * Per 256-element chunk of each row of x: the signed value `max` of largest

@@ -65,6 +65,8 @@ def load(build_if_missing=True):
     lib.plm_last_cuda_error.restype = ctypes.c_int
     lib.plm_device_fault.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]
     lib.plm_device_fault.restype = ctypes.c_int
+    lib.plm_probe_mma_rates.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)]
+    lib.plm_probe_mma_rates.restype = ctypes.c_int
     lib.plm_quantize_q8K.argtypes = [vp, vp, i64, i64, vp]
     lib.plm_quantize_q8K.restype = ctypes.c_int
     lib.plm_gemm_workspace_size.argtypes = [ctypes.c_int, i64, i64]
@@ -122,6 +124,14 @@ def plm_device_fault(clear=True):
     code = ctypes.c_uint32(0)
     _check("plm_device_fault", lib.plm_device_fault(ctypes.byref(code), 1 if clear else 0))
     return code.value
+
+
+def plm_probe_mma_rates():
+    """(mma.sync s8 TOPS, mma.sync f16 TFLOPS) measured on the current device; synchronizes."""
+    lib = load()
+    a, b = ctypes.c_double(0), ctypes.c_double(0)
+    _check("plm_probe_mma_rates", lib.plm_probe_mma_rates(ctypes.byref(a), ctypes.byref(b)))
+    return a.value, b.value
 
 
 def plm_quantize_q8K(x, xq, m, k, stream=None):
