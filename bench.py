@@ -68,6 +68,8 @@ def parse():
                     help="time one entry point alone, e.g. --case gemv q6K 151936 2048")
     ap.add_argument("--m", type=int, nargs="+", default=[1],
                     help="activation rows for --case (several values: a sweep)")
+    ap.add_argument("--no-chain", action="store_true",
+                    help="skip the dependent per-layer decode chain measurement")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the prefill GEMM, q6_K head and m-sweep measurements")
     return ap.parse_args()
@@ -268,6 +270,20 @@ def time_case(args):
                           "copies": copies, "fault": q.plm_device_fault()}), flush=True)
 
 
+def recorded_traffic(key):
+    """DRAM bytes per launch from the committed ncu record, or None when the
+    kernel sources changed since the capture."""
+    import hashlib
+    try:
+        rec = json.load(open(os.path.join(ROOT, "profiles", "ncu_traffic.json")))[key]
+        h = hashlib.sha256()
+        for p in rec["sources"]:
+            h.update(open(os.path.join(ROOT, p), "rb").read())
+        return rec["dram_bytes_per_launch"] if h.hexdigest()[:16] == rec["sources_sha256_16"] else None
+    except (OSError, ValueError, KeyError):
+        return None
+
+
 # --------------------------------------------------------------- other configs
 
 class ShapeTimer:
@@ -442,7 +458,8 @@ def main():
     with torch.cuda.stream(stream):
         for i in range(max(args.warmup, 3)):
             st.run(q, i % 2, stream)
-            st.run_chain(q, i % 2, stream)
+            if not args.no_chain:
+                st.run_chain(q, i % 2, stream)
     torch.cuda.synchronize()
     graphs, gemv_graphs, chain_graphs = [], [], []
     for c in range(2):
@@ -451,10 +468,11 @@ def main():
             with torch.cuda.graph(g, stream=stream):
                 st.run(q, c, stream, **kw)
             lst.append(g)
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            st.run_chain(q, c, stream)
-        chain_graphs.append(g)
+        if not args.no_chain:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                st.run_chain(q, c, stream)
+            chain_graphs.append(g)
     torch.cuda.synchronize()
 
     def barrier():
@@ -489,7 +507,8 @@ def main():
     with torch.cuda.stream(stream):
         for s in range(args.warmup):
             graphs[s % 2].replay()
-            chain_graphs[s % 2].replay()
+            if chain_graphs:
+                chain_graphs[s % 2].replay()
             e2e_step(s)
         torch.cuda.synchronize()
         sampler = ClockSampler(local)
@@ -497,7 +516,7 @@ def main():
         time.sleep(0.3)
         ms = timed(lambda s: graphs[s % 2].replay(), args.steps)
         gemv_ms = timed(lambda s: gemv_graphs[s % 2].replay(), args.steps)
-        chain_ms = timed(lambda s: chain_graphs[s % 2].replay(), args.steps)
+        chain_ms = timed(lambda s: chain_graphs[s % 2].replay(), args.steps) if chain_graphs else None
         t0 = time.perf_counter()
         e2e_ms = timed(e2e_step, args.steps)
         e2e_wall = (time.perf_counter() - t0) * 1e3
@@ -519,7 +538,7 @@ def main():
     peak = peaks.get("hbm_gbs", 6800.0)
     peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
     e2e_ms_step = max(e2e_ms, e2e_wall) / args.steps
-    chain_step = chain_ms / args.steps
+    chain_step = chain_ms / args.steps if chain_ms is not None else None
     chain_bytes = sum(gemv_bytes(sum(mats[l * 7 + f + j][2] for j in range(c)), mats[l * 7 + f][3])
                       + quant_bytes(mats[l * 7 + f][3]) for l in range(N_LAYERS) for f, c in CHAIN)
 
@@ -535,13 +554,15 @@ def main():
         "weights_per_s": world * sum(n * k for _, _, n, k, _ in mats) / (ms_step * 1e-3),
         "gpu_launches": (1 + launches_grouped) * args.steps,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": None, "peak_source": peak_src,
-                     "kernel": "gemv_kernel<q4_K, m=1, 32 warps, grouped>",
+                     "frac": achieved / peak, "traffic": recorded_traffic("gemv_q4K_grouped_m1"),
+                     "peak_source": peak_src,
+                     "kernel": "gemv_kernel<q4_K, m=1, 16 warps, grouped, register activations>",
                      "avg_launch_us": gemv_launch_ms * 1e3,
                      "bytes_per_launch": gemv_alg / launches_grouped},
-        "decode_chain": {"value": world * chain_bytes / (chain_step * 1e-3) / 1e9, "unit": "GB/s",
-                         "ms_per_step": chain_step, "launches_per_step": 8 * N_LAYERS,
-                         "what": "28 layers x 4 dependent (quantize, GEMV) stages, CUDA graph"},
+        "decode_chain": None if chain_step is None else {
+            "value": world * chain_bytes / (chain_step * 1e-3) / 1e9, "unit": "GB/s",
+            "ms_per_step": chain_step, "launches_per_step": 8 * N_LAYERS,
+            "what": "28 layers x 4 dependent (quantize, GEMV) stages, CUDA graph"},
         "e2e": {"value": world * alg / (e2e_ms_step * 1e-3) / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms_step},
         "clocks": clocks,
