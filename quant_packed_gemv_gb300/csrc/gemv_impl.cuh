@@ -39,6 +39,8 @@
 // the f32 result (verification export).
 #pragma once
 
+#include <type_traits>
+
 #include "plm_device.cuh"
 #include "plm_internal.h"
 
@@ -248,6 +250,17 @@ __device__ __forceinline__ void q6K_block(const uint8_t* slot, int off, const La
     }
 }
 
+// One block of the register path: adds this lane's f32 term of the block at
+// byte offset off of the stage to v[] (same arithmetic as the staged path).
+template <int FMT, int M>
+__device__ __forceinline__ void areg_block(const uint8_t* slot, int off, const LaneAct* act, const int* bsp, int t,
+                                           const Q4KScaleSel& sel, float* v) {
+    if constexpr (FMT == 4)
+        q4K_block<M, false>(slot + off, act, bsp, 0, t, sel, v, nullptr, 0);
+    else
+        q6K_block<M, false>(slot, off, act, 0, t, v, nullptr, 0);
+}
+
 // AREG: each lane keeps the activations of its (at most two) block columns
 // in registers for the whole segment; requires nb <= 16 and no SUBDOTS.
 template <int FMT, int M, bool SUBDOTS, int WARPS, int MAXP, bool AREG>
@@ -276,12 +289,19 @@ __global__ void __launch_bounds__(WARPS * 32, 1) gemv_kernel(const __grid_consta
     uint32_t issued = 0, consumed = 0;   // ring counters, uniform in the warp
     bool ok = true;                      // false once a wait ran out
 
-    for (int pi = 0; pi < B.count; ++pi) {
+    // problems are stored in byte order: start at the last one beginning at or before B0
+    int pfirst = 0;
+    for (int lo = 1, hi = B.count - 1; lo <= hi;) {
+        const int mid = (lo + hi) >> 1;
+        if (B.p[mid].byte_begin <= B0) { pfirst = mid; lo = mid + 1; } else { hi = mid - 1; }
+    }
+    for (int pi = pfirst; pi < B.count; ++pi) {
         const GemvProblem& P = B.p[pi];
         const long long rowbytes = (long long)P.nb * BYTES;
         const long long P0 = P.byte_begin;
         const long long P1 = P0 + (long long)P.n * rowbytes;
-        if (P1 <= B0 || P0 >= B1) continue;                       // CTA-uniform
+        if (P0 >= B1) break;                                      // CTA-uniform
+        if (P1 <= B0) continue;
         // rows whose first byte falls in [B0, B1)
         const int ra = (int)ceil_div_ll(B0 > P0 ? B0 - P0 : 0, rowbytes);
         const long long rb_ll = ceil_div_ll(B1 - P0, rowbytes);
@@ -325,18 +345,20 @@ __global__ void __launch_bounds__(WARPS * 32, 1) gemv_kernel(const __grid_consta
         ActSmem act{};
         LaneAct areg[AREG ? 2 : 1][M];
         int absp[AREG ? 2 : 1][M];
+        // register path geometry: packed rows -> row slot jrow, column quad % nb;
+        // otherwise columns quad and quad + 8, clamped to the row (a clamped
+        // column's result is discarded)
+        const int jrow = packed ? quad / nb : 0;
+        const int col0 = packed ? quad - jrow * nb : min(quad, nb - 1);
+        const int col1 = min(quad + BLOCKS_PER_STEP, nb - 1);
         if constexpr (AREG) {
-            // this lane's block columns: packed rows -> quad % nb; otherwise quad and quad + 8
             if (nst > 0) {
-                const int b0 = packed ? quad % nb : quad;
 #pragma unroll
                 for (int i = 0; i < M; ++i) {
-                    if (b0 < nb) {
-                        areg[0][i] = act_from_global<FMT>(P.xq, i * nb + b0, t);
-                        absp[0][i] = q4K_pair_sums(areg[0][i]);
-                    }
-                    if (!packed && b0 + 8 < nb) {
-                        areg[1][i] = act_from_global<FMT>(P.xq, i * nb + b0 + 8, t);
+                    areg[0][i] = act_from_global<FMT>(P.xq, i * nb + col0, t);
+                    absp[0][i] = q4K_pair_sums(areg[0][i]);
+                    if (!packed) {
+                        areg[1][i] = act_from_global<FMT>(P.xq, i * nb + col1, t);
                         absp[1][i] = q4K_pair_sums(areg[1][i]);
                     }
                 }
@@ -355,22 +377,14 @@ __global__ void __launch_bounds__(WARPS * 32, 1) gemv_kernel(const __grid_consta
         int crow = wa, cb0 = 0;
 
         // processes block bb of row rr of the slot; jreg selects the register column
-        auto do_block = [&](uint8_t* slot, const StageGeom& g, int rr, int bb, int b, int jreg, float* v,
+        auto do_block = [&](uint8_t* slot, const StageGeom& g, int rr, int bb, int b, float* v,
                             int32_t* sub_row) {
             LaneAct la[M];
             int lbsp[M];
-            if constexpr (AREG) {
 #pragma unroll
-                for (int i = 0; i < M; ++i) {
-                    la[i] = areg[jreg][i];
-                    lbsp[i] = absp[jreg][i];
-                }
-            } else {
-#pragma unroll
-                for (int i = 0; i < M; ++i) {
-                    la[i] = act_from_smem<FMT>(act, i * nb + b, t);
-                    lbsp[i] = q4K_pair_sums(la[i]);
-                }
+            for (int i = 0; i < M; ++i) {
+                la[i] = act_from_smem<FMT>(act, i * nb + b, t);
+                lbsp[i] = q4K_pair_sums(la[i]);
             }
             const int off = g.delta + (rr * nb + bb) * BYTES;
             if constexpr (FMT == 4)
@@ -398,18 +412,94 @@ __global__ void __launch_bounds__(WARPS * 32, 1) gemv_kernel(const __grid_consta
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
             }
-            if (packed) {
+            if constexpr (AREG) {
+                const int nr = g.nrows;
+                if (packed) {
+                    // a step covers 8/nb whole rows (a row owns 4*nb lanes); two steps
+                    // per iteration, rows past the stage clamped and not stored
+                    constexpr int PU = 2;                  // steps per iteration
+                    const int rw = BLOCKS_PER_STEP / nb;
+                    for (int r0 = 0; r0 < nr; r0 += PU * rw) {
+                        float v[PU][M];
+#pragma unroll
+                        for (int u = 0; u < PU; ++u) {
+#pragma unroll
+                            for (int i = 0; i < M; ++i) v[u][i] = 0.0f;
+                            const int rr = min(r0 + jrow + u * rw, nr - 1);
+                            areg_block<FMT, M>(slot, g.delta + (rr * nb + col0) * BYTES, areg[0], absp[0], t, sel,
+                                               v[u]);
+                        }
+#pragma unroll
+                        for (int o = 16; o >= 1; o >>= 1) {
+                            if (o <= 2 * nb) {
+#pragma unroll
+                                for (int u = 0; u < PU; ++u)
+#pragma unroll
+                                    for (int i = 0; i < M; ++i) v[u][i] += __shfl_xor_sync(0xFFFFFFFFu, v[u][i], o);
+                            }
+                        }
+                        if ((lane & (4 * nb - 1)) == 0) {
+#pragma unroll
+                            for (int u = 0; u < PU; ++u) {
+                                const int rr = r0 + jrow + u * rw;
+#pragma unroll
+                                for (int i = 0; i < M; ++i)
+                                    if (rr < nr) P.y[(size_t)i * P.n + crow + rr] = v[u][i];
+                            }
+                        }
+                    }
+                } else {
+                    // whole rows of at most 16 blocks: columns quad and quad + 8
+                    const bool has0 = quad < nb, has1 = quad + BLOCKS_PER_STEP < nb;
+                    // RU rows starting at stage row r0 (all below nr)
+                    auto rows = [&](auto ru_tag, int r0) {
+                        constexpr int RU = decltype(ru_tag)::value;
+                        float v[RU][M];
+#pragma unroll
+                        for (int u = 0; u < RU; ++u) {
+                            const int rr = r0 + u;
+                            float a0[M], a1[M];
+#pragma unroll
+                            for (int i = 0; i < M; ++i) a0[i] = 0.0f;
+                            areg_block<FMT, M>(slot, g.delta + (rr * nb + col0) * BYTES, areg[0], absp[0], t, sel,
+                                               a0);
+#pragma unroll
+                            for (int i = 0; i < M; ++i) a1[i] = a0[i];
+                            areg_block<FMT, M>(slot, g.delta + (rr * nb + col1) * BYTES, areg[1], absp[1], t, sel,
+                                               a1);
+#pragma unroll
+                            for (int i = 0; i < M; ++i) v[u][i] = has1 ? a1[i] : (has0 ? a0[i] : 0.0f);
+                        }
+#pragma unroll
+                        for (int o = 16; o >= 1; o >>= 1) {
+#pragma unroll
+                            for (int u = 0; u < RU; ++u)
+#pragma unroll
+                                for (int i = 0; i < M; ++i) v[u][i] += __shfl_xor_sync(0xFFFFFFFFu, v[u][i], o);
+                        }
+                        if (lane == 0) {
+#pragma unroll
+                            for (int u = 0; u < RU; ++u)
+#pragma unroll
+                                for (int i = 0; i < M; ++i) P.y[(size_t)i * P.n + crow + r0 + u] = v[u][i];
+                        }
+                    };
+                    int r0 = 0;
+                    if constexpr (M == 1)
+                        for (; r0 + 2 <= nr; r0 += 2) rows(std::integral_constant<int, 2>{}, r0);
+                    for (; r0 < nr; ++r0) rows(std::integral_constant<int, 1>{}, r0);
+                }
+            } else if (packed) {
                 // each step covers 8/nb whole rows; a row owns 4*nb lanes
                 const int rpstep = BLOCKS_PER_STEP / nb;
-                const int j = quad / nb, bq = quad - j * nb;
                 for (int r0 = 0; r0 < g.nrows; r0 += rpstep) {
-                    const int rr = r0 + j;
+                    const int rr = r0 + jrow;
                     const int row = crow + rr;
                     float v[M];
 #pragma unroll
                     for (int i = 0; i < M; ++i) v[i] = 0.0f;
                     int32_t* sub_row = SUBDOTS ? P.sub + (size_t)row * nb * Fmt<FMT>::SUB : nullptr;
-                    if (rr < g.nrows) do_block(slot, g, rr, bq, bq, 0, v, sub_row);
+                    if (rr < g.nrows) do_block(slot, g, rr, col0, col0, v, sub_row);
                     if constexpr (!SUBDOTS) {
 #pragma unroll
                         for (int i = 0; i < M; ++i) {
@@ -423,14 +513,8 @@ __global__ void __launch_bounds__(WARPS * 32, 1) gemv_kernel(const __grid_consta
                 for (int rr = 0; rr < g.nrows; ++rr) {
                     const int row = crow + rr;
                     int32_t* sub_row = SUBDOTS ? P.sub + (size_t)row * nb * Fmt<FMT>::SUB : nullptr;
-                    if constexpr (AREG) {
-                        // whole rows, nb <= 16: at most two blocks per lane
-                        if (quad < nb) do_block(slot, g, rr, quad, quad, 0, acc, sub_row);
-                        if (quad + 8 < nb) do_block(slot, g, rr, quad + 8, quad + 8, 1, acc, sub_row);
-                    } else {
-                        for (int bb = quad; bb < g.nblk; bb += BLOCKS_PER_STEP)
-                            do_block(slot, g, rr, bb, cb0 + bb, 0, acc, sub_row);
-                    }
+                    for (int bb = quad; bb < g.nblk; bb += BLOCKS_PER_STEP)
+                        do_block(slot, g, rr, bb, cb0 + bb, acc, sub_row);
                     const bool row_end = rps > 0 || cb0 + g.nblk >= nb;
                     if (row_end) {
                         if constexpr (!SUBDOTS) {
@@ -527,8 +611,9 @@ cudaError_t launch_batch(const HostProblem* hp, int count, int max_nb, int ns, c
 // Launches one pass (all problems share m = M rows of activations).
 template <int FMT, int M, bool SUB>
 cudaError_t launch_pass(const HostProblem* hp, int count, int max_nb, cudaStream_t stream) {
-    if constexpr (!SUB && M <= 2) {
-        // activations in registers: rows of at most 16 blocks
+    if constexpr (!SUB && M <= (FMT == 4 ? 2 : 1)) {
+        // activations in registers: rows of at most 16 blocks (q6_K: m = 1 only,
+        // the register budget of two activation rows is exceeded)
         if (max_nb <= 16) {
             const int ns = ring_depth<FMT>(0, max_nb, GEMV_WARPS);
             if (count == 1) return launch_batch<FMT, M, SUB, GEMV_WARPS, 1, true>(hp, count, max_nb, ns, stream);
