@@ -83,6 +83,7 @@ struct GemvBatch {
     int count;
     int nstages;            // ring depth per warp
     int act_bytes;          // 128-aligned size of the staged-activation region
+    int act_all;            // q4_K lane kernel: 1 = all segments staged at kernel start
     GemvProblem p[MAXP];
 };
 
@@ -287,6 +288,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1) gemv_kernel(const __grid_consta
     const long long B0 = T * blockIdx.x / gridDim.x;
     const long long B1 = T * (blockIdx.x + 1) / gridDim.x;
     uint32_t issued = 0, consumed = 0;   // ring counters, uniform in the warp
+    uint32_t islot = 0, cslot = 0, cphase = 0;   // next slot to fill / to consume, its phase parity
     bool ok = true;                      // false once a wait ran out
 
     // problems are stored in byte order: start at the last one beginning at or before B0
@@ -320,8 +322,8 @@ __global__ void __launch_bounds__(WARPS * 32, 1) gemv_kernel(const __grid_consta
         auto issue_one = [&]() {
             const StageGeom g = stage_geom<FMT>(irow, ib0, wb, rps, nb, wbytes);
             if (lane == 0) {
-                uint64_t* bar = &bars[issued % NS];
-                uint8_t* dst = ring + (issued % NS) * SLOT;
+                uint64_t* bar = &bars[islot];
+                uint8_t* dst = ring + islot * SLOT;
                 if (g.bytes > 0) {
                     mbar_arrive_expect_tx(bar, (uint32_t)g.bytes);
                     bulk_g2s(dst, P.w + g.src, (uint32_t)g.bytes, bar);
@@ -329,6 +331,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1) gemv_kernel(const __grid_consta
                     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(smem_u32(bar)) : "memory");
                 }
             }
+            islot = islot + 1 == (uint32_t)NS ? 0 : islot + 1;
             ++issued;
             ++inext;
             if (rps > 0) {
@@ -394,8 +397,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1) gemv_kernel(const __grid_consta
         };
 
         for (int s = 0; s < nst && ok; ++s) {
-            const uint32_t slot_i = consumed % NS;
-            if (!mbar_wait(&bars[slot_i], (consumed / NS) & 1)) {
+            if (!mbar_wait(&bars[cslot], cphase)) {
                 // a copy never completed: record it, let our other copies land, stop computing
                 if (lane == 0) {
                     atomicOr(B.fault, 1u);
@@ -405,7 +407,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1) gemv_kernel(const __grid_consta
                 ok = false;
                 break;
             }
-            uint8_t* slot = ring + slot_i * SLOT;
+            uint8_t* slot = ring + cslot * SLOT;
             const StageGeom g = stage_geom<FMT>(crow, cb0, wb, rps, nb, wbytes);
             if (FMT == 6 && g.tail > 0) {
                 if (lane < g.tail) slot[g.bytes + lane] = P.w[g.src + g.bytes + lane];
@@ -529,6 +531,10 @@ __global__ void __launch_bounds__(WARPS * 32, 1) gemv_kernel(const __grid_consta
                 }
             }
             ++consumed;
+            if (++cslot == (uint32_t)NS) {
+                cslot = 0;
+                cphase ^= 1u;
+            }
             if (rps > 0) {
                 crow += rps;
             } else {
