@@ -556,7 +556,7 @@ def main():
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": recorded_traffic("gemv_q4K_grouped_m1"),
                      "peak_source": peak_src,
-                     "kernel": "gemv_kernel<q4_K, m=1, 16 warps, grouped, register activations>",
+                     "kernel": "q4lane::lane_kernel<m=1, 16 warps, grouped> (q4_K, one lane per block)",
                      "avg_launch_us": gemv_launch_ms * 1e3,
                      "bytes_per_launch": gemv_alg / launches_grouped},
         "decode_chain": None if chain_step is None else {
