@@ -399,6 +399,7 @@ class Step:
         self.y = torch.empty(yo, dtype=torch.float32, device=dev)
         self.y_host = torch.empty(yo, dtype=torch.float32).pin_memory()
         self.nchunks = xo // QK
+        self.fused = None
         # grouped problem lists, one per weight copy
         self.problems = []
         for c in range(2):
@@ -406,6 +407,15 @@ class Step:
             self.problems.append([(wp + off, self.xq.data_ptr() + self.qoff[i],
                                    self.y.data_ptr() + 4 * self.yoff[i], n, k)
                                   for i, (_, _, n, k, off) in enumerate(mats)])
+
+    def fused_problems(self, copy):
+        wp, xp, yp = self.w[copy].data_ptr(), self.x.data_ptr(), self.y.data_ptr()
+        return [(wp + off, xp + 4 * self.xoff[i], yp + 4 * self.yoff[i], n, k)
+                for i, (_, _, n, k, off) in enumerate(self.mats)]
+
+    def run_fused(self, q, copy, stream):
+        """One launch: each CTA quantizes its activations and runs the GEMV."""
+        q.plm_quantize_gemv_q4K_grouped(self.fused[copy], 1, stream=stream)
 
     def run(self, q, copy, stream, quantize=True, gemv=True):
         if quantize:
@@ -455,14 +465,20 @@ def main():
     st = Step(torch, dev, mats, host_w, xs)
     stream = torch.cuda.Stream(device=dev)
 
+    st.fused = [st.fused_problems(c) for c in range(2)]
     with torch.cuda.stream(stream):
         for i in range(max(args.warmup, 3)):
             st.run(q, i % 2, stream)
+            st.run_fused(q, i % 2, stream)
             if not args.no_chain:
                 st.run_chain(q, i % 2, stream)
     torch.cuda.synchronize()
-    graphs, gemv_graphs, chain_graphs = [], [], []
+    graphs, gemv_graphs, chain_graphs, fused_graphs = [], [], [], []
     for c in range(2):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            st.run_fused(q, c, stream)
+        fused_graphs.append(g)
         for lst, kw in ((graphs, {}), (gemv_graphs, {"quantize": False})):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
@@ -516,6 +532,7 @@ def main():
         time.sleep(0.3)
         ms = timed(lambda s: graphs[s % 2].replay(), args.steps)
         gemv_ms = timed(lambda s: gemv_graphs[s % 2].replay(), args.steps)
+        fused_ms = timed(lambda s: fused_graphs[s % 2].replay(), args.steps)
         chain_ms = timed(lambda s: chain_graphs[s % 2].replay(), args.steps) if chain_graphs else None
         t0 = time.perf_counter()
         e2e_ms = timed(e2e_step, args.steps)
@@ -539,6 +556,8 @@ def main():
     peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
     e2e_ms_step = max(e2e_ms, e2e_wall) / args.steps
     chain_step = chain_ms / args.steps if chain_ms is not None else None
+    # fused step: weights, f32 activations read once, y written once
+    fused_bytes = sum(n * (k // QK) * Q4K_BYTES + 4 * k + 4 * n for _, _, n, k, _ in mats)
     chain_bytes = sum(gemv_bytes(sum(mats[l * 7 + f + j][2] for j in range(c)), mats[l * 7 + f][3])
                       + quant_bytes(mats[l * 7 + f][3]) for l in range(N_LAYERS) for f, c in CHAIN)
 
@@ -563,6 +582,11 @@ def main():
             "value": world * chain_bytes / (chain_step * 1e-3) / 1e9, "unit": "GB/s",
             "ms_per_step": chain_step, "launches_per_step": 8 * N_LAYERS,
             "what": "28 layers x 4 dependent (quantize, GEMV) stages, CUDA graph"},
+        "decode_set_fused": {
+            "value": world * fused_bytes / (fused_ms / args.steps * 1e-3) / 1e9, "unit": "GB/s",
+            "ms_per_step": fused_ms / args.steps, "launches_per_step": launches_grouped,
+            "what": "plm_quantize_gemv_q4K_grouped: the same step as one launch, q8_K produced in-kernel",
+            "bytes_per_step": fused_bytes},
         "e2e": {"value": world * alg / (e2e_ms_step * 1e-3) / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms_step},
         "clocks": clocks,

@@ -148,6 +148,35 @@ plm_status plm_gemv_q6K_grouped(const plm_gemv_problem* problems, int64_t count,
                                 cudaStream_t stream);
 
 /*
+ * Fused q8_K producer + decode GEMV (q4_K), y = W . x for 1 <= m <= 8, on
+ * f32 activations.  PocketLLM (Korean README), "Current status" table, row
+ * "src/": the packed matmul runs on int8 activations quantized per 256-value
+ * block; here that quantization happens inside the GEMV launch.  Each CTA
+ * quantizes the activation rows of the problems it covers with the same
+ * arithmetic as plm_quantize_q8K (first-occurrence signed amax,
+ * iscale = -128/max, round half to even, clamp at 127, d = 1/iscale), so y is
+ * bit-identical to plm_quantize_q8K followed by plm_gemv_q4K, without the
+ * q8_K round trip through memory or the second launch.
+ *   x  device f32 [m][k], 16-byte aligned (else PLM_ERR_MISALIGNED);
+ *   w, y as for plm_gemv_q4K.  No workspace, nothing allocated.
+ * Errors as for plm_gemv_q4K.
+ */
+plm_status plm_quantize_gemv_q4K(const void* w, const float* x, float* y, int64_t m, int64_t n, int64_t k,
+                                 cudaStream_t stream);
+
+/* Grouped form: independent problems sharing m, f32 activations each. */
+typedef struct {
+    const void* w;    /* q4_K [n][k/256] */
+    const float* x;   /* f32 [m][k], 16-byte aligned */
+    float* y;         /* f32 [m][n] */
+    int64_t n;
+    int64_t k;
+} plm_qgemv_problem;
+
+plm_status plm_quantize_gemv_q4K_grouped(const plm_qgemv_problem* problems, int64_t count, int64_t m,
+                                         cudaStream_t stream);
+
+/*
  * Prefill GEMM, y = X . W^T for any m >= 1 (intended for m = 512..2048).
  * For m >= 9 the activation codes are first widened to an f16 matrix in a
  * workspace; weight tiles are decoded in shared memory into exact

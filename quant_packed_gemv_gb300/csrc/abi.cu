@@ -95,6 +95,32 @@ plm_status grouped_common(int fmt, const plm_gemv_problem* problems, int64_t cou
     return PLM_OK;
 }
 
+// Fused quantize + GEMV: f32 activations, 16-byte aligned for vector loads.
+plm_status qgemv_common(const plm_qgemv_problem* problems, int64_t count, int64_t m, cudaStream_t stream) {
+    if (!problems || count <= 0 || count > kMaxIndex) return PLM_ERR_INVALID_ARG;
+    if (m <= 0 || m > plm::GEMV_MAX_M) return PLM_ERR_INVALID_ARG;
+    for (int64_t j = 0; j < count; ++j) {
+        const plm_qgemv_problem& p = problems[j];
+        plm_status s = check_matmul(p.w, p.x, p.y, m, p.n, p.k, plm::GEMV_MAX_M);
+        if (s != PLM_OK) return s;
+        if (!aligned(p.x, 16)) return PLM_ERR_MISALIGNED;
+    }
+    for (int64_t j = 0; j < count; ++j)
+        if (!plm::gemv_supported(4, (int)problems[j].k)) return PLM_ERR_UNSUPPORTED;
+    constexpr int kChunk = 256;
+    plm::GroupItem items[kChunk];
+    for (int64_t p0 = 0; p0 < count; p0 += kChunk) {
+        const int cnt = (int)(count - p0 < kChunk ? count - p0 : kChunk);
+        for (int j = 0; j < cnt; ++j) {
+            const plm_qgemv_problem& p = problems[p0 + j];
+            items[j] = plm::GroupItem{(const uint8_t*)p.w, (const uint8_t*)p.x, p.y, (int)p.n, (int)p.k};
+        }
+        plm_status s = cuda_status(plm::launch_quantize_gemv_q4K(items, cnt, (int)m, stream));
+        if (s != PLM_OK) return s;
+    }
+    return PLM_OK;
+}
+
 plm_status gemm_common(int fmt, const void* w, const void* xq, float* y, int64_t m, int64_t n,
                        int64_t k, cudaStream_t stream) {
     plm_status s = check_matmul(w, xq, y, m, n, k, kMaxIndex);
@@ -222,6 +248,17 @@ plm_status plm_gemm_q4K_noalloc(const void* w, const void* xq, float* y, int64_t
     if (!plm::gemv_supported(4, (int)k)) return PLM_ERR_UNSUPPORTED;
     return cuda_status(plm::launch_gemm_q4K_noalloc((const uint8_t*)w, (const uint8_t*)xq, y, m, (int)n, (int)k,
                                                     stream));
+}
+
+plm_status plm_quantize_gemv_q4K(const void* w, const float* x, float* y, int64_t m, int64_t n, int64_t k,
+                                 cudaStream_t stream) {
+    const plm_qgemv_problem p{w, x, y, n, k};
+    return qgemv_common(&p, 1, m, stream);
+}
+
+plm_status plm_quantize_gemv_q4K_grouped(const plm_qgemv_problem* problems, int64_t count, int64_t m,
+                                         cudaStream_t stream) {
+    return qgemv_common(problems, count, m, stream);
 }
 
 plm_status plm_subdots_q4K(const void* w, const void* xq, int32_t* out, int64_t m, int64_t n,

@@ -1,0 +1,588 @@
+// Decode GEMV over q4_K weights, one lane per 256-weight block
+// (PocketLLM "What it runs": K-quant weights decoded inside the kernel and
+// never widened; the weight stream is read once for all m <= 8 activation
+// rows, as the pages' 8-row activation tile does on the CPU).
+//
+// Work split: as in the generic GEMV (gemv_impl.cuh), the weight bytes of
+// all problems of a launch are split evenly over persistent CTAs; a CTA
+// splits each problem's rows in its range evenly over its warps, and each
+// warp streams its rows through a private ring of 4608-byte stages
+// (32 blocks) filled by bulk copies with bounded mbarrier waits.
+//
+// One warp step consumes one stage: lane L decodes block L of the stage in
+// full (scales, mins, all eight 32-weight sub-blocks) against every
+// activation row, so per-block fixed work is done once, not four times, and
+// the cross-lane reduction is paid once per 32 blocks.  A stage holds
+// floor(32 / nb) whole rows when nb <= 32 (row r on lanes [r*nb, r*nb+nb)),
+// else 32 blocks of one row.  Row sums: butterfly over nb lanes when nb is a
+// power of two, else a segmented shuffle-down; a row spanning several stages
+// accumulates per lane first.  The f32 order of a row depends only on nb, so
+// activation row i gives the same bits for every m and every grouping.
+//
+// Activations are staged once per CTA in shared memory, re-laid out per
+// (row, block): the 256 codes, then the eight sums of adjacent bsum pairs
+// (the min term's operands), 272 bytes apart so that eight lanes reading
+// eight different blocks at the same offset hit distinct banks; the scales d
+// sit in a separate float array, all at kernel start.
+//
+// XF32 (the fused q8_K producer): the problems carry f32 activations and the
+// CTA quantizes them itself while staging (q8K_quantize_warp, the same
+// arithmetic as the stand-alone quantizer), so the staged records and every
+// output bit equal those of quantize + GEMV, without the q8_K round trip
+// through memory or the second launch.
+#pragma once
+
+#include <algorithm>
+#include <cstdint>
+#include <type_traits>
+
+#include "gemv_impl.cuh"
+
+namespace plm {
+namespace q4lane {
+
+constexpr int STAGE_BLOCKS = 32;
+constexpr int SLOT = STAGE_BLOCKS * Q4K_BYTES;   // 4608
+constexpr int REC = 272;                         // staged bytes per activation block
+
+// Bytes of one staged segment of nblk activation blocks: records, then the
+// scales, padded to 16 bytes so the next segment's records stay aligned.
+__host__ __device__ __forceinline__ int seg_bytes(int nblk) { return nblk * REC + ((nblk * 4 + 15) & ~15); }
+
+// One problem of a launch.  Work is cut into units: rps whole rows (one
+// stage) when a row has at most 32 blocks, else one row (ceil(nb / 32)
+// stages, weight ceil(nb / 32)).  wbegin is the problem's first unit in the
+// launch's weighted unit space.
+struct LaneProblem {
+    const uint8_t* w;
+    const uint8_t* xq;
+    float* y;
+    int32_t* sub;
+    int n, nb;
+    int rps;                // rows per unit (0: one row per unit, several stages)
+    int wbegin;             // weighted units before this problem
+};
+
+template <int MAXP>
+struct LaneBatch {
+    unsigned* fault;
+    int count;
+    int nstages;            // ring depth per warp
+    int act_bytes;          // staged-activation region (all problems of the CTA)
+    int wtotal;             // weighted units of the launch
+    LaneProblem p[MAXP];
+};
+
+__host__ __device__ __forceinline__ int unit_weight(int nb) { return nb <= STAGE_BLOCKS ? 1 : (nb + STAGE_BLOCKS - 1) / STAGE_BLOCKS; }
+__host__ __device__ __forceinline__ int unit_count(int n, int rps) { return rps > 0 ? (n + rps - 1) / rps : n; }
+
+// A warp's position in its unit range: problem p, unit u of [u, uend), chunk ch
+// of the unit's row (one-row units only).  p < 0: the range is exhausted.
+struct Cursor {
+    int p, u, uend, ch;
+};
+
+// Moves to the first problem at or after p that has a unit starting in [W0, W1).
+template <int MAXP>
+__device__ __forceinline__ void cursor_enter(const LaneBatch<MAXP>& B, Cursor& c, int p, int W0, int W1) {
+    for (; p < B.count && B.p[p].wbegin < W1; ++p) {
+        const LaneProblem& P = B.p[p];
+        const int wt = unit_weight(P.nb);
+        const int a = W0 - P.wbegin, b = W1 - P.wbegin;
+        const int u0 = a > 0 ? (a + wt - 1) / wt : 0;
+        const int u1 = min(unit_count(P.n, P.rps), (b + wt - 1) / wt);
+        if (u0 < u1) {
+            c = Cursor{p, u0, u1, 0};
+            return;
+        }
+    }
+    c.p = -1;
+}
+
+template <int MAXP>
+__device__ __forceinline__ void cursor_next(const LaneBatch<MAXP>& B, Cursor& c, int nb, int W0, int W1) {
+    if (nb > STAGE_BLOCKS && ++c.ch < unit_weight(nb)) return;
+    c.ch = 0;
+    if (++c.u < c.uend) return;
+    cursor_enter(B, c, c.p + 1, W0, W1);
+}
+
+// Last problem whose weighted range starts at or before W.
+template <int MAXP>
+__device__ __forceinline__ int problem_at(const LaneBatch<MAXP>& B, int W) {
+    int r = 0;
+    for (int lo = 1, hi = B.count - 1; lo <= hi;) {
+        const int mid = (lo + hi) >> 1;
+        if (B.p[mid].wbegin <= W) { r = mid; lo = mid + 1; } else { hi = mid - 1; }
+    }
+    return r;
+}
+
+// Stages the q8_K blocks of one problem (m rows of nb blocks) for the lanes:
+// records of REC bytes (codes, then eight int16 sums of adjacent bsums) and
+// a float array of the scales.  All threads of the CTA take part.
+__device__ __forceinline__ void act_fill(uint8_t* rec, float* dy, const uint8_t* __restrict__ xq, int nblk) {
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(xq);
+    constexpr int WORDS = Q8K_BYTES / 4;   // 73
+    const int total = nblk * WORDS;
+    for (int idx = threadIdx.x; idx < total; idx += blockDim.x) {
+        const int blk = idx / WORDS;
+        const int wd = idx - blk * WORDS;
+        const uint32_t v = __ldg(src + idx);
+        if (wd == 0) {
+            dy[blk] = __uint_as_float(v);
+        } else if (wd <= 64) {
+            reinterpret_cast<uint32_t*>(rec + (size_t)blk * REC)[wd - 1] = v;
+        } else {
+            const int j = wd - 65;   // bsums 2j, 2j+1
+            const int pair = (int)(int16_t)(v & 0xFFFFu) + (int)(int16_t)(v >> 16);
+            reinterpret_cast<int16_t*>(rec + (size_t)blk * REC + 256)[j] = (int16_t)pair;
+        }
+    }
+}
+
+// Quantizes m rows of f32 activations (nblk 256-value chunks, row-major, so
+// chunk c starts at x + 256 c) straight into the staged layout: one warp per
+// chunk, the warps of the CTA taking chunks in turn.
+template <int WARPS>
+__device__ __forceinline__ void act_fill_f32(uint8_t* rec, float* dy, const float* __restrict__ x, int nblk,
+                                             int warp, int lane) {
+    for (int c = warp; c < nblk; c += WARPS) {
+        const float4* src = reinterpret_cast<const float4*>(x + (size_t)c * QK) + 2 * lane;
+        const float4 a = __ldg(src), b = __ldg(src + 1);
+        const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        int q[8];
+        const float d = q8K_quantize_warp(v, lane, q);
+        uint32_t w0, w1;
+        pack_codes8(q, w0, w1);
+        uint32_t* dst = reinterpret_cast<uint32_t*>(rec + (size_t)c * REC) + 2 * lane;
+        dst[0] = w0;
+        dst[1] = w1;
+        // lanes 4j .. 4j+3 hold values 32j .. 32j+31: the sum of bsums 2j and 2j+1
+        int s = q[0] + q[1] + q[2] + q[3] + q[4] + q[5] + q[6] + q[7];
+        s += __shfl_xor_sync(0xFFFFFFFFu, s, 1);
+        s += __shfl_xor_sync(0xFFFFFFFFu, s, 2);
+        if ((lane & 3) == 0) reinterpret_cast<int16_t*>(rec + (size_t)c * REC + 256)[lane >> 2] = (int16_t)s;
+        if (lane == 0) dy[c] = d;
+    }
+}
+
+__device__ __forceinline__ int dp2a_hi_su(int a, uint32_t b, int c) {
+    int d;
+    asm("dp2a.hi.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// One whole q4_K block against M staged activation blocks (same column,
+// records act_stride bytes apart, scales dy_stride floats apart).  Adds the
+// block's f32 term to v[i], or writes the eight exact sub-block dots.
+template <int M, bool SUBDOTS>
+__device__ __forceinline__ void lane_block(const uint8_t* w, const uint8_t* act, int act_stride, const float* dy,
+                                           int dy_stride, float* v, int32_t* sub, size_t sub_stride) {
+    const uint4 hdr = *reinterpret_cast<const uint4*>(w);
+    // six-bit scales (sc) and mins (m) as bytes: j = 0..3 and j = 4..7
+    const uint32_t scA = hdr.y & 0x3F3F3F3Fu;
+    const uint32_t mA = hdr.z & 0x3F3F3F3Fu;
+    const uint32_t scB = (hdr.w & 0x0F0F0F0Fu) | ((hdr.y >> 2) & 0x30303030u);
+    const uint32_t mB = ((hdr.w >> 4) & 0x0F0F0F0Fu) | ((hdr.z >> 2) & 0x30303030u);
+    int isum[M];
+#pragma unroll
+    for (int i = 0; i < M; ++i) isum[i] = 0;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const uint4 qa = *reinterpret_cast<const uint4*>(w + 16 + 32 * c);
+        const uint4 qb = *reinterpret_cast<const uint4*>(w + 32 + 32 * c);
+        const uint32_t q[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+        const uint32_t sw = c < 2 ? scA : scB;
+        const int s0 = (int)((sw >> (16 * (c & 1))) & 0xFFu);
+        const int s1 = (int)((sw >> (16 * (c & 1) + 8)) & 0xFFu);
+#pragma unroll
+        for (int i = 0; i < M; ++i) {
+            const int4* x = reinterpret_cast<const int4*>(act + (size_t)i * act_stride + 64 * c);
+            const int4 x0 = x[0], x1 = x[1], x2 = x[2], x3 = x[3];
+            const int xl[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+            const int xh[8] = {x2.x, x2.y, x2.z, x2.w, x3.x, x3.y, x3.z, x3.w};
+            int lo = 0, hi = 0;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                lo = dp4a_us(q[u] & 0x0F0F0F0Fu, xl[u], lo);
+                hi = dp4a_us(q[u] & 0xF0F0F0F0u, xh[u], hi);
+            }
+            hi >>= 4;   // the high nibbles were used in place (16 * q)
+            if constexpr (SUBDOTS) {
+                sub[i * sub_stride + 2 * c] = lo;
+                sub[i * sub_stride + 2 * c + 1] = hi;
+            } else {
+                isum[i] += s0 * lo + s1 * hi;
+            }
+        }
+    }
+    if constexpr (!SUBDOTS) {
+        const float d = half_bits_to_float(hdr.x);
+        const float dmin = half_bits_to_float(hdr.x >> 16);
+#pragma unroll
+        for (int i = 0; i < M; ++i) {
+            const int4 pr = *reinterpret_cast<const int4*>(act + (size_t)i * act_stride + 256);
+            int ms = dp2a_lo_su(pr.x, mA, 0);
+            ms = dp2a_hi_su(pr.y, mA, ms);
+            ms = dp2a_lo_su(pr.z, mB, ms);
+            ms = dp2a_hi_su(pr.w, mB, ms);
+            const float tt = __fmaf_rn(d, (float)isum[i], -__fmul_rn(dmin, (float)ms));
+            v[i] = __fmaf_rn(dy[i * dy_stride], tt, v[i]);
+        }
+    }
+}
+
+template <int M, bool SUBDOTS, bool XF32, int WARPS, int MAXP>
+__global__ void __launch_bounds__(WARPS * 32, 1) lane_kernel(const __grid_constant__ LaneBatch<MAXP> B) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int NS = B.nstages;
+    uint8_t* ring = smem + B.act_bytes + (size_t)warp * NS * SLOT;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + B.act_bytes + (size_t)WARPS * NS * SLOT) + warp * NS;
+    if (lane == 0) {
+        for (int j = 0; j < NS; ++j) mbar_init(&bars[j], 1);
+        fence_barrier_init();
+    }
+    __syncwarp();
+
+    // even split of the weighted units over all warps of the grid
+    const long long G = (long long)gridDim.x * WARPS;
+    const long long gw = (long long)blockIdx.x * WARPS + warp;
+    const int W0 = (int)(B.wtotal * gw / G), W1 = (int)(B.wtotal * (gw + 1) / G);
+    const int C0 = (int)(B.wtotal * ((long long)blockIdx.x * WARPS) / G);
+    const int C1 = (int)(B.wtotal * ((long long)blockIdx.x * WARPS + WARPS) / G);
+
+    // copy cursor: lane 0 issues; runs up to NS stages ahead, across problems
+    Cursor ic;
+    cursor_enter(B, ic, problem_at(B, W0), W0, W1);
+    uint32_t issued = 0, consumed = 0;           // ring counters, uniform in the warp
+    uint32_t islot = 0, cslot = 0, cphase = 0;   // next slot to fill / to consume, its phase parity
+    auto issue_one = [&]() {
+        const LaneProblem& Q = B.p[ic.p];
+        const int nb = Q.nb;
+        int blocks;
+        long long first;   // first block of the stage
+        if (nb <= STAGE_BLOCKS) {
+            const int r0 = ic.u * Q.rps;
+            blocks = min(Q.rps, Q.n - r0) * nb;
+            first = (long long)r0 * nb;
+        } else {
+            const int b0 = ic.ch * STAGE_BLOCKS;
+            blocks = min(STAGE_BLOCKS, nb - b0);
+            first = (long long)ic.u * nb + b0;
+        }
+        if (lane == 0) {
+            uint64_t* bar = &bars[islot];
+            const uint32_t bytes = (uint32_t)blocks * Q4K_BYTES;   // q4_K rows: whole 16-byte multiples
+            mbar_arrive_expect_tx(bar, bytes);
+            bulk_g2s(ring + islot * SLOT, Q.w + first * Q4K_BYTES, bytes, bar);
+        }
+        islot = islot + 1 == (uint32_t)NS ? 0 : islot + 1;
+        ++issued;
+        cursor_next(B, ic, nb, W0, W1);
+    };
+    while (ic.p >= 0 && issued < (uint32_t)NS) issue_one();
+
+    // stage the activations of every problem the CTA's warps touch
+    const int cfirst = problem_at(B, C0);
+    {
+        int off = 0;
+        for (int p = cfirst; p < B.count && B.p[p].wbegin < C1; ++p) {
+            const int nblk = M * B.p[p].nb;
+            float* dy = reinterpret_cast<float*>(smem + off + (size_t)nblk * REC);
+            if constexpr (XF32)
+                act_fill_f32<WARPS>(smem + off, dy, reinterpret_cast<const float*>(B.p[p].xq), nblk, warp, lane);
+            else
+                act_fill(smem + off, dy, B.p[p].xq, nblk);
+            off += seg_bytes(nblk);
+        }
+    }
+    __syncthreads();
+
+    Cursor cc;
+    cursor_enter(B, cc, problem_at(B, W0), W0, W1);
+    int act_p = cfirst, act_off = 0;   // staged offset of problem act_p
+    bool ok = true;                    // false once a wait ran out
+    while (cc.p >= 0 && ok) {
+        // per problem: geometry and pointers
+        const LaneProblem& P = B.p[cc.p];
+        const int p_now = cc.p;
+        const int nb = P.nb, n = P.n, rps = P.rps;
+        while (act_p < p_now) {
+            act_off += seg_bytes(M * B.p[act_p].nb);
+            ++act_p;
+        }
+        const uint8_t* rec = smem + act_off;
+        const float* dyv = reinterpret_cast<const float*>(rec + (size_t)M * nb * REC);
+        const int act_stride = nb * REC;
+        const size_t sub_stride = (size_t)n * nb * 8;
+        float* yv = P.y;
+        int32_t* subv = P.sub;
+        const int rl = rps > 0 ? lane / nb : 0;   // row mode: row slot and column of this lane
+        const int cl = rps > 0 ? lane - rl * nb : lane;
+        const bool pow2 = (nb & (nb - 1)) == 0;
+        float acc[M];
+#pragma unroll
+        for (int i = 0; i < M; ++i) acc[i] = 0.0f;
+
+        while (cc.p == p_now) {
+            if (!mbar_wait(&bars[cslot], cphase)) {
+                // a copy never completed: record it, let our other copies land, stop
+                if (lane == 0) {
+                    atomicOr(B.fault, 1u);
+                    for (uint32_t c2 = consumed; c2 < issued; ++c2) (void)mbar_wait(&bars[c2 % NS], (c2 / NS) & 1);
+                }
+                __syncwarp();
+                ok = false;
+                break;
+            }
+            const uint8_t* slot = ring + cslot * SLOT;
+            if (rps > 0) {
+                const int r0 = cc.u * rps;
+                const int nrows = min(rps, n - r0);
+                const bool valid = rl < nrows;
+                const int bl = valid ? lane : 0;   // clamped block of the stage; result discarded
+                const int col = valid ? cl : 0;
+                float v[M];
+#pragma unroll
+                for (int i = 0; i < M; ++i) v[i] = 0.0f;
+                int32_t* sub = SUBDOTS ? subv + ((size_t)(r0 + rl) * nb + col) * 8 : nullptr;
+                if (!SUBDOTS || valid)
+                    lane_block<M, SUBDOTS>(slot + bl * Q4K_BYTES, rec + (size_t)col * REC, act_stride, dyv + col,
+                                           nb, v, sub, sub_stride);
+                if constexpr (!SUBDOTS) {
+                    if (pow2) {
+#pragma unroll
+                        for (int o = 16; o >= 1; o >>= 1)
+                            if (o < nb) {
+#pragma unroll
+                                for (int i = 0; i < M; ++i) v[i] += __shfl_xor_sync(0xFFFFFFFFu, v[i], o);
+                            }
+                    } else {
+#pragma unroll
+                        for (int o = 1; o <= 16; o <<= 1) {
+#pragma unroll
+                            for (int i = 0; i < M; ++i) {
+                                const float u = __shfl_down_sync(0xFFFFFFFFu, v[i], o);
+                                if (cl + o < nb) v[i] += u;
+                            }
+                        }
+                    }
+                    if (valid && cl == 0) {
+#pragma unroll
+                        for (int i = 0; i < M; ++i) yv[(size_t)i * n + r0 + rl] = v[i];
+                    }
+                }
+            } else {
+                const int b0 = cc.ch * STAGE_BLOCKS;
+                const int nblk_s = min(STAGE_BLOCKS, nb - b0);
+                const bool valid = lane < nblk_s;
+                const int b = b0 + (valid ? lane : 0);
+                float v[M];
+#pragma unroll
+                for (int i = 0; i < M; ++i) v[i] = acc[i];
+                int32_t* sub = SUBDOTS ? subv + ((size_t)cc.u * nb + b) * 8 : nullptr;
+                if (!SUBDOTS || valid)
+                    lane_block<M, SUBDOTS>(slot + (valid ? lane : 0) * Q4K_BYTES, rec + (size_t)b * REC, act_stride,
+                                           dyv + b, nb, v, sub, sub_stride);
+#pragma unroll
+                for (int i = 0; i < M; ++i) acc[i] = valid ? v[i] : acc[i];
+                if (b0 + STAGE_BLOCKS >= nb) {   // last stage of the row
+                    if constexpr (!SUBDOTS) {
+#pragma unroll
+                        for (int i = 0; i < M; ++i) {
+                            const float x = warp_sum(acc[i]);
+                            if (lane == 0) yv[(size_t)i * n + cc.u] = x;
+                            acc[i] = 0.0f;
+                        }
+                    }
+                }
+            }
+            ++consumed;
+            if (++cslot == (uint32_t)NS) {
+                cslot = 0;
+                cphase ^= 1u;
+            }
+            __syncwarp();
+            if (ic.p >= 0) issue_one();
+            cursor_next(B, cc, nb, W0, W1);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+struct Config {
+    int warps, ns, grid, act_bytes;
+};
+
+inline size_t ring_bytes(int warps, int ns) { return (size_t)warps * ns * (SLOT + 8); }
+inline size_t align128(size_t x) { return (x + 127) & ~(size_t)127; }
+
+struct Plan {
+    int rps[GROUP_MAX], wbegin[GROUP_MAX];
+    long long wtotal;
+};
+
+// Units per problem.  A launch too small to give every warp of the GPU two
+// units takes fewer rows per unit (down to one), so that its rows still
+// spread over all SMs; rows per unit do not change any row's arithmetic.
+inline void make_plan(const HostProblem* hp, int count, int warps, Plan* pl) {
+    const long long target = 2LL * num_sms() * warps;
+    for (int shrink = 1;; shrink *= 2) {
+        long long w = 0;
+        bool reducible = false;
+        for (int i = 0; i < count; ++i) {
+            const int nb = hp[i].nb;
+            const int full = nb <= STAGE_BLOCKS ? STAGE_BLOCKS / nb : 0;
+            pl->rps[i] = full > 0 ? std::max(1, full / shrink) : 0;
+            reducible = reducible || pl->rps[i] > 1;
+            pl->wbegin[i] = (int)std::min(w, (long long)INT32_MAX);
+            w += (long long)unit_count(hp[i].n, pl->rps[i]) * unit_weight(nb);
+        }
+        pl->wtotal = w;
+        if (w >= target || !reducible) return;
+    }
+}
+
+// Largest staged-activation region over the CTAs: every problem whose
+// weighted range meets the CTA's (the kernel stages the same set).
+inline size_t act_need(const HostProblem* hp, int count, const Plan& pl, int m, int grid, int warps) {
+    const long long G = (long long)grid * warps;
+    size_t worst = 0;
+    int p = 0;
+    for (int c = 0; c < grid; ++c) {
+        const long long C0 = pl.wtotal * ((long long)c * warps) / G;
+        const long long C1 = pl.wtotal * ((long long)c * warps + warps) / G;
+        while (p + 1 < count && pl.wbegin[p + 1] <= C0) ++p;
+        size_t sum = 0;
+        for (int q = p; q < count && pl.wbegin[q] < C1; ++q) sum += (size_t)seg_bytes(m * hp[q].nb);
+        worst = std::max(worst, sum);
+    }
+    return align128(worst);
+}
+
+inline bool pick_config(const HostProblem* hp, int count, const Plan& pl, int m, Config* cfg) {
+    const size_t optin = (size_t)smem_optin_bytes();
+    const int opts[][2] = {{16, 3}, {16, 2}, {12, 2}};
+    for (const auto& o : opts) {
+        long long grid = num_sms();
+        const long long want = (pl.wtotal + o[0] - 1) / o[0];   // no CTA without a unit per warp
+        if (grid > want) grid = want;
+        if (grid < 1) grid = 1;
+        const size_t act = act_need(hp, count, pl, m, (int)grid, o[0]);
+        if (act + ring_bytes(o[0], o[1]) <= optin) {
+            *cfg = Config{o[0], o[1], (int)grid, (int)act};
+            return true;
+        }
+    }
+    return false;
+}
+
+template <int M, bool SUB, bool XF32, int WARPS, int MAXP>
+cudaError_t launch(const HostProblem* hp, int count, const Plan& pl, const Config& cfg, cudaStream_t stream) {
+    LaneBatch<MAXP> B;
+    B.fault = fault_word();
+    if (!B.fault) return cudaErrorInvalidDevicePointer;
+    for (int i = 0; i < count; ++i) {
+        B.p[i] = LaneProblem{hp[i].w, hp[i].xq, hp[i].y, hp[i].sub, hp[i].n, hp[i].nb, pl.rps[i], pl.wbegin[i]};
+    }
+    B.count = count;
+    B.nstages = cfg.ns;
+    B.act_bytes = cfg.act_bytes;
+    B.wtotal = (int)pl.wtotal;
+    const size_t smem = (size_t)cfg.act_bytes + ring_bytes(WARPS, cfg.ns);
+    const void* fn = (const void*)lane_kernel<M, SUB, XF32, WARPS, MAXP>;
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    lane_kernel<M, SUB, XF32, WARPS, MAXP><<<(unsigned)cfg.grid, WARPS * 32, smem, stream>>>(B);
+    return cudaGetLastError();
+}
+
+// Launches one pass of M activation rows; false in *fits when no ring and
+// staging layout fits in shared memory (the caller then splits the work).
+template <int M, bool SUB, bool XF32>
+cudaError_t launch_m(const HostProblem* hp, int count, cudaStream_t stream, bool* fits) {
+    Plan pl;
+    make_plan(hp, count, 16, &pl);
+    *fits = false;
+    if (pl.wtotal >= (1LL << 31)) return cudaSuccess;
+    Config cfg;
+    if (!pick_config(hp, count, pl, M, &cfg)) return cudaSuccess;
+    *fits = true;
+    if (cfg.warps == 16) {
+        if (count == 1) return launch<M, SUB, XF32, 16, 1>(hp, count, pl, cfg, stream);
+        if constexpr (!SUB) return launch<M, SUB, XF32, 16, GROUP_MAX>(hp, count, pl, cfg, stream);
+    } else {
+        if (count == 1) return launch<M, SUB, XF32, 12, 1>(hp, count, pl, cfg, stream);
+        if constexpr (!SUB) return launch<M, SUB, XF32, 12, GROUP_MAX>(hp, count, pl, cfg, stream);
+    }
+    return cudaErrorInvalidValue;
+}
+
+template <bool SUB, bool XF32>
+cudaError_t dispatch(int m, const HostProblem* hp, int count, cudaStream_t stream, bool* fits) {
+    switch (m) {
+        case 1: return launch_m<1, SUB, XF32>(hp, count, stream, fits);
+        case 2: return launch_m<2, SUB, XF32>(hp, count, stream, fits);
+        case 3: return launch_m<3, SUB, XF32>(hp, count, stream, fits);
+        case 4: return launch_m<4, SUB, XF32>(hp, count, stream, fits);
+        case 5: return launch_m<5, SUB, XF32>(hp, count, stream, fits);
+        case 6: return launch_m<6, SUB, XF32>(hp, count, stream, fits);
+        case 7: return launch_m<7, SUB, XF32>(hp, count, stream, fits);
+        case 8: return launch_m<8, SUB, XF32>(hp, count, stream, fits);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+// Runs problems [0, count) with activation rows [i0, i0 + mm): as one launch
+// when it fits, else the problems in two halves; a single problem that does
+// not fit is taken in smaller row passes.  The f32 order of an output row
+// depends only on nb, so none of these splits changes a bit.
+template <bool XF32>
+cudaError_t run_part(const HostProblem* probs, int count, int i0, int mm, bool subdots, cudaStream_t stream) {
+    HostProblem part[GROUP_MAX];
+    for (int j = 0; j < count; ++j) {
+        const HostProblem& s = probs[j];
+        part[j] = s;
+        // activation row i0: q8_K blocks, or f32 values when XF32
+        part[j].xq = s.xq + (size_t)i0 * s.nb * (XF32 ? QK * sizeof(float) : Q8K_BYTES);
+        part[j].y = s.y ? s.y + (size_t)i0 * s.n : nullptr;
+        part[j].sub = s.sub ? s.sub + (size_t)i0 * s.n * s.nb * 8 : nullptr;
+    }
+    bool fits = false;
+    cudaError_t e;
+    if constexpr (XF32)
+        e = dispatch<false, true>(mm, part, count, stream, &fits);
+    else
+        e = subdots ? dispatch<true, false>(mm, part, count, stream, &fits)
+                    : dispatch<false, false>(mm, part, count, stream, &fits);
+    if (e != cudaSuccess || fits) return e;
+    if (count > 1) {
+        const int h = count / 2;
+        e = run_part<XF32>(probs, h, i0, mm, subdots, stream);
+        if (e != cudaSuccess) return e;
+        return run_part<XF32>(probs + h, count - h, i0, mm, subdots, stream);
+    }
+    if (mm == 1) return cudaErrorInvalidConfiguration;
+    const int h = mm / 2;
+    e = run_part<XF32>(probs, 1, i0, h, subdots, stream);
+    if (e != cudaSuccess) return e;
+    return run_part<XF32>(probs, 1, i0 + h, mm - h, subdots, stream);
+}
+
+template <bool XF32>
+cudaError_t run_group(const HostProblem* probs, int count, int m, bool subdots, cudaStream_t stream) {
+    for (int p0 = 0; p0 < count; p0 += GROUP_MAX) {
+        const int cnt = count - p0 < GROUP_MAX ? count - p0 : GROUP_MAX;
+        const cudaError_t e = run_part<XF32>(probs + p0, cnt, 0, m, subdots, stream);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace q4lane
+}  // namespace plm

@@ -244,6 +244,50 @@ __device__ __forceinline__ uint2 lds8_align2(const uint8_t* base, int off) {
     return r;
 }
 
+// q8_K quantization of one 256-value chunk by one warp; lane L holds values
+// 8L .. 8L+7 in v[].  Signed amax with the first occurrence winning (the
+// index is carried through the reduction), iscale = -128/max and
+// d = 1/iscale as IEEE f32 divisions, codes min(127, rne(iscale * x)) from a
+// single rounded multiply; an all-zero chunk gives d = 0 and zero codes.
+// Writes the lane's eight codes and returns d.
+__device__ __forceinline__ float q8K_quantize_warp(const float v[8], int lane, int q[8]) {
+    float amax = 0.0f;
+    int idx = 0x7FFFFFFF;
+    float mx = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float av = fabsf(v[i]);
+        if (av > amax) { amax = av; mx = v[i]; idx = 8 * lane + i; }
+    }
+    // larger magnitude wins; on equal magnitude the smaller index wins
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float oa = __shfl_xor_sync(0xFFFFFFFFu, amax, o);
+        const float om = __shfl_xor_sync(0xFFFFFFFFu, mx, o);
+        const int oi = __shfl_xor_sync(0xFFFFFFFFu, idx, o);
+        if (oa > amax || (oa == amax && oi < idx)) { amax = oa; mx = om; idx = oi; }
+    }
+    if (amax == 0.0f) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) q[i] = 0;
+        return 0.0f;
+    }
+    const float iscale = __fdiv_rn(-128.0f, mx);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) q[i] = min(127, __float2int_rn(__fmul_rn(iscale, v[i])));
+    return __fdiv_rn(1.0f, iscale);
+}
+
+__device__ __forceinline__ void pack_codes8(const int q[8], uint32_t& w0, uint32_t& w1) {
+    w0 = 0;
+    w1 = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        w0 |= (uint32_t)(q[i] & 0xFF) << (8 * i);
+        w1 |= (uint32_t)(q[4 + i] & 0xFF) << (8 * i);
+    }
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);

@@ -2,11 +2,8 @@
 // matmul, PocketLLM "Current status" table, row "src/": one 256-element
 // block per task).  One warp per 256-element chunk, 8 values per lane.
 //
-// Bit-exactness with the scalar rule rests on: the first-occurrence signed
-// amax (index carried through the reduction), IEEE f32 division for
-// iscale = -128/max and d = 1/iscale (__fdiv_rn), a single rounded f32
-// multiply iscale*x (__fmul_rn, so no contraction), and round-half-even to
-// integer (__float2int_rn).
+// The arithmetic is q8K_quantize_warp (plm_device.cuh), shared with the
+// fused quantize + GEMV so that both give the same codes bit for bit.
 #include "plm_device.cuh"
 #include "plm_internal.h"
 
@@ -23,44 +20,11 @@ __global__ void __launch_bounds__(256) quantize_q8K_kernel(const float* __restri
         const float4 a = __ldg(src), b = __ldg(src + 1);
         const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 
-        // lane-local first-occurrence amax
-        float amax = 0.0f;
-        int idx = 0x7FFFFFFF;
-        float mx = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float av = fabsf(v[i]);
-            if (av > amax) { amax = av; mx = v[i]; idx = 8 * lane + i; }
-        }
-        // warp reduction: larger magnitude wins; on equal magnitude the
-        // smaller index (the earlier element) wins
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float oa = __shfl_xor_sync(0xFFFFFFFFu, amax, o);
-            const float om = __shfl_xor_sync(0xFFFFFFFFu, mx, o);
-            const int oi = __shfl_xor_sync(0xFFFFFFFFu, idx, o);
-            if (oa > amax || (oa == amax && oi < idx)) { amax = oa; mx = om; idx = oi; }
-        }
-
         uint8_t* blk = xq + ch * Q8K_BYTES;
         int q[8];
-        float d;
-        if (amax == 0.0f) {
-            d = 0.0f;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) q[i] = 0;
-        } else {
-            const float iscale = __fdiv_rn(-128.0f, mx);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) q[i] = min(127, __float2int_rn(__fmul_rn(iscale, v[i])));
-            d = __fdiv_rn(1.0f, iscale);
-        }
-        uint32_t w0 = 0, w1 = 0;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            w0 |= (uint32_t)(q[i] & 0xFF) << (8 * i);
-            w1 |= (uint32_t)(q[4 + i] & 0xFF) << (8 * i);
-        }
+        const float d = q8K_quantize_warp(v, lane, q);
+        uint32_t w0, w1;
+        pack_codes8(q, w0, w1);
         uint32_t* qsw = reinterpret_cast<uint32_t*>(blk + 4) + 2 * lane;
         qsw[0] = w0;
         qsw[1] = w1;

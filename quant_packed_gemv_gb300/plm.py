@@ -38,6 +38,11 @@ class _Problem(ctypes.Structure):
                 ("n", ctypes.c_int64), ("k", ctypes.c_int64)]
 
 
+class _QProblem(ctypes.Structure):
+    _fields_ = [("w", ctypes.c_void_p), ("x", ctypes.c_void_p), ("y", ctypes.c_void_p),
+                ("n", ctypes.c_int64), ("k", ctypes.c_int64)]
+
+
 _lib = None
 
 
@@ -79,8 +84,10 @@ def load(build_if_missing=True):
         fn = getattr(lib, name)
         fn.argtypes = [ctypes.POINTER(_Problem), i64, i64, vp]
         fn.restype = ctypes.c_int
+    lib.plm_quantize_gemv_q4K_grouped.argtypes = [ctypes.POINTER(_QProblem), i64, i64, vp]
+    lib.plm_quantize_gemv_q4K_grouped.restype = ctypes.c_int
     for name in ("plm_gemv_q4K", "plm_gemv_q6K", "plm_gemm_q4K", "plm_gemm_q6K", "plm_gemm_q4K_noalloc",
-                 "plm_subdots_q4K", "plm_subdots_q6K"):
+                 "plm_subdots_q4K", "plm_subdots_q6K", "plm_quantize_gemv_q4K"):
         fn = getattr(lib, name)
         fn.argtypes = [vp, vp, vp, i64, i64, i64, vp]
         fn.restype = ctypes.c_int
@@ -156,6 +163,8 @@ plm_gemm_q6K = _mm("plm_gemm_q6K")
 # that must not allocate device memory while running (see include/plm.h).
 plm_gemm_q4K_noalloc = _mm("plm_gemm_q4K_noalloc")
 plm_subdots_q4K = _mm("plm_subdots_q4K")
+# fused q8_K producer: f32 activations x in place of xq
+plm_quantize_gemv_q4K = _mm("plm_quantize_gemv_q4K")
 plm_subdots_q6K = _mm("plm_subdots_q6K")
 
 
@@ -174,6 +183,15 @@ def _grouped(name):
 
 plm_gemv_q4K_grouped = _grouped("plm_gemv_q4K_grouped")
 plm_gemv_q6K_grouped = _grouped("plm_gemv_q6K_grouped")
+
+
+def plm_quantize_gemv_q4K_grouped(problems, m, stream=None):
+    """problems: sequence of (w, x_f32, y, n, k) with device tensors or addresses."""
+    lib = load()
+    arr = (_QProblem * len(problems))()
+    for j, (w, x, y, n, k) in enumerate(problems):
+        arr[j] = _QProblem(_addr(w), _addr(x), _addr(y), n, k)
+    _check("plm_quantize_gemv_q4K_grouped", lib.plm_quantize_gemv_q4K_grouped(arr, len(problems), m, _stream(stream)))
 
 
 def plm_gemm_workspace_size(fmt, m, k):

@@ -41,7 +41,7 @@ A = 1 << 20  # a 16-byte aligned fake address; never dereferenced: every call be
 
 
 @pytest.mark.parametrize("name", ["plm_gemv_q4K", "plm_gemv_q6K", "plm_gemm_q4K", "plm_gemm_q6K",
-                                  "plm_subdots_q4K", "plm_subdots_q6K"])
+                                  "plm_subdots_q4K", "plm_subdots_q6K", "plm_quantize_gemv_q4K"])
 def test_matmul_argument_checks(name):
     st = lambda *a: P.raw_status(name, *a)  # noqa: E731
     bad = P.PLM_ERR_INVALID_ARG
@@ -59,6 +59,8 @@ def test_matmul_argument_checks(name):
     assert st(A, A, A + 1, 1, 8, 256, None) == P.PLM_ERR_MISALIGNED
     if "gemm" not in name:
         assert st(A, A, A, 9, 8, 256, None) == bad
+    if name == "plm_quantize_gemv_q4K":   # f32 activations: 16-byte aligned
+        assert st(A, A + 4, A, 1, 8, 256, None) == P.PLM_ERR_MISALIGNED
 
 
 def test_quantize_argument_checks():
@@ -89,3 +91,17 @@ def test_grouped_argument_checks():
     assert lib.plm_gemv_q4K_grouped(arr, 0, 1, None) == P.PLM_ERR_INVALID_ARG
     assert lib.plm_gemv_q4K_grouped(arr, 1, 9, None) == P.PLM_ERR_INVALID_ARG
     assert lib.plm_gemv_q4K_grouped(None, 1, 1, None) == P.PLM_ERR_INVALID_ARG
+
+
+def test_fused_grouped_argument_checks():
+    lib = q.load()
+    arr = (P._QProblem * 2)()
+    arr[0] = P._QProblem(A, A, A, 8, 256)
+    arr[1] = P._QProblem(A, A, A, 8, 300)          # bad k in the second problem
+    assert lib.plm_quantize_gemv_q4K_grouped(arr, 2, 1, None) == P.PLM_ERR_INVALID_ARG
+    arr[1] = P._QProblem(A, A + 8, A, 8, 256)      # x not 16-byte aligned
+    assert lib.plm_quantize_gemv_q4K_grouped(arr, 2, 1, None) == P.PLM_ERR_MISALIGNED
+    arr[1] = P._QProblem(A, A, A, 8, 256)
+    assert lib.plm_quantize_gemv_q4K_grouped(arr, 0, 1, None) == P.PLM_ERR_INVALID_ARG
+    assert lib.plm_quantize_gemv_q4K_grouped(arr, 2, 9, None) == P.PLM_ERR_INVALID_ARG
+    assert lib.plm_quantize_gemv_q4K_grouped(None, 1, 1, None) == P.PLM_ERR_INVALID_ARG
