@@ -257,10 +257,15 @@ def time_case(args):
             for i in range(max(args.warmup, 3)):
                 fn(ws[i % copies], xq, y, m, n, k, stream=stream)
             torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(args.steps):
+                    fn(ws[i % copies], xq, y, m, n, k, stream=stream)
+            g.replay()
+            torch.cuda.synchronize()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            for i in range(args.steps):
-                fn(ws[i % copies], xq, y, m, n, k, stream=stream)
+            g.replay()
             e1.record(stream)
             torch.cuda.synchronize()
         us = e0.elapsed_time(e1) * 1e3 / args.steps
@@ -327,10 +332,17 @@ class ShapeTimer:
             for i in range(warmup):
                 call(i)
             torch.cuda.synchronize()
+            # the timed calls replay from a CUDA graph, so host-side launch cost
+            # does not gap the device timeline
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                for i in range(steps):
+                    call(i)
+            g.replay()
+            torch.cuda.synchronize()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(s)
-            for i in range(steps):
-                call(i)
+            g.replay()
             e1.record(s)
             torch.cuda.synchronize()
         us = e0.elapsed_time(e1) * 1e3 / steps
