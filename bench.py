@@ -425,6 +425,21 @@ class Step:
         return [(wp + off, xp + 4 * self.xoff[i], yp + 4 * self.yoff[i], n, k)
                 for i, (_, _, n, k, off) in enumerate(self.mats)]
 
+    def gate_up(self, copy):
+        """The 28 ffn gate/up pairs (3072x1024 each) on the gate's activations:
+        as SwiGLU pairs, and as the same 56 matrices for plain grouped GEMVs."""
+        wp, qp, yp = self.w[copy].data_ptr(), self.xq.data_ptr(), self.y.data_ptr()
+        pairs, plain = [], []
+        for layer in range(N_LAYERS):
+            ig, iu = layer * 7 + 4, layer * 7 + 5
+            _, _, n, k, og = self.mats[ig]
+            ou = self.mats[iu][4]
+            xq = qp + self.qoff[ig]
+            pairs.append((wp + og, wp + ou, xq, yp + 4 * self.yoff[ig], n, k))
+            plain.append((wp + og, xq, yp + 4 * self.yoff[ig], n, k))
+            plain.append((wp + ou, xq, yp + 4 * self.yoff[iu], n, k))
+        return pairs, plain
+
     def run_fused(self, q, copy, stream):
         """One launch: each CTA quantizes its activations and runs the GEMV."""
         q.plm_quantize_gemv_q4K_grouped(self.fused[copy], 1, stream=stream)
@@ -486,7 +501,19 @@ def main():
                 st.run_chain(q, i % 2, stream)
     torch.cuda.synchronize()
     graphs, gemv_graphs, chain_graphs, fused_graphs = [], [], [], []
+    swiglu_graphs, gateup_graphs = [], []
     for c in range(2):
+        pairs, plain = st.gate_up(c)
+        with torch.cuda.stream(stream):
+            q.plm_gemv_q4K_swiglu_grouped(pairs, 1, stream=stream)
+            q.plm_gemv_q4K_grouped(plain, 1, stream=stream)
+        torch.cuda.synchronize()
+        for lst, fn, arg in ((swiglu_graphs, q.plm_gemv_q4K_swiglu_grouped, pairs),
+                             (gateup_graphs, q.plm_gemv_q4K_grouped, plain)):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                fn(arg, 1, stream=stream)
+            lst.append(g)
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             st.run_fused(q, c, stream)
@@ -545,6 +572,8 @@ def main():
         ms = timed(lambda s: graphs[s % 2].replay(), args.steps)
         gemv_ms = timed(lambda s: gemv_graphs[s % 2].replay(), args.steps)
         fused_ms = timed(lambda s: fused_graphs[s % 2].replay(), args.steps)
+        swiglu_ms = timed(lambda s: swiglu_graphs[s % 2].replay(), args.steps)
+        gateup_ms = timed(lambda s: gateup_graphs[s % 2].replay(), args.steps)
         chain_ms = timed(lambda s: chain_graphs[s % 2].replay(), args.steps) if chain_graphs else None
         t0 = time.perf_counter()
         e2e_ms = timed(e2e_step, args.steps)
@@ -568,6 +597,8 @@ def main():
     peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
     e2e_ms_step = max(e2e_ms, e2e_wall) / args.steps
     chain_step = chain_ms / args.steps if chain_ms is not None else None
+    swiglu_bytes = sum(2 * n * (k // QK) * Q4K_BYTES + (k // QK) * Q8K_BYTES + 4 * n
+                       for (_, j, n, k, _) in mats if j == 4)
     # fused step: weights, f32 activations read once, y written once
     fused_bytes = sum(n * (k // QK) * Q4K_BYTES + 4 * k + 4 * n for _, _, n, k, _ in mats)
     chain_bytes = sum(gemv_bytes(sum(mats[l * 7 + f + j][2] for j in range(c)), mats[l * 7 + f][3])
@@ -599,6 +630,12 @@ def main():
             "ms_per_step": fused_ms / args.steps, "launches_per_step": launches_grouped,
             "what": "plm_quantize_gemv_q4K_grouped: the same step as one launch, q8_K produced in-kernel",
             "bytes_per_step": fused_bytes},
+        "swiglu_gate_up": {
+            "value": world * swiglu_bytes / (swiglu_ms / args.steps * 1e-3) / 1e9, "unit": "GB/s",
+            "us_per_launch": swiglu_ms / args.steps * 1e3,
+            "two_matrix_grouped_gemv_us": gateup_ms / args.steps * 1e3,
+            "what": "28 q4_K gate/up pairs (3072x1024), m=1: plm_gemv_q4K_swiglu_grouped writes "
+                    "h = silu(g)*u; compared with one grouped GEMV over the same 56 matrices"},
         "e2e": {"value": world * alg / (e2e_ms_step * 1e-3) / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms_step},
         "clocks": clocks,

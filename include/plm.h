@@ -177,6 +177,34 @@ plm_status plm_quantize_gemv_q4K_grouped(const plm_qgemv_problem* problems, int6
                                          cudaStream_t stream);
 
 /*
+ * Gate/up pair with the SwiGLU epilogue (q4_K), 1 <= m <= 8:
+ *   h[i][r] = silu(g[i][r]) * u[i][r],  g = W_gate . x_i,  u = W_up . x_i,
+ *   silu(g) = g / (1 + exp(-g)).
+ * PocketLLM (Korean README), "Current status" table, row "src/": the decode
+ * path's silu_mul step after the ffn gate and up projections.  Both weight
+ * matrices stream in one launch; g and u are the same f32 values
+ * plm_gemv_q4K produces for each matrix (same order), combined in f32 with
+ * IEEE division and expf, so only the epilogue's rounding separates h from
+ * silu applied to plm_gemv_q4K's outputs.
+ *   w_gate, w_up  q4_K [n][k/256] each, 16-byte aligned; xq q8_K [m][k/256];
+ *   h f32 [m][n].  Errors as for plm_gemv_q4K.
+ */
+plm_status plm_gemv_q4K_swiglu(const void* w_gate, const void* w_up, const void* xq, float* h, int64_t m,
+                               int64_t n, int64_t k, cudaStream_t stream);
+
+typedef struct {
+    const void* w_gate;   /* q4_K [n][k/256] */
+    const void* w_up;     /* q4_K [n][k/256] */
+    const void* xq;       /* q8_K [m][k/256] */
+    float* h;             /* f32 [m][n] */
+    int64_t n;
+    int64_t k;
+} plm_swiglu_problem;
+
+plm_status plm_gemv_q4K_swiglu_grouped(const plm_swiglu_problem* problems, int64_t count, int64_t m,
+                                       cudaStream_t stream);
+
+/*
  * Prefill GEMM, y = X . W^T for any m >= 1 (intended for m = 512..2048).
  * For m >= 9 the activation codes are first widened to an f16 matrix in a
  * workspace; weight tiles are decoded in shared memory into exact

@@ -70,6 +70,8 @@ def _load():
         lib.plm_ref_q4K_scale_min.argtypes = [vp, ctypes.c_int, ctypes.POINTER(ctypes.c_int),
                                               ctypes.POINTER(ctypes.c_int)]
         lib.plm_ref_q4K_scale_min.restype = None
+        lib.plm_ref_swiglu_f64.argtypes = [vp, vp, vp, i64]
+        lib.plm_ref_swiglu_f64.restype = None
         lib.plm_ref_set_threads.argtypes = [ctypes.c_int]
         lib.plm_ref_set_threads.restype = None
         lib.plm_ref_max_threads.argtypes = []
@@ -153,6 +155,21 @@ def gemm_q6K_f64(w, xq, m, n, k):
 
 def gemm_q6K_f32(w, xq, m, n, k):
     return _call6("plm_ref_gemm_q6K_f32", w, xq, m, n, k, (m, n), np.float32)
+
+
+def swiglu_f64(g, u):
+    """h = silu(g) * u elementwise in f64 (the gate/up pair's epilogue)."""
+    g = np.ascontiguousarray(g, dtype=np.float64)
+    u = np.ascontiguousarray(u, dtype=np.float64)
+    assert g.shape == u.shape
+    h = np.empty_like(g)
+    _load().plm_ref_swiglu_f64(_p(g), _p(u), _p(h), g.size)
+    return h
+
+
+def swiglu_q4K_f64(w_gate, w_up, xq, m, n, k):
+    """h = silu(W_gate . x) * (W_up . x) in f64 on the oracle's integer path."""
+    return swiglu_f64(gemm_q4K_f64(w_gate, xq, m, n, k), gemm_q4K_f64(w_up, xq, m, n, k))
 
 
 def absscale_q4K(w, xq, m, n, k):

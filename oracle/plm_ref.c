@@ -425,3 +425,13 @@ int plm_ref_max_threads(void) {
 void plm_ref_f16_array(const uint16_t* h, float* out, int64_t count) {
     for (int64_t i = 0; i < count; ++i) out[i] = plm_ref_f16_to_f32(h[i]);
 }
+
+/*
+ * SwiGLU epilogue of an ffn gate/up pair (PocketLLM, Korean README,
+ * "Current status" table, row "src/": the decode path's silu_mul step):
+ *   h = silu(g) * u,  silu(g) = g * sigmoid(g) = g / (1 + exp(-g)),
+ * in f64, elementwise over count values.
+ */
+void plm_ref_swiglu_f64(const double* g, const double* u, double* h, int64_t count) {
+    for (int64_t i = 0; i < count; ++i) h[i] = g[i] / (1.0 + exp(-g[i])) * u[i];
+}

@@ -4,5 +4,6 @@ from .plm import (  # noqa: F401
     PlmError, load, library_path, plm_abi_version, plm_device_fault, plm_probe_mma_rates, plm_quantize_q8K,
     plm_gemv_q4K, plm_gemv_q6K, plm_gemv_q4K_grouped, plm_gemv_q6K_grouped, plm_gemm_q4K, plm_gemm_q6K, plm_gemm_q4K_noalloc, plm_gemm_q4K_ws, plm_gemm_q6K_ws, plm_gemm_workspace_size,
     plm_subdots_q4K, plm_subdots_q6K, plm_quantize_gemv_q4K, plm_quantize_gemv_q4K_grouped,
+    plm_gemv_q4K_swiglu, plm_gemv_q4K_swiglu_grouped,
     QK, Q4K_BYTES, Q6K_BYTES, Q8K_BYTES, GEMV_MAX_M,
 )

@@ -121,6 +121,34 @@ plm_status qgemv_common(const plm_qgemv_problem* problems, int64_t count, int64_
     return PLM_OK;
 }
 
+// Gate/up pairs: both matrices checked like a GEMV's weights.
+plm_status swiglu_common(const plm_swiglu_problem* problems, int64_t count, int64_t m, cudaStream_t stream) {
+    if (!problems || count <= 0 || count > kMaxIndex) return PLM_ERR_INVALID_ARG;
+    if (m <= 0 || m > plm::GEMV_MAX_M) return PLM_ERR_INVALID_ARG;
+    for (int64_t j = 0; j < count; ++j) {
+        const plm_swiglu_problem& p = problems[j];
+        plm_status s = check_matmul(p.w_gate, p.xq, p.h, m, p.n, p.k, plm::GEMV_MAX_M);
+        if (s != PLM_OK) return s;
+        s = check_matmul(p.w_up, p.xq, p.h, m, p.n, p.k, plm::GEMV_MAX_M);
+        if (s != PLM_OK) return s;
+    }
+    for (int64_t j = 0; j < count; ++j)
+        if (!plm::gemv_supported(4, (int)problems[j].k)) return PLM_ERR_UNSUPPORTED;
+    constexpr int kChunk = 256;
+    plm::GroupItem items[kChunk];
+    for (int64_t p0 = 0; p0 < count; p0 += kChunk) {
+        const int cnt = (int)(count - p0 < kChunk ? count - p0 : kChunk);
+        for (int j = 0; j < cnt; ++j) {
+            const plm_swiglu_problem& p = problems[p0 + j];
+            items[j] = plm::GroupItem{(const uint8_t*)p.w_gate, (const uint8_t*)p.xq, p.h, (int)p.n, (int)p.k,
+                                      (const uint8_t*)p.w_up};
+        }
+        plm_status s = cuda_status(plm::launch_gemv_q4K_swiglu(items, cnt, (int)m, stream));
+        if (s != PLM_OK) return s;
+    }
+    return PLM_OK;
+}
+
 plm_status gemm_common(int fmt, const void* w, const void* xq, float* y, int64_t m, int64_t n,
                        int64_t k, cudaStream_t stream) {
     plm_status s = check_matmul(w, xq, y, m, n, k, kMaxIndex);
@@ -259,6 +287,17 @@ plm_status plm_quantize_gemv_q4K(const void* w, const float* x, float* y, int64_
 plm_status plm_quantize_gemv_q4K_grouped(const plm_qgemv_problem* problems, int64_t count, int64_t m,
                                          cudaStream_t stream) {
     return qgemv_common(problems, count, m, stream);
+}
+
+plm_status plm_gemv_q4K_swiglu(const void* w_gate, const void* w_up, const void* xq, float* h, int64_t m,
+                               int64_t n, int64_t k, cudaStream_t stream) {
+    const plm_swiglu_problem p{w_gate, w_up, xq, h, n, k};
+    return swiglu_common(&p, 1, m, stream);
+}
+
+plm_status plm_gemv_q4K_swiglu_grouped(const plm_swiglu_problem* problems, int64_t count, int64_t m,
+                                       cudaStream_t stream) {
+    return swiglu_common(problems, count, m, stream);
 }
 
 plm_status plm_subdots_q4K(const void* w, const void* xq, int32_t* out, int64_t m, int64_t n,

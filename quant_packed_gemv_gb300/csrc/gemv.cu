@@ -6,6 +6,7 @@ namespace plm {
 
 cudaError_t run_group_q4K(const HostProblem* p, int count, int m, bool subdots, cudaStream_t stream);
 cudaError_t run_group_q4K_f32(const HostProblem* p, int count, int m, cudaStream_t stream);
+cudaError_t run_group_q4K_swiglu(const HostProblem* p, int count, int m, cudaStream_t stream);
 cudaError_t run_group_q6K(const HostProblem* p, int count, int m, bool subdots, cudaStream_t stream);
 bool gemv_supported_q4K(int k);
 bool gemv_supported_q6K(int k);
@@ -37,6 +38,20 @@ cudaError_t launch_gemv_grouped(int fmt, const GroupItem* items, int count, int 
             part[j] = HostProblem{g.w, g.xq, g.y, nullptr, g.n, g.k / QK};
         }
         const cudaError_t e = run_fmt(fmt, part, cnt, m, false, stream);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+cudaError_t launch_gemv_q4K_swiglu(const GroupItem* items, int count, int m, cudaStream_t stream) {
+    HostProblem part[GROUP_MAX];
+    for (int p0 = 0; p0 < count; p0 += GROUP_MAX) {
+        const int cnt = count - p0 < GROUP_MAX ? count - p0 : GROUP_MAX;
+        for (int j = 0; j < cnt; ++j) {
+            const GroupItem& g = items[p0 + j];
+            part[j] = HostProblem{g.w, g.xq, g.y, nullptr, g.n, g.k / QK, g.w2};
+        }
+        const cudaError_t e = run_group_q4K_swiglu(part, cnt, m, stream);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;

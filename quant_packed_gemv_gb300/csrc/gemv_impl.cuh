@@ -579,6 +579,7 @@ struct HostProblem {
     float* y;
     int32_t* sub;
     int n, nb;
+    const uint8_t* w2 = nullptr;   // paired q4_K launches: the up matrix
 };
 
 template <int FMT, int M, bool SUB, int WARPS, int MAXP, bool AREG>

@@ -4,7 +4,7 @@
 namespace plm {
 
 cudaError_t run_group_q4K(const HostProblem* probs, int count, int m, bool subdots, cudaStream_t stream) {
-    return q4lane::run_group<false>(probs, count, m, subdots, stream);
+    return q4lane::run_group<false, false>(probs, count, m, subdots, stream);
 }
 
 // One activation row of the widest row must fit beside the smallest ring.

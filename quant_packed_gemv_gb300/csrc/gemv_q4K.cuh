@@ -61,6 +61,7 @@ struct LaneProblem {
     int n, nb;
     int rps;                // rows per unit (0: one row per unit, several stages)
     int wbegin;             // weighted units before this problem
+    const uint8_t* w2;      // paired launches: the up matrix (w is the gate matrix)
 };
 
 template <int MAXP>
@@ -75,6 +76,8 @@ struct LaneBatch {
 
 __host__ __device__ __forceinline__ int unit_weight(int nb) { return nb <= STAGE_BLOCKS ? 1 : (nb + STAGE_BLOCKS - 1) / STAGE_BLOCKS; }
 __host__ __device__ __forceinline__ int unit_count(int n, int rps) { return rps > 0 ? (n + rps - 1) / rps : n; }
+// Stages of one unit: a paired launch streams the gate rows, then the same up rows.
+__host__ __device__ __forceinline__ int unit_stages(int nb, int pairf) { return unit_weight(nb) * pairf; }
 
 // A warp's position in its unit range: problem p, unit u of [u, uend), chunk ch
 // of the unit's row (one-row units only).  p < 0: the range is exhausted.
@@ -84,10 +87,10 @@ struct Cursor {
 
 // Moves to the first problem at or after p that has a unit starting in [W0, W1).
 template <int MAXP>
-__device__ __forceinline__ void cursor_enter(const LaneBatch<MAXP>& B, Cursor& c, int p, int W0, int W1) {
+__device__ __forceinline__ void cursor_enter(const LaneBatch<MAXP>& B, Cursor& c, int p, int W0, int W1, int pairf) {
     for (; p < B.count && B.p[p].wbegin < W1; ++p) {
         const LaneProblem& P = B.p[p];
-        const int wt = unit_weight(P.nb);
+        const int wt = unit_stages(P.nb, pairf);
         const int a = W0 - P.wbegin, b = W1 - P.wbegin;
         const int u0 = a > 0 ? (a + wt - 1) / wt : 0;
         const int u1 = min(unit_count(P.n, P.rps), (b + wt - 1) / wt);
@@ -100,11 +103,16 @@ __device__ __forceinline__ void cursor_enter(const LaneBatch<MAXP>& B, Cursor& c
 }
 
 template <int MAXP>
-__device__ __forceinline__ void cursor_next(const LaneBatch<MAXP>& B, Cursor& c, int nb, int W0, int W1) {
-    if (nb > STAGE_BLOCKS && ++c.ch < unit_weight(nb)) return;
+__device__ __forceinline__ void cursor_next(const LaneBatch<MAXP>& B, Cursor& c, int nb, int W0, int W1, int pairf) {
+    if (++c.ch < unit_stages(nb, pairf)) return;
     c.ch = 0;
     if (++c.u < c.uend) return;
-    cursor_enter(B, c, c.p + 1, W0, W1);
+    cursor_enter(B, c, c.p + 1, W0, W1, pairf);
+}
+
+// SwiGLU epilogue of a paired launch: silu(g) * u = g / (1 + e^-g) * u.
+__device__ __forceinline__ float swiglu(float g, float u) {
+    return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
 }
 
 // Last problem whose weighted range starts at or before W.
@@ -233,8 +241,9 @@ __device__ __forceinline__ void lane_block(const uint8_t* w, const uint8_t* act,
     }
 }
 
-template <int M, bool SUBDOTS, bool XF32, int WARPS, int MAXP>
+template <int M, bool SUBDOTS, bool XF32, bool PAIR, int WARPS, int MAXP>
 __global__ void __launch_bounds__(WARPS * 32, 1) lane_kernel(const __grid_constant__ LaneBatch<MAXP> B) {
+    constexpr int PF = PAIR ? 2 : 1;
     extern __shared__ __align__(128) uint8_t smem[];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -256,12 +265,15 @@ __global__ void __launch_bounds__(WARPS * 32, 1) lane_kernel(const __grid_consta
 
     // copy cursor: lane 0 issues; runs up to NS stages ahead, across problems
     Cursor ic;
-    cursor_enter(B, ic, problem_at(B, W0), W0, W1);
+    cursor_enter(B, ic, problem_at(B, W0), W0, W1, PF);
     uint32_t issued = 0, consumed = 0;           // ring counters, uniform in the warp
     uint32_t islot = 0, cslot = 0, cphase = 0;   // next slot to fill / to consume, its phase parity
     auto issue_one = [&]() {
         const LaneProblem& Q = B.p[ic.p];
         const int nb = Q.nb;
+        const int spr = unit_weight(nb);
+        const bool second = PAIR && ic.ch >= spr;   // paired: the up matrix's stages follow the gate's
+        const int ch = second ? ic.ch - spr : ic.ch;
         int blocks;
         long long first;   // first block of the stage
         if (nb <= STAGE_BLOCKS) {
@@ -269,7 +281,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1) lane_kernel(const __grid_consta
             blocks = min(Q.rps, Q.n - r0) * nb;
             first = (long long)r0 * nb;
         } else {
-            const int b0 = ic.ch * STAGE_BLOCKS;
+            const int b0 = ch * STAGE_BLOCKS;
             blocks = min(STAGE_BLOCKS, nb - b0);
             first = (long long)ic.u * nb + b0;
         }
@@ -277,11 +289,11 @@ __global__ void __launch_bounds__(WARPS * 32, 1) lane_kernel(const __grid_consta
             uint64_t* bar = &bars[islot];
             const uint32_t bytes = (uint32_t)blocks * Q4K_BYTES;   // q4_K rows: whole 16-byte multiples
             mbar_arrive_expect_tx(bar, bytes);
-            bulk_g2s(ring + islot * SLOT, Q.w + first * Q4K_BYTES, bytes, bar);
+            bulk_g2s(ring + islot * SLOT, (second ? Q.w2 : Q.w) + first * Q4K_BYTES, bytes, bar);
         }
         islot = islot + 1 == (uint32_t)NS ? 0 : islot + 1;
         ++issued;
-        cursor_next(B, ic, nb, W0, W1);
+        cursor_next(B, ic, nb, W0, W1, PF);
     };
     while (ic.p >= 0 && issued < (uint32_t)NS) issue_one();
 
@@ -302,7 +314,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1) lane_kernel(const __grid_consta
     __syncthreads();
 
     Cursor cc;
-    cursor_enter(B, cc, problem_at(B, W0), W0, W1);
+    cursor_enter(B, cc, problem_at(B, W0), W0, W1, PF);
     int act_p = cfirst, act_off = 0;   // staged offset of problem act_p
     bool ok = true;                    // false once a wait ran out
     while (cc.p >= 0 && ok) {
@@ -323,9 +335,9 @@ __global__ void __launch_bounds__(WARPS * 32, 1) lane_kernel(const __grid_consta
         const int rl = rps > 0 ? lane / nb : 0;   // row mode: row slot and column of this lane
         const int cl = rps > 0 ? lane - rl * nb : lane;
         const bool pow2 = (nb & (nb - 1)) == 0;
-        float acc[M];
+        float acc[M], gsum[M];   // gsum: paired launches, the gate row sums
 #pragma unroll
-        for (int i = 0; i < M; ++i) acc[i] = 0.0f;
+        for (int i = 0; i < M; ++i) acc[i] = gsum[i] = 0.0f;
 
         while (cc.p == p_now) {
             if (!mbar_wait(&bars[cslot], cphase)) {
@@ -370,13 +382,18 @@ __global__ void __launch_bounds__(WARPS * 32, 1) lane_kernel(const __grid_consta
                             }
                         }
                     }
-                    if (valid && cl == 0) {
+                    if (PAIR && cc.ch == 0) {
 #pragma unroll
-                        for (int i = 0; i < M; ++i) yv[(size_t)i * n + r0 + rl] = v[i];
+                        for (int i = 0; i < M; ++i) gsum[i] = v[i];
+                    } else if (valid && cl == 0) {
+#pragma unroll
+                        for (int i = 0; i < M; ++i) yv[(size_t)i * n + r0 + rl] = PAIR ? swiglu(gsum[i], v[i]) : v[i];
                     }
                 }
             } else {
-                const int b0 = cc.ch * STAGE_BLOCKS;
+                const int spr = unit_weight(nb);
+                const bool second = PAIR && cc.ch >= spr;
+                const int b0 = (second ? cc.ch - spr : cc.ch) * STAGE_BLOCKS;
                 const int nblk_s = min(STAGE_BLOCKS, nb - b0);
                 const bool valid = lane < nblk_s;
                 const int b = b0 + (valid ? lane : 0);
@@ -394,7 +411,10 @@ __global__ void __launch_bounds__(WARPS * 32, 1) lane_kernel(const __grid_consta
 #pragma unroll
                         for (int i = 0; i < M; ++i) {
                             const float x = warp_sum(acc[i]);
-                            if (lane == 0) yv[(size_t)i * n + cc.u] = x;
+                            if (PAIR && !second)
+                                gsum[i] = x;
+                            else if (lane == 0)
+                                yv[(size_t)i * n + cc.u] = PAIR ? swiglu(gsum[i], x) : x;
                             acc[i] = 0.0f;
                         }
                     }
@@ -407,7 +427,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1) lane_kernel(const __grid_consta
             }
             __syncwarp();
             if (ic.p >= 0) issue_one();
-            cursor_next(B, cc, nb, W0, W1);
+            cursor_next(B, cc, nb, W0, W1, PF);
         }
     }
 }
@@ -430,7 +450,7 @@ struct Plan {
 // Units per problem.  A launch too small to give every warp of the GPU two
 // units takes fewer rows per unit (down to one), so that its rows still
 // spread over all SMs; rows per unit do not change any row's arithmetic.
-inline void make_plan(const HostProblem* hp, int count, int warps, Plan* pl) {
+inline void make_plan(const HostProblem* hp, int count, int warps, int pairf, Plan* pl) {
     const long long target = 2LL * num_sms() * warps;
     for (int shrink = 1;; shrink *= 2) {
         long long w = 0;
@@ -441,7 +461,7 @@ inline void make_plan(const HostProblem* hp, int count, int warps, Plan* pl) {
             pl->rps[i] = full > 0 ? std::max(1, full / shrink) : 0;
             reducible = reducible || pl->rps[i] > 1;
             pl->wbegin[i] = (int)std::min(w, (long long)INT32_MAX);
-            w += (long long)unit_count(hp[i].n, pl->rps[i]) * unit_weight(nb);
+            w += (long long)unit_count(hp[i].n, pl->rps[i]) * unit_stages(nb, pairf);
         }
         pl->wtotal = w;
         if (w >= target || !reducible) return;
@@ -482,58 +502,59 @@ inline bool pick_config(const HostProblem* hp, int count, const Plan& pl, int m,
     return false;
 }
 
-template <int M, bool SUB, bool XF32, int WARPS, int MAXP>
+template <int M, bool SUB, bool XF32, bool PAIR, int WARPS, int MAXP>
 cudaError_t launch(const HostProblem* hp, int count, const Plan& pl, const Config& cfg, cudaStream_t stream) {
     LaneBatch<MAXP> B;
     B.fault = fault_word();
     if (!B.fault) return cudaErrorInvalidDevicePointer;
     for (int i = 0; i < count; ++i) {
-        B.p[i] = LaneProblem{hp[i].w, hp[i].xq, hp[i].y, hp[i].sub, hp[i].n, hp[i].nb, pl.rps[i], pl.wbegin[i]};
+        B.p[i] = LaneProblem{hp[i].w,  hp[i].xq, hp[i].y,      hp[i].sub, hp[i].n,
+                             hp[i].nb, pl.rps[i], pl.wbegin[i], hp[i].w2};
     }
     B.count = count;
     B.nstages = cfg.ns;
     B.act_bytes = cfg.act_bytes;
     B.wtotal = (int)pl.wtotal;
     const size_t smem = (size_t)cfg.act_bytes + ring_bytes(WARPS, cfg.ns);
-    const void* fn = (const void*)lane_kernel<M, SUB, XF32, WARPS, MAXP>;
+    const void* fn = (const void*)lane_kernel<M, SUB, XF32, PAIR, WARPS, MAXP>;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    lane_kernel<M, SUB, XF32, WARPS, MAXP><<<(unsigned)cfg.grid, WARPS * 32, smem, stream>>>(B);
+    lane_kernel<M, SUB, XF32, PAIR, WARPS, MAXP><<<(unsigned)cfg.grid, WARPS * 32, smem, stream>>>(B);
     return cudaGetLastError();
 }
 
 // Launches one pass of M activation rows; false in *fits when no ring and
 // staging layout fits in shared memory (the caller then splits the work).
-template <int M, bool SUB, bool XF32>
+template <int M, bool SUB, bool XF32, bool PAIR>
 cudaError_t launch_m(const HostProblem* hp, int count, cudaStream_t stream, bool* fits) {
     Plan pl;
-    make_plan(hp, count, 16, &pl);
+    make_plan(hp, count, 16, PAIR ? 2 : 1, &pl);
     *fits = false;
     if (pl.wtotal >= (1LL << 31)) return cudaSuccess;
     Config cfg;
     if (!pick_config(hp, count, pl, M, &cfg)) return cudaSuccess;
     *fits = true;
     if (cfg.warps == 16) {
-        if (count == 1) return launch<M, SUB, XF32, 16, 1>(hp, count, pl, cfg, stream);
-        if constexpr (!SUB) return launch<M, SUB, XF32, 16, GROUP_MAX>(hp, count, pl, cfg, stream);
+        if (count == 1) return launch<M, SUB, XF32, PAIR, 16, 1>(hp, count, pl, cfg, stream);
+        if constexpr (!SUB) return launch<M, SUB, XF32, PAIR, 16, GROUP_MAX>(hp, count, pl, cfg, stream);
     } else {
-        if (count == 1) return launch<M, SUB, XF32, 12, 1>(hp, count, pl, cfg, stream);
-        if constexpr (!SUB) return launch<M, SUB, XF32, 12, GROUP_MAX>(hp, count, pl, cfg, stream);
+        if (count == 1) return launch<M, SUB, XF32, PAIR, 12, 1>(hp, count, pl, cfg, stream);
+        if constexpr (!SUB) return launch<M, SUB, XF32, PAIR, 12, GROUP_MAX>(hp, count, pl, cfg, stream);
     }
     return cudaErrorInvalidValue;
 }
 
-template <bool SUB, bool XF32>
+template <bool SUB, bool XF32, bool PAIR>
 cudaError_t dispatch(int m, const HostProblem* hp, int count, cudaStream_t stream, bool* fits) {
     switch (m) {
-        case 1: return launch_m<1, SUB, XF32>(hp, count, stream, fits);
-        case 2: return launch_m<2, SUB, XF32>(hp, count, stream, fits);
-        case 3: return launch_m<3, SUB, XF32>(hp, count, stream, fits);
-        case 4: return launch_m<4, SUB, XF32>(hp, count, stream, fits);
-        case 5: return launch_m<5, SUB, XF32>(hp, count, stream, fits);
-        case 6: return launch_m<6, SUB, XF32>(hp, count, stream, fits);
-        case 7: return launch_m<7, SUB, XF32>(hp, count, stream, fits);
-        case 8: return launch_m<8, SUB, XF32>(hp, count, stream, fits);
+        case 1: return launch_m<1, SUB, XF32, PAIR>(hp, count, stream, fits);
+        case 2: return launch_m<2, SUB, XF32, PAIR>(hp, count, stream, fits);
+        case 3: return launch_m<3, SUB, XF32, PAIR>(hp, count, stream, fits);
+        case 4: return launch_m<4, SUB, XF32, PAIR>(hp, count, stream, fits);
+        case 5: return launch_m<5, SUB, XF32, PAIR>(hp, count, stream, fits);
+        case 6: return launch_m<6, SUB, XF32, PAIR>(hp, count, stream, fits);
+        case 7: return launch_m<7, SUB, XF32, PAIR>(hp, count, stream, fits);
+        case 8: return launch_m<8, SUB, XF32, PAIR>(hp, count, stream, fits);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -542,7 +563,7 @@ cudaError_t dispatch(int m, const HostProblem* hp, int count, cudaStream_t strea
 // when it fits, else the problems in two halves; a single problem that does
 // not fit is taken in smaller row passes.  The f32 order of an output row
 // depends only on nb, so none of these splits changes a bit.
-template <bool XF32>
+template <bool XF32, bool PAIR>
 cudaError_t run_part(const HostProblem* probs, int count, int i0, int mm, bool subdots, cudaStream_t stream) {
     HostProblem part[GROUP_MAX];
     for (int j = 0; j < count; ++j) {
@@ -555,30 +576,30 @@ cudaError_t run_part(const HostProblem* probs, int count, int i0, int mm, bool s
     }
     bool fits = false;
     cudaError_t e;
-    if constexpr (XF32)
-        e = dispatch<false, true>(mm, part, count, stream, &fits);
+    if constexpr (XF32 || PAIR)
+        e = dispatch<false, XF32, PAIR>(mm, part, count, stream, &fits);
     else
-        e = subdots ? dispatch<true, false>(mm, part, count, stream, &fits)
-                    : dispatch<false, false>(mm, part, count, stream, &fits);
+        e = subdots ? dispatch<true, false, false>(mm, part, count, stream, &fits)
+                    : dispatch<false, false, false>(mm, part, count, stream, &fits);
     if (e != cudaSuccess || fits) return e;
     if (count > 1) {
         const int h = count / 2;
-        e = run_part<XF32>(probs, h, i0, mm, subdots, stream);
+        e = run_part<XF32, PAIR>(probs, h, i0, mm, subdots, stream);
         if (e != cudaSuccess) return e;
-        return run_part<XF32>(probs + h, count - h, i0, mm, subdots, stream);
+        return run_part<XF32, PAIR>(probs + h, count - h, i0, mm, subdots, stream);
     }
     if (mm == 1) return cudaErrorInvalidConfiguration;
     const int h = mm / 2;
-    e = run_part<XF32>(probs, 1, i0, h, subdots, stream);
+    e = run_part<XF32, PAIR>(probs, 1, i0, h, subdots, stream);
     if (e != cudaSuccess) return e;
-    return run_part<XF32>(probs, 1, i0 + h, mm - h, subdots, stream);
+    return run_part<XF32, PAIR>(probs, 1, i0 + h, mm - h, subdots, stream);
 }
 
-template <bool XF32>
+template <bool XF32, bool PAIR>
 cudaError_t run_group(const HostProblem* probs, int count, int m, bool subdots, cudaStream_t stream) {
     for (int p0 = 0; p0 < count; p0 += GROUP_MAX) {
         const int cnt = count - p0 < GROUP_MAX ? count - p0 : GROUP_MAX;
-        const cudaError_t e = run_part<XF32>(probs + p0, cnt, 0, m, subdots, stream);
+        const cudaError_t e = run_part<XF32, PAIR>(probs + p0, cnt, 0, m, subdots, stream);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;

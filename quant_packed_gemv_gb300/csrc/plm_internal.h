@@ -29,12 +29,16 @@ struct GroupItem {
     const uint8_t* xq;
     float* y;
     int n, k;
+    const uint8_t* w2 = nullptr;   // gate/up pairs: the up matrix
 };
 cudaError_t launch_gemv_grouped(int fmt, const GroupItem* items, int count, int m, cudaStream_t stream);
 
 // Fused quantize + q4_K GEMV on f32 activations (GroupItem::xq holds the
 // f32 activation pointer), one launch per 256 problems.
 cudaError_t launch_quantize_gemv_q4K(const GroupItem* items, int count, int m, cudaStream_t stream);
+
+// q4_K gate/up pairs with the SwiGLU epilogue (GroupItem::w = gate, w2 = up).
+cudaError_t launch_gemv_q4K_swiglu(const GroupItem* items, int count, int m, cudaStream_t stream);
 
 // Sub-block integer dots through the GEMV's lane decode (1 <= m <= 8).
 cudaError_t launch_subdots(int fmt, const uint8_t* w, const uint8_t* xq, int32_t* out,

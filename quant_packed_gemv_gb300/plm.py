@@ -38,6 +38,11 @@ class _Problem(ctypes.Structure):
                 ("n", ctypes.c_int64), ("k", ctypes.c_int64)]
 
 
+class _SProblem(ctypes.Structure):
+    _fields_ = [("w_gate", ctypes.c_void_p), ("w_up", ctypes.c_void_p), ("xq", ctypes.c_void_p),
+                ("h", ctypes.c_void_p), ("n", ctypes.c_int64), ("k", ctypes.c_int64)]
+
+
 class _QProblem(ctypes.Structure):
     _fields_ = [("w", ctypes.c_void_p), ("x", ctypes.c_void_p), ("y", ctypes.c_void_p),
                 ("n", ctypes.c_int64), ("k", ctypes.c_int64)]
@@ -84,6 +89,10 @@ def load(build_if_missing=True):
         fn = getattr(lib, name)
         fn.argtypes = [ctypes.POINTER(_Problem), i64, i64, vp]
         fn.restype = ctypes.c_int
+    lib.plm_gemv_q4K_swiglu.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp]
+    lib.plm_gemv_q4K_swiglu.restype = ctypes.c_int
+    lib.plm_gemv_q4K_swiglu_grouped.argtypes = [ctypes.POINTER(_SProblem), i64, i64, vp]
+    lib.plm_gemv_q4K_swiglu_grouped.restype = ctypes.c_int
     lib.plm_quantize_gemv_q4K_grouped.argtypes = [ctypes.POINTER(_QProblem), i64, i64, vp]
     lib.plm_quantize_gemv_q4K_grouped.restype = ctypes.c_int
     for name in ("plm_gemv_q4K", "plm_gemv_q6K", "plm_gemm_q4K", "plm_gemm_q6K", "plm_gemm_q4K_noalloc",
@@ -183,6 +192,22 @@ def _grouped(name):
 
 plm_gemv_q4K_grouped = _grouped("plm_gemv_q4K_grouped")
 plm_gemv_q6K_grouped = _grouped("plm_gemv_q6K_grouped")
+
+
+def plm_gemv_q4K_swiglu(w_gate, w_up, xq, h, m, n, k, stream=None):
+    """h = silu(W_gate . x) * (W_up . x) (see include/plm.h)."""
+    lib = load()
+    _check("plm_gemv_q4K_swiglu", lib.plm_gemv_q4K_swiglu(_addr(w_gate), _addr(w_up), _addr(xq), _addr(h), m, n, k,
+                                                          _stream(stream)))
+
+
+def plm_gemv_q4K_swiglu_grouped(problems, m, stream=None):
+    """problems: sequence of (w_gate, w_up, xq, h, n, k) with device tensors or addresses."""
+    lib = load()
+    arr = (_SProblem * len(problems))()
+    for j, (wg, wu, xq, h, n, k) in enumerate(problems):
+        arr[j] = _SProblem(_addr(wg), _addr(wu), _addr(xq), _addr(h), n, k)
+    _check("plm_gemv_q4K_swiglu_grouped", lib.plm_gemv_q4K_swiglu_grouped(arr, len(problems), m, _stream(stream)))
 
 
 def plm_quantize_gemv_q4K_grouped(problems, m, stream=None):

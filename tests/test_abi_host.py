@@ -105,3 +105,23 @@ def test_fused_grouped_argument_checks():
     assert lib.plm_quantize_gemv_q4K_grouped(arr, 0, 1, None) == P.PLM_ERR_INVALID_ARG
     assert lib.plm_quantize_gemv_q4K_grouped(arr, 2, 9, None) == P.PLM_ERR_INVALID_ARG
     assert lib.plm_quantize_gemv_q4K_grouped(None, 1, 1, None) == P.PLM_ERR_INVALID_ARG
+
+
+def test_swiglu_argument_checks():
+    lib = q.load()
+    st = lambda *a: lib.plm_gemv_q4K_swiglu(*a)  # noqa: E731
+    bad = P.PLM_ERR_INVALID_ARG
+    assert st(None, A, A, A, 1, 8, 256, None) == bad
+    assert st(A, None, A, A, 1, 8, 256, None) == bad
+    assert st(A, A, None, A, 1, 8, 256, None) == bad
+    assert st(A, A, A, None, 1, 8, 256, None) == bad
+    assert st(A, A, A, A, 9, 8, 256, None) == bad
+    assert st(A, A, A, A, 1, 8, 300, None) == bad
+    assert st(A, A + 8, A, A, 1, 8, 256, None) == P.PLM_ERR_MISALIGNED
+    assert st(A + 8, A, A, A, 1, 8, 256, None) == P.PLM_ERR_MISALIGNED
+    arr = (P._SProblem * 2)()
+    arr[0] = P._SProblem(A, A, A, A, 8, 256)
+    arr[1] = P._SProblem(A, A + 4, A, A, 8, 256)   # misaligned up matrix in the second pair
+    assert lib.plm_gemv_q4K_swiglu_grouped(arr, 2, 1, None) == P.PLM_ERR_MISALIGNED
+    assert lib.plm_gemv_q4K_swiglu_grouped(arr, 0, 1, None) == bad
+    assert lib.plm_gemv_q4K_swiglu_grouped(None, 1, 1, None) == bad

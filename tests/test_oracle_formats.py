@@ -206,3 +206,20 @@ def test_generated_fields_have_stated_ranges():
     assert sc.min() == -64 and sc.max() == 63
     d6 = w6[:, 208:210].copy().view(np.float16).astype(np.float64)
     assert d6.min() >= 1e-4 * (1 - 1e-3) and d6.max() <= 2e-3 * (1 + 1e-3)
+
+
+def test_swiglu_epilogue_closed_forms():
+    """silu(g) * u against identities that do not restate the formula:
+    silu(0) = 0; silu(x) - silu(-x) = x; silu(ln 3) = (3/4) ln 3 (sigmoid(ln 3) = 3/4);
+    silu(x) -> x for large x and -> 0 for very negative x; u scales h linearly."""
+    x = np.linspace(-30.0, 30.0, 601)
+    one = np.ones_like(x)
+    h = oracle.swiglu_f64(x, one)
+    hm = oracle.swiglu_f64(-x, one)
+    np.testing.assert_allclose(h - hm, x, rtol=0, atol=1e-12)
+    assert oracle.swiglu_f64(np.array([0.0]), np.array([5.0]))[0] == 0.0
+    ln3 = np.log(3.0)
+    np.testing.assert_allclose(oracle.swiglu_f64(np.array([ln3]), np.array([1.0])), [0.75 * ln3], rtol=1e-15)
+    assert abs(oracle.swiglu_f64(np.array([40.0]), np.array([1.0]))[0] - 40.0) < 1e-12
+    assert abs(oracle.swiglu_f64(np.array([-40.0]), np.array([1.0]))[0]) < 1e-12
+    np.testing.assert_allclose(oracle.swiglu_f64(x, 3.0 * one), 3.0 * h, rtol=1e-15)
