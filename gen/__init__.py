@@ -18,6 +18,7 @@ _OUT_DIR = os.path.join(_HERE, "_build")
 _LIB = os.path.join(_OUT_DIR, "libplmgen.so")
 
 Q4K_BYTES = 144
+Q5K_BYTES = 176
 Q6K_BYTES = 210
 QK = 256
 
@@ -44,7 +45,7 @@ def _load():
     if _lib is None:
         lib = ctypes.CDLL(build())
         u64, i64, vp = ctypes.c_uint64, ctypes.c_int64, ctypes.c_void_p
-        for name in ("plmgen_q4K", "plmgen_q6K", "plmgen_normal_f32", "plmgen_raw"):
+        for name in ("plmgen_q4K", "plmgen_q5K", "plmgen_q6K", "plmgen_normal_f32", "plmgen_raw"):
             fn = getattr(lib, name)
             fn.argtypes = [u64, u64, i64, i64, vp]
             fn.restype = None
@@ -64,6 +65,17 @@ def q4K_blocks(seed, stream, n, k, row0=0, out=None):
         out = np.empty((n, nb * Q4K_BYTES), dtype=np.uint8)
     assert out.flags.c_contiguous and out.nbytes == n * nb * Q4K_BYTES
     _load().plmgen_q4K(seed, stream, row0 * nb, n * nb, _ptr(out))
+    return out
+
+
+def q5K_blocks(seed, stream, n, k, row0=0, out=None):
+    """Rows [row0, row0+n) of a q5_K matrix as uint8 [n, k/256*176]."""
+    assert k % QK == 0
+    nb = k // QK
+    if out is None:
+        out = np.empty((n, nb * Q5K_BYTES), dtype=np.uint8)
+    assert out.flags.c_contiguous and out.nbytes == n * nb * Q5K_BYTES
+    _load().plmgen_q5K(seed, stream, row0 * nb, n * nb, _ptr(out))
     return out
 
 

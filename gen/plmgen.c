@@ -9,6 +9,8 @@
  *          eight 6-bit (scale, min) pairs and the packing is a bijection on
  *          96 bits, so uniform bytes give scales and mins i.i.d. U{0..63};
  *          likewise uniform qs bytes give nibbles i.i.d. U{0..15}.
+ *   q5_K : as q4_K, plus 32 uniform qh bytes (the fifth bit of each weight),
+ *          so q5 ~ U{0..31}.
  *   q6_K : d ~ U(1e-4, 2e-3) rounded to f16; ql[128] and qh[64] uniform bytes
  *          (a bijection onto 256 six-bit values, so q6 ~ U{0..63});
  *          scales i8 ~ U{-64..63}.
@@ -25,6 +27,8 @@
  *   q4_K: 20 draws from 20*b.  draw 0 -> d, draw 1 -> dmin, draws 2..19 give
  *         8 bytes each (little-endian) for scales[12] then qs[128]
  *         (140 bytes used, 4 dropped).
+ *   q5_K: 24 draws from 24*b.  draw 0 -> d, draw 1 -> dmin, draws 2..23 give
+ *         8 bytes each for scales[12], qh[32] then qs[128] (172 bytes used).
  *   q6_K: 27 draws from 27*b.  draw 0 -> d, draws 1..24 give ql[128] then
  *         qh[64], draws 25..26 give 16 bytes b, scale = (b & 127) - 64.
  *   x   : element e takes draws 2e (u1) and 2e+1 (u2).
@@ -90,6 +94,17 @@ void plmgen_q4K(uint64_t seed, uint64_t stream, int64_t block0, int64_t nblocks,
         put_u16(blk + 2, draw_scale_half(draw(s, base + 1)));
         bytes_from_draws(s, base + 2, raw, 140);
         memcpy(blk + 4, raw, 140);
+    }
+}
+
+void plmgen_q5K(uint64_t seed, uint64_t stream, int64_t block0, int64_t nblocks, uint8_t* out) {
+    uint64_t s = stream_start(seed, stream);
+    for (int64_t b = 0; b < nblocks; ++b) {
+        uint64_t base = (uint64_t)(block0 + b) * 24u;
+        uint8_t* blk = out + b * 176;
+        put_u16(blk + 0, draw_scale_half(draw(s, base + 0)));
+        put_u16(blk + 2, draw_scale_half(draw(s, base + 1)));
+        bytes_from_draws(s, base + 2, blk + 4, 172);
     }
 }
 

@@ -26,6 +26,7 @@ _LIB = os.path.join(_OUT_DIR, "libplmref.so")
 
 QK = 256
 Q4K_BYTES = 144
+Q5K_BYTES = 176
 Q6K_BYTES = 210
 Q8K_BYTES = 292
 
@@ -54,13 +55,14 @@ def _load():
         lib = ctypes.CDLL(build())
         vp, i64 = ctypes.c_void_p, ctypes.c_int64
         sig6 = [vp, vp, vp, i64, i64, i64]
-        for name in ("plm_ref_subdots_q4K", "plm_ref_subdots_q6K",
+        for name in ("plm_ref_subdots_q4K", "plm_ref_subdots_q5K", "plm_ref_subdots_q6K",
+                     "plm_ref_gemm_q5K_f64", "plm_ref_gemm_q5K_f32", "plm_ref_absscale_q5K",
                      "plm_ref_gemm_q4K_f64", "plm_ref_gemm_q4K_f32",
                      "plm_ref_gemm_q6K_f64", "plm_ref_gemm_q6K_f32",
                      "plm_ref_absscale_q4K", "plm_ref_absscale_q6K"):
             getattr(lib, name).argtypes = sig6
             getattr(lib, name).restype = None
-        for name in ("plm_ref_dequant_q4K", "plm_ref_dequant_q6K", "plm_ref_dequant_q8K"):
+        for name in ("plm_ref_dequant_q4K", "plm_ref_dequant_q5K", "plm_ref_dequant_q6K", "plm_ref_dequant_q8K"):
             getattr(lib, name).argtypes = [vp, vp, i64, i64]
             getattr(lib, name).restype = None
         lib.plm_ref_quantize_q8K.argtypes = [vp, vp, i64, i64]
@@ -134,6 +136,29 @@ def _call6(name, w, xq, m, n, k, shape, dtype):
 def subdots_q4K(w, xq, m, n, k):
     """int32 [m, n, k/256*8]: per 32-weight sub-block integer dots."""
     return _call6("plm_ref_subdots_q4K", w, xq, m, n, k, (m, n, k // QK * 8), np.int32)
+
+
+def subdots_q5K(w, xq, m, n, k):
+    return _call6("plm_ref_subdots_q5K", w, xq, m, n, k, (m, n, k // 32), np.int32)
+
+
+def gemm_q5K_f64(w, xq, m, n, k):
+    return _call6("plm_ref_gemm_q5K_f64", w, xq, m, n, k, (m, n), np.float64)
+
+
+def gemm_q5K_f32(w, xq, m, n, k):
+    return _call6("plm_ref_gemm_q5K_f32", w, xq, m, n, k, (m, n), np.float32)
+
+
+def absscale_q5K(w, xq, m, n, k):
+    return _call6("plm_ref_absscale_q5K", w, xq, m, n, k, (m, n), np.float64)
+
+
+def dequant_q5K(w, n, k):
+    w = _u8(w)
+    out = np.empty((n, k), dtype=np.float64)
+    _load().plm_ref_dequant_q5K(_p(w), _p(out), n, k)
+    return out
 
 
 def subdots_q6K(w, xq, m, n, k):

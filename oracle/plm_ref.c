@@ -18,6 +18,11 @@
  *           6-bit (scale, min) pairs, u8 qs[128]; each 64-weight chunk keeps
  *           its first 32 weights in the low nibbles and the next 32 in the
  *           high nibbles; weight = d*sc_j*q - dmin*m_j.
+ *      q5_K (176 B / 256 w): as q4_K plus a fifth bit per weight: f16 d,
+ *           f16 dmin, u8 scales[12], u8 qh[32], u8 qs[128]; weight 64c + l
+ *           (l < 32) takes qs[32c + l] & 15 and bit 2c of qh[l], weight
+ *           64c + 32 + l takes qs[32c + l] >> 4 and bit 2c + 1 of qh[l];
+ *           q5 = nibble + 16 * bit, weight = d*sc_j*q5 - dmin*m_j.
  *      q6_K (210 B / 256 w): u8 ql[128], u8 qh[64], i8 scales[16] (one per
  *           16 weights), f16 d; weight = d*sc*(q6 - 32).
  *      q8_K (292 B / 256 x): f32 d, i8 qs[256], i16 bsums[16].
@@ -42,6 +47,7 @@
 
 #define QK 256
 #define Q4K_BYTES 144
+#define Q5K_BYTES 176
 #define Q6K_BYTES 210
 #define Q8K_BYTES 292
 
@@ -434,4 +440,128 @@ void plm_ref_f16_array(const uint16_t* h, float* out, int64_t count) {
  */
 void plm_ref_swiglu_f64(const double* g, const double* u, double* h, int64_t count) {
     for (int64_t i = 0; i < count; ++i) h[i] = g[i] / (1.0 + exp(-g[i])) * u[i];
+}
+
+/* ------------------------------------------------------------------ */
+/* q5_K: the q4_K layout plus qh[32] (the fifth bit of every weight).  */
+/* Byte 32c+l of qs and byte l of qh give weight 64c+l (low nibble,    */
+/* qh bit 2c, sub-block 2c) and weight 64c+32+l (high nibble, qh bit   */
+/* 2c+1, sub-block 2c+1).  The scale/min table is q4_K's.             */
+/* ------------------------------------------------------------------ */
+static void q5K_block_dots(const uint8_t* wb, const int8_t* q8, int32_t dots[8]) {
+    const uint8_t* qh = wb + 16;
+    const uint8_t* qs = wb + 48;
+    for (int c = 0; c < 4; ++c) {
+        int32_t lo = 0, hi = 0;
+        for (int l = 0; l < 32; ++l) {
+            int byte = qs[32 * c + l];
+            int q0 = (byte & 15) + 16 * ((qh[l] >> (2 * c)) & 1);
+            int q1 = (byte >> 4) + 16 * ((qh[l] >> (2 * c + 1)) & 1);
+            lo += q0 * q8[64 * c + l];
+            hi += q1 * q8[64 * c + 32 + l];
+        }
+        dots[2 * c] = lo;
+        dots[2 * c + 1] = hi;
+    }
+}
+
+static void q5K_block_ints(const uint8_t* wb, const uint8_t* xb, int32_t* isum, int32_t* msum) {
+    int32_t dots[8];
+    q5K_block_dots(wb, (const int8_t*)(xb + 4), dots);
+    int32_t is = 0, ms = 0;
+    for (int j = 0; j < 8; ++j) {
+        int sc, mn;
+        plm_ref_q4K_scale_min(wb + 4, j, &sc, &mn);
+        is += sc * dots[j];
+        ms += mn * ((int32_t)load_i16(xb + 260 + 4 * j) + (int32_t)load_i16(xb + 260 + 4 * j + 2));
+    }
+    *isum = is;
+    *msum = ms;
+}
+
+void plm_ref_subdots_q5K(const uint8_t* w, const uint8_t* xq, int32_t* out,
+                         int64_t m, int64_t n, int64_t k) {
+    int64_t nb = k / QK;
+    for (int64_t i = 0; i < m; ++i)
+        for (int64_t r = 0; r < n; ++r)
+            for (int64_t b = 0; b < nb; ++b)
+                q5K_block_dots(w + (r * nb + b) * Q5K_BYTES,
+                               (const int8_t*)(xq + (i * nb + b) * Q8K_BYTES + 4),
+                               out + ((i * n + r) * nb + b) * 8);
+}
+
+void plm_ref_gemm_q5K_f64(const uint8_t* w, const uint8_t* xq, double* y,
+                          int64_t m, int64_t n, int64_t k) {
+    int64_t nb = k / QK;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < n; ++r) {
+        for (int64_t i = 0; i < m; ++i) {
+            double acc = 0.0;
+            for (int64_t b = 0; b < nb; ++b) {
+                const uint8_t* wb = w + (r * nb + b) * Q5K_BYTES;
+                const uint8_t* xb = xq + (i * nb + b) * Q8K_BYTES;
+                int32_t isum, msum;
+                q5K_block_ints(wb, xb, &isum, &msum);
+                double dx = (double)load_f32(xb);
+                acc += (double)load_f16(wb) * dx * (double)isum
+                     - (double)load_f16(wb + 2) * dx * (double)msum;
+            }
+            y[i * n + r] = acc;
+        }
+    }
+}
+
+void plm_ref_gemm_q5K_f32(const uint8_t* w, const uint8_t* xq, float* y,
+                          int64_t m, int64_t n, int64_t k) {
+    int64_t nb = k / QK;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < n; ++r) {
+        for (int64_t i = 0; i < m; ++i) {
+            float acc = 0.0f;
+            for (int64_t b = 0; b < nb; ++b) {
+                const uint8_t* wb = w + (r * nb + b) * Q5K_BYTES;
+                const uint8_t* xb = xq + (i * nb + b) * Q8K_BYTES;
+                int32_t isum, msum;
+                q5K_block_ints(wb, xb, &isum, &msum);
+                float dx = load_f32(xb);
+                acc += load_f16(wb) * dx * (float)isum - load_f16(wb + 2) * dx * (float)msum;
+            }
+            y[i * n + r] = acc;
+        }
+    }
+}
+
+/* Per-weight f64 dequantization of q5_K (from the weight index). */
+void plm_ref_dequant_q5K(const uint8_t* w, double* out, int64_t n, int64_t k) {
+    int64_t nb = k / QK;
+    for (int64_t r = 0; r < n; ++r)
+        for (int64_t b = 0; b < nb; ++b) {
+            const uint8_t* wb = w + (r * nb + b) * Q5K_BYTES;
+            double d = load_f16(wb), dmin = load_f16(wb + 2);
+            for (int t = 0; t < QK; ++t) {
+                int chunk = t / 64, within = t % 64, l = within % 32, upper = within >= 32;
+                int byte = wb[48 + 32 * chunk + l];
+                int q = (upper ? (byte >> 4) : (byte & 15)) + 16 * ((wb[16 + l] >> (2 * chunk + upper)) & 1);
+                int sc, mn;
+                plm_ref_q4K_scale_min(wb + 4, t / 32, &sc, &mn);
+                out[r * k + b * QK + t] = d * sc * q - dmin * mn;
+            }
+        }
+}
+
+void plm_ref_absscale_q5K(const uint8_t* w, const uint8_t* xq, double* S,
+                          int64_t m, int64_t n, int64_t k) {
+    int64_t nb = k / QK;
+    double wr[QK];
+    for (int64_t i = 0; i < m * n; ++i) S[i] = 0.0;
+    for (int64_t r = 0; r < n; ++r)
+        for (int64_t b = 0; b < nb; ++b) {
+            plm_ref_dequant_q5K(w + (r * nb + b) * Q5K_BYTES, wr, 1, QK);
+            for (int64_t i = 0; i < m; ++i) {
+                const uint8_t* xb = xq + (i * nb + b) * Q8K_BYTES;
+                double dx = load_f32(xb), s = 0.0;
+                for (int t = 0; t < QK; ++t) s += fabs(wr[t] * dx * (double)(int8_t)xb[4 + t]);
+                S[i * n + r] += s;
+            }
+        }
 }

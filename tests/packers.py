@@ -42,6 +42,25 @@ def pack_q4K(d, dmin, sc, mn, q):
     return blk
 
 
+def pack_q5K(d, dmin, sc, mn, q):
+    """q5_K: q4_K's header and scale table, then qh[32] holding the fifth bit of
+    every weight, then qs[128].  q: 256 ints in 0..31.  Weight 64c + l (l < 32)
+    keeps its low four bits in the low nibble of qs[32c + l] and its fifth bit
+    in bit 2c of qh[l]; weight 64c + 32 + l uses the high nibble and bit 2c+1."""
+    q = np.asarray(q, dtype=np.int64)
+    q4 = pack_q4K(d, dmin, sc, mn, q & 15)
+    blk = np.zeros(176, dtype=np.uint8)
+    blk[0:16] = q4[0:16]
+    blk[48:176] = q4[16:144]
+    qh = np.zeros(32, dtype=np.int64)
+    for w in range(256):
+        chunk, within = divmod(w, 64)
+        l, upper = within % 32, int(within >= 32)
+        qh[l] |= ((q[w] >> 4) & 1) << (2 * chunk + upper)
+    blk[16:48] = qh.astype(np.uint8)
+    return blk
+
+
 def pack_q6K(d, scales, q):
     """d: float (f16); scales: 16 ints in -128..127; q: 256 six-bit codes 0..63."""
     q = np.asarray(q, dtype=np.int64)

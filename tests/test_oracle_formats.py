@@ -12,7 +12,7 @@ import pytest
 
 import gen
 import oracle
-from tests.packers import pack_q4K, pack_q6K, pack_q8K
+from tests.packers import pack_q4K, pack_q5K, pack_q6K, pack_q8K
 
 
 def test_f16_exhaustive_against_numpy():
@@ -175,12 +175,17 @@ def test_q6K_dequant_and_dots_from_fields():
 
 # ------------------------------------------------ whole matmul, f64 check
 
-@pytest.mark.parametrize("fmt", ["q4K", "q6K"])
+@pytest.mark.parametrize("fmt", ["q4K", "q5K", "q6K"])
 @pytest.mark.parametrize("seed,m,n,k", [(s, 3, 5, 256) for s in range(8)] + [(0, 4, 33, 1024), (7, 2, 9, 2048)])
 def test_integer_path_equals_f64_dequant_matmul(fmt, seed, m, n, k):
     x = gen.normal_f32(seed, 100, m, k)
     xq = oracle.quantize_q8K(x)
-    if fmt == "q4K":
+    if fmt == "q5K":
+        w = gen.q5K_blocks(seed, 0, n, k)
+        wd = oracle.dequant_q5K(w, n, k)
+        y, S = oracle.gemm_q5K_f64(w, xq, m, n, k), oracle.absscale_q5K(w, xq, m, n, k)
+        y32 = oracle.gemm_q5K_f32(w, xq, m, n, k)
+    elif fmt == "q4K":
         w = gen.q4K_blocks(seed, 0, n, k)
         wd = oracle.dequant_q4K(w, n, k)
         y, S = oracle.gemm_q4K_f64(w, xq, m, n, k), oracle.absscale_q4K(w, xq, m, n, k)
@@ -223,3 +228,75 @@ def test_swiglu_epilogue_closed_forms():
     assert abs(oracle.swiglu_f64(np.array([40.0]), np.array([1.0]))[0] - 40.0) < 1e-12
     assert abs(oracle.swiglu_f64(np.array([-40.0]), np.array([1.0]))[0]) < 1e-12
     np.testing.assert_allclose(oracle.swiglu_f64(x, 3.0 * one), 3.0 * h, rtol=1e-15)
+
+
+# ------------------------------------------------------------------ q5_K
+
+
+def test_q5K_single_bit_position_map():
+    """One set bit -- a low or high nibble bit, or a qh bit -- identifies
+    exactly one weight, at the position the format text gives."""
+    seen = {}
+    for where in range(128 + 32):
+        for bit in ((0, 3) if where < 128 else range(8)):
+            blk = np.zeros(176, dtype=np.uint8)
+            blk[0:2] = np.array([1.0], dtype=np.float16).view(np.uint8)
+            blk[4:8] = 1    # scales 0..3 = 1, mins 0..3 = 0
+            blk[12:16] = 1  # scales 4..7 = 1, mins 4..7 = 0
+            if where < 128:        # qs byte: bit 0 (low nibble) or 4 (high nibble)
+                blk[48 + where] = 1 << (4 * (bit // 3))
+            else:
+                blk[16 + where - 128] = 1 << bit
+            w = oracle.dequant_q5K(blk, 1, 256)[0]
+            nz = np.nonzero(w)[0]
+            assert len(nz) == 1
+            if where < 128:
+                chunk, l = divmod(where, 32)
+                hi = bit // 3
+                assert nz[0] == 64 * chunk + 32 * hi + l and w[nz[0]] == 1.0
+            else:
+                l = where - 128
+                chunk, hi = divmod(bit, 2)
+                assert nz[0] == 64 * chunk + 32 * hi + l and w[nz[0]] == 16.0
+                seen[int(nz[0])] = True
+    assert len(seen) == 256
+
+
+def test_q5K_dequant_dots_and_combine_from_fields():
+    rng = np.random.default_rng(11)
+    for _ in range(30):
+        d = float(np.float16(rng.uniform(1e-4, 2e-3)))
+        dmin = float(np.float16(rng.uniform(1e-4, 2e-3)))
+        sc, mn, q = rng.integers(0, 64, 8), rng.integers(0, 64, 8), rng.integers(0, 32, 256)
+        wblk = pack_q5K(d, dmin, sc, mn, q)
+        j = np.arange(256) // 32
+        np.testing.assert_array_equal(oracle.dequant_q5K(wblk, 1, 256)[0],
+                                      np.float64(d) * sc[j] * q - np.float64(dmin) * mn[j])
+        dx = np.float32(rng.uniform(-0.05, 0.05))
+        q8 = rng.integers(-128, 128, 256)
+        xblk = pack_q8K(dx, q8)
+        dots = oracle.subdots_q5K(wblk, xblk, 1, 1, 256)[0, 0]
+        np.testing.assert_array_equal(dots, (q * q8).reshape(8, 32).sum(axis=1))
+        isum = int((sc * dots).sum())
+        msum = int((mn * q8.reshape(8, 32).sum(axis=1)).sum())
+        y = oracle.gemm_q5K_f64(wblk, xblk, 1, 1, 256)[0, 0]
+        expect = float(np.float64(d) * np.float64(dx) * isum - np.float64(dmin) * np.float64(dx) * msum)
+        assert y == pytest.approx(expect, rel=1e-15, abs=1e-300)
+
+
+def test_q5K_reduces_to_q4K_without_fifth_bits():
+    """With qh all zero a q5_K block is the q4_K block of the same fields."""
+    rng = np.random.default_rng(12)
+    d, dmin = 0.001, 0.0005
+    sc, mn, q = rng.integers(0, 64, 8), rng.integers(0, 64, 8), rng.integers(0, 16, 256)
+    np.testing.assert_array_equal(oracle.dequant_q5K(pack_q5K(d, dmin, sc, mn, q), 1, 256),
+                                  oracle.dequant_q4K(pack_q4K(d, dmin, sc, mn, q), 1, 256))
+
+
+def test_q5K_generated_fields():
+    w = gen.q5K_blocks(5, 0, 64, 1024).reshape(-1, 176)
+    d = w[:, 0:4].copy().view(np.float16).astype(np.float64)
+    assert d.min() >= 1e-4 * (1 - 1e-3) and d.max() <= 2e-3 * (1 + 1e-3)
+    # fifth bits are uniform: about half set
+    bits = np.unpackbits(w[:, 16:48])
+    assert abs(bits.mean() - 0.5) < 0.01
