@@ -43,6 +43,8 @@ sys.path.insert(0, ROOT)
 QK = 256
 Q4K_BYTES = 144
 Q6K_BYTES = 210
+Q5K_BYTES = 176
+FMT_BYTES = {"q4K": Q4K_BYTES, "q5K": Q5K_BYTES, "q6K": Q6K_BYTES}
 Q8K_BYTES = 292
 
 # (name, n, k) of the seven matrices of one layer, in storage order
@@ -240,11 +242,11 @@ def time_case(args):
     kind, fmt, n, k = args.case[0], args.case[1], int(args.case[2]), int(args.case[3])
     torch.cuda.set_device(0)
     nb = k // QK
-    bpb = Q4K_BYTES if fmt == "q4K" else Q6K_BYTES
+    bpb = FMT_BYTES[fmt]
     wbytes = n * nb * bpb
     l2 = torch.cuda.get_device_properties(0).L2_cache_size
     copies = max(1, -(-3 * l2 // wbytes))
-    w_host = gen.q4K_blocks(4, 0, n, k) if fmt == "q4K" else gen.q6K_blocks(4, 0, n, k)
+    w_host = getattr(gen, "%s_blocks" % fmt)(4, 0, n, k)
     ws = [torch.from_numpy(w_host).cuda() for _ in range(copies)]
     fn = getattr(q, "plm_%s_%s" % (kind, fmt))
     stream = torch.cuda.Stream()
@@ -304,7 +306,7 @@ class ShapeTimer:
 
     def weights(self, fmt, seed, n, k):
         import gen
-        host = gen.q4K_blocks(seed, 0, n, k) if fmt == "q4K" else gen.q6K_blocks(seed, 0, n, k)
+        host = getattr(gen, "%s_blocks" % fmt)(seed, 0, n, k)
         copies = max(1, -(-3 * self.l2 // host.nbytes))
         return [self.torch.from_numpy(host).cuda() for _ in range(copies)], host.nbytes
 
@@ -385,6 +387,10 @@ def run_extras(torch, q, peaks):
         del ws
         torch.cuda.empty_cache()
     out["sweep_qwen3_8b"] = sweep
+    # the q5_K rung on the Qwen3-8B gate/up shape: decode GEMV and prefill GEMM
+    ws, wb = T.weights("q5K", 5, 12288, 4096)
+    out["q5K_12288x4096"] = [T.run("q5K", ws, wb, 12288, 4096, m, 10 if m <= 8 else 3, 2) for m in (1, 8, 512)]
+    del ws
     return out
 
 

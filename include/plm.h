@@ -148,6 +148,28 @@ plm_status plm_gemv_q6K_grouped(const plm_gemv_problem* problems, int64_t count,
                                 cudaStream_t stream);
 
 /*
+ * q5_K, the next rung of the pages' K-quant width ladder (PocketLLM README,
+ * "What it runs": q2_k, q3_k, q5_k join q4_k and q6_k as formats the engine
+ * decodes).  Block (176 bytes per 256 weights, the public GGML layout): f16 d,
+ * f16 dmin, u8 scales[12] (q4_K's eight 6-bit (scale, min) pairs), u8 qh[32],
+ * u8 qs[128]; weight 64c + l (l < 32) = low nibble of qs[32c + l] + 16 * bit
+ * 2c of qh[l], weight 64c + 32 + l = high nibble + 16 * bit 2c + 1;
+ * value d * sc_j * q5 - dmin * m_j.  Same contracts, layouts, alignment and
+ * errors as the q4_K entry points (w 16-byte aligned); the sub-dot export
+ * writes int32 [m][n][k/32] like q4_K's.
+ */
+plm_status plm_gemv_q5K(const void* w, const void* xq, float* y, int64_t m, int64_t n, int64_t k,
+                        cudaStream_t stream);
+plm_status plm_gemv_q5K_grouped(const plm_gemv_problem* problems, int64_t count, int64_t m,
+                                cudaStream_t stream);
+plm_status plm_gemm_q5K(const void* w, const void* xq, float* y, int64_t m, int64_t n, int64_t k,
+                        cudaStream_t stream);
+plm_status plm_gemm_q5K_ws(const void* w, const void* xq, float* y, int64_t m, int64_t n, int64_t k,
+                           void* workspace, size_t workspace_bytes, cudaStream_t stream);
+plm_status plm_subdots_q5K(const void* w, const void* xq, int32_t* out, int64_t m, int64_t n, int64_t k,
+                           cudaStream_t stream);
+
+/*
  * Fused q8_K producer + decode GEMV (q4_K), y = W . x for 1 <= m <= 8, on
  * f32 activations.  PocketLLM (Korean README), "Current status" table, row
  * "src/": the packed matmul runs on int8 activations quantized per 256-value
@@ -220,7 +242,8 @@ plm_status plm_gemm_q4K(const void* w, const void* xq, float* y,
 plm_status plm_gemm_q6K(const void* w, const void* xq, float* y,
                         int64_t m, int64_t n, int64_t k, cudaStream_t stream);
 
-/* Workspace bytes plm_gemm_q4K_ws (fmt = 4) / plm_gemm_q6K_ws (fmt = 6)
+/* Workspace bytes plm_gemm_q4K_ws (fmt = 4) / plm_gemm_q5K_ws (fmt = 5) /
+ * plm_gemm_q6K_ws (fmt = 6)
  * need for m activation rows of length k (0 when none is needed, and for
  * invalid arguments). */
 size_t plm_gemm_workspace_size(int fmt, int64_t m, int64_t k);

@@ -5,5 +5,6 @@ from .plm import (  # noqa: F401
     plm_gemv_q4K, plm_gemv_q6K, plm_gemv_q4K_grouped, plm_gemv_q6K_grouped, plm_gemm_q4K, plm_gemm_q6K, plm_gemm_q4K_noalloc, plm_gemm_q4K_ws, plm_gemm_q6K_ws, plm_gemm_workspace_size,
     plm_subdots_q4K, plm_subdots_q6K, plm_quantize_gemv_q4K, plm_quantize_gemv_q4K_grouped,
     plm_gemv_q4K_swiglu, plm_gemv_q4K_swiglu_grouped,
+    plm_gemv_q5K, plm_gemv_q5K_grouped, plm_gemm_q5K, plm_gemm_q5K_ws, plm_subdots_q5K, Q5K_BYTES,
     QK, Q4K_BYTES, Q6K_BYTES, Q8K_BYTES, GEMV_MAX_M,
 )

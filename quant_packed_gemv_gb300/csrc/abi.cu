@@ -242,6 +242,31 @@ plm_status plm_gemv_q6K_grouped(const plm_gemv_problem* problems, int64_t count,
     return grouped_common(6, problems, count, m, stream);
 }
 
+plm_status plm_gemv_q5K(const void* w, const void* xq, float* y, int64_t m, int64_t n, int64_t k,
+                        cudaStream_t stream) {
+    return gemv_common(5, w, xq, y, m, n, k, stream);
+}
+
+plm_status plm_gemv_q5K_grouped(const plm_gemv_problem* problems, int64_t count, int64_t m,
+                                cudaStream_t stream) {
+    return grouped_common(5, problems, count, m, stream);
+}
+
+plm_status plm_gemm_q5K(const void* w, const void* xq, float* y, int64_t m, int64_t n, int64_t k,
+                        cudaStream_t stream) {
+    return gemm_common(5, w, xq, y, m, n, k, stream);
+}
+
+plm_status plm_gemm_q5K_ws(const void* w, const void* xq, float* y, int64_t m, int64_t n, int64_t k,
+                           void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    return gemm_ws_common(5, w, xq, y, m, n, k, workspace, workspace_bytes, stream);
+}
+
+plm_status plm_subdots_q5K(const void* w, const void* xq, int32_t* out, int64_t m, int64_t n, int64_t k,
+                           cudaStream_t stream) {
+    return subdots_common(5, w, xq, out, m, n, k, stream);
+}
+
 plm_status plm_gemm_q4K(const void* w, const void* xq, float* y, int64_t m, int64_t n, int64_t k,
                         cudaStream_t stream) {
     return gemm_common(4, w, xq, y, m, n, k, stream);
@@ -253,7 +278,7 @@ plm_status plm_gemm_q6K(const void* w, const void* xq, float* y, int64_t m, int6
 }
 
 size_t plm_gemm_workspace_size(int fmt, int64_t m, int64_t k) {
-    if ((fmt != 4 && fmt != 6) || m <= 0 || k <= 0 || k % plm::QK != 0 || k > kMaxIndex) return 0;
+    if ((fmt != 4 && fmt != 5 && fmt != 6) || m <= 0 || k <= 0 || k % plm::QK != 0 || k > kMaxIndex) return 0;
     return plm::gemm_workspace_need(fmt, m, (int)k);
 }
 

@@ -1,4 +1,4 @@
-// Prefill GEMM over packed q4_K / q6_K weights on the 5th-generation tensor
+// Prefill GEMM over packed q4_K / q5_K / q6_K weights on the 5th-generation tensor
 // cores (tcgen05, kind::f16), for m >= 9 activation rows (PocketLLM "What
 // it runs": weights stay packed and are decoded inside the kernel; the
 // matmul is a dense contraction once m is large).
@@ -6,6 +6,7 @@
 // Exactness.  Per 256-weight block the method needs exact integers:
 //   q4_K: isum = sum_j sc_j * sum_l q*q8 and msum = sum_g m_(g/2) * bsum_g,
 //         term = d_x*d_w*isum - dmin_x*d_w*msum;
+//   q5_K: as q4_K with 5-bit q (sc*q <= 63*31 = 1953, still exact in f16);
 //   q6_K: isum = sum_g sc_g * sum_l (q6-32)*q8, term = d_x*d_w*isum.
 // The operands are integer-valued and exact in f16: activation codes
 // q8 in [-128, 127]; q4_K weights sc*q <= 945; q6_K weights sc*(q6-32) in
@@ -53,6 +54,7 @@ constexpr int GEMM_THREADS = 9 * 32;
 // per stage (the high and low parts of the scale), no min term.
 template <int FMT> struct GemmCfg;
 template <> struct GemmCfg<4> { static constexpr int ATILES = 1, NSTAGE = 4, MINB = 2 * TILE_BYTES; };
+template <> struct GemmCfg<5> : GemmCfg<4> {};   // q5_K: q4_K's operands, a fifth bit per weight
 template <> struct GemmCfg<6> { static constexpr int ATILES = 2, NSTAGE = 3, MINB = 0; };
 
 template <int FMT>
@@ -150,14 +152,20 @@ __device__ __forceinline__ __half2 bits_h2(uint32_t u) { return *reinterpret_cas
 // q4_K: stage c of a block is chunk c (weights 64c .. 64c+63): K positions
 // 0..31 are the low nibbles of qs[32c .. 32c+31] times sc_(2c), positions
 // 32..63 the high nibbles times sc_(2c+1).
-struct Q4KRow {
-    uint4 raw[9];            // the 144-byte block
+template <int NRAW>
+struct QxKRow {
+    uint4 raw[NRAW];         // the block (q4_K 144 bytes, q5_K 176 bytes)
     float d, dmin;
     uint32_t sc_lo2[4], off_lo2[4], sc_hi2[4], off_hi2[4];   // per chunk c: f16x2 constants
     int mins[8];
 };
 
-__device__ __forceinline__ void q4K_row_prepare(Q4KRow& R) {
+using Q4KRow = QxKRow<9>;
+using Q5KRow = QxKRow<11>;
+
+// header of a q4_K / q5_K block: d, dmin, the f16x2 constants of each chunk, the mins
+template <int NRAW>
+__device__ __forceinline__ void q4K_row_prepare(QxKRow<NRAW>& R) {
     const uint4 hdr = R.raw[0];
     R.d = half_bits_to_float(hdr.x);
     R.dmin = half_bits_to_float(hdr.x >> 16);
@@ -200,6 +208,39 @@ __device__ __forceinline__ void q4K_row_stage(const Q4KRow& R, int c, uint8_t* t
             lo[2 * h + 1] = h2_bits(__hfma2(bits_h2((x23 & 0x000F000Fu) | 0x64006400u), slo, olo));
             hi[2 * h] = h2_bits(__hfma2(bits_h2((x01 & 0x00F000F0u) | 0x64006400u), shi, ohi));
             hi[2 * h + 1] = h2_bits(__hfma2(bits_h2((x23 & 0x00F000F0u) | 0x64006400u), shi, ohi));
+        }
+        *reinterpret_cast<uint4*>(tile + sw128_chunk(row, ch)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        *reinterpret_cast<uint4*>(tile + sw128_chunk(row, ch + 4)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    }
+}
+
+// q5_K: as q4_K, with the fifth bit of each weight from qh[32] (raw[1..2]):
+// weight 64c + l takes bit 2c of qh[l], weight 64c + 32 + l bit 2c + 1.  In
+// f16, 1024 + q5 (low) and 1024 + 16 q5 (high) are still exact, so the same
+// multiply-add constants give sc * q5.
+__device__ __forceinline__ void q5K_row_stage(const Q5KRow& R, int c, uint8_t* tile, int row) {
+    const uint4 qa = R.raw[3 + 2 * c], qb = R.raw[4 + 2 * c];
+    const uint32_t q[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+    const uint32_t qh[8] = {R.raw[1].x, R.raw[1].y, R.raw[1].z, R.raw[1].w,
+                            R.raw[2].x, R.raw[2].y, R.raw[2].z, R.raw[2].w};
+    const __half2 slo = bits_h2(R.sc_lo2[c]), olo = bits_h2(R.off_lo2[c]);
+    const __half2 shi = bits_h2(R.sc_hi2[c]), ohi = bits_h2(R.off_hi2[c]);
+#pragma unroll
+    for (int ch = 0; ch < 4; ++ch) {
+        uint32_t lo[4], hi[4];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint32_t w = q[2 * ch + h], b = qh[2 * ch + h];
+            const uint32_t x01 = __byte_perm(w, 0, 0x4140), x23 = __byte_perm(w, 0, 0x4342);
+            const uint32_t h01 = __byte_perm(b, 0, 0x4140), h23 = __byte_perm(b, 0, 0x4342);
+            const uint32_t l01 = (x01 & 0x000F000Fu) | (((h01 >> (2 * c)) & 0x00010001u) << 4);
+            const uint32_t l23 = (x23 & 0x000F000Fu) | (((h23 >> (2 * c)) & 0x00010001u) << 4);
+            const uint32_t u01 = (x01 & 0x00F000F0u) | (((h01 >> (2 * c + 1)) & 0x00010001u) << 8);
+            const uint32_t u23 = (x23 & 0x00F000F0u) | (((h23 >> (2 * c + 1)) & 0x00010001u) << 8);
+            lo[2 * h] = h2_bits(__hfma2(bits_h2(l01 | 0x64006400u), slo, olo));
+            lo[2 * h + 1] = h2_bits(__hfma2(bits_h2(l23 | 0x64006400u), slo, olo));
+            hi[2 * h] = h2_bits(__hfma2(bits_h2(u01 | 0x64006400u), shi, ohi));
+            hi[2 * h + 1] = h2_bits(__hfma2(bits_h2(u23 | 0x64006400u), shi, ohi));
         }
         *reinterpret_cast<uint4*>(tile + sw128_chunk(row, ch)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         *reinterpret_cast<uint4*>(tile + sw128_chunk(row, ch + 4)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
@@ -348,17 +389,20 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
         const int t = tid;
         const int r = r0 + t, i = i0 + t;
         const bool wrow = r < A.n, xrow = i < A.m;
-        using Row = typename std::conditional<FMT == 4, Q4KRow, Q6KRow>::type;
+        using Row = typename std::conditional<FMT == 6, Q6KRow,
+                                              typename std::conditional<FMT == 5, Q5KRow, Q4KRow>::type>::type;
         Row R, Rn;
         auto load_row = [&](Row& dst, int b) {
-            if constexpr (FMT == 4) {
+            if constexpr (FMT != 6) {
+                constexpr int NRAW = FMT == 5 ? 11 : 9;
+                constexpr int BYTES = FMT == 5 ? Q5K_BYTES : Q4K_BYTES;
                 if (wrow) {
-                    const uint4* src = reinterpret_cast<const uint4*>(A.w + ((size_t)r * nb + b) * Q4K_BYTES);
+                    const uint4* src = reinterpret_cast<const uint4*>(A.w + ((size_t)r * nb + b) * BYTES);
 #pragma unroll
-                    for (int u = 0; u < 9; ++u) dst.raw[u] = __ldg(src + u);
+                    for (int u = 0; u < NRAW; ++u) dst.raw[u] = __ldg(src + u);
                 } else {
 #pragma unroll
-                    for (int u = 0; u < 9; ++u) dst.raw[u] = make_uint4(0, 0, 0, 0);
+                    for (int u = 0; u < NRAW; ++u) dst.raw[u] = make_uint4(0, 0, 0, 0);
                 }
             } else {
                 q6K_row_load(dst, A.w + ((size_t)r * nb + b) * Q6K_BYTES, wrow);
@@ -368,7 +412,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
         for (int b = 0; b < nb && ok; ++b) {
             const int j = b & 1;
             float dw, dmw = 0.0f;
-            if constexpr (FMT == 4) {
+            if constexpr (FMT != 6) {
                 q4K_row_prepare(R);
                 dw = R.d;
                 dmw = R.dmin;
@@ -382,7 +426,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
             float dx = 0.0f;
             const uint8_t* xb = A.xq + ((size_t)i * nb + b) * Q8K_BYTES;
             if (xrow) dx = __ldg(reinterpret_cast<const float*>(xb));
-            if constexpr (FMT == 4) {
+            if constexpr (FMT != 6) {
                 // min operands: K 0..15 the weight row's mins m_(g/2); K 16..31 the activation row's bsums
                 uint8_t* mt = sm + L::MIN + j * TILE_BYTES;
                 uint32_t mv[8], bv[8];
@@ -426,7 +470,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
                     mbar_expect_tx(&full[s], TILE_BYTES);
                     tma_load_2d(st + BOFF, &xmap, b * QK + c * KS, i0, &full[s]);
                 }
-                if constexpr (FMT == 4)
+                if constexpr (FMT == 5)
+                    q5K_row_stage(R, c, st, t);
+                else if constexpr (FMT == 4)
                     q4K_row_stage(R, c, st, t);
                 else
                     q6K_row_stage(R, c, st, st + TILE_BYTES, t);
@@ -450,7 +496,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
                     tc_fence_after();
                     const uint32_t sa = smem_u32(sm + L::RING + s * L::STAGE);
                     const uint64_t db = umma_desc_sw128(sa + BOFF);
-                    if constexpr (FMT == 4) {
+                    if constexpr (FMT != 6) {
                         const uint64_t da = umma_desc_sw128(sa);
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)    // K = 16 per MMA: +32 bytes = +2 descriptor units
@@ -468,7 +514,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
                 if (!ok) break;
                 if (!mbar_wait(&minfull[j], (b >> 1) & 1)) { ok = false; break; }
                 tc_fence_after();
-                if constexpr (FMT == 4) {
+                if constexpr (FMT != 6) {
                     const uint32_t ma = smem_u32(sm + L::MIN + j * TILE_BYTES);
                     mma_f16(d2, umma_desc_sw128(ma), umma_desc_sw128(ma) + 2, 0u);
                 }
@@ -504,7 +550,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
                 for (int c = 0; c < 16; ++c) {
                     const float dx = sj[2 * GT + 16 * cc + c];
                     float tt;
-                    if constexpr (FMT == 4)   // d*isum - dmin*msum
+                    if constexpr (FMT != 6)   // d*isum - dmin*msum
                         tt = __fmaf_rn(dw, __uint_as_float(v1[c]), -__fmul_rn(dmw, __uint_as_float(v2[c])));
                     else                      // d*(16*hi + lo)
                         tt = __fmul_rn(dw, __fmaf_rn(16.0f, __uint_as_float(v1[c]), __uint_as_float(v2[c])));
@@ -627,7 +673,9 @@ cudaError_t launch_gemm_ws(int fmt, const uint8_t* w, const uint8_t* xq, float* 
                            void* ws, size_t ws_bytes, cudaStream_t stream) {
     if (m >= GEMM_MIN_M && (long long)m <= 0x7FFFFFFF) {
         if (!ws || ws_bytes < gemm_workspace_bytes(m, k)) return cudaErrorInvalidValue;
-        return fmt == 4 ? gemm_tc_ws<4>(w, xq, y, m, n, k, ws, stream) : gemm_tc_ws<6>(w, xq, y, m, n, k, ws, stream);
+        return fmt == 4 ? gemm_tc_ws<4>(w, xq, y, m, n, k, ws, stream)
+               : fmt == 5 ? gemm_tc_ws<5>(w, xq, y, m, n, k, ws, stream)
+                          : gemm_tc_ws<6>(w, xq, y, m, n, k, ws, stream);
     }
     const int nb = k / QK;
     for (long long i0 = 0; i0 < m; i0 += GEMV_MAX_M) {

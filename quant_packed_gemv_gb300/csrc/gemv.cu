@@ -7,14 +7,20 @@ namespace plm {
 cudaError_t run_group_q4K(const HostProblem* p, int count, int m, bool subdots, cudaStream_t stream);
 cudaError_t run_group_q4K_f32(const HostProblem* p, int count, int m, cudaStream_t stream);
 cudaError_t run_group_q4K_swiglu(const HostProblem* p, int count, int m, cudaStream_t stream);
+cudaError_t run_group_q5K(const HostProblem* p, int count, int m, bool subdots, cudaStream_t stream);
 cudaError_t run_group_q6K(const HostProblem* p, int count, int m, bool subdots, cudaStream_t stream);
 bool gemv_supported_q4K(int k);
+bool gemv_supported_q5K(int k);
 bool gemv_supported_q6K(int k);
 
-bool gemv_supported(int fmt, int k) { return fmt == 4 ? gemv_supported_q4K(k) : gemv_supported_q6K(k); }
+bool gemv_supported(int fmt, int k) {
+    return fmt == 4 ? gemv_supported_q4K(k) : fmt == 5 ? gemv_supported_q5K(k) : gemv_supported_q6K(k);
+}
 
 static cudaError_t run_fmt(int fmt, const HostProblem* p, int count, int m, bool subdots, cudaStream_t s) {
-    return fmt == 4 ? run_group_q4K(p, count, m, subdots, s) : run_group_q6K(p, count, m, subdots, s);
+    return fmt == 4   ? run_group_q4K(p, count, m, subdots, s)
+           : fmt == 5 ? run_group_q5K(p, count, m, subdots, s)
+                      : run_group_q6K(p, count, m, subdots, s);
 }
 
 cudaError_t launch_gemv(int fmt, const uint8_t* w, const uint8_t* xq, float* y,

@@ -42,8 +42,21 @@ namespace plm {
 namespace q4lane {
 
 constexpr int STAGE_BLOCKS = 32;
-constexpr int SLOT = STAGE_BLOCKS * Q4K_BYTES;   // 4608
 constexpr int REC = 272;                         // staged bytes per activation block
+
+// Block formats of this kernel: q4_K and q5_K (q4_K plus qh[32], the fifth
+// bit of every weight, between the scale table and qs).  Both are whole
+// 16-byte multiples, so every block of a stage is 16-byte aligned.
+template <int FMT> struct LaneFmt;
+template <> struct LaneFmt<4> {
+    static constexpr int BYTES = Q4K_BYTES;
+    static constexpr int QS = 16;                            // offset of qs[128]
+};
+template <> struct LaneFmt<5> {
+    static constexpr int BYTES = Q5K_BYTES;
+    static constexpr int QS = 48;
+};
+template <int FMT> __host__ __device__ constexpr int slot_bytes() { return STAGE_BLOCKS * LaneFmt<FMT>::BYTES; }
 
 // Bytes of one staged segment of nblk activation blocks: records, then the
 // scales, padded to 16 bytes so the next segment's records stay aligned.
@@ -184,10 +197,16 @@ __device__ __forceinline__ int dp2a_hi_su(int a, uint32_t b, int c) {
 // One whole q4_K block against M staged activation blocks (same column,
 // records act_stride bytes apart, scales dy_stride floats apart).  Adds the
 // block's f32 term to v[i], or writes the eight exact sub-block dots.
-template <int M, bool SUBDOTS>
+template <int FMT, int M, bool SUBDOTS>
 __device__ __forceinline__ void lane_block(const uint8_t* w, const uint8_t* act, int act_stride, const float* dy,
                                            int dy_stride, float* v, int32_t* sub, size_t sub_stride) {
     const uint4 hdr = *reinterpret_cast<const uint4*>(w);
+    uint32_t qh[8];   // q5_K: the fifth bits, byte l <-> byte l of every qs chunk
+    if constexpr (FMT == 5) {
+        const uint4 h0 = *reinterpret_cast<const uint4*>(w + 16), h1 = *reinterpret_cast<const uint4*>(w + 32);
+        qh[0] = h0.x; qh[1] = h0.y; qh[2] = h0.z; qh[3] = h0.w;
+        qh[4] = h1.x; qh[5] = h1.y; qh[6] = h1.z; qh[7] = h1.w;
+    }
     // six-bit scales (sc) and mins (m) as bytes: j = 0..3 and j = 4..7
     const uint32_t scA = hdr.y & 0x3F3F3F3Fu;
     const uint32_t mA = hdr.z & 0x3F3F3F3Fu;
@@ -198,9 +217,22 @@ __device__ __forceinline__ void lane_block(const uint8_t* w, const uint8_t* act,
     for (int i = 0; i < M; ++i) isum[i] = 0;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-        const uint4 qa = *reinterpret_cast<const uint4*>(w + 16 + 32 * c);
-        const uint4 qb = *reinterpret_cast<const uint4*>(w + 32 + 32 * c);
+        const uint4 qa = *reinterpret_cast<const uint4*>(w + LaneFmt<FMT>::QS + 32 * c);
+        const uint4 qb = *reinterpret_cast<const uint4*>(w + LaneFmt<FMT>::QS + 16 + 32 * c);
         const uint32_t q[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+        // the codes of sub-blocks 2c (lo) and 2c+1 (hi) as bytes; q4_K's high
+        // nibbles stay in place (16 q), divided out of the dot below
+        uint32_t cl[8], ch[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            if constexpr (FMT == 5) {
+                cl[u] = (q[u] & 0x0F0F0F0Fu) | (((qh[u] >> (2 * c)) & 0x01010101u) << 4);
+                ch[u] = ((q[u] >> 4) & 0x0F0F0F0Fu) | (((qh[u] >> (2 * c + 1)) & 0x01010101u) << 4);
+            } else {
+                cl[u] = q[u] & 0x0F0F0F0Fu;
+                ch[u] = q[u] & 0xF0F0F0F0u;
+            }
+        }
         const uint32_t sw = c < 2 ? scA : scB;
         const int s0 = (int)((sw >> (16 * (c & 1))) & 0xFFu);
         const int s1 = (int)((sw >> (16 * (c & 1) + 8)) & 0xFFu);
@@ -213,10 +245,10 @@ __device__ __forceinline__ void lane_block(const uint8_t* w, const uint8_t* act,
             int lo = 0, hi = 0;
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
-                lo = dp4a_us(q[u] & 0x0F0F0F0Fu, xl[u], lo);
-                hi = dp4a_us(q[u] & 0xF0F0F0F0u, xh[u], hi);
+                lo = dp4a_us(cl[u], xl[u], lo);
+                hi = dp4a_us(ch[u], xh[u], hi);
             }
-            hi >>= 4;   // the high nibbles were used in place (16 * q)
+            if constexpr (FMT == 4) hi >>= 4;   // the high nibbles were used in place (16 * q)
             if constexpr (SUBDOTS) {
                 sub[i * sub_stride + 2 * c] = lo;
                 sub[i * sub_stride + 2 * c + 1] = hi;
@@ -241,9 +273,11 @@ __device__ __forceinline__ void lane_block(const uint8_t* w, const uint8_t* act,
     }
 }
 
-template <int M, bool SUBDOTS, bool XF32, bool PAIR, int WARPS, int MAXP>
+template <int FMT, int M, bool SUBDOTS, bool XF32, bool PAIR, int WARPS, int MAXP>
 __global__ void __launch_bounds__(WARPS * 32, 1) lane_kernel(const __grid_constant__ LaneBatch<MAXP> B) {
     constexpr int PF = PAIR ? 2 : 1;
+    constexpr int BYTES = LaneFmt<FMT>::BYTES;
+    constexpr int SLOT = slot_bytes<FMT>();
     extern __shared__ __align__(128) uint8_t smem[];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -287,9 +321,9 @@ __global__ void __launch_bounds__(WARPS * 32, 1) lane_kernel(const __grid_consta
         }
         if (lane == 0) {
             uint64_t* bar = &bars[islot];
-            const uint32_t bytes = (uint32_t)blocks * Q4K_BYTES;   // q4_K rows: whole 16-byte multiples
+            const uint32_t bytes = (uint32_t)blocks * BYTES;   // rows: whole 16-byte multiples
             mbar_arrive_expect_tx(bar, bytes);
-            bulk_g2s(ring + islot * SLOT, (second ? Q.w2 : Q.w) + first * Q4K_BYTES, bytes, bar);
+            bulk_g2s(ring + islot * SLOT, (second ? Q.w2 : Q.w) + first * BYTES, bytes, bar);
         }
         islot = islot + 1 == (uint32_t)NS ? 0 : islot + 1;
         ++issued;
@@ -362,7 +396,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1) lane_kernel(const __grid_consta
                 for (int i = 0; i < M; ++i) v[i] = 0.0f;
                 int32_t* sub = SUBDOTS ? subv + ((size_t)(r0 + rl) * nb + col) * 8 : nullptr;
                 if (!SUBDOTS || valid)
-                    lane_block<M, SUBDOTS>(slot + bl * Q4K_BYTES, rec + (size_t)col * REC, act_stride, dyv + col,
+                    lane_block<FMT, M, SUBDOTS>(slot + bl * BYTES, rec + (size_t)col * REC, act_stride, dyv + col,
                                            nb, v, sub, sub_stride);
                 if constexpr (!SUBDOTS) {
                     if (pow2) {
@@ -402,7 +436,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1) lane_kernel(const __grid_consta
                 for (int i = 0; i < M; ++i) v[i] = acc[i];
                 int32_t* sub = SUBDOTS ? subv + ((size_t)cc.u * nb + b) * 8 : nullptr;
                 if (!SUBDOTS || valid)
-                    lane_block<M, SUBDOTS>(slot + (valid ? lane : 0) * Q4K_BYTES, rec + (size_t)b * REC, act_stride,
+                    lane_block<FMT, M, SUBDOTS>(slot + (valid ? lane : 0) * BYTES, rec + (size_t)b * REC, act_stride,
                                            dyv + b, nb, v, sub, sub_stride);
 #pragma unroll
                 for (int i = 0; i < M; ++i) acc[i] = valid ? v[i] : acc[i];
@@ -439,7 +473,8 @@ struct Config {
     int warps, ns, grid, act_bytes;
 };
 
-inline size_t ring_bytes(int warps, int ns) { return (size_t)warps * ns * (SLOT + 8); }
+template <int FMT>
+inline size_t ring_bytes(int warps, int ns) { return (size_t)warps * ns * (slot_bytes<FMT>() + 8); }
 inline size_t align128(size_t x) { return (x + 127) & ~(size_t)127; }
 
 struct Plan {
@@ -485,6 +520,7 @@ inline size_t act_need(const HostProblem* hp, int count, const Plan& pl, int m, 
     return align128(worst);
 }
 
+template <int FMT>
 inline bool pick_config(const HostProblem* hp, int count, const Plan& pl, int m, Config* cfg) {
     const size_t optin = (size_t)smem_optin_bytes();
     const int opts[][2] = {{16, 3}, {16, 2}, {12, 2}};
@@ -494,7 +530,7 @@ inline bool pick_config(const HostProblem* hp, int count, const Plan& pl, int m,
         if (grid > want) grid = want;
         if (grid < 1) grid = 1;
         const size_t act = act_need(hp, count, pl, m, (int)grid, o[0]);
-        if (act + ring_bytes(o[0], o[1]) <= optin) {
+        if (act + ring_bytes<FMT>(o[0], o[1]) <= optin) {
             *cfg = Config{o[0], o[1], (int)grid, (int)act};
             return true;
         }
@@ -502,7 +538,7 @@ inline bool pick_config(const HostProblem* hp, int count, const Plan& pl, int m,
     return false;
 }
 
-template <int M, bool SUB, bool XF32, bool PAIR, int WARPS, int MAXP>
+template <int FMT, int M, bool SUB, bool XF32, bool PAIR, int WARPS, int MAXP>
 cudaError_t launch(const HostProblem* hp, int count, const Plan& pl, const Config& cfg, cudaStream_t stream) {
     LaneBatch<MAXP> B;
     B.fault = fault_word();
@@ -515,46 +551,46 @@ cudaError_t launch(const HostProblem* hp, int count, const Plan& pl, const Confi
     B.nstages = cfg.ns;
     B.act_bytes = cfg.act_bytes;
     B.wtotal = (int)pl.wtotal;
-    const size_t smem = (size_t)cfg.act_bytes + ring_bytes(WARPS, cfg.ns);
-    const void* fn = (const void*)lane_kernel<M, SUB, XF32, PAIR, WARPS, MAXP>;
+    const size_t smem = (size_t)cfg.act_bytes + ring_bytes<FMT>(WARPS, cfg.ns);
+    const void* fn = (const void*)lane_kernel<FMT, M, SUB, XF32, PAIR, WARPS, MAXP>;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    lane_kernel<M, SUB, XF32, PAIR, WARPS, MAXP><<<(unsigned)cfg.grid, WARPS * 32, smem, stream>>>(B);
+    lane_kernel<FMT, M, SUB, XF32, PAIR, WARPS, MAXP><<<(unsigned)cfg.grid, WARPS * 32, smem, stream>>>(B);
     return cudaGetLastError();
 }
 
 // Launches one pass of M activation rows; false in *fits when no ring and
 // staging layout fits in shared memory (the caller then splits the work).
-template <int M, bool SUB, bool XF32, bool PAIR>
+template <int FMT, int M, bool SUB, bool XF32, bool PAIR>
 cudaError_t launch_m(const HostProblem* hp, int count, cudaStream_t stream, bool* fits) {
     Plan pl;
     make_plan(hp, count, 16, PAIR ? 2 : 1, &pl);
     *fits = false;
     if (pl.wtotal >= (1LL << 31)) return cudaSuccess;
     Config cfg;
-    if (!pick_config(hp, count, pl, M, &cfg)) return cudaSuccess;
+    if (!pick_config<FMT>(hp, count, pl, M, &cfg)) return cudaSuccess;
     *fits = true;
     if (cfg.warps == 16) {
-        if (count == 1) return launch<M, SUB, XF32, PAIR, 16, 1>(hp, count, pl, cfg, stream);
-        if constexpr (!SUB) return launch<M, SUB, XF32, PAIR, 16, GROUP_MAX>(hp, count, pl, cfg, stream);
+        if (count == 1) return launch<FMT, M, SUB, XF32, PAIR, 16, 1>(hp, count, pl, cfg, stream);
+        if constexpr (!SUB) return launch<FMT, M, SUB, XF32, PAIR, 16, GROUP_MAX>(hp, count, pl, cfg, stream);
     } else {
-        if (count == 1) return launch<M, SUB, XF32, PAIR, 12, 1>(hp, count, pl, cfg, stream);
-        if constexpr (!SUB) return launch<M, SUB, XF32, PAIR, 12, GROUP_MAX>(hp, count, pl, cfg, stream);
+        if (count == 1) return launch<FMT, M, SUB, XF32, PAIR, 12, 1>(hp, count, pl, cfg, stream);
+        if constexpr (!SUB) return launch<FMT, M, SUB, XF32, PAIR, 12, GROUP_MAX>(hp, count, pl, cfg, stream);
     }
     return cudaErrorInvalidValue;
 }
 
-template <bool SUB, bool XF32, bool PAIR>
+template <int FMT, bool SUB, bool XF32, bool PAIR>
 cudaError_t dispatch(int m, const HostProblem* hp, int count, cudaStream_t stream, bool* fits) {
     switch (m) {
-        case 1: return launch_m<1, SUB, XF32, PAIR>(hp, count, stream, fits);
-        case 2: return launch_m<2, SUB, XF32, PAIR>(hp, count, stream, fits);
-        case 3: return launch_m<3, SUB, XF32, PAIR>(hp, count, stream, fits);
-        case 4: return launch_m<4, SUB, XF32, PAIR>(hp, count, stream, fits);
-        case 5: return launch_m<5, SUB, XF32, PAIR>(hp, count, stream, fits);
-        case 6: return launch_m<6, SUB, XF32, PAIR>(hp, count, stream, fits);
-        case 7: return launch_m<7, SUB, XF32, PAIR>(hp, count, stream, fits);
-        case 8: return launch_m<8, SUB, XF32, PAIR>(hp, count, stream, fits);
+        case 1: return launch_m<FMT, 1, SUB, XF32, PAIR>(hp, count, stream, fits);
+        case 2: return launch_m<FMT, 2, SUB, XF32, PAIR>(hp, count, stream, fits);
+        case 3: return launch_m<FMT, 3, SUB, XF32, PAIR>(hp, count, stream, fits);
+        case 4: return launch_m<FMT, 4, SUB, XF32, PAIR>(hp, count, stream, fits);
+        case 5: return launch_m<FMT, 5, SUB, XF32, PAIR>(hp, count, stream, fits);
+        case 6: return launch_m<FMT, 6, SUB, XF32, PAIR>(hp, count, stream, fits);
+        case 7: return launch_m<FMT, 7, SUB, XF32, PAIR>(hp, count, stream, fits);
+        case 8: return launch_m<FMT, 8, SUB, XF32, PAIR>(hp, count, stream, fits);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -563,7 +599,7 @@ cudaError_t dispatch(int m, const HostProblem* hp, int count, cudaStream_t strea
 // when it fits, else the problems in two halves; a single problem that does
 // not fit is taken in smaller row passes.  The f32 order of an output row
 // depends only on nb, so none of these splits changes a bit.
-template <bool XF32, bool PAIR>
+template <int FMT, bool XF32, bool PAIR>
 cudaError_t run_part(const HostProblem* probs, int count, int i0, int mm, bool subdots, cudaStream_t stream) {
     HostProblem part[GROUP_MAX];
     for (int j = 0; j < count; ++j) {
@@ -577,29 +613,29 @@ cudaError_t run_part(const HostProblem* probs, int count, int i0, int mm, bool s
     bool fits = false;
     cudaError_t e;
     if constexpr (XF32 || PAIR)
-        e = dispatch<false, XF32, PAIR>(mm, part, count, stream, &fits);
+        e = dispatch<FMT, false, XF32, PAIR>(mm, part, count, stream, &fits);
     else
-        e = subdots ? dispatch<true, false, false>(mm, part, count, stream, &fits)
-                    : dispatch<false, false, false>(mm, part, count, stream, &fits);
+        e = subdots ? dispatch<FMT, true, false, false>(mm, part, count, stream, &fits)
+                    : dispatch<FMT, false, false, false>(mm, part, count, stream, &fits);
     if (e != cudaSuccess || fits) return e;
     if (count > 1) {
         const int h = count / 2;
-        e = run_part<XF32, PAIR>(probs, h, i0, mm, subdots, stream);
+        e = run_part<FMT, XF32, PAIR>(probs, h, i0, mm, subdots, stream);
         if (e != cudaSuccess) return e;
-        return run_part<XF32, PAIR>(probs + h, count - h, i0, mm, subdots, stream);
+        return run_part<FMT, XF32, PAIR>(probs + h, count - h, i0, mm, subdots, stream);
     }
     if (mm == 1) return cudaErrorInvalidConfiguration;
     const int h = mm / 2;
-    e = run_part<XF32, PAIR>(probs, 1, i0, h, subdots, stream);
+    e = run_part<FMT, XF32, PAIR>(probs, 1, i0, h, subdots, stream);
     if (e != cudaSuccess) return e;
-    return run_part<XF32, PAIR>(probs, 1, i0 + h, mm - h, subdots, stream);
+    return run_part<FMT, XF32, PAIR>(probs, 1, i0 + h, mm - h, subdots, stream);
 }
 
-template <bool XF32, bool PAIR>
+template <int FMT, bool XF32, bool PAIR>
 cudaError_t run_group(const HostProblem* probs, int count, int m, bool subdots, cudaStream_t stream) {
     for (int p0 = 0; p0 < count; p0 += GROUP_MAX) {
         const int cnt = count - p0 < GROUP_MAX ? count - p0 : GROUP_MAX;
-        const cudaError_t e = run_part<XF32, PAIR>(probs + p0, cnt, 0, m, subdots, stream);
+        const cudaError_t e = run_part<FMT, XF32, PAIR>(probs + p0, cnt, 0, m, subdots, stream);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;

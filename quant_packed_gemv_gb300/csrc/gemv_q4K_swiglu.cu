@@ -5,7 +5,7 @@
 namespace plm {
 
 cudaError_t run_group_q4K_swiglu(const HostProblem* probs, int count, int m, cudaStream_t stream) {
-    return q4lane::run_group<false, true>(probs, count, m, false, stream);
+    return q4lane::run_group<4, false, true>(probs, count, m, false, stream);
 }
 
 }  // namespace plm

@@ -10,6 +10,7 @@ namespace plm {
 
 constexpr int QK = 256;          // weights (or activations) per block
 constexpr int Q4K_BYTES = 144;   // f16 d, f16 dmin, scales[12], qs[128]
+constexpr int Q5K_BYTES = 176;   // f16 d, f16 dmin, scales[12], qh[32], qs[128]
 constexpr int Q6K_BYTES = 210;   // ql[128], qh[64], scales[16], f16 d
 constexpr int Q8K_BYTES = 292;   // f32 d, qs[256], bsums[16]
 constexpr int GEMV_MAX_M = 8;

@@ -19,6 +19,7 @@ PLM_ERR_CUDA = 4
 
 QK = 256
 Q4K_BYTES = 144
+Q5K_BYTES = 176
 Q6K_BYTES = 210
 Q8K_BYTES = 292
 GEMV_MAX_M = 8
@@ -81,11 +82,11 @@ def load(build_if_missing=True):
     lib.plm_quantize_q8K.restype = ctypes.c_int
     lib.plm_gemm_workspace_size.argtypes = [ctypes.c_int, i64, i64]
     lib.plm_gemm_workspace_size.restype = ctypes.c_size_t
-    for name in ("plm_gemm_q4K_ws", "plm_gemm_q6K_ws"):
+    for name in ("plm_gemm_q4K_ws", "plm_gemm_q5K_ws", "plm_gemm_q6K_ws"):
         fn = getattr(lib, name)
         fn.argtypes = [vp, vp, vp, i64, i64, i64, vp, ctypes.c_size_t, vp]
         fn.restype = ctypes.c_int
-    for name in ("plm_gemv_q4K_grouped", "plm_gemv_q6K_grouped"):
+    for name in ("plm_gemv_q4K_grouped", "plm_gemv_q5K_grouped", "plm_gemv_q6K_grouped"):
         fn = getattr(lib, name)
         fn.argtypes = [ctypes.POINTER(_Problem), i64, i64, vp]
         fn.restype = ctypes.c_int
@@ -96,7 +97,8 @@ def load(build_if_missing=True):
     lib.plm_quantize_gemv_q4K_grouped.argtypes = [ctypes.POINTER(_QProblem), i64, i64, vp]
     lib.plm_quantize_gemv_q4K_grouped.restype = ctypes.c_int
     for name in ("plm_gemv_q4K", "plm_gemv_q6K", "plm_gemm_q4K", "plm_gemm_q6K", "plm_gemm_q4K_noalloc",
-                 "plm_subdots_q4K", "plm_subdots_q6K", "plm_quantize_gemv_q4K"):
+                 "plm_subdots_q4K", "plm_subdots_q6K", "plm_quantize_gemv_q4K",
+                 "plm_gemv_q5K", "plm_gemm_q5K", "plm_subdots_q5K"):
         fn = getattr(lib, name)
         fn.argtypes = [vp, vp, vp, i64, i64, i64, vp]
         fn.restype = ctypes.c_int
@@ -166,6 +168,9 @@ def _mm(name):
 
 plm_gemv_q4K = _mm("plm_gemv_q4K")
 plm_gemv_q6K = _mm("plm_gemv_q6K")
+plm_gemv_q5K = _mm("plm_gemv_q5K")
+plm_gemm_q5K = _mm("plm_gemm_q5K")
+plm_subdots_q5K = _mm("plm_subdots_q5K")
 plm_gemm_q4K = _mm("plm_gemm_q4K")
 plm_gemm_q6K = _mm("plm_gemm_q6K")
 # q4_K GEMM whose workspace is a fixed array inside the library: for callers
@@ -192,6 +197,7 @@ def _grouped(name):
 
 plm_gemv_q4K_grouped = _grouped("plm_gemv_q4K_grouped")
 plm_gemv_q6K_grouped = _grouped("plm_gemv_q6K_grouped")
+plm_gemv_q5K_grouped = _grouped("plm_gemv_q5K_grouped")
 
 
 def plm_gemv_q4K_swiglu(w_gate, w_up, xq, h, m, n, k, stream=None):
@@ -220,8 +226,8 @@ def plm_quantize_gemv_q4K_grouped(problems, m, stream=None):
 
 
 def plm_gemm_workspace_size(fmt, m, k):
-    """fmt: 'q4K' / 'q6K' or 4 / 6."""
-    f = {"q4K": 4, "q6K": 6}.get(fmt, fmt)
+    """fmt: 'q4K' / 'q5K' / 'q6K' or 4 / 5 / 6."""
+    f = {"q4K": 4, "q5K": 5, "q6K": 6}.get(fmt, fmt)
     return load().plm_gemm_workspace_size(f, m, k)
 
 
@@ -239,6 +245,7 @@ def _gemm_ws(name):
 
 plm_gemm_q4K_ws = _gemm_ws("plm_gemm_q4K_ws")
 plm_gemm_q6K_ws = _gemm_ws("plm_gemm_q6K_ws")
+plm_gemm_q5K_ws = _gemm_ws("plm_gemm_q5K_ws")
 
 
 def raw_status(name, *args):

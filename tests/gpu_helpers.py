@@ -20,7 +20,7 @@ def host(t):
 
 
 def make_weights(fmt, seed, stream, n, k):
-    return gen.q4K_blocks(seed, stream, n, k) if fmt == "q4K" else gen.q6K_blocks(seed, stream, n, k)
+    return getattr(gen, "%s_blocks" % fmt)(seed, stream, n, k)
 
 
 def gpu_quantize(x_np):
@@ -48,7 +48,7 @@ def gpu_matmul(kind, fmt, w_np, xq_np, m, n, k, poison=True):
 
 
 def gpu_subdots(fmt, w_np, xq_np, m, n, k):
-    per = 8 if fmt == "q4K" else 16
+    per = 16 if fmt == "q6K" else 8
     w, xq = dev(w_np), dev(xq_np)
     out = torch.full((m, n, k // 256 * per), -7, dtype=torch.int32, device="cuda")
     getattr(q, "plm_subdots_%s" % fmt)(w, xq, out, m, n, k)
@@ -56,9 +56,8 @@ def gpu_subdots(fmt, w_np, xq_np, m, n, k):
 
 
 def oracle_ref(fmt, w_np, xq_np, m, n, k):
-    if fmt == "q4K":
-        return oracle.gemm_q4K_f64(w_np, xq_np, m, n, k), oracle.absscale_q4K(w_np, xq_np, m, n, k)
-    return oracle.gemm_q6K_f64(w_np, xq_np, m, n, k), oracle.absscale_q6K(w_np, xq_np, m, n, k)
+    return (getattr(oracle, "gemm_%s_f64" % fmt)(w_np, xq_np, m, n, k),
+            getattr(oracle, "absscale_%s" % fmt)(w_np, xq_np, m, n, k))
 
 
 def assert_close(y, ref, S, tol=TOL):

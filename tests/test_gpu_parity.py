@@ -35,20 +35,20 @@ def test_quantize_scaled_and_tiny_values():
 
 # ------------------------------------------------------ integer sub-dots
 
-@pytest.mark.parametrize("fmt", ["q4K", "q6K"])
+@pytest.mark.parametrize("fmt", ["q4K", "q5K", "q6K"])
 @pytest.mark.parametrize("m,n,k", [(1, 1, 256), (1, 33, 1024), (3, 17, 1280), (8, 40, 2048),
                                    (5, 9, 2816)])
 def test_subdots_bit_exact(fmt, m, n, k):
     w = make_weights(fmt, 7, 0, n, k)
     xq = oracle.quantize_q8K(gen.normal_f32(7, 200, m, k))
     got = gpu_subdots(fmt, w, xq, m, n, k)
-    want = oracle.subdots_q4K(w, xq, m, n, k) if fmt == "q4K" else oracle.subdots_q6K(w, xq, m, n, k)
+    want = getattr(oracle, "subdots_%s" % fmt)(w, xq, m, n, k)
     np.testing.assert_array_equal(got, want)
 
 
 # --------------------------------------------------------------- GEMV
 
-@pytest.mark.parametrize("fmt", ["q4K", "q6K"])
+@pytest.mark.parametrize("fmt", ["q4K", "q5K", "q6K"])
 @pytest.mark.parametrize("m", [1, 2, 3, 4, 5, 6, 7, 8])
 @pytest.mark.parametrize("n,k", [(1, 256), (37, 1024), (100, 1280), (64, 3072)])
 def test_gemv_matches_oracle(fmt, m, n, k):
@@ -59,7 +59,7 @@ def test_gemv_matches_oracle(fmt, m, n, k):
     assert_close(y, ref, S)
 
 
-@pytest.mark.parametrize("fmt", ["q4K", "q6K"])
+@pytest.mark.parametrize("fmt", ["q4K", "q5K", "q6K"])
 def test_gemv_row_result_independent_of_m(fmt):
     # the pages' tiled kernels are bit-identical to the single-row kernel;
     # here activation row i must give the same bits at every m
@@ -72,13 +72,15 @@ def test_gemv_row_result_independent_of_m(fmt):
         np.testing.assert_array_equal(y1[0], y8[i])
 
 
-@pytest.mark.parametrize("fmt", ["q4K", "q6K"])
+@pytest.mark.parametrize("fmt", ["q4K", "q5K", "q6K"])
 def test_gemv_adversarial_extremes(fmt):
     # all codes at the extremes: largest integer sums the formats allow
-    from tests.packers import pack_q4K, pack_q6K
+    from tests.packers import pack_q4K, pack_q5K, pack_q6K
     k, n, m = 1024, 8, 2
     if fmt == "q4K":
         blk = pack_q4K(2e-3, 2e-3, [63] * 8, [63] * 8, np.full(256, 15))
+    elif fmt == "q5K":
+        blk = pack_q5K(2e-3, 2e-3, [63] * 8, [63] * 8, np.full(256, 31))
     else:
         blk = pack_q6K(2e-3, [-64] * 16, np.zeros(256, dtype=np.int64))
     w = np.tile(blk, n * k // 256).reshape(n, -1)
@@ -92,7 +94,7 @@ def test_gemv_adversarial_extremes(fmt):
 
 # --------------------------------------------------------------- GEMM
 
-@pytest.mark.parametrize("fmt", ["q4K", "q6K"])
+@pytest.mark.parametrize("fmt", ["q4K", "q5K", "q6K"])
 @pytest.mark.parametrize("m,n,k", [(9, 50, 1024), (17, 33, 256), (64, 128, 2048), (130, 70, 512),
                                    (128, 128, 256), (200, 300, 1536), (512, 1024, 1024), (257, 129, 4096)])
 def test_gemm_matches_oracle(fmt, m, n, k):
@@ -103,7 +105,7 @@ def test_gemm_matches_oracle(fmt, m, n, k):
     assert_close(y, ref, S)
 
 
-@pytest.mark.parametrize("fmt", ["q4K", "q6K"])
+@pytest.mark.parametrize("fmt", ["q4K", "q5K", "q6K"])
 def test_gemm_agrees_with_gemv_small_m(fmt):
     n, k = 96, 1024
     w = make_weights(fmt, 14, 0, n, k)
@@ -118,7 +120,7 @@ def test_gemm_agrees_with_gemv_small_m(fmt):
 
 # ------------------------------------------------------- grouped GEMV
 
-@pytest.mark.parametrize("fmt", ["q4K", "q6K"])
+@pytest.mark.parametrize("fmt", ["q4K", "q5K", "q6K"])
 @pytest.mark.parametrize("m", [1, 3, 8])
 def test_grouped_gemv_equals_single_calls(fmt, m):
     import torch
@@ -147,7 +149,7 @@ def test_no_device_fault_recorded():
     assert q.plm_device_fault() == 0
 
 
-@pytest.mark.parametrize("fmt", ["q4K", "q6K"])
+@pytest.mark.parametrize("fmt", ["q4K", "q5K", "q6K"])
 def test_gemm_with_caller_workspace_matches(fmt):
     import torch
     import quant_packed_gemv_gb300 as q
