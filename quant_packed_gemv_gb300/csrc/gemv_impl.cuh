@@ -1,7 +1,9 @@
-// Decode GEMV for m = 1..8 activation rows over packed q4_K / q6_K weights
-// (PocketLLM "What it runs": K-quant weights decoded inside the kernel,
-// never widened; the weight stream is read once for all m activation rows,
-// as the pages' 8-row activation tile does on the CPU).
+// Decode GEMV for m = 1..8 activation rows over packed q6_K weights (the
+// output head; PocketLLM "What it runs": K-quant weights decoded inside the
+// kernel, never widened; the weight stream is read once for all m activation
+// rows, as the pages' 8-row activation tile does on the CPU).  q4_K and q5_K
+// take the one-lane-per-block kernel of gemv_q4K.cuh; the problem and batch
+// descriptors and the stage geometry here are shared with it.
 //
 // One launch serves a group of independent problems {w, xq, y, n, k} that
 // share m (a single GEMV is a group of one).  The weight bytes of all
@@ -13,17 +15,15 @@
 // Each warp streams its rows (one contiguous byte range of W) through its
 // own ring of shared-memory stages filled by 1-D bulk copies
 // (cp.async.bulk, completion counted on one mbarrier per stage).  A stage
-// holds whole rows when a row is small, else a 32-block (q4_K) or
-// 16-block (q6_K) chunk of one row.  The
-// first copies of a segment are issued before the CTA stages that
+// holds whole rows when a row is small, else a 16-block chunk of one row.
+// The first copies of a segment are issued before the CTA stages that
 // segment's activations, so the two overlap.  Every wait is bounded; a wait
 // that runs out records a fault and the warp stops computing (it still
 // takes part in every CTA barrier).
 //
 // Four lanes share one 256-weight block, so a warp handles eight blocks per
-// step.  A q4_K lane owns one 64-weight chunk (sub-blocks 2c, 2c+1); a q6_K
-// lane owns four whole 16-weight groups.  Per block and activation row a
-// lane forms exact integer dots with dp4a, applies the sub-block scales in
+// step; a lane owns four whole 16-weight groups.  Per block and activation
+// row a lane forms exact integer dots with dp4a, applies the group scales in
 // int32 and adds one f32 term.  When nb divides 8, one step covers 8/nb
 // whole rows and each row is reduced over its own 4*nb lanes; otherwise a
 // row takes ceil(nb/8) steps and is reduced over the warp.  The f32 order
@@ -52,13 +52,6 @@ constexpr int GEMV_WARPS = 16;
 constexpr int GROUP_MAX = 256;         // problems per grouped launch
 
 template <int FMT> struct Fmt;
-template <> struct Fmt<4> {
-    static constexpr int BYTES = Q4K_BYTES;
-    static constexpr int CHUNK = 32;                           // blocks per stage in row-chunk mode
-    static constexpr int PAYLOAD = CHUNK * Q4K_BYTES;          // 4608
-    static constexpr int SLOT = PAYLOAD;                       // blocks stay 16-byte aligned
-    static constexpr int SUB = 8;                              // sub-dots per block
-};
 template <> struct Fmt<6> {
     static constexpr int BYTES = Q6K_BYTES;
     static constexpr int CHUNK = 16;
@@ -83,7 +76,6 @@ struct GemvBatch {
     int count;
     int nstages;            // ring depth per warp
     int act_bytes;          // 128-aligned size of the staged-activation region
-    int act_all;            // q4_K lane kernel: 1 = all segments staged at kernel start
     GemvProblem p[MAXP];
 };
 
@@ -118,7 +110,6 @@ __device__ __forceinline__ StageGeom stage_geom(int row, int b0, int wb, int rps
 }
 
 // The activation values one lane needs for one block of one activation row:
-//   q4_K lane t: chunks 4t..4t+3 (codes 64t .. 64t+64), bsums 4t..4t+3
 //   q6_K lane (h, p): chunks 8h+2qq+p for qq = 0..3, bsums 8h+2qq+p
 // bw[0] packs the first two bsums (low half first), bw[1] the last two.
 struct LaneAct {
@@ -127,24 +118,11 @@ struct LaneAct {
     float dy;
 };
 
-// q4_K: the two bsum pairs of a chunk as 16-bit halves, (bs0+bs1) | (bs2+bs3) << 16
-__device__ __forceinline__ int q4K_pair_sums(const LaneAct& A) {
-    const int s0 = (int)(int16_t)(A.bw[0] & 0xFFFF) + (A.bw[0] >> 16);
-    const int s1 = (int)(int16_t)(A.bw[1] & 0xFFFF) + (A.bw[1] >> 16);
-    return (s0 & 0xFFFF) | (s1 << 16);
-}
-
 template <int FMT>
 __device__ __forceinline__ LaneAct act_from_smem(const ActSmem& a, int blk, int t) {
     LaneAct r;
     r.dy = a.dy[blk];
-    if constexpr (FMT == 4) {
-#pragma unroll
-        for (int u = 0; u < 4; ++u) r.x[u] = *act_chunk<4>(a, blk, 4 * t + u);
-        const int2 v = *reinterpret_cast<const int2*>(a.bs + (size_t)blk * 16 + 4 * t);
-        r.bw[0] = v.x;
-        r.bw[1] = v.y;
-    } else {
+    {
         const int h = t >> 1, p = t & 1;
 #pragma unroll
         for (int qq = 0; qq < 4; ++qq) r.x[qq] = *act_chunk<6>(a, blk, 8 * h + 2 * qq + p);
@@ -167,15 +145,7 @@ __device__ __forceinline__ LaneAct act_from_global(const uint8_t* __restrict__ x
     r.dy = __ldg(reinterpret_cast<const float*>(base));
     const uint32_t* qs = reinterpret_cast<const uint32_t*>(base + 4);
     const uint32_t* bsw = reinterpret_cast<const uint32_t*>(base + 260);
-    if constexpr (FMT == 4) {
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const uint32_t* c = qs + 4 * (4 * t + u);
-            r.x[u] = make_int4((int)__ldg(c), (int)__ldg(c + 1), (int)__ldg(c + 2), (int)__ldg(c + 3));
-        }
-        r.bw[0] = (int)__ldg(bsw + 2 * t);
-        r.bw[1] = (int)__ldg(bsw + 2 * t + 1);
-    } else {
+    {
         const int h = t >> 1, p = t & 1;
         int g[4];
 #pragma unroll
@@ -194,34 +164,6 @@ __device__ __forceinline__ LaneAct act_from_global(const uint8_t* __restrict__ x
 
 __device__ __forceinline__ int lo16(int w) { return (int)(int16_t)(w & 0xFFFF); }
 __device__ __forceinline__ int hi16(int w) { return w >> 16; }
-
-// One q4_K block: lane t = chunk c.  Adds its f32 contribution to v[] or
-// writes the exact sub-dots of sub-blocks 2c, 2c+1.
-template <int M, bool SUBDOTS>
-__device__ __forceinline__ void q4K_block(const uint8_t* blk, const LaneAct* act, const int* bsp, int b, int t,
-                                          const Q4KScaleSel& sel, float* v, int32_t* sub_row,
-                                          size_t sub_stride_i) {
-    const uint4 hdr = *reinterpret_cast<const uint4*>(blk);
-    const uint4 q0 = *reinterpret_cast<const uint4*>(blk + 16 + 32 * t);
-    const uint4 q1 = *reinterpret_cast<const uint4*>(blk + 32 + 32 * t);
-    const Q4KLane L = q4K_lane_decode(hdr, q0, q1, sel);
-#pragma unroll
-    for (int i = 0; i < M; ++i) {
-        const LaneAct& A = act[i];
-        int dlo, dhi;
-        q4K_lane_dots(L, &A.x[0], &A.x[2], dlo, dhi);
-        if constexpr (SUBDOTS) {
-            int32_t* o = sub_row + i * sub_stride_i + (size_t)b * 8 + 2 * t;
-            o[0] = dlo;
-            o[1] = dhi;
-        } else {
-            const int isum = L.sc0 * dlo + L.sc1 * dhi;
-            const int msum = dp2a_lo_su(bsp[i], L.m01, 0);
-            const float tt = __fmaf_rn(L.d, (float)isum, -__fmul_rn(L.dmin, (float)msum));
-            v[i] = __fmaf_rn(A.dy, tt, v[i]);
-        }
-    }
-}
 
 // One q6_K block at an even offset of the slot: lane t = (h, p).
 template <int M, bool SUBDOTS>
@@ -254,12 +196,8 @@ __device__ __forceinline__ void q6K_block(const uint8_t* slot, int off, const La
 // One block of the register path: adds this lane's f32 term of the block at
 // byte offset off of the stage to v[] (same arithmetic as the staged path).
 template <int FMT, int M>
-__device__ __forceinline__ void areg_block(const uint8_t* slot, int off, const LaneAct* act, const int* bsp, int t,
-                                           const Q4KScaleSel& sel, float* v) {
-    if constexpr (FMT == 4)
-        q4K_block<M, false>(slot + off, act, bsp, 0, t, sel, v, nullptr, 0);
-    else
-        q6K_block<M, false>(slot, off, act, 0, t, v, nullptr, 0);
+__device__ __forceinline__ void areg_block(const uint8_t* slot, int off, const LaneAct* act, int t, float* v) {
+    q6K_block<M, false>(slot, off, act, 0, t, v, nullptr, 0);
 }
 
 // AREG: each lane keeps the activations of its (at most two) block columns
@@ -274,7 +212,6 @@ __global__ void __launch_bounds__(WARPS * 32, 1) gemv_kernel(const __grid_consta
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int quad = lane >> 2, t = lane & 3;
-    const Q4KScaleSel sel = q4K_scale_sel(t);
     const int NS = B.nstages;
     uint8_t* ring = smem + B.act_bytes + (size_t)warp * NS * SLOT;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + B.act_bytes + (size_t)WARPS * NS * SLOT) + warp * NS;
@@ -347,7 +284,6 @@ __global__ void __launch_bounds__(WARPS * 32, 1) gemv_kernel(const __grid_consta
         const bool packed = nb <= BLOCKS_PER_STEP && (BLOCKS_PER_STEP % nb) == 0;
         ActSmem act{};
         LaneAct areg[AREG ? 2 : 1][M];
-        int absp[AREG ? 2 : 1][M];
         // register path geometry: packed rows -> row slot jrow, column quad % nb;
         // otherwise columns quad and quad + 8, clamped to the row (a clamped
         // column's result is discarded)
@@ -359,10 +295,8 @@ __global__ void __launch_bounds__(WARPS * 32, 1) gemv_kernel(const __grid_consta
 #pragma unroll
                 for (int i = 0; i < M; ++i) {
                     areg[0][i] = act_from_global<FMT>(P.xq, i * nb + col0, t);
-                    absp[0][i] = q4K_pair_sums(areg[0][i]);
                     if (!packed) {
                         areg[1][i] = act_from_global<FMT>(P.xq, i * nb + col1, t);
-                        absp[1][i] = q4K_pair_sums(areg[1][i]);
                     }
                 }
             }
@@ -379,21 +313,13 @@ __global__ void __launch_bounds__(WARPS * 32, 1) gemv_kernel(const __grid_consta
         for (int i = 0; i < M; ++i) acc[i] = 0.0f;
         int crow = wa, cb0 = 0;
 
-        // processes block bb of row rr of the slot; jreg selects the register column
+        // processes block bb of row rr of the slot (activation column b)
         auto do_block = [&](uint8_t* slot, const StageGeom& g, int rr, int bb, int b, float* v,
                             int32_t* sub_row) {
             LaneAct la[M];
-            int lbsp[M];
 #pragma unroll
-            for (int i = 0; i < M; ++i) {
-                la[i] = act_from_smem<FMT>(act, i * nb + b, t);
-                lbsp[i] = q4K_pair_sums(la[i]);
-            }
-            const int off = g.delta + (rr * nb + bb) * BYTES;
-            if constexpr (FMT == 4)
-                q4K_block<M, SUBDOTS>(slot + off, la, lbsp, b, t, sel, v, sub_row, sub_stride_i);
-            else
-                q6K_block<M, SUBDOTS>(slot, off, la, b, t, v, sub_row, sub_stride_i);
+            for (int i = 0; i < M; ++i) la[i] = act_from_smem<FMT>(act, i * nb + b, t);
+            q6K_block<M, SUBDOTS>(slot, g.delta + (rr * nb + bb) * BYTES, la, b, t, v, sub_row, sub_stride_i);
         };
 
         for (int s = 0; s < nst && ok; ++s) {
@@ -428,8 +354,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1) gemv_kernel(const __grid_consta
 #pragma unroll
                             for (int i = 0; i < M; ++i) v[u][i] = 0.0f;
                             const int rr = min(r0 + jrow + u * rw, nr - 1);
-                            areg_block<FMT, M>(slot, g.delta + (rr * nb + col0) * BYTES, areg[0], absp[0], t, sel,
-                                               v[u]);
+                            areg_block<FMT, M>(slot, g.delta + (rr * nb + col0) * BYTES, areg[0], t, v[u]);
                         }
 #pragma unroll
                         for (int o = 16; o >= 1; o >>= 1) {
@@ -463,12 +388,10 @@ __global__ void __launch_bounds__(WARPS * 32, 1) gemv_kernel(const __grid_consta
                             float a0[M], a1[M];
 #pragma unroll
                             for (int i = 0; i < M; ++i) a0[i] = 0.0f;
-                            areg_block<FMT, M>(slot, g.delta + (rr * nb + col0) * BYTES, areg[0], absp[0], t, sel,
-                                               a0);
+                            areg_block<FMT, M>(slot, g.delta + (rr * nb + col0) * BYTES, areg[0], t, a0);
 #pragma unroll
                             for (int i = 0; i < M; ++i) a1[i] = a0[i];
-                            areg_block<FMT, M>(slot, g.delta + (rr * nb + col1) * BYTES, areg[1], absp[1], t, sel,
-                                               a1);
+                            areg_block<FMT, M>(slot, g.delta + (rr * nb + col1) * BYTES, areg[1], t, a1);
 #pragma unroll
                             for (int i = 0; i < M; ++i) v[u][i] = has1 ? a1[i] : (has0 ? a0[i] : 0.0f);
                         }
@@ -618,7 +541,7 @@ cudaError_t launch_batch(const HostProblem* hp, int count, int max_nb, int ns, c
 // Launches one pass (all problems share m = M rows of activations).
 template <int FMT, int M, bool SUB>
 cudaError_t launch_pass(const HostProblem* hp, int count, int max_nb, cudaStream_t stream) {
-    if constexpr (!SUB && M <= (FMT == 4 ? 2 : 1)) {
+    if constexpr (!SUB && M <= 1) {
         // activations in registers: rows of at most 16 blocks (q6_K: m = 1 only,
         // the register budget of two activation rows is exceeded)
         if (max_nb <= 16) {

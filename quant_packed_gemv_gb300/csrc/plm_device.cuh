@@ -95,10 +95,7 @@ __device__ __forceinline__ void act_smem_fill(const ActSmem& a, const uint8_t* _
 }
 
 // ---------------------------------------------------------------------------
-// q4_K, one block handled by 4 lanes.  Lane c (0..3) owns the 64-weight
-// chunk c: qs bytes [32c, 32c+32).  Byte 32c+l holds weight 64c+l in its low
-// nibble (sub-block 2c) and weight 64c+32+l in its high nibble (sub-block
-// 2c+1), l = 0..31.
+// Mixed-sign integer dot products used by the block decoders.
 // ---------------------------------------------------------------------------
 
 // Mixed-sign 4-way byte dot: unsigned bytes of a times signed bytes of b.
@@ -113,65 +110,6 @@ __device__ __forceinline__ int dp2a_lo_su(int a, uint32_t b, int c) {
     int d;
     asm("dp2a.lo.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
     return d;
-}
-
-// Per-lane constants of the 6-bit scale/min table decode for chunk c:
-// pairs 0..3 sit in the low six bits of scale bytes 0..3 (scales) and 4..7
-// (mins); pairs 4..7 take their low four bits from the nibbles of bytes
-// 8..11 and their top two bits from bits 6-7 of bytes 0..7.
-struct Q4KScaleSel {
-    uint32_t mask_lo, mask_hi;   // 0x3F3F3F3F, 0 (c < 2) or 0x0F0F0F0F, 0x30303030 (c >= 2)
-    int pick_w;                  // c >= 2: take the low bits from scale bytes 8..11
-    int sh;                      // bit offset of pair 2c (mod 4) in the selected word
-};
-
-__device__ __forceinline__ Q4KScaleSel q4K_scale_sel(int c) {
-    Q4KScaleSel s;
-    s.pick_w = c >= 2;
-    s.mask_lo = s.pick_w ? 0x0F0F0F0Fu : 0x3F3F3F3Fu;
-    s.mask_hi = s.pick_w ? 0x30303030u : 0u;
-    s.sh = 16 * (c & 1);
-    return s;
-}
-
-struct Q4KLane {
-    float d, dmin;
-    int sc0, sc1;        // scales of sub-blocks 2c and 2c+1
-    uint32_t m01;        // mins of sub-blocks 2c, 2c+1 in bytes 0, 1
-    uint32_t q[8];       // the chunk's 32 code bytes (low nibble: sub-block 2c, high: 2c+1)
-};
-
-// hdr: bytes 0..15 of the block (d, dmin, scales[12]);
-// q0, q1: qs[32c .. 32c+16) and qs[32c+16 .. 32c+32)
-__device__ __forceinline__ Q4KLane q4K_lane_decode(uint4 hdr, uint4 q0, uint4 q1, const Q4KScaleSel& S) {
-    Q4KLane L;
-    L.d = half_bits_to_float(hdr.x);
-    L.dmin = half_bits_to_float(hdr.x >> 16);
-    const uint32_t scw = ((S.pick_w ? hdr.w : hdr.y) & S.mask_lo) | ((hdr.y >> 2) & S.mask_hi);
-    const uint32_t mw = ((S.pick_w ? (hdr.w >> 4) : hdr.z) & S.mask_lo) | ((hdr.z >> 2) & S.mask_hi);
-    L.sc0 = (scw >> S.sh) & 0xFF;
-    L.sc1 = (scw >> (S.sh + 8)) & 0xFF;
-    L.m01 = mw >> S.sh;
-    L.q[0] = q0.x; L.q[1] = q0.y; L.q[2] = q0.z; L.q[3] = q0.w;
-    L.q[4] = q1.x; L.q[5] = q1.y; L.q[6] = q1.z; L.q[7] = q1.w;
-    return L;
-}
-
-// Exact integer dots of sub-blocks 2c (against the activation codes at
-// 64c .. 64c+32, words xl) and 2c+1 (64c+32 .. 64c+64, words xh).  The high
-// nibbles are used in place (16 * q), so their dot is divided by 16, exactly.
-__device__ __forceinline__ void q4K_lane_dots(const Q4KLane& L, const int4 xlo[2], const int4 xhi[2],
-                                              int& dlo, int& dhi) {
-    const int xl[8] = {xlo[0].x, xlo[0].y, xlo[0].z, xlo[0].w, xlo[1].x, xlo[1].y, xlo[1].z, xlo[1].w};
-    const int xh[8] = {xhi[0].x, xhi[0].y, xhi[0].z, xhi[0].w, xhi[1].x, xhi[1].y, xhi[1].z, xhi[1].w};
-    int lo = 0, hi = 0;
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-        lo = dp4a_us(L.q[u] & 0x0F0F0F0Fu, xl[u], lo);
-        hi = dp4a_us(L.q[u] & 0xF0F0F0F0u, xh[u], hi);
-    }
-    dlo = lo;
-    dhi = hi >> 4;
 }
 
 // ---------------------------------------------------------------------------
