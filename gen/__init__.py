@@ -19,6 +19,8 @@ _LIB = os.path.join(_OUT_DIR, "libplmgen.so")
 
 Q4K_BYTES = 144
 Q5K_BYTES = 176
+Q2K_BYTES = 84
+Q3K_BYTES = 110
 Q6K_BYTES = 210
 QK = 256
 
@@ -45,7 +47,8 @@ def _load():
     if _lib is None:
         lib = ctypes.CDLL(build())
         u64, i64, vp = ctypes.c_uint64, ctypes.c_int64, ctypes.c_void_p
-        for name in ("plmgen_q4K", "plmgen_q5K", "plmgen_q6K", "plmgen_normal_f32", "plmgen_raw"):
+        for name in ("plmgen_q2K", "plmgen_q3K", "plmgen_q4K", "plmgen_q5K", "plmgen_q6K", "plmgen_normal_f32",
+                     "plmgen_raw"):
             fn = getattr(lib, name)
             fn.argtypes = [u64, u64, i64, i64, vp]
             fn.restype = None
@@ -66,6 +69,26 @@ def q4K_blocks(seed, stream, n, k, row0=0, out=None):
     assert out.flags.c_contiguous and out.nbytes == n * nb * Q4K_BYTES
     _load().plmgen_q4K(seed, stream, row0 * nb, n * nb, _ptr(out))
     return out
+
+
+def _blocks(fn, bpb, seed, stream, n, k, row0, out):
+    assert k % QK == 0
+    nb = k // QK
+    if out is None:
+        out = np.empty((n, nb * bpb), dtype=np.uint8)
+    assert out.flags.c_contiguous and out.nbytes == n * nb * bpb
+    getattr(_load(), fn)(seed, stream, row0 * nb, n * nb, _ptr(out))
+    return out
+
+
+def q2K_blocks(seed, stream, n, k, row0=0, out=None):
+    """Rows [row0, row0+n) of a q2_K matrix as uint8 [n, k/256*84]."""
+    return _blocks("plmgen_q2K", Q2K_BYTES, seed, stream, n, k, row0, out)
+
+
+def q3K_blocks(seed, stream, n, k, row0=0, out=None):
+    """Rows [row0, row0+n) of a q3_K matrix as uint8 [n, k/256*110]."""
+    return _blocks("plmgen_q3K", Q3K_BYTES, seed, stream, n, k, row0, out)
 
 
 def q5K_blocks(seed, stream, n, k, row0=0, out=None):

@@ -11,6 +11,10 @@
  *          likewise uniform qs bytes give nibbles i.i.d. U{0..15}.
  *   q5_K : as q4_K, plus 32 uniform qh bytes (the fifth bit of each weight),
  *          so q5 ~ U{0..31}.
+ *   q2_K : d, dmin as q4_K; scales[16] and qs[64] uniform bytes (4-bit scales
+ *          and mins ~ U{0..15}, 2-bit codes ~ U{0..3}).
+ *   q3_K : d as q4_K; hmask[32], qs[64] and scales[12] uniform bytes (3-bit
+ *          codes ~ U{0..7} before the offset, 6-bit scales ~ U{0..63}).
  *   q6_K : d ~ U(1e-4, 2e-3) rounded to f16; ql[128] and qh[64] uniform bytes
  *          (a bijection onto 256 six-bit values, so q6 ~ U{0..63});
  *          scales i8 ~ U{-64..63}.
@@ -27,6 +31,10 @@
  *   q4_K: 20 draws from 20*b.  draw 0 -> d, draw 1 -> dmin, draws 2..19 give
  *         8 bytes each (little-endian) for scales[12] then qs[128]
  *         (140 bytes used, 4 dropped).
+ *   q2_K: 12 draws from 12*b.  draw 0 -> d, draw 1 -> dmin, draws 2..11 give
+ *         scales[16] then qs[64].
+ *   q3_K: 15 draws from 15*b.  draw 0 -> d, draws 1..14 give hmask[32],
+ *         qs[64] then scales[12].
  *   q5_K: 24 draws from 24*b.  draw 0 -> d, draw 1 -> dmin, draws 2..23 give
  *         8 bytes each for scales[12], qh[32] then qs[128] (172 bytes used).
  *   q6_K: 27 draws from 27*b.  draw 0 -> d, draws 1..24 give ql[128] then
@@ -94,6 +102,27 @@ void plmgen_q4K(uint64_t seed, uint64_t stream, int64_t block0, int64_t nblocks,
         put_u16(blk + 2, draw_scale_half(draw(s, base + 1)));
         bytes_from_draws(s, base + 2, raw, 140);
         memcpy(blk + 4, raw, 140);
+    }
+}
+
+void plmgen_q2K(uint64_t seed, uint64_t stream, int64_t block0, int64_t nblocks, uint8_t* out) {
+    uint64_t s = stream_start(seed, stream);
+    for (int64_t b = 0; b < nblocks; ++b) {
+        uint64_t base = (uint64_t)(block0 + b) * 12u;
+        uint8_t* blk = out + b * 84;
+        bytes_from_draws(s, base + 2, blk, 80);               /* scales[16], qs[64] */
+        put_u16(blk + 80, draw_scale_half(draw(s, base + 0)));
+        put_u16(blk + 82, draw_scale_half(draw(s, base + 1)));
+    }
+}
+
+void plmgen_q3K(uint64_t seed, uint64_t stream, int64_t block0, int64_t nblocks, uint8_t* out) {
+    uint64_t s = stream_start(seed, stream);
+    for (int64_t b = 0; b < nblocks; ++b) {
+        uint64_t base = (uint64_t)(block0 + b) * 15u;
+        uint8_t* blk = out + b * 110;
+        bytes_from_draws(s, base + 1, blk, 108);              /* hmask[32], qs[64], scales[12] */
+        put_u16(blk + 108, draw_scale_half(draw(s, base + 0)));
     }
 }
 

@@ -27,6 +27,8 @@ _LIB = os.path.join(_OUT_DIR, "libplmref.so")
 QK = 256
 Q4K_BYTES = 144
 Q5K_BYTES = 176
+Q2K_BYTES = 84
+Q3K_BYTES = 110
 Q6K_BYTES = 210
 Q8K_BYTES = 292
 
@@ -57,12 +59,15 @@ def _load():
         sig6 = [vp, vp, vp, i64, i64, i64]
         for name in ("plm_ref_subdots_q4K", "plm_ref_subdots_q5K", "plm_ref_subdots_q6K",
                      "plm_ref_gemm_q5K_f64", "plm_ref_gemm_q5K_f32", "plm_ref_absscale_q5K",
+                     "plm_ref_subdots_q2K", "plm_ref_gemm_q2K_f64", "plm_ref_gemm_q2K_f32", "plm_ref_absscale_q2K",
+                     "plm_ref_subdots_q3K", "plm_ref_gemm_q3K_f64", "plm_ref_gemm_q3K_f32", "plm_ref_absscale_q3K",
                      "plm_ref_gemm_q4K_f64", "plm_ref_gemm_q4K_f32",
                      "plm_ref_gemm_q6K_f64", "plm_ref_gemm_q6K_f32",
                      "plm_ref_absscale_q4K", "plm_ref_absscale_q6K"):
             getattr(lib, name).argtypes = sig6
             getattr(lib, name).restype = None
-        for name in ("plm_ref_dequant_q4K", "plm_ref_dequant_q5K", "plm_ref_dequant_q6K", "plm_ref_dequant_q8K"):
+        for name in ("plm_ref_dequant_q2K", "plm_ref_dequant_q3K", "plm_ref_dequant_q4K", "plm_ref_dequant_q5K",
+                     "plm_ref_dequant_q6K", "plm_ref_dequant_q8K"):
             getattr(lib, name).argtypes = [vp, vp, i64, i64]
             getattr(lib, name).restype = None
         lib.plm_ref_quantize_q8K.argtypes = [vp, vp, i64, i64]
@@ -72,6 +77,8 @@ def _load():
         lib.plm_ref_q4K_scale_min.argtypes = [vp, ctypes.c_int, ctypes.POINTER(ctypes.c_int),
                                               ctypes.POINTER(ctypes.c_int)]
         lib.plm_ref_q4K_scale_min.restype = None
+        lib.plm_ref_q3K_scale.argtypes = [vp, ctypes.c_int]
+        lib.plm_ref_q3K_scale.restype = ctypes.c_int
         lib.plm_ref_swiglu_f64.argtypes = [vp, vp, vp, i64]
         lib.plm_ref_swiglu_f64.restype = None
         lib.plm_ref_set_threads.argtypes = [ctypes.c_int]
@@ -136,6 +143,58 @@ def _call6(name, w, xq, m, n, k, shape, dtype):
 def subdots_q4K(w, xq, m, n, k):
     """int32 [m, n, k/256*8]: per 32-weight sub-block integer dots."""
     return _call6("plm_ref_subdots_q4K", w, xq, m, n, k, (m, n, k // QK * 8), np.int32)
+
+
+def _dequant(name, w, n, k):
+    w = _u8(w)
+    out = np.empty((n, k), dtype=np.float64)
+    getattr(_load(), name)(_p(w), _p(out), n, k)
+    return out
+
+
+def subdots_q2K(w, xq, m, n, k):
+    return _call6("plm_ref_subdots_q2K", w, xq, m, n, k, (m, n, k // 16), np.int32)
+
+
+def subdots_q3K(w, xq, m, n, k):
+    return _call6("plm_ref_subdots_q3K", w, xq, m, n, k, (m, n, k // 16), np.int32)
+
+
+def gemm_q2K_f64(w, xq, m, n, k):
+    return _call6("plm_ref_gemm_q2K_f64", w, xq, m, n, k, (m, n), np.float64)
+
+
+def gemm_q2K_f32(w, xq, m, n, k):
+    return _call6("plm_ref_gemm_q2K_f32", w, xq, m, n, k, (m, n), np.float32)
+
+
+def gemm_q3K_f64(w, xq, m, n, k):
+    return _call6("plm_ref_gemm_q3K_f64", w, xq, m, n, k, (m, n), np.float64)
+
+
+def gemm_q3K_f32(w, xq, m, n, k):
+    return _call6("plm_ref_gemm_q3K_f32", w, xq, m, n, k, (m, n), np.float32)
+
+
+def absscale_q2K(w, xq, m, n, k):
+    return _call6("plm_ref_absscale_q2K", w, xq, m, n, k, (m, n), np.float64)
+
+
+def absscale_q3K(w, xq, m, n, k):
+    return _call6("plm_ref_absscale_q3K", w, xq, m, n, k, (m, n), np.float64)
+
+
+def dequant_q2K(w, n, k):
+    return _dequant("plm_ref_dequant_q2K", w, n, k)
+
+
+def dequant_q3K(w, n, k):
+    return _dequant("plm_ref_dequant_q3K", w, n, k)
+
+
+def q3K_scale(table12, g):
+    t = _u8(np.asarray(table12, dtype=np.uint8))
+    return _load().plm_ref_q3K_scale(_p(t), g)
 
 
 def subdots_q5K(w, xq, m, n, k):

@@ -565,3 +565,209 @@ void plm_ref_absscale_q5K(const uint8_t* w, const uint8_t* xq, double* S,
             }
         }
 }
+
+/* ------------------------------------------------------------------ */
+/* q2_K and q3_K (the lower rungs of the width ladder), public GGML    */
+/* layouts.  Both use sixteen 16-weight groups; group g holds weights  */
+/* 16g .. 16g+15 and, with h = g/8, j = (g%8)/2, p = g%2, its codes    */
+/* sit in bits 2j, 2j+1 of qs[32h + 16p + l], l = 0..15.               */
+/*   q2_K (84 B): u8 scales[16] (low nibble scale, high nibble min),   */
+/*        u8 qs[64], f16 d, f16 dmin; weight = d*sc_g*q - dmin*m_g.    */
+/*   q3_K (110 B): u8 hmask[32], u8 qs[64], u8 scales[12], f16 d; the  */
+/*        third bit of weight 16g+l is bit 4h+j of hmask[16p+l]; code  */
+/*        q3 = q2 - 4 when that bit is clear, else q2 (-4..3); the     */
+/*        6-bit scale of group g takes its low 4 bits from             */
+/*        scales[g%8] (nibble g/8) and its top 2 bits from bits        */
+/*        2(g/4)..2(g/4)+1 of scales[8 + g%4]; weight = d*(s_g-32)*q3. */
+/* ------------------------------------------------------------------ */
+#define Q2K_BYTES 84
+#define Q3K_BYTES 110
+
+static int k2_code(const uint8_t* qs, int w) {
+    int g = w / 16, l = w % 16, h = g / 8, j = (g % 8) / 2, p = g % 2;
+    return (qs[32 * h + 16 * p + l] >> (2 * j)) & 3;
+}
+
+int plm_ref_q3K_scale(const uint8_t* sc12, int g) {
+    int low4 = (sc12[g % 8] >> (4 * (g / 8))) & 15;
+    int high2 = (sc12[8 + g % 4] >> (2 * (g / 4))) & 3;
+    return low4 | (high2 << 4);
+}
+
+static int k3_code(const uint8_t* wb, int w) {
+    int g = w / 16, l = w % 16, h = g / 8, j = (g % 8) / 2, p = g % 2;
+    int hbit = (wb[16 * p + l] >> (4 * h + j)) & 1;
+    return k2_code(wb + 32, w) - (hbit ? 0 : 4);
+}
+
+static void q2K_block_dots(const uint8_t* wb, const int8_t* q8, int32_t dots[16]) {
+    for (int g = 0; g < 16; ++g) {
+        int32_t s = 0;
+        for (int l = 0; l < 16; ++l) s += k2_code(wb + 16, 16 * g + l) * q8[16 * g + l];
+        dots[g] = s;
+    }
+}
+
+static void q3K_block_dots(const uint8_t* wb, const int8_t* q8, int32_t dots[16]) {
+    for (int g = 0; g < 16; ++g) {
+        int32_t s = 0;
+        for (int l = 0; l < 16; ++l) s += k3_code(wb, 16 * g + l) * q8[16 * g + l];
+        dots[g] = s;
+    }
+}
+
+void plm_ref_subdots_q2K(const uint8_t* w, const uint8_t* xq, int32_t* out, int64_t m, int64_t n, int64_t k) {
+    int64_t nb = k / QK;
+    for (int64_t i = 0; i < m; ++i)
+        for (int64_t r = 0; r < n; ++r)
+            for (int64_t b = 0; b < nb; ++b)
+                q2K_block_dots(w + (r * nb + b) * Q2K_BYTES, (const int8_t*)(xq + (i * nb + b) * Q8K_BYTES + 4),
+                               out + ((i * n + r) * nb + b) * 16);
+}
+
+void plm_ref_subdots_q3K(const uint8_t* w, const uint8_t* xq, int32_t* out, int64_t m, int64_t n, int64_t k) {
+    int64_t nb = k / QK;
+    for (int64_t i = 0; i < m; ++i)
+        for (int64_t r = 0; r < n; ++r)
+            for (int64_t b = 0; b < nb; ++b)
+                q3K_block_dots(w + (r * nb + b) * Q3K_BYTES, (const int8_t*)(xq + (i * nb + b) * Q8K_BYTES + 4),
+                               out + ((i * n + r) * nb + b) * 16);
+}
+
+/* Block integers: q2_K isum = sum_g sc_g dot_g, msum = sum_g m_g bsum_g;
+ * q3_K isum = sum_g (s_g - 32) dot_g (no min term). */
+static void q2K_block_ints(const uint8_t* wb, const uint8_t* xb, int32_t* isum, int32_t* msum) {
+    int32_t dots[16];
+    q2K_block_dots(wb, (const int8_t*)(xb + 4), dots);
+    int32_t is = 0, ms = 0;
+    for (int g = 0; g < 16; ++g) {
+        is += (wb[g] & 15) * dots[g];
+        ms += (wb[g] >> 4) * (int32_t)load_i16(xb + 260 + 2 * g);
+    }
+    *isum = is;
+    *msum = ms;
+}
+
+static int32_t q3K_block_ints(const uint8_t* wb, const uint8_t* xb) {
+    int32_t dots[16];
+    q3K_block_dots(wb, (const int8_t*)(xb + 4), dots);
+    int32_t is = 0;
+    for (int g = 0; g < 16; ++g) is += (plm_ref_q3K_scale(wb + 96, g) - 32) * dots[g];
+    return is;
+}
+
+void plm_ref_gemm_q2K_f64(const uint8_t* w, const uint8_t* xq, double* y, int64_t m, int64_t n, int64_t k) {
+    int64_t nb = k / QK;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < n; ++r)
+        for (int64_t i = 0; i < m; ++i) {
+            double acc = 0.0;
+            for (int64_t b = 0; b < nb; ++b) {
+                const uint8_t* wb = w + (r * nb + b) * Q2K_BYTES;
+                const uint8_t* xb = xq + (i * nb + b) * Q8K_BYTES;
+                int32_t isum, msum;
+                q2K_block_ints(wb, xb, &isum, &msum);
+                double dx = (double)load_f32(xb);
+                acc += (double)load_f16(wb + 80) * dx * (double)isum - (double)load_f16(wb + 82) * dx * (double)msum;
+            }
+            y[i * n + r] = acc;
+        }
+}
+
+void plm_ref_gemm_q2K_f32(const uint8_t* w, const uint8_t* xq, float* y, int64_t m, int64_t n, int64_t k) {
+    int64_t nb = k / QK;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < n; ++r)
+        for (int64_t i = 0; i < m; ++i) {
+            float acc = 0.0f;
+            for (int64_t b = 0; b < nb; ++b) {
+                const uint8_t* wb = w + (r * nb + b) * Q2K_BYTES;
+                const uint8_t* xb = xq + (i * nb + b) * Q8K_BYTES;
+                int32_t isum, msum;
+                q2K_block_ints(wb, xb, &isum, &msum);
+                float dx = load_f32(xb);
+                acc += load_f16(wb + 80) * dx * (float)isum - load_f16(wb + 82) * dx * (float)msum;
+            }
+            y[i * n + r] = acc;
+        }
+}
+
+void plm_ref_gemm_q3K_f64(const uint8_t* w, const uint8_t* xq, double* y, int64_t m, int64_t n, int64_t k) {
+    int64_t nb = k / QK;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < n; ++r)
+        for (int64_t i = 0; i < m; ++i) {
+            double acc = 0.0;
+            for (int64_t b = 0; b < nb; ++b) {
+                const uint8_t* wb = w + (r * nb + b) * Q3K_BYTES;
+                const uint8_t* xb = xq + (i * nb + b) * Q8K_BYTES;
+                acc += (double)load_f16(wb + 108) * (double)load_f32(xb) * (double)q3K_block_ints(wb, xb);
+            }
+            y[i * n + r] = acc;
+        }
+}
+
+void plm_ref_gemm_q3K_f32(const uint8_t* w, const uint8_t* xq, float* y, int64_t m, int64_t n, int64_t k) {
+    int64_t nb = k / QK;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < n; ++r)
+        for (int64_t i = 0; i < m; ++i) {
+            float acc = 0.0f;
+            for (int64_t b = 0; b < nb; ++b) {
+                const uint8_t* wb = w + (r * nb + b) * Q3K_BYTES;
+                const uint8_t* xb = xq + (i * nb + b) * Q8K_BYTES;
+                acc += load_f16(wb + 108) * load_f32(xb) * (float)q3K_block_ints(wb, xb);
+            }
+            y[i * n + r] = acc;
+        }
+}
+
+/* Per-weight f64 dequantization (from the weight index). */
+void plm_ref_dequant_q2K(const uint8_t* w, double* out, int64_t n, int64_t k) {
+    int64_t nb = k / QK;
+    for (int64_t r = 0; r < n; ++r)
+        for (int64_t b = 0; b < nb; ++b) {
+            const uint8_t* wb = w + (r * nb + b) * Q2K_BYTES;
+            double d = load_f16(wb + 80), dmin = load_f16(wb + 82);
+            for (int t = 0; t < QK; ++t) {
+                int sb = wb[t / 16];
+                out[r * k + b * QK + t] = d * (sb & 15) * k2_code(wb + 16, t) - dmin * (sb >> 4);
+            }
+        }
+}
+
+void plm_ref_dequant_q3K(const uint8_t* w, double* out, int64_t n, int64_t k) {
+    int64_t nb = k / QK;
+    for (int64_t r = 0; r < n; ++r)
+        for (int64_t b = 0; b < nb; ++b) {
+            const uint8_t* wb = w + (r * nb + b) * Q3K_BYTES;
+            double d = load_f16(wb + 108);
+            for (int t = 0; t < QK; ++t)
+                out[r * k + b * QK + t] = d * (plm_ref_q3K_scale(wb + 96, t / 16) - 32) * k3_code(wb, t);
+        }
+}
+
+static void absscale_generic(void (*deq)(const uint8_t*, double*, int64_t, int64_t), int bpb, const uint8_t* w,
+                             const uint8_t* xq, double* S, int64_t m, int64_t n, int64_t k) {
+    int64_t nb = k / QK;
+    double wr[QK];
+    for (int64_t i = 0; i < m * n; ++i) S[i] = 0.0;
+    for (int64_t r = 0; r < n; ++r)
+        for (int64_t b = 0; b < nb; ++b) {
+            deq(w + (r * nb + b) * bpb, wr, 1, QK);
+            for (int64_t i = 0; i < m; ++i) {
+                const uint8_t* xb = xq + (i * nb + b) * Q8K_BYTES;
+                double dx = load_f32(xb), s = 0.0;
+                for (int t = 0; t < QK; ++t) s += fabs(wr[t] * dx * (double)(int8_t)xb[4 + t]);
+                S[i * n + r] += s;
+            }
+        }
+}
+
+void plm_ref_absscale_q2K(const uint8_t* w, const uint8_t* xq, double* S, int64_t m, int64_t n, int64_t k) {
+    absscale_generic(plm_ref_dequant_q2K, Q2K_BYTES, w, xq, S, m, n, k);
+}
+
+void plm_ref_absscale_q3K(const uint8_t* w, const uint8_t* xq, double* S, int64_t m, int64_t n, int64_t k) {
+    absscale_generic(plm_ref_dequant_q3K, Q3K_BYTES, w, xq, S, m, n, k);
+}

@@ -61,6 +61,57 @@ def pack_q5K(d, dmin, sc, mn, q):
     return blk
 
 
+def _k2_positions():
+    """Weight w of a q2_K/q3_K block: group g = w // 16 (h = g // 8, j = (g % 8) // 2,
+    p = g % 2), lane l = w % 16; its two low bits are bits 2j, 2j+1 of
+    qs[32h + 16p + l]; q3_K's third bit is bit 4h + j of hmask[16p + l]."""
+    w = np.arange(256)
+    g, l = w // 16, w % 16
+    h, j, p = g // 8, (g % 8) // 2, g % 2
+    return 32 * h + 16 * p + l, 2 * j, 16 * p + l, 4 * h + j
+
+
+def pack_q2K(d, dmin, sc, mn, q):
+    """d, dmin: floats (f16); sc, mn: 16 ints in 0..15; q: 256 two-bit codes."""
+    q = np.asarray(q, dtype=np.int64)
+    byte, shift, _, _ = _k2_positions()
+    qs = np.zeros(64, dtype=np.int64)
+    for w in range(256):
+        qs[byte[w]] |= (q[w] & 3) << shift[w]
+    blk = np.zeros(84, dtype=np.uint8)
+    blk[0:16] = (np.asarray(sc, dtype=np.int64) & 15) | ((np.asarray(mn, dtype=np.int64) & 15) << 4)
+    blk[16:80] = qs.astype(np.uint8)
+    blk[80:82] = np.array([d], dtype=np.float16).view(np.uint8)
+    blk[82:84] = np.array([dmin], dtype=np.float16).view(np.uint8)
+    return blk
+
+
+def pack_q3K(d, s6, q3):
+    """d: float (f16); s6: 16 six-bit scales 0..63 (the weight uses s6 - 32);
+    q3: 256 codes in -4..3 (stored as two low bits plus a third bit that is set
+    when the code is >= 0)."""
+    q3 = np.asarray(q3, dtype=np.int64)
+    s6 = [int(v) for v in s6]
+    byte, shift, hbyte, hbit = _k2_positions()
+    qs = np.zeros(64, dtype=np.int64)
+    hm = np.zeros(32, dtype=np.int64)
+    for w in range(256):
+        high = 1 if q3[w] >= 0 else 0
+        low = q3[w] if high else q3[w] + 4
+        qs[byte[w]] |= low << shift[w]
+        hm[hbyte[w]] |= high << hbit[w]
+    t = np.zeros(12, dtype=np.int64)
+    for g in range(16):
+        t[g % 8] |= (s6[g] & 15) << (4 * (g // 8))
+        t[8 + g % 4] |= ((s6[g] >> 4) & 3) << (2 * (g // 4))
+    blk = np.zeros(110, dtype=np.uint8)
+    blk[0:32] = hm.astype(np.uint8)
+    blk[32:96] = qs.astype(np.uint8)
+    blk[96:108] = t.astype(np.uint8)
+    blk[108:110] = np.array([d], dtype=np.float16).view(np.uint8)
+    return blk
+
+
 def pack_q6K(d, scales, q):
     """d: float (f16); scales: 16 ints in -128..127; q: 256 six-bit codes 0..63."""
     q = np.asarray(q, dtype=np.int64)

@@ -12,7 +12,7 @@ import pytest
 
 import gen
 import oracle
-from tests.packers import pack_q4K, pack_q5K, pack_q6K, pack_q8K
+from tests.packers import pack_q2K, pack_q3K, pack_q4K, pack_q5K, pack_q6K, pack_q8K
 
 
 def test_f16_exhaustive_against_numpy():
@@ -175,12 +175,18 @@ def test_q6K_dequant_and_dots_from_fields():
 
 # ------------------------------------------------ whole matmul, f64 check
 
-@pytest.mark.parametrize("fmt", ["q4K", "q5K", "q6K"])
+@pytest.mark.parametrize("fmt", ["q2K", "q3K", "q4K", "q5K", "q6K"])
 @pytest.mark.parametrize("seed,m,n,k", [(s, 3, 5, 256) for s in range(8)] + [(0, 4, 33, 1024), (7, 2, 9, 2048)])
 def test_integer_path_equals_f64_dequant_matmul(fmt, seed, m, n, k):
     x = gen.normal_f32(seed, 100, m, k)
     xq = oracle.quantize_q8K(x)
-    if fmt == "q5K":
+    if fmt in ("q2K", "q3K"):
+        w = getattr(gen, "%s_blocks" % fmt)(seed, 0, n, k)
+        wd = getattr(oracle, "dequant_%s" % fmt)(w, n, k)
+        y = getattr(oracle, "gemm_%s_f64" % fmt)(w, xq, m, n, k)
+        S = getattr(oracle, "absscale_%s" % fmt)(w, xq, m, n, k)
+        y32 = getattr(oracle, "gemm_%s_f32" % fmt)(w, xq, m, n, k)
+    elif fmt == "q5K":
         w = gen.q5K_blocks(seed, 0, n, k)
         wd = oracle.dequant_q5K(w, n, k)
         y, S = oracle.gemm_q5K_f64(w, xq, m, n, k), oracle.absscale_q5K(w, xq, m, n, k)
@@ -300,3 +306,114 @@ def test_q5K_generated_fields():
     # fifth bits are uniform: about half set
     bits = np.unpackbits(w[:, 16:48])
     assert abs(bits.mean() - 0.5) < 0.01
+
+
+# ------------------------------------------------------------ q2_K, q3_K
+
+
+def test_q3K_scale_table_roundtrip_all_values():
+    for g in range(16):
+        for v in range(64):
+            s6 = [(5 * g + 7 * t) % 64 for t in range(16)]
+            s6[g] = v
+            blk = pack_q3K(1.0, s6, np.zeros(256, dtype=np.int64))
+            for gg in range(16):
+                assert oracle.q3K_scale(blk[96:108], gg) == s6[gg]
+
+
+def test_q2K_single_bit_position_map():
+    seen = set()
+    for byte in range(64):
+        for bit in range(8):
+            blk = np.zeros(84, dtype=np.uint8)
+            blk[0:16] = 1                      # scales 1, mins 0
+            blk[16 + byte] = 1 << bit
+            blk[80:82] = np.array([1.0], dtype=np.float16).view(np.uint8)
+            w = oracle.dequant_q2K(blk, 1, 256)[0]
+            nz = np.nonzero(w)[0]
+            assert len(nz) == 1 and w[nz[0]] == float(1 << (bit % 2))
+            h, rest = divmod(byte, 32)
+            p, l = divmod(rest, 16)
+            j = bit // 2
+            assert nz[0] == 16 * (8 * h + 2 * j + p) + l
+            seen.add(int(nz[0]))
+    assert seen == set(range(256))
+
+
+def test_q3K_single_bit_position_maps():
+    """qs bits with every third bit set (codes = the low bits), and hmask bits
+    over all-zero low bits (codes -4 except where the bit is set: 0)."""
+    base = np.zeros(110, dtype=np.uint8)
+    base[96:108] = pack_q3K(1.0, [33] * 16, np.zeros(256, dtype=np.int64))[96:108]   # s6 = 33: scale 1
+    base[108:110] = np.array([1.0], dtype=np.float16).view(np.uint8)
+    seen = set()
+    for byte in range(64):
+        for bit in range(8):
+            blk = base.copy()
+            blk[0:32] = 0xFF
+            blk[32 + byte] = 1 << bit
+            w = oracle.dequant_q3K(blk, 1, 256)[0]
+            nz = np.nonzero(w)[0]
+            assert len(nz) == 1 and w[nz[0]] == float(1 << (bit % 2))
+            h, rest = divmod(byte, 32)
+            p, l = divmod(rest, 16)
+            assert nz[0] == 16 * (8 * h + 2 * (bit // 2) + p) + l
+            seen.add(int(nz[0]))
+    assert seen == set(range(256))
+    seen = set()
+    for byte in range(32):
+        for bit in range(8):
+            blk = base.copy()
+            blk[byte] = 1 << bit
+            w = oracle.dequant_q3K(blk, 1, 256)[0]
+            z = np.nonzero(w == 0.0)[0]
+            assert len(z) == 1 and np.all(np.delete(w, z) == -4.0)
+            p, l = divmod(byte, 16)
+            h, j = divmod(bit, 4)
+            assert z[0] == 16 * (8 * h + 2 * j + p) + l
+            seen.add(int(z[0]))
+    assert seen == set(range(256))
+
+
+def test_q2K_q3K_dequant_dots_and_combine_from_fields():
+    rng = np.random.default_rng(21)
+    for _ in range(20):
+        d = float(np.float16(rng.uniform(1e-4, 2e-3)))
+        dmin = float(np.float16(rng.uniform(1e-4, 2e-3)))
+        dx = np.float32(rng.uniform(-0.05, 0.05))
+        q8 = rng.integers(-128, 128, 256)
+        xblk = pack_q8K(dx, q8)
+        g = np.arange(256) // 16
+        # q2_K
+        sc, mn, q = rng.integers(0, 16, 16), rng.integers(0, 16, 16), rng.integers(0, 4, 256)
+        wblk = pack_q2K(d, dmin, sc, mn, q)
+        np.testing.assert_array_equal(oracle.dequant_q2K(wblk, 1, 256)[0],
+                                      np.float64(d) * sc[g] * q - np.float64(dmin) * mn[g])
+        dots = oracle.subdots_q2K(wblk, xblk, 1, 1, 256)[0, 0]
+        np.testing.assert_array_equal(dots, (q * q8).reshape(16, 16).sum(axis=1))
+        isum = int((sc * dots).sum())
+        msum = int((mn * q8.reshape(16, 16).sum(axis=1)).sum())
+        expect = float(np.float64(d) * np.float64(dx) * isum - np.float64(dmin) * np.float64(dx) * msum)
+        assert oracle.gemm_q2K_f64(wblk, xblk, 1, 1, 256)[0, 0] == pytest.approx(expect, rel=1e-15, abs=1e-300)
+        # q3_K
+        s6, q3 = rng.integers(0, 64, 16), rng.integers(-4, 4, 256)
+        wblk = pack_q3K(d, s6, q3)
+        np.testing.assert_array_equal(oracle.dequant_q3K(wblk, 1, 256)[0], np.float64(d) * (s6[g] - 32) * q3)
+        dots = oracle.subdots_q3K(wblk, xblk, 1, 1, 256)[0, 0]
+        np.testing.assert_array_equal(dots, (q3 * q8).reshape(16, 16).sum(axis=1))
+        expect = float(np.float64(d) * np.float64(dx) * int(((s6 - 32) * dots).sum()))
+        assert oracle.gemm_q3K_f64(wblk, xblk, 1, 1, 256)[0, 0] == pytest.approx(expect, rel=1e-15, abs=1e-300)
+
+
+def test_q2K_zero_codes_and_q3K_zero_codes_closed_forms():
+    """q2_K with all codes 0: every weight is -dmin*m_g, so y = -dmin*dx*sum_g m_g*bsum_g;
+    q3_K with all codes 0 (low bits 0, third bits set): y = 0."""
+    rng = np.random.default_rng(22)
+    q8 = rng.integers(-128, 128, 256)
+    xblk = pack_q8K(0.01, q8)
+    mn = rng.integers(0, 16, 16)
+    dmin = 0.0009765625
+    y = oracle.gemm_q2K_f64(pack_q2K(0.5, dmin, rng.integers(0, 16, 16), mn, np.zeros(256)), xblk, 1, 1, 256)
+    expect = -dmin * np.float64(np.float32(0.01)) * float((mn * q8.reshape(16, 16).sum(axis=1)).sum())
+    assert y[0, 0] == pytest.approx(expect, rel=1e-15)
+    assert oracle.gemm_q3K_f64(pack_q3K(0.5, rng.integers(0, 64, 16), np.zeros(256)), xblk, 1, 1, 256)[0, 0] == 0.0
