@@ -44,7 +44,7 @@ QK = 256
 Q4K_BYTES = 144
 Q6K_BYTES = 210
 Q5K_BYTES = 176
-FMT_BYTES = {"q4K": Q4K_BYTES, "q5K": Q5K_BYTES, "q6K": Q6K_BYTES}
+FMT_BYTES = {"q2K": 84, "q3K": 110, "q4K": Q4K_BYTES, "q5K": Q5K_BYTES, "q6K": Q6K_BYTES}
 Q8K_BYTES = 292
 
 # (name, n, k) of the seven matrices of one layer, in storage order
@@ -391,6 +391,11 @@ def run_extras(torch, q, peaks):
     ws, wb = T.weights("q5K", 5, 12288, 4096)
     out["q5K_12288x4096"] = [T.run("q5K", ws, wb, 12288, 4096, m, 10 if m <= 8 else 3, 2) for m in (1, 8, 512)]
     del ws
+    # the q2_K and q3_K rungs (decode GEMV; their GEMM entry runs the GEMV in 8-row passes)
+    for fmt in ("q3K", "q2K"):
+        ws, wb = T.weights(fmt, 5, 12288, 4096)
+        out["%s_12288x4096" % fmt] = [T.run(fmt, ws, wb, 12288, 4096, m, 10, 2) for m in (1, 8)]
+        del ws
     return out
 
 

@@ -148,6 +148,47 @@ plm_status plm_gemv_q6K_grouped(const plm_gemv_problem* problems, int64_t count,
                                 cudaStream_t stream);
 
 /*
+ * q2_K and q3_K, the lowest rungs of the pages' K-quant width ladder
+ * (PocketLLM README, "What it runs": q2_k, q3_k and q5_k join q4_k and q6_k
+ * as formats the engine decodes).  Public GGML layouts, sixteen 16-weight
+ * groups per 256 weights; group g holds weights 16g..16g+15 and, with
+ * h = g/8, j = (g%8)/2, p = g%2, its 2-bit codes are bits 2j..2j+1 of
+ * qs[32h + 16p + l]:
+ *   q2_K (84 bytes): u8 scales[16] (low nibble scale sc_g, high nibble min
+ *        m_g), u8 qs[64], f16 d, f16 dmin; weight = d * sc_g * q - dmin * m_g.
+ *   q3_K (110 bytes): u8 hmask[32] (bit 4h + j of hmask[16p + l] is the
+ *        weight's third bit), u8 qs[64], u8 scales[12] (6-bit s_g: low four
+ *        bits from scales[g % 8], nibble g / 8; top two from scales[8 + g % 4],
+ *        bits 2(g/4)..), f16 d; code q3 = q - 4 when the third bit is clear,
+ *        weight = d * (s_g - 32) * q3.
+ * Blocks are 4-byte (q2_K) / 2-byte (q3_K) aligned inside a row; w must be
+ * 16-byte aligned.  Same contracts and errors as the q6_K entry points; the
+ * sub-dot export writes the int32 16-weight group dots, [m][n][k/16].  The
+ * GEMM entry points run the decode GEMV eight activation rows at a time (no
+ * tensor-core path for these formats; no workspace, size 0).
+ */
+plm_status plm_gemv_q2K(const void* w, const void* xq, float* y, int64_t m, int64_t n, int64_t k,
+                        cudaStream_t stream);
+plm_status plm_gemv_q2K_grouped(const plm_gemv_problem* problems, int64_t count, int64_t m,
+                                cudaStream_t stream);
+plm_status plm_gemm_q2K(const void* w, const void* xq, float* y, int64_t m, int64_t n, int64_t k,
+                        cudaStream_t stream);
+plm_status plm_gemm_q2K_ws(const void* w, const void* xq, float* y, int64_t m, int64_t n, int64_t k,
+                           void* workspace, size_t workspace_bytes, cudaStream_t stream);
+plm_status plm_subdots_q2K(const void* w, const void* xq, int32_t* out, int64_t m, int64_t n, int64_t k,
+                           cudaStream_t stream);
+plm_status plm_gemv_q3K(const void* w, const void* xq, float* y, int64_t m, int64_t n, int64_t k,
+                        cudaStream_t stream);
+plm_status plm_gemv_q3K_grouped(const plm_gemv_problem* problems, int64_t count, int64_t m,
+                                cudaStream_t stream);
+plm_status plm_gemm_q3K(const void* w, const void* xq, float* y, int64_t m, int64_t n, int64_t k,
+                        cudaStream_t stream);
+plm_status plm_gemm_q3K_ws(const void* w, const void* xq, float* y, int64_t m, int64_t n, int64_t k,
+                           void* workspace, size_t workspace_bytes, cudaStream_t stream);
+plm_status plm_subdots_q3K(const void* w, const void* xq, int32_t* out, int64_t m, int64_t n, int64_t k,
+                           cudaStream_t stream);
+
+/*
  * q5_K, the next rung of the pages' K-quant width ladder (PocketLLM README,
  * "What it runs": q2_k, q3_k, q5_k join q4_k and q6_k as formats the engine
  * decodes).  Block (176 bytes per 256 weights, the public GGML layout): f16 d,
@@ -242,8 +283,8 @@ plm_status plm_gemm_q4K(const void* w, const void* xq, float* y,
 plm_status plm_gemm_q6K(const void* w, const void* xq, float* y,
                         int64_t m, int64_t n, int64_t k, cudaStream_t stream);
 
-/* Workspace bytes plm_gemm_q4K_ws (fmt = 4) / plm_gemm_q5K_ws (fmt = 5) /
- * plm_gemm_q6K_ws (fmt = 6)
+/* Workspace bytes plm_gemm_qNK_ws needs (fmt = N: 2, 3, 4, 5, 6; q2_K and
+ * q3_K need none)
  * need for m activation rows of length k (0 when none is needed, and for
  * invalid arguments). */
 size_t plm_gemm_workspace_size(int fmt, int64_t m, int64_t k);

@@ -242,6 +242,56 @@ plm_status plm_gemv_q6K_grouped(const plm_gemv_problem* problems, int64_t count,
     return grouped_common(6, problems, count, m, stream);
 }
 
+plm_status plm_gemv_q2K(const void* w, const void* xq, float* y, int64_t m, int64_t n, int64_t k,
+                        cudaStream_t stream) {
+    return gemv_common(2, w, xq, y, m, n, k, stream);
+}
+
+plm_status plm_gemv_q2K_grouped(const plm_gemv_problem* problems, int64_t count, int64_t m,
+                                cudaStream_t stream) {
+    return grouped_common(2, problems, count, m, stream);
+}
+
+plm_status plm_gemm_q2K(const void* w, const void* xq, float* y, int64_t m, int64_t n, int64_t k,
+                        cudaStream_t stream) {
+    return gemm_common(2, w, xq, y, m, n, k, stream);
+}
+
+plm_status plm_gemm_q2K_ws(const void* w, const void* xq, float* y, int64_t m, int64_t n, int64_t k,
+                           void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    return gemm_ws_common(2, w, xq, y, m, n, k, workspace, workspace_bytes, stream);
+}
+
+plm_status plm_subdots_q2K(const void* w, const void* xq, int32_t* out, int64_t m, int64_t n, int64_t k,
+                           cudaStream_t stream) {
+    return subdots_common(2, w, xq, out, m, n, k, stream);
+}
+
+plm_status plm_gemv_q3K(const void* w, const void* xq, float* y, int64_t m, int64_t n, int64_t k,
+                        cudaStream_t stream) {
+    return gemv_common(3, w, xq, y, m, n, k, stream);
+}
+
+plm_status plm_gemv_q3K_grouped(const plm_gemv_problem* problems, int64_t count, int64_t m,
+                                cudaStream_t stream) {
+    return grouped_common(3, problems, count, m, stream);
+}
+
+plm_status plm_gemm_q3K(const void* w, const void* xq, float* y, int64_t m, int64_t n, int64_t k,
+                        cudaStream_t stream) {
+    return gemm_common(3, w, xq, y, m, n, k, stream);
+}
+
+plm_status plm_gemm_q3K_ws(const void* w, const void* xq, float* y, int64_t m, int64_t n, int64_t k,
+                           void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    return gemm_ws_common(3, w, xq, y, m, n, k, workspace, workspace_bytes, stream);
+}
+
+plm_status plm_subdots_q3K(const void* w, const void* xq, int32_t* out, int64_t m, int64_t n, int64_t k,
+                           cudaStream_t stream) {
+    return subdots_common(3, w, xq, out, m, n, k, stream);
+}
+
 plm_status plm_gemv_q5K(const void* w, const void* xq, float* y, int64_t m, int64_t n, int64_t k,
                         cudaStream_t stream) {
     return gemv_common(5, w, xq, y, m, n, k, stream);
@@ -278,7 +328,7 @@ plm_status plm_gemm_q6K(const void* w, const void* xq, float* y, int64_t m, int6
 }
 
 size_t plm_gemm_workspace_size(int fmt, int64_t m, int64_t k) {
-    if ((fmt != 4 && fmt != 5 && fmt != 6) || m <= 0 || k <= 0 || k % plm::QK != 0 || k > kMaxIndex) return 0;
+    if (fmt < 2 || fmt > 6 || m <= 0 || k <= 0 || k % plm::QK != 0 || k > kMaxIndex) return 0;
     return plm::gemm_workspace_need(fmt, m, (int)k);
 }
 

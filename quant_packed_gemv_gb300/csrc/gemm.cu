@@ -669,9 +669,15 @@ static cudaError_t gemm_tc_ws(const uint8_t* w, const uint8_t* xq, float* y, lon
 // time) serve the GEMM entry point.
 constexpr long long GEMM_MIN_M = 9;
 
+// q4_K, q5_K and q6_K prefill on the tensor cores; q2_K and q3_K (and any
+// m below GEMM_MIN_M) run the decode GEMV eight activation rows at a time.
+static bool gemm_on_tensor_cores(int fmt, long long m) {
+    return (fmt == 4 || fmt == 5 || fmt == 6) && m >= GEMM_MIN_M && m <= 0x7FFFFFFF;
+}
+
 cudaError_t launch_gemm_ws(int fmt, const uint8_t* w, const uint8_t* xq, float* y, long long m, int n, int k,
                            void* ws, size_t ws_bytes, cudaStream_t stream) {
-    if (m >= GEMM_MIN_M && (long long)m <= 0x7FFFFFFF) {
+    if (gemm_on_tensor_cores(fmt, m)) {
         if (!ws || ws_bytes < gemm_workspace_bytes(m, k)) return cudaErrorInvalidValue;
         return fmt == 4 ? gemm_tc_ws<4>(w, xq, y, m, n, k, ws, stream)
                : fmt == 5 ? gemm_tc_ws<5>(w, xq, y, m, n, k, ws, stream)
@@ -687,8 +693,7 @@ cudaError_t launch_gemm_ws(int fmt, const uint8_t* w, const uint8_t* xq, float* 
 }
 
 size_t gemm_workspace_need(int fmt, long long m, int k) {
-    (void)fmt;
-    return m >= GEMM_MIN_M ? gemm_workspace_bytes(m, k) : 0;
+    return gemm_on_tensor_cores(fmt, m) ? gemm_workspace_bytes(m, k) : 0;
 }
 
 cudaError_t launch_gemm(int fmt, const uint8_t* w, const uint8_t* xq, float* y, long long m, int n, int k,

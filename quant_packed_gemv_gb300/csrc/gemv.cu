@@ -7,20 +7,36 @@ namespace plm {
 cudaError_t run_group_q4K(const HostProblem* p, int count, int m, bool subdots, cudaStream_t stream);
 cudaError_t run_group_q4K_f32(const HostProblem* p, int count, int m, cudaStream_t stream);
 cudaError_t run_group_q4K_swiglu(const HostProblem* p, int count, int m, cudaStream_t stream);
+cudaError_t run_group_q2K(const HostProblem* p, int count, int m, bool subdots, cudaStream_t stream);
+cudaError_t run_group_q3K(const HostProblem* p, int count, int m, bool subdots, cudaStream_t stream);
 cudaError_t run_group_q5K(const HostProblem* p, int count, int m, bool subdots, cudaStream_t stream);
 cudaError_t run_group_q6K(const HostProblem* p, int count, int m, bool subdots, cudaStream_t stream);
+bool gemv_supported_q2K(int k);
+bool gemv_supported_q3K(int k);
 bool gemv_supported_q4K(int k);
 bool gemv_supported_q5K(int k);
 bool gemv_supported_q6K(int k);
 
 bool gemv_supported(int fmt, int k) {
-    return fmt == 4 ? gemv_supported_q4K(k) : fmt == 5 ? gemv_supported_q5K(k) : gemv_supported_q6K(k);
+    switch (fmt) {
+        case 2: return gemv_supported_q2K(k);
+        case 3: return gemv_supported_q3K(k);
+        case 4: return gemv_supported_q4K(k);
+        case 5: return gemv_supported_q5K(k);
+        case 6: return gemv_supported_q6K(k);
+        default: return false;
+    }
 }
 
 static cudaError_t run_fmt(int fmt, const HostProblem* p, int count, int m, bool subdots, cudaStream_t s) {
-    return fmt == 4   ? run_group_q4K(p, count, m, subdots, s)
-           : fmt == 5 ? run_group_q5K(p, count, m, subdots, s)
-                      : run_group_q6K(p, count, m, subdots, s);
+    switch (fmt) {
+        case 2: return run_group_q2K(p, count, m, subdots, s);
+        case 3: return run_group_q3K(p, count, m, subdots, s);
+        case 4: return run_group_q4K(p, count, m, subdots, s);
+        case 5: return run_group_q5K(p, count, m, subdots, s);
+        case 6: return run_group_q6K(p, count, m, subdots, s);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 cudaError_t launch_gemv(int fmt, const uint8_t* w, const uint8_t* xq, float* y,

@@ -1,5 +1,5 @@
 // Decode GEMV for m = 1..8 activation rows over packed q6_K weights (the
-// output head; PocketLLM "What it runs": K-quant weights decoded inside the
+// output head) and the low rungs q2_K and q3_K (PocketLLM "What it runs": K-quant weights decoded inside the
 // kernel, never widened; the weight stream is read once for all m activation
 // rows, as the pages' 8-row activation tile does on the CPU).  q4_K and q5_K
 // take the one-lane-per-block kernel of gemv_q4K.cuh; the problem and batch
@@ -59,6 +59,20 @@ template <> struct Fmt<6> {
     static constexpr int SLOT = 3456;                          // + 16-byte alignment slack
     static constexpr int SUB = 16;
 };
+template <> struct Fmt<2> {                                    // q2_K: 84-byte blocks, 4-byte aligned
+    static constexpr int BYTES = Q2K_BYTES;
+    static constexpr int CHUNK = 32;
+    static constexpr int PAYLOAD = CHUNK * Q2K_BYTES;          // 2688
+    static constexpr int SLOT = 2720;
+    static constexpr int SUB = 16;
+};
+template <> struct Fmt<3> {                                    // q3_K: 110-byte blocks, 2-byte aligned
+    static constexpr int BYTES = Q3K_BYTES;
+    static constexpr int CHUNK = 32;
+    static constexpr int PAYLOAD = CHUNK * Q3K_BYTES;          // 3520
+    static constexpr int SLOT = 3552;
+    static constexpr int SUB = 16;
+};
 
 struct GemvProblem {
     const uint8_t* w;
@@ -110,7 +124,7 @@ __device__ __forceinline__ StageGeom stage_geom(int row, int b0, int wb, int rps
 }
 
 // The activation values one lane needs for one block of one activation row:
-//   q6_K lane (h, p): chunks 8h+2qq+p for qq = 0..3, bsums 8h+2qq+p
+//   lane (h, p) (q2_K, q3_K, q6_K): chunks 8h+2qq+p for qq = 0..3, bsums 8h+2qq+p
 // bw[0] packs the first two bsums (low half first), bw[1] the last two.
 struct LaneAct {
     int4 x[4];
@@ -193,11 +207,114 @@ __device__ __forceinline__ void q6K_block(const uint8_t* slot, int off, const La
     }
 }
 
+
+// q2_K / q3_K: lane t = (h, p) owns groups 8h + 2j + p, j = 0..3 -- the
+// groups whose activations act_from_* gives it -- whose 2-bit codes are bits
+// 2j, 2j+1 of the 16 bytes qs[32h + 16p .. +16]; q3_K's third bits are bit
+// 4h + j of hmask[16p .. +16].
+template <int M, bool SUBDOTS>
+__device__ __forceinline__ void q2K_block(const uint8_t* slot, int off, const LaneAct* act, int b, int t,
+                                          float* v, int32_t* sub_row, size_t sub_stride_i) {
+    const int h = t >> 1, p = t & 1;
+    const uint4 Q = lds16_align2(slot, off + 16 + 32 * h + 16 * p);
+    const uint2 S = lds8_align2(slot, off + 8 * h);   // scale bytes 8h .. 8h+7: group 8h+2j+p at 2j+p
+    const float d = half_bits_to_float(*reinterpret_cast<const uint16_t*>(slot + off + 80));
+    const float dmin = half_bits_to_float(*reinterpret_cast<const uint16_t*>(slot + off + 82));
+    const uint32_t qw[4] = {Q.x, Q.y, Q.z, Q.w};
+    int sc[4], mn[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int byte = 2 * j + p;
+        const uint32_t v8 = ((byte < 4 ? S.x : S.y) >> (8 * (byte & 3))) & 0xFFu;
+        sc[j] = (int)(v8 & 15u);
+        mn[j] = (int)(v8 >> 4);
+    }
+#pragma unroll
+    for (int i = 0; i < M; ++i) {
+        const LaneAct& X = act[i];
+        const int bsum[4] = {lo16(X.bw[0]), hi16(X.bw[0]), lo16(X.bw[1]), hi16(X.bw[1])};
+        const int xs[4][4] = {{X.x[0].x, X.x[0].y, X.x[0].z, X.x[0].w}, {X.x[1].x, X.x[1].y, X.x[1].z, X.x[1].w},
+                              {X.x[2].x, X.x[2].y, X.x[2].z, X.x[2].w}, {X.x[3].x, X.x[3].y, X.x[3].z, X.x[3].w}};
+        int isum = 0, msum = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            int dot = 0;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) dot = dp4a_us((qw[u] >> (2 * j)) & 0x03030303u, xs[j][u], dot);
+            if constexpr (SUBDOTS)
+                sub_row[i * sub_stride_i + (size_t)b * 16 + 8 * h + 2 * j + p] = dot;
+            isum += sc[j] * dot;
+            msum += mn[j] * bsum[j];
+        }
+        if constexpr (!SUBDOTS) {
+            const float tt = __fmaf_rn(d, (float)isum, -__fmul_rn(dmin, (float)msum));
+            v[i] = __fmaf_rn(X.dy, tt, v[i]);
+        }
+    }
+}
+
+template <int M, bool SUBDOTS>
+__device__ __forceinline__ void q3K_block(const uint8_t* slot, int off, const LaneAct* act, int b, int t,
+                                          float* v, int32_t* sub_row, size_t sub_stride_i) {
+    const int h = t >> 1, p = t & 1;
+    const uint4 Q = lds16_align2(slot, off + 32 + 32 * h + 16 * p);
+    const uint4 Hm = lds16_align2(slot, off + 16 * p);
+    const uint4 T = lds16_align2(slot, off + 96);      // scales[12], then d
+    const float d = half_bits_to_float(T.w);           // bytes 108, 109
+    const uint32_t qw[4] = {Q.x, Q.y, Q.z, Q.w};
+    const uint32_t hw[4] = {Hm.x, Hm.y, Hm.z, Hm.w};
+    const uint32_t tw[3] = {T.x, T.y, T.z};
+    int sc[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        // group g = 8h + 2j + p: low four bits from scales[2j + p] (nibble h),
+        // top two from scales[8 + (2j + p) % 4], bits 2(2h + j/2)
+        const int lb = 2 * j + p, hb = 8 + ((2 * j + p) & 3), hs = 2 * (2 * h + j / 2);
+        const uint32_t low = ((tw[lb >> 2] >> (8 * (lb & 3) + 4 * h)) & 15u);
+        const uint32_t high = ((tw[hb >> 2] >> (8 * (hb & 3) + hs)) & 3u);
+        sc[j] = (int)(low | (high << 4)) - 32;
+    }
+#pragma unroll
+    for (int i = 0; i < M; ++i) {
+        const LaneAct& X = act[i];
+        const int bsum[4] = {lo16(X.bw[0]), hi16(X.bw[0]), lo16(X.bw[1]), hi16(X.bw[1])};
+        const int xs[4][4] = {{X.x[0].x, X.x[0].y, X.x[0].z, X.x[0].w}, {X.x[1].x, X.x[1].y, X.x[1].z, X.x[1].w},
+                              {X.x[2].x, X.x[2].y, X.x[2].z, X.x[2].w}, {X.x[3].x, X.x[3].y, X.x[3].z, X.x[3].w}};
+        int isum = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            int raw = 0;   // codes q3 + 4 in 0..7, so the exact dot is raw - 4 * bsum
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const uint32_t c = ((qw[u] >> (2 * j)) & 0x03030303u) | (((hw[u] >> (4 * h + j)) & 0x01010101u) << 2);
+                raw = dp4a_us(c, xs[j][u], raw);
+            }
+            const int dot = raw - 4 * bsum[j];
+            if constexpr (SUBDOTS)
+                sub_row[i * sub_stride_i + (size_t)b * 16 + 8 * h + 2 * j + p] = dot;
+            isum += sc[j] * dot;
+        }
+        if constexpr (!SUBDOTS) v[i] = __fmaf_rn(__fmul_rn(d, X.dy), (float)isum, v[i]);
+    }
+}
+
+// The per-lane block decode of format FMT (q2_K, q3_K, q6_K).
+template <int FMT, int M, bool SUBDOTS>
+__device__ __forceinline__ void fmt_block(const uint8_t* slot, int off, const LaneAct* act, int b, int t, float* v,
+                                          int32_t* sub_row, size_t sub_stride_i) {
+    if constexpr (FMT == 2)
+        q2K_block<M, SUBDOTS>(slot, off, act, b, t, v, sub_row, sub_stride_i);
+    else if constexpr (FMT == 3)
+        q3K_block<M, SUBDOTS>(slot, off, act, b, t, v, sub_row, sub_stride_i);
+    else
+        q6K_block<M, SUBDOTS>(slot, off, act, b, t, v, sub_row, sub_stride_i);
+}
+
 // One block of the register path: adds this lane's f32 term of the block at
 // byte offset off of the stage to v[] (same arithmetic as the staged path).
 template <int FMT, int M>
 __device__ __forceinline__ void areg_block(const uint8_t* slot, int off, const LaneAct* act, int t, float* v) {
-    q6K_block<M, false>(slot, off, act, 0, t, v, nullptr, 0);
+    fmt_block<FMT, M, false>(slot, off, act, 0, t, v, nullptr, 0);
 }
 
 // AREG: each lane keeps the activations of its (at most two) block columns
@@ -319,7 +436,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1) gemv_kernel(const __grid_consta
             LaneAct la[M];
 #pragma unroll
             for (int i = 0; i < M; ++i) la[i] = act_from_smem<FMT>(act, i * nb + b, t);
-            q6K_block<M, SUBDOTS>(slot, g.delta + (rr * nb + bb) * BYTES, la, b, t, v, sub_row, sub_stride_i);
+            fmt_block<FMT, M, SUBDOTS>(slot, g.delta + (rr * nb + bb) * BYTES, la, b, t, v, sub_row, sub_stride_i);
         };
 
         for (int s = 0; s < nst && ok; ++s) {
@@ -335,7 +452,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1) gemv_kernel(const __grid_consta
             }
             uint8_t* slot = ring + cslot * SLOT;
             const StageGeom g = stage_geom<FMT>(crow, cb0, wb, rps, nb, wbytes);
-            if (FMT == 6 && g.tail > 0) {
+            if (g.tail > 0) {   // the matrix's last bytes past its final 16-byte boundary
                 if (lane < g.tail) slot[g.bytes + lane] = P.w[g.src + g.bytes + lane];
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();

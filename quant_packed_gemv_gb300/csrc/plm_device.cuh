@@ -9,6 +9,8 @@
 namespace plm {
 
 constexpr int QK = 256;          // weights (or activations) per block
+constexpr int Q2K_BYTES = 84;    // scales[16], qs[64], f16 d, f16 dmin
+constexpr int Q3K_BYTES = 110;   // hmask[32], qs[64], scales[12], f16 d
 constexpr int Q4K_BYTES = 144;   // f16 d, f16 dmin, scales[12], qs[128]
 constexpr int Q5K_BYTES = 176;   // f16 d, f16 dmin, scales[12], qh[32], qs[128]
 constexpr int Q6K_BYTES = 210;   // ql[128], qh[64], scales[16], f16 d

@@ -20,6 +20,8 @@ PLM_ERR_CUDA = 4
 QK = 256
 Q4K_BYTES = 144
 Q5K_BYTES = 176
+Q2K_BYTES = 84
+Q3K_BYTES = 110
 Q6K_BYTES = 210
 Q8K_BYTES = 292
 GEMV_MAX_M = 8
@@ -82,11 +84,12 @@ def load(build_if_missing=True):
     lib.plm_quantize_q8K.restype = ctypes.c_int
     lib.plm_gemm_workspace_size.argtypes = [ctypes.c_int, i64, i64]
     lib.plm_gemm_workspace_size.restype = ctypes.c_size_t
-    for name in ("plm_gemm_q4K_ws", "plm_gemm_q5K_ws", "plm_gemm_q6K_ws"):
+    for name in ("plm_gemm_q2K_ws", "plm_gemm_q3K_ws", "plm_gemm_q4K_ws", "plm_gemm_q5K_ws", "plm_gemm_q6K_ws"):
         fn = getattr(lib, name)
         fn.argtypes = [vp, vp, vp, i64, i64, i64, vp, ctypes.c_size_t, vp]
         fn.restype = ctypes.c_int
-    for name in ("plm_gemv_q4K_grouped", "plm_gemv_q5K_grouped", "plm_gemv_q6K_grouped"):
+    for name in ("plm_gemv_q2K_grouped", "plm_gemv_q3K_grouped", "plm_gemv_q4K_grouped", "plm_gemv_q5K_grouped",
+                 "plm_gemv_q6K_grouped"):
         fn = getattr(lib, name)
         fn.argtypes = [ctypes.POINTER(_Problem), i64, i64, vp]
         fn.restype = ctypes.c_int
@@ -98,7 +101,8 @@ def load(build_if_missing=True):
     lib.plm_quantize_gemv_q4K_grouped.restype = ctypes.c_int
     for name in ("plm_gemv_q4K", "plm_gemv_q6K", "plm_gemm_q4K", "plm_gemm_q6K", "plm_gemm_q4K_noalloc",
                  "plm_subdots_q4K", "plm_subdots_q6K", "plm_quantize_gemv_q4K",
-                 "plm_gemv_q5K", "plm_gemm_q5K", "plm_subdots_q5K"):
+                 "plm_gemv_q5K", "plm_gemm_q5K", "plm_subdots_q5K",
+                 "plm_gemv_q2K", "plm_gemm_q2K", "plm_subdots_q2K", "plm_gemv_q3K", "plm_gemm_q3K", "plm_subdots_q3K"):
         fn = getattr(lib, name)
         fn.argtypes = [vp, vp, vp, i64, i64, i64, vp]
         fn.restype = ctypes.c_int
@@ -171,6 +175,12 @@ plm_gemv_q6K = _mm("plm_gemv_q6K")
 plm_gemv_q5K = _mm("plm_gemv_q5K")
 plm_gemm_q5K = _mm("plm_gemm_q5K")
 plm_subdots_q5K = _mm("plm_subdots_q5K")
+plm_gemv_q2K = _mm("plm_gemv_q2K")
+plm_gemm_q2K = _mm("plm_gemm_q2K")
+plm_subdots_q2K = _mm("plm_subdots_q2K")
+plm_gemv_q3K = _mm("plm_gemv_q3K")
+plm_gemm_q3K = _mm("plm_gemm_q3K")
+plm_subdots_q3K = _mm("plm_subdots_q3K")
 plm_gemm_q4K = _mm("plm_gemm_q4K")
 plm_gemm_q6K = _mm("plm_gemm_q6K")
 # q4_K GEMM whose workspace is a fixed array inside the library: for callers
@@ -198,6 +208,8 @@ def _grouped(name):
 plm_gemv_q4K_grouped = _grouped("plm_gemv_q4K_grouped")
 plm_gemv_q6K_grouped = _grouped("plm_gemv_q6K_grouped")
 plm_gemv_q5K_grouped = _grouped("plm_gemv_q5K_grouped")
+plm_gemv_q2K_grouped = _grouped("plm_gemv_q2K_grouped")
+plm_gemv_q3K_grouped = _grouped("plm_gemv_q3K_grouped")
 
 
 def plm_gemv_q4K_swiglu(w_gate, w_up, xq, h, m, n, k, stream=None):
@@ -226,8 +238,8 @@ def plm_quantize_gemv_q4K_grouped(problems, m, stream=None):
 
 
 def plm_gemm_workspace_size(fmt, m, k):
-    """fmt: 'q4K' / 'q5K' / 'q6K' or 4 / 5 / 6."""
-    f = {"q4K": 4, "q5K": 5, "q6K": 6}.get(fmt, fmt)
+    """fmt: 'q2K' .. 'q6K' or 2 .. 6."""
+    f = {"q2K": 2, "q3K": 3, "q4K": 4, "q5K": 5, "q6K": 6}.get(fmt, fmt)
     return load().plm_gemm_workspace_size(f, m, k)
 
 
@@ -246,6 +258,8 @@ def _gemm_ws(name):
 plm_gemm_q4K_ws = _gemm_ws("plm_gemm_q4K_ws")
 plm_gemm_q6K_ws = _gemm_ws("plm_gemm_q6K_ws")
 plm_gemm_q5K_ws = _gemm_ws("plm_gemm_q5K_ws")
+plm_gemm_q2K_ws = _gemm_ws("plm_gemm_q2K_ws")
+plm_gemm_q3K_ws = _gemm_ws("plm_gemm_q3K_ws")
 
 
 def raw_status(name, *args):

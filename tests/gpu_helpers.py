@@ -48,7 +48,7 @@ def gpu_matmul(kind, fmt, w_np, xq_np, m, n, k, poison=True):
 
 
 def gpu_subdots(fmt, w_np, xq_np, m, n, k):
-    per = 16 if fmt == "q6K" else 8
+    per = 8 if fmt in ("q4K", "q5K") else 16   # 32-weight sub-blocks or 16-weight groups
     w, xq = dev(w_np), dev(xq_np)
     out = torch.full((m, n, k // 256 * per), -7, dtype=torch.int32, device="cuda")
     getattr(q, "plm_subdots_%s" % fmt)(w, xq, out, m, n, k)

@@ -35,7 +35,7 @@ def test_quantize_scaled_and_tiny_values():
 
 # ------------------------------------------------------ integer sub-dots
 
-@pytest.mark.parametrize("fmt", ["q4K", "q5K", "q6K"])
+@pytest.mark.parametrize("fmt", ["q2K", "q3K", "q4K", "q5K", "q6K"])
 @pytest.mark.parametrize("m,n,k", [(1, 1, 256), (1, 33, 1024), (3, 17, 1280), (8, 40, 2048),
                                    (5, 9, 2816)])
 def test_subdots_bit_exact(fmt, m, n, k):
@@ -48,7 +48,7 @@ def test_subdots_bit_exact(fmt, m, n, k):
 
 # --------------------------------------------------------------- GEMV
 
-@pytest.mark.parametrize("fmt", ["q4K", "q5K", "q6K"])
+@pytest.mark.parametrize("fmt", ["q2K", "q3K", "q4K", "q5K", "q6K"])
 @pytest.mark.parametrize("m", [1, 2, 3, 4, 5, 6, 7, 8])
 @pytest.mark.parametrize("n,k", [(1, 256), (37, 1024), (100, 1280), (64, 3072)])
 def test_gemv_matches_oracle(fmt, m, n, k):
@@ -59,7 +59,7 @@ def test_gemv_matches_oracle(fmt, m, n, k):
     assert_close(y, ref, S)
 
 
-@pytest.mark.parametrize("fmt", ["q4K", "q5K", "q6K"])
+@pytest.mark.parametrize("fmt", ["q2K", "q3K", "q4K", "q5K", "q6K"])
 def test_gemv_row_result_independent_of_m(fmt):
     # the pages' tiled kernels are bit-identical to the single-row kernel;
     # here activation row i must give the same bits at every m
@@ -72,12 +72,16 @@ def test_gemv_row_result_independent_of_m(fmt):
         np.testing.assert_array_equal(y1[0], y8[i])
 
 
-@pytest.mark.parametrize("fmt", ["q4K", "q5K", "q6K"])
+@pytest.mark.parametrize("fmt", ["q2K", "q3K", "q4K", "q5K", "q6K"])
 def test_gemv_adversarial_extremes(fmt):
     # all codes at the extremes: largest integer sums the formats allow
-    from tests.packers import pack_q4K, pack_q5K, pack_q6K
+    from tests.packers import pack_q2K, pack_q3K, pack_q4K, pack_q5K, pack_q6K
     k, n, m = 1024, 8, 2
-    if fmt == "q4K":
+    if fmt == "q2K":
+        blk = pack_q2K(2e-3, 2e-3, [15] * 16, [15] * 16, np.full(256, 3))
+    elif fmt == "q3K":
+        blk = pack_q3K(2e-3, [0] * 16, np.full(256, -4))      # scale -32, code -4
+    elif fmt == "q4K":
         blk = pack_q4K(2e-3, 2e-3, [63] * 8, [63] * 8, np.full(256, 15))
     elif fmt == "q5K":
         blk = pack_q5K(2e-3, 2e-3, [63] * 8, [63] * 8, np.full(256, 31))
@@ -94,7 +98,7 @@ def test_gemv_adversarial_extremes(fmt):
 
 # --------------------------------------------------------------- GEMM
 
-@pytest.mark.parametrize("fmt", ["q4K", "q5K", "q6K"])
+@pytest.mark.parametrize("fmt", ["q2K", "q3K", "q4K", "q5K", "q6K"])
 @pytest.mark.parametrize("m,n,k", [(9, 50, 1024), (17, 33, 256), (64, 128, 2048), (130, 70, 512),
                                    (128, 128, 256), (200, 300, 1536), (512, 1024, 1024), (257, 129, 4096)])
 def test_gemm_matches_oracle(fmt, m, n, k):
@@ -105,7 +109,7 @@ def test_gemm_matches_oracle(fmt, m, n, k):
     assert_close(y, ref, S)
 
 
-@pytest.mark.parametrize("fmt", ["q4K", "q5K", "q6K"])
+@pytest.mark.parametrize("fmt", ["q2K", "q3K", "q4K", "q5K", "q6K"])
 def test_gemm_agrees_with_gemv_small_m(fmt):
     n, k = 96, 1024
     w = make_weights(fmt, 14, 0, n, k)
@@ -120,7 +124,7 @@ def test_gemm_agrees_with_gemv_small_m(fmt):
 
 # ------------------------------------------------------- grouped GEMV
 
-@pytest.mark.parametrize("fmt", ["q4K", "q5K", "q6K"])
+@pytest.mark.parametrize("fmt", ["q2K", "q3K", "q4K", "q5K", "q6K"])
 @pytest.mark.parametrize("m", [1, 3, 8])
 def test_grouped_gemv_equals_single_calls(fmt, m):
     import torch
@@ -149,7 +153,7 @@ def test_no_device_fault_recorded():
     assert q.plm_device_fault() == 0
 
 
-@pytest.mark.parametrize("fmt", ["q4K", "q5K", "q6K"])
+@pytest.mark.parametrize("fmt", ["q2K", "q3K", "q4K", "q5K", "q6K"])
 def test_gemm_with_caller_workspace_matches(fmt):
     import torch
     import quant_packed_gemv_gb300 as q
