@@ -123,6 +123,13 @@ __device__ __forceinline__ void cursor_next(const LaneBatch<MAXP>& B, Cursor& c,
     cursor_enter(B, c, c.p + 1, W0, W1, pairf);
 }
 
+// First block (within the row) of one-row stage ch; paired launches run the
+// up matrix's stages after the gate's.
+__device__ __forceinline__ int stage_b0(int ch, int nb) {
+    const int spr = unit_weight(nb);
+    return (ch >= spr ? ch - spr : ch) * STAGE_BLOCKS;
+}
+
 // SwiGLU epilogue of a paired launch: silu(g) * u = g / (1 + e^-g) * u.
 __device__ __forceinline__ float swiglu(float g, float u) {
     return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
@@ -197,13 +204,25 @@ __device__ __forceinline__ int dp2a_hi_su(int a, uint32_t b, int c) {
 // One whole q4_K block against M staged activation blocks (same column,
 // records act_stride bytes apart, scales dy_stride floats apart).  Adds the
 // block's f32 term to v[i], or writes the eight exact sub-block dots.
-template <int FMT, int M, bool SUBDOTS>
-__device__ __forceinline__ void lane_block(const uint8_t* w, const uint8_t* act, int act_stride, const float* dy,
+// A block's 16-byte words, read from the stage in shared memory or from a
+// copy the lane already holds in registers.
+struct SmemBlock {
+    const uint8_t* p;
+    __device__ __forceinline__ uint4 at(int i) const { return reinterpret_cast<const uint4*>(p)[i]; }
+};
+template <int N>
+struct RegBlock {
+    uint4 r[N];
+    __device__ __forceinline__ uint4 at(int i) const { return r[i]; }
+};
+
+template <int FMT, int M, bool SUBDOTS, class Blk>
+__device__ __forceinline__ void lane_block(const Blk& w, const uint8_t* act, int act_stride, const float* dy,
                                            int dy_stride, float* v, int32_t* sub, size_t sub_stride) {
-    const uint4 hdr = *reinterpret_cast<const uint4*>(w);
+    const uint4 hdr = w.at(0);
     uint32_t qh[8];   // q5_K: the fifth bits, byte l <-> byte l of every qs chunk
     if constexpr (FMT == 5) {
-        const uint4 h0 = *reinterpret_cast<const uint4*>(w + 16), h1 = *reinterpret_cast<const uint4*>(w + 32);
+        const uint4 h0 = w.at(1), h1 = w.at(2);
         qh[0] = h0.x; qh[1] = h0.y; qh[2] = h0.z; qh[3] = h0.w;
         qh[4] = h1.x; qh[5] = h1.y; qh[6] = h1.z; qh[7] = h1.w;
     }
@@ -217,8 +236,8 @@ __device__ __forceinline__ void lane_block(const uint8_t* w, const uint8_t* act,
     for (int i = 0; i < M; ++i) isum[i] = 0;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-        const uint4 qa = *reinterpret_cast<const uint4*>(w + LaneFmt<FMT>::QS + 32 * c);
-        const uint4 qb = *reinterpret_cast<const uint4*>(w + LaneFmt<FMT>::QS + 16 + 32 * c);
+        const uint4 qa = w.at(LaneFmt<FMT>::QS / 16 + 2 * c);
+        const uint4 qb = w.at(LaneFmt<FMT>::QS / 16 + 2 * c + 1);
         const uint32_t q[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
         // the codes of sub-blocks 2c (lo) and 2c+1 (hi) as bytes; q4_K's high
         // nibbles stay in place (16 q), divided out of the dot below
@@ -385,19 +404,43 @@ __global__ void __launch_bounds__(WARPS * 32, 1) lane_kernel(const __grid_consta
                 break;
             }
             const uint8_t* slot = ring + cslot * SLOT;
+            // this lane's block of the stage (clamped to block 0 when it has none; result discarded)
+            const int lane_blk = rps > 0 ? (rl < min(rps, n - cc.u * rps) ? lane : 0)
+                                         : (lane < min(STAGE_BLOCKS, nb - stage_b0(cc.ch, nb)) ? lane : 0);
+            // m <= 2: copy the block into registers and refill the slot at once,
+            // so every stage of the ring is in flight while this one is decoded
+            constexpr bool EARLY = !SUBDOTS && M <= 2;
+            RegBlock<BYTES / 16> rb;
+            if constexpr (EARLY) {
+#pragma unroll
+                for (int u = 0; u < BYTES / 16; ++u)
+                    rb.r[u] = reinterpret_cast<const uint4*>(slot + lane_blk * BYTES)[u];
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // reads before the refill
+                ++consumed;
+                if (++cslot == (uint32_t)NS) {
+                    cslot = 0;
+                    cphase ^= 1u;
+                }
+                __syncwarp();
+                if (ic.p >= 0) issue_one();
+            }
+            auto decode = [&](const uint8_t* act, const float* dyp, float* v, int32_t* sub) {
+                if constexpr (EARLY)
+                    lane_block<FMT, M, SUBDOTS>(rb, act, act_stride, dyp, nb, v, sub, sub_stride);
+                else
+                    lane_block<FMT, M, SUBDOTS>(SmemBlock{slot + lane_blk * BYTES}, act, act_stride, dyp, nb, v, sub,
+                                                sub_stride);
+            };
             if (rps > 0) {
                 const int r0 = cc.u * rps;
                 const int nrows = min(rps, n - r0);
                 const bool valid = rl < nrows;
-                const int bl = valid ? lane : 0;   // clamped block of the stage; result discarded
                 const int col = valid ? cl : 0;
                 float v[M];
 #pragma unroll
                 for (int i = 0; i < M; ++i) v[i] = 0.0f;
                 int32_t* sub = SUBDOTS ? subv + ((size_t)(r0 + rl) * nb + col) * 8 : nullptr;
-                if (!SUBDOTS || valid)
-                    lane_block<FMT, M, SUBDOTS>(slot + bl * BYTES, rec + (size_t)col * REC, act_stride, dyv + col,
-                                           nb, v, sub, sub_stride);
+                if (!SUBDOTS || valid) decode(rec + (size_t)col * REC, dyv + col, v, sub);
                 if constexpr (!SUBDOTS) {
                     if (pow2) {
 #pragma unroll
@@ -435,9 +478,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1) lane_kernel(const __grid_consta
 #pragma unroll
                 for (int i = 0; i < M; ++i) v[i] = acc[i];
                 int32_t* sub = SUBDOTS ? subv + ((size_t)cc.u * nb + b) * 8 : nullptr;
-                if (!SUBDOTS || valid)
-                    lane_block<FMT, M, SUBDOTS>(slot + (valid ? lane : 0) * BYTES, rec + (size_t)b * REC, act_stride,
-                                           dyv + b, nb, v, sub, sub_stride);
+                if (!SUBDOTS || valid) decode(rec + (size_t)b * REC, dyv + b, v, sub);
 #pragma unroll
                 for (int i = 0; i < M; ++i) acc[i] = valid ? v[i] : acc[i];
                 if (b0 + STAGE_BLOCKS >= nb) {   // last stage of the row
@@ -454,13 +495,15 @@ __global__ void __launch_bounds__(WARPS * 32, 1) lane_kernel(const __grid_consta
                     }
                 }
             }
-            ++consumed;
-            if (++cslot == (uint32_t)NS) {
-                cslot = 0;
-                cphase ^= 1u;
+            if constexpr (!EARLY) {
+                ++consumed;
+                if (++cslot == (uint32_t)NS) {
+                    cslot = 0;
+                    cphase ^= 1u;
+                }
+                __syncwarp();
+                if (ic.p >= 0) issue_one();
             }
-            __syncwarp();
-            if (ic.p >= 0) issue_one();
             cursor_next(B, cc, nb, W0, W1, PF);
         }
     }
