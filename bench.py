@@ -318,7 +318,7 @@ class ShapeTimer:
         xq = torch.empty(m * nb * Q8K_BYTES, dtype=torch.uint8, device="cuda")
         y = torch.empty(m * n, dtype=torch.float32, device="cuda")
         gemv = m <= 8
-        need = 0 if gemv else q.plm_gemm_workspace_size(fmt, m, k)
+        need = 0 if gemv else q.plm_gemm_workspace_size_split(fmt, m, n, k)
         work = torch.empty(max(need, 256), dtype=torch.uint8, device="cuda")
         fn = getattr(q, ("plm_gemv_%s" if gemv else "plm_gemm_%s_ws") % fmt)
         s = self.stream

@@ -289,6 +289,16 @@ plm_status plm_gemm_q6K(const void* w, const void* xq, float* y,
  * invalid arguments). */
 size_t plm_gemm_workspace_size(int fmt, int64_t m, int64_t k);
 
+/* Workspace that also holds the partial sums of a K split: when the output
+ * tiles of an m x n problem alone would leave most SMs idle (small m, small
+ * n), the tensor-core GEMM splits K over up to (SMs / tiles) CTAs per tile,
+ * writes each split's f32 partial y into the workspace and adds the splits
+ * in a fixed order (so the result does not depend on timing).  The _ws entry
+ * points split K only when given at least this many bytes; with the smaller
+ * plm_gemm_workspace_size they run unsplit.  0 for invalid arguments and when
+ * no workspace is needed. */
+size_t plm_gemm_workspace_size_split(int fmt, int64_t m, int64_t n, int64_t k);
+
 /* The GEMM with a caller-owned device workspace of at least
  * plm_gemm_workspace_size bytes, 256-byte aligned (may be null when that
  * size is 0).  The workspace must not be used by other work until the call's

@@ -2,7 +2,7 @@
 q4_K / q6_K decode GEMV and prefill GEMM behind a C ABI (include/plm.h)."""
 from .plm import (  # noqa: F401
     PlmError, load, library_path, plm_abi_version, plm_device_fault, plm_probe_mma_rates, plm_quantize_q8K,
-    plm_gemv_q4K, plm_gemv_q6K, plm_gemv_q4K_grouped, plm_gemv_q6K_grouped, plm_gemm_q4K, plm_gemm_q6K, plm_gemm_q4K_noalloc, plm_gemm_q4K_ws, plm_gemm_q6K_ws, plm_gemm_workspace_size,
+    plm_gemv_q4K, plm_gemv_q6K, plm_gemv_q4K_grouped, plm_gemv_q6K_grouped, plm_gemm_q4K, plm_gemm_q6K, plm_gemm_q4K_noalloc, plm_gemm_q4K_ws, plm_gemm_q6K_ws, plm_gemm_workspace_size, plm_gemm_workspace_size_split,
     plm_subdots_q4K, plm_subdots_q6K, plm_quantize_gemv_q4K, plm_quantize_gemv_q4K_grouped,
     plm_gemv_q4K_swiglu, plm_gemv_q4K_swiglu_grouped,
     plm_gemv_q5K, plm_gemv_q5K_grouped, plm_gemm_q5K, plm_gemm_q5K_ws, plm_subdots_q5K, Q5K_BYTES,

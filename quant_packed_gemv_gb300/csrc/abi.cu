@@ -327,6 +327,13 @@ plm_status plm_gemm_q6K(const void* w, const void* xq, float* y, int64_t m, int6
     return gemm_common(6, w, xq, y, m, n, k, stream);
 }
 
+size_t plm_gemm_workspace_size_split(int fmt, int64_t m, int64_t n, int64_t k) {
+    if (fmt < 2 || fmt > 6 || m <= 0 || n <= 0 || k <= 0 || k % plm::QK != 0 || k > kMaxIndex || n > kMaxIndex ||
+        m * n > (int64_t)1 << 40)
+        return 0;
+    return plm::gemm_workspace_need_split(fmt, m, (int)n, (int)k);
+}
+
 size_t plm_gemm_workspace_size(int fmt, int64_t m, int64_t k) {
     if (fmt < 2 || fmt > 6 || m <= 0 || k <= 0 || k % plm::QK != 0 || k > kMaxIndex) return 0;
     return plm::gemm_workspace_need(fmt, m, (int)k);

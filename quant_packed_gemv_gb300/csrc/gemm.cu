@@ -331,11 +331,13 @@ __device__ __forceinline__ void q6K_row_stage(const Q6KRow& R, int c, uint8_t* t
 // The GEMM kernel
 // ---------------------------------------------------------------------------
 struct GemmArgs {
-    const uint8_t* w;        // q4_K or q6_K [n][nb]
+    const uint8_t* w;        // q4_K, q5_K or q6_K [n][nb]
     const uint8_t* xq;       // q8_K [m][nb]
     float* y;                // [m][n]
+    float* part;             // split K: partial sums [gridDim.z][m][n] (null: write y)
     unsigned* fault;
     int m, n, nb;
+    int bsplit;              // blocks of K per split (blockIdx.z)
 };
 
 template <int FMT>
@@ -359,6 +361,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int r0 = blockIdx.x * GT, i0 = blockIdx.y * GT;
     const int nb = A.nb;
+    // this CTA's share of K: blocks [kb0, kb0 + kcount); loop indices below count from kb0
+    const int kb0 = blockIdx.z * A.bsplit;
+    const int kcount = min(A.bsplit, nb - kb0);
 
     if (tid == 0) {
         for (int s = 0; s < NSTAGE; ++s) {
@@ -408,8 +413,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
                 q6K_row_load(dst, A.w + ((size_t)r * nb + b) * Q6K_BYTES, wrow);
             }
         };
-        load_row(R, 0);
-        for (int b = 0; b < nb && ok; ++b) {
+        load_row(R, kb0);
+        for (int b = 0; b < kcount && ok; ++b) {
             const int j = b & 1;
             float dw, dmw = 0.0f;
             if constexpr (FMT != 6) {
@@ -424,7 +429,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
                 if (!ok) break;
             }
             float dx = 0.0f;
-            const uint8_t* xb = A.xq + ((size_t)i * nb + b) * Q8K_BYTES;
+            const uint8_t* xb = A.xq + ((size_t)i * nb + kb0 + b) * Q8K_BYTES;
             if (xrow) dx = __ldg(reinterpret_cast<const float*>(xb));
             if constexpr (FMT != 6) {
                 // min operands: K 0..15 the weight row's mins m_(g/2); K 16..31 the activation row's bsums
@@ -460,7 +465,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
             __syncwarp();
             if (lane == 0) mbar_arrive(&minfull[j]);
 
-            if (b + 1 < nb) load_row(Rn, b + 1);      // next block's bytes, in flight while this one is decoded
+            if (b + 1 < kcount) load_row(Rn, kb0 + b + 1);   // next block's bytes, in flight while this one is decoded
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 const int g = 4 * b + c, s = g % NSTAGE, u = g / NSTAGE;
@@ -468,7 +473,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
                 uint8_t* st = sm + L::RING + s * L::STAGE;
                 if (tid == 0) {
                     mbar_expect_tx(&full[s], TILE_BYTES);
-                    tma_load_2d(st + BOFF, &xmap, b * QK + c * KS, i0, &full[s]);
+                    tma_load_2d(st + BOFF, &xmap, (kb0 + b) * QK + c * KS, i0, &full[s]);
                 }
                 if constexpr (FMT == 5)
                     q5K_row_stage(R, c, st, t);
@@ -485,7 +490,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
     } else if (warp == 8) {
         // ------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            for (int b = 0; b < nb && ok; ++b) {
+            for (int b = 0; b < kcount && ok; ++b) {
                 const int j = b & 1;
                 const uint32_t d1 = tmem + j * 256, d2 = d1 + 128;
                 if (b >= 2 && !mbar_wait(&tempty[j], ((b >> 1) - 1) & 1)) { ok = false; break; }
@@ -530,7 +535,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
         float acc[GT];
 #pragma unroll
         for (int c = 0; c < GT; ++c) acc[c] = 0.0f;
-        for (int b = 0; b < nb && ok; ++b) {
+        for (int b = 0; b < kcount && ok; ++b) {
             const int j = b & 1;
             if (!mbar_wait(&tfull[j], (b >> 1) & 1) || !mbar_wait(&minfull[j], (b >> 1) & 1)) {
                 ok = false;
@@ -562,10 +567,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
             if (lane == 0) mbar_arrive(&tempty[j]);
         }
         const int r = r0 + e;
+        float* out = A.part ? A.part + (size_t)blockIdx.z * A.m * A.n : A.y;
         if (r < A.n) {
 #pragma unroll
             for (int c = 0; c < GT; ++c)
-                if (i0 + c < A.m) A.y[(size_t)(i0 + c) * A.n + r] = acc[c];
+                if (i0 + c < A.m) out[(size_t)(i0 + c) * A.n + r] = acc[c];
         }
     }
     if (!ok && lane == 0) atomicOr(A.fault, 2u);
@@ -600,6 +606,17 @@ __global__ void gemm_x16_kernel(const uint8_t* __restrict__ xq, __half* __restri
     }
 }
 
+// Split K: y = the splits' partial sums, added in split order (deterministic).
+__global__ void gemm_split_reduce_kernel(const float* __restrict__ part, float* __restrict__ y, long long count,
+                                         int splits) {
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < count;
+         i += (long long)gridDim.x * blockDim.x) {
+        float s = part[i];
+        for (int z = 1; z < splits; ++z) s = __fadd_rn(s, part[(size_t)z * count + i]);
+        y[i] = s;
+    }
+}
+
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
@@ -623,11 +640,29 @@ size_t gemm_workspace_bytes(long long m, int k) {
     return (((size_t)m * k * 2) + 255) & ~(size_t)255;
 }
 
+// K splits when the output tiles alone leave most SMs idle: as many as fill
+// the SMs once, each split at least four 256-weight blocks long.
+static int gemm_splits(long long m, int n, int nb) {
+    const long long tiles = (long long)((n + GT - 1) / GT) * ((m + GT - 1) / GT);
+    long long s = num_sms() / (tiles > 0 ? tiles : 1);
+    if (s > nb / 4) s = nb / 4;
+    return s > 1 ? (int)s : 1;
+}
+
+static size_t gemm_split_bytes(long long m, int n, int splits) {
+    return splits > 1 ? (size_t)splits * m * n * sizeof(float) : 0;
+}
+
 template <int FMT>
 static cudaError_t gemm_tc_ws(const uint8_t* w, const uint8_t* xq, float* y, long long m, int n, int k,
-                              void* ws, cudaStream_t stream) {
+                              void* ws, size_t ws_bytes, cudaStream_t stream) {
     const int nb = k / QK;
     __half* x16 = static_cast<__half*>(ws);
+    // split K only when the caller's workspace holds the partial sums too
+    int splits = gemm_splits(m, n, nb);
+    if (ws_bytes < gemm_workspace_bytes(m, k) + gemm_split_bytes(m, n, splits)) splits = 1;
+    float* part = splits > 1 ? reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + gemm_workspace_bytes(m, k))
+                             : nullptr;
     {
         const long long nblocks = m * nb;
         long long grid = (nblocks * 32 + 255) / 256;
@@ -657,11 +692,21 @@ static cudaError_t gemm_tc_ws(const uint8_t* w, const uint8_t* xq, float* y, lon
     A.m = (int)m;
     A.n = n;
     A.nb = nb;
+    A.part = part;
+    A.bsplit = (nb + splits - 1) / splits;
+    splits = (nb + A.bsplit - 1) / A.bsplit;   // no empty split
     constexpr int SMEM = GemmSmem<FMT>::ALLOC;
     cudaError_t e = cudaFuncSetAttribute(gemm_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
     if (e != cudaSuccess) return e;
-    const dim3 grid((unsigned)((n + GT - 1) / GT), (unsigned)((m + GT - 1) / GT));
+    const dim3 grid((unsigned)((n + GT - 1) / GT), (unsigned)((m + GT - 1) / GT), (unsigned)splits);
     gemm_kernel<FMT><<<grid, GEMM_THREADS, SMEM, stream>>>(map, A);
+    e = cudaGetLastError();
+    if (e != cudaSuccess || splits == 1) return e;
+    const long long count = m * (long long)n;
+    long long blocks = (count + 255) / 256;
+    const long long cap = (long long)num_sms() * 8;
+    if (blocks > cap) blocks = cap;
+    gemm_split_reduce_kernel<<<(unsigned)blocks, 256, 0, stream>>>(part, y, count, splits);
     return cudaGetLastError();
 }
 
@@ -679,9 +724,9 @@ cudaError_t launch_gemm_ws(int fmt, const uint8_t* w, const uint8_t* xq, float* 
                            void* ws, size_t ws_bytes, cudaStream_t stream) {
     if (gemm_on_tensor_cores(fmt, m)) {
         if (!ws || ws_bytes < gemm_workspace_bytes(m, k)) return cudaErrorInvalidValue;
-        return fmt == 4 ? gemm_tc_ws<4>(w, xq, y, m, n, k, ws, stream)
-               : fmt == 5 ? gemm_tc_ws<5>(w, xq, y, m, n, k, ws, stream)
-                          : gemm_tc_ws<6>(w, xq, y, m, n, k, ws, stream);
+        return fmt == 4 ? gemm_tc_ws<4>(w, xq, y, m, n, k, ws, ws_bytes, stream)
+               : fmt == 5 ? gemm_tc_ws<5>(w, xq, y, m, n, k, ws, ws_bytes, stream)
+                          : gemm_tc_ws<6>(w, xq, y, m, n, k, ws, ws_bytes, stream);
     }
     const int nb = k / QK;
     for (long long i0 = 0; i0 < m; i0 += GEMV_MAX_M) {
@@ -696,9 +741,14 @@ size_t gemm_workspace_need(int fmt, long long m, int k) {
     return gemm_on_tensor_cores(fmt, m) ? gemm_workspace_bytes(m, k) : 0;
 }
 
+size_t gemm_workspace_need_split(int fmt, long long m, int n, int k) {
+    if (!gemm_on_tensor_cores(fmt, m)) return 0;
+    return gemm_workspace_bytes(m, k) + gemm_split_bytes(m, n, gemm_splits(m, n, k / QK));
+}
+
 cudaError_t launch_gemm(int fmt, const uint8_t* w, const uint8_t* xq, float* y, long long m, int n, int k,
                         cudaStream_t stream) {
-    const size_t need = gemm_workspace_need(fmt, m, k);
+    const size_t need = gemm_workspace_need_split(fmt, m, n, k);
     if (need == 0) return launch_gemm_ws(fmt, w, xq, y, m, n, k, nullptr, 0, stream);
     void* ws = nullptr;
     cudaError_t e = cudaMallocAsync(&ws, need, stream);

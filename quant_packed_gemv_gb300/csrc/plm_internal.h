@@ -52,6 +52,9 @@ cudaError_t launch_gemm(int fmt, const uint8_t* w, const uint8_t* xq, float* y,
 cudaError_t launch_gemm_ws(int fmt, const uint8_t* w, const uint8_t* xq, float* y, long long m, int n, int k,
                            void* ws, size_t ws_bytes, cudaStream_t stream);
 size_t gemm_workspace_need(int fmt, long long m, int k);
+// The same plus the partial sums of a K split (used when the output tiles
+// alone would leave most SMs idle); the _ws form splits K only when given this.
+size_t gemm_workspace_need_split(int fmt, long long m, int n, int k);
 
 // Allocation-free q4_K GEMM: the workspace is a fixed device array inside the
 // library (PLM_NOALLOC_WORKSPACE_BYTES).

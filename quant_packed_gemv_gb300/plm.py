@@ -84,6 +84,8 @@ def load(build_if_missing=True):
     lib.plm_quantize_q8K.restype = ctypes.c_int
     lib.plm_gemm_workspace_size.argtypes = [ctypes.c_int, i64, i64]
     lib.plm_gemm_workspace_size.restype = ctypes.c_size_t
+    lib.plm_gemm_workspace_size_split.argtypes = [ctypes.c_int, i64, i64, i64]
+    lib.plm_gemm_workspace_size_split.restype = ctypes.c_size_t
     for name in ("plm_gemm_q2K_ws", "plm_gemm_q3K_ws", "plm_gemm_q4K_ws", "plm_gemm_q5K_ws", "plm_gemm_q6K_ws"):
         fn = getattr(lib, name)
         fn.argtypes = [vp, vp, vp, i64, i64, i64, vp, ctypes.c_size_t, vp]
@@ -241,6 +243,12 @@ def plm_gemm_workspace_size(fmt, m, k):
     """fmt: 'q2K' .. 'q6K' or 2 .. 6."""
     f = {"q2K": 2, "q3K": 3, "q4K": 4, "q5K": 5, "q6K": 6}.get(fmt, fmt)
     return load().plm_gemm_workspace_size(f, m, k)
+
+
+def plm_gemm_workspace_size_split(fmt, m, n, k):
+    """Workspace bytes that let the GEMM split K (see include/plm.h)."""
+    f = {"q2K": 2, "q3K": 3, "q4K": 4, "q5K": 5, "q6K": 6}.get(fmt, fmt)
+    return load().plm_gemm_workspace_size_split(f, m, n, k)
 
 
 def _gemm_ws(name):

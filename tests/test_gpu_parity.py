@@ -161,15 +161,48 @@ def test_gemm_with_caller_workspace_matches(fmt):
     m, n, k = 150, 260, 2048
     w = make_weights(fmt, 30, 0, n, k)
     xq = oracle.quantize_q8K(gen.normal_f32(30, 1, m, k))
+    # the plain entry takes the split-K workspace from the pool: with the same
+    # workspace size the caller-workspace form runs the same launches
+    full = q.plm_gemm_workspace_size_split(fmt, m, n, k)
+    wsf = torch.empty(max(full, 1), dtype=torch.uint8, device="cuda")
+    yf = torch.full((m, n), float("nan"), device="cuda")
+    getattr(q, "plm_gemm_%s_ws" % fmt)(dev(w), dev(xq), yf, m, n, k, wsf if full else None, full)
+    ref, S = oracle_ref(fmt, w, xq, m, n, k)
+    assert_close(host(yf), ref, S)
+    assert np.array_equal(host(yf), gpu_matmul("gemm", fmt, w, xq, m, n, k))
+    # the minimal workspace: unsplit, within tolerance
     need = q.plm_gemm_workspace_size(fmt, m, k)
     ws = torch.empty(max(need, 1), dtype=torch.uint8, device="cuda")
     y = torch.full((m, n), float("nan"), device="cuda")
     getattr(q, "plm_gemm_%s_ws" % fmt)(dev(w), dev(xq), y, m, n, k, ws if need else None, need)
-    ref, S = oracle_ref(fmt, w, xq, m, n, k)
     assert_close(host(y), ref, S)
-    assert np.array_equal(host(y), gpu_matmul("gemm", fmt, w, xq, m, n, k))
     if need:
         from quant_packed_gemv_gb300 import plm as P
         small = P.raw_status("plm_gemm_%s_ws" % fmt, dev(w).data_ptr(), dev(xq).data_ptr(), y.data_ptr(),
                              m, n, k, ws.data_ptr(), need - 1, None)
         assert small == P.PLM_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("fmt", ["q4K", "q5K", "q6K"])
+@pytest.mark.parametrize("m,n,k", [(64, 256, 4096), (9, 130, 8192), (200, 300, 12288)])
+def test_gemm_split_k(fmt, m, n, k):
+    """Few output tiles: with the larger workspace the GEMM splits K and adds
+    the splits in a fixed order; with the minimal one it does not split.  Both
+    match the oracle, and the split result repeats bit for bit."""
+    import torch
+    import quant_packed_gemv_gb300 as q
+    from tests.gpu_helpers import dev, host
+    w = make_weights(fmt, 40, 0, n, k)
+    xq = oracle.quantize_q8K(gen.normal_f32(40, 2, m, k))
+    ref, S = oracle_ref(fmt, w, xq, m, n, k)
+    wd, xd = dev(w), dev(xq)
+    big, small = q.plm_gemm_workspace_size_split(fmt, m, n, k), q.plm_gemm_workspace_size(fmt, m, k)
+    assert big > small > 0
+    outs = []
+    for need in (big, big, small):
+        ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+        y = torch.full((m, n), float("nan"), device="cuda")
+        getattr(q, "plm_gemm_%s_ws" % fmt)(wd, xd, y, m, n, k, ws, need)
+        outs.append(host(y))
+        assert_close(outs[-1], ref, S)
+    np.testing.assert_array_equal(outs[0], outs[1])
