@@ -3,11 +3,12 @@
 // never widened; the weight stream is read once for all m <= 8 activation
 // rows, as the pages' 8-row activation tile does on the CPU).
 //
-// Work split: as in the generic GEMV (gemv_impl.cuh), the weight bytes of
-// all problems of a launch are split evenly over persistent CTAs; a CTA
-// splits each problem's rows in its range evenly over its warps, and each
-// warp streams its rows through a private ring of 4608-byte stages
-// (32 blocks) filled by bulk copies with bounded mbarrier waits.
+// Work split: the weight stream of all problems of a launch is cut into
+// row-aligned units (one stage each when a row has at most 32 blocks, else
+// one row of several stages), and the units are split evenly over every
+// warp of a persistent grid (one CTA per SM); a warp's range may run across
+// problem boundaries.  Each warp streams its stages through a private ring
+// of 32-block stages filled by bulk copies with bounded mbarrier waits.
 //
 // One warp step consumes one stage: lane L decodes block L of the stage in
 // full (scales, mins, all eight 32-weight sub-blocks) against every
@@ -146,52 +147,123 @@ __device__ __forceinline__ int problem_at(const LaneBatch<MAXP>& B, int W) {
     return r;
 }
 
-// Stages the q8_K blocks of one problem (m rows of nb blocks) for the lanes:
-// records of REC bytes (codes, then eight int16 sums of adjacent bsums) and
-// a float array of the scales.  All threads of the CTA take part.
-__device__ __forceinline__ void act_fill(uint8_t* rec, float* dy, const uint8_t* __restrict__ xq, int nblk) {
-    const uint32_t* src = reinterpret_cast<const uint32_t*>(xq);
-    constexpr int WORDS = Q8K_BYTES / 4;   // 73
-    const int total = nblk * WORDS;
-    for (int idx = threadIdx.x; idx < total; idx += blockDim.x) {
-        const int blk = idx / WORDS;
-        const int wd = idx - blk * WORDS;
-        const uint32_t v = __ldg(src + idx);
-        if (wd == 0) {
-            dy[blk] = __uint_as_float(v);
-        } else if (wd <= 64) {
-            reinterpret_cast<uint32_t*>(rec + (size_t)blk * REC)[wd - 1] = v;
-        } else {
-            const int j = wd - 65;   // bsums 2j, 2j+1
-            const int pair = (int)(int16_t)(v & 0xFFFFu) + (int)(int16_t)(v >> 16);
-            reinterpret_cast<int16_t*>(rec + (size_t)blk * REC + 256)[j] = (int16_t)pair;
-        }
+// Activation staging.  A CTA stages the activations of every problem its
+// warps touch, problems [p0, pend) of the launch, one segment per problem in
+// launch order: m * nb records of REC bytes (the 256 codes, then the eight
+// int16 sums of adjacent bsums), then the m * nb scales d as floats.  The
+// first loads of a thread are issued before its warp fills the weight ring
+// (fill()), so they are not queued behind the first weight stages of every
+// SM; the staging then completes while those stages are in flight.
+
+// Walks a flat index over the concatenated problems [p, pend): problem p
+// covers [lo, hi) and its segment starts off bytes into the staging area.
+struct ActPos {
+    int p, lo, hi, off;
+};
+template <int M, int PER, int MAXP>
+__device__ __forceinline__ ActPos act_begin(const LaneBatch<MAXP>& B, int p0, int pend) {
+    return ActPos{p0, 0, p0 < pend ? M * B.p[p0].nb * PER : 0, 0};
+}
+template <int M, int PER, int MAXP>
+__device__ __forceinline__ void act_seek(const LaneBatch<MAXP>& B, ActPos& a, int idx, int pend) {
+    while (a.p < pend && idx >= a.hi) {
+        a.off += seg_bytes(M * B.p[a.p].nb);
+        a.lo = a.hi;
+        ++a.p;
+        a.hi = a.p < pend ? a.lo + M * B.p[a.p].nb * PER : a.lo;
     }
 }
 
-// Quantizes m rows of f32 activations (nblk 256-value chunks, row-major, so
-// chunk c starts at x + 256 c) straight into the staged layout: one warp per
-// chunk, the warps of the CTA taking chunks in turn.
-template <int WARPS>
-__device__ __forceinline__ void act_fill_f32(uint8_t* rec, float* dy, const float* __restrict__ x, int nblk,
-                                             int warp, int lane) {
-    for (int c = warp; c < nblk; c += WARPS) {
-        const float4* src = reinterpret_cast<const float4*>(x + (size_t)c * QK) + 2 * lane;
-        const float4 a = __ldg(src), b = __ldg(src + 1);
-        const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+// Word w of a problem's q8_K rows (records of 73 words: d, 64 code words,
+// 8 words of bsum pairs) into its staged segment of nblk records.
+__device__ __forceinline__ void act_store(uint8_t* seg, int nblk, int w, uint32_t v) {
+    constexpr int WORDS = Q8K_BYTES / 4;
+    const int blk = w / WORDS;
+    const int wd = w - blk * WORDS;
+    if (wd == 0) {
+        reinterpret_cast<float*>(seg + (size_t)nblk * REC)[blk] = __uint_as_float(v);
+    } else if (wd <= 64) {
+        reinterpret_cast<uint32_t*>(seg + (size_t)blk * REC)[wd - 1] = v;
+    } else {
+        const int j = wd - 65;   // bsums 2j, 2j+1
+        const int pair = (int)(int16_t)(v & 0xFFFFu) + (int)(int16_t)(v >> 16);
+        reinterpret_cast<int16_t*>(seg + (size_t)blk * REC + 256)[j] = (int16_t)pair;
+    }
+}
+
+// q8_K activations: all threads of the CTA copy words, PRE of them per thread
+// loaded before fill().
+template <int M, int PRE, int MAXP, typename Fill>
+__device__ __forceinline__ void stage_q8(const LaneBatch<MAXP>& B, int p0, int pend, uint8_t* smem, Fill fill) {
+    constexpr int WORDS = Q8K_BYTES / 4;
+    const int tid = threadIdx.x, bd = blockDim.x;
+    uint32_t pre[PRE];
+    ActPos a = act_begin<M, WORDS>(B, p0, pend);
+#pragma unroll
+    for (int j = 0; j < PRE; ++j) {
+        const int idx = tid + j * bd;
+        act_seek<M, WORDS>(B, a, idx, pend);
+        pre[j] = a.p < pend ? __ldg(reinterpret_cast<const uint32_t*>(B.p[a.p].xq) + (idx - a.lo)) : 0u;
+    }
+    fill();
+    a = act_begin<M, WORDS>(B, p0, pend);
+#pragma unroll
+    for (int j = 0; j < PRE; ++j) {
+        const int idx = tid + j * bd;
+        act_seek<M, WORDS>(B, a, idx, pend);
+        if (a.p < pend) act_store(smem + a.off, M * B.p[a.p].nb, idx - a.lo, pre[j]);
+    }
+    for (int idx = tid + PRE * bd;; idx += bd) {
+        act_seek<M, WORDS>(B, a, idx, pend);
+        if (a.p >= pend) break;
+        act_store(smem + a.off, M * B.p[a.p].nb, idx - a.lo,
+                  __ldg(reinterpret_cast<const uint32_t*>(B.p[a.p].xq) + (idx - a.lo)));
+    }
+}
+
+// f32 activations (the fused producer): the CTA quantizes each 256-value
+// chunk straight into the staged layout, one warp per chunk, the warps
+// taking the chunks of all its problems in turn (chunk c of a problem's m
+// rows starts at x + 256 c); a warp's first chunk is loaded before fill().
+template <int M, int WARPS, int MAXP, typename Fill>
+__device__ __forceinline__ void stage_f32(const LaneBatch<MAXP>& B, int p0, int pend, uint8_t* smem, int warp,
+                                          int lane, Fill fill) {
+    ActPos a = act_begin<M, 1>(B, p0, pend);
+    int fc = warp;
+    act_seek<M, 1>(B, a, fc, pend);
+    float4 v0 = make_float4(0.f, 0.f, 0.f, 0.f), v1 = v0;
+    if (a.p < pend) {
+        const float4* src = reinterpret_cast<const float4*>(B.p[a.p].xq) + (size_t)(fc - a.lo) * (QK / 4) + 2 * lane;
+        v0 = __ldg(src);
+        v1 = __ldg(src + 1);
+    }
+    fill();
+    while (a.p < pend) {
+        const int nblk = M * B.p[a.p].nb;
+        const int c = fc - a.lo;
+        uint8_t* seg = smem + a.off;
+        const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
         int q[8];
         const float d = q8K_quantize_warp(v, lane, q);
         uint32_t w0, w1;
         pack_codes8(q, w0, w1);
-        uint32_t* dst = reinterpret_cast<uint32_t*>(rec + (size_t)c * REC) + 2 * lane;
+        uint32_t* dst = reinterpret_cast<uint32_t*>(seg + (size_t)c * REC) + 2 * lane;
         dst[0] = w0;
         dst[1] = w1;
         // lanes 4j .. 4j+3 hold values 32j .. 32j+31: the sum of bsums 2j and 2j+1
-        int s = q[0] + q[1] + q[2] + q[3] + q[4] + q[5] + q[6] + q[7];
-        s += __shfl_xor_sync(0xFFFFFFFFu, s, 1);
-        s += __shfl_xor_sync(0xFFFFFFFFu, s, 2);
-        if ((lane & 3) == 0) reinterpret_cast<int16_t*>(rec + (size_t)c * REC + 256)[lane >> 2] = (int16_t)s;
-        if (lane == 0) dy[c] = d;
+        int sq = q[0] + q[1] + q[2] + q[3] + q[4] + q[5] + q[6] + q[7];
+        sq += __shfl_xor_sync(0xFFFFFFFFu, sq, 1);
+        sq += __shfl_xor_sync(0xFFFFFFFFu, sq, 2);
+        if ((lane & 3) == 0) reinterpret_cast<int16_t*>(seg + (size_t)c * REC + 256)[lane >> 2] = (int16_t)sq;
+        if (lane == 0) reinterpret_cast<float*>(seg + (size_t)nblk * REC)[c] = d;
+        fc += WARPS;
+        act_seek<M, 1>(B, a, fc, pend);
+        if (a.p < pend) {
+            const float4* src =
+                reinterpret_cast<const float4*>(B.p[a.p].xq) + (size_t)(fc - a.lo) * (QK / 4) + 2 * lane;
+            v0 = __ldg(src);
+            v1 = __ldg(src + 1);
+        }
     }
 }
 
@@ -348,22 +420,18 @@ __global__ void __launch_bounds__(WARPS * 32, 1) lane_kernel(const __grid_consta
         ++issued;
         cursor_next(B, ic, nb, W0, W1, PF);
     };
-    while (ic.p >= 0 && issued < (uint32_t)NS) issue_one();
-
-    // stage the activations of every problem the CTA's warps touch
+    // stage the activations of every problem the CTA's warps touch, filling
+    // the ring once the first activation loads are out
     const int cfirst = problem_at(B, C0);
-    {
-        int off = 0;
-        for (int p = cfirst; p < B.count && B.p[p].wbegin < C1; ++p) {
-            const int nblk = M * B.p[p].nb;
-            float* dy = reinterpret_cast<float*>(smem + off + (size_t)nblk * REC);
-            if constexpr (XF32)
-                act_fill_f32<WARPS>(smem + off, dy, reinterpret_cast<const float*>(B.p[p].xq), nblk, warp, lane);
-            else
-                act_fill(smem + off, dy, B.p[p].xq, nblk);
-            off += seg_bytes(nblk);
-        }
-    }
+    int cend = cfirst;
+    while (cend < B.count && B.p[cend].wbegin < C1) ++cend;
+    auto fill = [&]() {
+        while (ic.p >= 0 && issued < (uint32_t)NS) issue_one();
+    };
+    if constexpr (XF32)
+        stage_f32<M, WARPS>(B, cfirst, cend, smem, warp, lane, fill);
+    else
+        stage_q8<M, 8>(B, cfirst, cend, smem, fill);
     __syncthreads();
 
     Cursor cc;
@@ -515,6 +583,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1) lane_kernel(const __grid_consta
 struct Config {
     int warps, ns, grid, act_bytes;
 };
+
 
 template <int FMT>
 inline size_t ring_bytes(int warps, int ns) { return (size_t)warps * ns * (slot_bytes<FMT>() + 8); }
