@@ -65,6 +65,34 @@ typedef enum {
 /* ABI version of the loaded library (PLM_ABI_VERSION at build time). */
 int plm_abi_version(void);
 
+/*
+ * Early launch (no counterpart on the pages; a GB300 scheduling feature).
+ * Process-wide mode for every kernel launched after the call:
+ *   PLM_OVERLAP_OFF       plain stream order: a kernel starts when the work
+ *                         before it on the stream has finished.
+ *   PLM_OVERLAP_LAUNCH    (default) kernels are launched with programmatic
+ *                         stream serialization: a kernel may be scheduled
+ *                         while the kernel before it is still running, and
+ *                         waits for that kernel and its memory writes before
+ *                         its own first memory access.  Results are the same
+ *                         as in plain order; the launch latency is hidden.
+ *   PLM_OVERLAP_PREFETCH  as PLM_OVERLAP_LAUNCH, and a GEMV may start copying
+ *                         its weight bytes before that wait (activations are
+ *                         read and y written only after it), so its weight
+ *                         stream overlaps the tail of the kernel before it.
+ *                         The caller guarantees that no kernel issued earlier
+ *                         on the same stream writes the weight bytes of a
+ *                         GEMV call (weights are immutable once loaded);
+ *                         otherwise the GEMV may read stale weights.
+ * Returns the previous mode, or -PLM_ERR_INVALID_ARG (mode unchanged) for
+ * any other value.  Safe to call from any thread; launches already enqueued
+ * keep the mode they were issued with.
+ */
+#define PLM_OVERLAP_OFF 0
+#define PLM_OVERLAP_LAUNCH 1
+#define PLM_OVERLAP_PREFETCH 2
+int plm_set_overlap(int mode);
+
 /* Static, NUL-terminated name of a status code; "unknown status" otherwise. */
 const char* plm_status_string(int status);
 

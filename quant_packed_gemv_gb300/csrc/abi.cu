@@ -1,5 +1,6 @@
 // The C ABI of libplm: argument checks on the host, then one or more kernel
 // launches on the caller's stream.  Nothing is allocated and nothing waits.
+#include <atomic>
 #include <cstdint>
 
 #include "../../include/plm.h"
@@ -25,6 +26,11 @@ unsigned* fault_word() {
     if (dev >= 0 && dev < 64) cache[dev] = p;
     return static_cast<unsigned*>(p);
 }
+
+namespace {
+std::atomic<int> g_overlap{1};
+}
+int overlap_mode() { return g_overlap.load(std::memory_order_relaxed); }
 
 int num_sms() {
     int dev = 0, n = 0;
@@ -186,6 +192,11 @@ plm_status subdots_common(int fmt, const void* w, const void* xq, int32_t* out, 
 extern "C" {
 
 int plm_abi_version(void) { return PLM_ABI_VERSION; }
+
+int plm_set_overlap(int mode) {
+    if (mode < PLM_OVERLAP_OFF || mode > PLM_OVERLAP_PREFETCH) return -PLM_ERR_INVALID_ARG;
+    return plm::g_overlap.exchange(mode);
+}
 
 const char* plm_status_string(int status) {
     switch (status) {

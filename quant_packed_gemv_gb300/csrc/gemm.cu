@@ -383,6 +383,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
                      :: "r"(smem_u32(tmem_slot)) : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
+    grid_launch_dependents();
+    grid_wait_prior();   // global memory only after the kernels before this one end
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -585,6 +587,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
 
 // q8_K codes -> f16 activation matrix [m][k] (the GEMM's B operand source)
 __global__ void gemm_x16_kernel(const uint8_t* __restrict__ xq, __half* __restrict__ x16, long long nblocks) {
+    grid_launch_dependents();
+    grid_wait_prior();
     const long long total = nblocks * 32;                 // 8 codes per item
     for (long long it = (long long)blockIdx.x * blockDim.x + threadIdx.x; it < total;
          it += (long long)gridDim.x * blockDim.x) {
@@ -609,6 +613,8 @@ __global__ void gemm_x16_kernel(const uint8_t* __restrict__ xq, __half* __restri
 // Split K: y = the splits' partial sums, added in split order (deterministic).
 __global__ void gemm_split_reduce_kernel(const float* __restrict__ part, float* __restrict__ y, long long count,
                                          int splits) {
+    grid_launch_dependents();
+    grid_wait_prior();
     for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < count;
          i += (long long)gridDim.x * blockDim.x) {
         float s = part[i];
@@ -668,8 +674,7 @@ static cudaError_t gemm_tc_ws(const uint8_t* w, const uint8_t* xq, float* y, lon
         long long grid = (nblocks * 32 + 255) / 256;
         const long long cap = (long long)num_sms() * 8;
         if (grid > cap) grid = cap;
-        gemm_x16_kernel<<<(unsigned)grid, 256, 0, stream>>>(xq, x16, nblocks);
-        cudaError_t e = cudaGetLastError();
+        cudaError_t e = launch_kernel(gemm_x16_kernel, dim3((unsigned)grid), dim3(256), 0, stream, xq, x16, nblocks);
         if (e != cudaSuccess) return e;
     }
     EncodeTiledFn enc = encode_fn();
@@ -699,15 +704,14 @@ static cudaError_t gemm_tc_ws(const uint8_t* w, const uint8_t* xq, float* y, lon
     cudaError_t e = cudaFuncSetAttribute(gemm_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
     if (e != cudaSuccess) return e;
     const dim3 grid((unsigned)((n + GT - 1) / GT), (unsigned)((m + GT - 1) / GT), (unsigned)splits);
-    gemm_kernel<FMT><<<grid, GEMM_THREADS, SMEM, stream>>>(map, A);
-    e = cudaGetLastError();
+    e = launch_kernel(gemm_kernel<FMT>, grid, dim3(GEMM_THREADS), SMEM, stream, map, A);
     if (e != cudaSuccess || splits == 1) return e;
     const long long count = m * (long long)n;
     long long blocks = (count + 255) / 256;
     const long long cap = (long long)num_sms() * 8;
     if (blocks > cap) blocks = cap;
-    gemm_split_reduce_kernel<<<(unsigned)blocks, 256, 0, stream>>>(part, y, count, splits);
-    return cudaGetLastError();
+    return launch_kernel(gemm_split_reduce_kernel, dim3((unsigned)blocks), dim3(256), 0, stream,
+                         (const float*)part, y, count, splits);
 }
 
 // Below this many activation rows the decode GEMV kernels (eight rows at a

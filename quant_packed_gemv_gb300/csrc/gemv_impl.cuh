@@ -90,6 +90,7 @@ struct GemvBatch {
     int count;
     int nstages;            // ring depth per warp
     int act_bytes;          // 128-aligned size of the staged-activation region
+    int prefetch;           // copy weights before waiting for the kernels before this one
     GemvProblem p[MAXP];
 };
 
@@ -337,6 +338,10 @@ __global__ void __launch_bounds__(WARPS * 32, 1) gemv_kernel(const __grid_consta
         fence_barrier_init();
     }
     __syncwarp();
+    grid_launch_dependents();
+    // without weight prefetch, nothing is touched before the earlier kernels end
+    bool waited = !B.prefetch;
+    if (waited) grid_wait_prior();
 
     const long long T = B.total_bytes;
     const long long B0 = T * blockIdx.x / gridDim.x;
@@ -398,6 +403,10 @@ __global__ void __launch_bounds__(WARPS * 32, 1) gemv_kernel(const __grid_consta
         if (ok)
             while (inext < nst && issued - consumed < (uint32_t)NS) issue_one();
 
+        if (!waited) {   // activations are read, and y written, only after the earlier kernels end
+            grid_wait_prior();
+            waited = true;
+        }
         const bool packed = nb <= BLOCKS_PER_STEP && (BLOCKS_PER_STEP % nb) == 0;
         ActSmem act{};
         LaneAct areg[AREG ? 2 : 1][M];
@@ -651,8 +660,9 @@ cudaError_t launch_batch(const HostProblem* hp, int count, int max_nb, int ns, c
     const long long want = (rows + 7) / 8;
     if (grid > want) grid = want;
     if (grid < 1) grid = 1;
-    gemv_kernel<FMT, M, SUB, WARPS, MAXP, AREG><<<(unsigned)grid, WARPS * 32, smem, stream>>>(B);
-    return cudaGetLastError();
+    B.prefetch = overlap_mode() >= 2 ? 1 : 0;
+    return launch_kernel(gemv_kernel<FMT, M, SUB, WARPS, MAXP, AREG>, dim3((unsigned)grid), dim3(WARPS * 32), smem,
+                         stream, B);
 }
 
 // Launches one pass (all problems share m = M rows of activations).

@@ -85,6 +85,7 @@ struct LaneBatch {
     int nstages;            // ring depth per warp
     int act_bytes;          // staged-activation region (all problems of the CTA)
     int wtotal;             // weighted units of the launch
+    int prefetch;           // copy weights before waiting for the kernels before this one
     LaneProblem p[MAXP];
 };
 
@@ -380,6 +381,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1) lane_kernel(const __grid_consta
         fence_barrier_init();
     }
     __syncwarp();
+    grid_launch_dependents();
 
     // even split of the weighted units over all warps of the grid
     const long long G = (long long)gridDim.x * WARPS;
@@ -428,6 +430,10 @@ __global__ void __launch_bounds__(WARPS * 32, 1) lane_kernel(const __grid_consta
     auto fill = [&]() {
         while (ic.p >= 0 && issued < (uint32_t)NS) issue_one();
     };
+    // weights first when they may be copied before the earlier kernels end
+    // (nothing before this launch writes them); activations only after
+    if (B.prefetch) fill();
+    grid_wait_prior();
     if constexpr (XF32)
         stage_f32<M, WARPS>(B, cfirst, cend, smem, warp, lane, fill);
     else
@@ -663,12 +669,13 @@ cudaError_t launch(const HostProblem* hp, int count, const Plan& pl, const Confi
     B.nstages = cfg.ns;
     B.act_bytes = cfg.act_bytes;
     B.wtotal = (int)pl.wtotal;
+    B.prefetch = overlap_mode() >= 2 ? 1 : 0;
     const size_t smem = (size_t)cfg.act_bytes + ring_bytes<FMT>(WARPS, cfg.ns);
     const void* fn = (const void*)lane_kernel<FMT, M, SUB, XF32, PAIR, WARPS, MAXP>;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    lane_kernel<FMT, M, SUB, XF32, PAIR, WARPS, MAXP><<<(unsigned)cfg.grid, WARPS * 32, smem, stream>>>(B);
-    return cudaGetLastError();
+    return launch_kernel(lane_kernel<FMT, M, SUB, XF32, PAIR, WARPS, MAXP>, dim3((unsigned)cfg.grid),
+                         dim3(WARPS * 32), smem, stream, B);
 }
 
 // Launches one pass of M activation rows; false in *fits when no ring and

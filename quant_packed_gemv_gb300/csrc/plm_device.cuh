@@ -8,6 +8,12 @@
 
 namespace plm {
 
+// Early launch: let the next kernel of the stream be scheduled, and wait for
+// the kernels before this one (and their memory) before touching memory
+// they write.  Both are no-ops for a kernel launched in plain stream order.
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void grid_wait_prior() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 constexpr int QK = 256;          // weights (or activations) per block
 constexpr int Q2K_BYTES = 84;    // scales[16], qs[64], f16 d, f16 dmin
 constexpr int Q3K_BYTES = 110;   // hmask[32], qs[64], scales[12], f16 d

@@ -2,12 +2,37 @@
 #pragma once
 
 #include <cstdint>
+#include <utility>
 #include <cuda_runtime.h>
 
 namespace plm {
 
 // Number of SMs of the current device (queried per call; no cached state).
 int num_sms();
+
+// Early launch of the library's kernels (plm_set_overlap): 0 plain stream
+// order; 1 a kernel may be scheduled while the kernel before it on the stream
+// is still running and waits for it (griddepcontrol.wait) before its first
+// memory access; 2 as 1, and a GEMV may copy weight bytes before that wait.
+int overlap_mode();
+
+// Launches kernel k, marked for early launch when overlap_mode() >= 1 (the
+// kernel must then wait before touching memory that earlier work writes).
+template <typename... P, typename... A>
+inline cudaError_t launch_kernel(void (*k)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                                 A&&... args) {
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = grid;
+    lc.blockDim = block;
+    lc.dynamicSmemBytes = smem;
+    lc.stream = stream;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = at;
+    lc.numAttrs = overlap_mode() >= 1 ? 1 : 0;
+    return cudaLaunchKernelEx(&lc, k, std::forward<A>(args)...);
+}
 
 // Device address of the library's fault word on the current device (set by a
 // kernel whose bounded wait ran out), or nullptr if it cannot be resolved.

@@ -12,6 +12,8 @@ namespace plm {
 __global__ void __launch_bounds__(256) quantize_q8K_kernel(const float* __restrict__ x,
                                                            uint8_t* __restrict__ xq,
                                                            long long nchunks) {
+    grid_launch_dependents();
+    grid_wait_prior();
     const int lane = threadIdx.x & 31;
     const long long warp0 = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
@@ -47,8 +49,7 @@ cudaError_t launch_quantize_q8K(const float* x, uint8_t* xq, long long m, long l
     long long blocks = (nchunks + 7) / 8;
     const long long cap = (long long)num_sms() * 16;
     if (blocks > cap) blocks = cap;
-    quantize_q8K_kernel<<<(unsigned)blocks, threads, 0, stream>>>(x, xq, nchunks);
-    return cudaGetLastError();
+    return launch_kernel(quantize_q8K_kernel, dim3((unsigned)blocks), dim3(threads), 0, stream, x, xq, nchunks);
 }
 
 }  // namespace plm

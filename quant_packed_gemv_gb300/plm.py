@@ -72,6 +72,8 @@ def load(build_if_missing=True):
     vp, i64 = ctypes.c_void_p, ctypes.c_int64
     lib.plm_abi_version.argtypes = []
     lib.plm_abi_version.restype = ctypes.c_int
+    lib.plm_set_overlap.argtypes = [ctypes.c_int]
+    lib.plm_set_overlap.restype = ctypes.c_int
     lib.plm_status_string.argtypes = [ctypes.c_int]
     lib.plm_status_string.restype = ctypes.c_char_p
     lib.plm_last_cuda_error.argtypes = []
@@ -140,6 +142,18 @@ def _check(fn, status):
 
 def plm_abi_version():
     return load().plm_abi_version()
+
+
+PLM_OVERLAP_OFF, PLM_OVERLAP_LAUNCH, PLM_OVERLAP_PREFETCH = 0, 1, 2
+
+
+def plm_set_overlap(mode):
+    """Early-launch mode for later launches (PLM_OVERLAP_*); returns the previous mode."""
+    lib = load()
+    r = lib.plm_set_overlap(int(mode))
+    if r < 0:
+        raise PlmError("plm_set_overlap", -r, lib)
+    return r
 
 
 def plm_device_fault(clear=True):

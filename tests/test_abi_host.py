@@ -37,6 +37,20 @@ def test_abi_version_and_status_strings():
     assert lib.plm_last_cuda_error() == 0
 
 
+def test_overlap_mode_setting():
+    prev = q.plm_set_overlap(q.PLM_OVERLAP_OFF)
+    try:
+        assert prev == q.PLM_OVERLAP_LAUNCH   # the default; every test restores it
+        assert q.plm_set_overlap(q.PLM_OVERLAP_PREFETCH) == q.PLM_OVERLAP_OFF
+        assert q.plm_set_overlap(q.PLM_OVERLAP_LAUNCH) == q.PLM_OVERLAP_PREFETCH
+        for bad in (3, -1, 1 << 20):
+            with pytest.raises(q.PlmError):
+                q.plm_set_overlap(bad)
+        assert q.plm_set_overlap(q.PLM_OVERLAP_LAUNCH) == q.PLM_OVERLAP_LAUNCH
+    finally:
+        q.plm_set_overlap(prev)
+
+
 A = 1 << 20  # a 16-byte aligned fake address; never dereferenced: every call below is rejected
 
 
