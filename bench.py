@@ -10,7 +10,10 @@ rows to q8_K (one launch: all k are multiples of 256, so the rows form one
 flat array of 256-element chunks) and runs the 196 GEMVs through the grouped
 entry point (one launch).  The weight set is held twice and consecutive
 steps alternate copies; each copy is larger than the 129 MB L2, so weights
-come from HBM.
+come from HBM.  The K timed steps replay as one CUDA graph, launched with
+plm_set_overlap(--overlap, default 2): each kernel is scheduled while the
+one before it drains and starts copying its weights (which nothing writes)
+before it waits for that kernel; activations are read only after the wait.
 
 Reported beside it (same JSON line):
   decode_chain  the same layers run as a decoder must run them: per layer
@@ -74,6 +77,9 @@ def parse():
                     help="skip the dependent per-layer decode chain measurement")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the prefill GEMM, q6_K head and m-sweep measurements")
+    ap.add_argument("--overlap", type=int, default=2, choices=[0, 1, 2],
+                    help="plm_set_overlap mode: 0 plain stream order, 1 early launch, "
+                         "2 early launch with weight prefetch (the weights here are never written)")
     return ap.parse_args()
 
 
@@ -249,6 +255,7 @@ def time_case(args):
     w_host = getattr(gen, "%s_blocks" % fmt)(4, 0, n, k)
     ws = [torch.from_numpy(w_host).cuda() for _ in range(copies)]
     fn = getattr(q, "plm_%s_%s" % (kind, fmt))
+    q.plm_set_overlap(args.overlap)
     stream = torch.cuda.Stream()
     for m in args.m:
         x = torch.from_numpy(gen.normal_f32(4, 9, m, k)).cuda()
@@ -503,42 +510,40 @@ def main():
     st = Step(torch, dev, mats, host_w, xs)
     stream = torch.cuda.Stream(device=dev)
 
+    q.plm_set_overlap(args.overlap)
     st.fused = [st.fused_problems(c) for c in range(2)]
+    gate_up = [st.gate_up(c) for c in range(2)]
+    K = args.steps
     with torch.cuda.stream(stream):
         for i in range(max(args.warmup, 3)):
             st.run(q, i % 2, stream)
             st.run_fused(q, i % 2, stream)
+            q.plm_gemv_q4K_swiglu_grouped(gate_up[i % 2][0], 1, stream=stream)
+            q.plm_gemv_q4K_grouped(gate_up[i % 2][1], 1, stream=stream)
             if not args.no_chain:
                 st.run_chain(q, i % 2, stream)
     torch.cuda.synchronize()
-    graphs, gemv_graphs, chain_graphs, fused_graphs = [], [], [], []
-    swiglu_graphs, gateup_graphs = [], []
-    for c in range(2):
-        pairs, plain = st.gate_up(c)
-        with torch.cuda.stream(stream):
-            q.plm_gemv_q4K_swiglu_grouped(pairs, 1, stream=stream)
-            q.plm_gemv_q4K_grouped(plain, 1, stream=stream)
-        torch.cuda.synchronize()
-        for lst, fn, arg in ((swiglu_graphs, q.plm_gemv_q4K_swiglu_grouped, pairs),
-                             (gateup_graphs, q.plm_gemv_q4K_grouped, plain)):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                fn(arg, 1, stream=stream)
-            lst.append(g)
+
+    def capture(fn, steps):
+        """One CUDA graph of `steps` consecutive steps, weight copies alternating."""
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
-            st.run_fused(q, c, stream)
-        fused_graphs.append(g)
-        for lst, kw in ((graphs, {}), (gemv_graphs, {"quantize": False})):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                st.run(q, c, stream, **kw)
-            lst.append(g)
-        if not args.no_chain:
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                st.run_chain(q, c, stream)
-            chain_graphs.append(g)
+            for s in range(steps):
+                fn(s)
+        return g
+
+    run_step = lambda s: st.run(q, s % 2, stream)
+    run_gemv = lambda s: st.run(q, s % 2, stream, quantize=False)
+    run_fused = lambda s: st.run_fused(q, s % 2, stream)
+    run_swiglu = lambda s: q.plm_gemv_q4K_swiglu_grouped(gate_up[s % 2][0], 1, stream=stream)
+    run_gateup = lambda s: q.plm_gemv_q4K_grouped(gate_up[s % 2][1], 1, stream=stream)
+    run_chain = lambda s: st.run_chain(q, s % 2, stream)
+    # the timed graphs: K steps each; single-step graphs: the end-to-end loop
+    # and a per-step comparison
+    step_g, gemv_g, fused_g = capture(run_step, K), capture(run_gemv, K), capture(run_fused, K)
+    swiglu_g, gateup_g = capture(run_swiglu, K), capture(run_gateup, K)
+    chain_g = None if args.no_chain else capture(run_chain, K)
+    single = [capture(lambda s, c=c: st.run(q, c, stream), 1) for c in range(2)]
     torch.cuda.synchronize()
 
     def barrier():
@@ -562,32 +567,36 @@ def main():
             ms = float(t.item())
         return ms
 
+    def timed_graph(g):
+        g.replay()                       # untimed: graph upload
+        torch.cuda.synchronize()
+        return timed(lambda s: g.replay(), 1)
+
     h2d = st.x_host.numel() * 4
     d2h = st.y_host.numel() * 4
 
     def e2e_step(s):
         st.x.copy_(st.x_host, non_blocking=True)
-        graphs[s % 2].replay()
+        single[s % 2].replay()
         st.y_host.copy_(st.y, non_blocking=True)
 
     with torch.cuda.stream(stream):
         for s in range(args.warmup):
-            graphs[s % 2].replay()
-            if chain_graphs:
-                chain_graphs[s % 2].replay()
+            single[s % 2].replay()
             e2e_step(s)
         torch.cuda.synchronize()
         sampler = ClockSampler(local)
         sampler.start()
         time.sleep(0.3)
-        ms = timed(lambda s: graphs[s % 2].replay(), args.steps)
-        gemv_ms = timed(lambda s: gemv_graphs[s % 2].replay(), args.steps)
-        fused_ms = timed(lambda s: fused_graphs[s % 2].replay(), args.steps)
-        swiglu_ms = timed(lambda s: swiglu_graphs[s % 2].replay(), args.steps)
-        gateup_ms = timed(lambda s: gateup_graphs[s % 2].replay(), args.steps)
-        chain_ms = timed(lambda s: chain_graphs[s % 2].replay(), args.steps) if chain_graphs else None
+        ms = timed_graph(step_g)
+        gemv_ms = timed_graph(gemv_g)
+        fused_ms = timed_graph(fused_g)
+        swiglu_ms = timed_graph(swiglu_g)
+        gateup_ms = timed_graph(gateup_g)
+        chain_ms = timed_graph(chain_g) if chain_g is not None else None
+        single_ms = timed(lambda s: single[s % 2].replay(), K)
         t0 = time.perf_counter()
-        e2e_ms = timed(e2e_step, args.steps)
+        e2e_ms = timed(e2e_step, K)
         e2e_wall = (time.perf_counter() - t0) * 1e3
         clocks = sampler.stop()
     fault = q.plm_device_fault()
@@ -623,7 +632,11 @@ def main():
         "config": {"workload": WORKLOAD, "m": 1, "seed": SEED,
                    "weights_mb": sum(n * (k // QK) * Q4K_BYTES for _, _, n, k, _ in mats) / 1e6,
                    "l2": "inputs larger than L2: two 247.7 MB weight copies, alternate steps",
-                   "launch": "CUDA graph: 1 q8_K quantize + %d grouped GEMV launch(es)" % launches_grouped},
+                   "launch": "per step 1 q8_K quantize + %d grouped GEMV launch(es); the K timed steps "
+                             "replay as one CUDA graph" % launches_grouped,
+                   "overlap": {0: "plain stream order", 1: "early launch",
+                               2: "early launch with weight prefetch"}[args.overlap]},
+        "ms_per_step_one_graph_per_step": single_ms / args.steps,
         "weights_per_s": world * sum(n * k for _, _, n, k, _ in mats) / (ms_step * 1e-3),
         "gpu_launches": (1 + launches_grouped) * args.steps,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
