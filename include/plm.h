@@ -346,7 +346,9 @@ plm_status plm_gemm_q6K_ws(const void* w, const void* xq, float* y, int64_t m, i
  * memory while running, such as an engine whose memory is entirely claimed
  * by its own allocator at start-up, or a latency-critical loop that cannot
  * afford an allocation that might fail or wait.
- *   - Limit: 2*m*k bytes of workspace (m >= 9; smaller m needs none) must fit
+ *   - Limit: the workspace of plm_gemm_workspace_size(4, m, k) (2*m*k bytes
+ *     of f16 codes plus 48 bytes per 256-value block of activations, for
+ *     m >= 9; smaller m needs none) must fit
  *     PLM_NOALLOC_WORKSPACE_BYTES; larger problems return
  *     PLM_ERR_UNSUPPORTED and enqueue nothing.
  *   - Calls no cudaMalloc, cudaFree or allocating routine.  Every device

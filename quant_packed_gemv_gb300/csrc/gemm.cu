@@ -27,7 +27,11 @@
 //     the A operand (f16, 128-byte swizzled K-major, one 64-wide K stage
 //     at a time), writes the per-block min operands and scales, and warp 0
 //     issues the TMA load of the activation stage (f16, same layout) from
-//     the workspace the pre-pass fills;
+//     the workspace the pre-pass fills.  q4_K / q5_K: the raw weight
+//     blocks of the tile (128 rows x one 256-weight block) and the
+//     activations' per-block d_x and bsums arrive by TMA into a ring of
+//     block slots, two blocks ahead of the decode; q6_K rows (210 bytes, not
+//     a 16-byte multiple) are read by each producer thread one block ahead;
 //   warp 8 (one thread): issues the MMAs (M=128, N=128, K=16) and commits;
 //   warps 4-7 (epilogue): drain D1/D2 of each block from TMEM, apply the
 //     scales and accumulate the result in registers; store y at the end.
@@ -49,13 +53,22 @@ constexpr int GT = 128;                 // tile rows (weights) and columns (acti
 constexpr int KS = 64;                  // K per operand stage (one 128-byte swizzle row)
 constexpr int TILE_BYTES = GT * KS * 2; // 16 KB per operand tile
 constexpr int GEMM_THREADS = 9 * 32;
+// per (activation row, 256-value block) in the workspace: the eight bsum
+// words of the q8_K block (16 int16), its d as f32 bits, three zero words
+constexpr int AUXB = 48;
 
 // q4_K: one A tile per stage plus per-block min operands; q6_K: two A tiles
 // per stage (the high and low parts of the scale), no min term.
+// BSLOTS: slots of the TMA-fed ring of raw weight blocks (WROW bytes per
+// weight row) and activation side data; 0 for q6_K.
 template <int FMT> struct GemmCfg;
-template <> struct GemmCfg<4> { static constexpr int ATILES = 1, NSTAGE = 4, MINB = 2 * TILE_BYTES; };
-template <> struct GemmCfg<5> : GemmCfg<4> {};   // q5_K: q4_K's operands, a fifth bit per weight
-template <> struct GemmCfg<6> { static constexpr int ATILES = 2, NSTAGE = 3, MINB = 0; };
+template <> struct GemmCfg<4> {
+    static constexpr int ATILES = 1, NSTAGE = 4, MINB = 2 * TILE_BYTES, BSLOTS = 2, WROW = Q4K_BYTES;
+};
+template <> struct GemmCfg<5> {   // q5_K: q4_K's operands, a fifth bit per weight
+    static constexpr int ATILES = 1, NSTAGE = 4, MINB = 2 * TILE_BYTES, BSLOTS = 2, WROW = Q5K_BYTES;
+};
+template <> struct GemmCfg<6> { static constexpr int ATILES = 2, NSTAGE = 3, MINB = 0, BSLOTS = 0, WROW = 0; };
 
 template <int FMT>
 struct GemmSmem {
@@ -65,8 +78,12 @@ struct GemmSmem {
     static constexpr int RING = 0;
     static constexpr int MIN = RING + NSTAGE * STAGE;                        // q4_K: 2 x 16 KB
     static constexpr int SCL = MIN + GemmCfg<FMT>::MINB;                     // 2 x (d, dmin, dx) x 128 f32
-    static constexpr int BAR = SCL + 2 * 3 * GT * 4;
-    static constexpr int NBAR = 2 * NSTAGE + 8;
+    static constexpr int WT = GT * GemmCfg<FMT>::WROW;                       // raw weight tile of one block
+    static constexpr int BTX = WT + GT * AUXB;                               // bytes landing per block slot
+    static constexpr int BSLOT = (BTX + 1023) & ~1023;
+    static constexpr int BRING = (SCL + 2 * 3 * GT * 4 + 1023) & ~1023;
+    static constexpr int BAR = BRING + GemmCfg<FMT>::BSLOTS * BSLOT;
+    static constexpr int NBAR = 2 * NSTAGE + 8 + 2 * GemmCfg<FMT>::BSLOTS;
     static constexpr int TMEMP = BAR + NBAR * 8;
     static constexpr int BYTES = TMEMP + 16;
     static constexpr int ALLOC = BYTES + 1024;   // + alignment slack
@@ -342,6 +359,8 @@ struct GemmArgs {
 
 template <int FMT>
 __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_constant__ CUtensorMap xmap,
+                                                               const __grid_constant__ CUtensorMap wmap,
+                                                               const __grid_constant__ CUtensorMap amap,
                                                                const GemmArgs A) {
     using L = GemmSmem<FMT>;
     constexpr int NSTAGE = L::NSTAGE;
@@ -355,6 +374,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
     uint64_t* minempty = minfull + 2;       // [2], MMA commit
     uint64_t* tfull = minfull + 4;          // [2], MMA commit
     uint64_t* tempty = minfull + 6;         // [2], 4 epilogue-warp arrivals
+    uint64_t* bfull = minfull + 8;          // [BSLOTS], TMA bytes of a weight block and its side data
+    uint64_t* bempty = bfull + GemmCfg<FMT>::BSLOTS;   // [BSLOTS], 4 producer-warp arrivals
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::TMEMP);
     float* scl = reinterpret_cast<float*>(sm + L::SCL);   // [2][3][128]: d, dmin, dx
 
@@ -375,6 +396,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
             mbar_init(&minempty[j], 1);
             mbar_init(&tfull[j], 1);
             mbar_init(&tempty[j], 4);
+        }
+        for (int s = 0; s < GemmCfg<FMT>::BSLOTS; ++s) {
+            mbar_init(&bfull[s], 1);
+            mbar_init(&bempty[s], 4);
         }
         fence_barrier_init();
     }
@@ -415,9 +440,53 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
                 q6K_row_load(dst, A.w + ((size_t)r * nb + b) * Q6K_BYTES, wrow);
             }
         };
-        load_row(R, kb0);
-        for (int b = 0; b < kcount && ok; ++b) {
+        constexpr int BS = GemmCfg<FMT>::BSLOTS;
+        // q4_K / q5_K: block bb of this CTA's K range into slot bb % BS (thread 0)
+        int nissued = 0;   // thread 0: blocks issued so far
+        auto issue_block = [&](int bb) {
+            if constexpr (BS > 0) {
+                ++nissued;
+                const int s = bb % BS;
+                uint8_t* dst = sm + L::BRING + s * L::BSLOT;
+                mbar_arrive_expect_tx(&bfull[s], (uint32_t)L::BTX);
+                tma_load_2d(dst, &wmap, (kb0 + bb) * GemmCfg<FMT>::WROW, r0, &bfull[s]);
+                tma_load_2d(dst + L::WT, &amap, (kb0 + bb) * AUXB, i0, &bfull[s]);
+            }
+        };
+        if constexpr (BS > 0) {
+            if (tid == 0)
+                for (int bb = 0; bb < BS && bb < kcount; ++bb) issue_block(bb);
+        } else {
+            load_row(R, kb0);
+        }
+        int b = 0;
+        for (; b < kcount && ok; ++b) {
             const int j = b & 1;
+            float dx = 0.0f;
+            uint32_t bsw[8];   // q4_K / q5_K: the activation row's bsum words (bsums 2g, 2g+1)
+            if constexpr (BS > 0) {
+                // this block's weight row and activation side data, from the slot into registers
+                const int s = b % BS;
+                const uint32_t ph = (uint32_t)(b / BS) & 1u;
+                if (!mbar_wait(&bfull[s], ph)) { ok = false; break; }
+                const uint8_t* slot = sm + L::BRING + s * L::BSLOT;
+                constexpr int NRAW = GemmCfg<FMT>::WROW / 16;
+#pragma unroll
+                for (int u = 0; u < NRAW; ++u)
+                    R.raw[u] = reinterpret_cast<const uint4*>(slot + t * GemmCfg<FMT>::WROW)[u];
+                const uint4* ax = reinterpret_cast<const uint4*>(slot + L::WT + t * AUXB);
+                const uint4 a0 = ax[0], a1 = ax[1], a2 = ax[2];
+                bsw[0] = a0.x; bsw[1] = a0.y; bsw[2] = a0.z; bsw[3] = a0.w;
+                bsw[4] = a1.x; bsw[5] = a1.y; bsw[6] = a1.z; bsw[7] = a1.w;
+                dx = __uint_as_float(a2.x);
+                fence_async_smem();   // these reads before the slot's refill by TMA
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bempty[s]);
+                if (tid == 0 && b + BS < kcount) {
+                    if (!mbar_wait(&bempty[s], ph)) { ok = false; break; }   // all four warps have read it
+                    issue_block(b + BS);
+                }
+            }
             float dw, dmw = 0.0f;
             if constexpr (FMT != 6) {
                 q4K_row_prepare(R);
@@ -430,9 +499,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
                 ok = mbar_wait(&minempty[j], ((b >> 1) - 1) & 1) && mbar_wait(&tempty[j], ((b >> 1) - 1) & 1);
                 if (!ok) break;
             }
-            float dx = 0.0f;
-            const uint8_t* xb = A.xq + ((size_t)i * nb + kb0 + b) * Q8K_BYTES;
-            if (xrow) dx = __ldg(reinterpret_cast<const float*>(xb));
+            if constexpr (FMT == 6) {
+                const uint8_t* xb = A.xq + ((size_t)i * nb + kb0 + b) * Q8K_BYTES;
+                if (xrow) dx = __ldg(reinterpret_cast<const float*>(xb));
+            }
             if constexpr (FMT != 6) {
                 // min operands: K 0..15 the weight row's mins m_(g/2); K 16..31 the activation row's bsums
                 uint8_t* mt = sm + L::MIN + j * TILE_BYTES;
@@ -442,17 +512,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
                     const __half hm = __int2half_rn(R.mins[g]);
                     mv[g] = h2_bits(__halves2half2(hm, hm));
                 }
-                if (xrow) {
-                    const uint32_t* bw = reinterpret_cast<const uint32_t*>(xb + 260);
 #pragma unroll
-                    for (int g = 0; g < 8; ++g) {
-                        const uint32_t v = __ldg(bw + g);
-                        bv[g] = h2_bits(__halves2half2(__int2half_rn((int)(int16_t)(v & 0xFFFF)),
-                                                       __int2half_rn((int)(int16_t)(v >> 16))));
-                    }
-                } else {
-#pragma unroll
-                    for (int g = 0; g < 8; ++g) bv[g] = 0;
+                for (int g = 0; g < 8; ++g) {   // rows past m arrive as zeros
+                    const uint32_t v = bsw[g];
+                    bv[g] = h2_bits(__halves2half2(__int2half_rn((int)(int16_t)(v & 0xFFFF)),
+                                                   __int2half_rn((int)(int16_t)(v >> 16))));
                 }
                 *reinterpret_cast<uint4*>(mt + sw128_chunk(t, 0)) = make_uint4(mv[0], mv[1], mv[2], mv[3]);
                 *reinterpret_cast<uint4*>(mt + sw128_chunk(t, 1)) = make_uint4(mv[4], mv[5], mv[6], mv[7]);
@@ -467,7 +531,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
             __syncwarp();
             if (lane == 0) mbar_arrive(&minfull[j]);
 
-            if (b + 1 < kcount) load_row(Rn, kb0 + b + 1);   // next block's bytes, in flight while this one is decoded
+            if constexpr (BS == 0)
+                if (b + 1 < kcount) load_row(Rn, kb0 + b + 1);   // next block's bytes, in flight while this one is decoded
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 const int g = 4 * b + c, s = g % NSTAGE, u = g / NSTAGE;
@@ -487,7 +552,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&full[s]);
             }
-            R = Rn;
+            if constexpr (BS == 0) R = Rn;
+        }
+        if constexpr (BS > 0) {
+            // after a wait ran out: let this CTA's weight copies still in flight land before it exits
+            if (!ok && tid == 0)
+                for (int bb = b; bb < nissued; ++bb) (void)mbar_wait(&bfull[bb % BS], (uint32_t)(bb / BS) & 1u);
         }
     } else if (warp == 8) {
         // ------------------------------------------------------- MMA issuer
@@ -585,8 +655,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
     }
 }
 
-// q8_K codes -> f16 activation matrix [m][k] (the GEMM's B operand source)
-__global__ void gemm_x16_kernel(const uint8_t* __restrict__ xq, __half* __restrict__ x16, long long nblocks) {
+// q8_K codes -> f16 activation matrix [m][k] (the GEMM's B operand source),
+// and per block the side data the producers take by TMA: the bsum words, d
+// and three zero words (AUXB bytes)
+__global__ void gemm_x16_kernel(const uint8_t* __restrict__ xq, __half* __restrict__ x16, uint32_t* __restrict__ aux,
+                                long long nblocks) {
     grid_launch_dependents();
     grid_wait_prior();
     const long long total = nblocks * 32;                 // 8 codes per item
@@ -607,6 +680,15 @@ __global__ void gemm_x16_kernel(const uint8_t* __restrict__ xq, __half* __restri
                                                   __int2half_rn((int)(int8_t)(v >> 24))));
         }
         *reinterpret_cast<uint4*>(x16 + blk * QK + 8 * part) = make_uint4(o[0], o[1], o[2], o[3]);
+        if (part < AUXB / 4) {
+            const uint8_t* blkp = xq + blk * Q8K_BYTES;
+            uint32_t v = 0;
+            if (part < 8)
+                v = __ldg(reinterpret_cast<const uint32_t*>(blkp + 260) + part);
+            else if (part == 8)
+                v = __ldg(reinterpret_cast<const uint32_t*>(blkp));
+            aux[blk * (AUXB / 4) + part] = v;
+        }
     }
 }
 
@@ -642,8 +724,10 @@ static EncodeTiledFn encode_fn() {
     return fn;
 }
 
+// f16 activation codes [m][k], then the side data [m][k/256][AUXB bytes]
+static size_t gemm_x16_bytes(long long m, int k) { return (((size_t)m * k * 2) + 255) & ~(size_t)255; }
 size_t gemm_workspace_bytes(long long m, int k) {
-    return (((size_t)m * k * 2) + 255) & ~(size_t)255;
+    return gemm_x16_bytes(m, k) + ((((size_t)m * (k / QK) * AUXB) + 255) & ~(size_t)255);
 }
 
 // K splits when the output tiles alone leave most SMs idle: as many as fill
@@ -664,6 +748,7 @@ static cudaError_t gemm_tc_ws(const uint8_t* w, const uint8_t* xq, float* y, lon
                               void* ws, size_t ws_bytes, cudaStream_t stream) {
     const int nb = k / QK;
     __half* x16 = static_cast<__half*>(ws);
+    uint32_t* aux = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + gemm_x16_bytes(m, k));
     // split K only when the caller's workspace holds the partial sums too
     int splits = gemm_splits(m, n, nb);
     if (ws_bytes < gemm_workspace_bytes(m, k) + gemm_split_bytes(m, n, splits)) splits = 1;
@@ -674,7 +759,8 @@ static cudaError_t gemm_tc_ws(const uint8_t* w, const uint8_t* xq, float* y, lon
         long long grid = (nblocks * 32 + 255) / 256;
         const long long cap = (long long)num_sms() * 8;
         if (grid > cap) grid = cap;
-        cudaError_t e = launch_kernel(gemm_x16_kernel, dim3((unsigned)grid), dim3(256), 0, stream, xq, x16, nblocks);
+        cudaError_t e = launch_kernel(gemm_x16_kernel, dim3((unsigned)grid), dim3(256), 0, stream, xq, x16, aux,
+                                      nblocks);
         if (e != cudaSuccess) return e;
     }
     EncodeTiledFn enc = encode_fn();
@@ -688,6 +774,27 @@ static cudaError_t gemm_tc_ws(const uint8_t* w, const uint8_t* xq, float* y, lon
             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
+    // q4_K / q5_K: the raw weight blocks (rows of nb * WROW bytes; a box is
+    // one block of 128 rows, rows past n read as zeros) and the side data
+    // (rows of nb * AUXB bytes, one block of 128 activation rows)
+    CUtensorMap wmap = map, amap = map;
+    if constexpr (GemmCfg<FMT>::BSLOTS > 0) {
+        constexpr int WROW = GemmCfg<FMT>::WROW;
+        const cuuint64_t wd[2] = {(cuuint64_t)nb * WROW, (cuuint64_t)n};
+        const cuuint64_t ws_[1] = {(cuuint64_t)nb * WROW};
+        const cuuint32_t wb[2] = {(cuuint32_t)WROW, (cuuint32_t)GT};
+        if (enc(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(w), wd, ws_, wb, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+        const cuuint64_t ad[2] = {(cuuint64_t)nb * AUXB, (cuuint64_t)m};
+        const cuuint64_t as_[1] = {(cuuint64_t)nb * AUXB};
+        const cuuint32_t ab[2] = {(cuuint32_t)AUXB, (cuuint32_t)GT};
+        if (enc(&amap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, aux, ad, as_, ab, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
     GemmArgs A;
     A.w = w;
     A.xq = xq;
@@ -704,7 +811,7 @@ static cudaError_t gemm_tc_ws(const uint8_t* w, const uint8_t* xq, float* y, lon
     cudaError_t e = cudaFuncSetAttribute(gemm_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
     if (e != cudaSuccess) return e;
     const dim3 grid((unsigned)((n + GT - 1) / GT), (unsigned)((m + GT - 1) / GT), (unsigned)splits);
-    e = launch_kernel(gemm_kernel<FMT>, grid, dim3(GEMM_THREADS), SMEM, stream, map, A);
+    e = launch_kernel(gemm_kernel<FMT>, grid, dim3(GEMM_THREADS), SMEM, stream, map, wmap, amap, A);
     if (e != cudaSuccess || splits == 1) return e;
     const long long count = m * (long long)n;
     long long blocks = (count + 255) / 256;

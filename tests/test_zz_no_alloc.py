@@ -51,7 +51,7 @@ def test_noalloc_matches_allocating_gemm_on_two_calls_in_a_row():
 
 
 def test_noalloc_rejects_sizes_beyond_its_array():
-    # 2 * m * k bytes of workspace above PLM_NOALLOC_WORKSPACE_BYTES (32 MiB)
+    # about 2.19 * m * k bytes of workspace, above PLM_NOALLOC_WORKSPACE_BYTES (32 MiB)
     fake = 1 << 20   # never dereferenced: the call is rejected before any launch
     st = P.raw_status("plm_gemm_q4K_noalloc", fake, fake, fake, 2048, 256, 12288, None)
     assert st == P.PLM_ERR_UNSUPPORTED
