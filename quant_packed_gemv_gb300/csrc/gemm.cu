@@ -53,8 +53,8 @@ constexpr int GT = 128;                 // tile rows (weights) and columns (acti
 constexpr int KS = 64;                  // K per operand stage (one 128-byte swizzle row)
 constexpr int TILE_BYTES = GT * KS * 2; // 16 KB per operand tile
 constexpr int GEMM_THREADS = 9 * 32;
-// per (activation row, 256-value block) in the workspace: the eight bsum
-// words of the q8_K block (16 int16), its d as f32 bits, three zero words
+// per (activation row, 256-value block) in the workspace: the 16 bsums of
+// the q8_K block as f16 pairs, its d as f32 bits, three zero words
 constexpr int AUXB = 48;
 
 // q4_K: one A tile per stage plus per-block min operands; q6_K: two A tiles
@@ -190,16 +190,20 @@ __device__ __forceinline__ void q4K_row_prepare(QxKRow<NRAW>& R) {
     const uint32_t m_a = hdr.z & 0x3F3F3F3Fu;
     const uint32_t sc_b = (hdr.w & 0x0F0F0F0Fu) | ((hdr.y >> 2) & 0x30303030u);
     const uint32_t m_b = ((hdr.w >> 4) & 0x0F0F0F0Fu) | ((hdr.z >> 2) & 0x30303030u);
+    // 6-bit s as f16 pairs through the 1024 + s bit pattern (exact); the
+    // constants are exact multiples of s by powers of two
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
         const uint32_t scw = c < 2 ? sc_a : sc_b;
         const int sh = 16 * (c & 1);
-        const float slo = (float)((scw >> sh) & 0xFF), shi = (float)((scw >> (sh + 8)) & 0xFF);
+        const uint32_t slo = (scw >> sh) & 0xFFu, shi = (scw >> (sh + 8)) & 0xFFu;
+        const __half2 lo2 = __hsub2(bits_h2(0x64006400u | slo | (slo << 16)), bits_h2(0x64006400u));
+        const __half2 hi2 = __hsub2(bits_h2(0x64006400u | shi | (shi << 16)), bits_h2(0x64006400u));
         // low nibble magic: (1024 + q) * sc - 1024 * sc; high: (1024 + 16q) * sc/16 - 64 * sc
-        R.sc_lo2[c] = h2_bits(__float2half2_rn(slo));
-        R.off_lo2[c] = h2_bits(__float2half2_rn(-1024.0f * slo));
-        R.sc_hi2[c] = h2_bits(__float2half2_rn(shi * 0.0625f));
-        R.off_hi2[c] = h2_bits(__float2half2_rn(-64.0f * shi));
+        R.sc_lo2[c] = h2_bits(lo2);
+        R.off_lo2[c] = h2_bits(__hmul2(lo2, bits_h2(0xE400E400u)));   // x (-1024)
+        R.sc_hi2[c] = h2_bits(__hmul2(hi2, bits_h2(0x2C002C00u)));    // x 1/16
+        R.off_hi2[c] = h2_bits(__hmul2(hi2, bits_h2(0xD400D400u)));   // x (-64)
     }
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
@@ -463,7 +467,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
         for (; b < kcount && ok; ++b) {
             const int j = b & 1;
             float dx = 0.0f;
-            uint32_t bsw[8];   // q4_K / q5_K: the activation row's bsum words (bsums 2g, 2g+1)
+            uint32_t bsw[8];   // q4_K / q5_K: the activation row's bsums 2g, 2g+1 as f16 pairs
             if constexpr (BS > 0) {
                 // this block's weight row and activation side data, from the slot into registers
                 const int s = b % BS;
@@ -482,10 +486,6 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
                 fence_async_smem();   // these reads before the slot's refill by TMA
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bempty[s]);
-                if (tid == 0 && b + BS < kcount) {
-                    if (!mbar_wait(&bempty[s], ph)) { ok = false; break; }   // all four warps have read it
-                    issue_block(b + BS);
-                }
             }
             float dw, dmw = 0.0f;
             if constexpr (FMT != 6) {
@@ -509,14 +509,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
                 uint32_t mv[8], bv[8];
 #pragma unroll
                 for (int g = 0; g < 8; ++g) {
-                    const __half hm = __int2half_rn(R.mins[g]);
-                    mv[g] = h2_bits(__halves2half2(hm, hm));
-                }
-#pragma unroll
-                for (int g = 0; g < 8; ++g) {   // rows past m arrive as zeros
-                    const uint32_t v = bsw[g];
-                    bv[g] = h2_bits(__halves2half2(__int2half_rn((int)(int16_t)(v & 0xFFFF)),
-                                                   __int2half_rn((int)(int16_t)(v >> 16))));
+                    const uint32_t mm = (uint32_t)R.mins[g];
+                    mv[g] = h2_bits(__hsub2(bits_h2(0x64006400u | mm | (mm << 16)), bits_h2(0x64006400u)));
+                    bv[g] = bsw[g];   // f16 pairs from the pre-pass; rows past m arrive as zeros
                 }
                 *reinterpret_cast<uint4*>(mt + sw128_chunk(t, 0)) = make_uint4(mv[0], mv[1], mv[2], mv[3]);
                 *reinterpret_cast<uint4*>(mt + sw128_chunk(t, 1)) = make_uint4(mv[4], mv[5], mv[6], mv[7]);
@@ -527,9 +522,6 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
             sj[t] = dw;
             sj[GT + t] = dmw;
             sj[2 * GT + t] = dx;
-            fence_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&minfull[j]);
 
             if constexpr (BS == 0)
                 if (b + 1 < kcount) load_row(Rn, kb0 + b + 1);   // next block's bytes, in flight while this one is decoded
@@ -548,9 +540,33 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
                     q4K_row_stage(R, c, st, t);
                 else
                     q6K_row_stage(R, c, st, st + TILE_BYTES, t);
-                fence_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&full[s]);
+                if constexpr (NSTAGE < 4) {
+                    // a ring shorter than a block (q6_K): stage c + NSTAGE reuses this
+                    // slot, so the MMA must have it before the block is finished
+                    fence_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&full[s]);
+                }
+            }
+            if (!ok) break;
+            // one proxy fence for the block's min operands, scales and (ring of a
+            // whole block or more) its four stages
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&minfull[j]);
+                if constexpr (NSTAGE >= 4) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) mbar_arrive(&full[(4 * b + c) % NSTAGE]);
+                }
+            }
+            if constexpr (BS > 0) {
+                // refill this block's slot once all four warps have read it (thread 0,
+                // after its own decode so that warp 0 does not stall on the others)
+                if (tid == 0 && b + BS < kcount) {
+                    if (!mbar_wait(&bempty[b % BS], (uint32_t)(b / BS) & 1u)) { ok = false; break; }
+                    issue_block(b + BS);
+                }
             }
             if constexpr (BS == 0) R = Rn;
         }
@@ -656,8 +672,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
 }
 
 // q8_K codes -> f16 activation matrix [m][k] (the GEMM's B operand source),
-// and per block the side data the producers take by TMA: the bsum words, d
-// and three zero words (AUXB bytes)
+// and per block the side data the producers take by TMA: the bsums as f16
+// pairs, d and three zero words (AUXB bytes)
 __global__ void gemm_x16_kernel(const uint8_t* __restrict__ xq, __half* __restrict__ x16, uint32_t* __restrict__ aux,
                                 long long nblocks) {
     grid_launch_dependents();
@@ -683,8 +699,11 @@ __global__ void gemm_x16_kernel(const uint8_t* __restrict__ xq, __half* __restri
         if (part < AUXB / 4) {
             const uint8_t* blkp = xq + blk * Q8K_BYTES;
             uint32_t v = 0;
-            if (part < 8)
-                v = __ldg(reinterpret_cast<const uint32_t*>(blkp + 260) + part);
+            if (part < 8) {   // bsums 2 part, 2 part + 1 as an f16 pair (|bsum| <= 2048: exact)
+                const uint32_t u = __ldg(reinterpret_cast<const uint32_t*>(blkp + 260) + part);
+                v = h2_bits(__halves2half2(__int2half_rn((int)(int16_t)(u & 0xFFFF)),
+                                           __int2half_rn((int)(int16_t)(u >> 16))));
+            }
             else if (part == 8)
                 v = __ldg(reinterpret_cast<const uint32_t*>(blkp));
             aux[blk * (AUXB / 4) + part] = v;
