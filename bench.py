@@ -23,7 +23,11 @@ Reported beside it (same JSON line):
   roofline      the grouped GEMV kernel: algorithmic bytes per launch over
                 its average launch time (CUDA events on its stream).
   e2e           the step through the C ABI with the activations copied in
-                from pinned host memory and the outputs copied back.
+                from pinned host memory and the outputs copied back, the
+                copies of one step overlapping the compute of the next on a
+                second stream (and, as `serial`, without overlap).
+  decode_chain_fused  the chain with one fused quantize + GEMV launch per
+                stage.
   cpu_baseline  the oracle on the host cores, on a bounded sample.
 
 `--impl reference` times the oracle alone (the reference arm).
@@ -430,6 +434,7 @@ class Step:
         self.y_host = torch.empty(yo, dtype=torch.float32).pin_memory()
         self.nchunks = xo // QK
         self.fused = None
+        self.sets = None
         # grouped problem lists, one per weight copy
         self.problems = []
         for c in range(2):
@@ -437,6 +442,35 @@ class Step:
             self.problems.append([(wp + off, self.xq.data_ptr() + self.qoff[i],
                                    self.y.data_ptr() + 4 * self.yoff[i], n, k)
                                   for i, (_, _, n, k, off) in enumerate(mats)])
+
+    def add_io_sets(self, torch, dev):
+        """Two activation/output sets (the first is x, xq, y) for the end-to-end
+        loop, whose host copies of one step overlap the other step's compute."""
+        xq2 = torch.empty_like(self.xq)
+        x_host2 = self.x_host.clone().pin_memory()
+        self.sets = [dict(x=self.x, xq=self.xq, y=self.y, x_host=self.x_host, y_host=self.y_host),
+                     dict(x=x_host2.to(dev), xq=xq2, y=torch.empty_like(self.y), x_host=x_host2,
+                          y_host=torch.empty_like(self.y_host).pin_memory())]
+        for st in self.sets:
+            st["problems"] = [[(self.w[c].data_ptr() + off, st["xq"].data_ptr() + self.qoff[i],
+                                st["y"].data_ptr() + 4 * self.yoff[i], n, k)
+                               for i, (_, _, n, k, off) in enumerate(self.mats)] for c in range(2)]
+
+    def run_set(self, q, b, copy, stream):
+        st = self.sets[b]
+        q.plm_quantize_q8K(st["x"], st["xq"], self.nchunks, QK, stream=stream)
+        q.plm_gemv_q4K_grouped(st["problems"][copy], 1, stream=stream)
+
+    def run_chain_fused(self, q, copy, stream):
+        """Decode order with the fused producer: one launch per dependent stage."""
+        wp = self.w[copy].data_ptr()
+        for layer in range(N_LAYERS):
+            for first, cnt in CHAIN:
+                i = layer * 7 + first
+                _, _, _, k, off = self.mats[i]
+                n = sum(self.mats[i + j][2] for j in range(cnt))
+                q.plm_quantize_gemv_q4K(wp + off, self.x.data_ptr() + 4 * self.xoff[i],
+                                        self.y.data_ptr() + 4 * self.yoff[i], 1, n, k, stream=stream)
 
     def fused_problems(self, copy):
         wp, xp, yp = self.w[copy].data_ptr(), self.x.data_ptr(), self.y.data_ptr()
@@ -543,6 +577,7 @@ def main():
     step_g, gemv_g, fused_g = capture(run_step, K), capture(run_gemv, K), capture(run_fused, K)
     swiglu_g, gateup_g = capture(run_swiglu, K), capture(run_gateup, K)
     chain_g = None if args.no_chain else capture(run_chain, K)
+    chain_fused_g = None if args.no_chain else capture(lambda s: st.run_chain_fused(q, s % 2, stream), K)
     single = [capture(lambda s, c=c: st.run(q, c, stream), 1) for c in range(2)]
     torch.cuda.synchronize()
 
@@ -580,6 +615,47 @@ def main():
         single[s % 2].replay()
         st.y_host.copy_(st.y, non_blocking=True)
 
+    # End to end, pipelined: every step copies its activations in from pinned
+    # host memory and its outputs out, on a copy stream, with two
+    # activation/output sets so that step s+1's input copy and step s's output
+    # copy overlap the compute; the K steps are captured as one graph.
+    st.add_io_sets(torch, dev)
+    copy_stream = torch.cuda.Stream(device=dev)
+
+    def e2e_pipelined(steps):
+        sets = st.sets
+
+        def h2d_copy(s):
+            with torch.cuda.stream(copy_stream):
+                sets[s % 2]["x"].copy_(sets[s % 2]["x_host"], non_blocking=True)
+            ev = torch.cuda.Event()
+            ev.record(copy_stream)
+            return ev
+        fork = torch.cuda.Event()
+        fork.record(stream)
+        copy_stream.wait_event(fork)
+        ev_in = h2d_copy(0)
+        for s in range(steps):
+            b = s % 2
+            nxt = h2d_copy(s + 1) if s + 1 < steps else None   # after the output copy of step s - 1
+            stream.wait_event(ev_in)
+            st.run_set(q, b, s % 2, stream)
+            done = torch.cuda.Event()
+            done.record(stream)
+            copy_stream.wait_event(done)
+            with torch.cuda.stream(copy_stream):
+                sets[b]["y_host"].copy_(sets[b]["y"], non_blocking=True)
+            ev_in = nxt
+        join = torch.cuda.Event()
+        join.record(copy_stream)
+        stream.wait_event(join)
+
+    with torch.cuda.stream(stream):
+        e2e_pipelined(2)
+    torch.cuda.synchronize()
+    e2e_g = capture(lambda s: e2e_pipelined(K) if s == 0 else None, 1)
+    torch.cuda.synchronize()
+
     with torch.cuda.stream(stream):
         for s in range(args.warmup):
             single[s % 2].replay()
@@ -594,6 +670,8 @@ def main():
         swiglu_ms = timed_graph(swiglu_g)
         gateup_ms = timed_graph(gateup_g)
         chain_ms = timed_graph(chain_g) if chain_g is not None else None
+        chain_fused_ms = timed_graph(chain_fused_g) if chain_fused_g is not None else None
+        e2e_pipe_ms = timed_graph(e2e_g)
         single_ms = timed(lambda s: single[s % 2].replay(), K)
         t0 = time.perf_counter()
         e2e_ms = timed(e2e_step, K)
@@ -621,6 +699,9 @@ def main():
                        for (_, j, n, k, _) in mats if j == 4)
     # fused step: weights, f32 activations read once, y written once
     fused_bytes = sum(n * (k // QK) * Q4K_BYTES + 4 * k + 4 * n for _, _, n, k, _ in mats)
+    chain_fused_bytes = sum(sum(mats[l * 7 + f + j][2] for j in range(c)) * (mats[l * 7 + f][3] // QK) * Q4K_BYTES
+                            + 4 * mats[l * 7 + f][3] + 4 * sum(mats[l * 7 + f + j][2] for j in range(c))
+                            for l in range(N_LAYERS) for f, c in CHAIN)
     chain_bytes = sum(gemv_bytes(sum(mats[l * 7 + f + j][2] for j in range(c)), mats[l * 7 + f][3])
                       + quant_bytes(mats[l * 7 + f][3]) for l in range(N_LAYERS) for f, c in CHAIN)
 
@@ -649,6 +730,10 @@ def main():
             "value": world * chain_bytes / (chain_step * 1e-3) / 1e9, "unit": "GB/s",
             "ms_per_step": chain_step, "launches_per_step": 8 * N_LAYERS,
             "what": "28 layers x 4 dependent (quantize, GEMV) stages, CUDA graph"},
+        "decode_chain_fused": None if chain_fused_ms is None else {
+            "value": world * chain_fused_bytes / (chain_fused_ms / args.steps * 1e-3) / 1e9, "unit": "GB/s",
+            "ms_per_step": chain_fused_ms / args.steps, "launches_per_step": 4 * N_LAYERS,
+            "what": "the same chain with plm_quantize_gemv_q4K: one launch per dependent stage"},
         "decode_set_fused": {
             "value": world * fused_bytes / (fused_ms / args.steps * 1e-3) / 1e9, "unit": "GB/s",
             "ms_per_step": fused_ms / args.steps, "launches_per_step": launches_grouped,
@@ -660,8 +745,14 @@ def main():
             "two_matrix_grouped_gemv_us": gateup_ms / args.steps * 1e3,
             "what": "28 q4_K gate/up pairs (3072x1024), m=1: plm_gemv_q4K_swiglu_grouped writes "
                     "h = silu(g)*u; compared with one grouped GEMV over the same 56 matrices"},
-        "e2e": {"value": world * alg / (e2e_ms_step * 1e-3) / 1e9, "unit": "GB/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms_step},
+        "e2e": {"value": world * alg / (e2e_pipe_ms / args.steps * 1e-3) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_pipe_ms / args.steps,
+                "how": "per step: x copied in from pinned host memory, quantize + grouped GEMV, y copied "
+                       "out; copies on a second stream with two buffer sets so they overlap the compute; "
+                       "the K steps captured as one CUDA graph",
+                "serial": {"value": world * alg / (e2e_ms_step * 1e-3) / 1e9, "ms_per_step": e2e_ms_step,
+                           "how": "copy in, one-step graph, copy out, on one stream, no overlap"}},
         "clocks": clocks,
         "device_fault": fault,
     }
