@@ -23,7 +23,8 @@
 //
 // Tile: 128 weight rows (MMA M, TMEM lanes) x 128 activation rows (MMA N,
 // TMEM columns).  Roles per CTA (9 warps):
-//   warps 0-3 (producers): thread t decodes weight row t of the tile into
+//   warps 0-7 (producers, two warpgroups): thread t of warpgroup h decodes
+//     stages 2h, 2h+1 of every block of weight row t of the tile into
 //     the A operand (f16, 128-byte swizzled K-major, one 64-wide K stage
 //     at a time), writes the per-block min operands and scales, and warp 0
 //     issues the TMA load of the activation stage (f16, same layout) from
@@ -32,8 +33,8 @@
 //     activations' per-block d_x and bsums arrive by TMA into a ring of
 //     block slots, two blocks ahead of the decode; q6_K rows (210 bytes, not
 //     a 16-byte multiple) are read by each producer thread one block ahead;
-//   warp 8 (one thread): issues the MMAs (M=128, N=128, K=16) and commits;
-//   warps 4-7 (epilogue): drain D1/D2 of each block from TMEM, apply the
+//   warp 12 (one thread): issues the MMAs (M=128, N=128, K=16) and commits;
+//   warps 8-11 (epilogue): drain D1/D2 of each block from TMEM, apply the
 //     scales and accumulate the result in registers; store y at the end.
 // A ring of 4 operand stages, double-buffered per-block min operands and
 // scales, and double-buffered TMEM accumulators (2 x (128 + 128) columns)
@@ -52,7 +53,20 @@ namespace plm {
 constexpr int GT = 128;                 // tile rows (weights) and columns (activations)
 constexpr int KS = 64;                  // K per operand stage (one 128-byte swizzle row)
 constexpr int TILE_BYTES = GT * KS * 2; // 16 KB per operand tile
-constexpr int GEMM_THREADS = 9 * 32;
+// Roles: PWG producer warpgroups (warpgroup h decodes stages [4h/PWG, 4(h+1)/PWG)
+// of every block), one epilogue warpgroup, one MMA warp; PWG per format below.
+template <int PWG> struct GemmRoles {
+    static constexpr int EPI_WARP0 = 4 * PWG;      // first epilogue warp
+    static constexpr int MMA_WARP = EPI_WARP0 + 4;
+    static constexpr int THREADS = (MMA_WARP + 1) * 32;
+};
+// With two producer warpgroups the block launches at 128 registers a thread
+// (13 warps); the producers then give up 32 each and the epilogue warpgroup,
+// whose 128 f32 accumulators per thread need them, takes 64 more: 256 * 32 =
+// 128 * 64, so the block's launch total is redistributed, not exceeded.
+constexpr int REG_LAUNCH = 128, REG_PRODUCER = 96, REG_EPILOGUE = 192;
+static_assert(2 * 128 * (REG_LAUNCH - REG_PRODUCER) == 128 * (REG_EPILOGUE - REG_LAUNCH),
+              "register split must add up to the launch allocation");
 // per (activation row, 256-value block) in the workspace: the 16 bsums of
 // the q8_K block as f16 pairs, its d as f32 bits, three zero words
 constexpr int AUXB = 48;
@@ -61,14 +75,18 @@ constexpr int AUXB = 48;
 // per stage (the high and low parts of the scale), no min term.
 // BSLOTS: slots of the TMA-fed ring of raw weight blocks (WROW bytes per
 // weight row) and activation side data; 0 for q6_K.
+// PWG: producer warpgroups (q6_K keeps one: its rows are read per thread,
+// whole, and need the registers).
 template <int FMT> struct GemmCfg;
 template <> struct GemmCfg<4> {
-    static constexpr int ATILES = 1, NSTAGE = 4, MINB = 2 * TILE_BYTES, BSLOTS = 2, WROW = Q4K_BYTES;
+    static constexpr int ATILES = 1, NSTAGE = 4, MINB = 2 * TILE_BYTES, BSLOTS = 2, WROW = Q4K_BYTES, PWG = 2;
 };
 template <> struct GemmCfg<5> {   // q5_K: q4_K's operands, a fifth bit per weight
-    static constexpr int ATILES = 1, NSTAGE = 4, MINB = 2 * TILE_BYTES, BSLOTS = 2, WROW = Q5K_BYTES;
+    static constexpr int ATILES = 1, NSTAGE = 4, MINB = 2 * TILE_BYTES, BSLOTS = 2, WROW = Q5K_BYTES, PWG = 2;
 };
-template <> struct GemmCfg<6> { static constexpr int ATILES = 2, NSTAGE = 3, MINB = 0, BSLOTS = 0, WROW = 0; };
+template <> struct GemmCfg<6> {
+    static constexpr int ATILES = 2, NSTAGE = 3, MINB = 0, BSLOTS = 0, WROW = 0, PWG = 1;
+};
 
 template <int FMT>
 struct GemmSmem {
@@ -362,24 +380,26 @@ struct GemmArgs {
 };
 
 template <int FMT>
-__global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_constant__ CUtensorMap xmap,
+__global__ void __launch_bounds__(GemmRoles<GemmCfg<FMT>::PWG>::THREADS, 1) gemm_kernel(const __grid_constant__ CUtensorMap xmap,
                                                                const __grid_constant__ CUtensorMap wmap,
                                                                const __grid_constant__ CUtensorMap amap,
                                                                const GemmArgs A) {
     using L = GemmSmem<FMT>;
     constexpr int NSTAGE = L::NSTAGE;
+    constexpr int PWG = GemmCfg<FMT>::PWG;
+    constexpr int EPI_WARP0 = GemmRoles<PWG>::EPI_WARP0, MMA_WARP = GemmRoles<PWG>::MMA_WARP;
     constexpr int BOFF = GemmCfg<FMT>::ATILES * TILE_BYTES;   // B tile offset inside a stage
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BAR);
-    uint64_t* full = bars;                  // [NSTAGE], 4 producer-warp arrivals + TMA bytes
+    uint64_t* full = bars;                  // [NSTAGE], 4 arrivals (the stage's warpgroup) + TMA bytes
     uint64_t* empty = bars + NSTAGE;        // [NSTAGE], MMA commit
-    uint64_t* minfull = bars + 2 * NSTAGE;  // [2], 4 producer-warp arrivals (min operands, scales)
+    uint64_t* minfull = bars + 2 * NSTAGE;  // [2], 4 arrivals of warpgroup 0 (min operands, scales)
     uint64_t* minempty = minfull + 2;       // [2], MMA commit
     uint64_t* tfull = minfull + 4;          // [2], MMA commit
     uint64_t* tempty = minfull + 6;         // [2], 4 epilogue-warp arrivals
     uint64_t* bfull = minfull + 8;          // [BSLOTS], TMA bytes of a weight block and its side data
-    uint64_t* bempty = bfull + GemmCfg<FMT>::BSLOTS;   // [BSLOTS], 4 producer-warp arrivals
+    uint64_t* bempty = bfull + GemmCfg<FMT>::BSLOTS;   // [BSLOTS], one arrival per producer warp
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::TMEMP);
     float* scl = reinterpret_cast<float*>(sm + L::SCL);   // [2][3][128]: d, dmin, dx
 
@@ -403,11 +423,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
         }
         for (int s = 0; s < GemmCfg<FMT>::BSLOTS; ++s) {
             mbar_init(&bfull[s], 1);
-            mbar_init(&bempty[s], 4);
+            mbar_init(&bempty[s], 4 * PWG);
         }
         fence_barrier_init();
     }
-    if (warp == 8) {
+    if (warp == MMA_WARP) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;"
                      :: "r"(smem_u32(tmem_slot)) : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
@@ -420,9 +440,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
     const uint32_t tmem = *tmem_slot;
     bool ok = true;
 
-    if (warp < 4) {
+    if (warp < EPI_WARP0) {
         // ------------------------------------------------------- producers
-        const int t = tid;
+        const int t = tid & (GT - 1);          // weight row (and activation row) of the tile
+        const int half = warp >> 2;            // this warpgroup's stages: [c0, c0 + 4 / PWG)
+        const int c0 = half * (4 / PWG);
+        if constexpr (PWG == 2) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" :: "n"(REG_PRODUCER));
         const int r = r0 + t, i = i0 + t;
         const bool wrow = r < A.n, xrow = i < A.m;
         using Row = typename std::conditional<FMT == 6, Q6KRow,
@@ -495,15 +518,15 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
             } else {
                 dw = half_bits_to_float(R.raw[52]);
             }
-            if (b >= 2) {
+            if (half == 0 && b >= 2) {   // the block's min operands and scales: warpgroup 0
                 ok = mbar_wait(&minempty[j], ((b >> 1) - 1) & 1) && mbar_wait(&tempty[j], ((b >> 1) - 1) & 1);
                 if (!ok) break;
             }
             if constexpr (FMT == 6) {
                 const uint8_t* xb = A.xq + ((size_t)i * nb + kb0 + b) * Q8K_BYTES;
-                if (xrow) dx = __ldg(reinterpret_cast<const float*>(xb));
+                if (half == 0 && xrow) dx = __ldg(reinterpret_cast<const float*>(xb));
             }
-            if constexpr (FMT != 6) {
+            if constexpr (FMT != 6) if (half == 0) {
                 // min operands: K 0..15 the weight row's mins m_(g/2); K 16..31 the activation row's bsums
                 uint8_t* mt = sm + L::MIN + j * TILE_BYTES;
                 uint32_t mv[8], bv[8];
@@ -518,19 +541,22 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
                 *reinterpret_cast<uint4*>(mt + sw128_chunk(t, 2)) = make_uint4(bv[0], bv[1], bv[2], bv[3]);
                 *reinterpret_cast<uint4*>(mt + sw128_chunk(t, 3)) = make_uint4(bv[4], bv[5], bv[6], bv[7]);
             }
-            float* sj = scl + j * 3 * GT;
-            sj[t] = dw;
-            sj[GT + t] = dmw;
-            sj[2 * GT + t] = dx;
+            if (half == 0) {
+                float* sj = scl + j * 3 * GT;
+                sj[t] = dw;
+                sj[GT + t] = dmw;
+                sj[2 * GT + t] = dx;
+            }
 
             if constexpr (BS == 0)
                 if (b + 1 < kcount) load_row(Rn, kb0 + b + 1);   // next block's bytes, in flight while this one is decoded
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            // stage c of the block (c a compile-time constant, so R's fields stay in registers)
+            auto stage = [&](auto cc_) -> bool {
+                constexpr int c = decltype(cc_)::value;
                 const int g = 4 * b + c, s = g % NSTAGE, u = g / NSTAGE;
-                if (g >= NSTAGE && !mbar_wait(&empty[s], (u - 1) & 1)) { ok = false; break; }
+                if (g >= NSTAGE && !mbar_wait(&empty[s], (u - 1) & 1)) return false;
                 uint8_t* st = sm + L::RING + s * L::STAGE;
-                if (tid == 0) {
+                if (t == 0) {
                     mbar_expect_tx(&full[s], TILE_BYTES);
                     tma_load_2d(st + BOFF, &xmap, (kb0 + b) * QK + c * KS, i0, &full[s]);
                 }
@@ -547,21 +573,30 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&full[s]);
                 }
-            }
+                return true;
+            };
+            using C0 = std::integral_constant<int, 0>;
+            using C1 = std::integral_constant<int, 1>;
+            using C2 = std::integral_constant<int, 2>;
+            using C3 = std::integral_constant<int, 3>;
+            if constexpr (PWG == 1)
+                ok = stage(C0{}) && stage(C1{}) && stage(C2{}) && stage(C3{});
+            else
+                ok = half == 0 ? (stage(C0{}) && stage(C1{})) : (stage(C2{}) && stage(C3{}));
             if (!ok) break;
             // one proxy fence for the block's min operands, scales and (ring of a
             // whole block or more) its four stages
             fence_async_smem();
             __syncwarp();
             if (lane == 0) {
-                mbar_arrive(&minfull[j]);
+                if (half == 0) mbar_arrive(&minfull[j]);
                 if constexpr (NSTAGE >= 4) {
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) mbar_arrive(&full[(4 * b + c) % NSTAGE]);
+                    for (int cc = 0; cc < 4 / PWG; ++cc) mbar_arrive(&full[(4 * b + c0 + cc) % NSTAGE]);
                 }
             }
             if constexpr (BS > 0) {
-                // refill this block's slot once all four warps have read it (thread 0,
+                // refill this block's slot once every producer warp has read it (thread 0,
                 // after its own decode so that warp 0 does not stall on the others)
                 if (tid == 0 && b + BS < kcount) {
                     if (!mbar_wait(&bempty[b % BS], (uint32_t)(b / BS) & 1u)) { ok = false; break; }
@@ -575,7 +610,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
             if (!ok && tid == 0)
                 for (int bb = b; bb < nissued; ++bb) (void)mbar_wait(&bfull[bb % BS], (uint32_t)(bb / BS) & 1u);
         }
-    } else if (warp == 8) {
+    } else if (warp == MMA_WARP) {
         // ------------------------------------------------------- MMA issuer
         if (lane == 0) {
             for (int b = 0; b < kcount && ok; ++b) {
@@ -618,7 +653,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
         __syncwarp();
     } else {
         // ------------------------------------------------------- epilogue
-        const int e = tid - 128;                 // TMEM lane = weight row of the tile
+        if constexpr (PWG == 2) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" :: "n"(REG_EPILOGUE));
+        const int e = tid - EPI_WARP0 * 32;      // TMEM lane = weight row of the tile
         const int q = warp & 3;                  // this warp's lane quarter
         float acc[GT];
 #pragma unroll
@@ -665,7 +701,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
     if (!ok && lane == 0) atomicOr(A.fault, 2u);
     tc_fence_before();
     __syncthreads();
-    if (warp == 8) {
+    if (warp == MMA_WARP) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" :: "r"(tmem) : "memory");
     }
@@ -830,7 +866,15 @@ static cudaError_t gemm_tc_ws(const uint8_t* w, const uint8_t* xq, float* y, lon
     cudaError_t e = cudaFuncSetAttribute(gemm_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
     if (e != cudaSuccess) return e;
     const dim3 grid((unsigned)((n + GT - 1) / GT), (unsigned)((m + GT - 1) / GT), (unsigned)splits);
-    e = launch_kernel(gemm_kernel<FMT>, grid, dim3(GEMM_THREADS), SMEM, stream, map, wmap, amap, A);
+    constexpr int THREADS = GemmRoles<GemmCfg<FMT>::PWG>::THREADS;
+    if constexpr (GemmCfg<FMT>::PWG == 2) {
+        // the register hand-over inside the kernel assumes exactly REG_LAUNCH at launch
+        cudaFuncAttributes fa;
+        e = cudaFuncGetAttributes(&fa, gemm_kernel<FMT>);
+        if (e != cudaSuccess) return e;
+        if (fa.numRegs != REG_LAUNCH) return cudaErrorInvalidConfiguration;
+    }
+    e = launch_kernel(gemm_kernel<FMT>, grid, dim3(THREADS), SMEM, stream, map, wmap, amap, A);
     if (e != cudaSuccess || splits == 1) return e;
     const long long count = m * (long long)n;
     long long blocks = (count + 255) / 256;
