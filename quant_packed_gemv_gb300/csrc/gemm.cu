@@ -394,7 +394,7 @@ __global__ void __launch_bounds__(GemmRoles<GemmCfg<FMT>::PWG>::THREADS, 1) gemm
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BAR);
     uint64_t* full = bars;                  // [NSTAGE], 4 arrivals (the stage's warpgroup) + TMA bytes
     uint64_t* empty = bars + NSTAGE;        // [NSTAGE], MMA commit
-    uint64_t* minfull = bars + 2 * NSTAGE;  // [2], 4 arrivals of warpgroup 0 (min operands, scales)
+    uint64_t* minfull = bars + 2 * NSTAGE;  // [2], one arrival per producer warp (min operands, scales)
     uint64_t* minempty = minfull + 2;       // [2], MMA commit
     uint64_t* tfull = minfull + 4;          // [2], MMA commit
     uint64_t* tempty = minfull + 6;         // [2], 4 epilogue-warp arrivals
@@ -416,7 +416,7 @@ __global__ void __launch_bounds__(GemmRoles<GemmCfg<FMT>::PWG>::THREADS, 1) gemm
             mbar_init(&empty[s], 1);
         }
         for (int j = 0; j < 2; ++j) {
-            mbar_init(&minfull[j], 4);
+            mbar_init(&minfull[j], 4 * PWG);
             mbar_init(&minempty[j], 1);
             mbar_init(&tfull[j], 1);
             mbar_init(&tempty[j], 4);
@@ -518,7 +518,7 @@ __global__ void __launch_bounds__(GemmRoles<GemmCfg<FMT>::PWG>::THREADS, 1) gemm
             } else {
                 dw = half_bits_to_float(R.raw[52]);
             }
-            if (half == 0 && b >= 2) {   // the block's min operands and scales: warpgroup 0
+            if (b >= 2) {   // slot j's min operands (last warpgroup) and scales (warpgroup 0) are free again
                 ok = mbar_wait(&minempty[j], ((b >> 1) - 1) & 1) && mbar_wait(&tempty[j], ((b >> 1) - 1) & 1);
                 if (!ok) break;
             }
@@ -526,7 +526,7 @@ __global__ void __launch_bounds__(GemmRoles<GemmCfg<FMT>::PWG>::THREADS, 1) gemm
                 const uint8_t* xb = A.xq + ((size_t)i * nb + kb0 + b) * Q8K_BYTES;
                 if (half == 0 && xrow) dx = __ldg(reinterpret_cast<const float*>(xb));
             }
-            if constexpr (FMT != 6) if (half == 0) {
+            if constexpr (FMT != 6) if (half == PWG - 1) {
                 // min operands: K 0..15 the weight row's mins m_(g/2); K 16..31 the activation row's bsums
                 uint8_t* mt = sm + L::MIN + j * TILE_BYTES;
                 uint32_t mv[8], bv[8];
@@ -589,7 +589,7 @@ __global__ void __launch_bounds__(GemmRoles<GemmCfg<FMT>::PWG>::THREADS, 1) gemm
             fence_async_smem();
             __syncwarp();
             if (lane == 0) {
-                if (half == 0) mbar_arrive(&minfull[j]);
+                mbar_arrive(&minfull[j]);
                 if constexpr (NSTAGE >= 4) {
 #pragma unroll
                     for (int cc = 0; cc < 4 / PWG; ++cc) mbar_arrive(&full[(4 * b + c0 + cc) % NSTAGE]);
