@@ -22,20 +22,24 @@
 // 16*D_hi + D_lo in the epilogue.
 //
 // Tile: 128 weight rows (MMA M, TMEM lanes) x 128 activation rows (MMA N,
-// TMEM columns).  Roles per CTA (9 warps):
-//   warps 0-7 (producers, two warpgroups): thread t of warpgroup h decodes
-//     stages 2h, 2h+1 of every block of weight row t of the tile into
-//     the A operand (f16, 128-byte swizzled K-major, one 64-wide K stage
-//     at a time), writes the per-block min operands and scales, and warp 0
-//     issues the TMA load of the activation stage (f16, same layout) from
-//     the workspace the pre-pass fills.  q4_K / q5_K: the raw weight
-//     blocks of the tile (128 rows x one 256-weight block) and the
-//     activations' per-block d_x and bsums arrive by TMA into a ring of
-//     block slots, two blocks ahead of the decode; q6_K rows (210 bytes, not
-//     a 16-byte multiple) are read by each producer thread one block ahead;
-//   warp 12 (one thread): issues the MMAs (M=128, N=128, K=16) and commits;
-//   warps 8-11 (epilogue): drain D1/D2 of each block from TMEM, apply the
-//     scales and accumulate the result in registers; store y at the end.
+// TMEM columns).  Roles per CTA (q4_K / q5_K: 13 warps; q6_K: 9 warps):
+//   producer warpgroups (q4_K / q5_K: warps 0-7, two warpgroups; q6_K:
+//     warps 0-3, one): thread t of warpgroup h decodes weight row t of the
+//     tile into the A operand (f16, 128-byte swizzled K-major, one 64-wide
+//     K stage at a time), stages 2h and 2h+1 of every block (q6_K: all
+//     four); warpgroup 0 writes the per-block scales and the last
+//     warpgroup the min operands; thread 0 of a warpgroup issues the TMA
+//     load of the activation stage (f16, same layout) from the workspace
+//     the pre-pass fills.  q4_K / q5_K: the raw weight blocks of the tile
+//     (128 rows x one 256-weight block) and the activations' per-block d_x
+//     and bsums arrive by TMA into a ring of two block slots, up to two
+//     blocks ahead of the decode; q6_K rows (210 bytes, not a 16-byte
+//     multiple) are read by each producer thread one block ahead;
+//   the last warp (one thread): issues the MMAs (M=128, N=128, K=16) and
+//     commits;
+//   the epilogue warpgroup (the four warps before it): drains D1/D2 of each
+//     block from TMEM, applies the scales and accumulates the result in
+//     registers; stores y at the end.
 // A ring of 4 operand stages, double-buffered per-block min operands and
 // scales, and double-buffered TMEM accumulators (2 x (128 + 128) columns)
 // keep the roles overlapped.  Every wait is bounded; a wait that runs out
