@@ -312,9 +312,10 @@ plm_status plm_gemm_q6K(const void* w, const void* xq, float* y,
                         int64_t m, int64_t n, int64_t k, cudaStream_t stream);
 
 /* Workspace bytes plm_gemm_qNK_ws needs (fmt = N: 2, 3, 4, 5, 6; q2_K and
- * q3_K need none)
- * need for m activation rows of length k (0 when none is needed, and for
- * invalid arguments). */
+ * q3_K need none) for m activation rows of length k: for m >= 9, the codes
+ * widened to f16 (2*m*k bytes) and, per activation row and 256-value block,
+ * 48 bytes of side data (the bsums as f16 pairs and d), each part rounded up
+ * to 256 bytes.  0 when none is needed, and for invalid arguments. */
 size_t plm_gemm_workspace_size(int fmt, int64_t m, int64_t k);
 
 /* Workspace that also holds the partial sums of a K split: when the output
