@@ -311,6 +311,32 @@ plm_status plm_gemm_q4K(const void* w, const void* xq, float* y,
 plm_status plm_gemm_q6K(const void* w, const void* xq, float* y,
                         int64_t m, int64_t n, int64_t k, cudaStream_t stream);
 
+/*
+ * Gate/up pair with the SwiGLU epilogue for prefill (q4_K), any m >= 1:
+ *   h[i][r] = silu(g[i][r]) * u[i][r],  g = W_gate . x_i,  u = W_up . x_i,
+ * the same step as plm_gemv_q4K_swiglu (PocketLLM (Korean README), "Current
+ * status" table, row "src/": silu_mul after the ffn gate and up projections)
+ * at prefill sizes.  For m >= 9: the q4_K GEMM of the gate matrix into h,
+ * that of the up matrix into the workspace, then one elementwise pass
+ * h = silu(h) * u (IEEE division, expf) -- g and u are exactly what
+ * plm_gemm_q4K_ws gives for each matrix with the same workspace size.  For
+ * m <= 8 it runs plm_gemv_q4K_swiglu eight rows at a time.
+ *   w_gate, w_up  q4_K [n][k/256] each, 16-byte aligned; xq q8_K [m][k/256];
+ *   h f32 [m][n], not overlapping the inputs.  The plain form takes its
+ *   workspace from the stream-ordered pool; the _ws form takes the caller's:
+ *   plm_gemm_swiglu_workspace_size(m, n, k) bytes, 256-byte aligned (null
+ *   allowed when that is 0).  Errors as for plm_gemm_q4K / plm_gemm_q4K_ws.
+ */
+plm_status plm_gemm_q4K_swiglu(const void* w_gate, const void* w_up, const void* xq, float* h, int64_t m,
+                               int64_t n, int64_t k, cudaStream_t stream);
+plm_status plm_gemm_q4K_swiglu_ws(const void* w_gate, const void* w_up, const void* xq, float* h, int64_t m,
+                                  int64_t n, int64_t k, void* workspace, size_t workspace_bytes,
+                                  cudaStream_t stream);
+/* Workspace bytes of plm_gemm_q4K_swiglu_ws: m >= 9: m*n*4 (the up matrix's
+ * output, rounded up to 256 bytes) plus plm_gemm_workspace_size_split(4, m,
+ * n, k); 0 for m <= 8 and for invalid arguments. */
+size_t plm_gemm_swiglu_workspace_size(int64_t m, int64_t n, int64_t k);
+
 /* Workspace bytes plm_gemm_qNK_ws needs (fmt = N: 2, 3, 4, 5, 6; q2_K and
  * q3_K need none) for m activation rows of length k: for m >= 9, the codes
  * widened to f16 (2*m*k bytes) and, per activation row and 256-value block,

@@ -178,6 +178,24 @@ plm_status gemm_ws_common(int fmt, const void* w, const void* xq, float* y, int6
                                            ws, ws_bytes, stream));
 }
 
+plm_status gemm_swiglu_common(const void* wg, const void* wu, const void* xq, float* h, int64_t m, int64_t n,
+                              int64_t k, bool caller_ws, void* ws, size_t ws_bytes, cudaStream_t stream) {
+    plm_status s = check_matmul(wg, xq, h, m, n, k, kMaxIndex);
+    if (s != PLM_OK) return s;
+    s = check_matmul(wu, xq, h, m, n, k, kMaxIndex);
+    if (s != PLM_OK) return s;
+    if (m * n > (int64_t)1 << 40) return PLM_ERR_INVALID_ARG;
+    if (caller_ws) {
+        const size_t need = plm::gemm_swiglu_workspace_need(m, (int)n, (int)k);
+        if (need > 0 && (!ws || ws_bytes < need)) return PLM_ERR_INVALID_ARG;
+        if (ws && !aligned(ws, 256)) return PLM_ERR_MISALIGNED;
+    }
+    if (!plm::gemv_supported(4, (int)k)) return PLM_ERR_UNSUPPORTED;
+    const uint8_t *g8 = (const uint8_t*)wg, *u8 = (const uint8_t*)wu, *x8 = (const uint8_t*)xq;
+    return cuda_status(caller_ws ? plm::launch_gemm_q4K_swiglu_ws(g8, u8, x8, h, m, (int)n, (int)k, ws, ws_bytes, stream)
+                                 : plm::launch_gemm_q4K_swiglu(g8, u8, x8, h, m, (int)n, (int)k, stream));
+}
+
 plm_status subdots_common(int fmt, const void* w, const void* xq, int32_t* out, int64_t m,
                           int64_t n, int64_t k, cudaStream_t stream) {
     plm_status s = check_matmul(w, xq, out, m, n, k, plm::GEMV_MAX_M);
@@ -345,6 +363,12 @@ size_t plm_gemm_workspace_size_split(int fmt, int64_t m, int64_t n, int64_t k) {
     return plm::gemm_workspace_need_split(fmt, m, (int)n, (int)k);
 }
 
+size_t plm_gemm_swiglu_workspace_size(int64_t m, int64_t n, int64_t k) {
+    if (m <= 0 || n <= 0 || k <= 0 || k % plm::QK != 0 || k > kMaxIndex || n > kMaxIndex || m * n > (int64_t)1 << 40)
+        return 0;
+    return plm::gemm_swiglu_workspace_need(m, (int)n, (int)k);
+}
+
 size_t plm_gemm_workspace_size(int fmt, int64_t m, int64_t k) {
     if (fmt < 2 || fmt > 6 || m <= 0 || k <= 0 || k % plm::QK != 0 || k > kMaxIndex) return 0;
     return plm::gemm_workspace_need(fmt, m, (int)k);
@@ -386,6 +410,17 @@ plm_status plm_gemv_q4K_swiglu(const void* w_gate, const void* w_up, const void*
                                int64_t n, int64_t k, cudaStream_t stream) {
     const plm_swiglu_problem p{w_gate, w_up, xq, h, n, k};
     return swiglu_common(&p, 1, m, stream);
+}
+
+plm_status plm_gemm_q4K_swiglu(const void* w_gate, const void* w_up, const void* xq, float* h, int64_t m,
+                               int64_t n, int64_t k, cudaStream_t stream) {
+    return gemm_swiglu_common(w_gate, w_up, xq, h, m, n, k, false, nullptr, 0, stream);
+}
+
+plm_status plm_gemm_q4K_swiglu_ws(const void* w_gate, const void* w_up, const void* xq, float* h, int64_t m,
+                                  int64_t n, int64_t k, void* workspace, size_t workspace_bytes,
+                                  cudaStream_t stream) {
+    return gemm_swiglu_common(w_gate, w_up, xq, h, m, n, k, true, workspace, workspace_bytes, stream);
 }
 
 plm_status plm_gemv_q4K_swiglu_grouped(const plm_swiglu_problem* problems, int64_t count, int64_t m,

@@ -751,6 +751,18 @@ __global__ void gemm_x16_kernel(const uint8_t* __restrict__ xq, __half* __restri
     }
 }
 
+// SwiGLU of a gate/up pair: h = silu(h) * u = h / (1 + e^-h) * u, elementwise
+// (h holds the gate GEMM's output on entry).
+__global__ void gemm_swiglu_kernel(float* __restrict__ h, const float* __restrict__ u, long long count) {
+    grid_launch_dependents();
+    grid_wait_prior();
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < count;
+         i += (long long)gridDim.x * blockDim.x) {
+        const float g = h[i];
+        h[i] = __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u[i]);
+    }
+}
+
 // Split K: y = the splits' partial sums, added in split order (deterministic).
 __global__ void gemm_split_reduce_kernel(const float* __restrict__ part, float* __restrict__ y, long long count,
                                          int splits) {
@@ -913,6 +925,65 @@ cudaError_t launch_gemm_ws(int fmt, const uint8_t* w, const uint8_t* xq, float* 
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
+}
+
+// q4_K gate/up pair with the SwiGLU epilogue, any m.  From GEMM_MIN_M rows:
+// the gate GEMM into h, the up GEMM into the front of the workspace, then one
+// elementwise pass (a single launch streaming both matrices was tried and was
+// slower: the epilogue of a kernel that parks g and later combines it with
+// u ran out of registers).  Below: the decode GEMV pair, eight rows a launch.
+static size_t pair_u_bytes(long long m, int n) { return (((size_t)m * n * 4) + 255) & ~(size_t)255; }
+
+size_t gemm_swiglu_workspace_need(long long m, int n, int k) {
+    if (!gemm_on_tensor_cores(4, m)) return 0;
+    return pair_u_bytes(m, n) + gemm_workspace_need_split(4, m, n, k);
+}
+
+cudaError_t launch_gemm_q4K_swiglu_ws(const uint8_t* w_gate, const uint8_t* w_up, const uint8_t* xq, float* h,
+                                      long long m, int n, int k, void* ws, size_t ws_bytes, cudaStream_t stream) {
+    if (gemm_on_tensor_cores(4, m)) {
+        const size_t ub = pair_u_bytes(m, n);
+        if (!ws || ws_bytes < ub + gemm_workspace_bytes(m, k)) return cudaErrorInvalidValue;
+        float* u = static_cast<float*>(ws);
+        void* gws = static_cast<uint8_t*>(ws) + ub;
+        const size_t gbytes = ws_bytes - ub;
+        cudaError_t e = gemm_tc_ws<4>(w_gate, xq, h, m, n, k, gws, gbytes, stream);
+        if (e != cudaSuccess) return e;
+        e = gemm_tc_ws<4>(w_up, xq, u, m, n, k, gws, gbytes, stream);
+        if (e != cudaSuccess) return e;
+        const long long count = m * (long long)n;
+        long long blocks = (count + 255) / 256;
+        const long long cap = (long long)num_sms() * 8;
+        if (blocks > cap) blocks = cap;
+        return launch_kernel(gemm_swiglu_kernel, dim3((unsigned)blocks), dim3(256), 0, stream, h, (const float*)u,
+                             count);
+    }
+    const int nb = k / QK;
+    for (long long i0 = 0; i0 < m; i0 += GEMV_MAX_M) {
+        const int mm = (int)(m - i0 < GEMV_MAX_M ? m - i0 : GEMV_MAX_M);
+        GroupItem it;
+        it.w = w_gate;
+        it.w2 = w_up;
+        it.xq = xq + (size_t)i0 * nb * Q8K_BYTES;
+        it.y = h + (size_t)i0 * n;
+        it.n = n;
+        it.k = k;
+        cudaError_t e = launch_gemv_q4K_swiglu(&it, 1, mm, stream);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+cudaError_t launch_gemm_q4K_swiglu(const uint8_t* w_gate, const uint8_t* w_up, const uint8_t* xq, float* h,
+                                   long long m, int n, int k, cudaStream_t stream) {
+    const size_t need = gemm_swiglu_workspace_need(m, n, k);
+    if (need == 0) return launch_gemm_q4K_swiglu_ws(w_gate, w_up, xq, h, m, n, k, nullptr, 0, stream);
+    void* ws = nullptr;
+    cudaError_t e = cudaMallocAsync(&ws, need, stream);
+    if (e != cudaSuccess) return e;
+    e = launch_gemm_q4K_swiglu_ws(w_gate, w_up, xq, h, m, n, k, ws, need, stream);
+    const cudaError_t f = cudaFreeAsync(ws, stream);
+    return e != cudaSuccess ? e : f;
 }
 
 size_t gemm_workspace_need(int fmt, long long m, int k) {

@@ -77,6 +77,15 @@ cudaError_t launch_gemm(int fmt, const uint8_t* w, const uint8_t* xq, float* y,
 cudaError_t launch_gemm_ws(int fmt, const uint8_t* w, const uint8_t* xq, float* y, long long m, int n, int k,
                            void* ws, size_t ws_bytes, cudaStream_t stream);
 size_t gemm_workspace_need(int fmt, long long m, int k);
+
+// q4_K gate/up pair with the SwiGLU epilogue, any m; the _ws form needs
+// gemm_swiglu_workspace_need(m, n, k) bytes for the split form (the up
+// matrix's output, then a GEMM workspace; at least the unsplit size).
+size_t gemm_swiglu_workspace_need(long long m, int n, int k);
+cudaError_t launch_gemm_q4K_swiglu(const uint8_t* w_gate, const uint8_t* w_up, const uint8_t* xq, float* h,
+                                   long long m, int n, int k, cudaStream_t stream);
+cudaError_t launch_gemm_q4K_swiglu_ws(const uint8_t* w_gate, const uint8_t* w_up, const uint8_t* xq, float* h,
+                                      long long m, int n, int k, void* ws, size_t ws_bytes, cudaStream_t stream);
 // The same plus the partial sums of a K split (used when the output tiles
 // alone would leave most SMs idle); the _ws form splits K only when given this.
 size_t gemm_workspace_need_split(int fmt, long long m, int n, int k);

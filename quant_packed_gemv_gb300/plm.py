@@ -101,6 +101,12 @@ def load(build_if_missing=True):
     lib.plm_gemv_q4K_swiglu.restype = ctypes.c_int
     lib.plm_gemv_q4K_swiglu_grouped.argtypes = [ctypes.POINTER(_SProblem), i64, i64, vp]
     lib.plm_gemv_q4K_swiglu_grouped.restype = ctypes.c_int
+    lib.plm_gemm_q4K_swiglu.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp]
+    lib.plm_gemm_q4K_swiglu.restype = ctypes.c_int
+    lib.plm_gemm_q4K_swiglu_ws.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, ctypes.c_size_t, vp]
+    lib.plm_gemm_q4K_swiglu_ws.restype = ctypes.c_int
+    lib.plm_gemm_swiglu_workspace_size.argtypes = [i64, i64, i64]
+    lib.plm_gemm_swiglu_workspace_size.restype = ctypes.c_size_t
     lib.plm_quantize_gemv_q4K_grouped.argtypes = [ctypes.POINTER(_QProblem), i64, i64, vp]
     lib.plm_quantize_gemv_q4K_grouped.restype = ctypes.c_int
     for name in ("plm_gemv_q4K", "plm_gemv_q6K", "plm_gemm_q4K", "plm_gemm_q6K", "plm_gemm_q4K_noalloc",
@@ -233,6 +239,28 @@ def plm_gemv_q4K_swiglu(w_gate, w_up, xq, h, m, n, k, stream=None):
     lib = load()
     _check("plm_gemv_q4K_swiglu", lib.plm_gemv_q4K_swiglu(_addr(w_gate), _addr(w_up), _addr(xq), _addr(h), m, n, k,
                                                           _stream(stream)))
+
+
+def plm_gemm_swiglu_workspace_size(m, n, k):
+    """Workspace bytes of plm_gemm_q4K_swiglu_ws (0: none needed, or invalid arguments)."""
+    return load().plm_gemm_swiglu_workspace_size(m, n, k)
+
+
+def plm_gemm_q4K_swiglu(w_gate, w_up, xq, h, m, n, k, stream=None):
+    """Prefill gate/up pair: h = silu(W_gate . x) * (W_up . x) (see include/plm.h)."""
+    lib = load()
+    _check("plm_gemm_q4K_swiglu", lib.plm_gemm_q4K_swiglu(_addr(w_gate), _addr(w_up), _addr(xq), _addr(h), m, n, k,
+                                                          _stream(stream)))
+
+
+def plm_gemm_q4K_swiglu_ws(w_gate, w_up, xq, h, m, n, k, workspace, workspace_bytes=None, stream=None):
+    """plm_gemm_q4K_swiglu with a caller-owned workspace (plm_gemm_swiglu_workspace_size bytes)."""
+    lib = load()
+    if workspace_bytes is None:
+        workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("plm_gemm_q4K_swiglu_ws", lib.plm_gemm_q4K_swiglu_ws(_addr(w_gate), _addr(w_up), _addr(xq), _addr(h), m,
+                                                                n, k, _addr(workspace), workspace_bytes,
+                                                                _stream(stream)))
 
 
 def plm_gemv_q4K_swiglu_grouped(problems, m, stream=None):

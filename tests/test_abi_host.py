@@ -139,3 +139,27 @@ def test_swiglu_argument_checks():
     assert lib.plm_gemv_q4K_swiglu_grouped(arr, 2, 1, None) == P.PLM_ERR_MISALIGNED
     assert lib.plm_gemv_q4K_swiglu_grouped(arr, 0, 1, None) == bad
     assert lib.plm_gemv_q4K_swiglu_grouped(None, 1, 1, None) == bad
+
+
+def test_gemm_swiglu_argument_checks():
+    lib = q.load()
+    bad = P.PLM_ERR_INVALID_ARG
+    for name in ("plm_gemm_q4K_swiglu", "plm_gemm_q4K_swiglu_ws"):
+        ws = (A, 1 << 30) if name.endswith("_ws") else ()
+        st = lambda *a: getattr(lib, name)(*(a[:7] + ws + a[7:]))  # noqa: E731
+        assert st(None, A, A, A, 512, 8, 256, None) == bad
+        assert st(A, None, A, A, 512, 8, 256, None) == bad
+        assert st(A, A, None, A, 512, 8, 256, None) == bad
+        assert st(A, A, A, None, 512, 8, 256, None) == bad
+        assert st(A, A, A, A, 0, 8, 256, None) == bad
+        assert st(A, A, A, A, 512, 0, 256, None) == bad
+        assert st(A, A, A, A, 512, 8, 300, None) == bad
+        assert st(A, A + 8, A, A, 512, 8, 256, None) == P.PLM_ERR_MISALIGNED
+        assert st(A + 8, A, A, A, 512, 8, 256, None) == P.PLM_ERR_MISALIGNED
+    # caller workspace: too small, or not 256-byte aligned
+    need = q.plm_gemm_swiglu_workspace_size(512, 8, 256)
+    assert need >= 512 * 8 * 4 + q.plm_gemm_workspace_size(4, 512, 256)
+    assert q.plm_gemm_swiglu_workspace_size(8, 8, 256) == 0 and q.plm_gemm_swiglu_workspace_size(512, 8, 300) == 0
+    assert lib.plm_gemm_q4K_swiglu_ws(A, A, A, A, 512, 8, 256, A, need - 1, None) == bad
+    assert lib.plm_gemm_q4K_swiglu_ws(A, A, A, A, 512, 8, 256, None, need, None) == bad
+    assert lib.plm_gemm_q4K_swiglu_ws(A, A, A, A, 512, 8, 256, A + 16, need, None) == P.PLM_ERR_MISALIGNED
