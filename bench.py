@@ -374,6 +374,44 @@ class ShapeTimer:
         return r
 
 
+def time_pair(T, wg_list, wu_list, n, k, m, steps, warmup):
+    """The prefill gate/up pair with SwiGLU (plm_gemm_q4K_swiglu_ws) on one
+    shape, weights rotated as for ShapeTimer, a CUDA graph of `steps` calls."""
+    import gen
+    torch, q = T.torch, T.q
+    nb = k // QK
+    x = torch.from_numpy(gen.normal_f32(8, m, m, k)).cuda()
+    xq = torch.empty(m * nb * Q8K_BYTES, dtype=torch.uint8, device="cuda")
+    h = torch.empty(m * n, dtype=torch.float32, device="cuda")
+    need = q.plm_gemm_swiglu_workspace_size(m, n, k)
+    work = torch.empty(max(need, 256), dtype=torch.uint8, device="cuda")
+    s = T.stream
+
+    def call(i):
+        q.plm_gemm_q4K_swiglu_ws(wg_list[i % len(wg_list)], wu_list[i % len(wu_list)], xq, h, m, n, k,
+                                 work if need else None, need, stream=s)
+    with torch.cuda.stream(s):
+        q.plm_quantize_q8K(x, xq, m, k, stream=s)
+        for i in range(warmup):
+            call(i)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for i in range(steps):
+                call(i)
+        g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        g.replay()
+        e1.record(s)
+        torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / steps
+    tops = 4.0 * m * n * k / us / 1e6   # two matrices
+    return {"fmt": "q4K", "n": n, "k": k, "m": m, "us": round(us, 3), "entry": "plm_gemm_q4K_swiglu_ws",
+            "TOPS": round(tops, 1), "frac_f16_dense": round(tops / T.peaks["bf16_tflops"], 4)}
+
+
 def run_extras(torch, q, peaks):
     """Prefill GEMMs (Qwen3 m=512 shapes), the q6_K output head at m = 1, 8,
     512, and the Qwen3-8B sweep over m, each shape timed alone."""
@@ -402,6 +440,13 @@ def run_extras(torch, q, peaks):
     ws, wb = T.weights("q5K", 5, 12288, 4096)
     out["q5K_12288x4096"] = [T.run("q5K", ws, wb, 12288, 4096, m, 10 if m <= 8 else 3, 2) for m in (1, 8, 512)]
     del ws
+    # the prefill gate/up pair with the SwiGLU epilogue (two GEMMs and one elementwise pass)
+    wg, _ = T.weights("q4K", 6, 12288, 4096)
+    wu, _ = T.weights("q4K", 7, 12288, 4096)
+    out["prefill_swiglu_q4K_12288x4096"] = [time_pair(T, wg, wu, 12288, 4096, m, 5 if m < 2048 else 3, 2)
+                                            for m in (64, 512, 2048)]
+    del wg, wu
+    torch.cuda.empty_cache()
     # the q2_K and q3_K rungs (decode GEMV; their GEMM entry runs the GEMV in 8-row passes)
     for fmt in ("q3K", "q2K"):
         ws, wb = T.weights(fmt, 5, 12288, 4096)
