@@ -110,12 +110,28 @@ int plm_last_cuda_error(void);
 plm_status plm_device_fault(uint32_t* code, int clear);
 
 /*
+ * Failure-detection self-test (no counterpart on the pages; it checks the
+ * library's own error path).  Launches one warp on `stream` that waits on a
+ * shared-memory mbarrier with the bounded wait every streaming kernel uses,
+ * limited to `rounds` rounds of at most 20 microseconds each (1 <= rounds <=
+ * 65536, else PLM_ERR_INVALID_ARG and nothing is launched).  complete != 0:
+ * the barrier's one arrival is made before the wait, which then ends at once
+ * and leaves the fault word alone.  complete == 0: nothing arrives and no
+ * copy is in flight, so the wait runs out, the kernel sets bit 0 of the
+ * device fault word (read it with plm_device_fault) and returns; the device
+ * stays usable.  Allocates nothing, does not synchronize.  PLM_ERR_CUDA if
+ * the launch failed.
+ */
+plm_status plm_selftest_bounded_wait(uint32_t rounds, int complete, cudaStream_t stream);
+
+/*
  * Diagnostic (the pages have no counterpart): measured throughput of the
  * warp-level tensor instructions mma.sync m16n8k32 s8 (*s8_tops, TOPS) and
  * mma.sync m16n8k16 f16 with f32 accumulation (*f16_tflops, TFLOPS) on the
  * current device, from register-only loops on the legacy default stream.
- * tcgen05 on sm_103a has no int8 kind, so the s8 figure is the int8 tensor
- * rate this part offers.  Synchronizes; allocates nothing.
+ * Context only: tcgen05 on sm_103a has no int8 kind, and both legacy rates
+ * are far below the tcgen05 f16 dense rate.  Synchronizes; allocates
+ * nothing.
  */
 plm_status plm_probe_mma_rates(double* s8_tops, double* f16_tflops);
 

@@ -15,15 +15,20 @@ namespace plm {
 __device__ unsigned g_plm_fault = 0;
 
 unsigned* fault_word() {
-    // the symbol's address is fixed per device once the module is loaded;
-    // remember it for the first 64 devices
-    static void* cache[64] = {};
+    // the symbol's address is fixed per device while the device's primary
+    // context lives (the library must not be used across a cudaDeviceReset);
+    // remember it for the first 64 devices.  Threads that race here store
+    // the same address.
+    static std::atomic<void*> cache[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
-    if (dev >= 0 && dev < 64 && cache[dev]) return static_cast<unsigned*>(cache[dev]);
+    if (dev >= 0 && dev < 64) {
+        void* c = cache[dev].load(std::memory_order_acquire);
+        if (c) return static_cast<unsigned*>(c);
+    }
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_plm_fault) != cudaSuccess) return nullptr;
-    if (dev >= 0 && dev < 64) cache[dev] = p;
+    if (dev >= 0 && dev < 64) cache[dev].store(p, std::memory_order_release);
     return static_cast<unsigned*>(p);
 }
 

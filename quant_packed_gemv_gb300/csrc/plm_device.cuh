@@ -271,13 +271,13 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
 }
 
 // Returns true once the phase with the given parity has completed, false if
-// WAIT_LIMIT rounds pass first.  Each round lets the hardware suspend the
-// warp for up to SUSPEND_NS (it resumes as soon as the phase completes), so
-// waiting warps do not spin on the issue slots.
+// `limit` rounds (WAIT_LIMIT unless given) pass first.  Each round lets the
+// hardware suspend the warp for up to SUSPEND_NS (it resumes as soon as the
+// phase completes), so waiting warps do not spin on the issue slots.
 constexpr unsigned SUSPEND_NS = 20000;
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned limit = WAIT_LIMIT) {
     const uint32_t a = smem_u32(bar);
-    for (unsigned it = 0; it < WAIT_LIMIT; ++it) {
+    for (unsigned it = 0; it < limit; ++it) {
         uint32_t done;
         asm volatile("{\n\t.reg .pred p;\n\t"
                      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"

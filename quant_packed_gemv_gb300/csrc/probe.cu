@@ -1,12 +1,14 @@
 // Diagnostic: measured issue rates of the warp-level tensor instructions
-// that an int8 and an f16 contraction could use on this device.  On GB300
-// (sm_103a) tcgen05 has no int8 kind, so the int8 tensor rate available is
-// that of mma.sync.m16n8k32.s8; it is the denominator for "% of int8 tensor
-// peak".  Register-only loops; the one store per thread goes to a static
-// device word (nothing is allocated).
+// that an int8 and an f16 contraction could use on this device (context for
+// the tensor-core kernels: on GB300, sm_103a, tcgen05 has no int8 kind, and
+// these legacy warp-level rates are far below the tcgen05 f16 dense rate the
+// GEMM's roofline uses).  Register-only loops; the one store per thread goes
+// to a static device word (nothing is allocated).  Also the failure-detection
+// self-test of the bounded waits.
 #include <cstdint>
 
 #include "../../include/plm.h"
+#include "plm_device.cuh"
 #include "plm_internal.h"
 
 namespace plm {
@@ -70,7 +72,34 @@ static cudaError_t time_rate(double* out) {
     return cudaSuccess;
 }
 
+// Failure-detection self-test: one warp waits on an mbarrier of its own with
+// the same bounded wait the streaming kernels use, limited to `rounds`
+// rounds.  With complete != 0 the barrier's one arrival is made first, so the
+// wait ends at once; otherwise nothing ever arrives (no copy is issued), the
+// wait runs out and bit 0 of the fault word is set, exactly as a streaming
+// kernel records a copy that never landed.  The kernel then returns.
+__global__ void bounded_wait_kernel(unsigned rounds, int complete, unsigned* fault) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_barrier_init();
+    }
+    __syncwarp();
+    if (threadIdx.x == 0) {
+        if (complete) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(smem_u32(&bar)) : "memory");
+        if (!mbar_wait(&bar, 0, rounds)) atomicOr(fault, 1u);
+    }
+}
+
 }  // namespace plm
+
+extern "C" plm_status plm_selftest_bounded_wait(uint32_t rounds, int complete, cudaStream_t stream) {
+    if (rounds < 1 || rounds > plm::WAIT_LIMIT) return PLM_ERR_INVALID_ARG;
+    unsigned* fault = plm::fault_word();
+    if (!fault) return PLM_ERR_CUDA;
+    plm::bounded_wait_kernel<<<1, 32, 0, stream>>>(rounds, complete ? 1 : 0, fault);
+    return cudaGetLastError() == cudaSuccess ? PLM_OK : PLM_ERR_CUDA;
+}
 
 extern "C" plm_status plm_probe_mma_rates(double* s8_tops, double* f16_tflops) {
     if (!s8_tops || !f16_tflops) return PLM_ERR_INVALID_ARG;

@@ -82,6 +82,8 @@ def load(build_if_missing=True):
     lib.plm_device_fault.restype = ctypes.c_int
     lib.plm_probe_mma_rates.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)]
     lib.plm_probe_mma_rates.restype = ctypes.c_int
+    lib.plm_selftest_bounded_wait.argtypes = [ctypes.c_uint32, ctypes.c_int, vp]
+    lib.plm_selftest_bounded_wait.restype = ctypes.c_int
     lib.plm_quantize_q8K.argtypes = [vp, vp, i64, i64, vp]
     lib.plm_quantize_q8K.restype = ctypes.c_int
     lib.plm_gemm_workspace_size.argtypes = [ctypes.c_int, i64, i64]
@@ -168,6 +170,13 @@ def plm_device_fault(clear=True):
     code = ctypes.c_uint32(0)
     _check("plm_device_fault", lib.plm_device_fault(ctypes.byref(code), 1 if clear else 0))
     return code.value
+
+
+def plm_selftest_bounded_wait(rounds, complete, stream=None):
+    """Launches the bounded-wait self-test (see include/plm.h); asynchronous."""
+    lib = load()
+    _check("plm_selftest_bounded_wait", lib.plm_selftest_bounded_wait(int(rounds), 1 if complete else 0,
+                                                                      _stream(stream)))
 
 
 def plm_probe_mma_rates():

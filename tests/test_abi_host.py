@@ -163,3 +163,9 @@ def test_gemm_swiglu_argument_checks():
     assert lib.plm_gemm_q4K_swiglu_ws(A, A, A, A, 512, 8, 256, A, need - 1, None) == bad
     assert lib.plm_gemm_q4K_swiglu_ws(A, A, A, A, 512, 8, 256, None, need, None) == bad
     assert lib.plm_gemm_q4K_swiglu_ws(A, A, A, A, 512, 8, 256, A + 16, need, None) == P.PLM_ERR_MISALIGNED
+
+
+def test_selftest_bounded_wait_rejects_bad_limits():
+    # host-side checks only: nothing is launched for a rejected limit
+    for rounds in (0, (1 << 16) + 1):
+        assert P.raw_status("plm_selftest_bounded_wait", rounds, 0, None) == P.PLM_ERR_INVALID_ARG
