@@ -402,6 +402,12 @@ plm_status plm_gemm_q6K_ws(const void* w, const void* xq, float* y, int64_t m, i
  *   - All calls share the one array (it keeps the last call's contents, and
  *     each call rewrites the part it reads), so calls whose kernels may
  *     overlap on the GPU, e.g. on different streams, race: serialize them.
+ *   - It never splits K (the array holds no split partial sums), so where
+ *     plm_gemm_q4K would split K -- few output tiles, i.e. small m and n --
+ *     it can be slower, and its f32 sums are added in another order: it then
+ *     agrees with plm_gemm_q4K within the tolerance above, not bit for bit.
+ *   - The array's device address is kept per device for the life of the
+ *     process; do not call it across a cudaDeviceReset.
  */
 #define PLM_NOALLOC_WORKSPACE_BYTES (32u << 20)
 plm_status plm_gemm_q4K_noalloc(const void* w, const void* xq, float* y, int64_t m, int64_t n, int64_t k,

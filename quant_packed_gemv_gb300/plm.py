@@ -25,6 +25,7 @@ Q3K_BYTES = 110
 Q6K_BYTES = 210
 Q8K_BYTES = 292
 GEMV_MAX_M = 8
+PLM_NOALLOC_WORKSPACE_BYTES = 32 << 20   # the fixed array of plm_gemm_q4K_noalloc
 
 
 class PlmError(RuntimeError):

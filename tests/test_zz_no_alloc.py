@@ -50,10 +50,83 @@ def test_noalloc_matches_allocating_gemm_on_two_calls_in_a_row():
     assert q.plm_device_fault() == 0
 
 
+def test_noalloc_small_m_runs_the_gemv():
+    # m <= 8 needs no workspace: the call runs the decode GEMV, like plm_gemm_q4K
+    for m in (1, 8):
+        n, k = 96, 1024
+        w, xq = _case(43, m, n, k)
+        wd, xd = dev(w), dev(xq)
+        y = torch.full((m, n), float("nan"), device="cuda")
+        y_alloc = torch.full((m, n), float("nan"), device="cuda")
+        q.plm_gemm_q4K_noalloc(wd, xd, y, m, n, k)
+        q.plm_gemm_q4K(wd, xd, y_alloc, m, n, k)
+        np.testing.assert_array_equal(host(y), host(y_alloc))
+
+
+def test_noalloc_limit_edge():
+    # workspace bytes = 2*m*k + 48*m*k/256, each part rounded up to 256: at
+    # k = 256, m = 59918 needs 33,554,176 bytes (fits the 32 MiB array) and
+    # m = 59919 needs 33,554,688 (one size up: rejected before any launch)
+    k, n = 256, 64
+    assert q.plm_gemm_workspace_size("q4K", 59918, k) <= P.PLM_NOALLOC_WORKSPACE_BYTES
+    assert q.plm_gemm_workspace_size("q4K", 59919, k) > P.PLM_NOALLOC_WORKSPACE_BYTES
+    m = 59918
+    w, xq = _case(44, m, n, k)
+    wd, xd = dev(w), dev(xq)
+    y = torch.full((m, n), float("nan"), device="cuda")
+    y_alloc = torch.full((m, n), float("nan"), device="cuda")
+    q.plm_gemm_q4K_noalloc(wd, xd, y, m, n, k)
+    q.plm_gemm_q4K(wd, xd, y_alloc, m, n, k)
+    got, want = host(y), host(y_alloc)
+    assert not np.isnan(got).any()
+    rows = np.r_[0:64, m - 64:m]          # the first and last activation tiles against the oracle
+    ref, S = oracle_ref("q4K", w, xq[rows], len(rows), n, k)
+    assert_close(got[rows], ref, S)
+    # 469 output tiles fill the GPU, so plm_gemm_q4K does not split K either:
+    # the same launches, the same bits
+    np.testing.assert_array_equal(got, want)
+    st = P.raw_status("plm_gemm_q4K_noalloc", wd.data_ptr(), xd.data_ptr(), y.data_ptr(), m + 1, n, k, None)
+    assert st == P.PLM_ERR_UNSUPPORTED
+
+
 def test_noalloc_rejects_sizes_beyond_its_array():
     # about 2.19 * m * k bytes of workspace, above PLM_NOALLOC_WORKSPACE_BYTES (32 MiB)
     fake = 1 << 20   # never dereferenced: the call is rejected before any launch
     st = P.raw_status("plm_gemm_q4K_noalloc", fake, fake, fake, 2048, 256, 12288, None)
     assert st == P.PLM_ERR_UNSUPPORTED
-    # small m needs no workspace at all
+    # argument checks come first: m = 0 is an invalid argument, not a size problem
     assert P.raw_status("plm_gemm_q4K_noalloc", fake, fake, fake, 0, 256, 256, None) == P.PLM_ERR_INVALID_ARG
+
+
+def _pool_used_high():
+    """High-water mark of the current device's default stream-ordered memory
+    pool (the pool plm_gemm_q4K's cudaMallocAsync draws on), through the
+    driver API; it is reset to the current use before returning."""
+    import ctypes
+    cu = ctypes.CDLL("libcuda.so.1")
+    dev_h, pool = ctypes.c_int(0), ctypes.c_void_p(0)
+    assert cu.cuDeviceGet(ctypes.byref(dev_h), torch.cuda.current_device()) == 0
+    assert cu.cuDeviceGetDefaultMemPool(ctypes.byref(pool), dev_h) == 0
+    used_high = 8                         # CU_MEMPOOL_ATTR_USED_MEM_HIGH
+    val = ctypes.c_uint64(0)
+    assert cu.cuMemPoolGetAttribute(pool, used_high, ctypes.byref(val)) == 0
+    zero = ctypes.c_uint64(0)
+    assert cu.cuMemPoolSetAttribute(pool, used_high, ctypes.byref(zero)) == 0
+    return val.value
+
+
+def test_noalloc_draws_nothing_from_the_pool():
+    m, n, k = 300, 200, 2048
+    w, xq = _case(45, m, n, k)
+    wd, xd = dev(w), dev(xq)
+    y = torch.full((m, n), float("nan"), device="cuda")
+    torch.cuda.synchronize()
+    _pool_used_high()                     # reset the high-water mark
+    for _ in range(2):
+        q.plm_gemm_q4K_noalloc(wd, xd, y, m, n, k)
+    torch.cuda.synchronize()
+    assert _pool_used_high() == 0
+    # the measurement sees the allocating form's workspace
+    q.plm_gemm_q4K(wd, xd, y, m, n, k)
+    torch.cuda.synchronize()
+    assert _pool_used_high() >= q.plm_gemm_workspace_size("q4K", m, k)
