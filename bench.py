@@ -188,25 +188,63 @@ def cpu_oracle_pass(mats, host_w, xs, count, threads):
         oracle.gemm_q4K_f32(host_w[off:off + sz], xq, 1, n, k)
 
 
-def oracle_rate(mats, host_w, xs, budget_s):
+def oracle_rate(mats, host_w, xs, budget_s, threads=None):
     """Times the oracle (as it stands) on the first matrices of the set,
     as many full passes as fit the budget; returns (GB/s, sample text, cores)."""
     cores = len(os.sched_getaffinity(0))
+    th = cores if threads is None else threads
     t0 = time.perf_counter()
-    cpu_oracle_pass(mats, host_w, xs, 7, cores)           # one layer, warm
+    cpu_oracle_pass(mats, host_w, xs, 7, th)              # one layer, warm
     per_layer = time.perf_counter() - t0
     count = 7 * max(1, min(N_LAYERS, int(budget_s / 4 / max(per_layer, 1e-6))))
     reps, t0 = 0, time.perf_counter()
     while True:
-        cpu_oracle_pass(mats, host_w, xs, count, cores)
+        cpu_oracle_pass(mats, host_w, xs, count, th)
         reps += 1
         el = time.perf_counter() - t0
         if el > budget_s / 2:
             break
     alg = step_bytes(mats[:count]) * reps
     sample = ("%d of 196 matrices (%d of 28 layers) x %d passes: q8_K quantize + q4_K f32 oracle "
-              "GEMV, OpenMP over output rows, %.1f s" % (count, count // 7, reps, el))
+              "GEMV, %s, %.1f s" % (count, count // 7, reps,
+                                    "one thread" if th == 1 else "OpenMP over output rows, %d threads" % th, el))
     return alg / el / 1e9, sample, cores
+
+
+def oracle_details(cores):
+    """The oracle timed the ways the pages time the CPU path: the q8_K
+    quantizer alone on the 512x1024 prefill shape, single-threaded and on all
+    cores, and the q6_K output heads (151936 x 2048 and x 4096) on 1024-row
+    slices at m = 1, 8 and 512, reported per multiply-add and extrapolated to
+    the whole head."""
+    import gen
+    import oracle
+    out = {}
+    x = gen.normal_f32(2, 0, 512, 1024)
+    for label, th in (("single_thread", 1), ("openmp", cores)):
+        oracle.set_threads(th)
+        oracle.quantize_q8K(x)
+        reps, t0 = 0, time.perf_counter()
+        while reps < 3 or time.perf_counter() - t0 < 0.5:
+            oracle.quantize_q8K(x)
+            reps += 1
+        out["quantize_512x1024_" + label] = {"us": (time.perf_counter() - t0) / reps * 1e6, "threads": th}
+    heads = []
+    oracle.set_threads(cores)
+    for seed, k in ((3, 2048), (4, 4096)):
+        w = gen.q6K_blocks(seed, 0, 1024, k)
+        for m in (1, 8, 512):
+            xq = oracle.quantize_q8K(gen.normal_f32(seed, 50 + m, m, k))
+            reps, t0 = 0, time.perf_counter()
+            while reps < 1 or time.perf_counter() - t0 < 0.3:
+                oracle.gemm_q6K_f32(w, xq, m, 1024, k)
+                reps += 1
+            el = (time.perf_counter() - t0) / reps
+            heads.append({"shape": "q6_K 1024 of 151936 rows x %d" % k, "m": m, "s_per_slice": el,
+                          "mac_per_s": 1024.0 * k * m / el,
+                          "full_head_s_extrapolated": el * 151936 / 1024, "threads": cores})
+    out["q6K_head_slices"] = heads
+    return out
 
 
 def run_reference(args, rank):
@@ -288,18 +326,25 @@ def time_case(args):
                           "copies": copies, "fault": q.plm_device_fault()}), flush=True)
 
 
-def recorded_traffic(key):
-    """DRAM bytes per launch from the committed ncu record, or None when the
-    kernel sources changed since the capture."""
+def recorded_counters(key):
+    """The committed ncu record of one kernel (DRAM bytes per launch and other
+    counters), or None when the kernel sources changed since the capture."""
     import hashlib
     try:
         rec = json.load(open(os.path.join(ROOT, "profiles", "ncu_traffic.json")))[key]
         h = hashlib.sha256()
         for p in rec["sources"]:
             h.update(open(os.path.join(ROOT, p), "rb").read())
-        return rec["dram_bytes_per_launch"] if h.hexdigest()[:16] == rec["sources_sha256_16"] else None
+        return rec if h.hexdigest()[:16] == rec["sources_sha256_16"] else None
     except (OSError, ValueError, KeyError):
         return None
+
+
+def recorded_traffic(key):
+    """DRAM bytes per launch from the committed ncu record, or None when the
+    kernel sources changed since the capture."""
+    rec = recorded_counters(key)
+    return rec["dram_bytes_per_launch"] if rec else None
 
 
 # --------------------------------------------------------------- other configs
@@ -369,8 +414,7 @@ class ShapeTimer:
         else:
             tops = 2.0 * m * n * k / us / 1e6
             r.update({"TOPS": round(tops, 1),
-                      "frac_f16_dense": round(tops / self.peaks["bf16_tflops"], 4),
-                      "vs_int8_tensor_peak": round(tops / self.peaks["int8_mma_tops"], 3)})
+                      "frac_f16_dense": round(tops / self.peaks["bf16_tflops"], 4)})
         return r
 
 
@@ -453,6 +497,28 @@ def run_extras(torch, q, peaks):
         out["%s_12288x4096" % fmt] = [T.run(fmt, ws, wb, 12288, 4096, m, 10, 2) for m in (1, 8)]
         del ws
     return out
+
+
+def gemm_roofline(configs, peaks, peak_src):
+    """Roofline of the dominant prefill kernel: the q4_K tensor-core GEMM on
+    the Qwen3-8B gate/up shape 12288 x 4096 at m = 2048, from the sweep's
+    CUDA-event time per call (the call is the activation pre-pass, about 2 %,
+    plus the GEMM kernel, so the kernel's own rate is slightly higher)."""
+    row = next((r for r in configs.get("sweep_qwen3_8b", [])
+                if r["fmt"] == "q4K" and r["n"] == 12288 and r["k"] == 4096 and r["m"] == 2048), None)
+    if row is None:
+        return None
+    peak = peaks["bf16_tflops"]
+    flops = 2.0 * row["m"] * row["n"] * row["k"]
+    achieved = flops / (row["us"] * 1e-6) / 1e12
+    rec = recorded_counters("gemm_q4K_12288x4096_m2048")
+    return {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+            "traffic": rec.get("dram_bytes_per_launch") if rec else None,
+            "tensor_pipe_active_pct": rec.get("tensor_pipe_active_pct") if rec else None,
+            "peak_source": "measured bf16 dense (burst); f16, the kind the kernel runs, has the same nominal rate"
+                           if peak_src == "measured" else "fallback",
+            "kernel": "gemm_kernel<q4_K> (tcgen05.mma kind::f16 on exact integer-valued operands)",
+            "shape": "q4_K 12288x4096, m=2048", "flops_per_call": flops, "avg_call_us": row["us"]}
 
 
 # --------------------------------------------------------------- main arm
@@ -805,17 +871,22 @@ def main():
     out["peaks"] = {"hbm_gbs": peak, "hbm_source": peak_src,
                     "bf16_tflops": peaks.get("bf16_tflops", 1900.0),
                     "int8_mma_tops": s8_tops, "f16_mma_sync_tflops": f16_tflops,
-                    "note": "int8: mma.sync.m16n8k32.s8 measured live (tcgen05 has no int8 kind on sm_103a); "
-                            "the GEMM runs kind::f16, so its roofline is the bf16/f16 dense peak"}
+                    "note": "context only: legacy mma.sync rates measured live (tcgen05 has no int8 kind on "
+                            "sm_103a); the GEMM runs tcgen05 kind::f16, so its roofline is the measured bf16 dense "
+                            "peak (f16 has the same nominal rate)"}
     if rank == 0 and not args.no_extras:
         del st
         torch.cuda.empty_cache()
         out["configs"] = run_extras(torch, q, out["peaks"])
+        out["roofline_gemm"] = gemm_roofline(out["configs"], out["peaks"], peak_src)
     if rank == 0 and not args.no_cpu_baseline:
         val, sample, cores = oracle_rate(mats, host_w, xs, 12.0)
         import oracle
         out["cpu_baseline"] = {"value": val, "unit": "GB/s", "cores": cores, "kind": "oracle",
                                "threads": oracle.max_threads(), "sample": sample}
+        val1, sample1, _ = oracle_rate(mats, host_w, xs, 6.0, threads=1)
+        out["cpu_baseline"]["single_thread"] = {"value": val1, "unit": "GB/s", "threads": 1, "sample": sample1}
+        out["cpu_baseline"].update(oracle_details(cores))
     if rank == 0:
         print(json.dumps(out), flush=True)
     if pg is not None:
