@@ -296,7 +296,16 @@ def time_case(args):
     copies = max(1, -(-3 * l2 // wbytes))
     w_host = getattr(gen, "%s_blocks" % fmt)(4, 0, n, k)
     ws = [torch.from_numpy(w_host).cuda() for _ in range(copies)]
-    fn = getattr(q, "plm_%s_%s" % (kind, fmt))
+    if kind == "gemv_x16":
+        # the row-interleaved layout: repack every copy once (not timed)
+        packed = []
+        for wd in ws:
+            wx = torch.empty(q.plm_q4K_x16_size(n, k), dtype=torch.uint8, device="cuda")
+            q.plm_q4K_to_x16(wd, wx, n, k)
+            packed.append(wx)
+        torch.cuda.synchronize()
+        ws = packed
+    fn = getattr(q, "plm_%s_%s" % (kind, fmt)) if kind != "gemv_x16" else q.plm_gemv_q4K_x16
     q.plm_set_overlap(args.overlap)
     stream = torch.cuda.Stream()
     for m in args.m:
@@ -366,7 +375,18 @@ class ShapeTimer:
         copies = max(1, -(-3 * self.l2 // host.nbytes))
         return [self.torch.from_numpy(host).cuda() for _ in range(copies)], host.nbytes
 
-    def run(self, fmt, ws_list, wbytes, n, k, m, steps, warmup):
+    def x16(self, ws_list, n, k):
+        """The same weight copies repacked into the row-interleaved x16 layout."""
+        torch, q = self.torch, self.q
+        out = []
+        for w in ws_list:
+            wx = torch.empty(q.plm_q4K_x16_size(n, k), dtype=torch.uint8, device="cuda")
+            q.plm_q4K_to_x16(w, wx, n, k)
+            out.append(wx)
+        torch.cuda.synchronize()
+        return out
+
+    def run(self, fmt, ws_list, wbytes, n, k, m, steps, warmup, layout="ggml"):
         import gen
         torch, q = self.torch, self.q
         nb = k // QK
@@ -377,6 +397,8 @@ class ShapeTimer:
         need = 0 if gemv else q.plm_gemm_workspace_size_split(fmt, m, n, k)
         work = torch.empty(max(need, 256), dtype=torch.uint8, device="cuda")
         fn = getattr(q, ("plm_gemv_%s" if gemv else "plm_gemm_%s_ws") % fmt)
+        if layout == "x16":
+            fn = q.plm_gemv_q4K_x16
         s = self.stream
 
         def call(i):
@@ -406,7 +428,7 @@ class ShapeTimer:
         us = e0.elapsed_time(e1) * 1e3 / steps
         byt = wbytes + m * nb * Q8K_BYTES + m * n * 4
         r = {"fmt": fmt, "n": n, "k": k, "m": m, "us": round(us, 3),
-             "entry": "plm_gemv_%s" % fmt if gemv else "plm_gemm_%s_ws" % fmt}
+             "entry": fn.__name__}
         if gemv:
             gbs = byt / us / 1e3
             r.update({"GB_per_s": round(gbs, 1), "frac_hbm": round(gbs / self.peaks["hbm_gbs"], 4),
@@ -477,6 +499,12 @@ def run_extras(torch, q, peaks):
         for m in (1, 2, 4, 8, 64, 512, 2048):
             steps = 10 if m <= 8 else (5 if n * k * m < 3e11 else 2)
             sweep.append(T.run(fmt, ws, wb, n, k, m, steps, 1 if m > 512 else 2))
+        if fmt == "q4K":
+            # the decode GEMV on the row-interleaved layout (tensor-core tile)
+            wx = T.x16(ws, n, k)
+            for m in (1, 2, 4, 8):
+                sweep.append(T.run(fmt, wx, wb, n, k, m, 10, 2, layout="x16"))
+            del wx
         del ws
         torch.cuda.empty_cache()
     out["sweep_qwen3_8b"] = sweep

@@ -414,6 +414,43 @@ plm_status plm_gemm_q4K_noalloc(const void* w, const void* xq, float* y, int64_t
                                 cudaStream_t stream);
 
 /*
+ * Row-interleaved q4_K layout "x16" and its tensor-core decode GEMV.
+ * PocketLLM (Korean README), "Current status" table, row "src/": the packed
+ * q4_K dot runs faster on a load-time repack of the weights (an 8-column
+ * panel) with an 8-row activation tile.  Here the repack interleaves 16
+ * weight rows per 256-weight block, the layout a warp-level tensor-core tile
+ * reads with full 16-byte loads, and the m <= 8 activation rows form the
+ * MMA's columns.  The layout holds the same bytes as the GGML q4_K blocks,
+ * permuted in 16-byte units:
+ *   rows are grouped in tiles of 16 (rows n .. 16*ceil(n/16) - 1 are zero
+ *   blocks); the tile-block of tile T and block b (rows 16T .. 16T+15) is
+ *   2304 contiguous bytes at ((T * (k/256)) + b) * 2304; inside it, bytes
+ *   [0, 256) are the 16-byte headers (f16 d, f16 dmin, scales[12]) of the
+ *   tile's rows in row order, and for j = 0..3 and L = 0..31 (g = L/4,
+ *   t = L%4) bytes 256 + 512j + 16L .. +15 are qs[32t + 16(j%2) .. +15] of
+ *   row 16T + g (j < 2) or row 16T + g + 8 (j >= 2).
+ *
+ * plm_q4K_x16_size: bytes of the x16 form of an n x k q4_K matrix
+ *   (ceil(n/16) * (k/256) * 2304); 0 for invalid arguments.
+ * plm_q4K_to_x16: writes that form of w (q4_K [n][k/256], device, 16-byte
+ *   aligned) into w_x16 (device, plm_q4K_x16_size bytes, 16-byte aligned, not
+ *   overlapping w).  Run once when the weights are loaded.  Under
+ *   PLM_OVERLAP_PREFETCH, a GEMV that follows it on the same stream must not
+ *   read w_x16 before it is written: synchronize (or use another mode) between
+ *   the repack and the first GEMV.
+ * plm_gemv_q4K_x16: y = W . x for 1 <= m <= 8 with W in the x16 form (n, k
+ *   of the original matrix); xq and y as for plm_gemv_q4K.  Integer products
+ *   are exact (f16 operands sc*q and q8 codes, f32 accumulation), the block
+ *   terms d_x*(d*isum - dmin*msum) are formed in f32, and the result is within
+ *   1e-4 of sum_k |w_hat * x_hat| per element.  The result for activation row
+ *   i does not depend on m.  Errors as for plm_gemv_q4K.
+ */
+size_t plm_q4K_x16_size(int64_t n, int64_t k);
+plm_status plm_q4K_to_x16(const void* w, void* w_x16, int64_t n, int64_t k, cudaStream_t stream);
+plm_status plm_gemv_q4K_x16(const void* w_x16, const void* xq, float* y, int64_t m, int64_t n, int64_t k,
+                            cudaStream_t stream);
+
+/*
  * Verification export: the integer sub-block dots computed by the same
  * device decode/dot code the GEMV uses.
  *   q4_K: out int32 [m][n][k/32],  out[i][r][8b+j]  = sum_{l<32} q * q8

@@ -341,6 +341,39 @@ void plm_ref_dequant_q4K(const uint8_t* w, double* out, int64_t n, int64_t k) {
         }
 }
 
+/* The row-interleaved q4_K layout "x16" (a repack of the same bytes for the
+ * GPU decode GEMV, the analogue of the pages' panel repack of q4_K weights,
+ * Korean README, "Current status" table, row "src/").  Definition: rows in
+ * tiles of 16; the tile-block of tile T, block b is 2304 bytes at
+ * (T*nb + b)*2304; its bytes 16i .. 16i+15 are the header (d, dmin,
+ * scales[12]) of row 16T + i; for j = 0..3, L = 0..31 (g = L/4, t = L%4) its
+ * bytes 256 + 512j + 16L .. +15 are qs[32t + 16(j%2) .. +15] of row 16T + g
+ * (j < 2) or 16T + g + 8 (j >= 2).  Below: the inverse walk, from a row's
+ * qs byte c to its place, then the q4_K decode of dequant_q4K. */
+static const uint8_t* x16_qs_byte(const uint8_t* tb, int i, int c) {
+    int t = c / 32, within = c % 32;
+    int g = i % 8, j = (i < 8 ? 0 : 2) + within / 16;
+    return tb + 256 + 512 * j + 16 * (4 * g + t) + within % 16;
+}
+
+void plm_ref_dequant_q4K_x16(const uint8_t* wx, double* out, int64_t n, int64_t k) {
+    int64_t nb = k / QK;
+    for (int64_t r = 0; r < n; ++r)
+        for (int64_t b = 0; b < nb; ++b) {
+            const uint8_t* tb = wx + ((r / 16) * nb + b) * (16 * Q4K_BYTES);
+            const uint8_t* hdr = tb + 16 * (r % 16);
+            double d = load_f16(hdr), dmin = load_f16(hdr + 2);
+            for (int t = 0; t < QK; ++t) {
+                int chunk = t / 64, within = t % 64;
+                int byte = *x16_qs_byte(tb, (int)(r % 16), 32 * chunk + within % 32);
+                int q = within < 32 ? (byte & 15) : (byte >> 4);
+                int sc, mn;
+                plm_ref_q4K_scale_min(hdr + 4, t / 32, &sc, &mn);
+                out[r * k + b * QK + t] = d * sc * q - dmin * mn;
+            }
+        }
+}
+
 void plm_ref_dequant_q6K(const uint8_t* w, double* out, int64_t n, int64_t k) {
     int64_t nb = k / QK;
     for (int64_t r = 0; r < n; ++r)

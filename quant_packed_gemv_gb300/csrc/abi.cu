@@ -400,6 +400,28 @@ plm_status plm_gemm_q4K_noalloc(const void* w, const void* xq, float* y, int64_t
                                                     stream));
 }
 
+size_t plm_q4K_x16_size(int64_t n, int64_t k) {
+    if (n <= 0 || k <= 0 || k % plm::QK != 0 || n > kMaxIndex || k > kMaxIndex) return 0;
+    if (((n + 15) / 16) * (k / plm::QK) > kMaxIndex) return 0;
+    return plm::q4K_x16_bytes(n, (int)k);
+}
+
+plm_status plm_q4K_to_x16(const void* w, void* w_x16, int64_t n, int64_t k, cudaStream_t stream) {
+    if (!w || !w_x16) return PLM_ERR_INVALID_ARG;
+    if (plm_q4K_x16_size(n, k) == 0) return PLM_ERR_INVALID_ARG;
+    if (!aligned(w, 16) || !aligned(w_x16, 16)) return PLM_ERR_MISALIGNED;
+    return cuda_status(plm::launch_repack_q4K_x16((const uint8_t*)w, (uint8_t*)w_x16, (int)n, (int)k, stream));
+}
+
+plm_status plm_gemv_q4K_x16(const void* w_x16, const void* xq, float* y, int64_t m, int64_t n, int64_t k,
+                            cudaStream_t stream) {
+    plm_status s = check_matmul(w_x16, xq, y, m, n, k, plm::GEMV_MAX_M);
+    if (s != PLM_OK) return s;
+    if (plm_q4K_x16_size(n, k) == 0) return PLM_ERR_INVALID_ARG;
+    return cuda_status(plm::launch_gemv_q4K_x16((const uint8_t*)w_x16, (const uint8_t*)xq, y, (int)m, (int)n,
+                                                (int)k, stream));
+}
+
 plm_status plm_quantize_gemv_q4K(const void* w, const float* x, float* y, int64_t m, int64_t n, int64_t k,
                                  cudaStream_t stream) {
     const plm_qgemv_problem p{w, x, y, n, k};

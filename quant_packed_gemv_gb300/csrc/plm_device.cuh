@@ -270,6 +270,10 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                  :: "r"(smem_u32(bar)), "r"(bytes) : "memory");
 }
 
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(smem_u32(bar)) : "memory");
+}
+
 // Returns true once the phase with the given parity has completed, false if
 // `limit` rounds (WAIT_LIMIT unless given) pass first.  Each round lets the
 // hardware suspend the warp for up to SUSPEND_NS (it resumes as soon as the

@@ -140,3 +140,29 @@ def pack_q8K(d, qs):
     blk[4:260] = qs.astype(np.int8).view(np.uint8)
     blk[260:292] = qs.reshape(16, 16).sum(axis=1).astype(np.int16).view(np.uint8)
     return blk
+
+
+def pack_q4K_x16(w, n, k):
+    """The row-interleaved x16 form of q4_K weights w [n][k/256 * 144], built
+    from the layout text in the packing direction: for every tile T (rows
+    16T..16T+15, zero blocks past n) and block b, a 2304-byte tile-block made
+    of the 16 headers (bytes 0..15 of each row's block) and, for j = 0..3 and
+    L = 0..31, the 16-byte piece qs[32(L%4) + 16(j%2) ..] of row L//4 (+8 when
+    j >= 2)."""
+    nb = k // 256
+    ntiles = -(-n // 16)
+    src = np.zeros((ntiles * 16, nb, 144), dtype=np.uint8)
+    src[:n] = np.asarray(w, dtype=np.uint8).reshape(n, nb, 144)
+    out = np.zeros((ntiles, nb, 2304), dtype=np.uint8)
+    for T in range(ntiles):
+        for b in range(nb):
+            tb = out[T, b]
+            for i in range(16):
+                tb[16 * i:16 * i + 16] = src[16 * T + i, b, 0:16]
+            for j in range(4):
+                for L in range(32):
+                    row = 16 * T + L // 4 + (8 if j >= 2 else 0)
+                    q0 = 16 + 32 * (L % 4) + 16 * (j % 2)     # qs starts at byte 16 of the block
+                    off = 256 + 512 * j + 16 * L
+                    tb[off:off + 16] = src[row, b, q0:q0 + 16]
+    return out.reshape(-1)
