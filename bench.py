@@ -300,12 +300,12 @@ def time_case(args):
         # the row-interleaved layout: repack every copy once (not timed)
         packed = []
         for wd in ws:
-            wx = torch.empty(q.plm_q4K_x16_size(n, k), dtype=torch.uint8, device="cuda")
-            q.plm_q4K_to_x16(wd, wx, n, k)
+            wx = torch.empty(getattr(q, "plm_%s_x16_size" % fmt)(n, k), dtype=torch.uint8, device="cuda")
+            getattr(q, "plm_%s_to_x16" % fmt)(wd, wx, n, k)
             packed.append(wx)
         torch.cuda.synchronize()
         ws = packed
-    fn = getattr(q, "plm_%s_%s" % (kind, fmt)) if kind != "gemv_x16" else q.plm_gemv_q4K_x16
+    fn = getattr(q, "plm_%s_%s" % (kind, fmt)) if kind != "gemv_x16" else getattr(q, "plm_gemv_%s_x16" % fmt)
     q.plm_set_overlap(args.overlap)
     stream = torch.cuda.Stream()
     for m in args.m:
@@ -375,13 +375,13 @@ class ShapeTimer:
         copies = max(1, -(-3 * self.l2 // host.nbytes))
         return [self.torch.from_numpy(host).cuda() for _ in range(copies)], host.nbytes
 
-    def x16(self, ws_list, n, k):
+    def x16(self, fmt, ws_list, n, k):
         """The same weight copies repacked into the row-interleaved x16 layout."""
         torch, q = self.torch, self.q
         out = []
         for w in ws_list:
-            wx = torch.empty(q.plm_q4K_x16_size(n, k), dtype=torch.uint8, device="cuda")
-            q.plm_q4K_to_x16(w, wx, n, k)
+            wx = torch.empty(getattr(q, "plm_%s_x16_size" % fmt)(n, k), dtype=torch.uint8, device="cuda")
+            getattr(q, "plm_%s_to_x16" % fmt)(w, wx, n, k)
             out.append(wx)
         torch.cuda.synchronize()
         return out
@@ -398,7 +398,7 @@ class ShapeTimer:
         work = torch.empty(max(need, 256), dtype=torch.uint8, device="cuda")
         fn = getattr(q, ("plm_gemv_%s" if gemv else "plm_gemm_%s_ws") % fmt)
         if layout == "x16":
-            fn = q.plm_gemv_q4K_x16
+            fn = getattr(q, "plm_gemv_%s_x16" % fmt)
         s = self.stream
 
         def call(i):
@@ -492,20 +492,20 @@ def run_extras(torch, q, peaks):
     ws, wb = T.weights("q6K", 3, 151936, 2048)
     out["q6K_head_151936x2048"] = [T.run("q6K", ws, wb, 151936, 2048, m, 10 if m <= 8 else 4, 2)
                                    for m in (1, 8, 512)]
-    del ws
+    wx = T.x16("q6K", ws, 151936, 2048)
+    out["q6K_head_151936x2048"] += [T.run("q6K", wx, wb, 151936, 2048, m, 10, 2, layout="x16") for m in (1, 8)]
+    del ws, wx
     sweep = []
     for fmt, n, k in [("q4K", 12288, 4096), ("q4K", 4096, 12288), ("q6K", 151936, 4096)]:
         ws, wb = T.weights(fmt, 4, n, k)
         for m in (1, 2, 4, 8, 64, 512, 2048):
             steps = 10 if m <= 8 else (5 if n * k * m < 3e11 else 2)
             sweep.append(T.run(fmt, ws, wb, n, k, m, steps, 1 if m > 512 else 2))
-        if fmt == "q4K":
-            # the decode GEMV on the row-interleaved layout (tensor-core tile)
-            wx = T.x16(ws, n, k)
-            for m in (1, 2, 4, 8):
-                sweep.append(T.run(fmt, wx, wb, n, k, m, 10, 2, layout="x16"))
-            del wx
-        del ws
+        # the decode GEMV on the row-interleaved layout (tensor-core tile)
+        wx = T.x16(fmt, ws, n, k)
+        for m in (1, 2, 4, 8):
+            sweep.append(T.run(fmt, wx, wb, n, k, m, 10, 2, layout="x16"))
+        del ws, wx
         torch.cuda.empty_cache()
     out["sweep_qwen3_8b"] = sweep
     # the q5_K rung on the Qwen3-8B gate/up shape: decode GEMV and prefill GEMM

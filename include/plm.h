@@ -451,6 +451,32 @@ plm_status plm_gemv_q4K_x16(const void* w_x16, const void* xq, float* y, int64_t
                             cudaStream_t stream);
 
 /*
+ * The x16 layout of q6_K (the output head, "Current status" row "src/":
+ * summed in int32 because its sub-blocks overflow int16) and its tensor-core
+ * decode GEMV.  Same bytes as the GGML q6_K blocks, rearranged in 4-byte
+ * pieces: rows in tiles of 16 (rows n .. 16*ceil(n/16) - 1 zero); the
+ * tile-block of tile T, block b is 3360 bytes at ((T * (k/256)) + b) * 3360:
+ *   [0, 256)      the 16 int8 scales of row 16T + i at 16 i;
+ *   [256, 288)    the f16 d of row 16T + i at 256 + 2 i;
+ *   [288, 2336)   for j = 0..3, L = 0..31 (g = L/4, t = L%4): 16 bytes at
+ *                 288 + 512 j + 16 L holding ql[64h + 16w + 4t .. +3] for
+ *                 w = 0..3 (h = j % 2) of row 16T + g (j < 2) or 16T + g + 8;
+ *   [2336, 3360)  for j = 0..1: 16 bytes at 2336 + 512 j + 16 L holding
+ *                 qh[32h + 16s + 4t .. +3] for (h, s) = (0,0), (0,1), (1,0),
+ *                 (1,1) of row 16T + g + 8 j.
+ * plm_q6K_x16_size / plm_q6K_to_x16 / plm_gemv_q6K_x16: as the q4_K forms
+ * (w q6_K [n][k/256], device, 16-byte aligned; 3360 bytes per tile-block).
+ * The GEMV forms each 16-group's dot with (q6 - 32) codes exact in f16 and
+ * applies the group's int8 scale to the exact integer result in f32, so
+ * every int8 scale is exact; same tolerance, errors and m-independence as
+ * plm_gemv_q4K_x16.
+ */
+size_t plm_q6K_x16_size(int64_t n, int64_t k);
+plm_status plm_q6K_to_x16(const void* w, void* w_x16, int64_t n, int64_t k, cudaStream_t stream);
+plm_status plm_gemv_q6K_x16(const void* w_x16, const void* xq, float* y, int64_t m, int64_t n, int64_t k,
+                            cudaStream_t stream);
+
+/*
  * Verification export: the integer sub-block dots computed by the same
  * device decode/dot code the GEMV uses.
  *   q4_K: out int32 [m][n][k/32],  out[i][r][8b+j]  = sum_{l<32} q * q8

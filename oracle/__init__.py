@@ -67,7 +67,8 @@ def _load():
             getattr(lib, name).argtypes = sig6
             getattr(lib, name).restype = None
         for name in ("plm_ref_dequant_q2K", "plm_ref_dequant_q3K", "plm_ref_dequant_q4K", "plm_ref_dequant_q5K",
-                     "plm_ref_dequant_q6K", "plm_ref_dequant_q8K", "plm_ref_dequant_q4K_x16"):
+                     "plm_ref_dequant_q6K", "plm_ref_dequant_q8K", "plm_ref_dequant_q4K_x16",
+                     "plm_ref_dequant_q6K_x16"):
             getattr(lib, name).argtypes = [vp, vp, i64, i64]
             getattr(lib, name).restype = None
         lib.plm_ref_quantize_q8K.argtypes = [vp, vp, i64, i64]
@@ -277,6 +278,14 @@ def dequant_q4K_x16(wx, n, k):
     wx = _u8(wx)
     out = np.empty((n, k), dtype=np.float64)
     _load().plm_ref_dequant_q4K_x16(_p(wx), _p(out), n, k)
+    return out
+
+
+def dequant_q6K_x16(wx, n, k):
+    """f64 weights [n, k] read from the x16 layout of q6_K (see plm_ref.c)."""
+    wx = _u8(wx)
+    out = np.empty((n, k), dtype=np.float64)
+    _load().plm_ref_dequant_q6K_x16(_p(wx), _p(out), n, k)
     return out
 
 

@@ -374,6 +374,45 @@ void plm_ref_dequant_q4K_x16(const uint8_t* wx, double* out, int64_t n, int64_t 
         }
 }
 
+/* The x16 layout of q6_K: rows in tiles of 16; the tile-block of tile T,
+ * block b is 3360 bytes at (T*nb + b)*3360: bytes 16i .. 16i+15 are the int8
+ * scales of row 16T + i, bytes 256 + 2i .. +1 its f16 d; for j = 0..3 and
+ * L = 0..31 (g = L/4, t = L%4), bytes 288 + 512j + 16L + 4w .. +3 (w = 0..3)
+ * are ql[64(j%2) + 16w + 4t .. +3] of row 16T + g (j < 2) or 16T + g + 8;
+ * for j = 0..1, bytes 2336 + 512j + 16L + 4p .. +3 (p = 2h + s) are
+ * qh[32h + 16s + 4t .. +3] of row 16T + g + 8j.  Below: the inverse walk
+ * from a row's ql / qh byte to its place, then the q6_K decode of
+ * dequant_q6K. */
+static const uint8_t* x16_q6K_ql(const uint8_t* tb, int i, int c) {   /* ql[c], c < 128 */
+    int h = c / 64, w = (c % 64) / 16, t = (c % 16) / 4, e = c % 4;
+    int g = i % 8, j = (i < 8 ? 0 : 2) + h;
+    return tb + 288 + 512 * j + 16 * (4 * g + t) + 4 * w + e;
+}
+static const uint8_t* x16_q6K_qh(const uint8_t* tb, int i, int c) {   /* qh[c], c < 64 */
+    int h = c / 32, s = (c % 32) / 16, t = (c % 16) / 4, e = c % 4;
+    int g = i % 8, j = i < 8 ? 0 : 1;
+    return tb + 2336 + 512 * j + 16 * (4 * g + t) + 4 * (2 * h + s) + e;
+}
+
+void plm_ref_dequant_q6K_x16(const uint8_t* wx, double* out, int64_t n, int64_t k) {
+    int64_t nb = k / QK;
+    for (int64_t r = 0; r < n; ++r)
+        for (int64_t b = 0; b < nb; ++b) {
+            const uint8_t* tb = wx + ((r / 16) * nb + b) * (16 * Q6K_BYTES);
+            int i = (int)(r % 16);
+            double d = load_f16(tb + 256 + 2 * i);
+            for (int t = 0; t < QK; ++t) {
+                int half = t / 128, quarter = (t % 128) / 32, l = t % 32;
+                int lbyte = *x16_q6K_ql(tb, i, 64 * half + 32 * (quarter & 1) + l);
+                int low4 = (quarter & 2) ? (lbyte >> 4) : (lbyte & 15);
+                int high2 = (*x16_q6K_qh(tb, i, 32 * half + l) >> (2 * quarter)) & 3;
+                int q = low4 | (high2 << 4);
+                int sc = (int8_t)tb[16 * i + t / 16];
+                out[r * k + b * QK + t] = d * sc * (q - 32);
+            }
+        }
+}
+
 void plm_ref_dequant_q6K(const uint8_t* w, double* out, int64_t n, int64_t k) {
     int64_t nb = k / QK;
     for (int64_t r = 0; r < n; ++r)

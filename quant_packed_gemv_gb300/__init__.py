@@ -10,6 +10,6 @@ from .plm import (  # noqa: F401
     plm_gemv_q5K, plm_gemv_q5K_grouped, plm_gemm_q5K, plm_gemm_q5K_ws, plm_subdots_q5K, Q5K_BYTES,
     plm_gemv_q2K, plm_gemv_q2K_grouped, plm_gemm_q2K, plm_gemm_q2K_ws, plm_subdots_q2K, Q2K_BYTES,
     plm_gemv_q3K, plm_gemv_q3K_grouped, plm_gemm_q3K, plm_gemm_q3K_ws, plm_subdots_q3K, Q3K_BYTES,
-    plm_q4K_x16_size, plm_q4K_to_x16, plm_gemv_q4K_x16,
+    plm_q4K_x16_size, plm_q4K_to_x16, plm_gemv_q4K_x16, plm_q6K_x16_size, plm_q6K_to_x16, plm_gemv_q6K_x16,
     QK, Q4K_BYTES, Q6K_BYTES, Q8K_BYTES, GEMV_MAX_M,
 )

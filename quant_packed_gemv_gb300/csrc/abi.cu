@@ -210,6 +210,28 @@ plm_status subdots_common(int fmt, const void* w, const void* xq, int32_t* out, 
                                            (int)n, (int)k, stream));
 }
 
+size_t x16_size(int fmt, int64_t n, int64_t k) {
+    if (n <= 0 || k <= 0 || k % plm::QK != 0 || n > kMaxIndex || k > kMaxIndex) return 0;
+    if (((n + 15) / 16) * (k / plm::QK) > kMaxIndex) return 0;
+    return plm::x16_bytes(fmt, n, (int)k);
+}
+
+plm_status x16_repack(int fmt, const void* w, void* w_x16, int64_t n, int64_t k, cudaStream_t stream) {
+    if (!w || !w_x16) return PLM_ERR_INVALID_ARG;
+    if (x16_size(fmt, n, k) == 0) return PLM_ERR_INVALID_ARG;
+    if (!aligned(w, 16) || !aligned(w_x16, 16)) return PLM_ERR_MISALIGNED;
+    return cuda_status(plm::launch_repack_x16(fmt, (const uint8_t*)w, (uint8_t*)w_x16, (int)n, (int)k, stream));
+}
+
+plm_status x16_gemv(int fmt, const void* w_x16, const void* xq, float* y, int64_t m, int64_t n, int64_t k,
+                    cudaStream_t stream) {
+    plm_status s = check_matmul(w_x16, xq, y, m, n, k, plm::GEMV_MAX_M);
+    if (s != PLM_OK) return s;
+    if (x16_size(fmt, n, k) == 0) return PLM_ERR_INVALID_ARG;
+    return cuda_status(plm::launch_gemv_x16(fmt, (const uint8_t*)w_x16, (const uint8_t*)xq, y, (int)m, (int)n,
+                                            (int)k, stream));
+}
+
 }  // namespace
 
 extern "C" {
@@ -400,26 +422,23 @@ plm_status plm_gemm_q4K_noalloc(const void* w, const void* xq, float* y, int64_t
                                                     stream));
 }
 
-size_t plm_q4K_x16_size(int64_t n, int64_t k) {
-    if (n <= 0 || k <= 0 || k % plm::QK != 0 || n > kMaxIndex || k > kMaxIndex) return 0;
-    if (((n + 15) / 16) * (k / plm::QK) > kMaxIndex) return 0;
-    return plm::q4K_x16_bytes(n, (int)k);
-}
+size_t plm_q4K_x16_size(int64_t n, int64_t k) { return x16_size(4, n, k); }
+size_t plm_q6K_x16_size(int64_t n, int64_t k) { return x16_size(6, n, k); }
 
 plm_status plm_q4K_to_x16(const void* w, void* w_x16, int64_t n, int64_t k, cudaStream_t stream) {
-    if (!w || !w_x16) return PLM_ERR_INVALID_ARG;
-    if (plm_q4K_x16_size(n, k) == 0) return PLM_ERR_INVALID_ARG;
-    if (!aligned(w, 16) || !aligned(w_x16, 16)) return PLM_ERR_MISALIGNED;
-    return cuda_status(plm::launch_repack_q4K_x16((const uint8_t*)w, (uint8_t*)w_x16, (int)n, (int)k, stream));
+    return x16_repack(4, w, w_x16, n, k, stream);
+}
+plm_status plm_q6K_to_x16(const void* w, void* w_x16, int64_t n, int64_t k, cudaStream_t stream) {
+    return x16_repack(6, w, w_x16, n, k, stream);
 }
 
 plm_status plm_gemv_q4K_x16(const void* w_x16, const void* xq, float* y, int64_t m, int64_t n, int64_t k,
                             cudaStream_t stream) {
-    plm_status s = check_matmul(w_x16, xq, y, m, n, k, plm::GEMV_MAX_M);
-    if (s != PLM_OK) return s;
-    if (plm_q4K_x16_size(n, k) == 0) return PLM_ERR_INVALID_ARG;
-    return cuda_status(plm::launch_gemv_q4K_x16((const uint8_t*)w_x16, (const uint8_t*)xq, y, (int)m, (int)n,
-                                                (int)k, stream));
+    return x16_gemv(4, w_x16, xq, y, m, n, k, stream);
+}
+plm_status plm_gemv_q6K_x16(const void* w_x16, const void* xq, float* y, int64_t m, int64_t n, int64_t k,
+                            cudaStream_t stream) {
+    return x16_gemv(6, w_x16, xq, y, m, n, k, stream);
 }
 
 plm_status plm_quantize_gemv_q4K(const void* w, const float* x, float* y, int64_t m, int64_t n, int64_t k,

@@ -51,16 +51,22 @@ namespace plm {
 namespace x16 {
 
 constexpr int TR = 16;                      // weight rows per tile (MMA M)
-constexpr int TB = TR * Q4K_BYTES;          // 2304 bytes per tile-block
+// bytes of one tile-block (16 rows x one 256-weight block)
+template <int FMT> struct X16;
+// and the ring slots per warp that fit beside the partial sums
+template <> struct X16<4> { static constexpr int TB = TR * Q4K_BYTES, NS = 4; };   // 2304
+template <> struct X16<6> { static constexpr int TB = TR * Q6K_BYTES, NS = 3; };   // 3360
 constexpr int WARPS = 16;
 constexpr int THREADS = WARPS * 32;
 constexpr int R = 6;                        // tiles per team per round
-constexpr int NS = 4;                       // ring slots per warp
 constexpr int PSTRIDE = 20;                 // floats per activation row of a partial tile (16 rows + pad)
 constexpr int PART_FLOATS = 8 * PSTRIDE;    // one warp's partial sums of one tile: [col][row], padded
 constexpr int PART_BYTES = WARPS * R * PART_FLOATS * 4;   // 60 KB of partial sums per round
-constexpr int RING_BYTES = WARPS * NS * TB;
-constexpr int SMEM = PART_BYTES + RING_BYTES + WARPS * NS * 8;
+template <int FMT> __host__ __device__ constexpr int ring_bytes() { return WARPS * X16<FMT>::NS * X16<FMT>::TB; }
+template <int FMT> __host__ __device__ constexpr int smem_bytes() {
+    return PART_BYTES + ring_bytes<FMT>() + WARPS * X16<FMT>::NS * 8;
+}
+static_assert(smem_bytes<4>() <= 227 * 1024 && smem_bytes<6>() <= 227 * 1024, "x16 shared memory");
 
 struct Args {
     const uint8_t* w;        // x16 tile-blocks [ntiles][nb]
@@ -73,6 +79,8 @@ struct Args {
     // decode constants passed as values, so that they stay in registers
     // (0x000F000F, 0x00F000F0, 0x64006400, 1 << 24)
     uint32_t kmlo, kmhi, kmagic, k2p24;
+    uint32_t km1056;         // f16 pair (-1056, -1056)
+    uint32_t k0f, k30;       // 0x0F0F0F0F, 0x30303030
 };
 
 __device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
@@ -94,17 +102,28 @@ __device__ __forceinline__ uint32_t codes_to_h2(uint32_t p) {
 }
 
 // Activation fragments of one 256-value block for lane (g, t): row g of the
-// activations (zero when g >= m), the weights of chunk t in the kernel's k
-// order; the min term's bsum fragment; d of activation rows 2t, 2t + 1.
+// activations (zero when g >= m) in the kernel's k order; q4_K: the weights
+// of chunk t and the min term's bsum fragment; q6_K: values 16G + 4t ..
+// 16G + 4t + 3 of every 16-group G.  And d of activation rows 2t, 2t + 1.
 struct BFrag {
     uint32_t b[16][2];
     uint32_t bm[2];
     float dx[2];
 };
 
+template <int FMT>
 __device__ __forceinline__ void load_bfrag(BFrag& F, const uint8_t* __restrict__ xq, int m, int nb, int b, int g,
                                            int t) {
-    if (g < m) {
+    if (FMT == 6 && g < m) {
+        const uint32_t* cw = reinterpret_cast<const uint32_t*>(xq + ((size_t)g * nb + b) * Q8K_BYTES + 4) + t;
+#pragma unroll
+        for (int G = 0; G < 16; ++G) {
+            const uint32_t x = __ldg(cw + 4 * G);
+            F.b[G][0] = codes_to_h2(__byte_perm(x, 0, 0x4140));
+            F.b[G][1] = codes_to_h2(__byte_perm(x, 0, 0x4342));
+        }
+        F.bm[0] = F.bm[1] = 0u;
+    } else if (FMT == 4 && g < m) {
         const uint8_t* blk = xq + ((size_t)g * nb + b) * Q8K_BYTES;
         const uint32_t* cw = reinterpret_cast<const uint32_t*>(blk + 4 + 64 * t);
 #pragma unroll
@@ -222,13 +241,87 @@ __device__ __forceinline__ void tile_block(const uint8_t* slot, int g, int lane,
     }
 }
 
+// q6_K tile-block (x16 layout, 3360 bytes): [0, 256) the int8 scales of the
+// 16 rows (row i at 16 i); [256, 288) their f16 d; [288, 2336) ql: for
+// j = 0..3 and lane L = (g, t), 16 bytes at 288 + 512 j + 16 L holding the
+// 4-byte pieces ql[64h + 16w + 4t ..] (w = 0..3, h = j % 2) of row g (j < 2)
+// or g + 8; [2336, 3360) qh: for j = 0..1, 16 bytes at 2336 + 512 j + 16 L
+// holding qh[32h + 16s + 4t ..] for (h, s) = (0,0), (0,1), (1,0), (1,1) of row
+// g + 8 j.  One MMA per 16-group G = 8h + 2qq + s: lane t's A positions
+// 2t + e and 2t + 8 + e carry the codes of weights 16G + 4t + e and
+// 16G + 4t + 2 + e as the exact f16 values q6 - 32; the group's int8 scale
+// is applied to the MMA's exact integer result in f32 (sc * D < 2^24), so
+// every int8 scale is exact.
+struct Q6Consts {
+    uint32_t k0f, k30, magic, m1056;   // 0x0F0F0F0F, 0x30303030, 0x64, f16 (-1056, -1056)
+};
+
+__device__ __forceinline__ float sbyte_f32(uint32_t w_x80, uint32_t sel) {
+    // byte of (scales ^ 0x80) -> 2^23 + 128 + sc as f32 bits, then the offset off
+    return __fadd_rn(__uint_as_float(__byte_perm(w_x80, 0x4B000000u, sel)), -8388736.0f);
+}
+
+__device__ __forceinline__ void tile_block_q6(const uint8_t* slot, int g, int lane, const Q6Consts& K,
+                                              const BFrag& F, float (&acc)[4]) {
+    const uint4 sg = *reinterpret_cast<const uint4*>(slot + 16 * g);
+    const uint4 sh = *reinterpret_cast<const uint4*>(slot + 16 * (g + 8));
+    const float dg = __half2float(*reinterpret_cast<const __half*>(slot + 256 + 2 * g));
+    const float dh = __half2float(*reinterpret_cast<const __half*>(slot + 256 + 2 * (g + 8)));
+    const uint4* lp = reinterpret_cast<const uint4*>(slot + 288) + lane;
+    const uint4 l0 = lp[0], l1 = lp[32], l2 = lp[64], l3 = lp[96];
+    const uint4* hp = reinterpret_cast<const uint4*>(slot + 2336) + lane;
+    const uint4 h0 = hp[0], h1 = hp[32];
+    const uint32_t qlg[2][4] = {{l0.x, l0.y, l0.z, l0.w}, {l1.x, l1.y, l1.z, l1.w}};
+    const uint32_t qlh[2][4] = {{l2.x, l2.y, l2.z, l2.w}, {l3.x, l3.y, l3.z, l3.w}};
+    const uint32_t qhg[4] = {h0.x, h0.y, h0.z, h0.w}, qhh[4] = {h1.x, h1.y, h1.z, h1.w};
+    const uint32_t scg[4] = {sg.x ^ 0x80808080u, sg.y ^ 0x80808080u, sg.z ^ 0x80808080u, sg.w ^ 0x80808080u};
+    const uint32_t sch[4] = {sh.x ^ 0x80808080u, sh.y ^ 0x80808080u, sh.z ^ 0x80808080u, sh.w ^ 0x80808080u};
+    float is[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+            const uint32_t hg = qhg[2 * h + s], hh = qhh[2 * h + s];
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq) {
+                const int G = 8 * h + 2 * qq + s;
+                // top two bits of each code (bits 2qq, 2qq + 1 of qh) to bits 4-5
+                const uint32_t tg = (qq < 2 ? hg << (4 - 2 * qq) : hg >> (2 * qq - 4)) & K.k30;
+                const uint32_t th = (qq < 2 ? hh << (4 - 2 * qq) : hh >> (2 * qq - 4)) & K.k30;
+                // low four bits: low nibbles of ql for quarters 0, 1, high nibbles for 2, 3
+                const uint32_t lg = qlg[h][2 * (qq & 1) + s], lh = qlh[h][2 * (qq & 1) + s];
+                const uint32_t cg = and_or(qq < 2 ? lg : lg >> 4, K.k0f, tg);
+                const uint32_t ch = and_or(qq < 2 ? lh : lh >> 4, K.k0f, th);
+                // (1024 + q6) pairs through the bit pattern, minus 1056: q6 - 32, exact
+                const __half2 m1056 = u2h(K.m1056);
+                const uint32_t a0 = h2u(__hadd2(u2h(__byte_perm(cg, K.magic, 0x4140)), m1056));
+                const uint32_t a1 = h2u(__hadd2(u2h(__byte_perm(ch, K.magic, 0x4140)), m1056));
+                const uint32_t a2 = h2u(__hadd2(u2h(__byte_perm(cg, K.magic, 0x4342)), m1056));
+                const uint32_t a3 = h2u(__hadd2(u2h(__byte_perm(ch, K.magic, 0x4342)), m1056));
+                float dd[4] = {0.f, 0.f, 0.f, 0.f};
+                mma16816(dd, a0, a1, a2, a3, F.b[G][0], F.b[G][1]);
+                const uint32_t sel = (uint32_t)(G & 3) | 0x7540u;
+                const float s_g = sbyte_f32(scg[G >> 2], sel), s_h = sbyte_f32(sch[G >> 2], sel);
+                is[0] = __fmaf_rn(s_g, dd[0], is[0]);
+                is[1] = __fmaf_rn(s_g, dd[1], is[1]);
+                is[2] = __fmaf_rn(s_h, dd[2], is[2]);
+                is[3] = __fmaf_rn(s_h, dd[3], is[3]);
+            }
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[j] = __fmaf_rn(F.dx[j & 1], __fmul_rn(j < 2 ? dg : dh, is[j]), acc[j]);
+}
+
+template <int FMT>
 __global__ void __launch_bounds__(THREADS, 1) gemv_x16_kernel(const __grid_constant__ Args A) {
+    constexpr int TB = X16<FMT>::TB, NS = X16<FMT>::NS;
     extern __shared__ __align__(128) uint8_t smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, t = lane & 3;
     float* part = reinterpret_cast<float*>(smem);
     uint8_t* ring = smem + PART_BYTES + (size_t)warp * NS * TB;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + PART_BYTES + RING_BYTES) + warp * NS;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + PART_BYTES + ring_bytes<FMT>()) + warp * NS;
     if (lane == 0) {
         for (int j = 0; j < NS; ++j) mbar_init(&bars[j], 1);
         fence_barrier_init();
@@ -294,6 +387,11 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_x16_kernel(const __grid_const
     K.mhi = A.kmhi;
     K.magic = A.kmagic;
     K.p24 = A.k2p24;
+    Q6Consts K6;
+    K6.k0f = A.k0f;
+    K6.k30 = A.k30;
+    K6.magic = A.kmagic >> 24;               // 0x64
+    K6.m1056 = A.km1056;
 
     uint32_t consumed = 0, cslot = 0, cphase = 0;
     bool ok = true;
@@ -307,7 +405,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_x16_kernel(const __grid_const
         for (int bi = 0; bi < BPW && nt > 0 && ok; ++bi) {
             const int b = kw * BPW + bi;
             if (b != fbk) {
-                load_bfrag(F, A.xq, A.m, nb, b, g, t);
+                load_bfrag<FMT>(F, A.xq, A.m, nb, b, g, t);
                 fbk = b;
             }
 #pragma unroll 1
@@ -328,7 +426,10 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_x16_kernel(const __grid_const
                     acc[2] = pp[8];
                     acc[3] = pp[PSTRIDE + 8];
                 }
-                tile_block(ring + cslot * TB, g, lane, L, K, F, acc);
+                if constexpr (FMT == 4)
+                    tile_block(ring + cslot * TB, g, lane, L, K, F, acc);
+                else
+                    tile_block_q6(ring + cslot * TB, g, lane, K6, F, acc);
                 pp[0] = acc[0];
                 pp[PSTRIDE] = acc[1];
                 pp[8] = acc[2];
@@ -364,15 +465,16 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_x16_kernel(const __grid_const
         for (uint32_t c = consumed; c < issued; ++c) (void)mbar_wait(&bars[c % NS], (c / NS) & 1u);
 }
 
-// x16 repack: one thread per 16-byte unit of the output.
-__global__ void repack_x16_kernel(const uint8_t* __restrict__ w, uint8_t* __restrict__ out, int n, int nb,
-                                  long long units) {
+// x16 repack of q4_K: one thread per 16-byte unit of the output.
+__global__ void repack_x16_q4K_kernel(const uint8_t* __restrict__ w, uint8_t* __restrict__ out, int n, int nb,
+                                      long long units) {
     grid_launch_dependents();
     grid_wait_prior();
+    constexpr int UPB = X16<4>::TB / 16;   // 144 units per tile-block
     for (long long u = (long long)blockIdx.x * blockDim.x + threadIdx.x; u < units;
          u += (long long)gridDim.x * blockDim.x) {
-        const long long tb = u / (TB / 16);
-        const int o = (int)(u - tb * (TB / 16));
+        const long long tb = u / UPB;
+        const int o = (int)(u - tb * UPB);
         const long long tile = tb / nb;
         const int b = (int)(tb - tile * nb);
         int row, src;
@@ -391,23 +493,81 @@ __global__ void repack_x16_kernel(const uint8_t* __restrict__ w, uint8_t* __rest
     }
 }
 
-}  // namespace x16
-
-size_t q4K_x16_bytes(long long n, int k) {
-    return (size_t)((n + x16::TR - 1) / x16::TR) * (k / QK) * x16::TB;
+// x16 repack of q6_K: one thread per 16-byte unit of the output, gathered as
+// four 4-byte pieces (q6_K blocks are only 2-byte aligned: 16-bit loads).
+__global__ void repack_x16_q6K_kernel(const uint8_t* __restrict__ w, uint8_t* __restrict__ out, int n, int nb,
+                                      long long units) {
+    grid_launch_dependents();
+    grid_wait_prior();
+    constexpr int UPB = X16<6>::TB / 16;   // 210 units per tile-block
+    for (long long u = (long long)blockIdx.x * blockDim.x + threadIdx.x; u < units;
+         u += (long long)gridDim.x * blockDim.x) {
+        const long long tb = u / UPB;
+        const int o = (int)(u - tb * UPB);
+        const long long tile = tb / nb;
+        const int b = (int)(tb - tile * nb);
+        uint32_t v[4];
+        for (int p = 0; p < 4; ++p) {
+            // piece p of the unit: a row and a 4-byte offset inside its block
+            int row, off;
+            if (o < 16) {                      // scales of row o
+                row = o;
+                off = 192 + 4 * p;
+            } else if (o < 18) {               // d of rows 8(o-16) + 2p, + 1
+                row = -1;
+                off = 0;
+            } else if (o < 146) {              // ql pieces
+                const int j = (o - 18) >> 5, L = (o - 18) & 31;
+                row = (L >> 2) + (j >= 2 ? 8 : 0);
+                off = 64 * (j & 1) + 16 * p + 4 * (L & 3);
+            } else {                           // qh pieces, (h, s) = p >> 1, p & 1
+                const int j = (o - 146) >> 5, L = (o - 146) & 31;
+                row = (L >> 2) + 8 * j;
+                off = 128 + 32 * (p >> 1) + 16 * (p & 1) + 4 * (L & 3);
+            }
+            uint32_t x = 0;
+            if (row >= 0) {
+                const long long r = tile * TR + row;
+                if (r < n) {
+                    const uint16_t* q = reinterpret_cast<const uint16_t*>(w + ((size_t)r * nb + b) * Q6K_BYTES + off);
+                    x = (uint32_t)q[0] | ((uint32_t)q[1] << 16);
+                }
+            } else {
+                for (int e = 0; e < 2; ++e) {
+                    const long long r = tile * TR + 8 * (o - 16) + 2 * p + e;
+                    if (r < n) {
+                        const uint16_t dv = *reinterpret_cast<const uint16_t*>(w + ((size_t)r * nb + b) * Q6K_BYTES + 208);
+                        x |= (uint32_t)dv << (16 * e);
+                    }
+                }
+            }
+            v[p] = x;
+        }
+        reinterpret_cast<uint4*>(out)[u] = make_uint4(v[0], v[1], v[2], v[3]);
+    }
 }
 
-cudaError_t launch_repack_q4K_x16(const uint8_t* w, uint8_t* out, int n, int k, cudaStream_t stream) {
-    const long long units = (long long)q4K_x16_bytes(n, k) / 16;
+}  // namespace x16
+
+size_t x16_bytes(int fmt, long long n, int k) {
+    const int tb = fmt == 6 ? x16::X16<6>::TB : x16::X16<4>::TB;
+    return (size_t)((n + x16::TR - 1) / x16::TR) * (k / QK) * tb;
+}
+
+cudaError_t launch_repack_x16(int fmt, const uint8_t* w, uint8_t* out, int n, int k, cudaStream_t stream) {
+    const long long units = (long long)x16_bytes(fmt, n, k) / 16;
     long long grid = (units + 255) / 256;
     const long long cap = (long long)num_sms() * 8;
     if (grid > cap) grid = cap;
-    return launch_kernel(x16::repack_x16_kernel, dim3((unsigned)grid), dim3(256), 0, stream, w, out, n, k / QK,
+    if (fmt == 6)
+        return launch_kernel(x16::repack_x16_q6K_kernel, dim3((unsigned)grid), dim3(256), 0, stream, w, out, n,
+                             k / QK, units);
+    return launch_kernel(x16::repack_x16_q4K_kernel, dim3((unsigned)grid), dim3(256), 0, stream, w, out, n, k / QK,
                          units);
 }
 
-cudaError_t launch_gemv_q4K_x16(const uint8_t* w, const uint8_t* xq, float* y, int m, int n, int k,
-                                cudaStream_t stream) {
+template <int FMT>
+static cudaError_t gemv_x16(const uint8_t* w, const uint8_t* xq, float* y, int m, int n, int k, cudaStream_t stream) {
     x16::Args A;
     A.w = w;
     A.xq = xq;
@@ -426,13 +586,21 @@ cudaError_t launch_gemv_q4K_x16(const uint8_t* w, const uint8_t* xq, float* y, i
     A.kmhi = 0x00F000F0u;
     A.kmagic = 0x64006400u;
     A.k2p24 = 1u << 24;
-    cudaError_t e = cudaFuncSetAttribute(x16::gemv_x16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         x16::SMEM);
+    A.km1056 = 0xE420E420u;
+    A.k0f = 0x0F0F0F0Fu;
+    A.k30 = 0x30303030u;
+    constexpr int SMEM = x16::smem_bytes<FMT>();
+    cudaError_t e = cudaFuncSetAttribute(x16::gemv_x16_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
     if (e != cudaSuccess) return e;
     int grid = num_sms();
     if (grid > A.ntiles) grid = A.ntiles;
-    return launch_kernel(x16::gemv_x16_kernel, dim3((unsigned)grid), dim3(x16::THREADS), (size_t)x16::SMEM,
-                         stream, A);
+    return launch_kernel(x16::gemv_x16_kernel<FMT>, dim3((unsigned)grid), dim3(x16::THREADS), (size_t)SMEM, stream,
+                         A);
+}
+
+cudaError_t launch_gemv_x16(int fmt, const uint8_t* w, const uint8_t* xq, float* y, int m, int n, int k,
+                            cudaStream_t stream) {
+    return fmt == 6 ? gemv_x16<6>(w, xq, y, m, n, k, stream) : gemv_x16<4>(w, xq, y, m, n, k, stream);
 }
 
 }  // namespace plm

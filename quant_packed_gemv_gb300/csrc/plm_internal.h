@@ -96,12 +96,12 @@ bool gemm_noalloc_fits(long long m, int k);
 cudaError_t launch_gemm_q4K_noalloc(const uint8_t* w, const uint8_t* xq, float* y, long long m, int n, int k,
                                     cudaStream_t stream);
 
-// Row-interleaved q4_K layout "x16" (tiles of 16 rows per 256-weight block):
+// Row-interleaved q4_K / q6_K layouts "x16" (tiles of 16 rows per 256-weight block):
 // bytes of the repacked matrix, the repack, and the tensor-core decode GEMV
 // over it (1 <= m <= 8).
-size_t q4K_x16_bytes(long long n, int k);
-cudaError_t launch_repack_q4K_x16(const uint8_t* w, uint8_t* out, int n, int k, cudaStream_t stream);
-cudaError_t launch_gemv_q4K_x16(const uint8_t* w, const uint8_t* xq, float* y, int m, int n, int k,
-                                cudaStream_t stream);
+size_t x16_bytes(int fmt, long long n, int k);   // fmt 4 (q4_K) or 6 (q6_K)
+cudaError_t launch_repack_x16(int fmt, const uint8_t* w, uint8_t* out, int n, int k, cudaStream_t stream);
+cudaError_t launch_gemv_x16(int fmt, const uint8_t* w, const uint8_t* xq, float* y, int m, int n, int k,
+                            cudaStream_t stream);
 
 }  // namespace plm

@@ -85,10 +85,11 @@ def load(build_if_missing=True):
     lib.plm_probe_mma_rates.restype = ctypes.c_int
     lib.plm_selftest_bounded_wait.argtypes = [ctypes.c_uint32, ctypes.c_int, vp]
     lib.plm_selftest_bounded_wait.restype = ctypes.c_int
-    lib.plm_q4K_x16_size.argtypes = [i64, i64]
-    lib.plm_q4K_x16_size.restype = ctypes.c_size_t
-    lib.plm_q4K_to_x16.argtypes = [vp, vp, i64, i64, vp]
-    lib.plm_q4K_to_x16.restype = ctypes.c_int
+    for f in ("q4K", "q6K"):
+        getattr(lib, "plm_%s_x16_size" % f).argtypes = [i64, i64]
+        getattr(lib, "plm_%s_x16_size" % f).restype = ctypes.c_size_t
+        getattr(lib, "plm_%s_to_x16" % f).argtypes = [vp, vp, i64, i64, vp]
+        getattr(lib, "plm_%s_to_x16" % f).restype = ctypes.c_int
     lib.plm_quantize_q8K.argtypes = [vp, vp, i64, i64, vp]
     lib.plm_quantize_q8K.restype = ctypes.c_int
     lib.plm_gemm_workspace_size.argtypes = [ctypes.c_int, i64, i64]
@@ -120,7 +121,7 @@ def load(build_if_missing=True):
                  "plm_subdots_q4K", "plm_subdots_q6K", "plm_quantize_gemv_q4K",
                  "plm_gemv_q5K", "plm_gemm_q5K", "plm_subdots_q5K",
                  "plm_gemv_q2K", "plm_gemm_q2K", "plm_subdots_q2K", "plm_gemv_q3K", "plm_gemm_q3K", "plm_subdots_q3K",
-                 "plm_gemv_q4K_x16"):
+                 "plm_gemv_q4K_x16", "plm_gemv_q6K_x16"):
         fn = getattr(lib, name)
         fn.argtypes = [vp, vp, vp, i64, i64, i64, vp]
         fn.restype = ctypes.c_int
@@ -230,6 +231,7 @@ plm_subdots_q6K = _mm("plm_subdots_q6K")
 
 
 plm_gemv_q4K_x16 = _mm("plm_gemv_q4K_x16")
+plm_gemv_q6K_x16 = _mm("plm_gemv_q6K_x16")
 
 
 def plm_q4K_x16_size(n, k):
@@ -237,10 +239,21 @@ def plm_q4K_x16_size(n, k):
     return load().plm_q4K_x16_size(n, k)
 
 
+def plm_q6K_x16_size(n, k):
+    """Bytes of the row-interleaved x16 form of an n x k q6_K matrix (0: invalid)."""
+    return load().plm_q6K_x16_size(n, k)
+
+
 def plm_q4K_to_x16(w, w_x16, n, k, stream=None):
     """Repacks q4_K weights into the x16 layout (see include/plm.h)."""
     lib = load()
     _check("plm_q4K_to_x16", lib.plm_q4K_to_x16(_addr(w), _addr(w_x16), n, k, _stream(stream)))
+
+
+def plm_q6K_to_x16(w, w_x16, n, k, stream=None):
+    """Repacks q6_K weights into the x16 layout (see include/plm.h)."""
+    lib = load()
+    _check("plm_q6K_to_x16", lib.plm_q6K_to_x16(_addr(w), _addr(w_x16), n, k, _stream(stream)))
 
 
 def _grouped(name):

@@ -166,3 +166,40 @@ def pack_q4K_x16(w, n, k):
                     off = 256 + 512 * j + 16 * L
                     tb[off:off + 16] = src[row, b, q0:q0 + 16]
     return out.reshape(-1)
+
+
+def pack_q6K_x16(w, n, k):
+    """The x16 form of q6_K weights w [n][k/256 * 210], built from the layout
+    text in the packing direction: per tile T and block b, 3360 bytes: the 16
+    rows' int8 scales (16 bytes each), their f16 d (2 bytes each), then for
+    j = 0..3 and L = 0..31 the 16 bytes ql[64(j%2) + 16w + 4(L%4) ..+4] for
+    w = 0..3 of row L//4 (+8 when j >= 2), then for j = 0..1 the 16 bytes
+    qh[32h + 16s + 4(L%4) ..+4] for (h, s) = (0,0), (0,1), (1,0), (1,1) of row
+    L//4 + 8j."""
+    nb = k // 256
+    ntiles = -(-n // 16)
+    src = np.zeros((ntiles * 16, nb, 210), dtype=np.uint8)
+    src[:n] = np.asarray(w, dtype=np.uint8).reshape(n, nb, 210)
+    out = np.zeros((ntiles, nb, 3360), dtype=np.uint8)
+    for T in range(ntiles):
+        for b in range(nb):
+            tb = out[T, b]
+            blk = src[16 * T:16 * T + 16, b]
+            for i in range(16):
+                tb[16 * i:16 * i + 16] = blk[i, 192:208]
+                tb[256 + 2 * i:258 + 2 * i] = blk[i, 208:210]
+            for j in range(4):
+                for L in range(32):
+                    row = L // 4 + (8 if j >= 2 else 0)
+                    base = 288 + 512 * j + 16 * L
+                    for w4 in range(4):
+                        q = 64 * (j % 2) + 16 * w4 + 4 * (L % 4)
+                        tb[base + 4 * w4:base + 4 * w4 + 4] = blk[row, q:q + 4]
+            for j in range(2):
+                for L in range(32):
+                    row = L // 4 + 8 * j
+                    base = 2336 + 512 * j + 16 * L
+                    for p, (h, s) in enumerate([(0, 0), (0, 1), (1, 0), (1, 1)]):
+                        q = 128 + 32 * h + 16 * s + 4 * (L % 4)
+                        tb[base + 4 * p:base + 4 * p + 4] = blk[row, q:q + 4]
+    return out.reshape(-1)

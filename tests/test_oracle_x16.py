@@ -10,7 +10,7 @@ import pytest
 
 import gen
 import oracle
-from tests.packers import pack_q4K_x16
+from tests.packers import pack_q4K_x16, pack_q6K_x16
 
 
 @pytest.mark.parametrize("n,k", [(1, 256), (16, 512), (37, 1024), (130, 768)])
@@ -53,3 +53,32 @@ def test_x16_padding_rows_are_zero_blocks():
     for b in range(2):
         hdr = wx[1, b, :256].reshape(16, 16)
         assert (hdr[5:] == 0).all() and (hdr[:5] != 0).any()
+
+
+@pytest.mark.parametrize("n,k", [(1, 256), (16, 512), (37, 1024), (130, 768)])
+def test_q6K_x16_round_trip_equals_plain_decode(n, k):
+    w = gen.q6K_blocks(72, n, n, k)
+    wx = pack_q6K_x16(w, n, k)
+    assert wx.size == -(-n // 16) * (k // 256) * 3360
+    np.testing.assert_array_equal(oracle.dequant_q6K_x16(wx, n, k), oracle.dequant_q6K(w, n, k))
+
+
+def test_q6K_x16_every_code_bit_lands_once():
+    # a block of q6 = 32 (weight 0) with scale 1; set one code bit at a time
+    # (each ql nibble bit and each qh bit): exactly one weight moves, by the
+    # bit's value, at the position the q6_K format gives it
+    from tests.packers import pack_q6K
+    n, k = 16, 256
+    base = np.full(256, 32)
+    for r in (0, 9):
+        for wgt in range(0, 256, 7):
+            for bit in range(6):
+                q = base.copy()
+                q[wgt] ^= 1 << bit
+                blk = pack_q6K(1.0, [1] * 16, q)
+                w = np.tile(pack_q6K(1.0, [1] * 16, base), (n, 1))
+                w[r] = blk
+                deq = oracle.dequant_q6K_x16(pack_q6K_x16(w, n, k), n, k)
+                nz = np.argwhere(deq != 0)
+                assert len(nz) == 1 and tuple(nz[0]) == (r, wgt)
+                assert deq[r, wgt] == q[wgt] - 32
