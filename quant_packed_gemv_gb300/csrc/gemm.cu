@@ -22,7 +22,9 @@
 // 16*D_hi + D_lo in the epilogue.
 //
 // Tile: 128 weight rows (MMA M, TMEM lanes) x 128 activation rows (MMA N,
-// TMEM columns).  Roles per CTA (q4_K / q5_K: 13 warps; q6_K: 9 warps):
+// TMEM columns).  q4_K and q5_K run gemm_tm_kernel (below): the decoded A
+// operand goes to tensor memory instead of shared memory.  The description
+// that follows is gemm_kernel, the q6_K path.  Roles per CTA (9 warps):
 //   producer warpgroups (q4_K / q5_K: warps 0-7, two warpgroups; q6_K:
 //     warps 0-3, one): thread t of warpgroup h decodes weight row t of the
 //     tile into the A operand (f16, 128-byte swizzled K-major, one 64-wide
@@ -283,6 +285,45 @@ __device__ __forceinline__ void q5K_row_stage(const Q5KRow& R, int c, uint8_t* t
         }
         *reinterpret_cast<uint4*>(tile + sw128_chunk(row, ch)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         *reinterpret_cast<uint4*>(tile + sw128_chunk(row, ch + 4)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    }
+}
+
+// The same stage decoded into the 32 tensor-memory columns of row `row` of
+// the A operand (column i holds K positions 2i, 2i + 1 as an f16 pair; low
+// nibbles are columns 4ch .. 4ch + 3, high nibbles 16 + 4ch ..).
+template <int FMT, int NRAW>
+__device__ __forceinline__ void qxK_row_stage_regs(const QxKRow<NRAW>& R, int c, uint32_t (&v)[32]) {
+    constexpr int QW = FMT == 5 ? 3 : 1;   // first qs word of the block (q5_K: after qh[32])
+    const uint4 qa = R.raw[QW + 2 * c], qb = R.raw[QW + 1 + 2 * c];
+    const uint32_t q[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+    uint32_t qh[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    if constexpr (FMT == 5) {
+        qh[0] = R.raw[1].x; qh[1] = R.raw[1].y; qh[2] = R.raw[1].z; qh[3] = R.raw[1].w;
+        qh[4] = R.raw[2].x; qh[5] = R.raw[2].y; qh[6] = R.raw[2].z; qh[7] = R.raw[2].w;
+    }
+    const __half2 slo = bits_h2(R.sc_lo2[c]), olo = bits_h2(R.off_lo2[c]);
+    const __half2 shi = bits_h2(R.sc_hi2[c]), ohi = bits_h2(R.off_hi2[c]);
+#pragma unroll
+    for (int ch = 0; ch < 4; ++ch) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint32_t w = q[2 * ch + h];
+            const uint32_t x01 = __byte_perm(w, 0, 0x4140), x23 = __byte_perm(w, 0, 0x4342);
+            uint32_t l01 = x01 & 0x000F000Fu, l23 = x23 & 0x000F000Fu;
+            uint32_t u01 = x01 & 0x00F000F0u, u23 = x23 & 0x00F000F0u;
+            if constexpr (FMT == 5) {
+                const uint32_t b = qh[2 * ch + h];
+                const uint32_t h01 = __byte_perm(b, 0, 0x4140), h23 = __byte_perm(b, 0, 0x4342);
+                l01 |= ((h01 >> (2 * c)) & 0x00010001u) << 4;
+                l23 |= ((h23 >> (2 * c)) & 0x00010001u) << 4;
+                u01 |= ((h01 >> (2 * c + 1)) & 0x00010001u) << 8;
+                u23 |= ((h23 >> (2 * c + 1)) & 0x00010001u) << 8;
+            }
+            v[4 * ch + 2 * h] = h2_bits(__hfma2(bits_h2(l01 | 0x64006400u), slo, olo));
+            v[4 * ch + 2 * h + 1] = h2_bits(__hfma2(bits_h2(l23 | 0x64006400u), slo, olo));
+            v[16 + 4 * ch + 2 * h] = h2_bits(__hfma2(bits_h2(u01 | 0x64006400u), shi, ohi));
+            v[16 + 4 * ch + 2 * h + 1] = h2_bits(__hfma2(bits_h2(u23 | 0x64006400u), shi, ohi));
+        }
     }
 }
 
@@ -707,6 +748,321 @@ __global__ void __launch_bounds__(GemmRoles<GemmCfg<FMT>::PWG>::THREADS, 1) gemm
     }
 }
 
+// ---------------------------------------------------------------------------
+// q4_K / q5_K with the A operand in tensor memory.  The producers decode each
+// 64-wide K stage of their weight row straight into a ring of four 32-column
+// tensor-memory stages (tcgen05.st), and the MMA reads A from there
+// (tcgen05.mma [d], [a], b-desc): shared memory carries only the activation
+// tiles (TMA) and the per-block min operands, half the traffic of an A tile
+// in shared memory.  Tensor memory (512 columns): D1 (isum) double-buffered
+// at columns 0 and 128, D2 (msum) single-buffered at 256, the A ring at
+// 384 + 32 s.  The epilogue takes D2 of a block first and releases it before
+// D1, so the next block's min MMA (its last) rarely waits.  Roles: warps 0-7
+// producers (two warpgroups, stages 2h, 2h + 1 of every block), warps 8-15
+// epilogue (warp e: TMEM lanes 32 (e % 4) .., activation columns 64 (e / 4)
+// .. + 63), warp 16 issues the MMAs.  No register hand-over: 17 warps at 96.
+// ---------------------------------------------------------------------------
+constexpr int TM_EPI_WARP0 = 8, TM_MMA_WARP = 16, TM_THREADS = 17 * 32, TM_NSTAGE = 4;
+constexpr uint32_t TM_D1 = 0, TM_D2 = 256, TM_A = 384;
+
+template <int FMT>
+struct TmSmem {
+    static constexpr int RING = 0;                                            // B tiles, 4 x 16 KB
+    static constexpr int MIN = RING + TM_NSTAGE * TILE_BYTES;                 // 2 x 16 KB
+    static constexpr int SCL = MIN + 2 * TILE_BYTES;                          // 2 x (d, dmin, dx) x 128 f32
+    static constexpr int WT = GT * GemmCfg<FMT>::WROW;
+    static constexpr int BTX = WT + GT * AUXB;
+    static constexpr int BSLOT = (BTX + 1023) & ~1023;
+    static constexpr int BRING = (SCL + 2 * 3 * GT * 4 + 1023) & ~1023;
+    static constexpr int BAR = BRING + 2 * BSLOT;
+    static constexpr int NBAR = 2 * TM_NSTAGE + 8 + 4 + 1;
+    static constexpr int TMEMP = BAR + NBAR * 8;
+    static constexpr int BYTES = TMEMP + 16;
+    static constexpr int ALLOC = BYTES + 1024;
+};
+
+__device__ __forceinline__ void mma_f16_ta(uint32_t dtmem, uint32_t atmem, uint64_t db, uint32_t accumulate) {
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+                 :: "r"(dtmem), "r"(atmem), "l"(db), "r"(IDESC_F16_128x128), "r"(accumulate));
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+                 "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+                 :: "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
+                    "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+                    "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+                    "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+                    "r"(r[29]), "r"(r[30]), "r"(r[31]) : "memory");
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(TM_THREADS, 1) gemm_tm_kernel(const __grid_constant__ CUtensorMap xmap,
+                                                                const __grid_constant__ CUtensorMap wmap,
+                                                                const __grid_constant__ CUtensorMap amap,
+                                                                const GemmArgs A) {
+    using L = TmSmem<FMT>;
+    constexpr int NSTAGE = TM_NSTAGE;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BAR);
+    uint64_t* full = bars;                  // [4]: 4 producer-warp arrivals + the B tile's TMA bytes
+    uint64_t* empty = bars + NSTAGE;        // [4]: MMA commit (frees the TMEM A stage and the B tile)
+    uint64_t* minfull = bars + 2 * NSTAGE;  // [2]: 8 producer-warp arrivals (min operands, scales)
+    uint64_t* minempty = minfull + 2;       // [2]: MMA commit
+    uint64_t* tfull = minfull + 4;          // [2]: MMA commit
+    uint64_t* tempty = minfull + 6;         // [2]: 8 epilogue-warp arrivals
+    uint64_t* bfull = minfull + 8;          // [2]: TMA bytes of a weight block and its side data
+    uint64_t* bempty = bfull + 2;           // [2]: 8 producer-warp arrivals
+    uint64_t* d2free = bempty + 2;          // [1]: 8 epilogue-warp arrivals once D2 is read
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::TMEMP);
+    float* scl = reinterpret_cast<float*>(sm + L::SCL);   // [2][3][128]: d, dmin, dx
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // this CTA's tile: weight rows from r0, activation rows from i0, K blocks [kb0, kb0 + kcount)
+    const int r0 = blockIdx.x * GT, i0 = blockIdx.y * GT;
+    const int nb = A.nb;
+    const int kb0 = blockIdx.z * A.bsplit;
+    const int kcount = min(A.bsplit, nb - kb0);
+
+    if (tid == 0) {
+        for (int s = 0; s < NSTAGE; ++s) {
+            mbar_init(&full[s], 4);
+            mbar_init(&empty[s], 1);
+        }
+        for (int j = 0; j < 2; ++j) {
+            mbar_init(&minfull[j], 8);
+            mbar_init(&minempty[j], 1);
+            mbar_init(&tfull[j], 1);
+            mbar_init(&tempty[j], 8);
+            mbar_init(&bfull[j], 1);
+            mbar_init(&bempty[j], 8);
+        }
+        mbar_init(d2free, 8);
+        fence_barrier_init();
+    }
+    if (warp == TM_MMA_WARP) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;"
+                     :: "r"(smem_u32(tmem_slot)) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    grid_launch_dependents();
+    grid_wait_prior();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    bool ok = true;
+
+    if (warp < TM_EPI_WARP0) {
+        // ------------------------------------------------------- producers
+        const int t = tid & (GT - 1);          // weight row (and activation row) of the tile
+        const int half = warp >> 2;            // stages 2 half, 2 half + 1 of every block
+        const uint32_t alane = (uint32_t)((warp & 3) * 32) << 16;
+        using Row = typename std::conditional<FMT == 5, Q5KRow, Q4KRow>::type;
+        Row R;
+        int nissued = 0;
+        auto issue_block = [&](int bb) {   // thread 0: block bb of the tile into slot bb % 2
+            ++nissued;
+            const int s = bb & 1;
+            uint8_t* dst = sm + L::BRING + s * L::BSLOT;
+            mbar_arrive_expect_tx(&bfull[s], (uint32_t)L::BTX);
+            tma_load_2d(dst, &wmap, (kb0 + bb) * GemmCfg<FMT>::WROW, r0, &bfull[s]);
+            tma_load_2d(dst + L::WT, &amap, (kb0 + bb) * AUXB, i0, &bfull[s]);
+        };
+        if (tid == 0)
+            for (int bb = 0; bb < 2 && bb < kcount; ++bb) issue_block(bb);
+        int gb = 0;   // block of the tile: slots and phases
+        {
+            for (int b = 0; b < kcount && ok; ++b, ++gb) {
+                const int j = gb & 1;
+                uint32_t bsw[8];
+                float dx;
+                {
+                    const int s = gb & 1;
+                    if (!mbar_wait(&bfull[s], (uint32_t)(gb >> 1) & 1u)) { ok = false; break; }
+                    const uint8_t* slot = sm + L::BRING + s * L::BSLOT;
+                    constexpr int NRAW = GemmCfg<FMT>::WROW / 16;
+#pragma unroll
+                    for (int u = 0; u < NRAW; ++u)
+                        R.raw[u] = reinterpret_cast<const uint4*>(slot + t * GemmCfg<FMT>::WROW)[u];
+                    const uint4* ax = reinterpret_cast<const uint4*>(slot + L::WT + t * AUXB);
+                    const uint4 a0 = ax[0], a1 = ax[1], a2 = ax[2];
+                    bsw[0] = a0.x; bsw[1] = a0.y; bsw[2] = a0.z; bsw[3] = a0.w;
+                    bsw[4] = a1.x; bsw[5] = a1.y; bsw[6] = a1.z; bsw[7] = a1.w;
+                    dx = __uint_as_float(a2.x);
+                    fence_async_smem();   // these reads before the slot's refill by TMA
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bempty[s]);
+                }
+                q4K_row_prepare(R);
+                if (gb >= 2) {   // slot j's min operands and scales are free again
+                    ok = mbar_wait(&minempty[j], ((gb >> 1) - 1) & 1) && mbar_wait(&tempty[j], ((gb >> 1) - 1) & 1);
+                    if (!ok) break;
+                }
+                if (half == 1) {
+                    // min operands: K 0..15 the weight row's mins m_(g/2); K 16..31 the activation row's bsums
+                    uint8_t* mt = sm + L::MIN + j * TILE_BYTES;
+                    uint32_t mv[8];
+#pragma unroll
+                    for (int g = 0; g < 8; ++g) {
+                        const uint32_t mm = (uint32_t)R.mins[g];
+                        mv[g] = h2_bits(__hsub2(bits_h2(0x64006400u | mm | (mm << 16)), bits_h2(0x64006400u)));
+                    }
+                    *reinterpret_cast<uint4*>(mt + sw128_chunk(t, 0)) = make_uint4(mv[0], mv[1], mv[2], mv[3]);
+                    *reinterpret_cast<uint4*>(mt + sw128_chunk(t, 1)) = make_uint4(mv[4], mv[5], mv[6], mv[7]);
+                    *reinterpret_cast<uint4*>(mt + sw128_chunk(t, 2)) = make_uint4(bsw[0], bsw[1], bsw[2], bsw[3]);
+                    *reinterpret_cast<uint4*>(mt + sw128_chunk(t, 3)) = make_uint4(bsw[4], bsw[5], bsw[6], bsw[7]);
+                } else {
+                    float* sj = scl + j * 3 * GT;
+                    sj[t] = R.d;
+                    sj[GT + t] = R.dmin;
+                    sj[2 * GT + t] = dx;
+                }
+                // the block's two stages of this warpgroup: A into tensor memory, B by
+                // TMA (c a compile-time constant, so R's fields stay in registers)
+                auto stage = [&](auto cc_) -> bool {
+                    constexpr int c = decltype(cc_)::value;   // stage, and its ring slot (one block long)
+                    if (gb >= 1) {
+                        if (!mbar_wait(&empty[c], (uint32_t)(gb - 1) & 1u)) return false;
+                        tc_fence_after();
+                    }
+                    if (t == 0) {
+                        mbar_expect_tx(&full[c], TILE_BYTES);
+                        tma_load_2d(sm + L::RING + c * TILE_BYTES, &xmap, (kb0 + b) * QK + c * KS, i0, &full[c]);
+                    }
+                    uint32_t v[32];
+                    qxK_row_stage_regs<FMT>(R, c, v);
+                    tmem_st32(tmem + alane + TM_A + 32 * c, v);
+                    return true;
+                };
+                using C0 = std::integral_constant<int, 0>;
+                using C1 = std::integral_constant<int, 1>;
+                using C2 = std::integral_constant<int, 2>;
+                using C3 = std::integral_constant<int, 3>;
+                ok = half == 0 ? (stage(C0{}) && stage(C1{})) : (stage(C2{}) && stage(C3{}));
+                if (!ok) break;
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                tc_fence_before();
+                fence_async_smem();   // min operands and scales before the MMA / epilogue read them
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&minfull[j]);
+                    mbar_arrive(&full[2 * half]);
+                    mbar_arrive(&full[2 * half + 1]);
+                }
+                // refill this block's weight slot once every producer warp has read it
+                if (tid == 0 && b + 2 < kcount) {
+                    if (!mbar_wait(&bempty[gb & 1], (uint32_t)(gb >> 1) & 1u)) { ok = false; break; }
+                    issue_block(b + 2);
+                }
+            }
+        }
+        // after a wait ran out: let this CTA's weight copies still in flight land before it exits
+        if (!ok && tid == 0)
+            for (int bb = gb; bb < nissued; ++bb) (void)mbar_wait(&bfull[bb & 1], (uint32_t)(bb >> 1) & 1u);
+    } else if (warp == TM_MMA_WARP) {
+        // ------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            int gb = 0;
+            {
+                for (int b = 0; b < kcount && ok; ++b, ++gb) {
+                    const int j = gb & 1;
+                    const uint32_t d1 = tmem + TM_D1 + 128 * j;
+                    if (gb >= 2 && !mbar_wait(&tempty[j], ((gb >> 1) - 1) & 1)) { ok = false; break; }
+                    tc_fence_after();
+                    for (int c = 0; c < 4 && ok; ++c) {
+                        if (!mbar_wait(&full[c], (uint32_t)gb & 1u)) { ok = false; break; }
+                        tc_fence_after();
+                        const uint64_t db = umma_desc_sw128(smem_u32(sm + L::RING + c * TILE_BYTES));
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)    // K = 16 per MMA: 8 TMEM columns, +2 descriptor units
+                            mma_f16_ta(d1, tmem + TM_A + 32 * c + 8 * kk, db + 2 * kk, (c | kk) != 0);
+                        mma_commit(&empty[c]);
+                    }
+                    if (!ok) break;
+                    if (!mbar_wait(&minfull[j], (gb >> 1) & 1)) { ok = false; break; }
+                    if (gb >= 1 && !mbar_wait(d2free, (uint32_t)(gb - 1) & 1u)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t ma = smem_u32(sm + L::MIN + j * TILE_BYTES);
+                    mma_f16(tmem + TM_D2, umma_desc_sw128(ma), umma_desc_sw128(ma) + 2, 0u);
+                    mma_commit(&minempty[j]);
+                    mma_commit(&tfull[j]);
+                }
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------- epilogue
+        const int e = warp - TM_EPI_WARP0;
+        const int q = e & 3, chalf = e >> 2;     // TMEM lane quarter, activation-column half
+        const int row = 32 * q + lane;           // weight row of the tile
+        const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16);
+        int gb = 0;
+        {
+            float acc[64];
+#pragma unroll
+            for (int c = 0; c < 64; ++c) acc[c] = 0.0f;
+            for (int b = 0; b < kcount && ok; ++b, ++gb) {
+                const int j = gb & 1;
+                if (!mbar_wait(&tfull[j], (gb >> 1) & 1) || !mbar_wait(&minfull[j], (gb >> 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const float* sj = scl + j * 3 * GT;
+                const float dw = sj[row], dmw = sj[GT + row];
+                const float* dxv = sj + 2 * GT + 64 * chalf;
+                // D2 first (- dmin * dx * msum), then release it for the next block's min MMA
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    uint32_t v[16];
+                    tmem_ld16(tl + TM_D2 + 64 * chalf + 16 * cc, v);
+                    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+                    for (int c = 0; c < 16; ++c)
+                        acc[16 * cc + c] = __fmaf_rn(-__fmul_rn(dmw, dxv[16 * cc + c]), __uint_as_float(v[c]),
+                                                     acc[16 * cc + c]);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(d2free);
+                // D1: + d * dx * isum
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    uint32_t v[16];
+                    tmem_ld16(tl + TM_D1 + 128 * j + 64 * chalf + 16 * cc, v);
+                    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+                    for (int c = 0; c < 16; ++c)
+                        acc[16 * cc + c] = __fmaf_rn(__fmul_rn(dw, dxv[16 * cc + c]), __uint_as_float(v[c]),
+                                                     acc[16 * cc + c]);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tempty[j]);
+            }
+            const int r = r0 + row;
+            float* out = A.part ? A.part + (size_t)blockIdx.z * A.m * A.n : A.y;
+            if (ok && r < A.n) {
+#pragma unroll
+                for (int c = 0; c < 64; ++c) {
+                    const int i = i0 + 64 * chalf + c;
+                    if (i < A.m) out[(size_t)i * A.n + r] = acc[c];
+                }
+            }
+        }
+    }
+    if (!ok && lane == 0) atomicOr(A.fault, 2u);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == TM_MMA_WARP) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" :: "r"(tmem) : "memory");
+    }
+}
+
 // q8_K codes -> f16 activation matrix [m][k] (the GEMM's B operand source),
 // and per block the side data the producers take by TMA: the bsums as f16
 // pairs, d and three zero words (AUXB bytes)
@@ -874,19 +1230,20 @@ static cudaError_t gemm_tc_ws(const uint8_t* w, const uint8_t* xq, float* y, lon
     A.part = part;
     A.bsplit = (nb + splits - 1) / splits;
     splits = (nb + A.bsplit - 1) / A.bsplit;   // no empty split
-    constexpr int SMEM = GemmSmem<FMT>::ALLOC;
-    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
-    if (e != cudaSuccess) return e;
     const dim3 grid((unsigned)((n + GT - 1) / GT), (unsigned)((m + GT - 1) / GT), (unsigned)splits);
-    constexpr int THREADS = GemmRoles<GemmCfg<FMT>::PWG>::THREADS;
-    if constexpr (GemmCfg<FMT>::PWG == 2) {
-        // the register hand-over inside the kernel assumes exactly REG_LAUNCH at launch
-        cudaFuncAttributes fa;
-        e = cudaFuncGetAttributes(&fa, gemm_kernel<FMT>);
+    cudaError_t e;
+    if constexpr (FMT == 4 || FMT == 5) {
+        constexpr int SMEM = TmSmem<FMT>::ALLOC;
+        e = cudaFuncSetAttribute(gemm_tm_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
         if (e != cudaSuccess) return e;
-        if (fa.numRegs != REG_LAUNCH) return cudaErrorInvalidConfiguration;
+        e = launch_kernel(gemm_tm_kernel<FMT>, grid, dim3(TM_THREADS), SMEM, stream, map, wmap, amap, A);
+    } else {
+        constexpr int SMEM = GemmSmem<FMT>::ALLOC;
+        e = cudaFuncSetAttribute(gemm_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+        if (e != cudaSuccess) return e;
+        constexpr int THREADS = GemmRoles<GemmCfg<FMT>::PWG>::THREADS;
+        e = launch_kernel(gemm_kernel<FMT>, grid, dim3(THREADS), SMEM, stream, map, wmap, amap, A);
     }
-    e = launch_kernel(gemm_kernel<FMT>, grid, dim3(THREADS), SMEM, stream, map, wmap, amap, A);
     if (e != cudaSuccess || splits == 1) return e;
     const long long count = m * (long long)n;
     long long blocks = (count + 255) / 256;
