@@ -445,7 +445,9 @@ __global__ void __launch_bounds__(GemmRoles<GemmCfg<FMT>::PWG>::THREADS, 1) gemm
     float* scl = reinterpret_cast<float*>(sm + L::SCL);   // [2][3][128]: d, dmin, dx
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int r0 = blockIdx.x * GT, i0 = blockIdx.y * GT;
+    // x: activation tile, y: weight tile, so the CTAs that share a weight tile
+    // run next to each other and its re-reads come from L2
+    const int r0 = blockIdx.y * GT, i0 = blockIdx.x * GT;
     const int nb = A.nb;
     // this CTA's share of K: blocks [kb0, kb0 + kcount); loop indices below count from kb0
     const int kb0 = blockIdx.z * A.bsplit;
@@ -821,7 +823,9 @@ __global__ void __launch_bounds__(TM_THREADS, 1) gemm_tm_kernel(const __grid_con
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // this CTA's tile: weight rows from r0, activation rows from i0, K blocks [kb0, kb0 + kcount)
-    const int r0 = blockIdx.x * GT, i0 = blockIdx.y * GT;
+    // x: activation tile, y: weight tile, so the CTAs that share a weight tile
+    // run next to each other and its re-reads come from L2
+    const int r0 = blockIdx.y * GT, i0 = blockIdx.x * GT;
     const int nb = A.nb;
     const int kb0 = blockIdx.z * A.bsplit;
     const int kcount = min(A.bsplit, nb - kb0);
@@ -1230,7 +1234,7 @@ static cudaError_t gemm_tc_ws(const uint8_t* w, const uint8_t* xq, float* y, lon
     A.part = part;
     A.bsplit = (nb + splits - 1) / splits;
     splits = (nb + A.bsplit - 1) / A.bsplit;   // no empty split
-    const dim3 grid((unsigned)((n + GT - 1) / GT), (unsigned)((m + GT - 1) / GT), (unsigned)splits);
+    const dim3 grid((unsigned)((m + GT - 1) / GT), (unsigned)((n + GT - 1) / GT), (unsigned)splits);
     cudaError_t e;
     if constexpr (FMT == 4 || FMT == 5) {
         constexpr int SMEM = TmSmem<FMT>::ALLOC;
