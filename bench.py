@@ -74,7 +74,8 @@ def parse():
     ap.add_argument("--impl", default="plm", choices=["plm", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--case", nargs=4, metavar=("KIND", "FMT", "N", "K"), default=None,
-                    help="time one entry point alone, e.g. --case gemv q6K 151936 2048")
+                    help="time one entry point alone, e.g. --case gemv q6K 151936 2048 "
+                         "(KIND: gemv, gemv_x16, gemm, gemm_ws)")
     ap.add_argument("--m", type=int, nargs="+", default=[1],
                     help="activation rows for --case (several values: a sweep)")
     ap.add_argument("--no-chain", action="store_true",
@@ -305,7 +306,21 @@ def time_case(args):
             packed.append(wx)
         torch.cuda.synchronize()
         ws = packed
-    fn = getattr(q, "plm_%s_%s" % (kind, fmt)) if kind != "gemv_x16" else getattr(q, "plm_gemv_%s_x16" % fmt)
+    if kind == "gemv_x16":
+        fn = getattr(q, "plm_gemv_%s_x16" % fmt)
+    elif kind == "gemm_ws":
+        # the workspace form with the split-K workspace size
+        fws = getattr(q, "plm_gemm_%s_ws" % fmt)
+        works = {}
+
+        def fn(w, xq, y, m, n, k, stream):
+            if m not in works:
+                need = q.plm_gemm_workspace_size_split(fmt, m, n, k)
+                works[m] = (torch.empty(max(need, 256), dtype=torch.uint8, device="cuda"), need)
+            wk, need = works[m]
+            fws(w, xq, y, m, n, k, wk if need else None, need, stream=stream)
+    else:
+        fn = getattr(q, "plm_%s_%s" % (kind, fmt))
     q.plm_set_overlap(args.overlap)
     stream = torch.cuda.Stream()
     for m in args.m:
@@ -394,16 +409,19 @@ class ShapeTimer:
         xq = torch.empty(m * nb * Q8K_BYTES, dtype=torch.uint8, device="cuda")
         y = torch.empty(m * n, dtype=torch.float32, device="cuda")
         gemv = m <= 8
-        need = 0 if gemv else q.plm_gemm_workspace_size_split(fmt, m, n, k)
+        # GEMM: the workspace form (pre-pass, K split where it pays) or, with
+        # layout "plain", the entry without a workspace (codes widened in the kernel)
+        plain = gemv or layout == "plain"
+        need = 0 if plain else q.plm_gemm_workspace_size_split(fmt, m, n, k)
         work = torch.empty(max(need, 256), dtype=torch.uint8, device="cuda")
-        fn = getattr(q, ("plm_gemv_%s" if gemv else "plm_gemm_%s_ws") % fmt)
+        fn = getattr(q, ("plm_gemv_%s" if gemv else "plm_gemm_%s" if plain else "plm_gemm_%s_ws") % fmt)
         if layout == "x16":
             fn = getattr(q, "plm_gemv_%s_x16" % fmt)
         s = self.stream
 
         def call(i):
             w = ws_list[i % len(ws_list)]
-            if gemv:
+            if plain:
                 fn(w, xq, y, m, n, k, stream=s)
             else:
                 fn(w, xq, y, m, n, k, work, need, stream=s)
@@ -440,22 +458,27 @@ class ShapeTimer:
         return r
 
 
-def time_pair(T, wg_list, wu_list, n, k, m, steps, warmup):
-    """The prefill gate/up pair with SwiGLU (plm_gemm_q4K_swiglu_ws) on one
-    shape, weights rotated as for ShapeTimer, a CUDA graph of `steps` calls."""
+def time_pair(T, wg_list, wu_list, n, k, m, steps, warmup, plain=False):
+    """The prefill gate/up pair with SwiGLU on one shape (plm_gemm_q4K_swiglu_ws,
+    or with plain=True plm_gemm_q4K_swiglu: no workspace, the combine in the up
+    GEMM's epilogue), weights rotated as for ShapeTimer, a CUDA graph of
+    `steps` calls."""
     import gen
     torch, q = T.torch, T.q
     nb = k // QK
     x = torch.from_numpy(gen.normal_f32(8, m, m, k)).cuda()
     xq = torch.empty(m * nb * Q8K_BYTES, dtype=torch.uint8, device="cuda")
     h = torch.empty(m * n, dtype=torch.float32, device="cuda")
-    need = q.plm_gemm_swiglu_workspace_size(m, n, k)
+    need = 0 if plain else q.plm_gemm_swiglu_workspace_size(m, n, k)
     work = torch.empty(max(need, 256), dtype=torch.uint8, device="cuda")
     s = T.stream
 
     def call(i):
-        q.plm_gemm_q4K_swiglu_ws(wg_list[i % len(wg_list)], wu_list[i % len(wu_list)], xq, h, m, n, k,
-                                 work if need else None, need, stream=s)
+        if plain:
+            q.plm_gemm_q4K_swiglu(wg_list[i % len(wg_list)], wu_list[i % len(wu_list)], xq, h, m, n, k, stream=s)
+        else:
+            q.plm_gemm_q4K_swiglu_ws(wg_list[i % len(wg_list)], wu_list[i % len(wu_list)], xq, h, m, n, k,
+                                     work if need else None, need, stream=s)
     with torch.cuda.stream(s):
         q.plm_quantize_q8K(x, xq, m, k, stream=s)
         for i in range(warmup):
@@ -474,7 +497,8 @@ def time_pair(T, wg_list, wu_list, n, k, m, steps, warmup):
         torch.cuda.synchronize()
     us = e0.elapsed_time(e1) * 1e3 / steps
     tops = 4.0 * m * n * k / us / 1e6   # two matrices
-    return {"fmt": "q4K", "n": n, "k": k, "m": m, "us": round(us, 3), "entry": "plm_gemm_q4K_swiglu_ws",
+    return {"fmt": "q4K", "n": n, "k": k, "m": m, "us": round(us, 3),
+            "entry": "plm_gemm_q4K_swiglu" if plain else "plm_gemm_q4K_swiglu_ws",
             "TOPS": round(tops, 1), "frac_f16_dense": round(tops / T.peaks["bf16_tflops"], 4)}
 
 
@@ -501,6 +525,10 @@ def run_extras(torch, q, peaks):
         for m in (1, 2, 4, 8, 64, 512, 2048):
             steps = 10 if m <= 8 else (5 if n * k * m < 3e11 else 2)
             sweep.append(T.run(fmt, ws, wb, n, k, m, steps, 1 if m > 512 else 2))
+        # the GEMM entry without a workspace (activation codes widened in the kernel, no K split)
+        for m in (64, 512, 2048):
+            steps = 5 if n * k * m < 3e11 else 2
+            sweep.append(T.run(fmt, ws, wb, n, k, m, steps, 1 if m > 512 else 2, layout="plain"))
         # the decode GEMV on the row-interleaved layout (tensor-core tile)
         wx = T.x16(fmt, ws, n, k)
         for m in (1, 2, 4, 8):
@@ -512,11 +540,12 @@ def run_extras(torch, q, peaks):
     ws, wb = T.weights("q5K", 5, 12288, 4096)
     out["q5K_12288x4096"] = [T.run("q5K", ws, wb, 12288, 4096, m, 10 if m <= 8 else 3, 2) for m in (1, 8, 512)]
     del ws
-    # the prefill gate/up pair with the SwiGLU epilogue (two GEMMs and one elementwise pass)
+    # the prefill gate/up pair with the SwiGLU epilogue (workspace form: two GEMMs and one
+    # elementwise pass; plain form: the combine in the up GEMM's epilogue)
     wg, _ = T.weights("q4K", 6, 12288, 4096)
     wu, _ = T.weights("q4K", 7, 12288, 4096)
-    out["prefill_swiglu_q4K_12288x4096"] = [time_pair(T, wg, wu, 12288, 4096, m, 5 if m < 2048 else 3, 2)
-                                            for m in (64, 512, 2048)]
+    out["prefill_swiglu_q4K_12288x4096"] = [time_pair(T, wg, wu, 12288, 4096, m, 5 if m < 2048 else 3, 2, plain)
+                                            for plain in (False, True) for m in (64, 512, 2048)]
     del wg, wu
     torch.cuda.empty_cache()
     # the q2_K and q3_K rungs (decode GEMV; their GEMM entry runs the GEMV in 8-row passes)
@@ -545,7 +574,7 @@ def gemm_roofline(configs, peaks, peak_src):
             "tensor_pipe_active_pct": rec.get("tensor_pipe_active_pct") if rec else None,
             "peak_source": "measured bf16 dense (burst); f16, the kind the kernel runs, has the same nominal rate"
                            if peak_src == "measured" else "fallback",
-            "kernel": "gemm_kernel<q4_K> (tcgen05.mma kind::f16 on exact integer-valued operands)",
+            "kernel": "gemm_tm_kernel<q4_K> (tcgen05.mma kind::f16 on exact integer-valued operands, A in tensor memory)",
             "shape": "q4_K 12288x4096, m=2048", "flops_per_call": flops, "avg_call_us": row["us"]}
 
 

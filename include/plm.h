@@ -25,10 +25,8 @@
  *   y  f32  [m][n]       y[i][r] = sum over k of x_hat[i][.] * w_hat[r][.]
  *
  * Ownership and ordering: every pointer is a DEVICE pointer owned by the
- * caller.  The library never synchronizes.  It allocates nothing, except
- * that plm_gemm_q4K / plm_gemm_q6K take their temporary workspace from the
- * device's stream-ordered pool (cudaMallocAsync / cudaFreeAsync on the
- * call's stream); the _ws forms use a workspace the caller passes.  Each call
+ * caller.  The library never synchronizes and allocates nothing; the _ws
+ * forms use a workspace the caller passes.  Each call
  * enqueues its work on `stream` (0 = the legacy default stream) and returns
  * at once; results are visible to later work on that stream.  y is
  * overwritten, never accumulated into.  Calls on different streams that
@@ -313,14 +311,17 @@ plm_status plm_gemv_q4K_swiglu_grouped(const plm_swiglu_problem* problems, int64
 
 /*
  * Prefill GEMM, y = X . W^T for any m >= 1 (intended for m = 512..2048).
- * For m >= 9 the activation codes are first widened to an f16 matrix in a
- * workspace; weight tiles are decoded in shared memory into exact
- * integer-valued f16 operands (q4_K: sc*q; q6_K: sc*(q6-32)) and contracted
- * on the tensor cores (tcgen05, f32 accumulation in tensor memory), one
- * 256-weight block at a time; the per-block scales are applied in f32.
- * For m <= 8 it runs the decode GEMV.  Same buffers, layouts and tolerance
- * as the GEMV; no limit on m.  These two forms take the workspace from the
- * stream-ordered pool of the current device.
+ * For m >= 9, weight tiles are decoded into exact integer-valued f16
+ * operands (q4_K: sc*q; q6_K: sc*(q6-32), split as 16*hi + lo) and
+ * contracted on the tensor cores (tcgen05, f32 accumulation in tensor
+ * memory) against the activation codes as exact f16, one 256-weight block at
+ * a time; the per-block scales are applied in f32.  These plain forms widen
+ * the activation codes inside the GEMM kernel, straight from xq into shared
+ * memory: they need no workspace, allocate nothing and never split K.  For
+ * m <= 8 (and for q2_K / q3_K) they run the decode GEMV eight rows at a time.
+ * Same buffers, layouts and tolerance as the GEMV; no limit on m.  For the
+ * same (m, n, k) a plain call and a _ws call that does not split K give the
+ * same bits.
  */
 plm_status plm_gemm_q4K(const void* w, const void* xq, float* y,
                         int64_t m, int64_t n, int64_t k, cudaStream_t stream);
@@ -332,16 +333,20 @@ plm_status plm_gemm_q6K(const void* w, const void* xq, float* y,
  *   h[i][r] = silu(g[i][r]) * u[i][r],  g = W_gate . x_i,  u = W_up . x_i,
  * the same step as plm_gemv_q4K_swiglu (PocketLLM (Korean README), "Current
  * status" table, row "src/": silu_mul after the ffn gate and up projections)
- * at prefill sizes.  For m >= 9: the q4_K GEMM of the gate matrix into h,
- * that of the up matrix into the workspace, then one elementwise pass
- * h = silu(h) * u (IEEE division, expf) -- g and u are exactly what
- * plm_gemm_q4K_ws gives for each matrix with the same workspace size.  For
- * m <= 8 it runs plm_gemv_q4K_swiglu eight rows at a time.
+ * at prefill sizes, h = silu(g) * u = g / (1 + e^-g) * u (IEEE division,
+ * expf).  For m >= 9 the plain form runs the q4_K GEMM of the gate matrix
+ * into h, then that of the up matrix, whose epilogue reads each element's g
+ * back from h and writes silu(g) * u over it: no workspace, nothing
+ * allocated.  The _ws form runs the two GEMMs (the up matrix's into the
+ * workspace, K split when the workspace allows) and one elementwise pass;
+ * without a K split both forms give the same bits.  For m <= 8 both run
+ * plm_gemv_q4K_swiglu eight rows at a time.
  *   w_gate, w_up  q4_K [n][k/256] each, 16-byte aligned; xq q8_K [m][k/256];
- *   h f32 [m][n], not overlapping the inputs.  The plain form takes its
- *   workspace from the stream-ordered pool; the _ws form takes the caller's:
- *   plm_gemm_swiglu_workspace_size(m, n, k) bytes, 256-byte aligned (null
- *   allowed when that is 0).  Errors as for plm_gemm_q4K / plm_gemm_q4K_ws.
+ *   h f32 [m][n], not overlapping the inputs.  The _ws form's workspace:
+ *   plm_gemm_swiglu_workspace_size(m, n, k) bytes (K split where it pays)
+ *   or at least m*n*4 rounded up to 256 plus plm_gemm_workspace_size(4, m, k)
+ *   (unsplit), 256-byte aligned (null allowed when the size is 0).  Errors as
+ *   for plm_gemm_q4K / plm_gemm_q4K_ws.
  */
 plm_status plm_gemm_q4K_swiglu(const void* w_gate, const void* w_up, const void* xq, float* h, int64_t m,
                                int64_t n, int64_t k, cudaStream_t stream);
@@ -372,20 +377,24 @@ size_t plm_gemm_workspace_size_split(int fmt, int64_t m, int64_t n, int64_t k);
 
 /* The GEMM with a caller-owned device workspace of at least
  * plm_gemm_workspace_size bytes, 256-byte aligned (may be null when that
- * size is 0).  The workspace must not be used by other work until the call's
- * kernels have finished on `stream`.  PLM_ERR_INVALID_ARG if it is too
- * small. */
+ * size is 0).  A pre-pass widens the activation codes into the workspace and
+ * the GEMM kernel loads them by TMA; with plm_gemm_workspace_size_split
+ * bytes K is split where the output tiles alone would leave SMs idle (the
+ * faster choice for small m and n).  The workspace must not be used by other
+ * work until the call's kernels have finished on `stream`.
+ * PLM_ERR_INVALID_ARG if it is too small. */
 plm_status plm_gemm_q4K_ws(const void* w, const void* xq, float* y, int64_t m, int64_t n, int64_t k,
                            void* workspace, size_t workspace_bytes, cudaStream_t stream);
 plm_status plm_gemm_q6K_ws(const void* w, const void* xq, float* y, int64_t m, int64_t n, int64_t k,
                            void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
- * Allocation-free q4_K GEMM.  No counterpart on the PocketLLM pages: it is a
- * library convenience.  Same contract and results as plm_gemm_q4K (within
- * the same tolerance), except that its temporary f16 copy of the activations
- * lives in a fixed device array inside this library instead of memory the
- * call allocates.  It is meant for callers that must not allocate device
+ * Allocation-free q4_K GEMM through a fixed workspace.  No counterpart on
+ * the PocketLLM pages: it is a library convenience.  It runs the workspace
+ * form of the GEMM (plm_gemm_q4K_ws: pre-pass, TMA-loaded f16 activations,
+ * no K split) with the workspace in a fixed device array inside this
+ * library; results are bit-identical to plm_gemm_q4K, which needs no
+ * workspace at all.  It is meant for callers that must not allocate device
  * memory while running, such as an engine whose memory is entirely claimed
  * by its own allocator at start-up, or a latency-critical loop that cannot
  * afford an allocation that might fail or wait.
@@ -403,9 +412,8 @@ plm_status plm_gemm_q6K_ws(const void* w, const void* xq, float* y, int64_t m, i
  *     each call rewrites the part it reads), so calls whose kernels may
  *     overlap on the GPU, e.g. on different streams, race: serialize them.
  *   - It never splits K (the array holds no split partial sums), so where
- *     plm_gemm_q4K would split K -- few output tiles, i.e. small m and n --
- *     it can be slower, and its f32 sums are added in another order: it then
- *     agrees with plm_gemm_q4K within the tolerance above, not bit for bit.
+ *     plm_gemm_q4K_ws with the split workspace would split K -- few output
+ *     tiles, i.e. small m and n -- it can be slower.
  *   - The array's device address is kept per device for the life of the
  *     process; do not call it across a cudaDeviceReset.
  */

@@ -191,7 +191,7 @@ plm_status gemm_swiglu_common(const void* wg, const void* wu, const void* xq, fl
     if (s != PLM_OK) return s;
     if (m * n > (int64_t)1 << 40) return PLM_ERR_INVALID_ARG;
     if (caller_ws) {
-        const size_t need = plm::gemm_swiglu_workspace_need(m, (int)n, (int)k);
+        const size_t need = plm::gemm_swiglu_workspace_min(m, (int)n, (int)k);
         if (need > 0 && (!ws || ws_bytes < need)) return PLM_ERR_INVALID_ARG;
         if (ws && !aligned(ws, 256)) return PLM_ERR_MISALIGNED;
     }

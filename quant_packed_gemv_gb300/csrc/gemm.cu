@@ -49,6 +49,7 @@
 #include <cuda.h>
 #include <cuda_fp16.h>
 
+#include <cstring>
 #include <type_traits>
 
 #include "plm_device.cuh"
@@ -59,12 +60,17 @@ namespace plm {
 constexpr int GT = 128;                 // tile rows (weights) and columns (activations)
 constexpr int KS = 64;                  // K per operand stage (one 128-byte swizzle row)
 constexpr int TILE_BYTES = GT * KS * 2; // 16 KB per operand tile
+constexpr int XROW = 272;               // XIN: staged bytes per activation row and block
+constexpr int XSTAGE_BYTES = GT * XROW; // XIN: one staging buffer of a block's codes
 // Roles: PWG producer warpgroups (warpgroup h decodes stages [4h/PWG, 4(h+1)/PWG)
 // of every block), one epilogue warpgroup, one MMA warp; PWG per format below.
+// XIN (no workspace): NCV more warps after the MMA warp widen the activation
+// codes into the B tiles (xin_issue, xin_convert) in place of the TMA.
 template <int PWG> struct GemmRoles {
     static constexpr int EPI_WARP0 = 4 * PWG;      // first epilogue warp
     static constexpr int MMA_WARP = EPI_WARP0 + 4;
-    static constexpr int THREADS = (MMA_WARP + 1) * 32;
+    static constexpr int NCV = 2;
+    static constexpr int threads(bool xin) { return (MMA_WARP + 1 + (xin ? NCV : 0)) * 32; }
 };
 // With two producer warpgroups the block launches at 128 registers a thread
 // (13 warps); the producers then give up 32 each and the epilogue warpgroup,
@@ -94,7 +100,7 @@ template <> struct GemmCfg<6> {
     static constexpr int ATILES = 2, NSTAGE = 3, MINB = 0, BSLOTS = 0, WROW = 0, PWG = 1;
 };
 
-template <int FMT>
+template <int FMT, bool XIN>
 struct GemmSmem {
     // offsets from the 1024-aligned base
     static constexpr int NSTAGE = GemmCfg<FMT>::NSTAGE;
@@ -106,11 +112,13 @@ struct GemmSmem {
     static constexpr int BTX = WT + GT * AUXB;                               // bytes landing per block slot
     static constexpr int BSLOT = (BTX + 1023) & ~1023;
     static constexpr int BRING = (SCL + 2 * 3 * GT * 4 + 1023) & ~1023;
-    static constexpr int BAR = BRING + GemmCfg<FMT>::BSLOTS * BSLOT;
-    static constexpr int NBAR = 2 * NSTAGE + 8 + 2 * GemmCfg<FMT>::BSLOTS;
+    static constexpr int XST = BRING + GemmCfg<FMT>::BSLOTS * BSLOT;        // XIN: 2 staging buffers
+    static constexpr int BAR = XST + (XIN ? 2 * XSTAGE_BYTES : 0);
+    static constexpr int NBAR = 2 * NSTAGE + 8 + 2 * GemmCfg<FMT>::BSLOTS + (XIN ? 4 : 0);
     static constexpr int TMEMP = BAR + NBAR * 8;
     static constexpr int BYTES = TMEMP + 16;
     static constexpr int ALLOC = BYTES + 1024;   // + alignment slack
+    static_assert(ALLOC <= 227 * 1024, "shared memory");
 };
 
 // byte offset of element (row, k) in a 128-row x 64-wide f16 tile with the
@@ -182,6 +190,167 @@ __device__ __forceinline__ void tc_fence_after() {
 
 __device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 __device__ __forceinline__ __half2 bits_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
+
+// ---------------------------------------------------------------------------
+// In-kernel activation operand (the entry points without a workspace).
+// Converter warps widen the q8_K codes of the tile's 128 activation rows into
+// the f16 B tiles, in the layout the TMA would write.  Converter warp 0 brings
+// each block's codes into shared memory a block ahead of use: per activation
+// row one bulk copy of XROW bytes starting at the 16-byte boundary at or below
+// the row's 256 codes (the window ends inside the row's q8_K block and starts
+// no lower than the 16-byte chunk holding xq's first byte), into one of two
+// staging buffers.  All converter threads then widen the block's stages from
+// there: a code q becomes f16 (1024 + (q + 128)) - 1152 = q, exact; rows past
+// m become zeros.  The per-block side data (bsums as f16 pairs, d) is loaded
+// a block ahead into registers and written where the TMA would put it.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+    return r;
+}
+
+
+// Converter warp 0: block blk's codes of activation rows i0 .. into a
+// staging buffer.  xmap (when xq is 16-byte aligned and a row of q8_K blocks
+// a multiple of 16 bytes, i.e. nb % 4 == 0): one TMA box of 128 rows x 68
+// four-byte words from the 16-byte boundary at or below the block's codes
+// (the same for every row; rows past m arrive as zeros).  Otherwise one bulk
+// copy per row.
+__device__ __forceinline__ void xin_issue(uint8_t* st, uint64_t* bar, const CUtensorMap* xmap, bool xtma,
+                                          const uint8_t* xq, int nb, int m, int i0, int blk, int lane) {
+    if (xtma) {
+        if (lane == 0) {
+            mbar_arrive_expect_tx(bar, (uint32_t)XSTAGE_BYTES);
+            tma_load_2d(st, xmap, (((Q8K_BYTES * blk + 4) & ~15) >> 2), i0, bar);
+        }
+        return;
+    }
+    const int valid = min(GT, m - i0);
+    if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(valid * XROW));
+    __syncwarp();
+    for (int r = lane; r < valid; r += 32) {
+        const uint8_t* src = xq + ((size_t)(i0 + r) * nb + blk) * Q8K_BYTES + 4;
+        bulk_g2s(st + r * XROW, src - ((uintptr_t)src & 15u), XROW, bar);
+    }
+}
+
+// The widening work of a staged block is 512 units: unit k is stage c = k /
+// 128 and, within it, row phase ph = (k % 128) / 16 and word wi = k % 16,
+// i.e. the four codes 64c + 4wi .. of the 16 rows ph, ph + 8, ..., ph + 120.
+// Rows eight apart share their swizzle pattern and, since 8 * 292 * nb is a
+// multiple of 16, their skew in the staging window, so every load and store
+// of a unit sits at a constant offset from the first.
+__device__ __forceinline__ void xin_unit(const uint8_t* st, uint8_t* tile, uint32_t sk, int c, int ph, int wi) {
+    const uint8_t* src = st + ph * XROW + sk + c * KS + 4 * wi;
+    uint8_t* dst = tile + ph * 128 + ((((wi >> 1) ^ ph) & 7) << 4) + 8 * (wi & 1);
+    const __half2 off = bits_h2(0x64806480u);   // 1152, 1152
+    uint32_t v[16];
+#pragma unroll
+    for (int t = 0; t < 16; ++t) v[t] = *reinterpret_cast<const uint32_t*>(src + t * 8 * XROW);
+#pragma unroll
+    for (int t = 0; t < 16; ++t) {
+        const uint32_t x = v[t] ^ 0x80808080u;   // q + 128 per byte
+        const uint32_t lo = h2_bits(__hsub2(bits_h2(prmt(x, 0x64646464u, 0x4140u)), off));
+        const uint32_t hi = h2_bits(__hsub2(bits_h2(prmt(x, 0x64646464u, 0x4342u)), off));
+        *reinterpret_cast<uint2*>(dst + t * 1024) = make_uint2(lo, hi);   // rows 8 apart: 1 KB apart
+    }
+}
+
+// The skew of the rows of phase ph in their staging windows: the codes'
+// address mod 16 (a 32-bit wrap keeps it).
+__device__ __forceinline__ uint32_t xin_skew(const uint8_t* xq, int nb, int i0, int blk, int ph) {
+    return ((uint32_t)(uintptr_t)xq + 4u + (uint32_t)Q8K_BYTES * (uint32_t)blk +
+            (uint32_t)Q8K_BYTES * (uint32_t)nb * (uint32_t)(i0 + ph)) & 15u;
+}
+
+// One staged block: converter thread u (of NT, a multiple of 32) takes units
+// u, u + NT, ... in order, so each warp meets the stages in order and has
+// units in every stage.  Before its first unit of stage c it waits for the
+// slot (wait_slot(c)); after its last it publishes the stage (done(c)).
+template <int NT, class WaitSlot, class Tile, class Done>
+__device__ __forceinline__ bool xin_block(const uint8_t* st, const uint8_t* xq, int nb, int i0, int blk, int u,
+                                          WaitSlot wait_slot, Tile tile, Done done) {
+    // warp-uniform stages, and every warp meets every stage (steps of at most 128 units)
+    static_assert(NT % 32 == 0 && NT <= 128, "converter threads");
+    constexpr int PER = (512 + NT - 1) / NT;
+    const int k0 = u & ~31;   // the warp's first unit
+    int cur = -1;
+#pragma unroll 1
+    for (int t = 0; t < PER; ++t) {   // not unrolled: the kernel's roles share the instruction cache
+        const int kw = k0 + NT * t;   // warp-uniform
+        if (kw >= 512) break;
+        const int k = u + NT * t;
+        const int c = kw >> 7;
+        if (c != cur) {
+            if (cur >= 0) done(cur);
+            if (!wait_slot(c)) return false;
+            cur = c;
+        }
+        const int ph = (k >> 4) & 7, wi = k & 15;
+        xin_unit(st, tile(c), xin_skew(xq, nb, i0, blk, ph), c, ph, wi);
+    }
+    done(cur);
+    return true;
+}
+
+// Per-row copies leave the staging rows past m untouched: zero them once
+// (both buffers) so that those rows widen to zeros.
+__device__ __forceinline__ void xin_zero_tail(uint8_t* xst, int valid, int u, int nt) {
+    for (int o = valid * XROW / 16 + u; o < GT * XROW / 16; o += nt) {
+        reinterpret_cast<uint4*>(xst)[o] = make_uint4(0u, 0u, 0u, 0u);
+        reinterpret_cast<uint4*>(xst + XSTAGE_BYTES)[o] = make_uint4(0u, 0u, 0u, 0u);
+    }
+}
+
+// Side data of one block for the tile's rows u, u + NT, ...: the eight words
+// of bsums and d, loaded a block ahead, then written as AUXB bytes per row
+// (the 16 bsums as f16 pairs, |bsum| <= 2048: exact; d; three zero words).
+template <int NT>
+struct XinSide {
+    static constexpr int ROWS = (GT + NT - 1) / NT;
+    uint32_t v[ROWS][9];
+};
+
+template <int NT>
+__device__ __forceinline__ void xin_side_load(XinSide<NT>& S, const uint8_t* xq, int nb, int m, int i0, int blk,
+                                              int u) {
+#pragma unroll
+    for (int r = 0; r < XinSide<NT>::ROWS; ++r) {
+        const int t = u + NT * r, i = i0 + t;
+        const bool valid = t < GT && i < m;
+        const uint8_t* b = xq + ((size_t)(valid ? i : 0) * nb + blk) * Q8K_BYTES;
+#pragma unroll
+        for (int g = 0; g < 8; ++g)
+            S.v[r][g] = valid ? __ldg(reinterpret_cast<const uint32_t*>(b + 4 + QK) + g) : 0u;
+        S.v[r][8] = valid ? __ldg(reinterpret_cast<const uint32_t*>(b)) : 0u;
+    }
+}
+
+template <int NT>
+__device__ __forceinline__ void xin_side_store(const XinSide<NT>& S, uint8_t* side, int u) {
+#pragma unroll
+    for (int r = 0; r < XinSide<NT>::ROWS; ++r) {
+        const int t = u + NT * r;
+        if (t >= GT) break;
+        uint32_t o[8];
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+            const uint32_t v = S.v[r][g];
+            o[g] = h2_bits(__halves2half2(__int2half_rn((int)(int16_t)(v & 0xFFFFu)),
+                                          __int2half_rn((int)(int16_t)(v >> 16))));
+        }
+        uint4* dst = reinterpret_cast<uint4*>(side + t * AUXB);
+        dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+        dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+        dst[2] = make_uint4(S.v[r][8], 0u, 0u, 0u);
+    }
+}
+
+// SwiGLU of a gate/up pair: silu(g) * u = g / (1 + e^-g) * u
+__device__ __forceinline__ float swiglu1(float g, float u) {
+    return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
+}
 
 // ---------------------------------------------------------------------------
 // Weight decoders (one thread = one weight row of the tile)
@@ -415,17 +584,19 @@ struct GemmArgs {
     const uint8_t* xq;       // q8_K [m][nb]
     float* y;                // [m][n]
     float* part;             // split K: partial sums [gridDim.z][m][n] (null: write y)
+    const float* gate;       // GATE kernels (unsplit q4_K): y = silu(gate) * result, gate may be y itself
+    int xtma;                // XIN: the staged codes come by TMA (xmap), else by one bulk copy per row
     unsigned* fault;
     int m, n, nb;
     int bsplit;              // blocks of K per split (blockIdx.z)
 };
 
-template <int FMT>
-__global__ void __launch_bounds__(GemmRoles<GemmCfg<FMT>::PWG>::THREADS, 1) gemm_kernel(const __grid_constant__ CUtensorMap xmap,
+template <int FMT, bool XIN>
+__global__ void __launch_bounds__(GemmRoles<GemmCfg<FMT>::PWG>::threads(XIN), 1) gemm_kernel(const __grid_constant__ CUtensorMap xmap,
                                                                const __grid_constant__ CUtensorMap wmap,
                                                                const __grid_constant__ CUtensorMap amap,
                                                                const GemmArgs A) {
-    using L = GemmSmem<FMT>;
+    using L = GemmSmem<FMT, XIN>;
     constexpr int NSTAGE = L::NSTAGE;
     constexpr int PWG = GemmCfg<FMT>::PWG;
     constexpr int EPI_WARP0 = GemmRoles<PWG>::EPI_WARP0, MMA_WARP = GemmRoles<PWG>::MMA_WARP;
@@ -433,7 +604,7 @@ __global__ void __launch_bounds__(GemmRoles<GemmCfg<FMT>::PWG>::THREADS, 1) gemm
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BAR);
-    uint64_t* full = bars;                  // [NSTAGE], 4 arrivals (the stage's warpgroup) + TMA bytes
+    uint64_t* full = bars;                  // [NSTAGE], 4 arrivals (the stage's warpgroup) + TMA bytes (XIN: NCV arrivals)
     uint64_t* empty = bars + NSTAGE;        // [NSTAGE], MMA commit
     uint64_t* minfull = bars + 2 * NSTAGE;  // [2], one arrival per producer warp (min operands, scales)
     uint64_t* minempty = minfull + 2;       // [2], MMA commit
@@ -441,6 +612,8 @@ __global__ void __launch_bounds__(GemmRoles<GemmCfg<FMT>::PWG>::THREADS, 1) gemm
     uint64_t* tempty = minfull + 6;         // [2], 4 epilogue-warp arrivals
     uint64_t* bfull = minfull + 8;          // [BSLOTS], TMA bytes of a weight block and its side data
     uint64_t* bempty = bfull + GemmCfg<FMT>::BSLOTS;   // [BSLOTS], one arrival per producer warp
+    uint64_t* xfull = bempty + GemmCfg<FMT>::BSLOTS;   // XIN [2]: bulk-copy bytes of a staged block of codes
+    uint64_t* xempty = xfull + 2;                      // XIN [2]: converter-warp arrivals once it is widened
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::TMEMP);
     float* scl = reinterpret_cast<float*>(sm + L::SCL);   // [2][3][128]: d, dmin, dx
 
@@ -455,7 +628,7 @@ __global__ void __launch_bounds__(GemmRoles<GemmCfg<FMT>::PWG>::THREADS, 1) gemm
 
     if (tid == 0) {
         for (int s = 0; s < NSTAGE; ++s) {
-            mbar_init(&full[s], 4);
+            mbar_init(&full[s], 4 + (XIN ? GemmRoles<PWG>::NCV : 0));
             mbar_init(&empty[s], 1);
         }
         for (int j = 0; j < 2; ++j) {
@@ -467,6 +640,12 @@ __global__ void __launch_bounds__(GemmRoles<GemmCfg<FMT>::PWG>::THREADS, 1) gemm
         for (int s = 0; s < GemmCfg<FMT>::BSLOTS; ++s) {
             mbar_init(&bfull[s], 1);
             mbar_init(&bempty[s], 4 * PWG);
+        }
+        if constexpr (XIN) {
+            for (int j = 0; j < 2; ++j) {
+                mbar_init(&xfull[j], 1);
+                mbar_init(&xempty[j], GemmRoles<PWG>::NCV);
+            }
         }
         fence_barrier_init();
     }
@@ -599,7 +778,7 @@ __global__ void __launch_bounds__(GemmRoles<GemmCfg<FMT>::PWG>::THREADS, 1) gemm
                 const int g = 4 * b + c, s = g % NSTAGE, u = g / NSTAGE;
                 if (g >= NSTAGE && !mbar_wait(&empty[s], (u - 1) & 1)) return false;
                 uint8_t* st = sm + L::RING + s * L::STAGE;
-                if (t == 0) {
+                if (!XIN && t == 0) {
                     mbar_expect_tx(&full[s], TILE_BYTES);
                     tma_load_2d(st + BOFF, &xmap, (kb0 + b) * QK + c * KS, i0, &full[s]);
                 }
@@ -694,6 +873,52 @@ __global__ void __launch_bounds__(GemmRoles<GemmCfg<FMT>::PWG>::THREADS, 1) gemm
             }
         }
         __syncwarp();
+    } else if (warp > MMA_WARP) {
+        // ------------------------------------------------------- activation converters (XIN)
+        if constexpr (XIN) {
+            static_assert(!XIN || GemmCfg<FMT>::BSLOTS == 0, "XIN side data: q6_K only in this kernel");
+            constexpr int NT = GemmRoles<PWG>::NCV * 32;
+            const int u = tid - (MMA_WARP + 1) * 32, cw = u >> 5;
+            uint8_t* xst = sm + L::XST;
+            if (!A.xtma) {
+                xin_zero_tail(xst, min(GT, A.m - i0), u, NT);
+                asm volatile("bar.sync 1, %0;" :: "n"(NT) : "memory");
+            }
+            int nxi = 0;   // warp 0: blocks whose codes were issued
+            if (cw == 0)
+                for (; nxi < 2 && nxi < kcount; ++nxi)
+                    xin_issue(xst + nxi * XSTAGE_BYTES, &xfull[nxi], &xmap, A.xtma != 0, A.xq, nb, A.m, i0, kb0 + nxi, lane);
+            int b = 0;
+            for (; b < kcount && ok; ++b) {
+                const int xs = b & 1;
+                if (!mbar_wait(&xfull[xs], (uint32_t)(b >> 1) & 1u)) { ok = false; break; }
+                ok = xin_block<NT>(
+                    xst + xs * XSTAGE_BYTES, A.xq, nb, i0, kb0 + b, u,
+                    [&](int c) {
+                        const int g = 4 * b + c;
+                        return g < NSTAGE || mbar_wait(&empty[g % NSTAGE], (uint32_t)(g / NSTAGE - 1) & 1u);
+                    },
+                    [&](int c) { return sm + L::RING + ((4 * b + c) % NSTAGE) * L::STAGE + BOFF; },
+                    [&](int c) {
+                        fence_async_smem();   // generic writes before the tensor core reads them
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&full[(4 * b + c) % NSTAGE]);
+                    });
+                if (!ok) break;
+                // the staging buffer's reads before its refill
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&xempty[xs]);
+                if (cw == 0 && b + 2 < kcount) {
+                    if (!mbar_wait(&xempty[xs], (uint32_t)(b >> 1) & 1u)) { ok = false; break; }
+                    xin_issue(xst + xs * XSTAGE_BYTES, &xfull[xs], &xmap, A.xtma != 0, A.xq, nb, A.m, i0, kb0 + b + 2, lane);
+                    ++nxi;
+                }
+            }
+            // after a wait ran out: let the code copies still in flight land before the CTA exits
+            if (!ok && cw == 0 && lane == 0)
+                for (int bb = b; bb < nxi; ++bb) (void)mbar_wait(&xfull[bb & 1], (uint32_t)(bb >> 1) & 1u);
+        }
     } else {
         // ------------------------------------------------------- epilogue
         if constexpr (PWG == 2) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" :: "n"(REG_EPILOGUE));
@@ -763,11 +988,17 @@ __global__ void __launch_bounds__(GemmRoles<GemmCfg<FMT>::PWG>::THREADS, 1) gemm
 // producers (two warpgroups, stages 2h, 2h + 1 of every block), warps 8-15
 // epilogue (warp e: TMEM lanes 32 (e % 4) .., activation columns 64 (e / 4)
 // .. + 63), warp 16 issues the MMAs.  No register hand-over: 17 warps at 96.
+// XIN (no workspace): warps 17-19 widen the activation codes from xq into
+// the B tiles and write the side data into the block slots (xin_issue,
+// xin_convert, xin_side_store) in place of the TMA; 20 warps keep five per
+// sub-partition, so the register budget stays at 96.
 // ---------------------------------------------------------------------------
-constexpr int TM_EPI_WARP0 = 8, TM_MMA_WARP = 16, TM_THREADS = 17 * 32, TM_NSTAGE = 4;
+constexpr int TM_EPI_WARP0 = 8, TM_MMA_WARP = 16, TM_NSTAGE = 4;
+constexpr int TM_NCV = 3;   // converter warps (XIN)
+constexpr int tm_threads(bool xin) { return (TM_MMA_WARP + 1 + (xin ? TM_NCV : 0)) * 32; }
 constexpr uint32_t TM_D1 = 0, TM_D2 = 256, TM_A = 384;
 
-template <int FMT>
+template <int FMT, bool XIN>
 struct TmSmem {
     static constexpr int RING = 0;                                            // B tiles, 4 x 16 KB
     static constexpr int MIN = RING + TM_NSTAGE * TILE_BYTES;                 // 2 x 16 KB
@@ -776,11 +1007,13 @@ struct TmSmem {
     static constexpr int BTX = WT + GT * AUXB;
     static constexpr int BSLOT = (BTX + 1023) & ~1023;
     static constexpr int BRING = (SCL + 2 * 3 * GT * 4 + 1023) & ~1023;
-    static constexpr int BAR = BRING + 2 * BSLOT;
-    static constexpr int NBAR = 2 * TM_NSTAGE + 8 + 4 + 1;
+    static constexpr int XST = BRING + 2 * BSLOT;                             // XIN: 2 staging buffers
+    static constexpr int BAR = XST + (XIN ? 2 * XSTAGE_BYTES : 0);
+    static constexpr int NBAR = 2 * TM_NSTAGE + 8 + 4 + 1 + (XIN ? 4 : 0);
     static constexpr int TMEMP = BAR + NBAR * 8;
     static constexpr int BYTES = TMEMP + 16;
     static constexpr int ALLOC = BYTES + 1024;
+    static_assert(ALLOC <= 227 * 1024, "shared memory");
 };
 
 __device__ __forceinline__ void mma_f16_ta(uint32_t dtmem, uint32_t atmem, uint64_t db, uint32_t accumulate) {
@@ -799,25 +1032,27 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
                     "r"(r[29]), "r"(r[30]), "r"(r[31]) : "memory");
 }
 
-template <int FMT>
-__global__ void __launch_bounds__(TM_THREADS, 1) gemm_tm_kernel(const __grid_constant__ CUtensorMap xmap,
+template <int FMT, bool XIN, bool GATE>
+__global__ void __launch_bounds__(tm_threads(XIN), 1) gemm_tm_kernel(const __grid_constant__ CUtensorMap xmap,
                                                                 const __grid_constant__ CUtensorMap wmap,
                                                                 const __grid_constant__ CUtensorMap amap,
                                                                 const GemmArgs A) {
-    using L = TmSmem<FMT>;
+    using L = TmSmem<FMT, XIN>;
     constexpr int NSTAGE = TM_NSTAGE;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BAR);
-    uint64_t* full = bars;                  // [4]: 4 producer-warp arrivals + the B tile's TMA bytes
+    uint64_t* full = bars;                  // [4]: 4 producer-warp arrivals + the B tile (TMA bytes, or XIN: converter warps)
     uint64_t* empty = bars + NSTAGE;        // [4]: MMA commit (frees the TMEM A stage and the B tile)
     uint64_t* minfull = bars + 2 * NSTAGE;  // [2]: 8 producer-warp arrivals (min operands, scales)
     uint64_t* minempty = minfull + 2;       // [2]: MMA commit
     uint64_t* tfull = minfull + 4;          // [2]: MMA commit
     uint64_t* tempty = minfull + 6;         // [2]: 8 epilogue-warp arrivals
-    uint64_t* bfull = minfull + 8;          // [2]: TMA bytes of a weight block and its side data
+    uint64_t* bfull = minfull + 8;          // [2]: TMA bytes of a weight block and its side data (XIN: + converter warps)
     uint64_t* bempty = bfull + 2;           // [2]: 8 producer-warp arrivals
     uint64_t* d2free = bempty + 2;          // [1]: 8 epilogue-warp arrivals once D2 is read
+    uint64_t* xfull = d2free + 1;           // XIN [2]: bulk-copy bytes of a staged block of codes
+    uint64_t* xempty = xfull + 2;           // XIN [2]: converter-warp arrivals once it is widened
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::TMEMP);
     float* scl = reinterpret_cast<float*>(sm + L::SCL);   // [2][3][128]: d, dmin, dx
 
@@ -832,7 +1067,7 @@ __global__ void __launch_bounds__(TM_THREADS, 1) gemm_tm_kernel(const __grid_con
 
     if (tid == 0) {
         for (int s = 0; s < NSTAGE; ++s) {
-            mbar_init(&full[s], 4);
+            mbar_init(&full[s], 4 + (XIN ? TM_NCV : 0));
             mbar_init(&empty[s], 1);
         }
         for (int j = 0; j < 2; ++j) {
@@ -840,10 +1075,16 @@ __global__ void __launch_bounds__(TM_THREADS, 1) gemm_tm_kernel(const __grid_con
             mbar_init(&minempty[j], 1);
             mbar_init(&tfull[j], 1);
             mbar_init(&tempty[j], 8);
-            mbar_init(&bfull[j], 1);
+            mbar_init(&bfull[j], 1 + (XIN ? TM_NCV : 0));
             mbar_init(&bempty[j], 8);
         }
         mbar_init(d2free, 8);
+        if constexpr (XIN) {
+            for (int j = 0; j < 2; ++j) {
+                mbar_init(&xfull[j], 1);
+                mbar_init(&xempty[j], TM_NCV);
+            }
+        }
         fence_barrier_init();
     }
     if (warp == TM_MMA_WARP) {
@@ -871,9 +1112,9 @@ __global__ void __launch_bounds__(TM_THREADS, 1) gemm_tm_kernel(const __grid_con
             ++nissued;
             const int s = bb & 1;
             uint8_t* dst = sm + L::BRING + s * L::BSLOT;
-            mbar_arrive_expect_tx(&bfull[s], (uint32_t)L::BTX);
+            mbar_arrive_expect_tx(&bfull[s], (uint32_t)(XIN ? L::WT : L::BTX));
             tma_load_2d(dst, &wmap, (kb0 + bb) * GemmCfg<FMT>::WROW, r0, &bfull[s]);
-            tma_load_2d(dst + L::WT, &amap, (kb0 + bb) * AUXB, i0, &bfull[s]);
+            if constexpr (!XIN) tma_load_2d(dst + L::WT, &amap, (kb0 + bb) * AUXB, i0, &bfull[s]);
         };
         if (tid == 0)
             for (int bb = 0; bb < 2 && bb < kcount; ++bb) issue_block(bb);
@@ -932,7 +1173,7 @@ __global__ void __launch_bounds__(TM_THREADS, 1) gemm_tm_kernel(const __grid_con
                         if (!mbar_wait(&empty[c], (uint32_t)(gb - 1) & 1u)) return false;
                         tc_fence_after();
                     }
-                    if (t == 0) {
+                    if (!XIN && t == 0) {
                         mbar_expect_tx(&full[c], TILE_BYTES);
                         tma_load_2d(sm + L::RING + c * TILE_BYTES, &xmap, (kb0 + b) * QK + c * KS, i0, &full[c]);
                     }
@@ -997,6 +1238,57 @@ __global__ void __launch_bounds__(TM_THREADS, 1) gemm_tm_kernel(const __grid_con
             }
         }
         __syncwarp();
+    } else if (warp > TM_MMA_WARP) {
+        // ------------------------------------------------------- activation converters (XIN)
+        if constexpr (XIN) {
+            constexpr int NT = TM_NCV * 32;
+            const int u = tid - (TM_MMA_WARP + 1) * 32, cw = u >> 5;
+            uint8_t* xst = sm + L::XST;
+            if (!A.xtma) {
+                xin_zero_tail(xst, min(GT, A.m - i0), u, NT);
+                asm volatile("bar.sync 1, %0;" :: "n"(NT) : "memory");
+            }
+            int nxi = 0;   // warp 0: blocks whose codes were issued
+            if (cw == 0)
+                for (; nxi < 2 && nxi < kcount; ++nxi)
+                    xin_issue(xst + nxi * XSTAGE_BYTES, &xfull[nxi], &xmap, A.xtma != 0, A.xq, nb, A.m, i0, kb0 + nxi, lane);
+            XinSide<NT> sd;
+            xin_side_load(sd, A.xq, nb, A.m, i0, kb0, u);
+            int gb = 0;
+            for (int b = 0; b < kcount && ok; ++b, ++gb) {
+                const int s = gb & 1, blk = kb0 + b;
+                // the block's side data into its weight slot, the next block's into registers
+                if (gb >= 2 && !mbar_wait(&bempty[s], (uint32_t)((gb >> 1) - 1) & 1u)) { ok = false; break; }
+                xin_side_store(sd, sm + L::BRING + s * L::BSLOT + L::WT, u);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bfull[s]);
+                if (b + 1 < kcount) xin_side_load(sd, A.xq, nb, A.m, i0, blk + 1, u);
+                // the four B stages, each once the MMA has finished the previous block's
+                if (!mbar_wait(&xfull[s], (uint32_t)(gb >> 1) & 1u)) { ok = false; break; }
+                ok = xin_block<NT>(
+                    xst + s * XSTAGE_BYTES, A.xq, nb, i0, blk, u,
+                    [&](int c) { return gb == 0 || mbar_wait(&empty[c], (uint32_t)(gb - 1) & 1u); },
+                    [&](int c) { return sm + L::RING + c * TILE_BYTES; },
+                    [&](int c) {
+                        fence_async_smem();   // generic writes before the tensor core reads them
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&full[c]);
+                    });
+                if (!ok) break;
+                // the staging buffer's reads before its refill
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&xempty[s]);
+                if (cw == 0 && b + 2 < kcount) {
+                    if (!mbar_wait(&xempty[s], (uint32_t)(gb >> 1) & 1u)) { ok = false; break; }
+                    xin_issue(xst + s * XSTAGE_BYTES, &xfull[s], &xmap, A.xtma != 0, A.xq, nb, A.m, i0, blk + 2, lane);
+                    ++nxi;
+                }
+            }
+            // after a wait ran out: let the code copies still in flight land before the CTA exits
+            if (!ok && cw == 0 && lane == 0)
+                for (int bb = gb; bb < nxi; ++bb) (void)mbar_wait(&xfull[bb & 1], (uint32_t)(bb >> 1) & 1u);
+        }
     } else {
         // ------------------------------------------------------- epilogue
         const int e = warp - TM_EPI_WARP0;
@@ -1050,10 +1342,28 @@ __global__ void __launch_bounds__(TM_THREADS, 1) gemm_tm_kernel(const __grid_con
             const int r = r0 + row;
             float* out = A.part ? A.part + (size_t)blockIdx.z * A.m * A.n : A.y;
             if (ok && r < A.n) {
+                if constexpr (GATE) {
+                    // SwiGLU pair: the gate GEMM's result for the same element, 16 loads at a time
 #pragma unroll
-                for (int c = 0; c < 64; ++c) {
-                    const int i = i0 + 64 * chalf + c;
-                    if (i < A.m) out[(size_t)i * A.n + r] = acc[c];
+                    for (int cb = 0; cb < 64; cb += 16) {
+                        float g[16];
+#pragma unroll
+                        for (int c = 0; c < 16; ++c) {
+                            const int i = i0 + 64 * chalf + cb + c;
+                            g[c] = i < A.m ? A.gate[(size_t)i * A.n + r] : 0.0f;
+                        }
+#pragma unroll
+                        for (int c = 0; c < 16; ++c) {
+                            const int i = i0 + 64 * chalf + cb + c;
+                            if (i < A.m) out[(size_t)i * A.n + r] = swiglu1(g[c], acc[cb + c]);
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 64; ++c) {
+                        const int i = i0 + 64 * chalf + c;
+                        if (i < A.m) out[(size_t)i * A.n + r] = acc[c];
+                    }
                 }
             }
         }
@@ -1114,8 +1424,7 @@ __global__ void gemm_swiglu_kernel(float* __restrict__ h, const float* __restric
     grid_wait_prior();
     for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < count;
          i += (long long)gridDim.x * blockDim.x) {
-        const float g = h[i];
-        h[i] = __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u[i]);
+        h[i] = swiglu1(h[i], u[i]);
     }
 }
 
@@ -1170,18 +1479,42 @@ static size_t gemm_split_bytes(long long m, int n, int splits) {
     return splits > 1 ? (size_t)splits * m * n * sizeof(float) : 0;
 }
 
+// ws == nullptr: the XIN kernels (activation codes widened in the kernel, no
+// pre-pass, no K split, nothing allocated).  Otherwise the pre-pass writes
+// the f16 activations and side data into ws for the TMA, and K is split when
+// ws also holds the partial sums.  gate: see GemmArgs (unsplit q4_K only).
 template <int FMT>
-static cudaError_t gemm_tc_ws(const uint8_t* w, const uint8_t* xq, float* y, long long m, int n, int k,
-                              void* ws, size_t ws_bytes, cudaStream_t stream) {
+static cudaError_t gemm_tc(const uint8_t* w, const uint8_t* xq, float* y, long long m, int n, int k, void* ws,
+                           size_t ws_bytes, const float* gate, cudaStream_t stream) {
     const int nb = k / QK;
-    __half* x16 = static_cast<__half*>(ws);
-    uint32_t* aux = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + gemm_x16_bytes(m, k));
-    // split K only when the caller's workspace holds the partial sums too
-    int splits = gemm_splits(m, n, nb);
-    if (ws_bytes < gemm_workspace_bytes(m, k) + gemm_split_bytes(m, n, splits)) splits = 1;
-    float* part = splits > 1 ? reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + gemm_workspace_bytes(m, k))
-                             : nullptr;
-    {
+    const bool xin = ws == nullptr;
+    int splits = 1;
+    float* part = nullptr;
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    const cuuint32_t estr[2] = {1, 1};
+    CUtensorMap map, wmap, amap;   // unused ones stay zero and are never read
+    memset(&map, 0, sizeof(map));
+    memset(&wmap, 0, sizeof(wmap));
+    memset(&amap, 0, sizeof(amap));
+    bool xtma = false;
+    if (xin && nb % 4 == 0 && ((uintptr_t)xq & 15u) == 0) {
+        // the q8_K rows as four-byte words: a box of 128 rows x XROW bytes
+        const cuuint64_t dims[2] = {(cuuint64_t)nb * (Q8K_BYTES / 4), (cuuint64_t)m};
+        const cuuint64_t strides[1] = {(cuuint64_t)nb * Q8K_BYTES};
+        const cuuint32_t box[2] = {(cuuint32_t)(XROW / 4), (cuuint32_t)GT};
+        xtma = enc(&map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint8_t*>(xq), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+        if (!xtma) memset(&map, 0, sizeof(map));
+    }
+    if (!xin) {
+        __half* x16 = static_cast<__half*>(ws);
+        uint32_t* aux = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + gemm_x16_bytes(m, k));
+        // split K only when the caller's workspace holds the partial sums too
+        if (!gate) splits = gemm_splits(m, n, nb);
+        if (ws_bytes < gemm_workspace_bytes(m, k) + gemm_split_bytes(m, n, splits)) splits = 1;
+        if (splits > 1) part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + gemm_workspace_bytes(m, k));
         const long long nblocks = m * nb;
         long long grid = (nblocks * 32 + 255) / 256;
         const long long cap = (long long)num_sms() * 8;
@@ -1189,22 +1522,26 @@ static cudaError_t gemm_tc_ws(const uint8_t* w, const uint8_t* xq, float* y, lon
         cudaError_t e = launch_kernel(gemm_x16_kernel, dim3((unsigned)grid), dim3(256), 0, stream, xq, x16, aux,
                                       nblocks);
         if (e != cudaSuccess) return e;
+        const cuuint64_t dims[2] = {(cuuint64_t)k, (cuuint64_t)m};
+        const cuuint64_t strides[1] = {(cuuint64_t)k * 2};
+        const cuuint32_t box[2] = {(cuuint32_t)KS, (cuuint32_t)GT};
+        if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, x16, dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+        if constexpr (GemmCfg<FMT>::BSLOTS > 0) {
+            // the side data: rows of nb * AUXB bytes, a box is one block of 128 activation rows
+            const cuuint64_t ad[2] = {(cuuint64_t)nb * AUXB, (cuuint64_t)m};
+            const cuuint64_t as_[1] = {(cuuint64_t)nb * AUXB};
+            const cuuint32_t ab[2] = {(cuuint32_t)AUXB, (cuuint32_t)GT};
+            if (enc(&amap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, aux, ad, as_, ab, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+                return cudaErrorInvalidValue;
+        }
     }
-    EncodeTiledFn enc = encode_fn();
-    if (!enc) return cudaErrorNotSupported;
-    CUtensorMap map;
-    const cuuint64_t dims[2] = {(cuuint64_t)k, (cuuint64_t)m};
-    const cuuint64_t strides[1] = {(cuuint64_t)k * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)KS, (cuuint32_t)GT};
-    const cuuint32_t estr[2] = {1, 1};
-    if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, x16, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-        return cudaErrorInvalidValue;
     // q4_K / q5_K: the raw weight blocks (rows of nb * WROW bytes; a box is
-    // one block of 128 rows, rows past n read as zeros) and the side data
-    // (rows of nb * AUXB bytes, one block of 128 activation rows)
-    CUtensorMap wmap = map, amap = map;
+    // one block of 128 rows, rows past n read as zeros)
     if constexpr (GemmCfg<FMT>::BSLOTS > 0) {
         constexpr int WROW = GemmCfg<FMT>::WROW;
         const cuuint64_t wd[2] = {(cuuint64_t)nb * WROW, (cuuint64_t)n};
@@ -1214,18 +1551,13 @@ static cudaError_t gemm_tc_ws(const uint8_t* w, const uint8_t* xq, float* y, lon
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
-        const cuuint64_t ad[2] = {(cuuint64_t)nb * AUXB, (cuuint64_t)m};
-        const cuuint64_t as_[1] = {(cuuint64_t)nb * AUXB};
-        const cuuint32_t ab[2] = {(cuuint32_t)AUXB, (cuuint32_t)GT};
-        if (enc(&amap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, aux, ad, as_, ab, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return cudaErrorInvalidValue;
     }
     GemmArgs A;
     A.w = w;
     A.xq = xq;
     A.y = y;
+    A.gate = gate;
+    A.xtma = xtma ? 1 : 0;
     A.fault = fault_word();
     if (!A.fault) return cudaErrorInvalidDevicePointer;
     A.m = (int)m;
@@ -1235,18 +1567,25 @@ static cudaError_t gemm_tc_ws(const uint8_t* w, const uint8_t* xq, float* y, lon
     A.bsplit = (nb + splits - 1) / splits;
     splits = (nb + A.bsplit - 1) / A.bsplit;   // no empty split
     const dim3 grid((unsigned)((m + GT - 1) / GT), (unsigned)((n + GT - 1) / GT), (unsigned)splits);
+    auto run = [&](auto kernel, int threads, int smem) -> cudaError_t {
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        return launch_kernel(kernel, grid, dim3(threads), smem, stream, map, wmap, amap, A);
+    };
     cudaError_t e;
     if constexpr (FMT == 4 || FMT == 5) {
-        constexpr int SMEM = TmSmem<FMT>::ALLOC;
-        e = cudaFuncSetAttribute(gemm_tm_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
-        if (e != cudaSuccess) return e;
-        e = launch_kernel(gemm_tm_kernel<FMT>, grid, dim3(TM_THREADS), SMEM, stream, map, wmap, amap, A);
+        if (gate) {
+            if (FMT != 4 || !xin) return cudaErrorInvalidValue;
+            e = run(gemm_tm_kernel<4, true, true>, tm_threads(true), TmSmem<4, true>::ALLOC);
+        } else {
+            e = xin ? run(gemm_tm_kernel<FMT, true, false>, tm_threads(true), TmSmem<FMT, true>::ALLOC)
+                    : run(gemm_tm_kernel<FMT, false, false>, tm_threads(false), TmSmem<FMT, false>::ALLOC);
+        }
     } else {
-        constexpr int SMEM = GemmSmem<FMT>::ALLOC;
-        e = cudaFuncSetAttribute(gemm_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
-        if (e != cudaSuccess) return e;
-        constexpr int THREADS = GemmRoles<GemmCfg<FMT>::PWG>::THREADS;
-        e = launch_kernel(gemm_kernel<FMT>, grid, dim3(THREADS), SMEM, stream, map, wmap, amap, A);
+        if (gate) return cudaErrorInvalidValue;
+        using R = GemmRoles<GemmCfg<FMT>::PWG>;
+        e = xin ? run(gemm_kernel<FMT, true>, R::threads(true), GemmSmem<FMT, true>::ALLOC)
+                : run(gemm_kernel<FMT, false>, R::threads(false), GemmSmem<FMT, false>::ALLOC);
     }
     if (e != cudaSuccess || splits == 1) return e;
     const long long count = m * (long long)n;
@@ -1267,14 +1606,17 @@ static bool gemm_on_tensor_cores(int fmt, long long m) {
     return (fmt == 4 || fmt == 5 || fmt == 6) && m >= GEMM_MIN_M && m <= 0x7FFFFFFF;
 }
 
-cudaError_t launch_gemm_ws(int fmt, const uint8_t* w, const uint8_t* xq, float* y, long long m, int n, int k,
-                           void* ws, size_t ws_bytes, cudaStream_t stream) {
-    if (gemm_on_tensor_cores(fmt, m)) {
-        if (!ws || ws_bytes < gemm_workspace_bytes(m, k)) return cudaErrorInvalidValue;
-        return fmt == 4 ? gemm_tc_ws<4>(w, xq, y, m, n, k, ws, ws_bytes, stream)
-               : fmt == 5 ? gemm_tc_ws<5>(w, xq, y, m, n, k, ws, ws_bytes, stream)
-                          : gemm_tc_ws<6>(w, xq, y, m, n, k, ws, ws_bytes, stream);
-    }
+static cudaError_t gemm_tc_any(int fmt, const uint8_t* w, const uint8_t* xq, float* y, long long m, int n, int k,
+                               void* ws, size_t ws_bytes, cudaStream_t stream) {
+    return fmt == 4 ? gemm_tc<4>(w, xq, y, m, n, k, ws, ws_bytes, nullptr, stream)
+           : fmt == 5 ? gemm_tc<5>(w, xq, y, m, n, k, ws, ws_bytes, nullptr, stream)
+                      : gemm_tc<6>(w, xq, y, m, n, k, ws, ws_bytes, nullptr, stream);
+}
+
+// Decode GEMV passes of at most eight activation rows (the GEMM entry points
+// below GEMM_MIN_M rows, and q2_K / q3_K)
+static cudaError_t gemm_by_gemv(int fmt, const uint8_t* w, const uint8_t* xq, float* y, long long m, int n, int k,
+                                cudaStream_t stream) {
     const int nb = k / QK;
     for (long long i0 = 0; i0 < m; i0 += GEMV_MAX_M) {
         const int mm = (int)(m - i0 < GEMV_MAX_M ? m - i0 : GEMV_MAX_M);
@@ -1282,6 +1624,13 @@ cudaError_t launch_gemm_ws(int fmt, const uint8_t* w, const uint8_t* xq, float* 
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
+}
+
+cudaError_t launch_gemm_ws(int fmt, const uint8_t* w, const uint8_t* xq, float* y, long long m, int n, int k,
+                           void* ws, size_t ws_bytes, cudaStream_t stream) {
+    if (!gemm_on_tensor_cores(fmt, m)) return gemm_by_gemv(fmt, w, xq, y, m, n, k, stream);
+    if (!ws || ws_bytes < gemm_workspace_bytes(m, k)) return cudaErrorInvalidValue;
+    return gemm_tc_any(fmt, w, xq, y, m, n, k, ws, ws_bytes, stream);
 }
 
 // q4_K gate/up pair with the SwiGLU epilogue, any m.  From GEMM_MIN_M rows:
@@ -1296,6 +1645,12 @@ size_t gemm_swiglu_workspace_need(long long m, int n, int k) {
     return pair_u_bytes(m, n) + gemm_workspace_need_split(4, m, n, k);
 }
 
+// the least workspace the _ws pair accepts (no K split)
+size_t gemm_swiglu_workspace_min(long long m, int n, int k) {
+    if (!gemm_on_tensor_cores(4, m)) return 0;
+    return pair_u_bytes(m, n) + gemm_workspace_bytes(m, k);
+}
+
 cudaError_t launch_gemm_q4K_swiglu_ws(const uint8_t* w_gate, const uint8_t* w_up, const uint8_t* xq, float* h,
                                       long long m, int n, int k, void* ws, size_t ws_bytes, cudaStream_t stream) {
     if (gemm_on_tensor_cores(4, m)) {
@@ -1304,9 +1659,9 @@ cudaError_t launch_gemm_q4K_swiglu_ws(const uint8_t* w_gate, const uint8_t* w_up
         float* u = static_cast<float*>(ws);
         void* gws = static_cast<uint8_t*>(ws) + ub;
         const size_t gbytes = ws_bytes - ub;
-        cudaError_t e = gemm_tc_ws<4>(w_gate, xq, h, m, n, k, gws, gbytes, stream);
+        cudaError_t e = gemm_tc<4>(w_gate, xq, h, m, n, k, gws, gbytes, nullptr, stream);
         if (e != cudaSuccess) return e;
-        e = gemm_tc_ws<4>(w_up, xq, u, m, n, k, gws, gbytes, stream);
+        e = gemm_tc<4>(w_up, xq, u, m, n, k, gws, gbytes, nullptr, stream);
         if (e != cudaSuccess) return e;
         const long long count = m * (long long)n;
         long long blocks = (count + 255) / 256;
@@ -1331,16 +1686,16 @@ cudaError_t launch_gemm_q4K_swiglu_ws(const uint8_t* w_gate, const uint8_t* w_up
     return cudaSuccess;
 }
 
+// Without a workspace: the gate GEMM into h, then the up GEMM, whose
+// epilogue reads each element's gate result back from h and writes
+// silu(g) * u over it (same bits as the workspace form when that one does
+// not split K).
 cudaError_t launch_gemm_q4K_swiglu(const uint8_t* w_gate, const uint8_t* w_up, const uint8_t* xq, float* h,
                                    long long m, int n, int k, cudaStream_t stream) {
-    const size_t need = gemm_swiglu_workspace_need(m, n, k);
-    if (need == 0) return launch_gemm_q4K_swiglu_ws(w_gate, w_up, xq, h, m, n, k, nullptr, 0, stream);
-    void* ws = nullptr;
-    cudaError_t e = cudaMallocAsync(&ws, need, stream);
+    if (!gemm_on_tensor_cores(4, m)) return launch_gemm_q4K_swiglu_ws(w_gate, w_up, xq, h, m, n, k, nullptr, 0, stream);
+    cudaError_t e = gemm_tc<4>(w_gate, xq, h, m, n, k, nullptr, 0, nullptr, stream);
     if (e != cudaSuccess) return e;
-    e = launch_gemm_q4K_swiglu_ws(w_gate, w_up, xq, h, m, n, k, ws, need, stream);
-    const cudaError_t f = cudaFreeAsync(ws, stream);
-    return e != cudaSuccess ? e : f;
+    return gemm_tc<4>(w_up, xq, h, m, n, k, nullptr, 0, h, stream);
 }
 
 size_t gemm_workspace_need(int fmt, long long m, int k) {
@@ -1352,24 +1707,20 @@ size_t gemm_workspace_need_split(int fmt, long long m, int n, int k) {
     return gemm_workspace_bytes(m, k) + gemm_split_bytes(m, n, gemm_splits(m, n, k / QK));
 }
 
+// Without a workspace: the tensor-core kernels widen the activation codes
+// themselves and never split K; nothing is allocated.
 cudaError_t launch_gemm(int fmt, const uint8_t* w, const uint8_t* xq, float* y, long long m, int n, int k,
                         cudaStream_t stream) {
-    const size_t need = gemm_workspace_need_split(fmt, m, n, k);
-    if (need == 0) return launch_gemm_ws(fmt, w, xq, y, m, n, k, nullptr, 0, stream);
-    void* ws = nullptr;
-    cudaError_t e = cudaMallocAsync(&ws, need, stream);
-    if (e != cudaSuccess) return e;
-    e = launch_gemm_ws(fmt, w, xq, y, m, n, k, ws, need, stream);
-    const cudaError_t f = cudaFreeAsync(ws, stream);
-    return e != cudaSuccess ? e : f;
+    if (!gemm_on_tensor_cores(fmt, m)) return gemm_by_gemv(fmt, w, xq, y, m, n, k, stream);
+    return gemm_tc_any(fmt, w, xq, y, m, n, k, nullptr, 0, stream);
 }
 
 }  // namespace plm
 
 // ---------------------------------------------------------------------------
-// Allocation-free GEMM entry: the same q4_K GEMM, with its f16 activation
-// workspace in a fixed device array compiled into this library instead of
-// memory from cudaMalloc / the stream-ordered pool.  It exists for callers
+// Allocation-free GEMM entry through a fixed workspace: the workspace form
+// of the q4_K GEMM, with its f16 activation workspace in a fixed device array
+// compiled into this library.  It exists for callers
 // that must not allocate device memory once they are running, for example an
 // engine whose whole memory budget is claimed by its own allocator at start-up,
 // or a latency-critical loop that cannot risk an allocation failing or

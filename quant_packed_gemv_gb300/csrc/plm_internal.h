@@ -70,18 +70,20 @@ cudaError_t launch_subdots(int fmt, const uint8_t* w, const uint8_t* xq, int32_t
                            int m, int n, int k, cudaStream_t stream);
 
 // Prefill GEMM, any m >= 1.  The _ws form uses the caller's workspace
-// (gemm_workspace_need bytes, 256-byte aligned); the plain form takes it from
-// the stream-ordered pool for the duration of the call.
+// (gemm_workspace_need bytes, 256-byte aligned); the plain form needs none
+// (the kernel widens the activation codes itself).
 cudaError_t launch_gemm(int fmt, const uint8_t* w, const uint8_t* xq, float* y,
                         long long m, int n, int k, cudaStream_t stream);
 cudaError_t launch_gemm_ws(int fmt, const uint8_t* w, const uint8_t* xq, float* y, long long m, int n, int k,
                            void* ws, size_t ws_bytes, cudaStream_t stream);
 size_t gemm_workspace_need(int fmt, long long m, int k);
 
-// q4_K gate/up pair with the SwiGLU epilogue, any m; the _ws form needs
-// gemm_swiglu_workspace_need(m, n, k) bytes for the split form (the up
-// matrix's output, then a GEMM workspace; at least the unsplit size).
+// q4_K gate/up pair with the SwiGLU epilogue, any m; the _ws form takes the
+// up matrix's output, then a GEMM workspace: gemm_swiglu_workspace_need(m, n,
+// k) bytes splits K where that pays, gemm_swiglu_workspace_min is the least
+// it accepts (unsplit).
 size_t gemm_swiglu_workspace_need(long long m, int n, int k);
+size_t gemm_swiglu_workspace_min(long long m, int n, int k);
 cudaError_t launch_gemm_q4K_swiglu(const uint8_t* w_gate, const uint8_t* w_up, const uint8_t* xq, float* h,
                                    long long m, int n, int k, cudaStream_t stream);
 cudaError_t launch_gemm_q4K_swiglu_ws(const uint8_t* w_gate, const uint8_t* w_up, const uint8_t* xq, float* h,

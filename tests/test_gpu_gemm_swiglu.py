@@ -1,12 +1,12 @@
 """Prefill gate/up pair with the SwiGLU epilogue (plm_gemm_q4K_swiglu).
 
-As for the decode pair: (1) against silu applied in f64 to the q4_K GEMM's
-own outputs for each matrix with the same workspace size (the pair computes
-the same f32 g and u; m <= 8: the GEMV's) -- relative 1e-6; (2) against the oracle, h = silu(g) u
+As for the decode pair: (1) against silu applied in f64 to the plain q4_K
+GEMM's own outputs for each matrix (the pair computes the same f32 g and u;
+m <= 8: the GEMV's) -- relative 1e-6; (2) against the oracle, h = silu(g) u
 in f64 on the oracle's integer path, within the bound the GEMM tolerance
 implies: |dh| <= 1.1 |u| dg + (|silu(g)| + 1.1 dg) du + 1e-6 |h|, with
 dg = 1e-4 S_gate, du = 1e-4 S_up (|silu'| <= 1.1).  The caller-workspace form
-gives the same bits."""
+gives the same bits when it does not split K."""
 import numpy as np
 import pytest
 import torch
@@ -42,15 +42,13 @@ def unpoison(buf, m, n):
 
 
 def single(w, xq, m, n, k):
-    """The matrix alone, in the same f32 order as the pair: the GEMM with the
-    pair's GEMM workspace size (so the same K split), or the GEMV for m <= 8."""
+    """The matrix alone, in the same f32 order as the plain pair: the plain
+    GEMM (no K split), or the GEMV for m <= 8."""
     y = torch.full((m, n), float("nan"), device="cuda")
     if m <= 8:
         q.plm_gemv_q4K(w, xq, y, m, n, k)
     else:
-        need = q.plm_gemm_workspace_size_split(4, m, n, k)
-        ws = torch.empty(max(need, 256), dtype=torch.uint8, device="cuda")
-        q.plm_gemm_q4K_ws(w, xq, y, m, n, k, ws, need)
+        q.plm_gemm_q4K(w, xq, y, m, n, k)
     return host(y).astype(np.float64)
 
 
@@ -79,10 +77,17 @@ def test_gemm_swiglu(m, n, k):
         + 1e-6 * np.abs(h_ref)
     assert np.all(np.abs(h - h_ref) <= bound)
     assert np.mean(np.abs(g_ref) < 4.0) > 0.5   # the gate outputs do cover the bend of silu
-    # caller workspace: same bits
-    need = q.plm_gemm_swiglu_workspace_size(m, n, k)
-    ws = torch.empty(max(need, 256), dtype=torch.uint8, device="cuda")
-    hb2 = poisoned(m, n)
-    q.plm_gemm_q4K_swiglu_ws(wg, wu, xq, hb2, m, n, k, ws if need else None, need)
-    assert np.array_equal(unpoison(hb2, m, n), h.astype(np.float32))
+    # caller workspace: without a K split the same bits (the plain form
+    # combines in the up GEMM's epilogue, the _ws form in a separate pass);
+    # with the split-K workspace within the bound
+    split = q.plm_gemm_swiglu_workspace_size(m, n, k)
+    unsplit = 0 if split == 0 else -(-m * n * 4 // 256) * 256 + q.plm_gemm_workspace_size("q4K", m, k)
+    for need in sorted({unsplit, split}):
+        ws = torch.empty(max(need, 256), dtype=torch.uint8, device="cuda")
+        hb2 = poisoned(m, n)
+        q.plm_gemm_q4K_swiglu_ws(wg, wu, xq, hb2, m, n, k, ws if need else None, need)
+        h2 = unpoison(hb2, m, n)
+        if need == unsplit:
+            assert np.array_equal(h2, h.astype(np.float32))
+        assert np.all(np.abs(h2.astype(np.float64) - h_ref) <= bound)
     assert q.plm_device_fault() == 0

@@ -109,6 +109,32 @@ def test_gemm_matches_oracle(fmt, m, n, k):
     assert_close(y, ref, S)
 
 
+@pytest.mark.parametrize("fmt", ["q4K", "q5K", "q6K"])
+@pytest.mark.parametrize("shift", [4, 8, 12])
+def test_gemm_xq_4_byte_aligned(fmt, shift):
+    """xq needs only 4-byte alignment.  Off a 16-byte boundary the plain GEMM
+    stages the activation codes with one bulk copy per row (each from the
+    16-byte boundary at or below the row's codes) instead of one TMA box per
+    block: the same bits as with an aligned xq."""
+    import torch
+    import quant_packed_gemv_gb300 as q
+    from tests.gpu_helpers import dev
+    m, n, k = 140, 136, 2048
+    w = make_weights(fmt, 15, 0, n, k)
+    xq = oracle.quantize_q8K(gen.normal_f32(15, 3, m, k))
+    wd = dev(w)
+    buf = torch.zeros(xq.nbytes + 64, dtype=torch.uint8, device="cuda")
+    buf[shift:shift + xq.nbytes] = torch.from_numpy(xq.reshape(-1)).cuda()
+    ys = []
+    for x in (dev(xq), buf[shift:shift + xq.nbytes]):
+        y = torch.full((m, n), float("nan"), device="cuda")
+        getattr(q, "plm_gemm_%s" % fmt)(wd, x, y, m, n, k)
+        ys.append(host(y))
+    np.testing.assert_array_equal(ys[0], ys[1])
+    ref, S = oracle_ref(fmt, w, xq, m, n, k)
+    assert_close(ys[1], ref, S)
+
+
 @pytest.mark.parametrize("fmt", ["q2K", "q3K", "q4K", "q5K", "q6K"])
 def test_gemm_agrees_with_gemv_small_m(fmt):
     n, k = 96, 1024
@@ -161,21 +187,21 @@ def test_gemm_with_caller_workspace_matches(fmt):
     m, n, k = 150, 260, 2048
     w = make_weights(fmt, 30, 0, n, k)
     xq = oracle.quantize_q8K(gen.normal_f32(30, 1, m, k))
-    # the plain entry takes the split-K workspace from the pool: with the same
-    # workspace size the caller-workspace form runs the same launches
+    # the split-K workspace: within tolerance
     full = q.plm_gemm_workspace_size_split(fmt, m, n, k)
     wsf = torch.empty(max(full, 1), dtype=torch.uint8, device="cuda")
     yf = torch.full((m, n), float("nan"), device="cuda")
     getattr(q, "plm_gemm_%s_ws" % fmt)(dev(w), dev(xq), yf, m, n, k, wsf if full else None, full)
     ref, S = oracle_ref(fmt, w, xq, m, n, k)
     assert_close(host(yf), ref, S)
-    assert np.array_equal(host(yf), gpu_matmul("gemm", fmt, w, xq, m, n, k))
-    # the minimal workspace: unsplit, within tolerance
+    # the minimal workspace: unsplit, and the same bits as the plain entry,
+    # which widens the activation codes in the kernel instead of a pre-pass
     need = q.plm_gemm_workspace_size(fmt, m, k)
     ws = torch.empty(max(need, 1), dtype=torch.uint8, device="cuda")
     y = torch.full((m, n), float("nan"), device="cuda")
     getattr(q, "plm_gemm_%s_ws" % fmt)(dev(w), dev(xq), y, m, n, k, ws if need else None, need)
     assert_close(host(y), ref, S)
+    assert np.array_equal(host(y), gpu_matmul("gemm", fmt, w, xq, m, n, k))
     if need:
         from quant_packed_gemv_gb300 import plm as P
         small = P.raw_status("plm_gemm_%s_ws" % fmt, dev(w).data_ptr(), dev(xq).data_ptr(), y.data_ptr(),

@@ -1,11 +1,12 @@
-"""The allocation-free q4_K GEMM (plm_gemm_q4K_noalloc).
+"""The allocation-free GEMM entry points.
 
-It serves callers that must not allocate device memory while running: its
-workspace is a fixed device array inside the library rather than memory
-taken from the stream-ordered pool.  Its results must agree with
-plm_gemm_q4K, which allocates its workspace, within the tolerance every GEMM
-test uses (1e-4 of sum_k |w_hat * x_hat|).  This file is named so that
-pytest collects it last.
+plm_gemm_q4K_noalloc runs the workspace form of the q4_K GEMM with its
+workspace in a fixed device array inside the library; it must give the bits
+of plm_gemm_q4K (which widens the activation codes inside the kernel and
+needs no workspace) and match the oracle within the tolerance every GEMM
+test uses (1e-4 of sum_k |w_hat * x_hat|).  No plain GEMM entry point may
+draw on the device's stream-ordered pool.  This file is named so that pytest
+collects it last.
 """
 import numpy as np
 import pytest
@@ -45,7 +46,7 @@ def test_noalloc_matches_allocating_gemm_on_two_calls_in_a_row():
         w, xq = _case(seed, m, n, k)
         ref, S = oracle_ref("q4K", w, xq, m, n, k)
         assert not np.isnan(got).any()
-        assert np.all(np.abs(got.astype(np.float64) - want) <= TOL * S)
+        np.testing.assert_array_equal(got, want)   # neither splits K: the same MMA operands and order
         assert_close(got, ref, S)
     assert q.plm_device_fault() == 0
 
@@ -82,8 +83,7 @@ def test_noalloc_limit_edge():
     rows = np.r_[0:64, m - 64:m]          # the first and last activation tiles against the oracle
     ref, S = oracle_ref("q4K", w, xq[rows], len(rows), n, k)
     assert_close(got[rows], ref, S)
-    # 469 output tiles fill the GPU, so plm_gemm_q4K does not split K either:
-    # the same launches, the same bits
+    # neither form splits K: the same operands and sums, the same bits
     np.testing.assert_array_equal(got, want)
     st = P.raw_status("plm_gemm_q4K_noalloc", wd.data_ptr(), xd.data_ptr(), y.data_ptr(), m + 1, n, k, None)
     assert st == P.PLM_ERR_UNSUPPORTED
@@ -115,18 +115,36 @@ def _pool_used_high():
     return val.value
 
 
-def test_noalloc_draws_nothing_from_the_pool():
+def _pool_alloc_free(nbytes):
+    """Takes nbytes from the default pool and gives them back (driver API,
+    legacy stream), to show that the high-water mark sees pool use."""
+    import ctypes
+    cu = ctypes.CDLL("libcuda.so.1")
+    ptr = ctypes.c_uint64(0)
+    assert cu.cuMemAllocAsync(ctypes.byref(ptr), ctypes.c_size_t(nbytes), None) == 0
+    assert cu.cuMemFreeAsync(ptr, None) == 0
+    assert cu.cuCtxSynchronize() == 0
+
+
+def test_no_gemm_entry_draws_from_the_pool():
     m, n, k = 300, 200, 2048
     w, xq = _case(45, m, n, k)
     wd, xd = dev(w), dev(xq)
+    w5 = dev(gen.q5K_blocks(45, 0, n, k))
+    w6 = dev(gen.q6K_blocks(45, 0, n, k))
+    wu = dev(gen.q4K_blocks(46, 0, n, k))
     y = torch.full((m, n), float("nan"), device="cuda")
     torch.cuda.synchronize()
     _pool_used_high()                     # reset the high-water mark
     for _ in range(2):
         q.plm_gemm_q4K_noalloc(wd, xd, y, m, n, k)
+        q.plm_gemm_q4K(wd, xd, y, m, n, k)
+        q.plm_gemm_q5K(w5, xd, y, m, n, k)
+        q.plm_gemm_q6K(w6, xd, y, m, n, k)
+        q.plm_gemm_q4K_swiglu(wd, wu, xd, y, m, n, k)
     torch.cuda.synchronize()
     assert _pool_used_high() == 0
-    # the measurement sees the allocating form's workspace
-    q.plm_gemm_q4K(wd, xd, y, m, n, k)
-    torch.cuda.synchronize()
-    assert _pool_used_high() >= q.plm_gemm_workspace_size("q4K", m, k)
+    assert q.plm_device_fault() == 0
+    # the measurement does see memory taken from the pool
+    _pool_alloc_free(1 << 20)
+    assert _pool_used_high() >= 1 << 20
