@@ -548,10 +548,12 @@ def run_extras(torch, q, peaks):
                                             for plain in (False, True) for m in (64, 512, 2048)]
     del wg, wu
     torch.cuda.empty_cache()
-    # the q2_K and q3_K rungs (decode GEMV; their GEMM entry runs the GEMV in 8-row passes)
+    # the q2_K and q3_K rungs: decode GEMV, and the tensor-core GEMM (workspace and plain forms)
     for fmt in ("q3K", "q2K"):
         ws, wb = T.weights(fmt, 5, 12288, 4096)
-        out["%s_12288x4096" % fmt] = [T.run(fmt, ws, wb, 12288, 4096, m, 10, 2) for m in (1, 8)]
+        out["%s_12288x4096" % fmt] = ([T.run(fmt, ws, wb, 12288, 4096, m, 10, 2) for m in (1, 8)] +
+                                      [T.run(fmt, ws, wb, 12288, 4096, m, 3, 2, layout=lay)
+                                       for lay in ("ggml", "plain") for m in (512, 2048)])
         del ws
     return out
 

@@ -206,8 +206,12 @@ plm_status plm_gemv_q6K_grouped(const plm_gemv_problem* problems, int64_t count,
  * Blocks are 4-byte (q2_K) / 2-byte (q3_K) aligned inside a row; w must be
  * 16-byte aligned.  Same contracts and errors as the q6_K entry points; the
  * sub-dot export writes the int32 16-weight group dots, [m][n][k/16].  The
- * GEMM entry points run the decode GEMV eight activation rows at a time (no
- * tensor-core path for these formats; no workspace, size 0).
+ * GEMM entry points run on the tensor cores for m >= 9 when a row of blocks
+ * is a multiple of 16 bytes (q2_K: k/256 % 4 == 0; q3_K: k/256 % 8 == 0):
+ * operands sc_g * q (q2_K, with the mins as a second contraction against the
+ * bsums) and (s_g - 32) * (q3 + 4) (q3_K, with the -4 (s_g - 32) bsum part as
+ * the second contraction), all exact in f16.  Other shapes run the decode
+ * GEMV eight activation rows at a time (no workspace, size 0).
  */
 plm_status plm_gemv_q2K(const void* w, const void* xq, float* y, int64_t m, int64_t n, int64_t k,
                         cudaStream_t stream);
@@ -318,7 +322,8 @@ plm_status plm_gemv_q4K_swiglu_grouped(const plm_swiglu_problem* problems, int64
  * a time; the per-block scales are applied in f32.  These plain forms widen
  * the activation codes inside the GEMM kernel, straight from xq into shared
  * memory: they need no workspace, allocate nothing and never split K.  For
- * m <= 8 (and for q2_K / q3_K) they run the decode GEMV eight rows at a time.
+ * m <= 8 (and q2_K / q3_K shapes without the tensor-core path, see above)
+ * they run the decode GEMV eight rows at a time.
  * Same buffers, layouts and tolerance as the GEMV; no limit on m.  For the
  * same (m, n, k) a plain call and a _ws call that does not split K give the
  * same bits.
@@ -359,7 +364,8 @@ plm_status plm_gemm_q4K_swiglu_ws(const void* w_gate, const void* w_up, const vo
 size_t plm_gemm_swiglu_workspace_size(int64_t m, int64_t n, int64_t k);
 
 /* Workspace bytes plm_gemm_qNK_ws needs (fmt = N: 2, 3, 4, 5, 6; q2_K and
- * q3_K need none) for m activation rows of length k: for m >= 9, the codes
+ * q3_K only on shapes with the tensor-core path, see above, else none) for m
+ * activation rows of length k: for m >= 9, the codes
  * widened to f16 (2*m*k bytes) and, per activation row and 256-value block,
  * 48 bytes of side data (the bsums as f16 pairs and d), each part rounded up
  * to 256 bytes.  0 when none is needed, and for invalid arguments. */

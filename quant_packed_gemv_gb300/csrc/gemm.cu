@@ -89,15 +89,29 @@ constexpr int AUXB = 48;
 // weight row) and activation side data; 0 for q6_K.
 // PWG: producer warpgroups (q6_K keeps one: its rows are read per thread,
 // whole, and need the registers).
+// WPITCH: bytes per weight row in a block slot, the TMA box width (q2_K,
+// q3_K: a 16-byte-aligned window around the block, an odd number of 16-byte
+// units so that the producers' 16-byte reads of 32 rows hit distinct banks).
 template <int FMT> struct GemmCfg;
+template <> struct GemmCfg<2> {   // q2_K: 84-byte blocks, window of 96 bytes at most
+    static constexpr int ATILES = 1, NSTAGE = 4, MINB = 2 * TILE_BYTES, BSLOTS = 2, WROW = Q2K_BYTES, PWG = 2;
+    static constexpr int WPITCH = 112;
+};
+template <> struct GemmCfg<3> {   // q3_K: 110-byte blocks, window of 124 bytes at most
+    static constexpr int ATILES = 1, NSTAGE = 4, MINB = 2 * TILE_BYTES, BSLOTS = 2, WROW = Q3K_BYTES, PWG = 2;
+    static constexpr int WPITCH = 144;
+};
 template <> struct GemmCfg<4> {
     static constexpr int ATILES = 1, NSTAGE = 4, MINB = 2 * TILE_BYTES, BSLOTS = 2, WROW = Q4K_BYTES, PWG = 2;
+    static constexpr int WPITCH = WROW;
 };
 template <> struct GemmCfg<5> {   // q5_K: q4_K's operands, a fifth bit per weight
     static constexpr int ATILES = 1, NSTAGE = 4, MINB = 2 * TILE_BYTES, BSLOTS = 2, WROW = Q5K_BYTES, PWG = 2;
+    static constexpr int WPITCH = WROW;
 };
 template <> struct GemmCfg<6> {
     static constexpr int ATILES = 2, NSTAGE = 3, MINB = 0, BSLOTS = 0, WROW = 0, PWG = 1;
+    static constexpr int WPITCH = 0;
 };
 
 template <int FMT, bool XIN>
@@ -492,6 +506,143 @@ __device__ __forceinline__ void qxK_row_stage_regs(const QxKRow<NRAW>& R, int c,
             v[4 * ch + 2 * h + 1] = h2_bits(__hfma2(bits_h2(l23 | 0x64006400u), slo, olo));
             v[16 + 4 * ch + 2 * h] = h2_bits(__hfma2(bits_h2(u01 | 0x64006400u), shi, ohi));
             v[16 + 4 * ch + 2 * h + 1] = h2_bits(__hfma2(bits_h2(u23 | 0x64006400u), shi, ohi));
+        }
+    }
+}
+
+// q2_K / q3_K rows (tensor-memory GEMM).  A block arrives in a window that
+// starts at the 16-byte boundary at or below it (the same skew for every row
+// of the tile when the weights are 16-byte aligned and a row of blocks is a
+// multiple of 16 bytes); the producer realigns it into words.  Stage c holds
+// weights 64c .. 64c+63, the 16-weight groups 4c .. 4c+3.  In both formats
+// group g takes the two low code bits of weight l from bits 2j, 2j+1 of
+// qs[32h + 16p + l], h = g / 8, j = (g % 8) / 2, p = g % 2: stage c reads
+// qs[32h .. 32h + 31] (h = c / 2), field j0 = 2 (c % 2) for groups 4c, 4c+1
+// (K 0..31) and j1 = j0 + 1 for groups 4c+2, 4c+3 (K 32..63).  The field is
+// used in place: (x & (3 << 2j)) | 0x6400 is f16 1024 + 4^j q, exact, and one
+// multiply-add with s / 4^j and -1024 s / 4^j (exact powers of two) gives
+// s * q with a single rounding of an exact result.
+//   q2_K: s = sc_g (4 bits), operand sc_g * q (<= 45); the min operand is the
+//         16 m_g against the 16 bsums, term d_x (d isum - dmin msum).
+//   q3_K: the code is q3 = u - 4, u = low2 + 4 hbit (hbit: bit 4h + j of
+//         hmask[16p + l]), moved in place to bit 2j + 2; operand S_g * u with
+//         S_g = s6_g - 32 (|S u| <= 224), and the -4 S_g bsum_g part goes
+//         through the min operand (4 S_g against the bsums, dmin = d).
+template <int NW>
+struct QlowRow {
+    uint32_t w[NW];   // the block's words (q3_K: the last word's high half lies past the block)
+    float d, dmin;
+};
+using Q2KRow = QlowRow<21>;
+using Q3KRow = QlowRow<28>;
+
+// the block's words from its window (WW words, 16-byte aligned in shared
+// memory) shifted down by sk bytes (sk even, the same for the whole tile)
+template <int NW, int WW>
+__device__ __forceinline__ void qlow_row_load(QlowRow<NW>& R, const uint8_t* win, int sk) {
+    static_assert(NW + 4 <= WW, "window");
+    uint32_t x[WW];
+#pragma unroll
+    for (int u = 0; u < WW / 4; ++u) {
+        const uint4 q = reinterpret_cast<const uint4*>(win)[u];
+        x[4 * u] = q.x; x[4 * u + 1] = q.y; x[4 * u + 2] = q.z; x[4 * u + 3] = q.w;
+    }
+    const uint32_t sh = (uint32_t)(sk & 2) * 8u;   // 0 or 16 bits
+    switch (sk >> 2) {
+#define PLM_QLOW_CASE(K)                                                        \
+    case K:                                                                     \
+        _Pragma("unroll") for (int i = 0; i < NW; ++i) R.w[i] = __funnelshift_r(x[i + K], x[i + K + 1], sh); \
+        break;
+        PLM_QLOW_CASE(0)
+        PLM_QLOW_CASE(1)
+        PLM_QLOW_CASE(2)
+        default:
+        _Pragma("unroll") for (int i = 0; i < NW; ++i) R.w[i] = __funnelshift_r(x[i + 3], x[i + 4], sh);
+        break;
+#undef PLM_QLOW_CASE
+    }
+}
+
+__device__ __forceinline__ void q2K_row_prepare(Q2KRow& R) {
+    R.d = half_bits_to_float(R.w[20] & 0xFFFFu);    // bytes 80, 81
+    R.dmin = half_bits_to_float(R.w[20] >> 16);     // bytes 82, 83
+}
+
+__device__ __forceinline__ void q3K_row_prepare(Q3KRow& R) {
+    R.d = half_bits_to_float(R.w[27] & 0xFFFFu);    // bytes 108, 109
+    R.dmin = R.d;                                   // the -4 S bsum part
+}
+
+// q3_K six-bit scale s6_g of group g (0..15) from the 12 packed bytes
+// (words 24..26): low four bits from byte g % 8 (nibble g / 8), top two
+// from byte 8 + g % 4 (bits 2 (g / 4), +1)
+__device__ __forceinline__ uint32_t q3K_s6(const Q3KRow& R, int g) {
+    const int lb = g & 7, hb = 8 + (g & 3);
+    const uint32_t lo = (R.w[24 + (lb >> 2)] >> (8 * (lb & 3) + 4 * (g >> 3))) & 15u;
+    const uint32_t hi = (R.w[24 + (hb >> 2)] >> (8 * (hb & 3) + 2 * (g >> 2))) & 3u;
+    return lo | (hi << 4);
+}
+
+// f16 pair of two small non-negative integers a, b < 1024 (exact)
+__device__ __forceinline__ __half2 small_pair(uint32_t a, uint32_t b) {
+    return __hsub2(bits_h2(0x64006400u | a | (b << 16)), bits_h2(0x64006400u));
+}
+
+// the min operand's first 16 K positions as eight f16 pairs (groups 2i, 2i + 1)
+__device__ __forceinline__ void q2K_min_pairs(const Q2KRow& R, uint32_t (&mv)[8]) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t w = R.w[i >> 1] >> (16 * (i & 1));   // scale bytes 2i, 2i + 1
+        mv[i] = h2_bits(small_pair((w >> 4) & 15u, (w >> 12) & 15u));
+    }
+}
+
+__device__ __forceinline__ void q3K_min_pairs(const Q3KRow& R, uint32_t (&mv)[8]) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {   // 4 S = 4 s6 - 128, exact
+        const __half2 s = small_pair(q3K_s6(R, 2 * i), q3K_s6(R, 2 * i + 1));
+        mv[i] = h2_bits(__hfma2(s, bits_h2(0x44004400u), bits_h2(0xD800D800u)));   // x 4, - 128
+    }
+}
+
+// f16 of 4^-j and of -1024 * 4^-j
+__device__ __forceinline__ uint32_t pow4_inv_bits(int j) { return 0x3C00u - 0x0800u * (uint32_t)j; }
+__device__ __forceinline__ uint32_t neg1024_pow4_inv_bits(int j) { return 0xE400u - 0x0800u * (uint32_t)j; }
+
+template <int FMT, int NW>
+__device__ __forceinline__ void qlow_row_stage_regs(const QlowRow<NW>& R, int c, uint32_t (&v)[32]) {
+    const int h = c >> 1, j0 = 2 * (c & 1);
+#pragma unroll
+    for (int gg = 0; gg < 4; ++gg) {
+        const int g = 4 * c + gg, j = j0 + (gg >> 1), p = gg & 1;
+        // the group's multiply-add constants
+        __half2 sg;
+        if constexpr (FMT == 2) {
+            const uint32_t sc = (R.w[g >> 2] >> (8 * (g & 3))) & 15u;
+            sg = small_pair(sc, sc);
+        } else {
+            const uint32_t s6 = q3K_s6(R, g);
+            sg = __hsub2(bits_h2(0x64006400u | s6 | (s6 << 16)), bits_h2(0x64206420u));   // s6 - 32
+        }
+        const uint32_t m1 = pow4_inv_bits(j), m2 = neg1024_pow4_inv_bits(j);
+        const __half2 mul = __hmul2(sg, bits_h2(m1 | (m1 << 16)));
+        const __half2 add = __hmul2(sg, bits_h2(m2 | (m2 << 16)));
+        const uint32_t qmask = 0x00030003u << (2 * j);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int qwi = (FMT == 2 ? 4 : 8) + 8 * h + 4 * p + u;   // qs at byte 16 (q2_K) or 32 (q3_K)
+            const uint32_t qw = R.w[qwi];
+            uint32_t x01 = __byte_perm(qw, 0, 0x4140) & qmask, x23 = __byte_perm(qw, 0, 0x4342) & qmask;
+            if constexpr (FMT == 3) {
+                const uint32_t hw = R.w[4 * p + u];                 // hmask bytes 16p + 4u ..
+                const uint32_t h01 = __byte_perm(hw, 0, 0x4140), h23 = __byte_perm(hw, 0, 0x4342);
+                const int from = 4 * h + j, to = 2 * j + 2;         // hbit to bit 2j + 2 of each half
+                const uint32_t hmask = 0x00010001u << to;
+                x01 |= (to >= from ? h01 << (to - from) : h01 >> (from - to)) & hmask;
+                x23 |= (to >= from ? h23 << (to - from) : h23 >> (from - to)) & hmask;
+            }
+            v[8 * gg + 2 * u] = h2_bits(__hfma2(bits_h2(x01 | 0x64006400u), mul, add));
+            v[8 * gg + 2 * u + 1] = h2_bits(__hfma2(bits_h2(x23 | 0x64006400u), mul, add));
         }
     }
 }
@@ -1003,7 +1154,7 @@ struct TmSmem {
     static constexpr int RING = 0;                                            // B tiles, 4 x 16 KB
     static constexpr int MIN = RING + TM_NSTAGE * TILE_BYTES;                 // 2 x 16 KB
     static constexpr int SCL = MIN + 2 * TILE_BYTES;                          // 2 x (d, dmin, dx) x 128 f32
-    static constexpr int WT = GT * GemmCfg<FMT>::WROW;
+    static constexpr int WT = GT * GemmCfg<FMT>::WPITCH;
     static constexpr int BTX = WT + GT * AUXB;
     static constexpr int BSLOT = (BTX + 1023) & ~1023;
     static constexpr int BRING = (SCL + 2 * 3 * GT * 4 + 1023) & ~1023;
@@ -1105,7 +1256,11 @@ __global__ void __launch_bounds__(tm_threads(XIN), 1) gemm_tm_kernel(const __gri
         const int t = tid & (GT - 1);          // weight row (and activation row) of the tile
         const int half = warp >> 2;            // stages 2 half, 2 half + 1 of every block
         const uint32_t alane = (uint32_t)((warp & 3) * 32) << 16;
-        using Row = typename std::conditional<FMT == 5, Q5KRow, Q4KRow>::type;
+        using Row = typename std::conditional<
+            FMT == 2, Q2KRow,
+            typename std::conditional<FMT == 3, Q3KRow,
+                                      typename std::conditional<FMT == 5, Q5KRow, Q4KRow>::type>::type>::type;
+        constexpr int WROW = GemmCfg<FMT>::WROW, WPITCH = GemmCfg<FMT>::WPITCH;
         Row R;
         int nissued = 0;
         auto issue_block = [&](int bb) {   // thread 0: block bb of the tile into slot bb % 2
@@ -1113,7 +1268,7 @@ __global__ void __launch_bounds__(tm_threads(XIN), 1) gemm_tm_kernel(const __gri
             const int s = bb & 1;
             uint8_t* dst = sm + L::BRING + s * L::BSLOT;
             mbar_arrive_expect_tx(&bfull[s], (uint32_t)(XIN ? L::WT : L::BTX));
-            tma_load_2d(dst, &wmap, (kb0 + bb) * GemmCfg<FMT>::WROW, r0, &bfull[s]);
+            tma_load_2d(dst, &wmap, ((kb0 + bb) * WROW) & ~15, r0, &bfull[s]);   // the block's 16-byte window
             if constexpr (!XIN) tma_load_2d(dst + L::WT, &amap, (kb0 + bb) * AUXB, i0, &bfull[s]);
         };
         if (tid == 0)
@@ -1128,10 +1283,14 @@ __global__ void __launch_bounds__(tm_threads(XIN), 1) gemm_tm_kernel(const __gri
                     const int s = gb & 1;
                     if (!mbar_wait(&bfull[s], (uint32_t)(gb >> 1) & 1u)) { ok = false; break; }
                     const uint8_t* slot = sm + L::BRING + s * L::BSLOT;
-                    constexpr int NRAW = GemmCfg<FMT>::WROW / 16;
+                    if constexpr (FMT <= 3) {
+                        qlow_row_load<sizeof(R.w) / 4, WPITCH / 4>(R, slot + t * WPITCH, ((kb0 + b) * WROW) & 15);
+                    } else {
+                        constexpr int NRAW = WROW / 16;
 #pragma unroll
-                    for (int u = 0; u < NRAW; ++u)
-                        R.raw[u] = reinterpret_cast<const uint4*>(slot + t * GemmCfg<FMT>::WROW)[u];
+                        for (int u = 0; u < NRAW; ++u)
+                            R.raw[u] = reinterpret_cast<const uint4*>(slot + t * WPITCH)[u];
+                    }
                     const uint4* ax = reinterpret_cast<const uint4*>(slot + L::WT + t * AUXB);
                     const uint4 a0 = ax[0], a1 = ax[1], a2 = ax[2];
                     bsw[0] = a0.x; bsw[1] = a0.y; bsw[2] = a0.z; bsw[3] = a0.w;
@@ -1141,7 +1300,12 @@ __global__ void __launch_bounds__(tm_threads(XIN), 1) gemm_tm_kernel(const __gri
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&bempty[s]);
                 }
-                q4K_row_prepare(R);
+                if constexpr (FMT == 2)
+                    q2K_row_prepare(R);
+                else if constexpr (FMT == 3)
+                    q3K_row_prepare(R);
+                else
+                    q4K_row_prepare(R);
                 if (gb >= 2) {   // slot j's min operands and scales are free again
                     ok = mbar_wait(&minempty[j], ((gb >> 1) - 1) & 1) && mbar_wait(&tempty[j], ((gb >> 1) - 1) & 1);
                     if (!ok) break;
@@ -1150,10 +1314,16 @@ __global__ void __launch_bounds__(tm_threads(XIN), 1) gemm_tm_kernel(const __gri
                     // min operands: K 0..15 the weight row's mins m_(g/2); K 16..31 the activation row's bsums
                     uint8_t* mt = sm + L::MIN + j * TILE_BYTES;
                     uint32_t mv[8];
+                    if constexpr (FMT == 2) {
+                        q2K_min_pairs(R, mv);
+                    } else if constexpr (FMT == 3) {
+                        q3K_min_pairs(R, mv);
+                    } else {
 #pragma unroll
-                    for (int g = 0; g < 8; ++g) {
-                        const uint32_t mm = (uint32_t)R.mins[g];
-                        mv[g] = h2_bits(__hsub2(bits_h2(0x64006400u | mm | (mm << 16)), bits_h2(0x64006400u)));
+                        for (int g = 0; g < 8; ++g) {
+                            const uint32_t mm = (uint32_t)R.mins[g];
+                            mv[g] = h2_bits(__hsub2(bits_h2(0x64006400u | mm | (mm << 16)), bits_h2(0x64006400u)));
+                        }
                     }
                     *reinterpret_cast<uint4*>(mt + sw128_chunk(t, 0)) = make_uint4(mv[0], mv[1], mv[2], mv[3]);
                     *reinterpret_cast<uint4*>(mt + sw128_chunk(t, 1)) = make_uint4(mv[4], mv[5], mv[6], mv[7]);
@@ -1178,7 +1348,10 @@ __global__ void __launch_bounds__(tm_threads(XIN), 1) gemm_tm_kernel(const __gri
                         tma_load_2d(sm + L::RING + c * TILE_BYTES, &xmap, (kb0 + b) * QK + c * KS, i0, &full[c]);
                     }
                     uint32_t v[32];
-                    qxK_row_stage_regs<FMT>(R, c, v);
+                    if constexpr (FMT <= 3)
+                        qlow_row_stage_regs<FMT>(R, c, v);
+                    else
+                        qxK_row_stage_regs<FMT>(R, c, v);
                     tmem_st32(tmem + alane + TM_A + 32 * c, v);
                     return true;
                 };
@@ -1540,13 +1713,14 @@ static cudaError_t gemm_tc(const uint8_t* w, const uint8_t* xq, float* y, long l
                 return cudaErrorInvalidValue;
         }
     }
-    // q4_K / q5_K: the raw weight blocks (rows of nb * WROW bytes; a box is
-    // one block of 128 rows, rows past n read as zeros)
+    // q2_K .. q5_K: the raw weight blocks (rows of nb * WROW bytes; a box is
+    // one block's 16-byte-aligned window, WPITCH bytes, of 128 rows; rows past
+    // n and bytes past a row's end read as zeros)
     if constexpr (GemmCfg<FMT>::BSLOTS > 0) {
         constexpr int WROW = GemmCfg<FMT>::WROW;
         const cuuint64_t wd[2] = {(cuuint64_t)nb * WROW, (cuuint64_t)n};
         const cuuint64_t ws_[1] = {(cuuint64_t)nb * WROW};
-        const cuuint32_t wb[2] = {(cuuint32_t)WROW, (cuuint32_t)GT};
+        const cuuint32_t wb[2] = {(cuuint32_t)GemmCfg<FMT>::WPITCH, (cuuint32_t)GT};
         if (enc(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(w), wd, ws_, wb, estr,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
@@ -1573,7 +1747,7 @@ static cudaError_t gemm_tc(const uint8_t* w, const uint8_t* xq, float* y, long l
         return launch_kernel(kernel, grid, dim3(threads), smem, stream, map, wmap, amap, A);
     };
     cudaError_t e;
-    if constexpr (FMT == 4 || FMT == 5) {
+    if constexpr (FMT != 6) {
         if (gate) {
             if (FMT != 4 || !xin) return cudaErrorInvalidValue;
             e = run(gemm_tm_kernel<4, true, true>, tm_threads(true), TmSmem<4, true>::ALLOC);
@@ -1600,17 +1774,29 @@ static cudaError_t gemm_tc(const uint8_t* w, const uint8_t* xq, float* y, long l
 // time) serve the GEMM entry point.
 constexpr long long GEMM_MIN_M = 9;
 
-// q4_K, q5_K and q6_K prefill on the tensor cores; q2_K and q3_K (and any
-// m below GEMM_MIN_M) run the decode GEMV eight activation rows at a time.
-static bool gemm_on_tensor_cores(int fmt, long long m) {
-    return (fmt == 4 || fmt == 5 || fmt == 6) && m >= GEMM_MIN_M && m <= 0x7FFFFFFF;
+// Prefill on the tensor cores from GEMM_MIN_M rows: q4_K, q5_K and q6_K
+// always; q2_K and q3_K when a row of blocks is a multiple of 16 bytes (nb %
+// 4 == 0, resp. nb % 8 == 0: their blocks come by TMA in 16-byte windows)
+// and the weights are 16-byte aligned.  Otherwise the decode GEMV runs eight
+// activation rows at a time.
+static bool gemm_tc_shape(int fmt, long long m, int k) {
+    const int nb = k / QK;
+    const bool fmt_ok = fmt == 4 || fmt == 5 || fmt == 6 || (fmt == 2 && nb % 4 == 0) || (fmt == 3 && nb % 8 == 0);
+    return fmt_ok && m >= GEMM_MIN_M && m <= 0x7FFFFFFF;
+}
+static bool gemm_on_tensor_cores(int fmt, long long m, int k, const uint8_t* w) {
+    return gemm_tc_shape(fmt, m, k) && (fmt > 3 || ((uintptr_t)w & 15u) == 0);
 }
 
 static cudaError_t gemm_tc_any(int fmt, const uint8_t* w, const uint8_t* xq, float* y, long long m, int n, int k,
                                void* ws, size_t ws_bytes, cudaStream_t stream) {
-    return fmt == 4 ? gemm_tc<4>(w, xq, y, m, n, k, ws, ws_bytes, nullptr, stream)
-           : fmt == 5 ? gemm_tc<5>(w, xq, y, m, n, k, ws, ws_bytes, nullptr, stream)
-                      : gemm_tc<6>(w, xq, y, m, n, k, ws, ws_bytes, nullptr, stream);
+    switch (fmt) {
+        case 2: return gemm_tc<2>(w, xq, y, m, n, k, ws, ws_bytes, nullptr, stream);
+        case 3: return gemm_tc<3>(w, xq, y, m, n, k, ws, ws_bytes, nullptr, stream);
+        case 4: return gemm_tc<4>(w, xq, y, m, n, k, ws, ws_bytes, nullptr, stream);
+        case 5: return gemm_tc<5>(w, xq, y, m, n, k, ws, ws_bytes, nullptr, stream);
+        default: return gemm_tc<6>(w, xq, y, m, n, k, ws, ws_bytes, nullptr, stream);
+    }
 }
 
 // Decode GEMV passes of at most eight activation rows (the GEMM entry points
@@ -1628,8 +1814,8 @@ static cudaError_t gemm_by_gemv(int fmt, const uint8_t* w, const uint8_t* xq, fl
 
 cudaError_t launch_gemm_ws(int fmt, const uint8_t* w, const uint8_t* xq, float* y, long long m, int n, int k,
                            void* ws, size_t ws_bytes, cudaStream_t stream) {
-    if (!gemm_on_tensor_cores(fmt, m)) return gemm_by_gemv(fmt, w, xq, y, m, n, k, stream);
-    if (!ws || ws_bytes < gemm_workspace_bytes(m, k)) return cudaErrorInvalidValue;
+    if (gemm_tc_shape(fmt, m, k) && (!ws || ws_bytes < gemm_workspace_bytes(m, k))) return cudaErrorInvalidValue;
+    if (!gemm_on_tensor_cores(fmt, m, k, w)) return gemm_by_gemv(fmt, w, xq, y, m, n, k, stream);
     return gemm_tc_any(fmt, w, xq, y, m, n, k, ws, ws_bytes, stream);
 }
 
@@ -1641,19 +1827,19 @@ cudaError_t launch_gemm_ws(int fmt, const uint8_t* w, const uint8_t* xq, float* 
 static size_t pair_u_bytes(long long m, int n) { return (((size_t)m * n * 4) + 255) & ~(size_t)255; }
 
 size_t gemm_swiglu_workspace_need(long long m, int n, int k) {
-    if (!gemm_on_tensor_cores(4, m)) return 0;
+    if (!gemm_tc_shape(4, m, k)) return 0;
     return pair_u_bytes(m, n) + gemm_workspace_need_split(4, m, n, k);
 }
 
 // the least workspace the _ws pair accepts (no K split)
 size_t gemm_swiglu_workspace_min(long long m, int n, int k) {
-    if (!gemm_on_tensor_cores(4, m)) return 0;
+    if (!gemm_tc_shape(4, m, k)) return 0;
     return pair_u_bytes(m, n) + gemm_workspace_bytes(m, k);
 }
 
 cudaError_t launch_gemm_q4K_swiglu_ws(const uint8_t* w_gate, const uint8_t* w_up, const uint8_t* xq, float* h,
                                       long long m, int n, int k, void* ws, size_t ws_bytes, cudaStream_t stream) {
-    if (gemm_on_tensor_cores(4, m)) {
+    if (gemm_tc_shape(4, m, k)) {
         const size_t ub = pair_u_bytes(m, n);
         if (!ws || ws_bytes < ub + gemm_workspace_bytes(m, k)) return cudaErrorInvalidValue;
         float* u = static_cast<float*>(ws);
@@ -1692,18 +1878,18 @@ cudaError_t launch_gemm_q4K_swiglu_ws(const uint8_t* w_gate, const uint8_t* w_up
 // not split K).
 cudaError_t launch_gemm_q4K_swiglu(const uint8_t* w_gate, const uint8_t* w_up, const uint8_t* xq, float* h,
                                    long long m, int n, int k, cudaStream_t stream) {
-    if (!gemm_on_tensor_cores(4, m)) return launch_gemm_q4K_swiglu_ws(w_gate, w_up, xq, h, m, n, k, nullptr, 0, stream);
+    if (!gemm_tc_shape(4, m, k)) return launch_gemm_q4K_swiglu_ws(w_gate, w_up, xq, h, m, n, k, nullptr, 0, stream);
     cudaError_t e = gemm_tc<4>(w_gate, xq, h, m, n, k, nullptr, 0, nullptr, stream);
     if (e != cudaSuccess) return e;
     return gemm_tc<4>(w_up, xq, h, m, n, k, nullptr, 0, h, stream);
 }
 
 size_t gemm_workspace_need(int fmt, long long m, int k) {
-    return gemm_on_tensor_cores(fmt, m) ? gemm_workspace_bytes(m, k) : 0;
+    return gemm_tc_shape(fmt, m, k) ? gemm_workspace_bytes(m, k) : 0;
 }
 
 size_t gemm_workspace_need_split(int fmt, long long m, int n, int k) {
-    if (!gemm_on_tensor_cores(fmt, m)) return 0;
+    if (!gemm_tc_shape(fmt, m, k)) return 0;
     return gemm_workspace_bytes(m, k) + gemm_split_bytes(m, n, gemm_splits(m, n, k / QK));
 }
 
@@ -1711,7 +1897,7 @@ size_t gemm_workspace_need_split(int fmt, long long m, int n, int k) {
 // themselves and never split K; nothing is allocated.
 cudaError_t launch_gemm(int fmt, const uint8_t* w, const uint8_t* xq, float* y, long long m, int n, int k,
                         cudaStream_t stream) {
-    if (!gemm_on_tensor_cores(fmt, m)) return gemm_by_gemv(fmt, w, xq, y, m, n, k, stream);
+    if (!gemm_on_tensor_cores(fmt, m, k, w)) return gemm_by_gemv(fmt, w, xq, y, m, n, k, stream);
     return gemm_tc_any(fmt, w, xq, y, m, n, k, nullptr, 0, stream);
 }
 

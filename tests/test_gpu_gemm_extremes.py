@@ -100,8 +100,7 @@ def test_gemm_adversarial_extremes(fmt, m):
     wd, xd = dev(w), dev(xq)
     unsplit = q.plm_gemm_workspace_size(fmt, m, k)
     split = q.plm_gemm_workspace_size_split(fmt, m, n, k)
-    if fmt in ("q4K", "q5K", "q6K"):
-        assert split > unsplit > 0            # the tensor-core path, both K layouts
+    assert split > unsplit > 0                # the tensor-core path (k = 2048 qualifies q2_K, q3_K too), both K layouts
     outs = []
     for need in sorted({unsplit, split}):
         ws = torch.empty(max(need, 256), dtype=torch.uint8, device="cuda")
