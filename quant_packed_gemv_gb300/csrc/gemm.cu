@@ -183,6 +183,12 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
                  : "r"(taddr));
 }
 
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+}
+
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
                  "%14,%15}, [%16];"
@@ -1483,34 +1489,26 @@ __global__ void __launch_bounds__(tm_threads(XIN), 1) gemm_tm_kernel(const __gri
                 const float* sj = scl + j * 3 * GT;
                 const float dw = sj[row], dmw = sj[GT + row];
                 const float* dxv = sj + 2 * GT + 64 * chalf;
-                // D2 first (- dmin * dx * msum), then release it for the next block's min MMA
+                // D1 and D2 together: + dx * (d * isum - dmin * msum)
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    uint32_t v[16];
-                    tmem_ld16(tl + TM_D2 + 64 * chalf + 16 * cc, v);
+                for (int cc = 0; cc < 8; ++cc) {
+                    uint32_t v1[8], v2[8];
+                    tmem_ld8(tl + TM_D2 + 64 * chalf + 8 * cc, v2);
+                    tmem_ld8(tl + TM_D1 + 128 * j + 64 * chalf + 8 * cc, v1);
                     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-                    for (int c = 0; c < 16; ++c)
-                        acc[16 * cc + c] = __fmaf_rn(-__fmul_rn(dmw, dxv[16 * cc + c]), __uint_as_float(v[c]),
-                                                     acc[16 * cc + c]);
+                    for (int c = 0; c < 8; ++c) {
+                        const float t = __fmaf_rn(dw, __uint_as_float(v1[c]), -__fmul_rn(dmw, __uint_as_float(v2[c])));
+                        acc[8 * cc + c] = __fmaf_rn(dxv[8 * cc + c], t, acc[8 * cc + c]);
+                    }
                 }
+                // both accumulators read: D2 for the next block's min MMA, D1 for the block after
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(d2free);
-                // D1: + d * dx * isum
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    uint32_t v[16];
-                    tmem_ld16(tl + TM_D1 + 128 * j + 64 * chalf + 16 * cc, v);
-                    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-                    for (int c = 0; c < 16; ++c)
-                        acc[16 * cc + c] = __fmaf_rn(__fmul_rn(dw, dxv[16 * cc + c]), __uint_as_float(v[c]),
-                                                     acc[16 * cc + c]);
+                if (lane == 0) {
+                    mbar_arrive(d2free);
+                    mbar_arrive(&tempty[j]);
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&tempty[j]);
             }
             const int r = r0 + row;
             float* out = A.part ? A.part + (size_t)blockIdx.z * A.m * A.n : A.y;
