@@ -516,6 +516,94 @@ __device__ __forceinline__ void qxK_row_stage_regs(const QxKRow<NRAW>& R, int c,
     }
 }
 
+// One producer warpgroup's share of a q4_K / q5_K row (tensor-memory GEMM):
+// the header and the qs (q5_K: and qh) of its two chunks 2h, 2h + 1 with
+// their f16x2 constants, so a warpgroup holds half the block in registers.
+template <int FMT>
+struct QxKHalf {
+    uint4 hdr;
+    uint4 qs[4];      // chunk 2h: qs[0..1], chunk 2h + 1: qs[2..3]
+    uint4 qh[2];      // q5_K: the fifth bits of all 256 weights
+    float d, dmin;
+    uint32_t sc_lo2[2], off_lo2[2], sc_hi2[2], off_hi2[2];
+};
+
+template <int FMT>
+__device__ __forceinline__ void qxK_half_load(QxKHalf<FMT>& R, const uint8_t* row, int half) {
+    const uint4* p = reinterpret_cast<const uint4*>(row);
+    constexpr int QW = FMT == 5 ? 3 : 1;   // first qs word (q5_K: after qh[32])
+    R.hdr = p[0];
+    if constexpr (FMT == 5) {
+        R.qh[0] = p[1];
+        R.qh[1] = p[2];
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) R.qs[u] = p[QW + 4 * half + u];
+}
+
+// d, dmin and the multiply-add constants of chunks 2h, 2h + 1 (as q4K_row_prepare)
+template <int FMT>
+__device__ __forceinline__ void qxK_half_prepare(QxKHalf<FMT>& R, int half) {
+    const uint4 hdr = R.hdr;
+    R.d = half_bits_to_float(hdr.x);
+    R.dmin = half_bits_to_float(hdr.x >> 16);
+    const uint32_t scw = half ? ((hdr.w & 0x0F0F0F0Fu) | ((hdr.y >> 2) & 0x30303030u)) : (hdr.y & 0x3F3F3F3Fu);
+#pragma unroll
+    for (int cl = 0; cl < 2; ++cl) {
+        const uint32_t slo = (scw >> (16 * cl)) & 0xFFu, shi = (scw >> (16 * cl + 8)) & 0xFFu;
+        const __half2 lo2 = __hsub2(bits_h2(0x64006400u | slo | (slo << 16)), bits_h2(0x64006400u));
+        const __half2 hi2 = __hsub2(bits_h2(0x64006400u | shi | (shi << 16)), bits_h2(0x64006400u));
+        R.sc_lo2[cl] = h2_bits(lo2);
+        R.off_lo2[cl] = h2_bits(__hmul2(lo2, bits_h2(0xE400E400u)));   // x (-1024)
+        R.sc_hi2[cl] = h2_bits(__hmul2(hi2, bits_h2(0x2C002C00u)));    // x 1/16
+        R.off_hi2[cl] = h2_bits(__hmul2(hi2, bits_h2(0xD400D400u)));   // x (-64)
+    }
+}
+
+// the min operand's first 16 K positions: m_(g/2) for K g (f16 pairs)
+__device__ __forceinline__ void qxK_min_pairs(const uint4 hdr, uint32_t (&mv)[8]) {
+    const uint32_t m_a = hdr.z & 0x3F3F3F3Fu;
+    const uint32_t m_b = ((hdr.w >> 4) & 0x0F0F0F0Fu) | ((hdr.z >> 2) & 0x30303030u);
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+        const uint32_t mm = ((g < 4 ? m_a : m_b) >> (8 * (g & 3))) & 0xFFu;
+        mv[g] = h2_bits(__hsub2(bits_h2(0x64006400u | mm | (mm << 16)), bits_h2(0x64006400u)));
+    }
+}
+
+// chunk c = 2h + CL into the 32 tensor-memory columns of the row (as qxK_row_stage_regs)
+template <int FMT, int CL>
+__device__ __forceinline__ void qxK_half_stage_regs(const QxKHalf<FMT>& R, int c, uint32_t (&v)[32]) {
+    const uint4 qa = R.qs[2 * CL], qb = R.qs[2 * CL + 1];
+    const uint32_t q[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+    const __half2 slo = bits_h2(R.sc_lo2[CL]), olo = bits_h2(R.off_lo2[CL]);
+    const __half2 shi = bits_h2(R.sc_hi2[CL]), ohi = bits_h2(R.off_hi2[CL]);
+#pragma unroll
+    for (int ch = 0; ch < 4; ++ch) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint32_t w = q[2 * ch + h];
+            const uint32_t x01 = __byte_perm(w, 0, 0x4140), x23 = __byte_perm(w, 0, 0x4342);
+            uint32_t l01 = x01 & 0x000F000Fu, l23 = x23 & 0x000F000Fu;
+            uint32_t u01 = x01 & 0x00F000F0u, u23 = x23 & 0x00F000F0u;
+            if constexpr (FMT == 5) {
+                const uint4 qhv = R.qh[ch >> 1];
+                const uint32_t qw[4] = {qhv.x, qhv.y, qhv.z, qhv.w};
+                const uint32_t b = qw[2 * (ch & 1) + h];
+                const uint32_t h01 = __byte_perm(b, 0, 0x4140), h23 = __byte_perm(b, 0, 0x4342);
+                l01 |= ((h01 >> (2 * c)) & 0x00010001u) << 4;
+                l23 |= ((h23 >> (2 * c)) & 0x00010001u) << 4;
+                u01 |= ((h01 >> (2 * c + 1)) & 0x00010001u) << 8;
+                u23 |= ((h23 >> (2 * c + 1)) & 0x00010001u) << 8;
+            }
+            v[4 * ch + 2 * h] = h2_bits(__hfma2(bits_h2(l01 | 0x64006400u), slo, olo));
+            v[4 * ch + 2 * h + 1] = h2_bits(__hfma2(bits_h2(l23 | 0x64006400u), slo, olo));
+            v[16 + 4 * ch + 2 * h] = h2_bits(__hfma2(bits_h2(u01 | 0x64006400u), shi, ohi));
+            v[16 + 4 * ch + 2 * h + 1] = h2_bits(__hfma2(bits_h2(u23 | 0x64006400u), shi, ohi));
+        }
+    }
+}
+
 // q2_K / q3_K rows (tensor-memory GEMM).  A block arrives in a window that
 // starts at the 16-byte boundary at or below it (the same skew for every row
 // of the tile when the weights are 16-byte aligned and a row of blocks is a
@@ -611,23 +699,114 @@ __device__ __forceinline__ void q3K_min_pairs(const Q3KRow& R, uint32_t (&mv)[8]
     }
 }
 
+// One producer warpgroup's share of a q2_K / q3_K row: the qs words of its
+// half h (bytes 32h .. 32h + 31), the scale words (all of them: the min
+// operand needs every group's), q3_K's hmask, and the d word.  Each range is
+// read as whole 16-byte units of the window (at a runtime offset) and
+// shifted down by the tile-uniform skew sk.
+template <int FMT>
+struct QlowHalf {
+    uint32_t qs[8];
+    uint32_t sc[4];   // q2_K: scale bytes 0..15; q3_K: words 24..26 (sc[3] unused)
+    uint32_t hm[8];   // q3_K: hmask[32]
+    float d, dmin;
+};
+
+// words [first, first + N) of the block: window units from first / 4 on
+// (first a multiple of 4), then down by sk bytes
+template <int N>
+__device__ __forceinline__ void qlow_words(const uint8_t* row, int first, int sk, uint32_t (&out)[N]) {
+    constexpr int U = (N + 4 + 3) / 4;   // units covering N + 1 words past a shift of up to 3 words
+    uint32_t x[4 * U];
+    const uint4* p = reinterpret_cast<const uint4*>(row) + (first >> 2);
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const uint4 q = p[u];
+        x[4 * u] = q.x; x[4 * u + 1] = q.y; x[4 * u + 2] = q.z; x[4 * u + 3] = q.w;
+    }
+    const uint32_t sh = (uint32_t)(sk & 2) * 8u;   // 0 or 16 bits
+    switch (sk >> 2) {
+        case 0:
+#pragma unroll
+            for (int i = 0; i < N; ++i) out[i] = __funnelshift_r(x[i], x[i + 1], sh);
+            break;
+        case 1:
+#pragma unroll
+            for (int i = 0; i < N; ++i) out[i] = __funnelshift_r(x[i + 1], x[i + 2], sh);
+            break;
+        case 2:
+#pragma unroll
+            for (int i = 0; i < N; ++i) out[i] = __funnelshift_r(x[i + 2], x[i + 3], sh);
+            break;
+        default:
+#pragma unroll
+            for (int i = 0; i < N; ++i) out[i] = __funnelshift_r(x[i + 3], x[i + 4], sh);
+            break;
+    }
+}
+
+template <int FMT>
+__device__ __forceinline__ void qlow_half_load(QlowHalf<FMT>& R, const uint8_t* row, int sk, int half) {
+    if constexpr (FMT == 2) {
+        qlow_words<8>(row, 4 + 8 * half, sk, R.qs);
+        qlow_words<4>(row, 0, sk, R.sc);
+        uint32_t dw[1];
+        qlow_words<1>(row, 20, sk, dw);
+        R.d = half_bits_to_float(dw[0] & 0xFFFFu);    // bytes 80, 81
+        R.dmin = half_bits_to_float(dw[0] >> 16);     // bytes 82, 83
+    } else {
+        qlow_words<8>(row, 8 + 8 * half, sk, R.qs);
+        qlow_words<8>(row, 0, sk, R.hm);
+        uint32_t sw[4];
+        qlow_words<4>(row, 24, sk, sw);               // scales (words 24..26), d (word 27)
+        R.sc[0] = sw[0]; R.sc[1] = sw[1]; R.sc[2] = sw[2]; R.sc[3] = 0;
+        R.d = half_bits_to_float(sw[3] & 0xFFFFu);    // bytes 108, 109
+        R.dmin = R.d;                                 // the -4 S bsum part
+    }
+}
+
+// q3_K six-bit scale of group g = 8 gh + gl (gl = g % 8 known at compile time)
+__device__ __forceinline__ uint32_t q3K_s6h(const uint32_t (&sc)[4], int gl, int gh) {
+    const int g4 = gl & 3;
+    const uint32_t lo = (sc[gl >> 2] >> (8 * g4 + 4 * gh)) & 15u;
+    const uint32_t hi = (sc[2] >> (8 * g4 + 2 * (2 * gh + (gl >> 2)))) & 3u;
+    return lo | (hi << 4);
+}
+
+template <int FMT>
+__device__ __forceinline__ void qlow_half_min_pairs(const QlowHalf<FMT>& R, uint32_t (&mv)[8]) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {   // groups 2i, 2i + 1
+        if constexpr (FMT == 2) {
+            const uint32_t w = R.sc[i >> 1] >> (16 * (i & 1));
+            mv[i] = h2_bits(small_pair((w >> 4) & 15u, (w >> 12) & 15u));
+        } else {   // 4 S = 4 s6 - 128, exact
+            const int g0 = 2 * i, g1 = 2 * i + 1;
+            const __half2 sp = small_pair(q3K_s6h(R.sc, g0 & 7, g0 >> 3), q3K_s6h(R.sc, g1 & 7, g1 >> 3));
+            mv[i] = h2_bits(__hfma2(sp, bits_h2(0x44004400u), bits_h2(0xD800D800u)));
+        }
+    }
+}
+
 // f16 of 4^-j and of -1024 * 4^-j
 __device__ __forceinline__ uint32_t pow4_inv_bits(int j) { return 0x3C00u - 0x0800u * (uint32_t)j; }
 __device__ __forceinline__ uint32_t neg1024_pow4_inv_bits(int j) { return 0xE400u - 0x0800u * (uint32_t)j; }
 
-template <int FMT, int NW>
-__device__ __forceinline__ void qlow_row_stage_regs(const QlowRow<NW>& R, int c, uint32_t (&v)[32]) {
-    const int h = c >> 1, j0 = 2 * (c & 1);
+template <int FMT, int CL>
+__device__ __forceinline__ void qlow_half_stage_regs(const QlowHalf<FMT>& R, int h, uint32_t (&v)[32]) {
+    constexpr int j0 = 2 * CL;   // stage c = 2h + CL: groups 8h + 4 CL + gg
 #pragma unroll
     for (int gg = 0; gg < 4; ++gg) {
-        const int g = 4 * c + gg, j = j0 + (gg >> 1), p = gg & 1;
+        const int gl = 4 * CL + gg;   // group within the half
+        const int j = j0 + (gg >> 1), p = gg & 1;
         // the group's multiply-add constants
         __half2 sg;
         if constexpr (FMT == 2) {
-            const uint32_t sc = (R.w[g >> 2] >> (8 * (g & 3))) & 15u;
+            const uint32_t w = h ? R.sc[2 + (gl >> 2)] : R.sc[gl >> 2];   // scale bytes of groups 8h ..
+            const uint32_t sc = (w >> (8 * (gl & 3))) & 15u;
             sg = small_pair(sc, sc);
         } else {
-            const uint32_t s6 = q3K_s6(R, g);
+            const uint32_t s6 = q3K_s6h(R.sc, gl, h);
             sg = __hsub2(bits_h2(0x64006400u | s6 | (s6 << 16)), bits_h2(0x64206420u));   // s6 - 32
         }
         const uint32_t m1 = pow4_inv_bits(j), m2 = neg1024_pow4_inv_bits(j);
@@ -636,16 +815,15 @@ __device__ __forceinline__ void qlow_row_stage_regs(const QlowRow<NW>& R, int c,
         const uint32_t qmask = 0x00030003u << (2 * j);
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-            const int qwi = (FMT == 2 ? 4 : 8) + 8 * h + 4 * p + u;   // qs at byte 16 (q2_K) or 32 (q3_K)
-            const uint32_t qw = R.w[qwi];
+            const uint32_t qw = R.qs[4 * p + u];   // qs[32h + 16p + 4u ..]
             uint32_t x01 = __byte_perm(qw, 0, 0x4140) & qmask, x23 = __byte_perm(qw, 0, 0x4342) & qmask;
             if constexpr (FMT == 3) {
-                const uint32_t hw = R.w[4 * p + u];                 // hmask bytes 16p + 4u ..
+                const uint32_t hw = R.hm[4 * p + u];   // hmask bytes 16p + 4u ..
                 const uint32_t h01 = __byte_perm(hw, 0, 0x4140), h23 = __byte_perm(hw, 0, 0x4342);
-                const int from = 4 * h + j, to = 2 * j + 2;         // hbit to bit 2j + 2 of each half
-                const uint32_t hmask = 0x00010001u << to;
-                x01 |= (to >= from ? h01 << (to - from) : h01 >> (from - to)) & hmask;
-                x23 |= (to >= from ? h23 << (to - from) : h23 >> (from - to)) & hmask;
+                // hbit (bit 4h + j of the byte) to bit 2j + 2 of each half: up by j + 2, down by 4h
+                const uint32_t hmask = 0x00010001u << (2 * j + 2);
+                x01 |= ((h01 << (j + 2)) >> (4 * h)) & hmask;
+                x23 |= ((h23 << (j + 2)) >> (4 * h)) & hmask;
             }
             v[8 * gg + 2 * u] = h2_bits(__hfma2(bits_h2(x01 | 0x64006400u), mul, add));
             v[8 * gg + 2 * u + 1] = h2_bits(__hfma2(bits_h2(x23 | 0x64006400u), mul, add));
@@ -1262,10 +1440,7 @@ __global__ void __launch_bounds__(tm_threads(XIN), 1) gemm_tm_kernel(const __gri
         const int t = tid & (GT - 1);          // weight row (and activation row) of the tile
         const int half = warp >> 2;            // stages 2 half, 2 half + 1 of every block
         const uint32_t alane = (uint32_t)((warp & 3) * 32) << 16;
-        using Row = typename std::conditional<
-            FMT == 2, Q2KRow,
-            typename std::conditional<FMT == 3, Q3KRow,
-                                      typename std::conditional<FMT == 5, Q5KRow, Q4KRow>::type>::type>::type;
+        using Row = typename std::conditional<FMT <= 3, QlowHalf<FMT>, QxKHalf<FMT>>::type;
         constexpr int WROW = GemmCfg<FMT>::WROW, WPITCH = GemmCfg<FMT>::WPITCH;
         Row R;
         int nissued = 0;
@@ -1290,12 +1465,9 @@ __global__ void __launch_bounds__(tm_threads(XIN), 1) gemm_tm_kernel(const __gri
                     if (!mbar_wait(&bfull[s], (uint32_t)(gb >> 1) & 1u)) { ok = false; break; }
                     const uint8_t* slot = sm + L::BRING + s * L::BSLOT;
                     if constexpr (FMT <= 3) {
-                        qlow_row_load<sizeof(R.w) / 4, WPITCH / 4>(R, slot + t * WPITCH, ((kb0 + b) * WROW) & 15);
+                        qlow_half_load<FMT>(R, slot + t * WPITCH, ((kb0 + b) * WROW) & 15, half);
                     } else {
-                        constexpr int NRAW = WROW / 16;
-#pragma unroll
-                        for (int u = 0; u < NRAW; ++u)
-                            R.raw[u] = reinterpret_cast<const uint4*>(slot + t * WPITCH)[u];
+                        qxK_half_load<FMT>(R, slot + t * WPITCH, half);
                     }
                     const uint4* ax = reinterpret_cast<const uint4*>(slot + L::WT + t * AUXB);
                     const uint4 a0 = ax[0], a1 = ax[1], a2 = ax[2];
@@ -1306,12 +1478,7 @@ __global__ void __launch_bounds__(tm_threads(XIN), 1) gemm_tm_kernel(const __gri
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&bempty[s]);
                 }
-                if constexpr (FMT == 2)
-                    q2K_row_prepare(R);
-                else if constexpr (FMT == 3)
-                    q3K_row_prepare(R);
-                else
-                    q4K_row_prepare(R);
+                if constexpr (FMT >= 4) qxK_half_prepare<FMT>(R, half);
                 if (gb >= 2) {   // slot j's min operands and scales are free again
                     ok = mbar_wait(&minempty[j], ((gb >> 1) - 1) & 1) && mbar_wait(&tempty[j], ((gb >> 1) - 1) & 1);
                     if (!ok) break;
@@ -1320,17 +1487,10 @@ __global__ void __launch_bounds__(tm_threads(XIN), 1) gemm_tm_kernel(const __gri
                     // min operands: K 0..15 the weight row's mins m_(g/2); K 16..31 the activation row's bsums
                     uint8_t* mt = sm + L::MIN + j * TILE_BYTES;
                     uint32_t mv[8];
-                    if constexpr (FMT == 2) {
-                        q2K_min_pairs(R, mv);
-                    } else if constexpr (FMT == 3) {
-                        q3K_min_pairs(R, mv);
-                    } else {
-#pragma unroll
-                        for (int g = 0; g < 8; ++g) {
-                            const uint32_t mm = (uint32_t)R.mins[g];
-                            mv[g] = h2_bits(__hsub2(bits_h2(0x64006400u | mm | (mm << 16)), bits_h2(0x64006400u)));
-                        }
-                    }
+                    if constexpr (FMT <= 3)
+                        qlow_half_min_pairs<FMT>(R, mv);
+                    else
+                        qxK_min_pairs(R.hdr, mv);
                     *reinterpret_cast<uint4*>(mt + sw128_chunk(t, 0)) = make_uint4(mv[0], mv[1], mv[2], mv[3]);
                     *reinterpret_cast<uint4*>(mt + sw128_chunk(t, 1)) = make_uint4(mv[4], mv[5], mv[6], mv[7]);
                     *reinterpret_cast<uint4*>(mt + sw128_chunk(t, 2)) = make_uint4(bsw[0], bsw[1], bsw[2], bsw[3]);
@@ -1341,10 +1501,11 @@ __global__ void __launch_bounds__(tm_threads(XIN), 1) gemm_tm_kernel(const __gri
                     sj[GT + t] = R.dmin;
                     sj[2 * GT + t] = dx;
                 }
-                // the block's two stages of this warpgroup: A into tensor memory, B by
-                // TMA (c a compile-time constant, so R's fields stay in registers)
-                auto stage = [&](auto cc_) -> bool {
-                    constexpr int c = decltype(cc_)::value;   // stage, and its ring slot (one block long)
+                // the block's two stages of this warpgroup, c = 2 half + CL: A into tensor
+                // memory, B by TMA (CL a compile-time constant, so R's fields stay in registers)
+                auto stage = [&](auto cl_) -> bool {
+                    constexpr int CL = decltype(cl_)::value;
+                    const int c = 2 * half + CL;   // stage, and its ring slot (one block long)
                     if (gb >= 1) {
                         if (!mbar_wait(&empty[c], (uint32_t)(gb - 1) & 1u)) return false;
                         tc_fence_after();
@@ -1355,17 +1516,15 @@ __global__ void __launch_bounds__(tm_threads(XIN), 1) gemm_tm_kernel(const __gri
                     }
                     uint32_t v[32];
                     if constexpr (FMT <= 3)
-                        qlow_row_stage_regs<FMT>(R, c, v);
+                        qlow_half_stage_regs<FMT, CL>(R, half, v);
                     else
-                        qxK_row_stage_regs<FMT>(R, c, v);
+                        qxK_half_stage_regs<FMT, CL>(R, c, v);
                     tmem_st32(tmem + alane + TM_A + 32 * c, v);
                     return true;
                 };
                 using C0 = std::integral_constant<int, 0>;
                 using C1 = std::integral_constant<int, 1>;
-                using C2 = std::integral_constant<int, 2>;
-                using C3 = std::integral_constant<int, 3>;
-                ok = half == 0 ? (stage(C0{}) && stage(C1{})) : (stage(C2{}) && stage(C3{}));
+                ok = stage(C0{}) && stage(C1{});
                 if (!ok) break;
                 asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
                 tc_fence_before();
