@@ -560,11 +560,13 @@ def run_extras(torch, q, peaks):
 
 def gemm_roofline(configs, peaks, peak_src):
     """Roofline of the dominant prefill kernel: the q4_K tensor-core GEMM on
-    the Qwen3-8B gate/up shape 12288 x 4096 at m = 2048, from the sweep's
-    CUDA-event time per call (the call is the activation pre-pass, about 2 %,
-    plus the GEMM kernel, so the kernel's own rate is slightly higher)."""
+    the Qwen3-8B gate/up shape 12288 x 4096 at m = 2048 in its workspace
+    form, from the sweep's CUDA-event time per call (the call is the
+    activation pre-pass, about 2 %, plus the GEMM kernel, so the kernel's own
+    rate is slightly higher)."""
     row = next((r for r in configs.get("sweep_qwen3_8b", [])
-                if r["fmt"] == "q4K" and r["n"] == 12288 and r["k"] == 4096 and r["m"] == 2048), None)
+                if r["fmt"] == "q4K" and r["n"] == 12288 and r["k"] == 4096 and r["m"] == 2048
+                and r["entry"] == "plm_gemm_q4K_ws"), None)
     if row is None:
         return None
     peak = peaks["bf16_tflops"]
