@@ -321,12 +321,17 @@ plm_status plm_gemv_q4K_swiglu_grouped(const plm_swiglu_problem* problems, int64
  * memory) against the activation codes as exact f16, one 256-weight block at
  * a time; the per-block scales are applied in f32.  These plain forms widen
  * the activation codes inside the GEMM kernel, straight from xq into shared
- * memory: they need no workspace, allocate nothing and never split K.  For
+ * memory: they need no workspace and allocate nothing.  When the output
+ * tiles alone would leave SMs idle (small m and n), q2_K .. q5_K split K
+ * over a thread-block cluster of up to eight CTAs per tile and rank 0 adds
+ * the partial tiles from the others' shared memory in rank order (the same
+ * bits every run); q6_K does not split.  For
  * m <= 8 (and q2_K / q3_K shapes without the tensor-core path, see above)
  * they run the decode GEMV eight rows at a time.
- * Same buffers, layouts and tolerance as the GEMV; no limit on m.  For the
- * same (m, n, k) a plain call and a _ws call that does not split K give the
- * same bits.
+ * Same buffers, layouts and tolerance as the GEMV; no limit on m.  A _ws
+ * call that splits K the same way (given plm_gemm_workspace_size_split bytes,
+ * at most eight splits) or does not split where the plain call does not
+ * gives the same bits.
  */
 plm_status plm_gemm_q4K(const void* w, const void* xq, float* y,
                         int64_t m, int64_t n, int64_t k, cudaStream_t stream);
@@ -344,7 +349,8 @@ plm_status plm_gemm_q6K(const void* w, const void* xq, float* y,
  * back from h and writes silu(g) * u over it: no workspace, nothing
  * allocated.  The _ws form runs the two GEMMs (the up matrix's into the
  * workspace, K split when the workspace allows) and one elementwise pass;
- * without a K split both forms give the same bits.  For m <= 8 both run
+ * where both split K alike (or neither does) they give the same bits.  For
+ * m <= 8 both run
  * plm_gemv_q4K_swiglu eight rows at a time.
  *   w_gate, w_up  q4_K [n][k/256] each, 16-byte aligned; xq q8_K [m][k/256];
  *   h f32 [m][n], not overlapping the inputs.  The _ws form's workspace:
@@ -399,8 +405,8 @@ plm_status plm_gemm_q6K_ws(const void* w, const void* xq, float* y, int64_t m, i
  * the PocketLLM pages: it is a library convenience.  It runs the workspace
  * form of the GEMM (plm_gemm_q4K_ws: pre-pass, TMA-loaded f16 activations,
  * no K split) with the workspace in a fixed device array inside this
- * library; results are bit-identical to plm_gemm_q4K, which needs no
- * workspace at all.  It is meant for callers that must not allocate device
+ * library; results agree with plm_gemm_q4K, which needs no workspace at
+ * all, bit for bit where that one does not split K either.  It is meant for callers that must not allocate device
  * memory while running, such as an engine whose memory is entirely claimed
  * by its own allocator at start-up, or a latency-critical loop that cannot
  * afford an allocation that might fail or wait.

@@ -162,6 +162,24 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
                  :: "r"(smem_u32(bar)) : "memory");
 }
 
+// thread-block cluster: barrier over all threads of all its CTAs, rank, peer shared memory
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ float4 ld_peer_f4(const void* local, uint32_t rank) {
+    uint32_t addr;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(addr) : "r"(smem_u32(local)), "r"(rank));
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
     asm volatile("mbarrier.expect_tx.shared::cta.b64 [%0], %1;" :: "r"(smem_u32(bar)), "r"(bytes) : "memory");
 }
@@ -921,6 +939,7 @@ struct GemmArgs {
     float* part;             // split K: partial sums [gridDim.z][m][n] (null: write y)
     const float* gate;       // GATE kernels (unsplit q4_K): y = silu(gate) * result, gate may be y itself
     int xtma;                // XIN: the staged codes come by TMA (xmap), else by one bulk copy per row
+    int csplit;              // > 1: the grid's z CTAs of a tile form a cluster, rank 0 adds their partials
     unsigned* fault;
     int m, n, nb;
     int bsplit;              // blocks of K per split (blockIdx.z)
@@ -1671,7 +1690,14 @@ __global__ void __launch_bounds__(tm_threads(XIN), 1) gemm_tm_kernel(const __gri
             }
             const int r = r0 + row;
             float* out = A.part ? A.part + (size_t)blockIdx.z * A.m * A.n : A.y;
-            if (ok && r < A.n) {
+            if (A.csplit > 1) {
+                // cluster K split: this CTA's partial tile into its B ring (idle once the last
+                // block's MMAs are done), four columns per 16 bytes, thread-major
+                float4* red = reinterpret_cast<float4*>(sm + L::RING) + e * 32 + lane;
+#pragma unroll
+                for (int c4 = 0; c4 < 16; ++c4)
+                    red[c4 * 256] = make_float4(acc[4 * c4], acc[4 * c4 + 1], acc[4 * c4 + 2], acc[4 * c4 + 3]);
+            } else if (ok && r < A.n) {
                 if constexpr (GATE) {
                     // SwiGLU pair: the gate GEMM's result for the same element, 16 loads at a time
 #pragma unroll
@@ -1701,6 +1727,43 @@ __global__ void __launch_bounds__(tm_threads(XIN), 1) gemm_tm_kernel(const __gri
     if (!ok && lane == 0) atomicOr(A.fault, 2u);
     tc_fence_before();
     __syncthreads();
+    if (A.csplit > 1) {
+        // every thread of every CTA of the cluster passes both barriers: the partials
+        // are visible, rank 0 adds them in rank order (the same bits every run) and
+        // stores the tile, and no CTA leaves while its shared memory is still read
+        cluster_sync_all();
+        if (cluster_rank() == 0 && warp >= TM_EPI_WARP0 && warp < TM_MMA_WARP) {
+            const int e = warp - TM_EPI_WARP0, q = e & 3, chalf = e >> 2;
+            const int r = r0 + 32 * q + lane;
+            const float4* red = reinterpret_cast<const float4*>(sm + L::RING) + e * 32 + lane;
+            if (r < A.n) {
+#pragma unroll 4
+                for (int c4 = 0; c4 < 16; ++c4) {
+                    float4 v = red[c4 * 256];
+                    for (int z = 1; z < A.csplit; ++z) {
+                        const float4 u = ld_peer_f4(red + c4 * 256, (uint32_t)z);
+                        v.x = __fadd_rn(v.x, u.x);
+                        v.y = __fadd_rn(v.y, u.y);
+                        v.z = __fadd_rn(v.z, u.z);
+                        v.w = __fadd_rn(v.w, u.w);
+                    }
+                    const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        const int i = i0 + 64 * chalf + 4 * c4 + t;
+                        if (i < A.m) {
+                            if constexpr (GATE)
+                                A.y[(size_t)i * A.n + r] = swiglu1(A.gate[(size_t)i * A.n + r], vv[t]);
+                            else
+                                A.y[(size_t)i * A.n + r] = vv[t];
+                        }
+                    }
+                }
+            }
+        }
+        __syncwarp();
+        cluster_sync_all();
+    }
     if (warp == TM_MMA_WARP) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" :: "r"(tmem) : "memory");
@@ -1889,6 +1952,7 @@ static cudaError_t gemm_tc(const uint8_t* w, const uint8_t* xq, float* y, long l
     A.y = y;
     A.gate = gate;
     A.xtma = xtma ? 1 : 0;
+    A.csplit = 1;
     A.fault = fault_word();
     if (!A.fault) return cudaErrorInvalidDevicePointer;
     A.m = (int)m;
@@ -1903,13 +1967,32 @@ static cudaError_t gemm_tc(const uint8_t* w, const uint8_t* xq, float* y, long l
         if (e != cudaSuccess) return e;
         return launch_kernel(kernel, grid, dim3(threads), smem, stream, map, wmap, amap, A);
     };
+    // no workspace, few output tiles (q2_K .. q5_K): split K over a cluster of up to
+    // eight CTAs per tile, the partial tiles added through distributed shared memory
+    auto run_cluster = [&](auto kernel, int threads, int smem) -> cudaError_t {
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        int want = gemm_splits(m, n, nb);
+        if (want > 8) want = 8;
+        for (int cz = want; cz >= 2; --cz) {
+            const int bs = (nb + cz - 1) / cz;
+            const int z = (nb + bs - 1) / bs;   // no empty split
+            const dim3 g(grid.x, grid.y, (unsigned)z);
+            if (z < 2 || max_active_clusters(kernel, g, dim3(threads), (size_t)smem, (unsigned)z) < 1) continue;
+            GemmArgs B = A;
+            B.bsplit = bs;
+            B.csplit = z;
+            return launch_kernel_cluster(kernel, g, dim3(threads), smem, stream, (unsigned)z, map, wmap, amap, B);
+        }
+        return launch_kernel(kernel, grid, dim3(threads), smem, stream, map, wmap, amap, A);
+    };
     cudaError_t e;
     if constexpr (FMT != 6) {
         if (gate) {
             if (FMT != 4 || !xin) return cudaErrorInvalidValue;
-            e = run(gemm_tm_kernel<4, true, true>, tm_threads(true), TmSmem<4, true>::ALLOC);
+            e = run_cluster(gemm_tm_kernel<4, true, true>, tm_threads(true), TmSmem<4, true>::ALLOC);
         } else {
-            e = xin ? run(gemm_tm_kernel<FMT, true, false>, tm_threads(true), TmSmem<FMT, true>::ALLOC)
+            e = xin ? run_cluster(gemm_tm_kernel<FMT, true, false>, tm_threads(true), TmSmem<FMT, true>::ALLOC)
                     : run(gemm_tm_kernel<FMT, false, false>, tm_threads(false), TmSmem<FMT, false>::ALLOC);
         }
     } else {

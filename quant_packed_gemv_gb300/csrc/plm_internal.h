@@ -34,6 +34,50 @@ inline cudaError_t launch_kernel(void (*k)(P...), dim3 grid, dim3 block, size_t 
     return cudaLaunchKernelEx(&lc, k, std::forward<A>(args)...);
 }
 
+// The same with thread-block clusters of (1, 1, cz) CTAs along the grid's z.
+template <typename... P, typename... A>
+inline cudaError_t launch_kernel_cluster(void (*k)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                                         unsigned cz, A&&... args) {
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = grid;
+    lc.blockDim = block;
+    lc.dynamicSmemBytes = smem;
+    lc.stream = stream;
+    cudaLaunchAttribute at[2];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 1;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = cz;
+    at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[1].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = at;
+    lc.numAttrs = overlap_mode() >= 1 ? 2 : 1;
+    return cudaLaunchKernelEx(&lc, k, std::forward<A>(args)...);
+}
+
+// Clusters of (1, 1, cz) CTAs of kernel k with this block and shared memory
+// that the GPU can hold at once (0: none; the launch would fail).
+template <typename... P>
+inline int max_active_clusters(void (*k)(P...), dim3 grid, dim3 block, size_t smem, unsigned cz) {
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = grid;
+    lc.blockDim = block;
+    lc.dynamicSmemBytes = smem;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 1;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = cz;
+    lc.attrs = at;
+    lc.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, (const void*)k, &lc) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
 // Device address of the library's fault word on the current device (set by a
 // kernel whose bounded wait ran out), or nullptr if it cannot be resolved.
 unsigned* fault_word();

@@ -6,7 +6,7 @@ m <= 8: the GEMV's) -- relative 1e-6; (2) against the oracle, h = silu(g) u
 in f64 on the oracle's integer path, within the bound the GEMM tolerance
 implies: |dh| <= 1.1 |u| dg + (|silu(g)| + 1.1 dg) du + 1e-6 |h|, with
 dg = 1e-4 S_gate, du = 1e-4 S_up (|silu'| <= 1.1).  The caller-workspace form
-gives the same bits when it does not split K."""
+gives the same bits when it splits K as the plain form does."""
 import numpy as np
 import pytest
 import torch
@@ -43,7 +43,7 @@ def unpoison(buf, m, n):
 
 def single(w, xq, m, n, k):
     """The matrix alone, in the same f32 order as the plain pair: the plain
-    GEMM (no K split), or the GEMV for m <= 8."""
+    GEMM (the same K split), or the GEMV for m <= 8."""
     y = torch.full((m, n), float("nan"), device="cuda")
     if m <= 8:
         q.plm_gemv_q4K(w, xq, y, m, n, k)
@@ -77,9 +77,9 @@ def test_gemm_swiglu(m, n, k):
         + 1e-6 * np.abs(h_ref)
     assert np.all(np.abs(h - h_ref) <= bound)
     assert np.mean(np.abs(g_ref) < 4.0) > 0.5   # the gate outputs do cover the bend of silu
-    # caller workspace: without a K split the same bits (the plain form
-    # combines in the up GEMM's epilogue, the _ws form in a separate pass);
-    # with the split-K workspace within the bound
+    # caller workspace: with the split-K size (K split as the plain form splits
+    # it over a cluster) the same bits -- the plain form combines in the up
+    # GEMM's epilogue, the _ws form in a separate pass; unsplit within the bound
     split = q.plm_gemm_swiglu_workspace_size(m, n, k)
     unsplit = 0 if split == 0 else -(-m * n * 4 // 256) * 256 + q.plm_gemm_workspace_size("q4K", m, k)
     for need in sorted({unsplit, split}):
@@ -87,7 +87,7 @@ def test_gemm_swiglu(m, n, k):
         hb2 = poisoned(m, n)
         q.plm_gemm_q4K_swiglu_ws(wg, wu, xq, hb2, m, n, k, ws if need else None, need)
         h2 = unpoison(hb2, m, n)
-        if need == unsplit:
+        if need == split:
             assert np.array_equal(h2, h.astype(np.float32))
         assert np.all(np.abs(h2.astype(np.float64) - h_ref) <= bound)
     assert q.plm_device_fault() == 0

@@ -1,10 +1,11 @@
 """The allocation-free GEMM entry points.
 
 plm_gemm_q4K_noalloc runs the workspace form of the q4_K GEMM with its
-workspace in a fixed device array inside the library; it must give the bits
-of plm_gemm_q4K (which widens the activation codes inside the kernel and
-needs no workspace) and match the oracle within the tolerance every GEMM
-test uses (1e-4 of sum_k |w_hat * x_hat|).  No plain GEMM entry point may
+workspace in a fixed device array inside the library; it must agree with
+plm_gemm_q4K (which widens the activation codes inside the kernel, needs no
+workspace and may split K over a cluster) -- bit for bit where neither
+splits -- and match the oracle within the tolerance every GEMM test uses
+(1e-4 of sum_k |w_hat * x_hat|).  No plain GEMM entry point may
 draw on the device's stream-ordered pool.  This file is named so that pytest
 collects it last.
 """
@@ -46,7 +47,8 @@ def test_noalloc_matches_allocating_gemm_on_two_calls_in_a_row():
         w, xq = _case(seed, m, n, k)
         ref, S = oracle_ref("q4K", w, xq, m, n, k)
         assert not np.isnan(got).any()
-        np.testing.assert_array_equal(got, want)   # neither splits K: the same MMA operands and order
+        # plm_gemm_q4K may split K over a cluster where this entry does not: the tolerance
+        assert np.all(np.abs(got.astype(np.float64) - want) <= TOL * S)
         assert_close(got, ref, S)
     assert q.plm_device_fault() == 0
 
@@ -83,7 +85,7 @@ def test_noalloc_limit_edge():
     rows = np.r_[0:64, m - 64:m]          # the first and last activation tiles against the oracle
     ref, S = oracle_ref("q4K", w, xq[rows], len(rows), n, k)
     assert_close(got[rows], ref, S)
-    # neither form splits K: the same operands and sums, the same bits
+    # one block of K: neither form splits, the same operands and sums, the same bits
     np.testing.assert_array_equal(got, want)
     st = P.raw_status("plm_gemm_q4K_noalloc", wd.data_ptr(), xd.data_ptr(), y.data_ptr(), m + 1, n, k, None)
     assert st == P.PLM_ERR_UNSUPPORTED
