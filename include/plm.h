@@ -316,16 +316,17 @@ plm_status plm_gemv_q4K_swiglu_grouped(const plm_swiglu_problem* problems, int64
 /*
  * Prefill GEMM, y = X . W^T for any m >= 1 (intended for m = 512..2048).
  * For m >= 9, weight tiles are decoded into exact integer-valued f16
- * operands (q4_K: sc*q; q6_K: sc*(q6-32), split as 16*hi + lo) and
+ * operands (q4_K: sc*q; q6_K: 16*hi*(q6-32) and lo*(q6-32) for sc = 16*hi
+ * + lo, two contractions into one accumulator) and
  * contracted on the tensor cores (tcgen05, f32 accumulation in tensor
  * memory) against the activation codes as exact f16, one 256-weight block at
  * a time; the per-block scales are applied in f32.  These plain forms widen
  * the activation codes inside the GEMM kernel, straight from xq into shared
  * memory: they need no workspace and allocate nothing.  When the output
- * tiles alone would leave SMs idle (small m and n), q2_K .. q5_K split K
- * over a thread-block cluster of up to eight CTAs per tile and rank 0 adds
- * the partial tiles from the others' shared memory in rank order (the same
- * bits every run); q6_K does not split.  For
+ * tiles alone would leave SMs idle (small m and n), they split K over a
+ * thread-block cluster of up to eight CTAs per tile and rank 0 adds the
+ * partial tiles from the others' shared memory in rank order (the same bits
+ * every run; q6_K only where k/256 % 8 == 0, its other shapes do not split).  For
  * m <= 8 (and q2_K / q3_K shapes without the tensor-core path, see above)
  * they run the decode GEMV eight rows at a time.
  * Same buffers, layouts and tolerance as the GEMV; no limit on m.  A _ws

@@ -113,6 +113,13 @@ template <> struct GemmCfg<6> {
     static constexpr int ATILES = 2, NSTAGE = 3, MINB = 0, BSLOTS = 0, WROW = 0, PWG = 1;
     static constexpr int WPITCH = 0;
 };
+// q6_K in the tensor-memory kernel (gemm_tm_kernel<Q6TM>): 210-byte blocks
+// in 16-byte windows of at most 224 bytes, 15 units a row
+constexpr int Q6TM = 7;
+template <> struct GemmCfg<Q6TM> {
+    static constexpr int ATILES = 1, NSTAGE = 4, MINB = 0, BSLOTS = 2, WROW = Q6K_BYTES, PWG = 2;
+    static constexpr int WPITCH = 240;
+};
 
 template <int FMT, bool XIN>
 struct GemmSmem {
@@ -806,6 +813,61 @@ __device__ __forceinline__ void qlow_half_min_pairs(const QlowHalf<FMT>& R, uint
     }
 }
 
+// One producer warpgroup's share of a q6_K row (tensor-memory GEMM): half
+// h = stages 2h, 2h + 1 = weights 128h .. 128h + 127, whose low four bits are
+// ql[64h .. 64h + 63] and top two bits qh[32h .. 32h + 31]; the int8 scales
+// and d.  Stage c = 2h + CL, K position p (0..63): code = (ql[64h + p] >> 4 CL
+// & 15) | (qh[32h + p % 32] >> (4 CL + 2 (p >= 32)) & 3) << 4, group 4c + p / 16.
+// Each scale is split as sc = 16 hi + lo (lo in 0..15): the two operands
+// 16 hi (q - 32) (a multiple of 16 up to 4096 in magnitude) and lo (q - 32)
+// are exact in f16 and go into the same accumulator.
+struct Q6Half {
+    uint32_t ql[16];
+    uint32_t qh[8];
+    uint32_t sc[4];   // the 16 int8 scales
+    float d;
+};
+
+__device__ __forceinline__ void q6_half_load(Q6Half& R, const uint8_t* row, int sk, int half) {
+    qlow_words<16>(row, 16 * half, sk, R.ql);
+    qlow_words<8>(row, 32 + 8 * half, sk, R.qh);
+    qlow_words<4>(row, 48, sk, R.sc);
+    uint32_t dw[1];
+    qlow_words<1>(row, 52, sk, dw);
+    R.d = half_bits_to_float(dw[0] & 0xFFFFu);   // bytes 208, 209
+}
+
+// columns 16 P .. 16 P + 15 of stage c = 2h + CL (K positions 32 P .. 32 P + 31)
+// of both operands
+template <int CL, int P>
+__device__ __forceinline__ void q6_half_stage_regs(const Q6Half& R, int h, uint32_t (&vh)[16], uint32_t (&vl)[16]) {
+    const __half2 m1056 = bits_h2(0xE420E420u);   // -1056
+#pragma unroll
+    for (int gq = 0; gq < 2; ++gq) {              // the two 16-weight groups of these positions
+        const int gl = 4 * CL + 2 * P + gq;       // group within the half
+        const uint32_t w = h ? R.sc[2 + (gl >> 2)] : R.sc[gl >> 2];
+        const int sc = (int)(int8_t)((w >> (8 * (gl & 3))) & 0xFFu);
+        const __half2 hi16 = __float2half2_rn((float)((sc >> 4) * 16));
+        const uint32_t lo = (uint32_t)(sc & 15);
+        const __half2 lo2 = small_pair(lo, lo);
+        const __half2 lo_off = __hmul2(lo2, m1056);   // -1056 lo, exact
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int wi = 8 * P + 4 * gq + u;         // positions 4 wi .. 4 wi + 3
+            const uint32_t nib = (R.ql[wi] >> (4 * CL)) & 0x0F0F0F0Fu;
+            const uint32_t hb = (R.qh[wi & 7] >> (4 * CL + 2 * (wi >> 3))) & 0x03030303u;
+            const uint32_t code = nib | (hb << 4);
+            const __half2 x01 = bits_h2(prmt(code, 0x64646464u, 0x4140u));   // 1024 + q
+            const __half2 x23 = bits_h2(prmt(code, 0x64646464u, 0x4342u));
+            const int col = 8 * gq + 2 * u;
+            vh[col] = h2_bits(__hmul2(__hadd2(x01, m1056), hi16));
+            vh[col + 1] = h2_bits(__hmul2(__hadd2(x23, m1056), hi16));
+            vl[col] = h2_bits(__hfma2(x01, lo2, lo_off));
+            vl[col + 1] = h2_bits(__hfma2(x23, lo2, lo_off));
+        }
+    }
+}
+
 // f16 of 4^-j and of -1024 * 4^-j
 __device__ __forceinline__ uint32_t pow4_inv_bits(int j) { return 0x3C00u - 0x0800u * (uint32_t)j; }
 __device__ __forceinline__ uint32_t neg1024_pow4_inv_bits(int j) { return 0xE400u - 0x0800u * (uint32_t)j; }
@@ -1355,8 +1417,8 @@ constexpr uint32_t TM_D1 = 0, TM_D2 = 256, TM_A = 384;
 template <int FMT, bool XIN>
 struct TmSmem {
     static constexpr int RING = 0;                                            // B tiles, 4 x 16 KB
-    static constexpr int MIN = RING + TM_NSTAGE * TILE_BYTES;                 // 2 x 16 KB
-    static constexpr int SCL = MIN + 2 * TILE_BYTES;                          // 2 x (d, dmin, dx) x 128 f32
+    static constexpr int MIN = RING + TM_NSTAGE * TILE_BYTES;                 // 2 x 16 KB (none for q6_K)
+    static constexpr int SCL = MIN + (FMT == Q6TM ? 0 : 2 * TILE_BYTES);      // 2 x (d, dmin, dx) x 128 f32
     static constexpr int WT = GT * GemmCfg<FMT>::WPITCH;
     static constexpr int BTX = WT + GT * AUXB;
     static constexpr int BSLOT = (BTX + 1023) & ~1023;
@@ -1374,6 +1436,14 @@ __device__ __forceinline__ void mma_f16_ta(uint32_t dtmem, uint32_t atmem, uint6
     asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
                  "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
                  :: "r"(dtmem), "r"(atmem), "l"(db), "r"(IDESC_F16_128x128), "r"(accumulate));
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+                 "%15,%16};"
+                 :: "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
+                    "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+                    "r"(r[15]) : "memory");
 }
 
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
@@ -1459,7 +1529,8 @@ __global__ void __launch_bounds__(tm_threads(XIN), 1) gemm_tm_kernel(const __gri
         const int t = tid & (GT - 1);          // weight row (and activation row) of the tile
         const int half = warp >> 2;            // stages 2 half, 2 half + 1 of every block
         const uint32_t alane = (uint32_t)((warp & 3) * 32) << 16;
-        using Row = typename std::conditional<FMT <= 3, QlowHalf<FMT>, QxKHalf<FMT>>::type;
+        using Row = typename std::conditional<
+            FMT == Q6TM, Q6Half, typename std::conditional<FMT <= 3, QlowHalf<FMT>, QxKHalf<FMT>>::type>::type;
         constexpr int WROW = GemmCfg<FMT>::WROW, WPITCH = GemmCfg<FMT>::WPITCH;
         Row R;
         int nissued = 0;
@@ -1483,7 +1554,9 @@ __global__ void __launch_bounds__(tm_threads(XIN), 1) gemm_tm_kernel(const __gri
                     const int s = gb & 1;
                     if (!mbar_wait(&bfull[s], (uint32_t)(gb >> 1) & 1u)) { ok = false; break; }
                     const uint8_t* slot = sm + L::BRING + s * L::BSLOT;
-                    if constexpr (FMT <= 3) {
+                    if constexpr (FMT == Q6TM) {
+                        q6_half_load(R, slot + t * WPITCH, ((kb0 + b) * WROW) & 15, half);
+                    } else if constexpr (FMT <= 3) {
                         qlow_half_load<FMT>(R, slot + t * WPITCH, ((kb0 + b) * WROW) & 15, half);
                     } else {
                         qxK_half_load<FMT>(R, slot + t * WPITCH, half);
@@ -1497,12 +1570,13 @@ __global__ void __launch_bounds__(tm_threads(XIN), 1) gemm_tm_kernel(const __gri
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&bempty[s]);
                 }
-                if constexpr (FMT >= 4) qxK_half_prepare<FMT>(R, half);
+                if constexpr (FMT == 4 || FMT == 5) qxK_half_prepare<FMT>(R, half);
                 if (gb >= 2) {   // slot j's min operands and scales are free again
                     ok = mbar_wait(&minempty[j], ((gb >> 1) - 1) & 1) && mbar_wait(&tempty[j], ((gb >> 1) - 1) & 1);
                     if (!ok) break;
                 }
                 if (half == 1) {
+                    if constexpr (FMT != Q6TM) {
                     // min operands: K 0..15 the weight row's mins m_(g/2); K 16..31 the activation row's bsums
                     uint8_t* mt = sm + L::MIN + j * TILE_BYTES;
                     uint32_t mv[8];
@@ -1514,10 +1588,11 @@ __global__ void __launch_bounds__(tm_threads(XIN), 1) gemm_tm_kernel(const __gri
                     *reinterpret_cast<uint4*>(mt + sw128_chunk(t, 1)) = make_uint4(mv[4], mv[5], mv[6], mv[7]);
                     *reinterpret_cast<uint4*>(mt + sw128_chunk(t, 2)) = make_uint4(bsw[0], bsw[1], bsw[2], bsw[3]);
                     *reinterpret_cast<uint4*>(mt + sw128_chunk(t, 3)) = make_uint4(bsw[4], bsw[5], bsw[6], bsw[7]);
+                    }
                 } else {
                     float* sj = scl + j * 3 * GT;
                     sj[t] = R.d;
-                    sj[GT + t] = R.dmin;
+                    if constexpr (FMT != Q6TM) sj[GT + t] = R.dmin;
                     sj[2 * GT + t] = dx;
                 }
                 // the block's two stages of this warpgroup, c = 2 half + CL: A into tensor
@@ -1533,12 +1608,23 @@ __global__ void __launch_bounds__(tm_threads(XIN), 1) gemm_tm_kernel(const __gri
                         mbar_expect_tx(&full[c], TILE_BYTES);
                         tma_load_2d(sm + L::RING + c * TILE_BYTES, &xmap, (kb0 + b) * QK + c * KS, i0, &full[c]);
                     }
-                    uint32_t v[32];
-                    if constexpr (FMT <= 3)
-                        qlow_half_stage_regs<FMT, CL>(R, half, v);
-                    else
-                        qxK_half_stage_regs<FMT, CL>(R, c, v);
-                    tmem_st32(tmem + alane + TM_A + 32 * c, v);
+                    if constexpr (FMT == Q6TM) {
+                        // two operands (16 hi (q - 32) at columns 256 .., lo (q - 32) at 384 ..), 16 columns at a time
+                        uint32_t vh[16], vl[16];
+                        q6_half_stage_regs<CL, 0>(R, half, vh, vl);
+                        tmem_st16(tmem + alane + TM_D2 + 32 * c, vh);
+                        tmem_st16(tmem + alane + TM_A + 32 * c, vl);
+                        q6_half_stage_regs<CL, 1>(R, half, vh, vl);
+                        tmem_st16(tmem + alane + TM_D2 + 32 * c + 16, vh);
+                        tmem_st16(tmem + alane + TM_A + 32 * c + 16, vl);
+                    } else {
+                        uint32_t v[32];
+                        if constexpr (FMT <= 3)
+                            qlow_half_stage_regs<FMT, CL>(R, half, v);
+                        else
+                            qxK_half_stage_regs<FMT, CL>(R, c, v);
+                        tmem_st32(tmem + alane + TM_A + 32 * c, v);
+                    }
                     return true;
                 };
                 using C0 = std::integral_constant<int, 0>;
@@ -1579,16 +1665,24 @@ __global__ void __launch_bounds__(tm_threads(XIN), 1) gemm_tm_kernel(const __gri
                         tc_fence_after();
                         const uint64_t db = umma_desc_sw128(smem_u32(sm + L::RING + c * TILE_BYTES));
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)    // K = 16 per MMA: 8 TMEM columns, +2 descriptor units
-                            mma_f16_ta(d1, tmem + TM_A + 32 * c + 8 * kk, db + 2 * kk, (c | kk) != 0);
+                        for (int kk = 0; kk < 4; ++kk) {  // K = 16 per MMA: 8 TMEM columns, +2 descriptor units
+                            if constexpr (FMT == Q6TM) {   // both parts of the scale into the one accumulator
+                                mma_f16_ta(d1, tmem + TM_D2 + 32 * c + 8 * kk, db + 2 * kk, (c | kk) != 0);
+                                mma_f16_ta(d1, tmem + TM_A + 32 * c + 8 * kk, db + 2 * kk, 1u);
+                            } else {
+                                mma_f16_ta(d1, tmem + TM_A + 32 * c + 8 * kk, db + 2 * kk, (c | kk) != 0);
+                            }
+                        }
                         mma_commit(&empty[c]);
                     }
                     if (!ok) break;
                     if (!mbar_wait(&minfull[j], (gb >> 1) & 1)) { ok = false; break; }
-                    if (gb >= 1 && !mbar_wait(d2free, (uint32_t)(gb - 1) & 1u)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint32_t ma = smem_u32(sm + L::MIN + j * TILE_BYTES);
-                    mma_f16(tmem + TM_D2, umma_desc_sw128(ma), umma_desc_sw128(ma) + 2, 0u);
+                    if constexpr (FMT != Q6TM) {   // q6_K: no min term
+                        if (gb >= 1 && !mbar_wait(d2free, (uint32_t)(gb - 1) & 1u)) { ok = false; break; }
+                        tc_fence_after();
+                        const uint32_t ma = smem_u32(sm + L::MIN + j * TILE_BYTES);
+                        mma_f16(tmem + TM_D2, umma_desc_sw128(ma), umma_desc_sw128(ma) + 2, 0u);
+                    }
                     mma_commit(&minempty[j]);
                     mma_commit(&tfull[j]);
                 }
@@ -1665,18 +1759,22 @@ __global__ void __launch_bounds__(tm_threads(XIN), 1) gemm_tm_kernel(const __gri
                 }
                 tc_fence_after();
                 const float* sj = scl + j * 3 * GT;
-                const float dw = sj[row], dmw = sj[GT + row];
+                const float dw = sj[row], dmw = FMT == Q6TM ? 0.0f : sj[GT + row];
                 const float* dxv = sj + 2 * GT + 64 * chalf;
                 // D1 and D2 together: + dx * (d * isum - dmin * msum)
 #pragma unroll
                 for (int cc = 0; cc < 8; ++cc) {
                     uint32_t v1[8], v2[8];
-                    tmem_ld8(tl + TM_D2 + 64 * chalf + 8 * cc, v2);
+                    if constexpr (FMT != Q6TM) tmem_ld8(tl + TM_D2 + 64 * chalf + 8 * cc, v2);
                     tmem_ld8(tl + TM_D1 + 128 * j + 64 * chalf + 8 * cc, v1);
                     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
                     for (int c = 0; c < 8; ++c) {
-                        const float t = __fmaf_rn(dw, __uint_as_float(v1[c]), -__fmul_rn(dmw, __uint_as_float(v2[c])));
+                        float t;
+                        if constexpr (FMT == Q6TM)
+                            t = __fmul_rn(dw, __uint_as_float(v1[c]));
+                        else
+                            t = __fmaf_rn(dw, __uint_as_float(v1[c]), -__fmul_rn(dmw, __uint_as_float(v2[c])));
                         acc[8 * cc + c] = __fmaf_rn(dxv[8 * cc + c], t, acc[8 * cc + c]);
                     }
                 }
@@ -2035,7 +2133,12 @@ static cudaError_t gemm_tc_any(int fmt, const uint8_t* w, const uint8_t* xq, flo
         case 3: return gemm_tc<3>(w, xq, y, m, n, k, ws, ws_bytes, nullptr, stream);
         case 4: return gemm_tc<4>(w, xq, y, m, n, k, ws, ws_bytes, nullptr, stream);
         case 5: return gemm_tc<5>(w, xq, y, m, n, k, ws, ws_bytes, nullptr, stream);
-        default: return gemm_tc<6>(w, xq, y, m, n, k, ws, ws_bytes, nullptr, stream);
+        default:
+            // q6_K on the tensor-memory kernel when its blocks come by TMA windows (a
+            // row of blocks a multiple of 16 bytes: nb % 8 == 0; 16-byte aligned weights)
+            if ((k / QK) % 8 == 0 && ((uintptr_t)w & 15u) == 0)
+                return gemm_tc<Q6TM>(w, xq, y, m, n, k, ws, ws_bytes, nullptr, stream);
+            return gemm_tc<6>(w, xq, y, m, n, k, ws, ws_bytes, nullptr, stream);
     }
 }
 
