@@ -1,51 +1,42 @@
-// Prefill GEMM over packed q4_K / q5_K / q6_K weights on the 5th-generation tensor
-// cores (tcgen05, kind::f16), for m >= 9 activation rows (PocketLLM "What
-// it runs": weights stay packed and are decoded inside the kernel; the
-// matmul is a dense contraction once m is large).
+// Prefill GEMM over packed K-quant weights (q2_K .. q6_K) on the
+// 5th-generation tensor cores (tcgen05, kind::f16), for m >= 9 activation rows
+// (PocketLLM "What it runs": weights stay packed and are decoded inside the
+// kernel; the matmul is a dense contraction once m is large).
 //
 // Exactness.  Per 256-weight block the method needs exact integers:
 //   q4_K: isum = sum_j sc_j * sum_l q*q8 and msum = sum_g m_(g/2) * bsum_g,
 //         term = d_x*d_w*isum - dmin_x*d_w*msum;
 //   q5_K: as q4_K with 5-bit q (sc*q <= 63*31 = 1953, still exact in f16);
+//   q2_K: as q4_K with 2-bit q and 16 (sc, m) pairs;
+//   q3_K: isum over (s-32)*(q3+4), msum = sum_g 4 (s_g-32) bsum_g, dmin = d;
 //   q6_K: isum = sum_g sc_g * sum_l (q6-32)*q8, term = d_x*d_w*isum.
-// The operands are integer-valued and exact in f16: activation codes
-// q8 in [-128, 127]; q4_K weights sc*q <= 945; q6_K weights sc*(q6-32) in
-// [-2048, 2048]; bsums in [-2048, 2048]; mins <= 63.  Products and partial
-// sums are integers accumulated in f32, exact while below 2^24 (only an
-// adversarial block can exceed it; the f32 rounding there is far inside the
-// 1e-4 tolerance).  Because d, dmin and d_x change every block, each block
-// accumulates into fresh TMEM columns and is drained and scaled in f32.
-//
-// q6_K scales are int8, so sc*(q6-32) can reach 4096 and is not always
-// exact in f16; the scale is split as sc = 16*hi + lo and the two exact
-// operand tiles hi*(q6-32), lo*(q6-32) go to two accumulators, combined as
-// 16*D_hi + D_lo in the epilogue.
+// The operands are integer-valued and exact in f16: activation codes q8 in
+// [-128, 127]; q4_K weights sc*q <= 945; bsums in [-2048, 2048]; mins <= 63.
+// q6_K scales are int8, so sc*(q6-32) can reach 4096 and is not always exact
+// in f16: the scale is split as sc = 16*hi + lo and the exact operands
+// 16*hi*(q6-32) and lo*(q6-32) are contracted one after the other.  Products
+// and partial sums are integers accumulated in f32, exact while below 2^24
+// (only an adversarial block can exceed it; the f32 rounding there is far
+// inside the 1e-4 tolerance).  Because d, dmin and d_x change every block,
+// each block accumulates into fresh TMEM columns and is drained and scaled in
+// f32.
 //
 // Tile: 128 weight rows (MMA M, TMEM lanes) x 128 activation rows (MMA N,
-// TMEM columns).  q4_K and q5_K run gemm_tm_kernel (below): the decoded A
-// operand goes to tensor memory instead of shared memory.  The description
-// that follows is gemm_kernel, the q6_K path.  Roles per CTA (9 warps):
-//   producer warpgroups (q4_K / q5_K: warps 0-7, two warpgroups; q6_K:
-//     warps 0-3, one): thread t of warpgroup h decodes weight row t of the
-//     tile into the A operand (f16, 128-byte swizzled K-major, one 64-wide
-//     K stage at a time), stages 2h and 2h+1 of every block (q6_K: all
-//     four); warpgroup 0 writes the per-block scales and the last
-//     warpgroup the min operands; thread 0 of a warpgroup issues the TMA
-//     load of the activation stage (f16, same layout) from the workspace
-//     the pre-pass fills.  q4_K / q5_K: the raw weight blocks of the tile
-//     (128 rows x one 256-weight block) and the activations' per-block d_x
-//     and bsums arrive by TMA into a ring of two block slots, up to two
-//     blocks ahead of the decode; q6_K rows (210 bytes, not a 16-byte
-//     multiple) are read by each producer thread one block ahead;
-//   the last warp (one thread): issues the MMAs (M=128, N=128, K=16) and
-//     commits;
-//   the epilogue warpgroup (the four warps before it): drains D1/D2 of each
-//     block from TMEM, applies the scales and accumulates the result in
-//     registers; stores y at the end.
-// A ring of 4 operand stages, double-buffered per-block min operands and
-// scales, and double-buffered TMEM accumulators (2 x (128 + 128) columns)
-// keep the roles overlapped.  Every wait is bounded; a wait that runs out
-// records a fault and the kernel winds down.
+// TMEM columns).  gemm_tm_kernel (q2_K .. q5_K, and q6_K on shapes whose
+// blocks come by TMA) keeps the decoded A operand in tensor memory; its roles
+// are described above it.  gemm_kernel is the q6_K path for the other shapes:
+//   producer warpgroup (warps 0-3): thread t reads weight row t's 210-byte
+//     block one block ahead with its own loads and decodes it into the two
+//     A operand tiles (f16, 128-byte swizzled K-major, one 64-wide K stage
+//     at a time), writes the per-block scales, and thread 0 issues the TMA
+//     load of the activation stage from the workspace the pre-pass fills;
+//   the epilogue warpgroup (warps 4-7): drains D_hi and D_lo of each block
+//     from TMEM, applies the scales and accumulates in registers; stores y;
+//   warp 8 (one thread): issues the MMAs (M=128, N=128, K=16) and commits.
+// A ring of 3 operand stages, double-buffered scales and double-buffered
+// TMEM accumulators (2 x (128 + 128) columns) keep the roles overlapped.
+// Every wait is bounded; a wait that runs out records a fault and the kernel
+// winds down.
 #include <cuda.h>
 #include <cuda_fp16.h>
 
@@ -72,13 +63,6 @@ template <int PWG> struct GemmRoles {
     static constexpr int NCV = 2;
     static constexpr int threads(bool xin) { return (MMA_WARP + 1 + (xin ? NCV : 0)) * 32; }
 };
-// With two producer warpgroups the block launches at 128 registers a thread
-// (13 warps); the producers then give up 32 each and the epilogue warpgroup,
-// whose 128 f32 accumulators per thread need them, takes 64 more: 256 * 32 =
-// 128 * 64, so the block's launch total is redistributed, not exceeded.
-constexpr int REG_LAUNCH = 128, REG_PRODUCER = 96, REG_EPILOGUE = 192;
-static_assert(2 * 128 * (REG_LAUNCH - REG_PRODUCER) == 128 * (REG_EPILOGUE - REG_LAUNCH),
-              "register split must add up to the launch allocation");
 // per (activation row, 256-value block) in the workspace: the 16 bsums of
 // the q8_K block as f16 pairs, its d as f32 bits, three zero words
 constexpr int AUXB = 48;
@@ -195,17 +179,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
     asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
                  " [%0], [%1, {%2, %3}], [%4];"
                  :: "r"(smem_u32(dst)), "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar)) : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-                 "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-                   "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-                   "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-                   "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-                   "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-                 : "r"(taddr));
 }
 
 __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
@@ -397,149 +370,6 @@ __device__ __forceinline__ float swiglu1(float g, float u) {
     return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
 }
 
-// ---------------------------------------------------------------------------
-// Weight decoders (one thread = one weight row of the tile)
-// ---------------------------------------------------------------------------
-// q4_K: stage c of a block is chunk c (weights 64c .. 64c+63): K positions
-// 0..31 are the low nibbles of qs[32c .. 32c+31] times sc_(2c), positions
-// 32..63 the high nibbles times sc_(2c+1).
-template <int NRAW>
-struct QxKRow {
-    uint4 raw[NRAW];         // the block (q4_K 144 bytes, q5_K 176 bytes)
-    float d, dmin;
-    uint32_t sc_lo2[4], off_lo2[4], sc_hi2[4], off_hi2[4];   // per chunk c: f16x2 constants
-    int mins[8];
-};
-
-using Q4KRow = QxKRow<9>;
-using Q5KRow = QxKRow<11>;
-
-// header of a q4_K / q5_K block: d, dmin, the f16x2 constants of each chunk, the mins
-template <int NRAW>
-__device__ __forceinline__ void q4K_row_prepare(QxKRow<NRAW>& R) {
-    const uint4 hdr = R.raw[0];
-    R.d = half_bits_to_float(hdr.x);
-    R.dmin = half_bits_to_float(hdr.x >> 16);
-    const uint32_t sc_a = hdr.y & 0x3F3F3F3Fu;
-    const uint32_t m_a = hdr.z & 0x3F3F3F3Fu;
-    const uint32_t sc_b = (hdr.w & 0x0F0F0F0Fu) | ((hdr.y >> 2) & 0x30303030u);
-    const uint32_t m_b = ((hdr.w >> 4) & 0x0F0F0F0Fu) | ((hdr.z >> 2) & 0x30303030u);
-    // 6-bit s as f16 pairs through the 1024 + s bit pattern (exact); the
-    // constants are exact multiples of s by powers of two
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        const uint32_t scw = c < 2 ? sc_a : sc_b;
-        const int sh = 16 * (c & 1);
-        const uint32_t slo = (scw >> sh) & 0xFFu, shi = (scw >> (sh + 8)) & 0xFFu;
-        const __half2 lo2 = __hsub2(bits_h2(0x64006400u | slo | (slo << 16)), bits_h2(0x64006400u));
-        const __half2 hi2 = __hsub2(bits_h2(0x64006400u | shi | (shi << 16)), bits_h2(0x64006400u));
-        // low nibble magic: (1024 + q) * sc - 1024 * sc; high: (1024 + 16q) * sc/16 - 64 * sc
-        R.sc_lo2[c] = h2_bits(lo2);
-        R.off_lo2[c] = h2_bits(__hmul2(lo2, bits_h2(0xE400E400u)));   // x (-1024)
-        R.sc_hi2[c] = h2_bits(__hmul2(hi2, bits_h2(0x2C002C00u)));    // x 1/16
-        R.off_hi2[c] = h2_bits(__hmul2(hi2, bits_h2(0xD400D400u)));   // x (-64)
-    }
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const uint32_t mw = j < 4 ? m_a : m_b;
-        R.mins[j] = (mw >> (8 * (j & 3))) & 0xFF;
-    }
-}
-
-// writes the 64 f16 values of stage c into row `row` of a swizzled tile
-__device__ __forceinline__ void q4K_row_stage(const Q4KRow& R, int c, uint8_t* tile, int row) {
-    const uint4 qa = R.raw[1 + 2 * c], qb = R.raw[2 + 2 * c];
-    const uint32_t q[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
-    const __half2 slo = bits_h2(R.sc_lo2[c]), olo = bits_h2(R.off_lo2[c]);
-    const __half2 shi = bits_h2(R.sc_hi2[c]), ohi = bits_h2(R.off_hi2[c]);
-#pragma unroll
-    for (int ch = 0; ch < 4; ++ch) {          // 16-byte chunk ch: positions 8ch .. 8ch+7 (and 32 + ...)
-        uint32_t lo[4], hi[4];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const uint32_t w = q[2 * ch + h];
-            const uint32_t x01 = __byte_perm(w, 0, 0x4140), x23 = __byte_perm(w, 0, 0x4342);
-            lo[2 * h] = h2_bits(__hfma2(bits_h2((x01 & 0x000F000Fu) | 0x64006400u), slo, olo));
-            lo[2 * h + 1] = h2_bits(__hfma2(bits_h2((x23 & 0x000F000Fu) | 0x64006400u), slo, olo));
-            hi[2 * h] = h2_bits(__hfma2(bits_h2((x01 & 0x00F000F0u) | 0x64006400u), shi, ohi));
-            hi[2 * h + 1] = h2_bits(__hfma2(bits_h2((x23 & 0x00F000F0u) | 0x64006400u), shi, ohi));
-        }
-        *reinterpret_cast<uint4*>(tile + sw128_chunk(row, ch)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-        *reinterpret_cast<uint4*>(tile + sw128_chunk(row, ch + 4)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-    }
-}
-
-// q5_K: as q4_K, with the fifth bit of each weight from qh[32] (raw[1..2]):
-// weight 64c + l takes bit 2c of qh[l], weight 64c + 32 + l bit 2c + 1.  In
-// f16, 1024 + q5 (low) and 1024 + 16 q5 (high) are still exact, so the same
-// multiply-add constants give sc * q5.
-__device__ __forceinline__ void q5K_row_stage(const Q5KRow& R, int c, uint8_t* tile, int row) {
-    const uint4 qa = R.raw[3 + 2 * c], qb = R.raw[4 + 2 * c];
-    const uint32_t q[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
-    const uint32_t qh[8] = {R.raw[1].x, R.raw[1].y, R.raw[1].z, R.raw[1].w,
-                            R.raw[2].x, R.raw[2].y, R.raw[2].z, R.raw[2].w};
-    const __half2 slo = bits_h2(R.sc_lo2[c]), olo = bits_h2(R.off_lo2[c]);
-    const __half2 shi = bits_h2(R.sc_hi2[c]), ohi = bits_h2(R.off_hi2[c]);
-#pragma unroll
-    for (int ch = 0; ch < 4; ++ch) {
-        uint32_t lo[4], hi[4];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const uint32_t w = q[2 * ch + h], b = qh[2 * ch + h];
-            const uint32_t x01 = __byte_perm(w, 0, 0x4140), x23 = __byte_perm(w, 0, 0x4342);
-            const uint32_t h01 = __byte_perm(b, 0, 0x4140), h23 = __byte_perm(b, 0, 0x4342);
-            const uint32_t l01 = (x01 & 0x000F000Fu) | (((h01 >> (2 * c)) & 0x00010001u) << 4);
-            const uint32_t l23 = (x23 & 0x000F000Fu) | (((h23 >> (2 * c)) & 0x00010001u) << 4);
-            const uint32_t u01 = (x01 & 0x00F000F0u) | (((h01 >> (2 * c + 1)) & 0x00010001u) << 8);
-            const uint32_t u23 = (x23 & 0x00F000F0u) | (((h23 >> (2 * c + 1)) & 0x00010001u) << 8);
-            lo[2 * h] = h2_bits(__hfma2(bits_h2(l01 | 0x64006400u), slo, olo));
-            lo[2 * h + 1] = h2_bits(__hfma2(bits_h2(l23 | 0x64006400u), slo, olo));
-            hi[2 * h] = h2_bits(__hfma2(bits_h2(u01 | 0x64006400u), shi, ohi));
-            hi[2 * h + 1] = h2_bits(__hfma2(bits_h2(u23 | 0x64006400u), shi, ohi));
-        }
-        *reinterpret_cast<uint4*>(tile + sw128_chunk(row, ch)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-        *reinterpret_cast<uint4*>(tile + sw128_chunk(row, ch + 4)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-    }
-}
-
-// The same stage decoded into the 32 tensor-memory columns of row `row` of
-// the A operand (column i holds K positions 2i, 2i + 1 as an f16 pair; low
-// nibbles are columns 4ch .. 4ch + 3, high nibbles 16 + 4ch ..).
-template <int FMT, int NRAW>
-__device__ __forceinline__ void qxK_row_stage_regs(const QxKRow<NRAW>& R, int c, uint32_t (&v)[32]) {
-    constexpr int QW = FMT == 5 ? 3 : 1;   // first qs word of the block (q5_K: after qh[32])
-    const uint4 qa = R.raw[QW + 2 * c], qb = R.raw[QW + 1 + 2 * c];
-    const uint32_t q[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
-    uint32_t qh[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    if constexpr (FMT == 5) {
-        qh[0] = R.raw[1].x; qh[1] = R.raw[1].y; qh[2] = R.raw[1].z; qh[3] = R.raw[1].w;
-        qh[4] = R.raw[2].x; qh[5] = R.raw[2].y; qh[6] = R.raw[2].z; qh[7] = R.raw[2].w;
-    }
-    const __half2 slo = bits_h2(R.sc_lo2[c]), olo = bits_h2(R.off_lo2[c]);
-    const __half2 shi = bits_h2(R.sc_hi2[c]), ohi = bits_h2(R.off_hi2[c]);
-#pragma unroll
-    for (int ch = 0; ch < 4; ++ch) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const uint32_t w = q[2 * ch + h];
-            const uint32_t x01 = __byte_perm(w, 0, 0x4140), x23 = __byte_perm(w, 0, 0x4342);
-            uint32_t l01 = x01 & 0x000F000Fu, l23 = x23 & 0x000F000Fu;
-            uint32_t u01 = x01 & 0x00F000F0u, u23 = x23 & 0x00F000F0u;
-            if constexpr (FMT == 5) {
-                const uint32_t b = qh[2 * ch + h];
-                const uint32_t h01 = __byte_perm(b, 0, 0x4140), h23 = __byte_perm(b, 0, 0x4342);
-                l01 |= ((h01 >> (2 * c)) & 0x00010001u) << 4;
-                l23 |= ((h23 >> (2 * c)) & 0x00010001u) << 4;
-                u01 |= ((h01 >> (2 * c + 1)) & 0x00010001u) << 8;
-                u23 |= ((h23 >> (2 * c + 1)) & 0x00010001u) << 8;
-            }
-            v[4 * ch + 2 * h] = h2_bits(__hfma2(bits_h2(l01 | 0x64006400u), slo, olo));
-            v[4 * ch + 2 * h + 1] = h2_bits(__hfma2(bits_h2(l23 | 0x64006400u), slo, olo));
-            v[16 + 4 * ch + 2 * h] = h2_bits(__hfma2(bits_h2(u01 | 0x64006400u), shi, ohi));
-            v[16 + 4 * ch + 2 * h + 1] = h2_bits(__hfma2(bits_h2(u23 | 0x64006400u), shi, ohi));
-        }
-    }
-}
 
 // One producer warpgroup's share of a q4_K / q5_K row (tensor-memory GEMM):
 // the header and the qs (q5_K: and qh) of its two chunks 2h, 2h + 1 with
@@ -566,7 +396,9 @@ __device__ __forceinline__ void qxK_half_load(QxKHalf<FMT>& R, const uint8_t* ro
     for (int u = 0; u < 4; ++u) R.qs[u] = p[QW + 4 * half + u];
 }
 
-// d, dmin and the multiply-add constants of chunks 2h, 2h + 1 (as q4K_row_prepare)
+// d, dmin and the multiply-add constants of chunks 2h, 2h + 1: the 6-bit s as f16
+// through the 1024 + s bit pattern; low nibbles (1024 + q) * sc - 1024 * sc,
+// high nibbles in place (1024 + 16 q) * sc / 16 - 64 * sc, all exact
 template <int FMT>
 __device__ __forceinline__ void qxK_half_prepare(QxKHalf<FMT>& R, int half) {
     const uint4 hdr = R.hdr;
@@ -596,7 +428,10 @@ __device__ __forceinline__ void qxK_min_pairs(const uint4 hdr, uint32_t (&mv)[8]
     }
 }
 
-// chunk c = 2h + CL into the 32 tensor-memory columns of the row (as qxK_row_stage_regs)
+// chunk c = 2h + CL (weights 64c .. 64c + 63) into the 32 tensor-memory columns of
+// the row: column i holds K positions 2i, 2i + 1 as an f16 pair; K 0..31 are the low
+// nibbles of qs[32c .. 32c + 31] times sc_(2c), K 32..63 the high nibbles times
+// sc_(2c+1) (q5_K: the fifth bit from qh[l], bit 2c resp. 2c + 1)
 template <int FMT, int CL>
 __device__ __forceinline__ void qxK_half_stage_regs(const QxKHalf<FMT>& R, int c, uint32_t (&v)[32]) {
     const uint4 qa = R.qs[2 * CL], qb = R.qs[2 * CL + 1];
@@ -629,99 +464,10 @@ __device__ __forceinline__ void qxK_half_stage_regs(const QxKHalf<FMT>& R, int c
     }
 }
 
-// q2_K / q3_K rows (tensor-memory GEMM).  A block arrives in a window that
-// starts at the 16-byte boundary at or below it (the same skew for every row
-// of the tile when the weights are 16-byte aligned and a row of blocks is a
-// multiple of 16 bytes); the producer realigns it into words.  Stage c holds
-// weights 64c .. 64c+63, the 16-weight groups 4c .. 4c+3.  In both formats
-// group g takes the two low code bits of weight l from bits 2j, 2j+1 of
-// qs[32h + 16p + l], h = g / 8, j = (g % 8) / 2, p = g % 2: stage c reads
-// qs[32h .. 32h + 31] (h = c / 2), field j0 = 2 (c % 2) for groups 4c, 4c+1
-// (K 0..31) and j1 = j0 + 1 for groups 4c+2, 4c+3 (K 32..63).  The field is
-// used in place: (x & (3 << 2j)) | 0x6400 is f16 1024 + 4^j q, exact, and one
-// multiply-add with s / 4^j and -1024 s / 4^j (exact powers of two) gives
-// s * q with a single rounding of an exact result.
-//   q2_K: s = sc_g (4 bits), operand sc_g * q (<= 45); the min operand is the
-//         16 m_g against the 16 bsums, term d_x (d isum - dmin msum).
-//   q3_K: the code is q3 = u - 4, u = low2 + 4 hbit (hbit: bit 4h + j of
-//         hmask[16p + l]), moved in place to bit 2j + 2; operand S_g * u with
-//         S_g = s6_g - 32 (|S u| <= 224), and the -4 S_g bsum_g part goes
-//         through the min operand (4 S_g against the bsums, dmin = d).
-template <int NW>
-struct QlowRow {
-    uint32_t w[NW];   // the block's words (q3_K: the last word's high half lies past the block)
-    float d, dmin;
-};
-using Q2KRow = QlowRow<21>;
-using Q3KRow = QlowRow<28>;
-
-// the block's words from its window (WW words, 16-byte aligned in shared
-// memory) shifted down by sk bytes (sk even, the same for the whole tile)
-template <int NW, int WW>
-__device__ __forceinline__ void qlow_row_load(QlowRow<NW>& R, const uint8_t* win, int sk) {
-    static_assert(NW + 4 <= WW, "window");
-    uint32_t x[WW];
-#pragma unroll
-    for (int u = 0; u < WW / 4; ++u) {
-        const uint4 q = reinterpret_cast<const uint4*>(win)[u];
-        x[4 * u] = q.x; x[4 * u + 1] = q.y; x[4 * u + 2] = q.z; x[4 * u + 3] = q.w;
-    }
-    const uint32_t sh = (uint32_t)(sk & 2) * 8u;   // 0 or 16 bits
-    switch (sk >> 2) {
-#define PLM_QLOW_CASE(K)                                                        \
-    case K:                                                                     \
-        _Pragma("unroll") for (int i = 0; i < NW; ++i) R.w[i] = __funnelshift_r(x[i + K], x[i + K + 1], sh); \
-        break;
-        PLM_QLOW_CASE(0)
-        PLM_QLOW_CASE(1)
-        PLM_QLOW_CASE(2)
-        default:
-        _Pragma("unroll") for (int i = 0; i < NW; ++i) R.w[i] = __funnelshift_r(x[i + 3], x[i + 4], sh);
-        break;
-#undef PLM_QLOW_CASE
-    }
-}
-
-__device__ __forceinline__ void q2K_row_prepare(Q2KRow& R) {
-    R.d = half_bits_to_float(R.w[20] & 0xFFFFu);    // bytes 80, 81
-    R.dmin = half_bits_to_float(R.w[20] >> 16);     // bytes 82, 83
-}
-
-__device__ __forceinline__ void q3K_row_prepare(Q3KRow& R) {
-    R.d = half_bits_to_float(R.w[27] & 0xFFFFu);    // bytes 108, 109
-    R.dmin = R.d;                                   // the -4 S bsum part
-}
-
-// q3_K six-bit scale s6_g of group g (0..15) from the 12 packed bytes
-// (words 24..26): low four bits from byte g % 8 (nibble g / 8), top two
-// from byte 8 + g % 4 (bits 2 (g / 4), +1)
-__device__ __forceinline__ uint32_t q3K_s6(const Q3KRow& R, int g) {
-    const int lb = g & 7, hb = 8 + (g & 3);
-    const uint32_t lo = (R.w[24 + (lb >> 2)] >> (8 * (lb & 3) + 4 * (g >> 3))) & 15u;
-    const uint32_t hi = (R.w[24 + (hb >> 2)] >> (8 * (hb & 3) + 2 * (g >> 2))) & 3u;
-    return lo | (hi << 4);
-}
 
 // f16 pair of two small non-negative integers a, b < 1024 (exact)
 __device__ __forceinline__ __half2 small_pair(uint32_t a, uint32_t b) {
     return __hsub2(bits_h2(0x64006400u | a | (b << 16)), bits_h2(0x64006400u));
-}
-
-// the min operand's first 16 K positions as eight f16 pairs (groups 2i, 2i + 1)
-__device__ __forceinline__ void q2K_min_pairs(const Q2KRow& R, uint32_t (&mv)[8]) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const uint32_t w = R.w[i >> 1] >> (16 * (i & 1));   // scale bytes 2i, 2i + 1
-        mv[i] = h2_bits(small_pair((w >> 4) & 15u, (w >> 12) & 15u));
-    }
-}
-
-__device__ __forceinline__ void q3K_min_pairs(const Q3KRow& R, uint32_t (&mv)[8]) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {   // 4 S = 4 s6 - 128, exact
-        const __half2 s = small_pair(q3K_s6(R, 2 * i), q3K_s6(R, 2 * i + 1));
-        mv[i] = h2_bits(__hfma2(s, bits_h2(0x44004400u), bits_h2(0xD800D800u)));   // x 4, - 128
-    }
 }
 
 // One producer warpgroup's share of a q2_K / q3_K row: the qs words of its
@@ -1081,113 +827,29 @@ __global__ void __launch_bounds__(GemmRoles<GemmCfg<FMT>::PWG>::threads(XIN), 1)
     if (warp < EPI_WARP0) {
         // ------------------------------------------------------- producers
         const int t = tid & (GT - 1);          // weight row (and activation row) of the tile
-        const int half = warp >> 2;            // this warpgroup's stages: [c0, c0 + 4 / PWG)
-        const int c0 = half * (4 / PWG);
-        if constexpr (PWG == 2) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" :: "n"(REG_PRODUCER));
         const int r = r0 + t, i = i0 + t;
         const bool wrow = r < A.n, xrow = i < A.m;
-        using Row = typename std::conditional<FMT == 6, Q6KRow,
-                                              typename std::conditional<FMT == 5, Q5KRow, Q4KRow>::type>::type;
-        Row R, Rn;
-        auto load_row = [&](Row& dst, int b) {
-            if constexpr (FMT != 6) {
-                constexpr int NRAW = FMT == 5 ? 11 : 9;
-                constexpr int BYTES = FMT == 5 ? Q5K_BYTES : Q4K_BYTES;
-                if (wrow) {
-                    const uint4* src = reinterpret_cast<const uint4*>(A.w + ((size_t)r * nb + b) * BYTES);
-#pragma unroll
-                    for (int u = 0; u < NRAW; ++u) dst.raw[u] = __ldg(src + u);
-                } else {
-#pragma unroll
-                    for (int u = 0; u < NRAW; ++u) dst.raw[u] = make_uint4(0, 0, 0, 0);
-                }
-            } else {
-                q6K_row_load(dst, A.w + ((size_t)r * nb + b) * Q6K_BYTES, wrow);
-            }
+        Q6KRow R, Rn;
+        auto load_row = [&](Q6KRow& dst, int b) {
+            q6K_row_load(dst, A.w + ((size_t)r * nb + b) * Q6K_BYTES, wrow);
         };
-        constexpr int BS = GemmCfg<FMT>::BSLOTS;
-        // q4_K / q5_K: block bb of this CTA's K range into slot bb % BS (thread 0)
-        int nissued = 0;   // thread 0: blocks issued so far
-        auto issue_block = [&](int bb) {
-            if constexpr (BS > 0) {
-                ++nissued;
-                const int s = bb % BS;
-                uint8_t* dst = sm + L::BRING + s * L::BSLOT;
-                mbar_arrive_expect_tx(&bfull[s], (uint32_t)L::BTX);
-                tma_load_2d(dst, &wmap, (kb0 + bb) * GemmCfg<FMT>::WROW, r0, &bfull[s]);
-                tma_load_2d(dst + L::WT, &amap, (kb0 + bb) * AUXB, i0, &bfull[s]);
-            }
-        };
-        if constexpr (BS > 0) {
-            if (tid == 0)
-                for (int bb = 0; bb < BS && bb < kcount; ++bb) issue_block(bb);
-        } else {
-            load_row(R, kb0);
-        }
+        load_row(R, kb0);
         int b = 0;
         for (; b < kcount && ok; ++b) {
             const int j = b & 1;
-            float dx = 0.0f;
-            uint32_t bsw[8];   // q4_K / q5_K: the activation row's bsums 2g, 2g+1 as f16 pairs
-            if constexpr (BS > 0) {
-                // this block's weight row and activation side data, from the slot into registers
-                const int s = b % BS;
-                const uint32_t ph = (uint32_t)(b / BS) & 1u;
-                if (!mbar_wait(&bfull[s], ph)) { ok = false; break; }
-                const uint8_t* slot = sm + L::BRING + s * L::BSLOT;
-                constexpr int NRAW = GemmCfg<FMT>::WROW / 16;
-#pragma unroll
-                for (int u = 0; u < NRAW; ++u)
-                    R.raw[u] = reinterpret_cast<const uint4*>(slot + t * GemmCfg<FMT>::WROW)[u];
-                const uint4* ax = reinterpret_cast<const uint4*>(slot + L::WT + t * AUXB);
-                const uint4 a0 = ax[0], a1 = ax[1], a2 = ax[2];
-                bsw[0] = a0.x; bsw[1] = a0.y; bsw[2] = a0.z; bsw[3] = a0.w;
-                bsw[4] = a1.x; bsw[5] = a1.y; bsw[6] = a1.z; bsw[7] = a1.w;
-                dx = __uint_as_float(a2.x);
-                fence_async_smem();   // these reads before the slot's refill by TMA
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bempty[s]);
-            }
-            float dw, dmw = 0.0f;
-            if constexpr (FMT != 6) {
-                q4K_row_prepare(R);
-                dw = R.d;
-                dmw = R.dmin;
-            } else {
-                dw = half_bits_to_float(R.raw[52]);
-            }
-            if (b >= 2) {   // slot j's min operands (last warpgroup) and scales (warpgroup 0) are free again
+            const float dw = half_bits_to_float(R.raw[52]);
+            if (b >= 2) {   // slot j's scales are free again
                 ok = mbar_wait(&minempty[j], ((b >> 1) - 1) & 1) && mbar_wait(&tempty[j], ((b >> 1) - 1) & 1);
                 if (!ok) break;
             }
-            if constexpr (FMT == 6) {
-                const uint8_t* xb = A.xq + ((size_t)i * nb + kb0 + b) * Q8K_BYTES;
-                if (half == 0 && xrow) dx = __ldg(reinterpret_cast<const float*>(xb));
-            }
-            if constexpr (FMT != 6) if (half == PWG - 1) {
-                // min operands: K 0..15 the weight row's mins m_(g/2); K 16..31 the activation row's bsums
-                uint8_t* mt = sm + L::MIN + j * TILE_BYTES;
-                uint32_t mv[8], bv[8];
-#pragma unroll
-                for (int g = 0; g < 8; ++g) {
-                    const uint32_t mm = (uint32_t)R.mins[g];
-                    mv[g] = h2_bits(__hsub2(bits_h2(0x64006400u | mm | (mm << 16)), bits_h2(0x64006400u)));
-                    bv[g] = bsw[g];   // f16 pairs from the pre-pass; rows past m arrive as zeros
-                }
-                *reinterpret_cast<uint4*>(mt + sw128_chunk(t, 0)) = make_uint4(mv[0], mv[1], mv[2], mv[3]);
-                *reinterpret_cast<uint4*>(mt + sw128_chunk(t, 1)) = make_uint4(mv[4], mv[5], mv[6], mv[7]);
-                *reinterpret_cast<uint4*>(mt + sw128_chunk(t, 2)) = make_uint4(bv[0], bv[1], bv[2], bv[3]);
-                *reinterpret_cast<uint4*>(mt + sw128_chunk(t, 3)) = make_uint4(bv[4], bv[5], bv[6], bv[7]);
-            }
-            if (half == 0) {
+            {
                 float* sj = scl + j * 3 * GT;
+                const uint8_t* xb = A.xq + ((size_t)i * nb + kb0 + b) * Q8K_BYTES;
                 sj[t] = dw;
-                sj[GT + t] = dmw;
-                sj[2 * GT + t] = dx;
+                sj[GT + t] = 0.0f;
+                sj[2 * GT + t] = xrow ? __ldg(reinterpret_cast<const float*>(xb)) : 0.0f;
             }
-
-            if constexpr (BS == 0)
-                if (b + 1 < kcount) load_row(Rn, kb0 + b + 1);   // next block's bytes, in flight while this one is decoded
+            if (b + 1 < kcount) load_row(Rn, kb0 + b + 1);   // next block's bytes, in flight while this one is decoded
             // stage c of the block (c a compile-time constant, so R's fields stay in registers)
             auto stage = [&](auto cc_) -> bool {
                 constexpr int c = decltype(cc_)::value;
@@ -1198,55 +860,24 @@ __global__ void __launch_bounds__(GemmRoles<GemmCfg<FMT>::PWG>::threads(XIN), 1)
                     mbar_expect_tx(&full[s], TILE_BYTES);
                     tma_load_2d(st + BOFF, &xmap, (kb0 + b) * QK + c * KS, i0, &full[s]);
                 }
-                if constexpr (FMT == 5)
-                    q5K_row_stage(R, c, st, t);
-                else if constexpr (FMT == 4)
-                    q4K_row_stage(R, c, st, t);
-                else
-                    q6K_row_stage(R, c, st, st + TILE_BYTES, t);
-                if constexpr (NSTAGE < 4) {
-                    // a ring shorter than a block (q6_K): stage c + NSTAGE reuses this
-                    // slot, so the MMA must have it before the block is finished
-                    fence_async_smem();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&full[s]);
-                }
+                q6K_row_stage(R, c, st, st + TILE_BYTES, t);
+                // the ring is shorter than a block: stage c + NSTAGE reuses this
+                // slot, so the MMA must have it before the block is finished
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&full[s]);
                 return true;
             };
             using C0 = std::integral_constant<int, 0>;
             using C1 = std::integral_constant<int, 1>;
             using C2 = std::integral_constant<int, 2>;
             using C3 = std::integral_constant<int, 3>;
-            if constexpr (PWG == 1)
-                ok = stage(C0{}) && stage(C1{}) && stage(C2{}) && stage(C3{});
-            else
-                ok = half == 0 ? (stage(C0{}) && stage(C1{})) : (stage(C2{}) && stage(C3{}));
+            ok = stage(C0{}) && stage(C1{}) && stage(C2{}) && stage(C3{});
             if (!ok) break;
-            // one proxy fence for the block's min operands, scales and (ring of a
-            // whole block or more) its four stages
-            fence_async_smem();
+            // the block's scales before the epilogue reads them
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&minfull[j]);
-                if constexpr (NSTAGE >= 4) {
-#pragma unroll
-                    for (int cc = 0; cc < 4 / PWG; ++cc) mbar_arrive(&full[(4 * b + c0 + cc) % NSTAGE]);
-                }
-            }
-            if constexpr (BS > 0) {
-                // refill this block's slot once every producer warp has read it (thread 0,
-                // after its own decode so that warp 0 does not stall on the others)
-                if (tid == 0 && b + BS < kcount) {
-                    if (!mbar_wait(&bempty[b % BS], (uint32_t)(b / BS) & 1u)) { ok = false; break; }
-                    issue_block(b + BS);
-                }
-            }
-            if constexpr (BS == 0) R = Rn;
-        }
-        if constexpr (BS > 0) {
-            // after a wait ran out: let this CTA's weight copies still in flight land before it exits
-            if (!ok && tid == 0)
-                for (int bb = b; bb < nissued; ++bb) (void)mbar_wait(&bfull[bb % BS], (uint32_t)(bb / BS) & 1u);
+            if (lane == 0) mbar_arrive(&minfull[j]);
+            R = Rn;
         }
     } else if (warp == MMA_WARP) {
         // ------------------------------------------------------- MMA issuer
@@ -1262,28 +893,17 @@ __global__ void __launch_bounds__(GemmRoles<GemmCfg<FMT>::PWG>::threads(XIN), 1)
                     tc_fence_after();
                     const uint32_t sa = smem_u32(sm + L::RING + s * L::STAGE);
                     const uint64_t db = umma_desc_sw128(sa + BOFF);
-                    if constexpr (FMT != 6) {
-                        const uint64_t da = umma_desc_sw128(sa);
+                    const uint64_t dh = umma_desc_sw128(sa), dl = umma_desc_sw128(sa + TILE_BYTES);
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)    // K = 16 per MMA: +32 bytes = +2 descriptor units
-                            mma_f16(d1, da + 2 * kk, db + 2 * kk, (c | kk) != 0);
-                    } else {
-                        const uint64_t dh = umma_desc_sw128(sa), dl = umma_desc_sw128(sa + TILE_BYTES);
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            mma_f16(d1, dh + 2 * kk, db + 2 * kk, (c | kk) != 0);
-                            mma_f16(d2, dl + 2 * kk, db + 2 * kk, (c | kk) != 0);
-                        }
+                    for (int kk = 0; kk < 4; ++kk) {   // K = 16 per MMA: +32 bytes = +2 descriptor units
+                        mma_f16(d1, dh + 2 * kk, db + 2 * kk, (c | kk) != 0);
+                        mma_f16(d2, dl + 2 * kk, db + 2 * kk, (c | kk) != 0);
                     }
                     mma_commit(&empty[s]);
                 }
                 if (!ok) break;
                 if (!mbar_wait(&minfull[j], (b >> 1) & 1)) { ok = false; break; }
                 tc_fence_after();
-                if constexpr (FMT != 6) {
-                    const uint32_t ma = smem_u32(sm + L::MIN + j * TILE_BYTES);
-                    mma_f16(d2, umma_desc_sw128(ma), umma_desc_sw128(ma) + 2, 0u);
-                }
                 mma_commit(&minempty[j]);
                 mma_commit(&tfull[j]);
             }
@@ -1337,7 +957,6 @@ __global__ void __launch_bounds__(GemmRoles<GemmCfg<FMT>::PWG>::threads(XIN), 1)
         }
     } else {
         // ------------------------------------------------------- epilogue
-        if constexpr (PWG == 2) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" :: "n"(REG_EPILOGUE));
         const int e = tid - EPI_WARP0 * 32;      // TMEM lane = weight row of the tile
         const int q = warp & 3;                  // this warp's lane quarter
         float acc[GT];
@@ -1351,7 +970,7 @@ __global__ void __launch_bounds__(GemmRoles<GemmCfg<FMT>::PWG>::threads(XIN), 1)
             }
             tc_fence_after();
             const float* sj = scl + j * 3 * GT;
-            const float dw = sj[e], dmw = sj[GT + e];
+            const float dw = sj[e];
             const uint32_t base = tmem + ((uint32_t)(q * 32) << 16) + j * 256;
 #pragma unroll
             for (int cc = 0; cc < 8; ++cc) {
@@ -1362,11 +981,8 @@ __global__ void __launch_bounds__(GemmRoles<GemmCfg<FMT>::PWG>::threads(XIN), 1)
 #pragma unroll
                 for (int c = 0; c < 16; ++c) {
                     const float dx = sj[2 * GT + 16 * cc + c];
-                    float tt;
-                    if constexpr (FMT != 6)   // d*isum - dmin*msum
-                        tt = __fmaf_rn(dw, __uint_as_float(v1[c]), -__fmul_rn(dmw, __uint_as_float(v2[c])));
-                    else                      // d*(16*hi + lo)
-                        tt = __fmul_rn(dw, __fmaf_rn(16.0f, __uint_as_float(v1[c]), __uint_as_float(v2[c])));
+                    // d * (16 D_hi + D_lo)
+                    const float tt = __fmul_rn(dw, __fmaf_rn(16.0f, __uint_as_float(v1[c]), __uint_as_float(v2[c])));
                     acc[16 * cc + c] = __fmaf_rn(dx, tt, acc[16 * cc + c]);
                 }
             }
