@@ -441,20 +441,29 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_x16_kernel(const __grid_const
             }
         }
         __syncthreads();
-        // y for the round's tiles: thread i takes (tile slot j, row) = (i / 16, i % 16)
-        // of each activation row; the KW partials are added in kw order
-        const int ntr = min(RT, ntc - rb);
-        for (int col = 0; col < A.m; ++col) {
-            for (int i = threadIdx.x; i < ntr * TR; i += WARPS * 32) {
-                const int j = i >> 4, row = i & 15;
-                const int grow = (ct0 + rb + j) * TR + row;
-                if (grow < A.n) {
-                    const float* pp =
-                        part + ((size_t)((j & (TEAMS - 1)) * R + (j >> tl)) * KW) * PART_FLOATS + col * PSTRIDE + row;
-                    float sum = pp[0];
-                    for (int q = 1; q < KW; ++q) sum += pp[q * PART_FLOATS];
-                    A.y[(size_t)col * A.n + grow] = sum;
+        // y for the round's tiles, all m activation rows at once (the other warps
+        // wait meanwhile): item i is activation row col = i / nout and tile row
+        // r = i % nout, i.e. (tile slot j, row) = (r / 16, r % 16); its KW
+        // partials are loaded together and added in kw order
+        const int nout = min(RT, ntc - rb) * TR;
+        for (int i = threadIdx.x; i < A.m * nout; i += THREADS) {
+            const int col = i / nout, r = i - col * nout;
+            const int j = r >> 4, row = r & 15;
+            const int grow = (ct0 + rb + j) * TR + row;
+            if (grow < A.n) {
+                const float* pp =
+                    part + ((size_t)((j & (TEAMS - 1)) * R + (j >> tl)) * KW) * PART_FLOATS + col * PSTRIDE + row;
+                float sum = pp[0];
+#pragma unroll
+                for (int q0 = 0; q0 < WARPS; q0 += 8) {   // eight loads in flight, then their adds
+                    float v[8];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) v[q] = q0 + q < KW ? pp[(q0 + q) * PART_FLOATS] : 0.0f;
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        if (q0 + q >= 1 && q0 + q < KW) sum += v[q];
                 }
+                A.y[(size_t)col * A.n + grow] = sum;
             }
         }
         __syncthreads();
