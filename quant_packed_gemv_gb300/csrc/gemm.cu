@@ -187,6 +187,12 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
                  : "r"(taddr));
 }
 
+__device__ __forceinline__ void tmem_ld_n(uint32_t taddr, uint32_t (&r)[8]) { tmem_ld8(taddr, r); }
+__device__ __forceinline__ void tmem_ld_n(uint32_t taddr, uint32_t (&r)[4]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(taddr));
+}
+
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
                  "%14,%15}, [%16];"
@@ -208,6 +214,27 @@ __device__ __forceinline__ void tc_fence_after() {
 
 __device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 __device__ __forceinline__ __half2 bits_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
+
+// Two f32 values in one 64-bit register and the packed f32x2 arithmetic on
+// them (each half rounded as its scalar instruction would round it)
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
 
 // ---------------------------------------------------------------------------
 // In-kernel activation operand (the entry points without a workspace).
@@ -1364,9 +1391,9 @@ __global__ void __launch_bounds__(tm_threads(XIN), 1) gemm_tm_kernel(const __gri
         const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16);
         int gb = 0;
         {
-            float acc[64];
+            uint64_t acc2[32];   // columns 2c, 2c + 1 as f32 pairs (packed f32x2 arithmetic)
 #pragma unroll
-            for (int c = 0; c < 64; ++c) acc[c] = 0.0f;
+            for (int c = 0; c < 32; ++c) acc2[c] = 0ull;
             for (int b = 0; b < kcount && ok; ++b, ++gb) {
                 const int j = gb & 1;
                 if (!mbar_wait(&tfull[j], (gb >> 1) & 1) || !mbar_wait(&minfull[j], (gb >> 1) & 1)) {
@@ -1376,22 +1403,30 @@ __global__ void __launch_bounds__(tm_threads(XIN), 1) gemm_tm_kernel(const __gri
                 tc_fence_after();
                 const float* sj = scl + j * 3 * GT;
                 const float dw = sj[row], dmw = FMT == Q6TM ? 0.0f : sj[GT + row];
-                const float* dxv = sj + 2 * GT + 64 * chalf;
-                // D1 and D2 together: + dx * (d * isum - dmin * msum)
+                const uint64_t dw2 = f2_pack(dw, dw), ndmw2 = f2_pack(-dmw, -dmw);
+                const uint64_t* dxv = reinterpret_cast<const uint64_t*>(sj + 2 * GT + 64 * chalf);
+                // D1 and D2 together: + dx * (d * isum - dmin * msum), two columns per
+                // instruction, each rounded as fma(dx, fma(d, isum, (-dmin) * msum), acc)
+                // CH columns per tensor-memory load (the form without the widening
+                // converters has the registers for fewer, longer-lived loads: 4)
+                constexpr int CH = XIN ? 8 : 4;
 #pragma unroll
-                for (int cc = 0; cc < 8; ++cc) {
-                    uint32_t v1[8], v2[8];
-                    if constexpr (FMT != Q6TM) tmem_ld8(tl + TM_D2 + 64 * chalf + 8 * cc, v2);
-                    tmem_ld8(tl + TM_D1 + 128 * j + 64 * chalf + 8 * cc, v1);
+                for (int cc = 0; cc < 64 / CH; ++cc) {
+                    uint32_t v1[CH], v2[CH];
+                    if constexpr (FMT != Q6TM) tmem_ld_n(tl + TM_D2 + 64 * chalf + CH * cc, v2);
+                    tmem_ld_n(tl + TM_D1 + 128 * j + 64 * chalf + CH * cc, v1);
                     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        float t;
-                        if constexpr (FMT == Q6TM)
-                            t = __fmul_rn(dw, __uint_as_float(v1[c]));
-                        else
-                            t = __fmaf_rn(dw, __uint_as_float(v1[c]), -__fmul_rn(dmw, __uint_as_float(v2[c])));
-                        acc[8 * cc + c] = __fmaf_rn(dxv[8 * cc + c], t, acc[8 * cc + c]);
+                    for (int c = 0; c < CH / 2; ++c) {
+                        const uint64_t i2 = f2_pack(__uint_as_float(v1[2 * c]), __uint_as_float(v1[2 * c + 1]));
+                        uint64_t t;
+                        if constexpr (FMT == Q6TM) {
+                            t = mul_f32x2(dw2, i2);
+                        } else {
+                            const uint64_t m2 = f2_pack(__uint_as_float(v2[2 * c]), __uint_as_float(v2[2 * c + 1]));
+                            t = fma_f32x2(dw2, i2, mul_f32x2(ndmw2, m2));
+                        }
+                        acc2[CH / 2 * cc + c] = fma_f32x2(dxv[CH / 2 * cc + c], t, acc2[CH / 2 * cc + c]);
                     }
                 }
                 // both accumulators read: D2 for the next block's min MMA, D1 for the block after
@@ -1402,6 +1437,9 @@ __global__ void __launch_bounds__(tm_threads(XIN), 1) gemm_tm_kernel(const __gri
                     mbar_arrive(&tempty[j]);
                 }
             }
+            float acc[64];
+#pragma unroll
+            for (int c = 0; c < 32; ++c) f2_unpack(acc2[c], acc[2 * c], acc[2 * c + 1]);
             const int r = r0 + row;
             float* out = A.part ? A.part + (size_t)blockIdx.z * A.m * A.n : A.y;
             if (A.csplit > 1) {
