@@ -5,23 +5,28 @@ Workload of one step: the Qwen3-0.6B decode GEMV set at m = 1.  Each of the
 28 layers holds seven distinct q4_K matrices (n x k): q 2048x1024,
 k 1024x1024, v 1024x1024, o 1024x2048, gate 3072x1024, up 3072x1024,
 down 1024x3072, laid out contiguously (247.7 MB).  Every matrix gets its own
-f32 activation row (N(0,1), seed 1).  A step quantizes all 196 activation
-rows to q8_K (one launch: all k are multiples of 256, so the rows form one
-flat array of 256-element chunks) and runs the 196 GEMVs through the grouped
-entry point (one launch).  The weight set is held twice and consecutive
-steps alternate copies; each copy is larger than the 129 MB L2, so weights
-come from HBM.  The K timed steps replay as one CUDA graph, launched with
-plm_set_overlap(--overlap, default 2): each kernel is scheduled while the
-one before it drains and starts copying its weights (which nothing writes)
-before it waits for that kernel; activations are read only after the wait.
+f32 activation row (N(0,1), seed 1).  A step is one launch of the fused
+producer + grouped GEMV (plm_quantize_gemv_q4K_grouped): each CTA quantizes
+the f32 activations of its problems to q8_K in shared memory, then streams
+its share of the 196 matrices' weight blocks.  The weight set is held twice
+and consecutive steps alternate copies; each copy is larger than the 129 MB
+L2, so weights come from HBM.  The K timed steps replay as one CUDA graph,
+launched with plm_set_overlap(--overlap, default 2): each kernel is
+scheduled while the one before it drains and starts copying its weights
+(which nothing writes) before it waits for that kernel; activations are
+read only after the wait.
 
 Reported beside it (same JSON line):
+  roofline      the fused kernel: algorithmic bytes per launch (weights,
+                f32 activations, y) over its average launch time (CUDA
+                events on its stream).
+  decode_set_two_launch  the same step as two launches (plm_quantize_q8K
+                over all 196 rows, then plm_gemv_q4K_grouped), with the
+                GEMV's own roofline.
   decode_chain  the same layers run as a decoder must run them: per layer
                 four dependent stages (qkv as one 4096-row matrix, o,
                 gate/up as one 6144-row matrix, down), each a quantize and a
                 single GEMV launch, in a CUDA graph.  Latency-bound.
-  roofline      the grouped GEMV kernel: algorithmic bytes per launch over
-                its average launch time (CUDA events on its stream).
   e2e           the step through the C ABI with the activations copied in
                 from pinned host memory and the outputs copied back, the
                 copies of one step overlapping the compute of the next on a
@@ -80,6 +85,8 @@ def parse():
                     help="activation rows for --case (several values: a sweep)")
     ap.add_argument("--no-chain", action="store_true",
                     help="skip the dependent per-layer decode chain measurement")
+    ap.add_argument("--no-two-launch", action="store_true",
+                    help="skip the two-launch (quantize, then grouped GEMV) comparison of the step")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the prefill GEMM, q6_K head and m-sweep measurements")
     ap.add_argument("--overlap", type=int, default=2, choices=[0, 1, 2],
@@ -108,7 +115,14 @@ def quant_bytes(k, m=1):
 
 
 def step_bytes(mats):
+    """Two-launch step: the quantizer (f32 x in, q8_K out), then the GEMV."""
     return sum(gemv_bytes(n, k) + quant_bytes(k) for _, _, n, k, _ in mats)
+
+
+def fused_step_bytes(mats):
+    """The headline step, one fused launch: weights and f32 x read once, y
+    written once (the q8_K codes never leave the chip)."""
+    return sum(n * (k // QK) * Q4K_BYTES + 4 * k + 4 * n for _, _, n, k, _ in mats)
 
 
 # --------------------------------------------------------------- clocks
@@ -624,14 +638,13 @@ class Step:
                      dict(x=x_host2.to(dev), xq=xq2, y=torch.empty_like(self.y), x_host=x_host2,
                           y_host=torch.empty_like(self.y_host).pin_memory())]
         for st in self.sets:
-            st["problems"] = [[(self.w[c].data_ptr() + off, st["xq"].data_ptr() + self.qoff[i],
-                                st["y"].data_ptr() + 4 * self.yoff[i], n, k)
-                               for i, (_, _, n, k, off) in enumerate(self.mats)] for c in range(2)]
+            st["fused"] = [[(self.w[c].data_ptr() + off, st["x"].data_ptr() + 4 * self.xoff[i],
+                             st["y"].data_ptr() + 4 * self.yoff[i], n, k)
+                            for i, (_, _, n, k, off) in enumerate(self.mats)] for c in range(2)]
 
     def run_set(self, q, b, copy, stream):
-        st = self.sets[b]
-        q.plm_quantize_q8K(st["x"], st["xq"], self.nchunks, QK, stream=stream)
-        q.plm_gemv_q4K_grouped(st["problems"][copy], 1, stream=stream)
+        """The headline step on activation/output set b: one fused launch."""
+        q.plm_quantize_gemv_q4K_grouped(self.sets[b]["fused"][copy], 1, stream=stream)
 
     def run_chain_fused(self, q, copy, stream):
         """Decode order with the fused producer: one launch per dependent stage."""
@@ -722,7 +735,8 @@ def main():
     K = args.steps
     with torch.cuda.stream(stream):
         for i in range(max(args.warmup, 3)):
-            st.run(q, i % 2, stream)
+            if not args.no_two_launch:
+                st.run(q, i % 2, stream)
             st.run_fused(q, i % 2, stream)
             q.plm_gemv_q4K_swiglu_grouped(gate_up[i % 2][0], 1, stream=stream)
             q.plm_gemv_q4K_grouped(gate_up[i % 2][1], 1, stream=stream)
@@ -746,11 +760,13 @@ def main():
     run_chain = lambda s: st.run_chain(q, s % 2, stream)
     # the timed graphs: K steps each; single-step graphs: the end-to-end loop
     # and a per-step comparison
-    step_g, gemv_g, fused_g = capture(run_step, K), capture(run_gemv, K), capture(run_fused, K)
+    fused_g = capture(run_fused, K)
+    step_g = None if args.no_two_launch else capture(run_step, K)
+    gemv_g = None if args.no_two_launch else capture(run_gemv, K)
     swiglu_g, gateup_g = capture(run_swiglu, K), capture(run_gateup, K)
     chain_g = None if args.no_chain else capture(run_chain, K)
     chain_fused_g = None if args.no_chain else capture(lambda s: st.run_chain_fused(q, s % 2, stream), K)
-    single = [capture(lambda s, c=c: st.run(q, c, stream), 1) for c in range(2)]
+    single = [capture(lambda s, c=c: st.run_fused(q, c, stream), 1) for c in range(2)]
     torch.cuda.synchronize()
 
     def barrier():
@@ -836,8 +852,8 @@ def main():
         sampler = ClockSampler(local)
         sampler.start()
         time.sleep(0.3)
-        ms = timed_graph(step_g)
-        gemv_ms = timed_graph(gemv_g)
+        ms = timed_graph(step_g) if step_g is not None else None
+        gemv_ms = timed_graph(gemv_g) if gemv_g is not None else None
         fused_ms = timed_graph(fused_g)
         swiglu_ms = timed_graph(swiglu_g)
         gateup_ms = timed_graph(gateup_g)
@@ -851,13 +867,17 @@ def main():
         clocks = sampler.stop()
     fault = q.plm_device_fault()
 
-    alg = step_bytes(mats)
+    # the headline step: the fused producer + GEMV, one grouped launch per 256 problems
+    alg = fused_step_bytes(mats)
+    two_alg = step_bytes(mats)
     gemv_alg = sum(gemv_bytes(n, k) for _, _, n, k, _ in mats)
-    ms_step = ms / args.steps
+    ms_step = fused_ms / args.steps
     value = world * alg / (ms_step * 1e-3) / 1e9
-    launches_grouped = -(-len(mats) // 256)                  # grouped GEMV launches per step
-    gemv_launch_ms = gemv_ms / args.steps / launches_grouped
-    achieved = gemv_alg / launches_grouped / (gemv_launch_ms * 1e-3) / 1e9
+    launches_grouped = -(-len(mats) // 256)                  # grouped launches per step
+    fused_launch_ms = ms_step / launches_grouped
+    achieved = alg / launches_grouped / (fused_launch_ms * 1e-3) / 1e9
+    gemv_launch_ms = gemv_ms / args.steps / launches_grouped if gemv_ms is not None else None
+    gemv_achieved = gemv_alg / launches_grouped / (gemv_launch_ms * 1e-3) / 1e9 if gemv_ms is not None else None
     peaks = {}
     try:
         peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
@@ -869,8 +889,6 @@ def main():
     chain_step = chain_ms / args.steps if chain_ms is not None else None
     swiglu_bytes = sum(2 * n * (k // QK) * Q4K_BYTES + (k // QK) * Q8K_BYTES + 4 * n
                        for (_, j, n, k, _) in mats if j == 4)
-    # fused step: weights, f32 activations read once, y written once
-    fused_bytes = sum(n * (k // QK) * Q4K_BYTES + 4 * k + 4 * n for _, _, n, k, _ in mats)
     chain_fused_bytes = sum(sum(mats[l * 7 + f + j][2] for j in range(c)) * (mats[l * 7 + f][3] // QK) * Q4K_BYTES
                             + 4 * mats[l * 7 + f][3] + 4 * sum(mats[l * 7 + f + j][2] for j in range(c))
                             for l in range(N_LAYERS) for f, c in CHAIN)
@@ -885,19 +903,31 @@ def main():
         "config": {"workload": WORKLOAD, "m": 1, "seed": SEED,
                    "weights_mb": sum(n * (k // QK) * Q4K_BYTES for _, _, n, k, _ in mats) / 1e6,
                    "l2": "inputs larger than L2: two 247.7 MB weight copies, alternate steps",
-                   "launch": "per step 1 q8_K quantize + %d grouped GEMV launch(es); the K timed steps "
-                             "replay as one CUDA graph" % launches_grouped,
+                   "launch": "per step %d launch(es) of plm_quantize_gemv_q4K_grouped (each CTA quantizes "
+                             "its f32 activations to q8_K, then runs the GEMV); the K timed steps replay as "
+                             "one CUDA graph" % launches_grouped,
                    "overlap": {0: "plain stream order", 1: "early launch",
                                2: "early launch with weight prefetch"}[args.overlap]},
         "ms_per_step_one_graph_per_step": single_ms / args.steps,
         "weights_per_s": world * sum(n * k for _, _, n, k, _ in mats) / (ms_step * 1e-3),
-        "gpu_launches": (1 + launches_grouped) * args.steps,
+        "gpu_launches": launches_grouped * args.steps,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": recorded_traffic("gemv_q4K_grouped_m1"),
+                     "frac": achieved / peak, "traffic": recorded_traffic("gemv_q4K_fused_grouped_m1"),
                      "peak_source": peak_src,
-                     "kernel": "q4lane::lane_kernel<m=1, 16 warps, grouped> (q4_K, one lane per block)",
-                     "avg_launch_us": gemv_launch_ms * 1e3,
-                     "bytes_per_launch": gemv_alg / launches_grouped},
+                     "kernel": "q4lane::lane_kernel<m=1, 16 warps, grouped, f32 activations quantized in the CTA> "
+                               "(q4_K, one lane per block)",
+                     "avg_launch_us": fused_launch_ms * 1e3,
+                     "bytes_per_launch": alg / launches_grouped},
+        "decode_set_two_launch": None if ms is None else {
+            "value": world * two_alg / (ms / args.steps * 1e-3) / 1e9, "unit": "GB/s",
+            "ms_per_step": ms / args.steps, "launches_per_step": 1 + launches_grouped,
+            "bytes_per_step": two_alg,
+            "what": "the same step as plm_quantize_q8K then plm_gemv_q4K_grouped (q8_K through HBM)",
+            "gemv_roofline": {"bound": "hbm", "achieved": gemv_achieved, "peak": peak, "unit": "GB/s",
+                              "frac": gemv_achieved / peak, "traffic": recorded_traffic("gemv_q4K_grouped_m1"),
+                              "kernel": "q4lane::lane_kernel<m=1, 16 warps, grouped> on q8_K activations",
+                              "avg_launch_us": gemv_launch_ms * 1e3,
+                              "bytes_per_launch": gemv_alg / launches_grouped}},
         "decode_chain": None if chain_step is None else {
             "value": world * chain_bytes / (chain_step * 1e-3) / 1e9, "unit": "GB/s",
             "ms_per_step": chain_step, "launches_per_step": 8 * N_LAYERS,
@@ -906,11 +936,6 @@ def main():
             "value": world * chain_fused_bytes / (chain_fused_ms / args.steps * 1e-3) / 1e9, "unit": "GB/s",
             "ms_per_step": chain_fused_ms / args.steps, "launches_per_step": 4 * N_LAYERS,
             "what": "the same chain with plm_quantize_gemv_q4K: one launch per dependent stage"},
-        "decode_set_fused": {
-            "value": world * fused_bytes / (fused_ms / args.steps * 1e-3) / 1e9, "unit": "GB/s",
-            "ms_per_step": fused_ms / args.steps, "launches_per_step": launches_grouped,
-            "what": "plm_quantize_gemv_q4K_grouped: the same step as one launch, q8_K produced in-kernel",
-            "bytes_per_step": fused_bytes},
         "swiglu_gate_up": {
             "value": world * swiglu_bytes / (swiglu_ms / args.steps * 1e-3) / 1e9, "unit": "GB/s",
             "us_per_launch": swiglu_ms / args.steps * 1e3,
@@ -920,9 +945,9 @@ def main():
         "e2e": {"value": world * alg / (e2e_pipe_ms / args.steps * 1e-3) / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_pipe_ms / args.steps,
-                "how": "per step: x copied in from pinned host memory, quantize + grouped GEMV, y copied "
-                       "out; copies on a second stream with two buffer sets so they overlap the compute; "
-                       "the K steps captured as one CUDA graph",
+                "how": "per step: x copied in from pinned host memory, the fused quantize + grouped GEMV, "
+                       "y copied out; copies on a second stream with two buffer sets so they overlap the "
+                       "compute; the K steps captured as one CUDA graph",
                 "serial": {"value": world * alg / (e2e_ms_step * 1e-3) / 1e9, "ms_per_step": e2e_ms_step,
                            "how": "copy in, one-step graph, copy out, on one stream, no overlap"}},
         "clocks": clocks,

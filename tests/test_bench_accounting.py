@@ -35,3 +35,13 @@ def test_step_bytes_add_the_quantizer():
     assert k_sum == 286_720
     quant = k_sum * 4 + (k_sum // 256) * 292                      # f32 read + q8_K written
     assert bench.step_bytes(mats) == 249_429_376 + quant
+
+
+def test_fused_step_bytes_are_weights_f32_activations_and_y():
+    # the headline step reads the weights and the f32 activations once and
+    # writes y once; the q8_K codes stay on the chip
+    mats, weights = bench.mat_list()
+    assert weights == 247_726_080
+    x_f32 = 4 * 28 * (1024 + 1024 + 1024 + 2048 + 1024 + 1024 + 3072)
+    y = 4 * 28 * (2048 + 1024 + 1024 + 1024 + 3072 + 3072 + 1024)
+    assert bench.fused_step_bytes(mats) == weights + x_f32 + y == 250_249_216
