@@ -256,9 +256,9 @@ struct Q6Consts {
     uint32_t k0f, k30, magic, m1056;   // 0x0F0F0F0F, 0x30303030, 0x64, f16 (-1056, -1056)
 };
 
-__device__ __forceinline__ float sbyte_f32(uint32_t w_x80, uint32_t sel) {
-    // byte of (scales ^ 0x80) -> 2^23 + 128 + sc as f32 bits, then the offset off
-    return __fadd_rn(__uint_as_float(__byte_perm(w_x80, 0x4B000000u, sel)), -8388736.0f);
+// Signed byte b of w as f32, by the integer-to-float conversion (exact)
+__device__ __forceinline__ float sbyte_i2f(uint32_t w, int b) {
+    return __int2float_rn((int)(int8_t)(uint8_t)(w >> (8 * b)));
 }
 
 __device__ __forceinline__ void tile_block_q6(const uint8_t* slot, int g, int lane, const Q6Consts& K,
@@ -274,8 +274,8 @@ __device__ __forceinline__ void tile_block_q6(const uint8_t* slot, int g, int la
     const uint32_t qlg[2][4] = {{l0.x, l0.y, l0.z, l0.w}, {l1.x, l1.y, l1.z, l1.w}};
     const uint32_t qlh[2][4] = {{l2.x, l2.y, l2.z, l2.w}, {l3.x, l3.y, l3.z, l3.w}};
     const uint32_t qhg[4] = {h0.x, h0.y, h0.z, h0.w}, qhh[4] = {h1.x, h1.y, h1.z, h1.w};
-    const uint32_t scg[4] = {sg.x ^ 0x80808080u, sg.y ^ 0x80808080u, sg.z ^ 0x80808080u, sg.w ^ 0x80808080u};
-    const uint32_t sch[4] = {sh.x ^ 0x80808080u, sh.y ^ 0x80808080u, sh.z ^ 0x80808080u, sh.w ^ 0x80808080u};
+    const uint32_t scg[4] = {sg.x, sg.y, sg.z, sg.w};
+    const uint32_t sch[4] = {sh.x, sh.y, sh.z, sh.w};
     float is[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -300,8 +300,7 @@ __device__ __forceinline__ void tile_block_q6(const uint8_t* slot, int g, int la
                 const uint32_t a3 = h2u(__hadd2(u2h(__byte_perm(ch, K.magic, 0x4342)), m1056));
                 float dd[4] = {0.f, 0.f, 0.f, 0.f};
                 mma16816(dd, a0, a1, a2, a3, F.b[G][0], F.b[G][1]);
-                const uint32_t sel = (uint32_t)(G & 3) | 0x7540u;
-                const float s_g = sbyte_f32(scg[G >> 2], sel), s_h = sbyte_f32(sch[G >> 2], sel);
+                const float s_g = sbyte_i2f(scg[G >> 2], G & 3), s_h = sbyte_i2f(sch[G >> 2], G & 3);
                 is[0] = __fmaf_rn(s_g, dd[0], is[0]);
                 is[1] = __fmaf_rn(s_g, dd[1], is[1]);
                 is[2] = __fmaf_rn(s_h, dd[2], is[2]);
