@@ -9,7 +9,7 @@ cudaError_t run_group_q4K(const HostProblem* probs, int count, int m, bool subdo
 
 // One activation row of the widest row must fit beside the smallest ring.
 bool gemv_supported_q4K(int k) {
-    return q4lane::align128((size_t)q4lane::seg_bytes(k / QK)) + q4lane::ring_bytes<4>(12, 2) <=
+    return q4lane::align128((size_t)q4lane::seg_bytes<4>(k / QK)) + q4lane::ring_bytes<4>(12, 2) <=
            (size_t)smem_optin_bytes();
 }
 

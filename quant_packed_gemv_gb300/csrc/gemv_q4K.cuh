@@ -43,11 +43,19 @@ namespace plm {
 namespace q4lane {
 
 constexpr int STAGE_BLOCKS = 32;
-constexpr int REC = 272;                         // staged bytes per activation block
+// Staged bytes per activation block: the 256 codes, then q4_K/q5_K the eight
+// sums of adjacent bsum pairs (272 bytes, a stride of 68 words), q6_K the
+// sixteen bsums (304 bytes, 76 words); either way eight lanes reading eight
+// different blocks at one offset hit distinct banks.
+template <int FMT> __host__ __device__ constexpr int rec_bytes() { return FMT == 6 ? 304 : 272; }
 
 // Block formats of this kernel: q4_K and q5_K (q4_K plus qh[32], the fifth
-// bit of every weight, between the scale table and qs).  Both are whole
-// 16-byte multiples, so every block of a stage is 16-byte aligned.
+// bit of every weight, between the scale table and qs), whole 16-byte
+// multiples, so every block of a stage is 16-byte aligned; and q6_K (210
+// bytes: ql[128], qh[64], int8 scales[16], f16 d), whose blocks sit at even
+// offsets of a stage.  A q6_K stage is a 16-byte multiple and starts on a
+// 16-byte boundary when a row holds a multiple of eight blocks (8 * 210 =
+// 105 * 16), which the host requires of this path.
 template <int FMT> struct LaneFmt;
 template <> struct LaneFmt<4> {
     static constexpr int BYTES = Q4K_BYTES;
@@ -57,11 +65,18 @@ template <> struct LaneFmt<5> {
     static constexpr int BYTES = Q5K_BYTES;
     static constexpr int QS = 48;
 };
+template <> struct LaneFmt<6> {
+    static constexpr int BYTES = Q6K_BYTES;
+    static constexpr int QS = 0;
+};
+// integer sub-block dots per block in the verification export
+template <int FMT> __host__ __device__ constexpr int sub_per_block() { return FMT == 6 ? 16 : 8; }
 template <int FMT> __host__ __device__ constexpr int slot_bytes() { return STAGE_BLOCKS * LaneFmt<FMT>::BYTES; }
 
 // Bytes of one staged segment of nblk activation blocks: records, then the
 // scales, padded to 16 bytes so the next segment's records stay aligned.
-__host__ __device__ __forceinline__ int seg_bytes(int nblk) { return nblk * REC + ((nblk * 4 + 15) & ~15); }
+template <int FMT>
+__host__ __device__ __forceinline__ int seg_bytes(int nblk) { return nblk * rec_bytes<FMT>() + ((nblk * 4 + 15) & ~15); }
 
 // One problem of a launch.  Work is cut into units: rps whole rows (one
 // stage) when a row has at most 32 blocks, else one row (ceil(nb / 32)
@@ -165,10 +180,10 @@ template <int M, int PER, int MAXP>
 __device__ __forceinline__ ActPos act_begin(const LaneBatch<MAXP>& B, int p0, int pend) {
     return ActPos{p0, 0, p0 < pend ? M * B.p[p0].nb * PER : 0, 0};
 }
-template <int M, int PER, int MAXP>
+template <int FMT, int M, int PER, int MAXP>
 __device__ __forceinline__ void act_seek(const LaneBatch<MAXP>& B, ActPos& a, int idx, int pend) {
     while (a.p < pend && idx >= a.hi) {
-        a.off += seg_bytes(M * B.p[a.p].nb);
+        a.off += seg_bytes<FMT>(M * B.p[a.p].nb);
         a.lo = a.hi;
         ++a.p;
         a.hi = a.p < pend ? a.lo + M * B.p[a.p].nb * PER : a.lo;
@@ -177,14 +192,18 @@ __device__ __forceinline__ void act_seek(const LaneBatch<MAXP>& B, ActPos& a, in
 
 // Word w of a problem's q8_K rows (records of 73 words: d, 64 code words,
 // 8 words of bsum pairs) into its staged segment of nblk records.
+template <int FMT>
 __device__ __forceinline__ void act_store(uint8_t* seg, int nblk, int w, uint32_t v) {
     constexpr int WORDS = Q8K_BYTES / 4;
+    constexpr int REC = rec_bytes<FMT>();
     const int blk = w / WORDS;
     const int wd = w - blk * WORDS;
     if (wd == 0) {
         reinterpret_cast<float*>(seg + (size_t)nblk * REC)[blk] = __uint_as_float(v);
     } else if (wd <= 64) {
         reinterpret_cast<uint32_t*>(seg + (size_t)blk * REC)[wd - 1] = v;
+    } else if constexpr (FMT == 6) {
+        reinterpret_cast<uint32_t*>(seg + (size_t)blk * REC + 256)[wd - 65] = v;   // bsums 2j, 2j+1 as they are
     } else {
         const int j = wd - 65;   // bsums 2j, 2j+1
         const int pair = (int)(int16_t)(v & 0xFFFFu) + (int)(int16_t)(v >> 16);
@@ -194,7 +213,7 @@ __device__ __forceinline__ void act_store(uint8_t* seg, int nblk, int w, uint32_
 
 // q8_K activations: all threads of the CTA copy words, PRE of them per thread
 // loaded before fill().
-template <int M, int PRE, int MAXP, typename Fill>
+template <int FMT, int M, int PRE, int MAXP, typename Fill>
 __device__ __forceinline__ void stage_q8(const LaneBatch<MAXP>& B, int p0, int pend, uint8_t* smem, Fill fill) {
     constexpr int WORDS = Q8K_BYTES / 4;
     const int tid = threadIdx.x, bd = blockDim.x;
@@ -203,7 +222,7 @@ __device__ __forceinline__ void stage_q8(const LaneBatch<MAXP>& B, int p0, int p
 #pragma unroll
     for (int j = 0; j < PRE; ++j) {
         const int idx = tid + j * bd;
-        act_seek<M, WORDS>(B, a, idx, pend);
+        act_seek<FMT, M, WORDS>(B, a, idx, pend);
         pre[j] = a.p < pend ? __ldg(reinterpret_cast<const uint32_t*>(B.p[a.p].xq) + (idx - a.lo)) : 0u;
     }
     fill();
@@ -211,14 +230,14 @@ __device__ __forceinline__ void stage_q8(const LaneBatch<MAXP>& B, int p0, int p
 #pragma unroll
     for (int j = 0; j < PRE; ++j) {
         const int idx = tid + j * bd;
-        act_seek<M, WORDS>(B, a, idx, pend);
-        if (a.p < pend) act_store(smem + a.off, M * B.p[a.p].nb, idx - a.lo, pre[j]);
+        act_seek<FMT, M, WORDS>(B, a, idx, pend);
+        if (a.p < pend) act_store<FMT>(smem + a.off, M * B.p[a.p].nb, idx - a.lo, pre[j]);
     }
     for (int idx = tid + PRE * bd;; idx += bd) {
-        act_seek<M, WORDS>(B, a, idx, pend);
+        act_seek<FMT, M, WORDS>(B, a, idx, pend);
         if (a.p >= pend) break;
-        act_store(smem + a.off, M * B.p[a.p].nb, idx - a.lo,
-                  __ldg(reinterpret_cast<const uint32_t*>(B.p[a.p].xq) + (idx - a.lo)));
+        act_store<FMT>(smem + a.off, M * B.p[a.p].nb, idx - a.lo,
+                       __ldg(reinterpret_cast<const uint32_t*>(B.p[a.p].xq) + (idx - a.lo)));
     }
 }
 
@@ -229,9 +248,10 @@ __device__ __forceinline__ void stage_q8(const LaneBatch<MAXP>& B, int p0, int p
 template <int M, int WARPS, int MAXP, typename Fill>
 __device__ __forceinline__ void stage_f32(const LaneBatch<MAXP>& B, int p0, int pend, uint8_t* smem, int warp,
                                           int lane, Fill fill) {
+    constexpr int REC = rec_bytes<4>();
     ActPos a = act_begin<M, 1>(B, p0, pend);
     int fc = warp;
-    act_seek<M, 1>(B, a, fc, pend);
+    act_seek<4, M, 1>(B, a, fc, pend);
     float4 v0 = make_float4(0.f, 0.f, 0.f, 0.f), v1 = v0;
     if (a.p < pend) {
         const float4* src = reinterpret_cast<const float4*>(B.p[a.p].xq) + (size_t)(fc - a.lo) * (QK / 4) + 2 * lane;
@@ -258,7 +278,7 @@ __device__ __forceinline__ void stage_f32(const LaneBatch<MAXP>& B, int p0, int 
         if ((lane & 3) == 0) reinterpret_cast<int16_t*>(seg + (size_t)c * REC + 256)[lane >> 2] = (int16_t)sq;
         if (lane == 0) reinterpret_cast<float*>(seg + (size_t)nblk * REC)[c] = d;
         fc += WARPS;
-        act_seek<M, 1>(B, a, fc, pend);
+        act_seek<4, M, 1>(B, a, fc, pend);
         if (a.p < pend) {
             const float4* src =
                 reinterpret_cast<const float4*>(B.p[a.p].xq) + (size_t)(fc - a.lo) * (QK / 4) + 2 * lane;
@@ -365,11 +385,100 @@ __device__ __forceinline__ void lane_block(const Blk& w, const uint8_t* act, int
     }
 }
 
+// q6_K: the block's first 208 bytes (ql[128], qh[64], scales[16]) as 52
+// four-byte words and d.  The block sits at an even offset of the stage: the
+// words are read from the 4-byte boundary at or below it and, for a block at
+// 2 mod 4, realigned by a byte permute (bytes 2, 3 of one word, 0, 1 of the
+// next); d has its own 2-byte load.  Every load stays inside the block's
+// first 212 bytes from the boundary, i.e. inside the stage slot.
+struct Q6Block {
+    uint32_t w[52];
+    uint32_t d;
+};
+__device__ __forceinline__ void q6_block_load(const uint8_t* blk, Q6Block& B) {
+    const uint32_t mis = (uint32_t)(uintptr_t)blk & 2u;
+    const uint32_t* p = reinterpret_cast<const uint32_t*>(blk - mis);
+    const uint32_t sel = mis ? 0x5432u : 0x3210u;
+    uint32_t prev = p[0];
+#pragma unroll
+    for (int j = 0; j < 52; ++j) {
+        const uint32_t next = p[j + 1];
+        B.w[j] = __byte_perm(prev, next, sel);
+        prev = next;
+    }
+    B.d = *reinterpret_cast<const uint16_t*>(blk + 208);
+}
+
+// One whole q6_K block against M staged activation blocks (records
+// act_stride bytes apart: 256 codes, then the 16 bsums; scales dy_stride
+// floats apart).  Weight 128h + 32qq + l takes its low four bits from
+// ql[64h + 32(qq % 2) + l] (the low nibble for qq < 2) and its top two from
+// bits 2qq, 2qq + 1 of qh[32h + l]; both are assembled four codes to a word
+// and dotted with dp4a, and (q6 - 32) . x = q6 . x - 32 bsum per 16-weight
+// group, exact in int32.  isum = sum of scale * group dot, exact in int32;
+// then one f32 term per block, or the sixteen exact group dots.
+template <int M, bool SUBDOTS>
+__device__ __forceinline__ void lane_block_q6(const Q6Block& B, const uint8_t* act, int act_stride, const float* dy,
+                                              int dy_stride, float* v, int32_t* sub, size_t sub_stride) {
+    int isum[M];
+#pragma unroll
+    for (int i = 0; i < M; ++i) isum[i] = 0;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+#pragma unroll
+        for (int qq = 0; qq < 4; ++qq) {
+            uint32_t c[8];   // codes of weights 128h + 32qq + 4u .. 4u + 3
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const uint32_t ql = B.w[16 * h + 8 * (qq & 1) + u], qh = B.w[32 + 8 * h + u];
+                const uint32_t lo = qq < 2 ? ql : ql >> 4;
+                const uint32_t hi = qq == 0 ? qh << 4 : qq == 1 ? qh << 2 : qq == 2 ? qh : qh >> 2;
+                c[u] = (lo & 0x0F0F0F0Fu) | (hi & 0x30303030u);
+            }
+            const int g = 8 * h + 2 * qq;   // groups g (u < 4) and g + 1
+            const uint32_t sw = B.w[48 + (g >> 2)];
+            const int s0 = (int)(int8_t)(uint8_t)(sw >> (8 * (g & 3)));
+            const int s1 = (int)(int8_t)(uint8_t)(sw >> (8 * (g & 3) + 8));
+#pragma unroll
+            for (int i = 0; i < M; ++i) {
+                const uint8_t* a = act + (size_t)i * act_stride;
+                const int4 x0 = *reinterpret_cast<const int4*>(a + 128 * h + 32 * qq);
+                const int4 x1 = *reinterpret_cast<const int4*>(a + 128 * h + 32 * qq + 16);
+                const int bs = *reinterpret_cast<const int*>(a + 256 + 2 * g);   // bsums g, g + 1
+                int d0 = dp4a_us(c[0], x0.x, 0);
+                d0 = dp4a_us(c[1], x0.y, d0);
+                d0 = dp4a_us(c[2], x0.z, d0);
+                d0 = dp4a_us(c[3], x0.w, d0);
+                int d1 = dp4a_us(c[4], x1.x, 0);
+                d1 = dp4a_us(c[5], x1.y, d1);
+                d1 = dp4a_us(c[6], x1.z, d1);
+                d1 = dp4a_us(c[7], x1.w, d1);
+                d0 -= 32 * (int)(int16_t)(bs & 0xFFFF);
+                d1 -= 32 * (bs >> 16);
+                if constexpr (SUBDOTS) {
+                    sub[i * sub_stride + g] = d0;
+                    sub[i * sub_stride + g + 1] = d1;
+                } else {
+                    isum[i] += s0 * d0 + s1 * d1;
+                }
+            }
+        }
+    }
+    if constexpr (!SUBDOTS) {
+        const float d = half_bits_to_float(B.d);
+#pragma unroll
+        for (int i = 0; i < M; ++i) v[i] = __fmaf_rn(dy[i * dy_stride], __fmul_rn(d, (float)isum[i]), v[i]);
+    }
+}
+
 template <int FMT, int M, bool SUBDOTS, bool XF32, bool PAIR, int WARPS, int MAXP>
 __global__ void __launch_bounds__(WARPS * 32, 1) lane_kernel(const __grid_constant__ LaneBatch<MAXP> B) {
     constexpr int PF = PAIR ? 2 : 1;
     constexpr int BYTES = LaneFmt<FMT>::BYTES;
     constexpr int SLOT = slot_bytes<FMT>();
+    constexpr int REC = rec_bytes<FMT>();
+    constexpr int SUBN = sub_per_block<FMT>();
+    static_assert(!XF32 || FMT == 4, "the fused producer stages q4_K records");
     extern __shared__ __align__(128) uint8_t smem[];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -437,7 +546,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1) lane_kernel(const __grid_consta
     if constexpr (XF32)
         stage_f32<M, WARPS>(B, cfirst, cend, smem, warp, lane, fill);
     else
-        stage_q8<M, 8>(B, cfirst, cend, smem, fill);
+        stage_q8<FMT, M, 8>(B, cfirst, cend, smem, fill);
     __syncthreads();
 
     Cursor cc;
@@ -450,13 +559,13 @@ __global__ void __launch_bounds__(WARPS * 32, 1) lane_kernel(const __grid_consta
         const int p_now = cc.p;
         const int nb = P.nb, n = P.n, rps = P.rps;
         while (act_p < p_now) {
-            act_off += seg_bytes(M * B.p[act_p].nb);
+            act_off += seg_bytes<FMT>(M * B.p[act_p].nb);
             ++act_p;
         }
         const uint8_t* rec = smem + act_off;
         const float* dyv = reinterpret_cast<const float*>(rec + (size_t)M * nb * REC);
         const int act_stride = nb * REC;
-        const size_t sub_stride = (size_t)n * nb * 8;
+        const size_t sub_stride = (size_t)n * nb * SUBN;
         float* yv = P.y;
         int32_t* subv = P.sub;
         const int rl = rps > 0 ? lane / nb : 0;   // row mode: row slot and column of this lane
@@ -484,11 +593,15 @@ __global__ void __launch_bounds__(WARPS * 32, 1) lane_kernel(const __grid_consta
             // m <= 2: copy the block into registers and refill the slot at once,
             // so every stage of the ring is in flight while this one is decoded
             constexpr bool EARLY = !SUBDOTS && M <= 2;
-            RegBlock<BYTES / 16> rb;
+            typename std::conditional<FMT == 6, Q6Block, RegBlock<BYTES / 16>>::type rb;
             if constexpr (EARLY) {
+                if constexpr (FMT == 6) {
+                    q6_block_load(slot + lane_blk * BYTES, rb);
+                } else {
 #pragma unroll
-                for (int u = 0; u < BYTES / 16; ++u)
-                    rb.r[u] = reinterpret_cast<const uint4*>(slot + lane_blk * BYTES)[u];
+                    for (int u = 0; u < BYTES / 16; ++u)
+                        rb.r[u] = reinterpret_cast<const uint4*>(slot + lane_blk * BYTES)[u];
+                }
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // reads before the refill
                 ++consumed;
                 if (++cslot == (uint32_t)NS) {
@@ -499,11 +612,20 @@ __global__ void __launch_bounds__(WARPS * 32, 1) lane_kernel(const __grid_consta
                 if (ic.p >= 0) issue_one();
             }
             auto decode = [&](const uint8_t* act, const float* dyp, float* v, int32_t* sub) {
-                if constexpr (EARLY)
+                if constexpr (FMT == 6) {
+                    if constexpr (EARLY) {
+                        lane_block_q6<M, SUBDOTS>(rb, act, act_stride, dyp, nb, v, sub, sub_stride);
+                    } else {
+                        Q6Block qb;
+                        q6_block_load(slot + lane_blk * BYTES, qb);
+                        lane_block_q6<M, SUBDOTS>(qb, act, act_stride, dyp, nb, v, sub, sub_stride);
+                    }
+                } else if constexpr (EARLY) {
                     lane_block<FMT, M, SUBDOTS>(rb, act, act_stride, dyp, nb, v, sub, sub_stride);
-                else
+                } else {
                     lane_block<FMT, M, SUBDOTS>(SmemBlock{slot + lane_blk * BYTES}, act, act_stride, dyp, nb, v, sub,
                                                 sub_stride);
+                }
             };
             if (rps > 0) {
                 const int r0 = cc.u * rps;
@@ -513,7 +635,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1) lane_kernel(const __grid_consta
                 float v[M];
 #pragma unroll
                 for (int i = 0; i < M; ++i) v[i] = 0.0f;
-                int32_t* sub = SUBDOTS ? subv + ((size_t)(r0 + rl) * nb + col) * 8 : nullptr;
+                int32_t* sub = SUBDOTS ? subv + ((size_t)(r0 + rl) * nb + col) * SUBN : nullptr;
                 if (!SUBDOTS || valid) decode(rec + (size_t)col * REC, dyv + col, v, sub);
                 if constexpr (!SUBDOTS) {
                     if (pow2) {
@@ -551,7 +673,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1) lane_kernel(const __grid_consta
                 float v[M];
 #pragma unroll
                 for (int i = 0; i < M; ++i) v[i] = acc[i];
-                int32_t* sub = SUBDOTS ? subv + ((size_t)cc.u * nb + b) * 8 : nullptr;
+                int32_t* sub = SUBDOTS ? subv + ((size_t)cc.u * nb + b) * SUBN : nullptr;
                 if (!SUBDOTS || valid) decode(rec + (size_t)b * REC, dyv + b, v, sub);
 #pragma unroll
                 for (int i = 0; i < M; ++i) acc[i] = valid ? v[i] : acc[i];
@@ -623,6 +745,7 @@ inline void make_plan(const HostProblem* hp, int count, int warps, int pairf, Pl
 
 // Largest staged-activation region over the CTAs: every problem whose
 // weighted range meets the CTA's (the kernel stages the same set).
+template <int FMT>
 inline size_t act_need(const HostProblem* hp, int count, const Plan& pl, int m, int grid, int warps) {
     const long long G = (long long)grid * warps;
     size_t worst = 0;
@@ -632,7 +755,7 @@ inline size_t act_need(const HostProblem* hp, int count, const Plan& pl, int m, 
         const long long C1 = pl.wtotal * ((long long)c * warps + warps) / G;
         while (p + 1 < count && pl.wbegin[p + 1] <= C0) ++p;
         size_t sum = 0;
-        for (int q = p; q < count && pl.wbegin[q] < C1; ++q) sum += (size_t)seg_bytes(m * hp[q].nb);
+        for (int q = p; q < count && pl.wbegin[q] < C1; ++q) sum += (size_t)seg_bytes<FMT>(m * hp[q].nb);
         worst = std::max(worst, sum);
     }
     return align128(worst);
@@ -647,7 +770,7 @@ inline bool pick_config(const HostProblem* hp, int count, const Plan& pl, int m,
         const long long want = (pl.wtotal + o[0] - 1) / o[0];   // no CTA without a unit per warp
         if (grid > want) grid = want;
         if (grid < 1) grid = 1;
-        const size_t act = act_need(hp, count, pl, m, (int)grid, o[0]);
+        const size_t act = act_need<FMT>(hp, count, pl, m, (int)grid, o[0]);
         if (act + ring_bytes<FMT>(o[0], o[1]) <= optin) {
             *cfg = Config{o[0], o[1], (int)grid, (int)act};
             return true;
@@ -727,7 +850,7 @@ cudaError_t run_part(const HostProblem* probs, int count, int i0, int mm, bool s
         // activation row i0: q8_K blocks, or f32 values when XF32
         part[j].xq = s.xq + (size_t)i0 * s.nb * (XF32 ? QK * sizeof(float) : Q8K_BYTES);
         part[j].y = s.y ? s.y + (size_t)i0 * s.n : nullptr;
-        part[j].sub = s.sub ? s.sub + (size_t)i0 * s.n * s.nb * 8 : nullptr;
+        part[j].sub = s.sub ? s.sub + (size_t)i0 * s.n * s.nb * sub_per_block<FMT>() : nullptr;
     }
     bool fits = false;
     cudaError_t e;
