@@ -44,18 +44,21 @@ namespace q4lane {
 
 constexpr int STAGE_BLOCKS = 32;
 // Staged bytes per activation block: the 256 codes, then q4_K/q5_K the eight
-// sums of adjacent bsum pairs (272 bytes, a stride of 68 words), q6_K the
-// sixteen bsums (304 bytes, 76 words); either way eight lanes reading eight
-// different blocks at one offset hit distinct banks.
-template <int FMT> __host__ __device__ constexpr int rec_bytes() { return FMT == 6 ? 304 : 272; }
+// sums of adjacent bsum pairs (272 bytes, a stride of 68 words), q2_K, q3_K
+// and q6_K the sixteen bsums (304 bytes, 76 words); either way eight lanes
+// reading eight different blocks at one offset hit distinct banks.
+template <int FMT> __host__ __device__ constexpr int rec_bytes() { return FMT == 4 || FMT == 5 ? 272 : 304; }
 
 // Block formats of this kernel: q4_K and q5_K (q4_K plus qh[32], the fifth
 // bit of every weight, between the scale table and qs), whole 16-byte
-// multiples, so every block of a stage is 16-byte aligned; and q6_K (210
-// bytes: ql[128], qh[64], int8 scales[16], f16 d), whose blocks sit at even
-// offsets of a stage.  A q6_K stage is a 16-byte multiple and starts on a
-// 16-byte boundary when a row holds a multiple of eight blocks (8 * 210 =
-// 105 * 16), which the host requires of this path.
+// multiples, so every block of a stage is 16-byte aligned; q2_K (84 bytes:
+// scales[16], qs[64], f16 d, f16 dmin), whose blocks are 4-byte aligned in a
+// stage; q3_K (110 bytes: hmask[32], qs[64], scales[12], f16 d) and q6_K
+// (210 bytes: ql[128], qh[64], int8 scales[16], f16 d), whose blocks sit at
+// even offsets.  Their stages are 16-byte multiples starting on 16-byte
+// boundaries when a row holds a multiple of four (q2_K: 4 * 84 = 21 * 16) or
+// eight blocks (q3_K: 8 * 110 = 55 * 16; q6_K: 8 * 210 = 105 * 16), which
+// the host requires of these formats on this kernel.
 template <int FMT> struct LaneFmt;
 template <> struct LaneFmt<4> {
     static constexpr int BYTES = Q4K_BYTES;
@@ -69,8 +72,16 @@ template <> struct LaneFmt<6> {
     static constexpr int BYTES = Q6K_BYTES;
     static constexpr int QS = 0;
 };
+template <> struct LaneFmt<2> {
+    static constexpr int BYTES = Q2K_BYTES;
+    static constexpr int QS = 16;
+};
+template <> struct LaneFmt<3> {
+    static constexpr int BYTES = Q3K_BYTES;
+    static constexpr int QS = 32;
+};
 // integer sub-block dots per block in the verification export
-template <int FMT> __host__ __device__ constexpr int sub_per_block() { return FMT == 6 ? 16 : 8; }
+template <int FMT> __host__ __device__ constexpr int sub_per_block() { return FMT == 4 || FMT == 5 ? 8 : 16; }
 template <int FMT> __host__ __device__ constexpr int slot_bytes() { return STAGE_BLOCKS * LaneFmt<FMT>::BYTES; }
 
 // Bytes of one staged segment of nblk activation blocks: records, then the
@@ -202,7 +213,7 @@ __device__ __forceinline__ void act_store(uint8_t* seg, int nblk, int w, uint32_
         reinterpret_cast<float*>(seg + (size_t)nblk * REC)[blk] = __uint_as_float(v);
     } else if (wd <= 64) {
         reinterpret_cast<uint32_t*>(seg + (size_t)blk * REC)[wd - 1] = v;
-    } else if constexpr (FMT == 6) {
+    } else if constexpr (FMT != 4 && FMT != 5) {
         reinterpret_cast<uint32_t*>(seg + (size_t)blk * REC + 256)[wd - 65] = v;   // bsums 2j, 2j+1 as they are
     } else {
         const int j = wd - 65;   // bsums 2j, 2j+1
@@ -385,28 +396,43 @@ __device__ __forceinline__ void lane_block(const Blk& w, const uint8_t* act, int
     }
 }
 
-// q6_K: the block's first 208 bytes (ql[128], qh[64], scales[16]) as 52
-// four-byte words and d.  The block sits at an even offset of the stage: the
-// words are read from the 4-byte boundary at or below it and, for a block at
-// 2 mod 4, realigned by a byte permute (bytes 2, 3 of one word, 0, 1 of the
-// next); d has its own 2-byte load.  Every load stays inside the block's
-// first 212 bytes from the boundary, i.e. inside the stage slot.
-struct Q6Block {
-    uint32_t w[52];
-    uint32_t d;
-};
-__device__ __forceinline__ void q6_block_load(const uint8_t* blk, Q6Block& B) {
-    const uint32_t mis = (uint32_t)(uintptr_t)blk & 2u;
-    const uint32_t* p = reinterpret_cast<const uint32_t*>(blk - mis);
-    const uint32_t sel = mis ? 0x5432u : 0x3210u;
-    uint32_t prev = p[0];
+// q2_K, q3_K, q6_K: a block as four-byte words, read into registers.
+// q2_K (4-byte aligned): all 21 words.  q3_K and q6_K sit at even offsets
+// of the stage: their first 108 (27 words: hmask, qs, scales) and 208 bytes
+// (52 words: ql, qh, scales) are read from the 4-byte boundary at or below
+// the block and, for a block at 2 mod 4, realigned by a byte permute (bytes
+// 2, 3 of one word, 0, 1 of the next); d has its own 2-byte load.  The NW + 1
+// words read end with the block's last byte for a block at 2 mod 4, and two
+// bytes past it for a block at 0 mod 4, which is never the last of a full
+// slot (the 32nd block of 110- or 210-byte blocks sits at 2 mod 4): every
+// load stays inside the stage slot.
+template <int FMT> struct WordBlock;
+template <> struct WordBlock<2> { static constexpr int NW = 21; uint32_t w[NW]; uint32_t d; };
+template <> struct WordBlock<3> { static constexpr int NW = 27; uint32_t w[NW]; uint32_t d; };
+template <> struct WordBlock<6> { static constexpr int NW = 52; uint32_t w[NW]; uint32_t d; };
+using Q6Block = WordBlock<6>;
+
+template <int FMT>
+__device__ __forceinline__ void word_block_load(const uint8_t* blk, WordBlock<FMT>& B) {
+    constexpr int NW = WordBlock<FMT>::NW;
+    if constexpr (FMT == 2) {
+        const uint32_t* p = reinterpret_cast<const uint32_t*>(blk);
 #pragma unroll
-    for (int j = 0; j < 52; ++j) {
-        const uint32_t next = p[j + 1];
-        B.w[j] = __byte_perm(prev, next, sel);
-        prev = next;
+        for (int j = 0; j < NW; ++j) B.w[j] = p[j];
+        B.d = 0u;   // d, dmin are word 20
+    } else {
+        const uint32_t mis = (uint32_t)(uintptr_t)blk & 2u;
+        const uint32_t* p = reinterpret_cast<const uint32_t*>(blk - mis);
+        const uint32_t sel = mis ? 0x5432u : 0x3210u;
+        uint32_t prev = p[0];
+#pragma unroll
+        for (int j = 0; j < NW; ++j) {
+            const uint32_t next = p[j + 1];
+            B.w[j] = __byte_perm(prev, next, sel);
+            prev = next;
+        }
+        B.d = *reinterpret_cast<const uint16_t*>(blk + LaneFmt<FMT>::BYTES - 2);
     }
-    B.d = *reinterpret_cast<const uint16_t*>(blk + 208);
 }
 
 // One whole q6_K block against M staged activation blocks (records
@@ -468,6 +494,98 @@ __device__ __forceinline__ void lane_block_q6(const Q6Block& B, const uint8_t* a
         const float d = half_bits_to_float(B.d);
 #pragma unroll
         for (int i = 0; i < M; ++i) v[i] = __fmaf_rn(dy[i * dy_stride], __fmul_rn(d, (float)isum[i]), v[i]);
+    }
+}
+
+// One whole q2_K or q3_K block against M staged activation blocks (records
+// as for q6_K).  Weight 128h + 32j + 16p + l takes its two low bits from
+// bits 2j, 2j + 1 of qs[32h + 16p + l], so four codes of a word come from
+// one qs word by a shift and a mask; q3_K adds bit 4h + j of hmask[16p + l]
+// as the third bit (code q3 + 4 in 0..7, corrected by 4 bsum).  q2_K: isum =
+// sum of sc * dot, msum = sum of m * bsum over the sixteen groups, term
+// d (d isum - dmin msum) as for q4_K; q3_K: scale s - 32 from its six bits
+// (low four from scales[g % 8], nibble g / 8, top two from scales[8 + g %
+// 4], bits 2 (g / 4)).  The sixteen exact group dots go to the export (q2_K
+// the raw code dots, q3_K the corrected ones, as the four-lane kernel
+// writes them).
+template <int FMT, int M, bool SUBDOTS>
+__device__ __forceinline__ void lane_block_q23(const WordBlock<FMT>& B, const uint8_t* act, int act_stride,
+                                               const float* dy, int dy_stride, float* v, int32_t* sub,
+                                               size_t sub_stride) {
+    constexpr int QSW = LaneFmt<FMT>::QS / 4;   // first qs word
+    int isum[M], msum[M];
+#pragma unroll
+    for (int i = 0; i < M; ++i) isum[i] = msum[i] = 0;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            uint32_t c[8];   // codes of weights 128h + 32j + 4u .. 4u + 3
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                c[u] = (B.w[QSW + 8 * h + u] >> (2 * j)) & 0x03030303u;
+                if constexpr (FMT == 3) c[u] |= ((B.w[u] >> (4 * h + j)) & 0x01010101u) << 2;
+            }
+            const int g = 8 * h + 2 * j;   // groups g (u < 4) and g + 1
+            int s0, s1, m0 = 0, m1 = 0;
+            if constexpr (FMT == 2) {
+                const uint32_t sb = B.w[g >> 2] >> (8 * (g & 3));   // scale bytes g, g + 1
+                s0 = (int)(sb & 15u);
+                m0 = (int)((sb >> 4) & 15u);
+                s1 = (int)((sb >> 8) & 15u);
+                m1 = (int)((sb >> 12) & 15u);
+            } else {
+                auto scale = [&](int gg) {
+                    const int lb = gg & 7, hb = 8 + (gg & 3);
+                    const uint32_t low = (B.w[24 + (lb >> 2)] >> (8 * (lb & 3) + 4 * (gg >> 3))) & 15u;
+                    const uint32_t high = (B.w[24 + (hb >> 2)] >> (8 * (hb & 3) + 2 * (gg >> 2))) & 3u;
+                    return (int)(low | (high << 4)) - 32;
+                };
+                s0 = scale(g);
+                s1 = scale(g + 1);
+            }
+#pragma unroll
+            for (int i = 0; i < M; ++i) {
+                const uint8_t* a = act + (size_t)i * act_stride;
+                const int4 x0 = *reinterpret_cast<const int4*>(a + 128 * h + 32 * j);
+                const int4 x1 = *reinterpret_cast<const int4*>(a + 128 * h + 32 * j + 16);
+                const int bs = *reinterpret_cast<const int*>(a + 256 + 2 * g);   // bsums g, g + 1
+                const int b0 = (int)(int16_t)(bs & 0xFFFF), b1 = bs >> 16;
+                int d0 = dp4a_us(c[0], x0.x, 0);
+                d0 = dp4a_us(c[1], x0.y, d0);
+                d0 = dp4a_us(c[2], x0.z, d0);
+                d0 = dp4a_us(c[3], x0.w, d0);
+                int d1 = dp4a_us(c[4], x1.x, 0);
+                d1 = dp4a_us(c[5], x1.y, d1);
+                d1 = dp4a_us(c[6], x1.z, d1);
+                d1 = dp4a_us(c[7], x1.w, d1);
+                if constexpr (FMT == 3) {
+                    d0 -= 4 * b0;
+                    d1 -= 4 * b1;
+                }
+                if constexpr (SUBDOTS) {
+                    sub[i * sub_stride + g] = d0;
+                    sub[i * sub_stride + g + 1] = d1;
+                } else {
+                    isum[i] += s0 * d0 + s1 * d1;
+                    if constexpr (FMT == 2) msum[i] += m0 * b0 + m1 * b1;
+                }
+            }
+        }
+    }
+    if constexpr (!SUBDOTS) {
+        if constexpr (FMT == 2) {
+            const float d = half_bits_to_float(B.w[20]), dmin = half_bits_to_float(B.w[20] >> 16);
+#pragma unroll
+            for (int i = 0; i < M; ++i) {
+                const float tt = __fmaf_rn(d, (float)isum[i], -__fmul_rn(dmin, (float)msum[i]));
+                v[i] = __fmaf_rn(dy[i * dy_stride], tt, v[i]);
+            }
+        } else {
+            const float d = half_bits_to_float(B.d);
+#pragma unroll
+            for (int i = 0; i < M; ++i) v[i] = __fmaf_rn(dy[i * dy_stride], __fmul_rn(d, (float)isum[i]), v[i]);
+        }
     }
 }
 
@@ -593,10 +711,11 @@ __global__ void __launch_bounds__(WARPS * 32, 1) lane_kernel(const __grid_consta
             // m <= 2: copy the block into registers and refill the slot at once,
             // so every stage of the ring is in flight while this one is decoded
             constexpr bool EARLY = !SUBDOTS && M <= 2;
-            typename std::conditional<FMT == 6, Q6Block, RegBlock<BYTES / 16>>::type rb;
+            constexpr bool WORDS = FMT == 2 || FMT == 3 || FMT == 6;   // blocks read as 4-byte words
+            typename std::conditional<WORDS, WordBlock<WORDS ? FMT : 6>, RegBlock<BYTES / 16>>::type rb;
             if constexpr (EARLY) {
-                if constexpr (FMT == 6) {
-                    q6_block_load(slot + lane_blk * BYTES, rb);
+                if constexpr (WORDS) {
+                    word_block_load<FMT>(slot + lane_blk * BYTES, rb);
                 } else {
 #pragma unroll
                     for (int u = 0; u < BYTES / 16; ++u)
@@ -612,14 +731,16 @@ __global__ void __launch_bounds__(WARPS * 32, 1) lane_kernel(const __grid_consta
                 if (ic.p >= 0) issue_one();
             }
             auto decode = [&](const uint8_t* act, const float* dyp, float* v, int32_t* sub) {
-                if constexpr (FMT == 6) {
-                    if constexpr (EARLY) {
-                        lane_block_q6<M, SUBDOTS>(rb, act, act_stride, dyp, nb, v, sub, sub_stride);
-                    } else {
-                        Q6Block qb;
-                        q6_block_load(slot + lane_blk * BYTES, qb);
-                        lane_block_q6<M, SUBDOTS>(qb, act, act_stride, dyp, nb, v, sub, sub_stride);
-                    }
+                if constexpr (WORDS) {
+                    WordBlock<WORDS ? FMT : 6> wb;
+                    if constexpr (EARLY)
+                        wb = rb;
+                    else
+                        word_block_load<FMT>(slot + lane_blk * BYTES, wb);
+                    if constexpr (FMT == 6)
+                        lane_block_q6<M, SUBDOTS>(wb, act, act_stride, dyp, nb, v, sub, sub_stride);
+                    else
+                        lane_block_q23<FMT, M, SUBDOTS>(wb, act, act_stride, dyp, nb, v, sub, sub_stride);
                 } else if constexpr (EARLY) {
                     lane_block<FMT, M, SUBDOTS>(rb, act, act_stride, dyp, nb, v, sub, sub_stride);
                 } else {
@@ -881,6 +1002,37 @@ cudaError_t run_group(const HostProblem* probs, int count, int m, bool subdots, 
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
+}
+
+// q2_K, q3_K, q6_K: this kernel takes a problem whose rows hold a multiple
+// of four (q2_K) or eight blocks (so every stage copy starts and ends on a
+// 16-byte boundary), whose matrix starts on a 16-byte boundary and one of
+// whose activation rows fits beside the smallest ring; the four-lanes-per-
+// block kernel of gemv_impl.cuh takes the others.  The choice depends on
+// the problem alone (not on m or on the rest of its group), so a row's bits
+// are the same for every m and every grouping.
+template <int FMT>
+inline bool lane_eligible(const HostProblem& p) {
+    constexpr int ROWS_OF = FMT == 2 ? 4 : 8;
+    return p.nb % ROWS_OF == 0 && ((uintptr_t)p.w & 15u) == 0 &&
+           align128((size_t)seg_bytes<FMT>(p.nb)) + ring_bytes<FMT>(12, 2) <= (size_t)smem_optin_bytes();
+}
+
+template <int FMT>
+cudaError_t run_group_words(const HostProblem* p, int count, int m, bool subdots, cudaStream_t stream) {
+    if (count > GROUP_MAX) return cudaErrorInvalidValue;   // callers pass at most GROUP_MAX problems
+    HostProblem lane[GROUP_MAX], quad[GROUP_MAX];
+    int nl = 0, nq = 0;
+    for (int i = 0; i < count; ++i) {
+        if (lane_eligible<FMT>(p[i]))
+            lane[nl++] = p[i];
+        else
+            quad[nq++] = p[i];
+    }
+    cudaError_t e = cudaSuccess;
+    if (nl > 0) e = run_group<FMT, false, false>(lane, nl, m, subdots, stream);
+    if (e == cudaSuccess && nq > 0) e = plm::run_group<FMT>(quad, nq, m, subdots, stream);
+    return e;
 }
 
 }  // namespace q4lane
