@@ -50,8 +50,11 @@ def test_subdots_bit_exact(fmt, m, n, k):
 
 @pytest.mark.parametrize("fmt", ["q2K", "q3K", "q4K", "q5K", "q6K"])
 @pytest.mark.parametrize("m", [1, 2, 3, 4, 5, 6, 7, 8])
-@pytest.mark.parametrize("n,k", [(1, 256), (37, 1024), (100, 1280), (64, 3072)])
+@pytest.mark.parametrize("n,k", [(1, 256), (37, 1024), (100, 1280), (64, 3072), (37, 2048)])
 def test_gemv_matches_oracle(fmt, m, n, k):
+    # k = 2048 (8 blocks a row): q2_K, q3_K and q6_K on the one-lane-per-block
+    # kernel, 37 rows leaving a partial stage; the other k: q3_K and q6_K on
+    # the four-lanes-per-block kernel
     w = make_weights(fmt, 11, 0, n, k)
     xq = oracle.quantize_q8K(gen.normal_f32(11, 300 + m, m, k))
     y = gpu_matmul("gemv", fmt, w, xq, m, n, k)
@@ -72,11 +75,13 @@ def test_gemv_row_result_independent_of_m(fmt):
         np.testing.assert_array_equal(y1[0], y8[i])
 
 
-@pytest.mark.parametrize("fmt", ["q2K", "q3K", "q4K", "q5K", "q6K"])
-def test_gemv_adversarial_extremes(fmt):
-    # all codes at the extremes: largest integer sums the formats allow
+@pytest.mark.parametrize("fmt", ["q2K", "q3K", "q4K", "q5K", "q6K", "q6K+"])
+@pytest.mark.parametrize("k", [1024, 2048])
+def test_gemv_adversarial_extremes(fmt, k):
+    # all codes at the extremes: largest integer sums the formats allow, on
+    # both decode kernels of q3_K and q6_K (k = 2048: one lane per block)
     from tests.packers import pack_q2K, pack_q3K, pack_q4K, pack_q5K, pack_q6K
-    k, n, m = 1024, 8, 2
+    n, m = 8, 2
     if fmt == "q2K":
         blk = pack_q2K(2e-3, 2e-3, [15] * 16, [15] * 16, np.full(256, 3))
     elif fmt == "q3K":
@@ -85,8 +90,11 @@ def test_gemv_adversarial_extremes(fmt):
         blk = pack_q4K(2e-3, 2e-3, [63] * 8, [63] * 8, np.full(256, 15))
     elif fmt == "q5K":
         blk = pack_q5K(2e-3, 2e-3, [63] * 8, [63] * 8, np.full(256, 31))
+    elif fmt == "q6K":
+        blk = pack_q6K(2e-3, [-64] * 16, np.zeros(256, dtype=np.int64))   # scale -64, q6 - 32 = -32
     else:
-        blk = pack_q6K(2e-3, [-64] * 16, np.zeros(256, dtype=np.int64))
+        blk = pack_q6K(2e-3, [127] * 16, np.full(256, 63))                 # scale 127, q6 - 32 = 31
+        fmt = "q6K"
     w = np.tile(blk, n * k // 256).reshape(n, -1)
     x = np.full((m, k), -1.0, dtype=np.float32)
     x[1, ::2] = 1.0
