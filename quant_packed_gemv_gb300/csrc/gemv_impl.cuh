@@ -1,9 +1,12 @@
 // Decode GEMV for m = 1..8 activation rows over packed q6_K weights (the
-// output head) and the low rungs q2_K and q3_K (PocketLLM "What it runs": K-quant weights decoded inside the
-// kernel, never widened; the weight stream is read once for all m activation
-// rows, as the pages' 8-row activation tile does on the CPU).  q4_K and q5_K
-// take the one-lane-per-block kernel of gemv_q4K.cuh; the problem and batch
-// descriptors and the stage geometry here are shared with it.
+// output head) and the low rungs q2_K and q3_K (PocketLLM "What it runs":
+// K-quant weights decoded inside the kernel, never widened; the weight stream
+// is read once for all m activation rows, as the pages' 8-row activation tile
+// does on the CPU), for the problems the one-lane-per-block kernel of
+// gemv_q4K.cuh does not take: rows whose blocks would leave a stage copy off
+// a 16-byte boundary (q6_K, q3_K: a multiple of eight blocks; q2_K: four).
+// q4_K and q5_K always take that kernel; the host problem descriptor here is
+// shared with it.
 //
 // One launch serves a group of independent problems {w, xq, y, n, k} that
 // share m (a single GEMV is a group of one).  The weight bytes of all

@@ -1,7 +1,9 @@
-// Decode GEMV over q4_K weights, one lane per 256-weight block
-// (PocketLLM "What it runs": K-quant weights decoded inside the kernel and
-// never widened; the weight stream is read once for all m <= 8 activation
-// rows, as the pages' 8-row activation tile does on the CPU).
+// Decode GEMV, one lane per 256-weight block: q4_K and q5_K always, q2_K,
+// q3_K and q6_K when a row's blocks keep every stage copy on 16-byte
+// boundaries (lane_eligible, at the end) (PocketLLM "What it runs": K-quant
+// weights decoded inside the kernel and never widened; the weight stream is
+// read once for all m <= 8 activation rows, as the pages' 8-row activation
+// tile does on the CPU).
 //
 // Work split: the weight stream of all problems of a launch is cut into
 // row-aligned units (one stage each when a row has at most 32 blocks, else
