@@ -30,7 +30,9 @@ Reported beside it (same JSON line):
   e2e           the step through the C ABI with the activations copied in
                 from pinned host memory and the outputs copied back, the
                 copies of one step overlapping the compute of the next on a
-                second stream (and, as `serial`, without overlap).
+                second stream (and, as `serial`, without overlap; as
+                `zero_copy`, the fused launch reading x from and writing y to
+                pinned host memory itself, over the coherent CPU-GPU link).
   decode_chain_fused  the chain with one fused quantize + GEMV launch per
                 stage.
   cpu_baseline  the oracle on the host cores, on a bounded sample.
@@ -842,6 +844,17 @@ def main():
         e2e_pipelined(2)
     torch.cuda.synchronize()
     e2e_g = capture(lambda s: e2e_pipelined(K) if s == 0 else None, 1)
+    # End to end without copy calls: the fused step reads the activations from
+    # pinned host memory and writes y to pinned host memory itself (the GPU
+    # reaches host memory coherently over the CPU-GPU link); the same bytes
+    # cross the link inside the timed region
+    zc = [[(st.w[c].data_ptr() + off, st.x_host.data_ptr() + 4 * st.xoff[i], st.y_host.data_ptr() + 4 * st.yoff[i],
+            n, kk) for i, (_, _, n, kk, off) in enumerate(mats)] for c in range(2)]
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            q.plm_quantize_gemv_q4K_grouped(zc[i % 2], 1, stream=stream)
+    torch.cuda.synchronize()
+    zc_g = capture(lambda s: q.plm_quantize_gemv_q4K_grouped(zc[s % 2], 1, stream=stream), K)
     torch.cuda.synchronize()
 
     with torch.cuda.stream(stream):
@@ -860,6 +873,7 @@ def main():
         chain_ms = timed_graph(chain_g) if chain_g is not None else None
         chain_fused_ms = timed_graph(chain_fused_g) if chain_fused_g is not None else None
         e2e_pipe_ms = timed_graph(e2e_g)
+        zc_ms = timed_graph(zc_g)
         single_ms = timed(lambda s: single[s % 2].replay(), K)
         t0 = time.perf_counter()
         e2e_ms = timed(e2e_step, K)
@@ -948,6 +962,10 @@ def main():
                 "how": "per step: x copied in from pinned host memory, the fused quantize + grouped GEMV, "
                        "y copied out; copies on a second stream with two buffer sets so they overlap the "
                        "compute; the K steps captured as one CUDA graph",
+                "zero_copy": {"value": world * alg / (zc_ms / args.steps * 1e-3) / 1e9,
+                              "ms_per_step": zc_ms / args.steps,
+                              "how": "the fused step reading x from and writing y to pinned host memory "
+                                     "directly, no copy calls; same bytes per step"},
                 "serial": {"value": world * alg / (e2e_ms_step * 1e-3) / 1e9, "ms_per_step": e2e_ms_step,
                            "how": "copy in, one-step graph, copy out, on one stream, no overlap"}},
         "clocks": clocks,
