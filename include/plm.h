@@ -268,6 +268,9 @@ plm_status plm_subdots_q5K(const void* w, const void* xq, int32_t* out, int64_t 
  * q8_K round trip through memory or the second launch.
  *   x  device f32 [m][k], 16-byte aligned (else PLM_ERR_MISALIGNED);
  *   w, y as for plm_gemv_q4K.  No workspace, nothing allocated.
+ *   x and y may also be pinned host memory that the device addresses
+ *   directly (unified addressing): the kernel then reads x and writes y
+ *   across the CPU-GPU link itself, with no copy call.
  * Errors as for plm_gemv_q4K.
  */
 plm_status plm_quantize_gemv_q4K(const void* w, const float* x, float* y, int64_t m, int64_t n, int64_t k,

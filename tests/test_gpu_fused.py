@@ -106,3 +106,18 @@ def test_fused_decode_set_grouped():
     q.plm_gemv_q4K_grouped(gprobs, 1)
     for a, b in zip(yf, yg):
         np.testing.assert_array_equal(host(a), host(b))
+
+
+@pytest.mark.parametrize("m", [1, 4])
+def test_fused_reads_and_writes_pinned_host_memory(m):
+    # x and y in pinned host memory, which the GPU reaches directly: the same
+    # bits as with device buffers (the end-to-end zero-copy measurement)
+    n, k = 300, 2048
+    w = dev(gen.q4K_blocks(43, 0, n, k))
+    x_np = gen.normal_f32(43, 1, m, k)
+    x_host = torch.from_numpy(x_np).pin_memory()
+    y_host = torch.full((m, n), float("nan")).pin_memory()
+    q.plm_quantize_gemv_q4K_grouped([(w, x_host.data_ptr(), y_host.data_ptr(), n, k)], m)
+    torch.cuda.synchronize()
+    want = fused(w, torch.from_numpy(x_np).cuda(), m, n, k)
+    np.testing.assert_array_equal(y_host.numpy(), want)
