@@ -778,6 +778,7 @@ struct GemmArgs {
     unsigned* fault;
     int m, n, nb;
     int bsplit;              // blocks of K per split (blockIdx.z)
+    int ty0;                 // the launch's first weight tile (grid y counts from it)
 };
 
 template <int FMT, bool XIN>
@@ -809,7 +810,7 @@ __global__ void __launch_bounds__(GemmRoles<GemmCfg<FMT>::PWG>::threads(XIN), 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // x: activation tile, y: weight tile, so the CTAs that share a weight tile
     // run next to each other and its re-reads come from L2
-    const int r0 = blockIdx.y * GT, i0 = blockIdx.x * GT;
+    const int r0 = (blockIdx.y + A.ty0) * GT, i0 = blockIdx.x * GT;
     const int nb = A.nb;
     // this CTA's share of K: blocks [kb0, kb0 + kcount); loop indices below count from kb0
     const int kb0 = blockIdx.z * A.bsplit;
@@ -1127,7 +1128,7 @@ __global__ void __launch_bounds__(tm_threads(XIN), 1) gemm_tm_kernel(const __gri
     // this CTA's tile: weight rows from r0, activation rows from i0, K blocks [kb0, kb0 + kcount)
     // x: activation tile, y: weight tile, so the CTAs that share a weight tile
     // run next to each other and its re-reads come from L2
-    const int r0 = blockIdx.y * GT, i0 = blockIdx.x * GT;
+    const int r0 = (blockIdx.y + A.ty0) * GT, i0 = blockIdx.x * GT;
     const int nb = A.nb;
     const int kb0 = blockIdx.z * A.bsplit;
     const int kcount = min(A.bsplit, nb - kb0);
@@ -1705,6 +1706,7 @@ static cudaError_t gemm_tc(const uint8_t* w, const uint8_t* xq, float* y, long l
     A.gate = gate;
     A.xtma = xtma ? 1 : 0;
     A.csplit = 1;
+    A.ty0 = 0;
     A.fault = fault_word();
     if (!A.fault) return cudaErrorInvalidDevicePointer;
     A.m = (int)m;
@@ -1718,6 +1720,47 @@ static cudaError_t gemm_tc(const uint8_t* w, const uint8_t* xq, float* y, long l
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         return launch_kernel(kernel, grid, dim3(threads), smem, stream, map, wmap, amap, A);
+    };
+    // Many output tiles, unsplit: when the grid's last wave would hold at most
+    // half the SMs' worth of tiles, the weight-tile rows that make it up run as
+    // a second launch after the others, K split over a cluster of up to four
+    // CTAs per tile (partial tiles added through distributed shared memory), so
+    // that wave takes a fraction of a tile's time.  The split changes the f32
+    // order of those rows only; the same shape always splits the same way.
+    auto run_tail = [&](auto kernel, int threads, int smem) -> cudaError_t {
+        const long long S = num_sms(), X = grid.x, Y = grid.y, tiles = X * Y;
+        if (grid.z == 1 && tiles > S) {
+            const long long waves = tiles / S, rem = tiles - waves * S, ymain = waves * S / X;
+            if (rem > 0 && rem <= S / 2 && ymain > 0 && ymain < Y) {
+                const long long ytail = Y - ymain;
+                long long want = S / (X * ytail);
+                if (want > 4) want = 4;
+                if (want > nb / 4) want = nb / 4;
+                for (int cz = (int)want; cz >= 2; --cz) {
+                    const int bs = (nb + cz - 1) / cz;
+                    const int z = (nb + bs - 1) / bs;   // no empty split
+                    const dim3 gt(grid.x, (unsigned)ytail, (unsigned)z);
+                    if (z < 2 || max_active_clusters(kernel, gt, dim3(threads), (size_t)smem, (unsigned)z) < 1)
+                        continue;
+                    cudaError_t e = launch_kernel(kernel, dim3(grid.x, (unsigned)ymain, 1), dim3(threads), smem,
+                                                  stream, map, wmap, amap, A);
+                    if (e != cudaSuccess) return e;
+                    GemmArgs T = A;
+                    T.ty0 = (int)ymain;
+                    T.bsplit = bs;
+                    T.csplit = z;
+                    return launch_kernel_cluster(kernel, gt, dim3(threads), smem, stream, (unsigned)z, map, wmap,
+                                                 amap, T);
+                }
+            }
+        }
+        return launch_kernel(kernel, grid, dim3(threads), smem, stream, map, wmap, amap, A);
+    };
+    // the tensor-memory kernels without a workspace split: the tail above
+    auto run_tm = [&](auto kernel, int threads, int smem) -> cudaError_t {
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        return run_tail(kernel, threads, smem);
     };
     // no workspace, few output tiles (q2_K .. q5_K): split K over a cluster of up to
     // eight CTAs per tile, the partial tiles added through distributed shared memory
@@ -1736,7 +1779,7 @@ static cudaError_t gemm_tc(const uint8_t* w, const uint8_t* xq, float* y, long l
             B.csplit = z;
             return launch_kernel_cluster(kernel, g, dim3(threads), smem, stream, (unsigned)z, map, wmap, amap, B);
         }
-        return launch_kernel(kernel, grid, dim3(threads), smem, stream, map, wmap, amap, A);
+        return run_tail(kernel, threads, smem);
     };
     cudaError_t e;
     if constexpr (FMT != 6) {
@@ -1745,7 +1788,7 @@ static cudaError_t gemm_tc(const uint8_t* w, const uint8_t* xq, float* y, long l
             e = run_cluster(gemm_tm_kernel<4, true, true>, tm_threads(true), TmSmem<4, true>::ALLOC);
         } else {
             e = xin ? run_cluster(gemm_tm_kernel<FMT, true, false>, tm_threads(true), TmSmem<FMT, true>::ALLOC)
-                    : run(gemm_tm_kernel<FMT, false, false>, tm_threads(false), TmSmem<FMT, false>::ALLOC);
+                    : run_tm(gemm_tm_kernel<FMT, false, false>, tm_threads(false), TmSmem<FMT, false>::ALLOC);
         }
     } else {
         if (gate) return cudaErrorInvalidValue;

@@ -242,3 +242,33 @@ def test_gemm_split_k(fmt, m, n, k):
         outs.append(host(y))
         assert_close(outs[-1], ref, S)
     np.testing.assert_array_equal(outs[0], outs[1])
+
+
+@pytest.mark.parametrize("fmt", ["q2K", "q4K", "q6K"])
+def test_gemm_short_last_wave(fmt):
+    """More output tiles than SMs with a short last wave: 640 x 4096 gives
+    5 x 32 = 160 tiles on 152 SMs, so the last weight-tile rows run as a
+    second launch with K split over a cluster.  Every element matches the
+    oracle in both entry forms, which give the same bits, run after run."""
+    import torch
+    import quant_packed_gemv_gb300 as q
+    from tests.gpu_helpers import dev, host
+    m, n, k = 640, 4096, 2048
+    w = make_weights(fmt, 41, 0, n, k)
+    xq = oracle.quantize_q8K(gen.normal_f32(41, 3, m, k))
+    ref, S = oracle_ref(fmt, w, xq, m, n, k)
+    wd, xd = dev(w), dev(xq)
+    need = q.plm_gemm_workspace_size_split(fmt, m, n, k)
+    ws = torch.empty(max(need, 256), dtype=torch.uint8, device="cuda")
+    outs = []
+    for form in ("ws", "ws", "plain"):
+        y = torch.full((m, n), float("nan"), device="cuda")
+        if form == "ws":
+            getattr(q, "plm_gemm_%s_ws" % fmt)(wd, xd, y, m, n, k, ws, need)
+        else:
+            getattr(q, "plm_gemm_%s" % fmt)(wd, xd, y, m, n, k)
+        outs.append(host(y))
+        assert_close(outs[-1], ref, S)
+    np.testing.assert_array_equal(outs[0], outs[1])
+    np.testing.assert_array_equal(outs[0], outs[2])
+    assert q.plm_device_fault() == 0
