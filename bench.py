@@ -578,8 +578,9 @@ def gemm_roofline(configs, peaks, peak_src):
     """Roofline of the dominant prefill kernel: the q4_K tensor-core GEMM on
     the Qwen3-8B gate/up shape 12288 x 4096 at m = 2048 in its workspace
     form, from the sweep's CUDA-event time per call (the call is the
-    activation pre-pass, about 2 %, plus the GEMM kernel, so the kernel's own
-    rate is slightly higher)."""
+    activation pre-pass, about 2 %, then the GEMM kernel as its main grid and
+    the short last wave's launch, so the kernel's own rate is slightly
+    higher); traffic and tensor-pipe activity per call from the ncu record."""
     row = next((r for r in configs.get("sweep_qwen3_8b", [])
                 if r["fmt"] == "q4K" and r["n"] == 12288 and r["k"] == 4096 and r["m"] == 2048
                 and r["entry"] == "plm_gemm_q4K_ws"), None)
