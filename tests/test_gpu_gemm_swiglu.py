@@ -53,8 +53,10 @@ def single(w, xq, m, n, k):
 
 
 @pytest.mark.parametrize("m,n,k", [(512, 256, 1024), (300, 200, 2048), (9, 128, 256), (4, 100, 512),
-                                   (1000, 256, 2048), (130, 1024, 3072)])
+                                   (1000, 256, 2048), (130, 1024, 3072), (640, 4096, 2048)])
 def test_gemm_swiglu(m, n, k):
+    # (640, 4096, 2048): 160 output tiles on 152 SMs, the last weight-tile rows
+    # as a second launch with K split over clusters
     wg_np = gen.q4K_blocks(70, n, n, k)
     wu_np = gen.q4K_blocks(71, n, n, k)
     x_np = scaled_x(wg_np, 70 + m, m, k)
