@@ -768,7 +768,7 @@ __device__ __forceinline__ void q6K_row_stage(const Q6KRow& R, int c, uint8_t* t
 // The GEMM kernel
 // ---------------------------------------------------------------------------
 struct GemmArgs {
-    const uint8_t* w;        // q4_K, q5_K or q6_K [n][nb]
+    const uint8_t* w;        // q2_K .. q6_K blocks [n][nb]
     const uint8_t* xq;       // q8_K [m][nb]
     float* y;                // [m][n]
     float* part;             // split K: partial sums [gridDim.z][m][n] (null: write y)
@@ -1686,7 +1686,7 @@ static cudaError_t gemm_tc(const uint8_t* w, const uint8_t* xq, float* y, long l
                 return cudaErrorInvalidValue;
         }
     }
-    // q2_K .. q5_K: the raw weight blocks (rows of nb * WROW bytes; a box is
+    // the tensor-memory kernels (q2_K .. q6_K): the raw weight blocks (rows of nb * WROW bytes; a box is
     // one block's 16-byte-aligned window, WPITCH bytes, of 128 rows; rows past
     // n and bytes past a row's end read as zeros)
     if constexpr (GemmCfg<FMT>::BSLOTS > 0) {
@@ -1762,8 +1762,9 @@ static cudaError_t gemm_tc(const uint8_t* w, const uint8_t* xq, float* y, long l
         if (e != cudaSuccess) return e;
         return run_tail(kernel, threads, smem);
     };
-    // no workspace, few output tiles (q2_K .. q5_K): split K over a cluster of up to
-    // eight CTAs per tile, the partial tiles added through distributed shared memory
+    // the tensor-memory kernels without a workspace: few output tiles, split K over a
+    // cluster of up to eight CTAs per tile (partial tiles added through distributed
+    // shared memory); many tiles, the short last wave as above
     auto run_cluster = [&](auto kernel, int threads, int smem) -> cudaError_t {
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
