@@ -1043,11 +1043,18 @@ __global__ void __launch_bounds__(GemmRoles<GemmCfg<FMT>::PWG>::threads(XIN), 1)
 // tiles (TMA) and the per-block min operands, half the traffic of an A tile
 // in shared memory.  Tensor memory (512 columns): D1 (isum) double-buffered
 // at columns 0 and 128, D2 (msum) single-buffered at 256, the A ring at
-// 384 + 32 s.  The epilogue takes D2 of a block first and releases it before
-// D1, so the next block's min MMA (its last) rarely waits.  Roles: warps 0-7
-// producers (two warpgroups, stages 2h, 2h + 1 of every block), warps 8-15
-// epilogue (warp e: TMEM lanes 32 (e % 4) .., activation columns 64 (e / 4)
-// .. + 63), warp 16 issues the MMAs.  No register hand-over: 17 warps at 96.
+// 384 + 32 s.  The epilogue drains D1 and D2 of a block together and then
+// releases both.  Roles: warps 0-7 producers (two warpgroups, stages 2h,
+// 2h + 1 of every block), warps 8-15 epilogue (warp e: TMEM lanes 32 (e % 4)
+// .., activation columns 64 (e / 4) .. + 63), warp 16 issues the MMAs.  No
+// register hand-over: 17 warps at 96.
+// The MMA thread waits as seldom as it can: an mbarrier wait takes a few
+// hundred cycles even when the phase is complete, and the tensor pipe's
+// instruction queue is short, so each wait leaves the pipe idle for a while.
+// Each producer warpgroup publishes its two stages (and their activation
+// tiles) on one barrier; the second warpgroup's barrier also covers the min
+// operands, written and fenced before it.  Four waits a block: D1's slot, the
+// two halves, D2.  The weight blocks come through a four-slot TMA ring.
 // XIN (no workspace): warps 17-19 widen the activation codes from xq into
 // the B tiles and write the side data into the block slots (xin_issue,
 // xin_convert, xin_side_store) in place of the TMA; 20 warps keep five per
@@ -1057,6 +1064,9 @@ constexpr int TM_EPI_WARP0 = 8, TM_MMA_WARP = 16, TM_NSTAGE = 4;
 constexpr int TM_NCV = 3;   // converter warps (XIN)
 constexpr int tm_threads(bool xin) { return (TM_MMA_WARP + 1 + (xin ? TM_NCV : 0)) * 32; }
 constexpr uint32_t TM_D1 = 0, TM_D2 = 256, TM_A = 384;
+// slots of the ring of weight blocks: block b + slots is requested once block b
+// is decoded (the form with the widening converters has room for two)
+__host__ __device__ constexpr int tm_bslots(bool xin) { return xin ? 2 : 4; }
 
 template <int FMT, bool XIN>
 struct TmSmem {
@@ -1067,9 +1077,9 @@ struct TmSmem {
     static constexpr int BTX = WT + GT * AUXB;
     static constexpr int BSLOT = (BTX + 1023) & ~1023;
     static constexpr int BRING = (SCL + 2 * 3 * GT * 4 + 1023) & ~1023;
-    static constexpr int XST = BRING + 2 * BSLOT;                             // XIN: 2 staging buffers
+    static constexpr int XST = BRING + tm_bslots(XIN) * BSLOT;                // XIN: 2 staging buffers
     static constexpr int BAR = XST + (XIN ? 2 * XSTAGE_BYTES : 0);
-    static constexpr int NBAR = 2 * TM_NSTAGE + 8 + 4 + 1 + (XIN ? 4 : 0);
+    static constexpr int NBAR = 2 * TM_NSTAGE + 8 + 2 * tm_bslots(XIN) + 1 + (XIN ? 4 : 0);
     static constexpr int TMEMP = BAR + NBAR * 8;
     static constexpr int BYTES = TMEMP + 16;
     static constexpr int ALLOC = BYTES + 1024;
@@ -1106,19 +1116,20 @@ __global__ void __launch_bounds__(tm_threads(XIN), 1) gemm_tm_kernel(const __gri
                                                                 const __grid_constant__ CUtensorMap amap,
                                                                 const GemmArgs A) {
     using L = TmSmem<FMT, XIN>;
-    constexpr int NSTAGE = TM_NSTAGE;
+    constexpr int NSTAGE = TM_NSTAGE, NBS = tm_bslots(XIN);
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BAR);
-    uint64_t* full = bars;                  // [4]: 4 producer-warp arrivals + the B tile (TMA bytes, or XIN: converter warps)
+    uint64_t* full = bars;                  // [0], [2]: stages 0-1 / 2-3: 4 producer-warp arrivals + the two B tiles
+                                            // (TMA bytes, or XIN: converter warps); [1], [3] unused
     uint64_t* empty = bars + NSTAGE;        // [4]: MMA commit (frees the TMEM A stage and the B tile)
     uint64_t* minfull = bars + 2 * NSTAGE;  // [2]: 8 producer-warp arrivals (min operands, scales)
     uint64_t* minempty = minfull + 2;       // [2]: MMA commit
     uint64_t* tfull = minfull + 4;          // [2]: MMA commit
     uint64_t* tempty = minfull + 6;         // [2]: 8 epilogue-warp arrivals
-    uint64_t* bfull = minfull + 8;          // [2]: TMA bytes of a weight block and its side data (XIN: + converter warps)
-    uint64_t* bempty = bfull + 2;           // [2]: 8 producer-warp arrivals
-    uint64_t* d2free = bempty + 2;          // [1]: 8 epilogue-warp arrivals once D2 is read
+    uint64_t* bfull = minfull + 8;          // [NBS]: TMA bytes of a weight block and its side data (XIN: + converter warps)
+    uint64_t* bempty = bfull + NBS;         // [NBS]: 8 producer-warp arrivals
+    uint64_t* d2free = bempty + NBS;        // [1]: 8 epilogue-warp arrivals once D2 is read
     uint64_t* xfull = d2free + 1;           // XIN [2]: bulk-copy bytes of a staged block of codes
     uint64_t* xempty = xfull + 2;           // XIN [2]: converter-warp arrivals once it is widened
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::TMEMP);
@@ -1135,7 +1146,7 @@ __global__ void __launch_bounds__(tm_threads(XIN), 1) gemm_tm_kernel(const __gri
 
     if (tid == 0) {
         for (int s = 0; s < NSTAGE; ++s) {
-            mbar_init(&full[s], 4 + (XIN ? TM_NCV : 0));
+            mbar_init(&full[s], 4 + (XIN ? 2 * TM_NCV : 0));
             mbar_init(&empty[s], 1);
         }
         for (int j = 0; j < 2; ++j) {
@@ -1143,8 +1154,10 @@ __global__ void __launch_bounds__(tm_threads(XIN), 1) gemm_tm_kernel(const __gri
             mbar_init(&minempty[j], 1);
             mbar_init(&tfull[j], 1);
             mbar_init(&tempty[j], 8);
-            mbar_init(&bfull[j], 1 + (XIN ? TM_NCV : 0));
-            mbar_init(&bempty[j], 8);
+        }
+        for (int s = 0; s < NBS; ++s) {
+            mbar_init(&bfull[s], 1 + (XIN ? TM_NCV : 0));
+            mbar_init(&bempty[s], 8);
         }
         mbar_init(d2free, 8);
         if constexpr (XIN) {
@@ -1178,16 +1191,16 @@ __global__ void __launch_bounds__(tm_threads(XIN), 1) gemm_tm_kernel(const __gri
         constexpr int WROW = GemmCfg<FMT>::WROW, WPITCH = GemmCfg<FMT>::WPITCH;
         Row R;
         int nissued = 0;
-        auto issue_block = [&](int bb) {   // thread 0: block bb of the tile into slot bb % 2
+        auto issue_block = [&](int bb) {   // thread 0: block bb of the tile into slot bb % NBS
             ++nissued;
-            const int s = bb & 1;
+            const int s = bb % NBS;
             uint8_t* dst = sm + L::BRING + s * L::BSLOT;
             mbar_arrive_expect_tx(&bfull[s], (uint32_t)(XIN ? L::WT : L::BTX));
             tma_load_2d(dst, &wmap, ((kb0 + bb) * WROW) & ~15, r0, &bfull[s]);   // the block's 16-byte window
             if constexpr (!XIN) tma_load_2d(dst + L::WT, &amap, (kb0 + bb) * AUXB, i0, &bfull[s]);
         };
         if (tid == 0)
-            for (int bb = 0; bb < 2 && bb < kcount; ++bb) issue_block(bb);
+            for (int bb = 0; bb < NBS && bb < kcount; ++bb) issue_block(bb);
         int gb = 0;   // block of the tile: slots and phases
         {
             for (int b = 0; b < kcount && ok; ++b, ++gb) {
@@ -1195,8 +1208,8 @@ __global__ void __launch_bounds__(tm_threads(XIN), 1) gemm_tm_kernel(const __gri
                 uint32_t bsw[8];
                 float dx;
                 {
-                    const int s = gb & 1;
-                    if (!mbar_wait(&bfull[s], (uint32_t)(gb >> 1) & 1u)) { ok = false; break; }
+                    const int s = gb % NBS;
+                    if (!mbar_wait(&bfull[s], (uint32_t)(gb / NBS) & 1u)) { ok = false; break; }
                     const uint8_t* slot = sm + L::BRING + s * L::BSLOT;
                     if constexpr (FMT == Q6TM) {
                         q6_half_load(R, slot + t * WPITCH, ((kb0 + b) * WROW) & 15, half);
@@ -1248,9 +1261,9 @@ __global__ void __launch_bounds__(tm_threads(XIN), 1) gemm_tm_kernel(const __gri
                         if (!mbar_wait(&empty[c], (uint32_t)(gb - 1) & 1u)) return false;
                         tc_fence_after();
                     }
-                    if (!XIN && t == 0) {
-                        mbar_expect_tx(&full[c], TILE_BYTES);
-                        tma_load_2d(sm + L::RING + c * TILE_BYTES, &xmap, (kb0 + b) * QK + c * KS, i0, &full[c]);
+                    if (!XIN && t == 0) {   // the half's barrier counts both of its stages' tiles
+                        mbar_expect_tx(&full[c & 2], TILE_BYTES);
+                        tma_load_2d(sm + L::RING + c * TILE_BYTES, &xmap, (kb0 + b) * QK + c * KS, i0, &full[c & 2]);
                     }
                     if constexpr (FMT == Q6TM) {
                         // two operands (16 hi (q - 32) at columns 256 .., lo (q - 32) at 384 ..), 16 columns at a time
@@ -1282,18 +1295,17 @@ __global__ void __launch_bounds__(tm_threads(XIN), 1) gemm_tm_kernel(const __gri
                 if (lane == 0) {
                     mbar_arrive(&minfull[j]);
                     mbar_arrive(&full[2 * half]);
-                    mbar_arrive(&full[2 * half + 1]);
                 }
                 // refill this block's weight slot once every producer warp has read it
-                if (tid == 0 && b + 2 < kcount) {
-                    if (!mbar_wait(&bempty[gb & 1], (uint32_t)(gb >> 1) & 1u)) { ok = false; break; }
-                    issue_block(b + 2);
+                if (tid == 0 && b + NBS < kcount) {
+                    if (!mbar_wait(&bempty[gb % NBS], (uint32_t)(gb / NBS) & 1u)) { ok = false; break; }
+                    issue_block(b + NBS);
                 }
             }
         }
         // after a wait ran out: let this CTA's weight copies still in flight land before it exits
         if (!ok && tid == 0)
-            for (int bb = gb; bb < nissued; ++bb) (void)mbar_wait(&bfull[bb & 1], (uint32_t)(bb >> 1) & 1u);
+            for (int bb = gb; bb < nissued; ++bb) (void)mbar_wait(&bfull[bb % NBS], (uint32_t)(bb / NBS) & 1u);
     } else if (warp == TM_MMA_WARP) {
         // ------------------------------------------------------- MMA issuer
         if (lane == 0) {
@@ -1305,8 +1317,11 @@ __global__ void __launch_bounds__(tm_threads(XIN), 1) gemm_tm_kernel(const __gri
                     if (gb >= 2 && !mbar_wait(&tempty[j], ((gb >> 1) - 1) & 1)) { ok = false; break; }
                     tc_fence_after();
                     for (int c = 0; c < 4 && ok; ++c) {
-                        if (!mbar_wait(&full[c], (uint32_t)gb & 1u)) { ok = false; break; }
-                        tc_fence_after();
+                        // one wait per producer half: its two stages are published together
+                        if ((c & 1) == 0) {
+                            if (!mbar_wait(&full[c], (uint32_t)gb & 1u)) { ok = false; break; }
+                            tc_fence_after();
+                        }
                         const uint64_t db = umma_desc_sw128(smem_u32(sm + L::RING + c * TILE_BYTES));
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk) {  // K = 16 per MMA: 8 TMEM columns, +2 descriptor units
@@ -1320,7 +1335,8 @@ __global__ void __launch_bounds__(tm_threads(XIN), 1) gemm_tm_kernel(const __gri
                         mma_commit(&empty[c]);
                     }
                     if (!ok) break;
-                    if (!mbar_wait(&minfull[j], (gb >> 1) & 1)) { ok = false; break; }
+                    // the min operands were written (and fenced) before the second half's
+                    // stages were published, so the wait on full[2] covers them
                     if constexpr (FMT != Q6TM) {   // q6_K: no min term
                         if (gb >= 1 && !mbar_wait(d2free, (uint32_t)(gb - 1) & 1u)) { ok = false; break; }
                         tc_fence_after();
@@ -1336,6 +1352,7 @@ __global__ void __launch_bounds__(tm_threads(XIN), 1) gemm_tm_kernel(const __gri
     } else if (warp > TM_MMA_WARP) {
         // ------------------------------------------------------- activation converters (XIN)
         if constexpr (XIN) {
+            static_assert(NBS == 2, "the converters index the weight-block ring in pairs");
             constexpr int NT = TM_NCV * 32;
             const int u = tid - (TM_MMA_WARP + 1) * 32, cw = u >> 5;
             uint8_t* xst = sm + L::XST;
@@ -1367,7 +1384,7 @@ __global__ void __launch_bounds__(tm_threads(XIN), 1) gemm_tm_kernel(const __gri
                     [&](int c) {
                         fence_async_smem();   // generic writes before the tensor core reads them
                         __syncwarp();
-                        if (lane == 0) mbar_arrive(&full[c]);
+                        if (lane == 0) mbar_arrive(&full[c & 2]);
                     });
                 if (!ok) break;
                 // the staging buffer's reads before its refill
