@@ -1054,7 +1054,9 @@ __global__ void __launch_bounds__(GemmRoles<GemmCfg<FMT>::PWG>::threads(XIN), 1)
 // Each producer warpgroup publishes its two stages (and their activation
 // tiles) on one barrier; the second warpgroup's barrier also covers the min
 // operands, written and fenced before it.  Four waits a block: D1's slot, the
-// two halves, D2.  The weight blocks come through a four-slot TMA ring.
+// two halves, D2.  (XIN keeps a barrier per stage: its converters finish the
+// B tiles one stage at a time.)  The weight blocks come through a four-slot
+// TMA ring.
 // XIN (no workspace): warps 17-19 widen the activation codes from xq into
 // the B tiles and write the side data into the block slots (xin_issue,
 // xin_convert, xin_side_store) in place of the TMA; 20 warps keep five per
@@ -1120,8 +1122,11 @@ __global__ void __launch_bounds__(tm_threads(XIN), 1) gemm_tm_kernel(const __gri
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BAR);
-    uint64_t* full = bars;                  // [0], [2]: stages 0-1 / 2-3: 4 producer-warp arrivals + the two B tiles
-                                            // (TMA bytes, or XIN: converter warps); [1], [3] unused
+    // full[c]: stage c's A rows (4 producer-warp arrivals) and B tile (TMA bytes; XIN: converter warps).
+    // Without XIN the two stages of a producer half share one barrier, full[c & 2] (the half publishes
+    // them together); with XIN the converters finish the B tiles one stage at a time, so each has its own.
+    constexpr bool MERGE = !XIN;
+    uint64_t* full = bars;                  // [4]
     uint64_t* empty = bars + NSTAGE;        // [4]: MMA commit (frees the TMEM A stage and the B tile)
     uint64_t* minfull = bars + 2 * NSTAGE;  // [2]: 8 producer-warp arrivals (min operands, scales)
     uint64_t* minempty = minfull + 2;       // [2]: MMA commit
@@ -1146,7 +1151,7 @@ __global__ void __launch_bounds__(tm_threads(XIN), 1) gemm_tm_kernel(const __gri
 
     if (tid == 0) {
         for (int s = 0; s < NSTAGE; ++s) {
-            mbar_init(&full[s], 4 + (XIN ? 2 * TM_NCV : 0));
+            mbar_init(&full[s], 4 + (XIN ? TM_NCV : 0));
             mbar_init(&empty[s], 1);
         }
         for (int j = 0; j < 2; ++j) {
@@ -1295,6 +1300,7 @@ __global__ void __launch_bounds__(tm_threads(XIN), 1) gemm_tm_kernel(const __gri
                 if (lane == 0) {
                     mbar_arrive(&minfull[j]);
                     mbar_arrive(&full[2 * half]);
+                    if constexpr (!MERGE) mbar_arrive(&full[2 * half + 1]);
                 }
                 // refill this block's weight slot once every producer warp has read it
                 if (tid == 0 && b + NBS < kcount) {
@@ -1317,8 +1323,8 @@ __global__ void __launch_bounds__(tm_threads(XIN), 1) gemm_tm_kernel(const __gri
                     if (gb >= 2 && !mbar_wait(&tempty[j], ((gb >> 1) - 1) & 1)) { ok = false; break; }
                     tc_fence_after();
                     for (int c = 0; c < 4 && ok; ++c) {
-                        // one wait per producer half: its two stages are published together
-                        if ((c & 1) == 0) {
+                        // without XIN, one wait per producer half: its two stages are published together
+                        if (!MERGE || (c & 1) == 0) {
                             if (!mbar_wait(&full[c], (uint32_t)gb & 1u)) { ok = false; break; }
                             tc_fence_after();
                         }
@@ -1336,7 +1342,7 @@ __global__ void __launch_bounds__(tm_threads(XIN), 1) gemm_tm_kernel(const __gri
                     }
                     if (!ok) break;
                     // the min operands were written (and fenced) before the second half's
-                    // stages were published, so the wait on full[2] covers them
+                    // stages were published, so the wait on full[2] (or full[3]) covers them
                     if constexpr (FMT != Q6TM) {   // q6_K: no min term
                         if (gb >= 1 && !mbar_wait(d2free, (uint32_t)(gb - 1) & 1u)) { ok = false; break; }
                         tc_fence_after();
@@ -1384,7 +1390,7 @@ __global__ void __launch_bounds__(tm_threads(XIN), 1) gemm_tm_kernel(const __gri
                     [&](int c) {
                         fence_async_smem();   // generic writes before the tensor core reads them
                         __syncwarp();
-                        if (lane == 0) mbar_arrive(&full[c & 2]);
+                        if (lane == 0) mbar_arrive(&full[c]);
                     });
                 if (!ok) break;
                 // the staging buffer's reads before its refill
