@@ -306,6 +306,12 @@ __device__ __forceinline__ int dp2a_hi_su(int a, uint32_t b, int c) {
     asm("dp2a.hi.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
     return d;
 }
+// signed 16-bit halves of a times signed bytes 0, 1 of b
+__device__ __forceinline__ int dp2a_lo_ss(int a, uint32_t b, int c) {
+    int d;
+    asm("dp2a.lo.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
 
 // One whole q4_K block against M staged activation blocks (same column,
 // records act_stride bytes apart, scales dy_stride floats apart).  Adds the
@@ -501,92 +507,184 @@ __device__ __forceinline__ void lane_block_q6(const Q6Block& B, const uint8_t* a
 
 // One whole q2_K or q3_K block against M staged activation blocks (records
 // as for q6_K).  Weight 128h + 32j + 16p + l takes its two low bits from
-// bits 2j, 2j + 1 of qs[32h + 16p + l], so four codes of a word come from
-// one qs word by a shift and a mask; q3_K adds bit 4h + j of hmask[16p + l]
-// as the third bit (code q3 + 4 in 0..7, corrected by 4 bsum).  q2_K: isum =
-// sum of sc * dot, msum = sum of m * bsum over the sixteen groups, term
-// d (d isum - dmin msum) as for q4_K; q3_K: scale s - 32 from its six bits
-// (low four from scales[g % 8], nibble g / 8, top two from scales[8 + g %
-// 4], bits 2 (g / 4)).  The sixteen exact group dots go to the export (q2_K
+// bits 2j, 2j + 1 of qs[32h + 16p + l]; q3_K adds bit 4h + j of
+// hmask[16p + l] as the third bit (code q3 + 4 in 0..7, corrected by
+// 4 bsum).  q2_K: isum = sum of sc * dot, msum = sum of m * bsum over the
+// sixteen groups, term d (d isum - dmin msum) as for q4_K; q3_K: scale
+// s - 32 from its six bits (low four from scales[g % 8], nibble g / 8, top
+// two from scales[8 + g % 4], bits 2 (g / 4)), isum = sum of s * dot -
+// 4 sum of s * bsum.  The sixteen exact group dots go to the export (q2_K
 // the raw code dots, q3_K the corrected ones, as the four-lane kernel
 // writes them).
+//
+// Without the export (every m of q2_K, m <= 3 of q3_K: above, the form's
+// extra registers spill) the codes stay where they sit in the qs word: plane j
+// is masked, not shifted, so each byte holds 4^e times its code (e = j; for
+// q3_K e = min(j, 2), since the third bit must fit in the byte), and the dot
+// comes out 4^e times too large.  The group pair's sum s0 dot0 + s1 dot1 is
+// then multiplied by 4^(3 - e) instead, every plane ends up 64 times too
+// large, and the sum is divided by 64 once per block (exactly: it is a
+// multiple of 64).  The min term (q2_K) and the 4 bsum correction (q3_K) are
+// one two-way dot of the pair's bsums with its two mins or scales.
 template <int FMT, int M, bool SUBDOTS>
 __device__ __forceinline__ void lane_block_q23(const WordBlock<FMT>& B, const uint8_t* act, int act_stride,
                                                const float* dy, int dy_stride, float* v, int32_t* sub,
                                                size_t sub_stride) {
-    constexpr int QSW = LaneFmt<FMT>::QS / 4;   // first qs word
-    int isum[M], msum[M];
+    // the in-place form for every m of q2_K and for m <= 3 of q3_K (above, its extra
+    // registers spill); the export and the other q3_K cases take the codes shifted down
+    constexpr bool INPLACE = !SUBDOTS && (FMT == 2 || M <= 3);
+    if constexpr (!INPLACE) {
+        constexpr int QSW = LaneFmt<FMT>::QS / 4;   // first qs word
+        int isum[M], msum[M];
 #pragma unroll
-    for (int i = 0; i < M; ++i) isum[i] = msum[i] = 0;
+        for (int i = 0; i < M; ++i) isum[i] = msum[i] = 0;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
+        for (int h = 0; h < 2; ++h) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            uint32_t c[8];   // codes of weights 128h + 32j + 4u .. 4u + 3
+            for (int j = 0; j < 4; ++j) {
+                uint32_t c[8];   // codes of weights 128h + 32j + 4u .. 4u + 3
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                c[u] = (B.w[QSW + 8 * h + u] >> (2 * j)) & 0x03030303u;
-                if constexpr (FMT == 3) c[u] |= ((B.w[u] >> (4 * h + j)) & 0x01010101u) << 2;
-            }
-            const int g = 8 * h + 2 * j;   // groups g (u < 4) and g + 1
-            int s0, s1, m0 = 0, m1 = 0;
-            if constexpr (FMT == 2) {
-                const uint32_t sb = B.w[g >> 2] >> (8 * (g & 3));   // scale bytes g, g + 1
-                s0 = (int)(sb & 15u);
-                m0 = (int)((sb >> 4) & 15u);
-                s1 = (int)((sb >> 8) & 15u);
-                m1 = (int)((sb >> 12) & 15u);
-            } else {
-                auto scale = [&](int gg) {
-                    const int lb = gg & 7, hb = 8 + (gg & 3);
-                    const uint32_t low = (B.w[24 + (lb >> 2)] >> (8 * (lb & 3) + 4 * (gg >> 3))) & 15u;
-                    const uint32_t high = (B.w[24 + (hb >> 2)] >> (8 * (hb & 3) + 2 * (gg >> 2))) & 3u;
-                    return (int)(low | (high << 4)) - 32;
-                };
-                s0 = scale(g);
-                s1 = scale(g + 1);
-            }
-#pragma unroll
-            for (int i = 0; i < M; ++i) {
-                const uint8_t* a = act + (size_t)i * act_stride;
-                const int4 x0 = *reinterpret_cast<const int4*>(a + 128 * h + 32 * j);
-                const int4 x1 = *reinterpret_cast<const int4*>(a + 128 * h + 32 * j + 16);
-                const int bs = *reinterpret_cast<const int*>(a + 256 + 2 * g);   // bsums g, g + 1
-                const int b0 = (int)(int16_t)(bs & 0xFFFF), b1 = bs >> 16;
-                int d0 = dp4a_us(c[0], x0.x, 0);
-                d0 = dp4a_us(c[1], x0.y, d0);
-                d0 = dp4a_us(c[2], x0.z, d0);
-                d0 = dp4a_us(c[3], x0.w, d0);
-                int d1 = dp4a_us(c[4], x1.x, 0);
-                d1 = dp4a_us(c[5], x1.y, d1);
-                d1 = dp4a_us(c[6], x1.z, d1);
-                d1 = dp4a_us(c[7], x1.w, d1);
-                if constexpr (FMT == 3) {
-                    d0 -= 4 * b0;
-                    d1 -= 4 * b1;
+                for (int u = 0; u < 8; ++u) {
+                    c[u] = (B.w[QSW + 8 * h + u] >> (2 * j)) & 0x03030303u;
+                    if constexpr (FMT == 3) c[u] |= ((B.w[u] >> (4 * h + j)) & 0x01010101u) << 2;
                 }
-                if constexpr (SUBDOTS) {
-                    sub[i * sub_stride + g] = d0;
-                    sub[i * sub_stride + g + 1] = d1;
+                const int g = 8 * h + 2 * j;   // groups g (u < 4) and g + 1
+                int s0, s1, m0 = 0, m1 = 0;
+                if constexpr (FMT == 2) {
+                    const uint32_t sb = B.w[g >> 2] >> (8 * (g & 3));   // scale bytes g, g + 1
+                    s0 = (int)(sb & 15u);
+                    m0 = (int)((sb >> 4) & 15u);
+                    s1 = (int)((sb >> 8) & 15u);
+                    m1 = (int)((sb >> 12) & 15u);
                 } else {
-                    isum[i] += s0 * d0 + s1 * d1;
-                    if constexpr (FMT == 2) msum[i] += m0 * b0 + m1 * b1;
+                    auto scale = [&](int gg) {
+                        const int lb = gg & 7, hb = 8 + (gg & 3);
+                        const uint32_t low = (B.w[24 + (lb >> 2)] >> (8 * (lb & 3) + 4 * (gg >> 3))) & 15u;
+                        const uint32_t high = (B.w[24 + (hb >> 2)] >> (8 * (hb & 3) + 2 * (gg >> 2))) & 3u;
+                        return (int)(low | (high << 4)) - 32;
+                    };
+                    s0 = scale(g);
+                    s1 = scale(g + 1);
+                }
+#pragma unroll
+                for (int i = 0; i < M; ++i) {
+                    const uint8_t* a = act + (size_t)i * act_stride;
+                    const int4 x0 = *reinterpret_cast<const int4*>(a + 128 * h + 32 * j);
+                    const int4 x1 = *reinterpret_cast<const int4*>(a + 128 * h + 32 * j + 16);
+                    const int bs = *reinterpret_cast<const int*>(a + 256 + 2 * g);   // bsums g, g + 1
+                    const int b0 = (int)(int16_t)(bs & 0xFFFF), b1 = bs >> 16;
+                    int d0 = dp4a_us(c[0], x0.x, 0);
+                    d0 = dp4a_us(c[1], x0.y, d0);
+                    d0 = dp4a_us(c[2], x0.z, d0);
+                    d0 = dp4a_us(c[3], x0.w, d0);
+                    int d1 = dp4a_us(c[4], x1.x, 0);
+                    d1 = dp4a_us(c[5], x1.y, d1);
+                    d1 = dp4a_us(c[6], x1.z, d1);
+                    d1 = dp4a_us(c[7], x1.w, d1);
+                    if constexpr (FMT == 3) {
+                        d0 -= 4 * b0;
+                        d1 -= 4 * b1;
+                    }
+                    if constexpr (SUBDOTS) {
+                        sub[i * sub_stride + g] = d0;
+                        sub[i * sub_stride + g + 1] = d1;
+                    } else {
+                        isum[i] += s0 * d0 + s1 * d1;
+                        if constexpr (FMT == 2) msum[i] += m0 * b0 + m1 * b1;
+                    }
                 }
             }
         }
-    }
-    if constexpr (!SUBDOTS) {
+        if constexpr (!SUBDOTS) {
+            if constexpr (FMT == 2) {
+                const float d = half_bits_to_float(B.w[20]), dmin = half_bits_to_float(B.w[20] >> 16);
+#pragma unroll
+                for (int i = 0; i < M; ++i) {
+                    const float tt = __fmaf_rn(d, (float)isum[i], -__fmul_rn(dmin, (float)msum[i]));
+                    v[i] = __fmaf_rn(dy[i * dy_stride], tt, v[i]);
+                }
+            } else {
+                const float d = half_bits_to_float(B.d);
+#pragma unroll
+                for (int i = 0; i < M; ++i) v[i] = __fmaf_rn(dy[i * dy_stride], __fmul_rn(d, (float)isum[i]), v[i]);
+            }
+        }
+    } else {
+        constexpr int QSW = LaneFmt<FMT>::QS / 4;   // first qs word
+        auto scale3 = [&](int gg) {   // q3_K: the signed 6-bit scale of group gg
+            const int lb = gg & 7, hb = 8 + (gg & 3);
+            const uint32_t low = (B.w[24 + (lb >> 2)] >> (8 * (lb & 3) + 4 * (gg >> 3))) & 15u;
+            const uint32_t high = (B.w[24 + (hb >> 2)] >> (8 * (hb & 3) + 2 * (gg >> 2))) & 3u;
+            return (int)(low | (high << 4)) - 32;
+        };
+        int iacc[M], bacc[M];   // 64 sum_g s_g dot_g; q2_K sum_g m_g bsum_g, q3_K sum_g s_g bsum_g
+#pragma unroll
+        for (int i = 0; i < M; ++i) iacc[i] = bacc[i] = 0;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int e = FMT == 3 && j == 3 ? 2 : j;   // the plane's bytes hold 4^e x the code
+                uint32_t c[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const uint32_t w = B.w[QSW + 8 * h + u];
+                    c[u] = (e == j ? w : w >> 2) & (0x03030303u << (2 * e));
+                    if constexpr (FMT == 3) {   // the third bit, from bit 4h + j to bit 2e + 2
+                        const uint32_t hb = B.w[u] & (0x01010101u << (4 * h + j));
+                        const int sh = 2 * e + 2 - (4 * h + j);
+                        c[u] |= sh >= 0 ? hb << sh : hb >> -sh;
+                    }
+                }
+                const int g = 8 * h + 2 * j;   // groups g (u < 4) and g + 1
+                int s0, s1;
+                uint32_t pair;   // bytes 0, 1: q2_K the two mins, q3_K the two scales (signed)
+                if constexpr (FMT == 2) {
+                    const uint32_t sb = B.w[g >> 2] >> (8 * (g & 3));   // scale bytes g, g + 1
+                    s0 = (int)(sb & 15u);
+                    s1 = (int)((sb >> 8) & 15u);
+                    pair = (sb >> 4) & 0x0F0Fu;
+                } else {
+                    s0 = scale3(g);
+                    s1 = scale3(g + 1);
+                    pair = __byte_perm((uint32_t)s0, (uint32_t)s1, 0x0040u);
+                }
+#pragma unroll
+                for (int i = 0; i < M; ++i) {
+                    const uint8_t* a = act + (size_t)i * act_stride;
+                    const int4 x0 = *reinterpret_cast<const int4*>(a + 128 * h + 32 * j);
+                    const int4 x1 = *reinterpret_cast<const int4*>(a + 128 * h + 32 * j + 16);
+                    const int bs = *reinterpret_cast<const int*>(a + 256 + 2 * g);   // bsums g, g + 1
+                    int d0 = dp4a_us(c[0], x0.x, 0);
+                    d0 = dp4a_us(c[1], x0.y, d0);
+                    d0 = dp4a_us(c[2], x0.z, d0);
+                    d0 = dp4a_us(c[3], x0.w, d0);
+                    int d1 = dp4a_us(c[4], x1.x, 0);
+                    d1 = dp4a_us(c[5], x1.y, d1);
+                    d1 = dp4a_us(c[6], x1.z, d1);
+                    d1 = dp4a_us(c[7], x1.w, d1);
+                    iacc[i] += (s0 * d0 + s1 * d1) * (1 << (6 - 2 * e));
+                    if constexpr (FMT == 2)
+                        bacc[i] = dp2a_lo_su(bs, pair, bacc[i]);
+                    else
+                        bacc[i] = dp2a_lo_ss(bs, pair, bacc[i]);
+                }
+            }
+        }
         if constexpr (FMT == 2) {
             const float d = half_bits_to_float(B.w[20]), dmin = half_bits_to_float(B.w[20] >> 16);
 #pragma unroll
             for (int i = 0; i < M; ++i) {
-                const float tt = __fmaf_rn(d, (float)isum[i], -__fmul_rn(dmin, (float)msum[i]));
+                const float tt = __fmaf_rn(d, (float)(iacc[i] >> 6), -__fmul_rn(dmin, (float)bacc[i]));
                 v[i] = __fmaf_rn(dy[i * dy_stride], tt, v[i]);
             }
         } else {
             const float d = half_bits_to_float(B.d);
 #pragma unroll
-            for (int i = 0; i < M; ++i) v[i] = __fmaf_rn(dy[i * dy_stride], __fmul_rn(d, (float)isum[i]), v[i]);
+            for (int i = 0; i < M; ++i) {
+                const int isum = (iacc[i] >> 6) - 4 * bacc[i];
+                v[i] = __fmaf_rn(dy[i * dy_stride], __fmul_rn(d, (float)isum), v[i]);
+            }
         }
     }
 }
