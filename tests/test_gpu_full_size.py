@@ -125,8 +125,8 @@ def test_config4_qwen3_8b_sweep(fmt, n, k):
     w = weights(fmt, 4, n, k)
     w_dev = dev(w)
     for m in (1, 2, 4, 8, 64, 512, 2048):
-        if fmt == "q6K" and m == 2048:
-            continue   # 2.5e12 MACs; m = 512 covers the same kernel path at this shape
+        # the q6_K head at m = 2048: 1.27e12 MACs on the GPU, a 1.2 GB result; the oracle
+        # takes the sampled rows only
         x = gen.normal_f32(4, 100 + m, m, k)
         y, xq = run_gpu(fmt, w_dev, x, n, k)
         check_rows(fmt, w, xq, y, sample_rows(n, 16 if m >= 512 else 32, m), k)
