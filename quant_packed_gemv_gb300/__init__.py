@@ -1,5 +1,5 @@
 """GB300 (sm_103a) packed K-quant matmul: q8_K activation quantization and
-q4_K / q6_K decode GEMV and prefill GEMM behind a C ABI (include/plm.h)."""
+q2_K .. q6_K decode GEMV and prefill GEMM behind a C ABI (include/plm.h)."""
 from .plm import (  # noqa: F401
     PlmError, load, library_path, plm_abi_version, plm_set_overlap,
     PLM_OVERLAP_OFF, PLM_OVERLAP_LAUNCH, PLM_OVERLAP_PREFETCH, plm_device_fault, plm_selftest_bounded_wait, plm_probe_mma_rates, plm_quantize_q8K,
