@@ -45,3 +45,17 @@ def test_fused_step_bytes_are_weights_f32_activations_and_y():
     x_f32 = 4 * 28 * (1024 + 1024 + 1024 + 2048 + 1024 + 1024 + 3072)
     y = 4 * 28 * (2048 + 1024 + 1024 + 1024 + 3072 + 3072 + 1024)
     assert bench.fused_step_bytes(mats) == weights + x_f32 + y == 250_249_216
+
+
+def test_ncu_records_match_the_kernel_sources():
+    """Every committed ncu traffic record still describes the kernel sources as they are:
+    the bench reports `traffic` only while the sources' hash matches the capture's, so
+    a source edit without a new capture would turn the bench line's traffic to null."""
+    import json
+    import os
+    recs = json.load(open(os.path.join(bench.ROOT, "profiles", "ncu_traffic.json")))
+    assert set(recs) >= {"gemv_q4K_fused_grouped_m1", "gemv_q4K_grouped_m1", "gemm_q4K_12288x4096_m2048"}
+    for key, rec in recs.items():
+        assert bench.recorded_counters(key) is not None, "%s: stale (sources changed since the capture)" % key
+        assert rec["dram_bytes_per_launch"] == rec["dram_read_bytes"] + rec["dram_write_bytes"]
+        assert os.path.exists(os.path.join(bench.ROOT, rec["capture"]))
