@@ -973,12 +973,15 @@ def main():
         "device_fault": fault,
     }
     s8_tops, f16_tflops = q.plm_probe_mma_rates()
+    tc_cyc, tc_cyc_wait, tc_tflops = q.plm_probe_tcgen05_rate()
     out["peaks"] = {"hbm_gbs": peak, "hbm_source": peak_src,
                     "bf16_tflops": peaks.get("bf16_tflops", 1900.0),
                     "int8_mma_tops": s8_tops, "f16_mma_sync_tflops": f16_tflops,
-                    "note": "context only: legacy mma.sync rates measured live (tcgen05 has no int8 kind on "
-                            "sm_103a); the GEMM runs tcgen05 kind::f16, so its roofline is the measured bf16 dense "
-                            "peak (f16 has the same nominal rate)"}
+                    "tcgen05_f16_128x128x16": {"cycles_per_mma": tc_cyc, "cycles_per_mma_wait_after_commit": tc_cyc_wait,
+                                               "tflops_zero_operands": tc_tflops},
+                    "note": "context only: legacy mma.sync rates and the GEMM's tcgen05 MMA (one thread, commit "
+                            "every four; zero operands) measured live (tcgen05 has no int8 kind on sm_103a); the "
+                            "GEMM's roofline is the measured bf16 dense peak (f16 has the same nominal rate)"}
     if rank == 0 and not args.no_extras:
         del st
         torch.cuda.empty_cache()

@@ -134,6 +134,23 @@ plm_status plm_selftest_bounded_wait(uint32_t rounds, int complete, cudaStream_t
 plm_status plm_probe_mma_rates(double* s8_tops, double* f16_tflops);
 
 /*
+ * Diagnostic (the pages have no counterpart): the tcgen05 MMA the prefill
+ * GEMM issues (kind::f16, M = 128, N = 128, K = 16, A from tensor memory, B
+ * from shared memory, zero operands), streamed by one thread with a commit
+ * every four MMAs.
+ *   *cycles_per_mma      : SM cycles per MMA, one CTA;
+ *   *cycles_per_mma_wait : the same with an mbarrier wait on an already
+ *                          completed phase after each commit (what a wait
+ *                          in the MMA-issuing thread costs the tensor pipe);
+ *   *tflops              : the first pattern on one CTA per SM (dense rate on
+ *                          zero operands: context, not a roofline peak).
+ * Synchronizes; allocates nothing (a static device array holds the cycle
+ * counts).  PLM_ERR_CUDA if a launch failed; a wait that runs out sets bit 1
+ * of plm_device_fault.
+ */
+plm_status plm_probe_tcgen05_rate(double* cycles_per_mma, double* cycles_per_mma_wait, double* tflops);
+
+/*
  * q8_K activation quantization ("Current status" row "src/": activations
  * quantized to int8 the llama.cpp way, one 256-element block per task).
  * Per 256-element chunk of each row of x: the signed value `max` of largest

@@ -3,8 +3,9 @@
 // the tensor-core kernels: on GB300, sm_103a, tcgen05 has no int8 kind, and
 // these legacy warp-level rates are far below the tcgen05 f16 dense rate the
 // GEMM's roofline uses).  Register-only loops; the one store per thread goes
-// to a static device word (nothing is allocated).  Also the failure-detection
-// self-test of the bounded waits.
+// to a static device word (nothing is allocated).  The rate of the tcgen05
+// MMA the GEMM issues, alone and with an mbarrier wait after each commit.
+// Also the failure-detection self-test of the bounded waits.
 #include <cstdint>
 
 #include "../../include/plm.h"
@@ -72,6 +73,116 @@ static cudaError_t time_rate(double* out) {
     return cudaSuccess;
 }
 
+// tcgen05 MMA rate: one thread of one CTA issues `nmma` MMAs of the GEMM's
+// shape (kind::f16, M = 128, N = 128, K = 16, f32 accumulator in tensor
+// memory, A from tensor memory, B from shared memory; zero operands) with a
+// commit every four.  With WAIT, each commit is followed by an mbarrier wait
+// on a phase that is already complete, as the GEMM's MMA thread waits for its
+// next stage.  clock64 cycles from the first issue to the last commit's
+// completion go to tc_cycles[blockIdx.x].  120 KB of shared memory keep one
+// CTA per SM.
+constexpr int TC_SMEM = 120 * 1024;
+constexpr uint32_t TC_IDESC = (1u << 4) | ((128u >> 3) << 17) | ((128u >> 4) << 24);   // f16 x f16 -> f32, 128 x 128
+static __device__ unsigned long long tc_cycles[1024];
+
+__device__ __forceinline__ uint64_t tc_desc_sw128(uint32_t saddr) {   // K-major, 128-byte swizzle
+    return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+template <bool WAIT>
+__global__ void __launch_bounds__(128, 1) tc_rate_kernel(int nmma, unsigned* fault) {
+    extern __shared__ __align__(1024) uint8_t tc_raw[];
+    uint8_t* sm = tc_raw + ((1024u - (smem_u32(tc_raw) & 1023u)) & 1023u);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + 16384);   // [0] last commit, [1] commits, [2] complete
+    uint32_t* slot = reinterpret_cast<uint32_t*>(bars + 4);
+    const int warp = threadIdx.x >> 5;
+    for (int i = threadIdx.x; i < 16384 / 16; i += blockDim.x) reinterpret_cast<uint4*>(sm)[i] = make_uint4(0, 0, 0, 0);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 3; ++i) mbar_init(&bars[i], 1);
+        fence_barrier_init();
+        mbar_arrive(&bars[2]);
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" :: "r"(smem_u32(slot)) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // the zero B tile, for the tensor core
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const uint32_t tm = *slot;
+    {   // A: columns 256 .. 287 of every lane, zero
+        const uint32_t z = 0u;
+        asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,"
+                     "%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1};"
+                     :: "r"(tm + ((uint32_t)(warp * 32) << 16) + 256u), "r"(z) : "memory");
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    if (threadIdx.x == 0) {
+        const uint64_t db = tc_desc_sw128(smem_u32(sm));
+        const unsigned long long t0 = clock64();
+        bool ok = true;
+        for (int i = 0; i < nmma && ok; ++i) {
+            const int kk = i & 3;
+            asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                         "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+                         :: "r"(tm), "r"(tm + 256u + 8u * kk), "l"(db + 2 * kk), "r"(TC_IDESC), "r"((uint32_t)(i > 0)));
+            if (kk == 3) {
+                asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                             :: "r"(smem_u32(&bars[1])) : "memory");
+                if (WAIT) ok = mbar_wait(&bars[2], 0u);
+            }
+        }
+        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                     :: "r"(smem_u32(&bars[0])) : "memory");
+        if (!mbar_wait(&bars[0], 0u)) ok = false;
+        if (!ok) atomicOr(fault, 2u);
+        tc_cycles[blockIdx.x] = clock64() - t0;
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    if (warp == 0) {
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" :: "r"(tm) : "memory");
+    }
+}
+
+template <bool WAIT>
+static cudaError_t tc_rate(int grid, int nmma, double* cycles_per_mma, double* ms) {
+    unsigned* fault = fault_word();
+    if (!fault) return cudaErrorInvalidDevicePointer;
+    cudaError_t e = cudaFuncSetAttribute(tc_rate_kernel<WAIT>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
+    if (e != cudaSuccess) return e;
+    cudaEvent_t e0, e1;
+    if ((e = cudaEventCreate(&e0)) != cudaSuccess) return e;
+    if ((e = cudaEventCreate(&e1)) != cudaSuccess) { cudaEventDestroy(e0); return e; }
+    float best = 1e30f;
+    for (int rep = 0; rep < 3 && e == cudaSuccess; ++rep) {   // the first is a warm-up
+        cudaEventRecord(e0, 0);
+        tc_rate_kernel<WAIT><<<grid, 128, TC_SMEM, 0>>>(nmma, fault);
+        cudaEventRecord(e1, 0);
+        e = cudaGetLastError();
+        if (e == cudaSuccess) e = cudaEventSynchronize(e1);
+        float t = 0.0f;
+        if (e == cudaSuccess) e = cudaEventElapsedTime(&t, e0, e1);
+        if (e == cudaSuccess && rep > 0 && t < best) best = t;
+    }
+    cudaEventDestroy(e0);
+    cudaEventDestroy(e1);
+    if (e != cudaSuccess) return e;
+    unsigned long long c[1024];
+    if ((e = cudaMemcpyFromSymbol(c, tc_cycles, sizeof(unsigned long long) * grid)) != cudaSuccess) return e;
+    double sum = 0.0;
+    for (int i = 0; i < grid; ++i) sum += (double)c[i];
+    *cycles_per_mma = sum / grid / nmma;
+    *ms = best;
+    return cudaSuccess;
+}
+
 // Failure-detection self-test: one warp waits on an mbarrier of its own with
 // the same bounded wait the streaming kernels use, limited to `rounds`
 // rounds.  With complete != 0 the barrier's one arrival is made first, so the
@@ -106,5 +217,18 @@ extern "C" plm_status plm_probe_mma_rates(double* s8_tops, double* f16_tflops) {
     cudaError_t e = plm::time_rate<0>(s8_tops);
     if (e == cudaSuccess) e = plm::time_rate<1>(f16_tflops);
     if (e != cudaSuccess) return PLM_ERR_CUDA;
+    return PLM_OK;
+}
+
+extern "C" plm_status plm_probe_tcgen05_rate(double* cycles_per_mma, double* cycles_per_mma_wait, double* tflops) {
+    if (!cycles_per_mma || !cycles_per_mma_wait || !tflops) return PLM_ERR_INVALID_ARG;
+    const int nmma = 4096, sms = plm::num_sms();
+    if (sms < 1 || sms > 1024) return PLM_ERR_UNSUPPORTED;
+    double ms = 0.0, unused = 0.0;
+    cudaError_t e = plm::tc_rate<false>(1, nmma, cycles_per_mma, &ms);
+    if (e == cudaSuccess) e = plm::tc_rate<true>(1, nmma, cycles_per_mma_wait, &ms);
+    if (e == cudaSuccess) e = plm::tc_rate<false>(sms, nmma, &unused, &ms);
+    if (e != cudaSuccess) return PLM_ERR_CUDA;
+    *tflops = 2.0 * 128 * 128 * 16 * (double)nmma * sms / (ms * 1e-3) / 1e12;
     return PLM_OK;
 }

@@ -83,6 +83,8 @@ def load(build_if_missing=True):
     lib.plm_device_fault.restype = ctypes.c_int
     lib.plm_probe_mma_rates.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)]
     lib.plm_probe_mma_rates.restype = ctypes.c_int
+    lib.plm_probe_tcgen05_rate.argtypes = [ctypes.POINTER(ctypes.c_double)] * 3
+    lib.plm_probe_tcgen05_rate.restype = ctypes.c_int
     lib.plm_selftest_bounded_wait.argtypes = [ctypes.c_uint32, ctypes.c_int, vp]
     lib.plm_selftest_bounded_wait.restype = ctypes.c_int
     for f in ("q4K", "q6K"):
@@ -192,6 +194,15 @@ def plm_probe_mma_rates():
     a, b = ctypes.c_double(0), ctypes.c_double(0)
     _check("plm_probe_mma_rates", lib.plm_probe_mma_rates(ctypes.byref(a), ctypes.byref(b)))
     return a.value, b.value
+
+
+def plm_probe_tcgen05_rate():
+    """(cycles per MMA, cycles per MMA with an mbarrier wait after each commit, TFLOPS on every
+    SM) of the GEMM's tcgen05 MMA on the current device; synchronizes."""
+    lib = load()
+    a, b, c = ctypes.c_double(0), ctypes.c_double(0), ctypes.c_double(0)
+    _check("plm_probe_tcgen05_rate", lib.plm_probe_tcgen05_rate(ctypes.byref(a), ctypes.byref(b), ctypes.byref(c)))
+    return a.value, b.value, c.value
 
 
 def plm_quantize_q8K(x, xq, m, k, stream=None):
