@@ -65,7 +65,9 @@ def test_gemv_matches_oracle(fmt, m, n, k):
 @pytest.mark.parametrize("fmt", ["q2K", "q3K", "q4K", "q5K", "q6K"])
 def test_gemv_row_result_independent_of_m(fmt):
     # the pages' tiled kernels are bit-identical to the single-row kernel;
-    # here activation row i must give the same bits at every m
+    # here activation row i must give the same bits at every m.  For q3_K at
+    # k = 2048 this also holds the one-lane kernel's two decodes to each other:
+    # codes kept in place for m <= 3, shifted down for m > 3
     n, k = 300, 2048
     w = make_weights(fmt, 12, 0, n, k)
     xq = oracle.quantize_q8K(gen.normal_f32(12, 1, 8, k))
